@@ -1,0 +1,159 @@
+"""fp64 CPU oracle for paged decode attention, kv_write and copy_blocks.
+
+TEST INFRASTRUCTURE ONLY: the tests, ``__graft_entry__.smoke()`` and the
+benchmark's CPU-baseline leg (and its ``--impl reference`` arm) are the only
+callers.  The oracle is plain C (``pa_oracle.c``) loaded through ctypes; it
+shares no code with the CUDA library and never imports it.
+
+Parity is pinned by the tests in ``tests/test_oracle_pins.py`` (closed forms,
+library attention on contiguous caches, permutation invariance, shared versus
+copied prefixes, poison invariance, exhaustive element decoding, and the block
+tables printed on the pages).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+from typing import Optional
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "pa_oracle.c")
+_HDR = os.path.join(_HERE, "pa_oracle.h")
+_BUILD_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD_DIR, "liboracle.so")
+
+ELEM_TYPE = {"f32": 0, "f16": 1, "bf16": 2}
+ELEM_BYTES = {"f32": 4, "f16": 2, "bf16": 2}
+ERR_BLOCK_OOB = 1
+ERR_CTX_OOB = 2
+ERR_SLOT_OOB = 4
+
+_lock = threading.Lock()
+_lib: Optional[ctypes.CDLL] = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc (no fast-math: IEEE fp64 throughout)."""
+    os.makedirs(_BUILD_DIR, exist_ok=True)
+    stale = (not os.path.exists(_LIB_PATH)
+             or os.path.getmtime(_LIB_PATH) < max(os.path.getmtime(_SRC), os.path.getmtime(_HDR)))
+    if force or stale:
+        tmp = _LIB_PATH + f".tmp{os.getpid()}"
+        subprocess.check_call(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fno-fast-math",
+                               "-ffp-contract=off", "-o", tmp, _SRC, "-lm"])
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load() -> ctypes.CDLL:
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            c_int, c_uint, c_double, vp = ctypes.c_int, ctypes.c_uint, ctypes.c_double, ctypes.c_void_p
+            lib.oracle_elem.restype = c_double
+            lib.oracle_elem.argtypes = [vp, ctypes.c_size_t, c_int]
+            lib.oracle_decode_head.restype = c_uint
+            lib.oracle_decode_head.argtypes = [vp, vp, vp, vp, vp, c_int, c_int, c_int, c_int,
+                                               c_int, c_int, c_int, c_double, c_int]
+            lib.oracle_decode.restype = c_uint
+            lib.oracle_decode.argtypes = [vp, vp, vp, vp, vp, c_int, vp, c_int, c_int, c_int,
+                                          c_int, c_int, c_int, c_double, c_int]
+            lib.oracle_kv_write.restype = c_uint
+            lib.oracle_kv_write.argtypes = [vp, vp, vp, vp, vp, c_int, c_int, c_int, c_int, c_int,
+                                            c_int]
+            lib.oracle_copy_blocks.restype = c_uint
+            lib.oracle_copy_blocks.argtypes = [vp, vp, vp, c_int, c_int, c_int, c_int, c_int,
+                                               c_int]
+            _lib = lib
+    return _lib
+
+
+def _ptr(a: np.ndarray) -> int:
+    assert a.flags["C_CONTIGUOUS"], "oracle inputs must be C-contiguous"
+    return a.ctypes.data
+
+
+def elem_to_f64(a: np.ndarray, dtype: str) -> np.ndarray:
+    """Decode every element of a raw array through the oracle's own decoder."""
+    lib = _load()
+    flat = np.ascontiguousarray(a).reshape(-1)
+    return np.array([lib.oracle_elem(_ptr(flat), i, ELEM_TYPE[dtype]) for i in range(flat.size)],
+                    dtype=np.float64).reshape(a.shape)
+
+
+def decode(q, k_cache, v_cache, block_tables, context_lens, *, scale: float, dtype: str,
+           num_kv_heads: Optional[int] = None):
+    """out[s][h] = softmax(scale * q[s][h] . K_s^T) V_s over the first
+    context_lens[s] tokens gathered through block_tables[s]; fp64 [S][Hq][d].
+    Returns (out, error bits)."""
+    lib = _load()
+    S, Hq, d = q.shape
+    NB, Hkv, B, d2 = k_cache.shape
+    assert d2 == d and v_cache.shape == k_cache.shape
+    assert num_kv_heads in (None, Hkv)
+    MB = block_tables.shape[1]
+    bt = np.ascontiguousarray(block_tables, dtype=np.int32)
+    cl = np.ascontiguousarray(context_lens, dtype=np.int32)
+    out = np.zeros((S, Hq, d), dtype=np.float64)
+    q = np.ascontiguousarray(q)
+    kc = np.ascontiguousarray(k_cache)
+    vc = np.ascontiguousarray(v_cache)
+    err = lib.oracle_decode(_ptr(out), _ptr(q), _ptr(kc), _ptr(vc), _ptr(bt), MB, _ptr(cl), S, Hq,
+                            Hkv, d, B, NB, float(scale), ELEM_TYPE[dtype])
+    return out, int(err)
+
+
+def decode_head(q, k_cache, v_cache, block_tables, context_lens, s: int, h: int, *,
+                scale: float, dtype: str):
+    """One (sequence, query head) of ``decode``; fp64 [d]."""
+    lib = _load()
+    S, Hq, d = q.shape
+    NB, Hkv, B, _ = k_cache.shape
+    MB = block_tables.shape[1]
+    g = Hq // Hkv
+    out = np.zeros(d, dtype=np.float64)
+    q_row = np.ascontiguousarray(q[s, h])
+    row = np.ascontiguousarray(block_tables[s], dtype=np.int32)
+    err = lib.oracle_decode_head(_ptr(out), _ptr(q_row), _ptr(k_cache), _ptr(v_cache), _ptr(row),
+                                 MB, int(context_lens[s]), h // g, Hkv, d, B, NB, float(scale),
+                                 ELEM_TYPE[dtype])
+    return out, int(err)
+
+
+def kv_write(k_cache, v_cache, k_new, v_new, slot_mapping, *, dtype: str):
+    """In-place on the host pool copies k_cache / v_cache.  Returns error bits."""
+    lib = _load()
+    NB, Hkv, B, d = k_cache.shape
+    T = slot_mapping.shape[0]
+    sm = np.ascontiguousarray(slot_mapping, dtype=np.int64)
+    kn = np.ascontiguousarray(k_new)
+    vn = np.ascontiguousarray(v_new)
+    return int(lib.oracle_kv_write(_ptr(k_cache), _ptr(v_cache), _ptr(kn), _ptr(vn), _ptr(sm), T,
+                                   Hkv, d, B, NB, ELEM_BYTES[dtype]))
+
+
+def copy_blocks(k_cache, v_cache, block_mapping, *, dtype: str):
+    """In-place block copies on host pool copies.  Returns error bits."""
+    lib = _load()
+    NB, Hkv, B, d = k_cache.shape
+    bm = np.ascontiguousarray(block_mapping, dtype=np.int32).reshape(-1, 2)
+    return int(lib.oracle_copy_blocks(_ptr(k_cache), _ptr(v_cache), _ptr(bm), bm.shape[0], Hkv, d,
+                                      B, NB, ELEM_BYTES[dtype]))
+
+
+def step(w, *, do_copy: bool = True):
+    """One decode step of a workload on host copies: copy_blocks, kv_write,
+    decode.  Returns (k_cache, v_cache, out, error bits)."""
+    kc = w.k_cache.copy()
+    vc = w.v_cache.copy()
+    err = 0
+    if do_copy and w.block_mapping.size:
+        err |= copy_blocks(kc, vc, w.block_mapping, dtype=w.dtype)
+    err |= kv_write(kc, vc, w.k_new, w.v_new, w.slot_mapping, dtype=w.dtype)
+    out, e = decode(w.q, kc, vc, w.block_tables, w.context_lens, scale=w.scale, dtype=w.dtype)
+    return kc, vc, out, err | e

@@ -1,0 +1,191 @@
+/* pa_oracle.c -- plain, slow fp64 CPU oracle for the paged decode path.
+ *
+ * TEST INFRASTRUCTURE ONLY (see pa_oracle.h): the tests, the smoke check and
+ * the benchmark's CPU-baseline leg are its only users.  No blocking, fusion or
+ * reordering: each function is the definition written out.
+ *
+ * What it follows:
+ *  - decode: for each sequence and head, walk the block table in logical
+ *    order and gather the K/V rows of the first context_len tokens (logical
+ *    block i -> physical block table[i], offset t mod B), then take the
+ *    scaled dot products with q, a softmax, and the weighted sum of V.
+ *    "PagedAttention" (compassingai.com) §5 (block table, base address plus
+ *    in-block offset) and §8 (outer loop over the table's blocks, inner loop
+ *    over the tokens of a block; dot, softmax, times V);
+ *    "PagedAttention 深度解析" §二 items 1-3 (blocks of 16 tokens, table
+ *    lookup by the kernel, model sees a contiguous cache).
+ *  - only the last block is partly filled: tokens at or after context_len
+ *    are never read ("PagedAttention" (compassingai.com) §7).
+ *  - kv_write: the new token's K/V goes into its slot of the current block
+ *    (kwkr.cn "vLLM PagedAttention 技术深度解析" §1.2.2 allocation flow;
+ *    wmrh.cn "paged attention": only the new token's K/V is computed).
+ *  - copy_blocks: copy-on-write of a shared block copies its whole content
+ *    to a fresh block ("PagedAttention" (compassingai.com) §6).
+ *  - bounds checks: a bad block id, slot or length is skipped and reported,
+ *    never followed ("PagedAttention" (compassingai.com) §13).
+ */
+#include "pa_oracle.h"
+
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define OR_BLOCK_OOB 1u
+#define OR_CTX_OOB 2u
+#define OR_SLOT_OOB 4u
+
+/* IEEE 754 binary16: 1 sign bit, 5 exponent bits (bias 15), 10 fraction bits. */
+static double half_bits_to_double(uint16_t h) {
+    int sign = (h >> 15) & 1;
+    int e = (h >> 10) & 0x1f;
+    int f = h & 0x3ff;
+    double v;
+    if (e == 0)
+        v = ldexp((double)f, -24);               /* subnormal: f * 2^(1-15-10) */
+    else if (e == 31)
+        v = f ? NAN : INFINITY;
+    else
+        v = ldexp((double)(f + 1024), e - 25);   /* (1 + f/2^10) * 2^(e-15) */
+    return sign ? -v : v;
+}
+
+/* bfloat16: the upper 16 bits of an IEEE binary32. */
+static double bf16_bits_to_double(uint16_t b) {
+    uint32_t u = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+double oracle_elem(const void* base, size_t idx, int elem_type) {
+    if (elem_type == 0) {
+        float f;
+        memcpy(&f, (const char*)base + idx * 4, 4);
+        return (double)f;
+    }
+    uint16_t h;
+    memcpy(&h, (const char*)base + idx * 2, 2);
+    return elem_type == 1 ? half_bits_to_double(h) : bf16_bits_to_double(h);
+}
+
+unsigned oracle_decode_head(double* out, const void* q_row, const void* k_cache,
+                            const void* v_cache, const int32_t* table, int max_blocks_per_seq,
+                            int context_len, int kv_head, int num_kv_heads, int head_dim,
+                            int block_size, int num_blocks, double scale, int elem_type) {
+    const int d = head_dim, B = block_size;
+    unsigned err = 0;
+    for (int j = 0; j < d; ++j) out[j] = 0.0;
+    if (context_len < 0 || (long long)context_len > (long long)max_blocks_per_seq * B)
+        return OR_CTX_OOB;
+    if (context_len == 0) return 0;
+
+    /* 1. Materialise the logical K and V of this sequence and kv head. */
+    double* K = (double*)malloc(sizeof(double) * (size_t)context_len * d);
+    double* V = (double*)malloc(sizeof(double) * (size_t)context_len * d);
+    double* x = (double*)malloc(sizeof(double) * (size_t)context_len);
+    double* qd = (double*)malloc(sizeof(double) * (size_t)d);
+    if (!K || !V || !x || !qd) abort();
+    for (int j = 0; j < d; ++j) qd[j] = oracle_elem(q_row, (size_t)j, elem_type);
+    int n = 0;
+    for (int t = 0; t < context_len; ++t) {
+        int p = table[t / B];
+        if (p < 0 || p >= num_blocks) {
+            err |= OR_BLOCK_OOB;
+            continue;
+        }
+        size_t row = (((size_t)p * num_kv_heads + kv_head) * B + (size_t)(t % B)) * d;
+        for (int j = 0; j < d; ++j) {
+            K[(size_t)n * d + j] = oracle_elem(k_cache, row + j, elem_type);
+            V[(size_t)n * d + j] = oracle_elem(v_cache, row + j, elem_type);
+        }
+        ++n;
+    }
+
+    /* 2. Scaled dot products with the query. */
+    for (int i = 0; i < n; ++i) {
+        double acc = 0.0;
+        for (int j = 0; j < d; ++j) acc += qd[j] * K[(size_t)i * d + j];
+        x[i] = scale * acc;
+    }
+
+    /* 3. Softmax over the n logits and the weighted sum of V rows. */
+    if (n > 0) {
+        double m = x[0];
+        for (int i = 1; i < n; ++i)
+            if (x[i] > m) m = x[i];
+        double den = 0.0;
+        for (int i = 0; i < n; ++i) {
+            double w = exp(x[i] - m);
+            den += w;
+            for (int j = 0; j < d; ++j) out[j] += w * V[(size_t)i * d + j];
+        }
+        for (int j = 0; j < d; ++j) out[j] /= den;
+    }
+    free(K);
+    free(V);
+    free(x);
+    free(qd);
+    return err;
+}
+
+unsigned oracle_decode(double* out, const void* q, const void* k_cache, const void* v_cache,
+                       const int32_t* block_tables, int max_blocks_per_seq,
+                       const int32_t* context_lens, int num_seqs, int num_q_heads,
+                       int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                       double scale, int elem_type) {
+    unsigned err = 0;
+    const int group = num_q_heads / num_kv_heads; /* query heads per kv head */
+    const size_t es = elem_type == 0 ? 4 : 2;
+    for (int s = 0; s < num_seqs; ++s) {
+        for (int h = 0; h < num_q_heads; ++h) {
+            const char* q_row = (const char*)q + (((size_t)s * num_q_heads + h) * head_dim) * es;
+            err |= oracle_decode_head(out + ((size_t)s * num_q_heads + h) * head_dim, q_row,
+                                      k_cache, v_cache,
+                                      block_tables + (size_t)s * max_blocks_per_seq,
+                                      max_blocks_per_seq, context_lens[s], h / group,
+                                      num_kv_heads, head_dim, block_size, num_blocks, scale,
+                                      elem_type);
+        }
+    }
+    return err;
+}
+
+unsigned oracle_kv_write(void* k_cache, void* v_cache, const void* k_new, const void* v_new,
+                         const int64_t* slot_mapping, int num_tokens, int num_kv_heads,
+                         int head_dim, int block_size, int num_blocks, int elem_bytes) {
+    unsigned err = 0;
+    const size_t row = (size_t)head_dim * elem_bytes;
+    for (int t = 0; t < num_tokens; ++t) {
+        int64_t slot = slot_mapping[t];
+        if (slot < 0) continue; /* padding token: nothing to write */
+        if (slot >= (int64_t)num_blocks * block_size) {
+            err |= OR_SLOT_OOB;
+            continue;
+        }
+        int64_t blk = slot / block_size, off = slot % block_size;
+        for (int h = 0; h < num_kv_heads; ++h) {
+            size_t dst = (((size_t)blk * num_kv_heads + h) * block_size + (size_t)off) * row;
+            size_t src = ((size_t)t * num_kv_heads + h) * row;
+            memcpy((char*)k_cache + dst, (const char*)k_new + src, row);
+            memcpy((char*)v_cache + dst, (const char*)v_new + src, row);
+        }
+    }
+    return err;
+}
+
+unsigned oracle_copy_blocks(void* k_cache, void* v_cache, const int32_t* block_mapping,
+                            int num_pairs, int num_kv_heads, int head_dim, int block_size,
+                            int num_blocks, int elem_bytes) {
+    unsigned err = 0;
+    const size_t blk_bytes = (size_t)num_kv_heads * block_size * head_dim * elem_bytes;
+    for (int i = 0; i < num_pairs; ++i) {
+        int src = block_mapping[2 * i], dst = block_mapping[2 * i + 1];
+        if (src < 0 || src >= num_blocks || dst < 0 || dst >= num_blocks) {
+            err |= OR_BLOCK_OOB;
+            continue;
+        }
+        memmove((char*)k_cache + (size_t)dst * blk_bytes, (const char*)k_cache + (size_t)src * blk_bytes, blk_bytes);
+        memmove((char*)v_cache + (size_t)dst * blk_bytes, (const char*)v_cache + (size_t)src * blk_bytes, blk_bytes);
+    }
+    return err;
+}

@@ -1,0 +1,61 @@
+/* pa_oracle.h -- fp64 CPU oracle for paged decode attention, kv_write and
+ * copy_blocks.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the tests, the smoke check and the CPU
+ * baseline leg of the benchmark may load this library.  It shares no code,
+ * header, table or helper with the CUDA library; it reads the same raw bytes
+ * the GPU reads and nothing else.
+ *
+ * All pointers are host memory owned by the caller.  Element types are given
+ * as a code: 0 = IEEE binary32, 1 = IEEE binary16, 2 = bfloat16 (the upper
+ * half of a binary32).  Every function returns a bit set of data errors:
+ *   1 = a needed block id is outside [0, num_blocks)   (entry skipped)
+ *   2 = a context length is negative or above max_blocks_per_seq*block_size
+ *       (that sequence's output is all zeros)
+ *   4 = a slot is at or beyond num_blocks*block_size    (token skipped)
+ */
+#ifndef PA_ORACLE_H
+#define PA_ORACLE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Value of element idx of an array of the given element type, as a double. */
+double oracle_elem(const void* base, size_t idx, int elem_type);
+
+/* Decode attention for one (sequence, query head).
+ *   out      [d] doubles
+ *   q_row    [d] elements of the query of this head
+ *   table    the sequence's block-table row (max_blocks_per_seq entries)
+ *   kv_head  the kv head this query head reads
+ */
+unsigned oracle_decode_head(double* out, const void* q_row, const void* k_cache,
+                            const void* v_cache, const int32_t* table, int max_blocks_per_seq,
+                            int context_len, int kv_head, int num_kv_heads, int head_dim,
+                            int block_size, int num_blocks, double scale, int elem_type);
+
+/* Decode attention for every (sequence, query head); out is [S][Hq][d] doubles. */
+unsigned oracle_decode(double* out, const void* q, const void* k_cache, const void* v_cache,
+                       const int32_t* block_tables, int max_blocks_per_seq,
+                       const int32_t* context_lens, int num_seqs, int num_q_heads,
+                       int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                       double scale, int elem_type);
+
+/* Write each new token's K and V rows into its slot of the pool. */
+unsigned oracle_kv_write(void* k_cache, void* v_cache, const void* k_new, const void* v_new,
+                         const int64_t* slot_mapping, int num_tokens, int num_kv_heads,
+                         int head_dim, int block_size, int num_blocks, int elem_bytes);
+
+/* Copy whole blocks (all kv heads, all slots, K and V) for each (src, dst) pair. */
+unsigned oracle_copy_blocks(void* k_cache, void* v_cache, const int32_t* block_mapping,
+                            int num_pairs, int num_kv_heads, int head_dim, int block_size,
+                            int num_blocks, int elem_bytes);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

@@ -1,0 +1,360 @@
+"""Pins for the fp64 oracle: each test ties it to something other than itself.
+
+* element decoding: every binary16 / bfloat16 bit pattern against numpy / torch
+* identity block table: equal to library attention (torch SDPA in float64) on
+  the contiguous cache -- the pages' statement that the model sees a
+  contiguous cache ("PagedAttention 深度解析" §二 item 3)
+* permutation invariance of the physical placement ("PagedAttention"
+  (compassingai.com) §5: logical blocks may sit anywhere in the pool)
+* shared refcounted prefix blocks give the same outputs as private copies
+  ("PagedAttention" (compassingai.com) §6)
+* only the first context_len tokens count: poison elsewhere changes nothing
+  ("PagedAttention" (compassingai.com) §7, waste confined to the last block)
+* closed forms: one token, zero query, equal keys, known logits, a dominant key
+* the worked block table of "PagedAttention 深度解析" §二 (tests/golden)
+* bounds checks reported, never followed ("PagedAttention" (compassingai.com) §13)
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from paged_kv_cache_314_gb300 import workloads as wl
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _f64(a: np.ndarray, dtype: str) -> np.ndarray:
+    """Library decode of raw element storage to float64 (numpy / torch)."""
+    if dtype == "f32":
+        return a.astype(np.float64)
+    if dtype == "f16":
+        return a.astype(np.float16).astype(np.float64)
+    t = torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16)
+    return t.to(torch.float64).numpy()
+
+
+def _store(x: np.ndarray, dtype: str) -> np.ndarray:
+    return wl._to_storage(np.asarray(x, dtype=np.float32), dtype)
+
+
+# ---------------------------------------------------------------------------
+# element decoding
+# ---------------------------------------------------------------------------
+
+def test_f16_decoder_exhaustive():
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    got = oracle.elem_to_f64(bits, "f16")
+    want = bits.view(np.float16).astype(np.float64)
+    nan = np.isnan(want)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], want[~nan])
+    # a few values fixed by the binary16 definition
+    assert oracle.elem_to_f64(np.array([0x3C00], np.uint16), "f16")[0] == 1.0
+    assert oracle.elem_to_f64(np.array([0x7BFF], np.uint16), "f16")[0] == 65504.0
+    assert oracle.elem_to_f64(np.array([0x0001], np.uint16), "f16")[0] == 2.0 ** -24
+    assert oracle.elem_to_f64(np.array([0xC000], np.uint16), "f16")[0] == -2.0
+
+
+def test_bf16_decoder_exhaustive():
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    got = oracle.elem_to_f64(bits, "bf16")
+    want = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(torch.float64).numpy()
+    nan = np.isnan(want)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], want[~nan])
+    assert oracle.elem_to_f64(np.array([0x3F80], np.uint16), "bf16")[0] == 1.0
+
+
+def test_f32_decoder():
+    rng = np.random.default_rng(0)
+    bits = rng.integers(0, 2 ** 32, size=4096, dtype=np.uint64).astype(np.uint32)
+    got = oracle.elem_to_f64(bits.view(np.float32), "f32")
+    with np.errstate(invalid="ignore"):
+        want = bits.view(np.float32).astype(np.float64)
+    nan = np.isnan(want)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], want[~nan])
+
+
+# ---------------------------------------------------------------------------
+# identity table == library attention on the contiguous cache
+# ---------------------------------------------------------------------------
+
+def _contiguous_case(rng, S, Hq, Hkv, d, B, ctx, dtype):
+    MB = max(1, max((n + B - 1) // B for n in ctx))
+    Kc = _store(rng.standard_normal((S, Hkv, MB * B, d)), dtype)
+    Vc = _store(rng.standard_normal((S, Hkv, MB * B, d)), dtype)
+    q = _store(rng.standard_normal((S, Hq, d)), dtype)
+    # identity table: sequence s owns pool blocks s*MB .. s*MB+MB-1 in order
+    k_pool = np.ascontiguousarray(Kc.reshape(S, Hkv, MB, B, d).transpose(0, 2, 1, 3, 4)
+                                  .reshape(S * MB, Hkv, B, d))
+    v_pool = np.ascontiguousarray(Vc.reshape(S, Hkv, MB, B, d).transpose(0, 2, 1, 3, 4)
+                                  .reshape(S * MB, Hkv, B, d))
+    tables = np.arange(S * MB, dtype=np.int32).reshape(S, MB)
+    return q, Kc, Vc, k_pool, v_pool, tables
+
+
+def _sdpa(q64, K64, V64, scale):
+    """torch scaled_dot_product_attention in float64; K/V heads repeated for GQA."""
+    Hq, Hkv = q64.shape[0], K64.shape[0]
+    g = Hq // Hkv
+    Kt = torch.from_numpy(K64).repeat_interleave(g, dim=0)
+    Vt = torch.from_numpy(V64).repeat_interleave(g, dim=0)
+    qt = torch.from_numpy(q64)[:, None, :]
+    return torch.nn.functional.scaled_dot_product_attention(qt, Kt, Vt, scale=scale)[:, 0].numpy()
+
+
+@pytest.mark.parametrize("dtype", ["f32", "f16", "bf16"])
+@pytest.mark.parametrize("Hq,Hkv", [(4, 4), (8, 2)])
+@pytest.mark.parametrize("B", [4, 16])
+def test_identity_table_equals_library_attention(dtype, Hq, Hkv, B):
+    rng = np.random.default_rng(7 + B + Hq)
+    d = 64
+    ctx = [1, B - 1, B, B + 1, 3 * B + 2]
+    S = len(ctx)
+    q, Kc, Vc, kp, vp, tables = _contiguous_case(rng, S, Hq, Hkv, d, B, ctx, dtype)
+    scale = 1.0 / math.sqrt(d)
+    out, err = oracle.decode(q, kp, vp, tables, np.array(ctx, np.int32), scale=scale, dtype=dtype)
+    assert err == 0
+    for s, n in enumerate(ctx):
+        want = _sdpa(_f64(q[s], dtype), _f64(Kc[s, :, :n], dtype), _f64(Vc[s, :, :n], dtype), scale)
+        np.testing.assert_allclose(out[s], want, rtol=1e-12, atol=1e-12)
+
+
+# ---------------------------------------------------------------------------
+# placement invariances
+# ---------------------------------------------------------------------------
+
+def _small(dtype="f16", Hq=4, Hkv=2, d=64, B=16, ctx=(1, 15, 16, 17, 40, 77), seed=3):
+    return wl.custom("pin", list(ctx), dtype=dtype, num_q_heads=Hq, num_kv_heads=Hkv, head_dim=d,
+                     block_size=B, seed=seed, pool_factor=1.5)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_permutation_invariance(dtype):
+    w = _small(dtype=dtype)
+    _, _, base, err = oracle.step(w)
+    assert err == 0 and np.isfinite(base).all()
+    rng = np.random.default_rng(11)
+    for _ in range(3):
+        wp = wl.permute_physical(w, rng)
+        assert not np.array_equal(wp.block_tables, w.block_tables)
+        _, _, out, err = oracle.step(wp)
+        assert err == 0
+        assert np.array_equal(out, base)  # same arithmetic order -> bit-identical
+
+
+def test_shared_prefix_equals_private_copies():
+    w = wl.gqa_share(groups=2, samples=3, prefix_len=40, max_suffix=37, num_q_heads=8,
+                     num_kv_heads=2)
+    assert w.num_pairs == 2 * 2
+    kc, vc, shared_out, err = oracle.step(w)
+    assert err == 0 and np.isfinite(shared_out).all()
+    # Give every sequence private copies of all of its blocks, then decode again.
+    B = w.block_size
+    k_rows, v_rows = [kc], [vc]
+    tables = np.full_like(w.block_tables, -1)
+    nxt = w.num_blocks
+    for s in range(w.num_seqs):
+        nblk = (int(w.context_lens[s]) + B - 1) // B
+        for i in range(nblk):
+            p = int(w.block_tables[s, i])
+            k_rows.append(kc[p:p + 1])
+            v_rows.append(vc[p:p + 1])
+            tables[s, i] = nxt
+            nxt += 1
+    kp = np.ascontiguousarray(np.concatenate(k_rows))
+    vp = np.ascontiguousarray(np.concatenate(v_rows))
+    priv, err = oracle.decode(w.q, kp, vp, tables, w.context_lens, scale=w.scale, dtype=w.dtype)
+    assert err == 0
+    assert np.array_equal(priv, shared_out)
+
+
+def test_poison_is_never_read():
+    w = _small(dtype="f16")
+    _, _, out_nan, err = oracle.step(w)
+    assert err == 0 and np.isfinite(out_nan).all()
+    # Replace every poisoned element with huge finite values: nothing changes.
+    w2 = _small(dtype="f16")
+    for a in (w2.k_cache, w2.v_cache):
+        m = np.isnan(a.astype(np.float32))
+        a[m] = np.float16(60000.0)
+    _, _, out_big, err = oracle.step(w2)
+    assert err == 0 and np.array_equal(out_big, out_nan)
+
+
+# ---------------------------------------------------------------------------
+# closed forms
+# ---------------------------------------------------------------------------
+
+def _one_seq(K, V, q, B=16, dtype="f32"):
+    """Pool holding one sequence's logical K/V [n][Hkv][d] in scattered blocks."""
+    n, Hkv, d = K.shape
+    nblk = (n + B - 1) // B
+    NB = nblk + 7
+    order = [int(b) for b in np.random.default_rng(99).permutation(NB)[:nblk]]
+    kp = wl._poison_fill((NB, Hkv, B, d), dtype, True)
+    vp = wl._poison_fill((NB, Hkv, B, d), dtype, True)
+    for t in range(n):
+        kp[order[t // B], :, t % B] = K[t]
+        vp[order[t // B], :, t % B] = V[t]
+    table = np.full((1, nblk), -1, np.int32)
+    table[0, :] = order
+    return q[None], kp, vp, table
+
+
+def test_single_token_returns_its_value_row():
+    rng = np.random.default_rng(1)
+    K = rng.standard_normal((1, 2, 64)).astype(np.float32)
+    V = rng.standard_normal((1, 2, 64)).astype(np.float32)
+    q = rng.standard_normal((4, 64)).astype(np.float32)
+    qq, kp, vp, tb = _one_seq(K, V, q)
+    out, err = oracle.decode(qq, kp, vp, tb, np.array([1], np.int32), scale=0.125, dtype="f32")
+    assert err == 0
+    for h in range(4):
+        assert np.array_equal(out[0, h], V[0, h // 2].astype(np.float64))
+
+
+def test_zero_query_and_equal_keys_give_mean_of_values():
+    rng = np.random.default_rng(2)
+    n = 37
+    V = rng.standard_normal((n, 1, 64)).astype(np.float32)
+    K = rng.standard_normal((n, 1, 64)).astype(np.float32)
+    q0 = np.zeros((1, 64), np.float32)
+    qq, kp, vp, tb = _one_seq(K, V, q0)
+    out, _ = oracle.decode(qq, kp, vp, tb, np.array([n], np.int32), scale=0.125, dtype="f32")
+    np.testing.assert_allclose(out[0, 0], V[:, 0].astype(np.float64).mean(0), rtol=0, atol=1e-14)
+    Keq = np.repeat(K[:1], n, axis=0)
+    qr = rng.standard_normal((1, 64)).astype(np.float32)
+    qq, kp, vp, tb = _one_seq(Keq, V, qr)
+    out, _ = oracle.decode(qq, kp, vp, tb, np.array([n], np.int32), scale=0.125, dtype="f32")
+    np.testing.assert_allclose(out[0, 0], V[:, 0].astype(np.float64).mean(0), rtol=0, atol=1e-14)
+
+
+def test_known_logits_fix_the_scale():
+    # logits 0 and ln 3 -> softmax weights exactly 1/4 and 3/4 (scale 1/8, d = 64)
+    d = 64
+    K = np.zeros((2, 1, d), np.float32)
+    K[1, 0, 0] = 8.0 * math.log(3.0)
+    q = np.zeros((1, d), np.float32)
+    q[0, 0] = 1.0
+    rng = np.random.default_rng(3)
+    V = rng.standard_normal((2, 1, d)).astype(np.float32)
+    qq, kp, vp, tb = _one_seq(K, V, q)
+    out, _ = oracle.decode(qq, kp, vp, tb, np.array([2], np.int32), scale=0.125, dtype="f32")
+    want = 0.25 * V[0, 0].astype(np.float64) + 0.75 * V[1, 0].astype(np.float64)
+    np.testing.assert_allclose(out[0, 0], want, rtol=0, atol=1e-6)
+
+
+def test_dominant_key_selects_its_value():
+    rng = np.random.default_rng(4)
+    n, d = 50, 64
+    K = (0.01 * rng.standard_normal((n, 1, d))).astype(np.float32)
+    q = np.zeros((1, d), np.float32)
+    q[0, 5] = 1.0
+    K[23, 0, 5] = 400.0  # logit 50 against |logits| < 0.1 elsewhere
+    V = rng.standard_normal((n, 1, d)).astype(np.float32)
+    qq, kp, vp, tb = _one_seq(K, V, q)
+    out, _ = oracle.decode(qq, kp, vp, tb, np.array([n], np.int32), scale=0.125, dtype="f32")
+    np.testing.assert_allclose(out[0, 0], V[23, 0].astype(np.float64), rtol=0, atol=1e-18)
+
+
+# ---------------------------------------------------------------------------
+# lengths and bounds checks
+# ---------------------------------------------------------------------------
+
+def test_context_length_edge_cases():
+    rng = np.random.default_rng(5)
+    K = rng.standard_normal((20, 1, 64)).astype(np.float32)
+    V = rng.standard_normal((20, 1, 64)).astype(np.float32)
+    q = rng.standard_normal((1, 64)).astype(np.float32)
+    qq, kp, vp, tb = _one_seq(K, V, q)  # 2 blocks -> max context 32
+    for n, want_err in ((0, 0), (-1, oracle.ERR_CTX_OOB), (33, oracle.ERR_CTX_OOB)):
+        out, err = oracle.decode(qq, kp, vp, tb, np.array([n], np.int32), scale=0.125, dtype="f32")
+        assert err == want_err
+        assert np.array_equal(out, np.zeros_like(out))
+
+
+def test_bad_block_id_is_skipped_and_reported():
+    rng = np.random.default_rng(6)
+    n, B = 40, 16
+    K = rng.standard_normal((n, 1, 64)).astype(np.float32)
+    V = rng.standard_normal((n, 1, 64)).astype(np.float32)
+    q = rng.standard_normal((1, 64)).astype(np.float32)
+    qq, kp, vp, tb = _one_seq(K, V, q, B=B)
+    tb[0, 1] = kp.shape[0] + 3  # logical block 1 (tokens 16..31) points outside the pool
+    out, err = oracle.decode(qq, kp, vp, tb, np.array([n], np.int32), scale=0.125, dtype="f32")
+    assert err == oracle.ERR_BLOCK_OOB
+    keep = [t for t in range(n) if not (B <= t < 2 * B)]
+    want = _sdpa(q.astype(np.float64), K[keep].transpose(1, 0, 2).astype(np.float64),
+                 V[keep].transpose(1, 0, 2).astype(np.float64), 0.125)
+    np.testing.assert_allclose(out[0], want, rtol=1e-12, atol=1e-12)
+
+
+# ---------------------------------------------------------------------------
+# kv_write and copy_blocks
+# ---------------------------------------------------------------------------
+
+def test_worked_block_table_from_the_pages():
+    g = json.load(open(os.path.join(GOLDEN, "p3_block_table.json")))
+    B, n, table = g["block_size"], g["num_tokens"], g["block_table"]
+    assert (n + B - 1) // B == g["num_logical_blocks"] == len(table)
+    NB, Hkv, d = max(table) + 1, 2, 64
+    rng = np.random.default_rng(8)
+    kc = wl._poison_fill((NB, Hkv, B, d), "f32", True)
+    vc = wl._poison_fill((NB, Hkv, B, d), "f32", True)
+    k_new = rng.standard_normal((n, Hkv, d)).astype(np.float32)
+    v_new = rng.standard_normal((n, Hkv, d)).astype(np.float32)
+    slots = np.array([table[t // B] * B + t % B for t in range(n)], np.int64)
+    assert oracle.kv_write(kc, vc, k_new, v_new, slots, dtype="f32") == 0
+    # token 99 sits in logical block 6 -> physical block 9, offset 3
+    assert np.array_equal(kc[9, :, 3], k_new[99]) and np.array_equal(vc[9, :, 3], v_new[99])
+    assert np.array_equal(kc[5, :, 0], k_new[0])
+    # blocks not in the table stay poisoned; tail slots of block 9 too
+    for p in set(range(NB)) - set(table):
+        assert np.isnan(kc[p]).all()
+    assert np.isnan(kc[9, :, 4:]).all()
+    # zero query: every written V row weighs the same
+    q0 = np.zeros((1, 2 * Hkv, d), np.float32)
+    out, err = oracle.decode(q0, kc, vc, np.array([table], np.int32), np.array([n], np.int32),
+                             scale=0.125, dtype="f32")
+    assert err == 0
+    for h in range(2 * Hkv):
+        np.testing.assert_allclose(out[0, h], v_new[:, h // 2].astype(np.float64).mean(0),
+                                   rtol=0, atol=1e-14)
+
+
+def test_kv_write_skip_and_bounds():
+    NB, Hkv, B, d = 4, 2, 16, 64
+    kc = wl._poison_fill((NB, Hkv, B, d), "bf16", False)
+    vc = kc.copy()
+    rng = np.random.default_rng(9)
+    kn = _store(rng.standard_normal((3, Hkv, d)), "bf16")
+    vn = _store(rng.standard_normal((3, Hkv, d)), "bf16")
+    slots = np.array([-1, NB * B, 17], np.int64)
+    err = oracle.kv_write(kc, vc, kn, vn, slots, dtype="bf16")
+    assert err == oracle.ERR_SLOT_OOB
+    assert np.array_equal(kc[1, :, 1], kn[2]) and np.array_equal(vc[1, :, 1], vn[2])
+    mask = np.ones(kc.shape, bool)
+    mask[1, :, 1] = False
+    assert (kc[mask] == 0).all() and (vc[mask] == 0).all()
+
+
+def test_copy_blocks_copies_whole_blocks_only():
+    rng = np.random.default_rng(10)
+    NB, Hkv, B, d = 8, 2, 16, 64
+    kc = _store(rng.standard_normal((NB, Hkv, B, d)), "f16")
+    vc = _store(rng.standard_normal((NB, Hkv, B, d)), "f16")
+    k0, v0 = kc.copy(), vc.copy()
+    pairs = np.array([[1, 5], [2, 6], [3, NB]], np.int32)
+    err = oracle.copy_blocks(kc, vc, pairs, dtype="f16")
+    assert err == oracle.ERR_BLOCK_OOB
+    for s, t in ((1, 5), (2, 6)):
+        assert np.array_equal(kc[t], k0[s]) and np.array_equal(vc[t], v0[s])
+    for p in (0, 1, 2, 3, 4, 7):
+        assert np.array_equal(kc[p], k0[p]) and np.array_equal(vc[p], v0[p])

@@ -1,0 +1,121 @@
+"""Host-side logic: the refcounting block allocator and the workload plans.
+
+The allocator is replayed against the block-sharing walk-through of the wmrh.cn
+"paged attention" tutorial (tests/golden/p2_sharing.json), and the workload
+plans are checked for the structure the named workloads promise.
+"""
+import json
+import os
+
+import numpy as np
+import pytest
+
+from paged_kv_cache_314_gb300 import workloads as wl
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def test_refcount_walkthrough_from_the_pages():
+    g = json.load(open(os.path.join(GOLDEN, "p2_sharing.json")))
+    # two virtual blocks of one sequence land on physical 1 and 3
+    a = wl.BlockAllocator(8, free_order=[1, 3, 0, 2, 4, 5, 6, 7])
+    assert [a.allocate(), a.allocate()] == g["two_block_sequence"]["physical"]
+
+    # two requests with the same input share three blocks, then diverge
+    sh = g["shared_requests"]
+    a = wl.BlockAllocator(8, free_order=[1, 3, 4, 2, 5, 0, 6, 7])
+    req1 = [a.allocate() for _ in range(3)]
+    req2 = [a.share(b) for b in req1]
+    assert req1 == req2 == sh["shared_physical"]
+    assert all(a.refcount[b] == sh["refcount"] for b in req1)
+    req1.append(a.allocate())
+    req2.append(a.allocate())
+    assert [req1[3], req2[3]] == sh["diverged_physical"]
+    assert a.refcount[req1[3]] == a.refcount[req2[3]] == 1
+
+    # three beams share a prefix: count 3
+    a = wl.BlockAllocator(8)
+    prefix = [a.allocate() for _ in range(2)]
+    for _ in range(g["beams"]["num_beams"] - 1):
+        for b in prefix:
+            a.share(b)
+    assert all(a.refcount[b] == g["beams"]["refcount"] for b in prefix)
+
+
+def test_copy_on_write_rule():
+    a = wl.BlockAllocator(4, free_order=[2, 0, 1, 3])
+    b = a.allocate()
+    a.share(b)
+    nb, pair = a.cow(b)  # count 2 -> a fresh block and one copy
+    assert pair == (b, nb) and nb != b
+    assert a.refcount[b] == 1 and a.refcount[nb] == 1
+    same, pair = a.cow(b)  # sole owner writes in place
+    assert same == b and pair is None
+
+
+def test_allocator_exhaustion_is_an_error():
+    a = wl.BlockAllocator(2)
+    a.allocate()
+    a.allocate()
+    with pytest.raises(wl.OutOfBlocks):
+        a.allocate()
+    a.free(0)
+    assert a.allocate() == 0
+
+
+def test_shared_prefix_plan_structure():
+    rng = np.random.default_rng(0)
+    groups, samples, prefix, B = 32, 8, 1024, 16
+    suffix = rng.integers(0, 257, size=groups * samples)
+    npre = prefix // B
+    NB = 32 * npre + 32 * 7 + int(sum(((prefix + u + 1 + B - 1) // B) - npre for u in suffix)) + 10
+    plan = wl.plan_shared_prefix(groups, samples, prefix, suffix, B, 82, NB, rng)
+    assert len(plan.pairs) == 224  # one copy per later sample of every group
+    for g in range(groups):
+        rows = plan.tables[g * samples:(g + 1) * samples]
+        # the first 63 prefix blocks are shared by all 8 samples (refcount 8)
+        assert (rows[:, :npre - 1] == rows[0, :npre - 1]).all()
+        assert all(plan.refcount[b] == samples for b in rows[0, :npre - 1])
+        # the last prefix block: sample 0 keeps it, the others own copies of it
+        last = rows[:, npre - 1]
+        assert len(set(last.tolist())) == samples
+        assert all(plan.refcount[b] == 1 for b in last)
+        srcs = {p[0] for p in plan.pairs if p[1] in set(last[1:].tolist())}
+        assert srcs == {int(last[0])}
+    assert len(plan.write_tokens) == groups * samples  # only each sample's newest token
+
+
+def test_partial_prefix_plan_writes_into_the_copies():
+    rng = np.random.default_rng(1)
+    suffix = np.array([0, 3, 12, 20])
+    plan = wl.plan_shared_prefix(1, 4, 1016, suffix, 16, 80, 200, rng)
+    ctx = 1016 + suffix + 1
+    # tokens 1016..1023 that exist land in each sample's own copy of block 63
+    for s in range(4):
+        want = list(range(1016, min(1024, int(ctx[s]) - 1))) + [int(ctx[s]) - 1]
+        got = [t for (ss, t) in plan.write_tokens if ss == s]
+        assert got == want
+
+
+def test_named_workloads_shapes():
+    w = wl.tiny()
+    assert list(w.context_lens) == [1, 17, 33, 50] and w.num_blocks == 64
+    assert w.q.dtype == np.float32 and w.k_cache.shape == (64, 4, 16, 64)
+    assert abs(w.scale - 0.125) < 1e-9
+    used = w.block_tables[w.block_tables >= 0]
+    assert len(set(used.tolist())) == used.size == 10
+    # slot of each new token: the table entry of position ctx-1
+    for s in range(4):
+        n = int(w.context_lens[s])
+        assert w.slot_mapping[s] == w.block_tables[s, (n - 1) // 16] * 16 + (n - 1) % 16
+
+
+def test_permute_physical_keeps_the_logical_cache():
+    w = wl.custom("p", [5, 33, 64], dtype="f32", num_q_heads=2, num_kv_heads=2, head_dim=64,
+                  block_size=16, seed=1)
+    wp = wl.permute_physical(w, np.random.default_rng(2))
+    for s in range(3):
+        for t in range(int(w.context_lens[s]) - 1):
+            a = w.k_cache[w.block_tables[s, t // 16], :, t % 16]
+            b = wp.k_cache[wp.block_tables[s, t // 16], :, t % 16]
+            assert np.array_equal(a, b)
