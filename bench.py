@@ -1,0 +1,436 @@
+#!/usr/bin/env python3
+"""Benchmark of the paged decode step on GB300: one JSON line on rank 0.
+
+A step is one pass of the whole hot path over one batch: copy_blocks (when the
+workload has copy-on-write pairs), kv_write of the step's new tokens, and
+paged decode attention (partition kernel + split-K merge).  The default
+workload is the LLaMA-7B-shaped decode batch (64 sequences, 32 heads,
+head_dim 128, fp16 K/V, 16-token blocks, context lengths uniform in
+[128, 2048], physical blocks randomly permuted, pool 1.1x the blocks needed).
+
+value = K+V bytes decode must read per step / device time per step (GB/s),
+with every input resident in HBM before timing starts; the KV pool (>1 GB) is
+larger than L2 and L2 is also flushed (256 MB write) before every step,
+outside the timed events.  e2e = the same bytes over a step that also copies
+that step's inputs from pinned host memory and reads the output back.
+
+--impl reference times the fp64 CPU oracle on the same workload (kv_write and
+decode of the whole batch per step, host threads), the baseline arm.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "paged decode attn KV-read GB/s (fraction of GB300 HBM peak); seq-heads/s"
+L2_FLUSH_BYTES = 256 << 20
+
+WORKLOAD_TEXT = {
+    "llama7b": "LLaMA-7B-shaped single-layer decode: 64 seqs, 32 q/kv heads, head_dim 128, fp16 "
+               "K/V ~N(0,1), block 16, context U[128,2048], pool 1.1x needed, blocks randomly "
+               "permuted; kv_write of 1 new token/seq",
+    "llama13b": "LLaMA-13B-shaped decode: 256 seqs, 40 heads, head_dim 128, bf16, block 16, "
+                "context log-normal (median 400, sigma 1) capped 4096; kv_write 1 token/seq",
+    "gqa_share": "parallel sampling, shared 1024-token prefix: 32 groups x 8 samples, suffix "
+                 "U[0,256], GQA 64 q / 8 kv heads, head_dim 128, bf16, block 16; 224 CoW "
+                 "copy_blocks pairs + kv_write",
+    "gqa_share_p1016": "as gqa_share with a 1016-token prefix (partial last prefix block)",
+    "long_b16": "long context: 8 seqs, 32 heads, head_dim 128, bf16, context U[32768,131072], "
+                "block 16, 512-token split-K partitions + reduce",
+    "long_b128": "long context as long_b16 with 128-token blocks",
+    "tiny": "tiny: 4 seqs, 4 heads, head_dim 64, fp32, block 16, context {1,17,33,50}, "
+            "64-block pool",
+}
+
+
+def _dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def _kernel_source_hash():
+    csrc = os.path.join(ROOT, "paged_kv_cache_314_gb300", "csrc")
+    h = hashlib.sha256()
+    for name in ("decode_kernels.cuh", "pa_device.cuh"):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def _ncu_traffic(config: str):
+    """DRAM bytes per decode launch from the committed ncu summary, if it was
+    taken on the current kernel sources (else None)."""
+    path = os.path.join(ROOT, "profiles", f"decode_{config}_ncu.md")
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    m = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]+)", text)
+    t = re.search(r"traffic_bytes_per_launch:\s*([0-9]+)", text)
+    if not m or not t or m.group(1) != _kernel_source_hash():
+        return None
+    return int(t.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+                out = ""
+            self.lines = [l for l in out.splitlines() if l.strip()]
+        return False
+
+    def summary(self):
+        if not getattr(self, "lines", None):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm, smax, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for l in self.lines:
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": float(np.median(sm)) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+
+def _to_torch(a, dtype):
+    import torch
+    if dtype == "bf16":
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16)
+    return torch.from_numpy(np.ascontiguousarray(a))
+
+
+def _cpu_baseline(w, budget_s=20.0):
+    """The oracle, as it stands, on this workload's decode (whole sequences,
+    in order, until the budget is spent) on all host cores."""
+    import concurrent.futures as cf
+    import oracle
+    threads = os.cpu_count() or 1
+    kc, vc = w.k_cache, w.v_cache
+    done_bytes, n_seqs, t0 = 0, 0, time.perf_counter()
+    per_tok = 2 * w.num_kv_heads * w.head_dim * w.elem_bytes
+    with cf.ThreadPoolExecutor(threads) as ex:
+        while n_seqs < w.num_seqs and time.perf_counter() - t0 < budget_s:
+            seqs = list(range(n_seqs, min(w.num_seqs, n_seqs + threads)))
+
+            def one(s):
+                o, _ = oracle.decode(np.ascontiguousarray(w.q[s:s + 1]), kc, vc,
+                                     np.ascontiguousarray(w.block_tables[s:s + 1]),
+                                     np.ascontiguousarray(w.context_lens[s:s + 1]),
+                                     scale=w.scale, dtype=w.dtype)
+                return o
+
+            list(ex.map(one, seqs))
+            done_bytes += int(w.context_lens[seqs].clip(0).sum()) * per_tok
+            n_seqs += len(seqs)
+    dt = time.perf_counter() - t0
+    return {"value": done_bytes / dt / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "sample": f"decode of the first {n_seqs} of {w.num_seqs} sequences of the same "
+                      f"workload ({done_bytes / 1e6:.0f} MB of K/V), fp64 C oracle, one "
+                      f"sequence per host thread, {dt:.1f} s"}
+
+
+def run_gpu(args):
+    import torch
+    import paged_kv_cache_314_gb300 as pa
+    from paged_kv_cache_314_gb300 import _build, workloads as wl
+
+    ws, rank, local = _dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist = None
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    if rank == 0:
+        _build.build()
+    if dist is not None:
+        dist.barrier()
+    pa.load()
+
+    w = wl.by_name(args.config, poison=False, **({"partition_tokens": args.partition}
+                                                   if args.partition is not None else {}))
+    P = pa.decode_partition_tokens(w.max_blocks_per_seq, w.block_size, w.partition_tokens)
+    dt = w.dtype
+    d = {k: v.to(dev) for k, v in {
+        "q": _to_torch(w.q, dt), "k_cache": _to_torch(w.k_cache, dt),
+        "v_cache": _to_torch(w.v_cache, dt), "k_new": _to_torch(w.k_new, dt),
+        "v_new": _to_torch(w.v_new, dt), "block_tables": torch.from_numpy(w.block_tables),
+        "context_lens": torch.from_numpy(w.context_lens),
+        "slot_mapping": torch.from_numpy(w.slot_mapping),
+        "block_mapping": torch.from_numpy(w.block_mapping.reshape(-1, 2))}.items()}
+    out = torch.empty_like(d["q"])
+    workspace = pa.decode_workspace(d["q"], d["k_cache"], d["block_tables"], w.partition_tokens)
+    d_err = torch.zeros(1, dtype=torch.int32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    max_parts = math.ceil(w.max_blocks_per_seq * w.block_size / P)
+    launches_per_step = (1 if w.num_pairs else 0) + (1 if w.num_tokens else 0) + 1 + (
+        1 if max_parts > 1 else 0)
+
+    def step(dd, ev_dec=None):
+        if w.num_pairs:
+            pa.copy_blocks(dd["k_cache"], dd["v_cache"], dd["block_mapping"], d_err=d_err)
+        if w.num_tokens:
+            pa.kv_write(dd["k_new"], dd["v_new"], dd["k_cache"], dd["v_cache"],
+                        dd["slot_mapping"], d_err=d_err)
+        if ev_dec is not None:
+            ev_dec[0].record(stream)
+        pa.decode(out, dd["q"], dd["k_cache"], dd["v_cache"], dd["block_tables"],
+                  dd["context_lens"], w.scale, partition_tokens=w.partition_tokens,
+                  workspace=workspace, d_err=d_err)
+        if ev_dec is not None:
+            ev_dec[1].record(stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step(d)
+    torch.cuda.synchronize()
+    if int(d_err.item()) != 0:
+        raise RuntimeError(f"device error word {int(d_err.item())} during warm-up")
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        t_wall = time.perf_counter()
+        for i in range(args.steps):
+            flush.zero_()
+            ev[i][0].record(stream)
+            step(d, (ev[i][1], ev[i][2]))
+            ev[i][3].record(stream)
+        torch.cuda.synchronize()
+        t_wall = time.perf_counter() - t_wall
+    step_ms = [a.elapsed_time(b) for a, _, _, b in ev]
+    dec_ms = [a.elapsed_time(b) for _, a, b, _ in ev]
+    ms_per_step = float(np.mean(step_ms))
+    dec_ms_avg = float(np.mean(dec_ms))
+    if dist is not None:
+        t = torch.tensor([ms_per_step, dec_ms_avg], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_per_step, dec_ms_avg = float(t[0]), float(t[1])
+
+    # end to end through the public API: the step's inputs from pinned host memory,
+    # the output back to pinned host memory, every step.
+    host_in = {k: d[k].cpu().pin_memory() for k in
+               ("q", "k_new", "v_new", "slot_mapping", "block_tables", "context_lens",
+                "block_mapping")}
+    host_out = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    d2h = host_out.numel() * host_out.element_size()
+    dstep = dict(d)
+    e2e_ms = []
+    for i in range(args.warmup + args.steps):
+        flush.zero_()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for k, t in host_in.items():
+            dstep[k].copy_(t, non_blocking=True)
+        step(dstep)
+        host_out.copy_(out, non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        if i >= args.warmup:
+            e2e_ms.append(e0.elapsed_time(e1))
+    e2e_avg = float(np.mean(e2e_ms))
+    if dist is not None:
+        t = torch.tensor([e2e_avg], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_avg = float(t[0])
+    torch.cuda.synchronize()
+    if int(d_err.item()) != 0:
+        raise RuntimeError(f"device error word {int(d_err.item())} during timing")
+
+    kv_bytes = w.kv_read_bytes()
+    value = ws * kv_bytes / (ms_per_step * 1e-3) / 1e9
+    peak, peak_kind = _peaks()
+    achieved = kv_bytes / (dec_ms_avg * 1e-3) / 1e9
+    seq_heads = w.num_seqs * w.num_q_heads
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": dt,
+        "data": "synthetic (seeded PCG64 N(0,1) K/V/q; block tables from a seeded random "
+                "permutation of the pool)",
+        "config": {"workload": WORKLOAD_TEXT.get(args.config, args.config), "name": args.config,
+                   "num_seqs": w.num_seqs, "num_q_heads": w.num_q_heads,
+                   "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim,
+                   "block_size": w.block_size, "num_blocks": w.num_blocks,
+                   "partition_tokens": P, "kv_read_bytes_per_step": kv_bytes,
+                   "l2": "KV pool larger than L2 and a 256 MB L2 flush before every step "
+                         "(outside the timed events)",
+                   "parallelism": f"weak: {ws} independent replicas of the batch, one per GPU"},
+        "seq_heads_per_s": round(ws * seq_heads / (ms_per_step * 1e-3), 1),
+        "hbm_frac": round(value / ws / peak, 4),
+        "roofline": {"bound": "hbm", "kernel": "pa_decode (partition kernel + split-K merge)",
+                     "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "peak_source": f"{peak_kind} hbm_gbs",
+                     "traffic": _ncu_traffic(args.config),
+                     "algorithmic_bytes_per_launch": kv_bytes,
+                     "avg_launch_ms": round(dec_ms_avg, 5)},
+        "e2e": {"value": round(ws * kv_bytes / (e2e_avg * 1e-3) / 1e9, 2), "unit": "GB/s",
+                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+                "ms_per_step": round(e2e_avg, 5)},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk.summary(),
+        "wall_s_timed_region": round(t_wall, 4),
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = _cpu_baseline(w)
+    print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+# ---------------------------------------------------------------------------
+# reference arm: the oracle on the host cores
+# ---------------------------------------------------------------------------
+
+def run_reference(args):
+    ws, rank, _ = _dist_env()
+    if rank != 0:
+        return
+    import concurrent.futures as cf
+    import oracle
+    from paged_kv_cache_314_gb300 import workloads as wl
+    oracle.build()
+    w = wl.by_name(args.config, poison=False, **({"partition_tokens": args.partition}
+                                                   if args.partition is not None else {}))
+    threads = os.cpu_count() or 1
+    # each step: the oracle's copy_blocks and kv_write, then decode of a bounded
+    # sample of sequences (whole sequences, in order) spread over host threads
+    per_tok = 2 * w.num_kv_heads * w.head_dim * w.elem_bytes
+    cum = np.cumsum(np.clip(w.context_lens, 0, None).astype(np.int64) * per_tok)
+    n = int(np.searchsorted(cum, args.reference_sample_bytes)) + 1
+    n = max(1, min(w.num_seqs, n))
+    sample_bytes = int(cum[n - 1])
+    kc, vc = w.k_cache, w.v_cache
+
+    def one(s):
+        oracle.decode(np.ascontiguousarray(w.q[s:s + 1]), kc, vc,
+                      np.ascontiguousarray(w.block_tables[s:s + 1]),
+                      np.ascontiguousarray(w.context_lens[s:s + 1]), scale=w.scale, dtype=w.dtype)
+
+    times = []
+    with cf.ThreadPoolExecutor(threads) as ex:
+        for i in range(args.warmup + args.steps):
+            t0 = time.perf_counter()
+            if w.num_pairs:
+                oracle.copy_blocks(kc, vc, w.block_mapping, dtype=w.dtype)
+            oracle.kv_write(kc, vc, w.k_new, w.v_new, w.slot_mapping, dtype=w.dtype)
+            list(ex.map(one, range(n)))
+            if i >= args.warmup:
+                times.append(time.perf_counter() - t0)
+    ms = float(np.mean(times)) * 1e3
+    value = sample_bytes / (ms * 1e-3) / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+        "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
+        "data": "synthetic (same seeded workload as the GPU arm)",
+        "config": {"workload": WORKLOAD_TEXT.get(args.config, args.config), "name": args.config,
+                   "sample_seqs": n, "sample_kv_bytes": sample_bytes},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads,
+                         "kind": "oracle",
+                         "sample": f"per step: oracle copy_blocks + kv_write + decode of the "
+                                   f"first {n} of {w.num_seqs} sequences ({sample_bytes / 1e6:.0f}"
+                                   f" MB of K/V), fp64 C oracle, {threads} host threads"},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--config", default="llama7b", choices=sorted(WORKLOAD_TEXT))
+    ap.add_argument("--partition", type=int, default=None,
+                    help="tokens per split-K partition (default: the workload's, else the library's)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--reference-sample-bytes", type=int, default=400 << 20)
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)  # at least three untimed warm-up steps
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,158 @@
+/* pa.h -- C ABI of libpa: paged KV-cache decode attention for one GB300 (sm_103a).
+ *
+ * Three operations over a KV cache held in fixed-size physical blocks:
+ *
+ *   pa_kv_write     write each new token's K and V rows into its slot
+ *   pa_copy_blocks  copy whole blocks (copy-on-write of shared blocks)
+ *   pa_decode       one query per sequence attends to its cached tokens,
+ *                   walking the sequence's block table
+ *
+ * Memory model ("PagedAttention" (compassingai.com) §5; "PagedAttention 深度解析"
+ * §二): the cache is a pool of num_blocks physical blocks of block_size tokens;
+ * sequence s owns a block table whose entry i is the physical block that holds
+ * its tokens [i*block_size, (i+1)*block_size); only the first context_len[s]
+ * tokens are meaningful, so only the last block of a sequence is partly filled
+ * ("PagedAttention" (compassingai.com) §7).
+ *
+ * Layouts (row-major, element type = dtype unless stated):
+ *   q, out           [num_seqs][num_q_heads][head_dim]
+ *   k_cache, v_cache [num_blocks][num_kv_heads][block_size][head_dim]
+ *   k_new, v_new     [num_tokens][num_kv_heads][head_dim]
+ *   block_tables     int32 [num_seqs][max_blocks_per_seq]
+ *   context_lens     int32 [num_seqs]
+ *   slot_mapping     int64 [num_tokens], slot = block * block_size + offset
+ *   block_mapping    int32 [num_pairs][2] = (src, dst)
+ *
+ * Conventions shared by every call:
+ *   - Ownership: every pointer is device memory owned by the caller.  The
+ *     library allocates nothing, keeps no state between calls and never
+ *     synchronises the stream.  Device pointers must be 16-byte aligned.
+ *   - Asynchrony: work is enqueued on `stream` (NULL = the legacy default
+ *     stream).  The returned status covers what the host can check (null
+ *     pointers, sizes, unsupported shapes, launch failures); nothing is
+ *     enqueued when it is not PA_OK.
+ *   - Data errors never trap and never touch memory out of range ("PagedAttention"
+ *     (compassingai.com) §13: bounds checks in the kernel, explicit errors
+ *     instead of crashes).  The offending entry is skipped and a PA_DERR_* bit
+ *     is OR-ed into *d_err (a device word the caller zeroes and reads after
+ *     the stream synchronises; d_err may be NULL).
+ */
+#ifndef PA_H
+#define PA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t. */
+struct CUstream_st;
+typedef struct CUstream_st* pa_stream_t;
+
+typedef enum pa_status {
+    PA_OK = 0,
+    PA_ERR_INVALID_ARG = 1,         /* null pointer, bad size, misaligned pointer      */
+    PA_ERR_UNSUPPORTED = 2,         /* valid but not built: head_dim, block_size, dtype */
+    PA_ERR_WORKSPACE_TOO_SMALL = 3, /* decode workspace below pa_decode_workspace_size  */
+    PA_ERR_CUDA = 4                 /* a CUDA runtime call or launch failed             */
+} pa_status;
+
+typedef enum pa_dtype {
+    PA_F32 = 0,  /* IEEE binary32 */
+    PA_F16 = 1,  /* IEEE binary16 */
+    PA_BF16 = 2  /* bfloat16      */
+} pa_dtype;
+
+/* Bits OR-ed into *d_err by the kernels. */
+#define PA_DERR_BLOCK_OOB 1u        /* a needed block id is outside [0, num_blocks): its tokens are skipped */
+#define PA_DERR_CTX_OOB 2u          /* context_len < 0 or > max_blocks_per_seq*block_size: output row zeroed */
+#define PA_DERR_SLOT_OOB 4u         /* slot >= num_blocks*block_size: that token is not written            */
+#define PA_DERR_TIMEOUT 8u          /* a bounded wait inside a kernel gave up; outputs of that CTA unset   */
+#define PA_DERR_MAPPING_CONFLICT 16u /* pa_copy_blocks_check: a dst repeats or is also a src                */
+
+/* ABI version of this header (incremented on any signature change). */
+int pa_abi_version(void);
+
+/* Human-readable name of a status code (static storage). */
+const char* pa_status_string(pa_status status);
+
+/* pa_kv_write -- slot-mapped write of the new tokens' K/V.
+ *
+ * For each token t with slot_mapping[t] >= 0: blk = slot / block_size,
+ * off = slot % block_size, and for every kv head h the rows k_new[t][h][:] and
+ * v_new[t][h][:] are copied to k_cache[blk][h][off][:] and v_cache[blk][h][off][:].
+ * The new token's K/V is the only K/V computed in a decode step and goes into
+ * the sequence's current block (kwkr.cn "vLLM PagedAttention 技术深度解析"
+ * §1.2.2, block allocation flow; wmrh.cn "paged attention", KV cache part).
+ * Negative slots are padding and are skipped silently; slots at or beyond
+ * num_blocks*block_size are skipped and flagged PA_DERR_SLOT_OOB.  Two tokens
+ * with the same slot leave one of the two rows (which one is unspecified).
+ * Requires head_dim * element size to be a multiple of 16 bytes.
+ */
+pa_status pa_kv_write(const void* k_new, const void* v_new, void* k_cache, void* v_cache,
+                      const int64_t* slot_mapping, int num_tokens, int num_kv_heads, int head_dim,
+                      int block_size, int num_blocks, pa_dtype dtype, uint32_t* d_err,
+                      pa_stream_t stream);
+
+/* pa_copy_blocks -- copy-on-write block copies.
+ *
+ * For each pair i, block block_mapping[i][0] (all kv heads, all block_size
+ * slots, K and V) is copied to block block_mapping[i][1].  A write to a block
+ * shared by several sequences (reference count above one) first takes a fresh
+ * block and copies the shared block's content into it ("PagedAttention"
+ * (compassingai.com) §6; kwkr.cn "vLLM PagedAttention 技术深度解析" §1.3.2).
+ * Pairs with an id outside [0, num_blocks) are skipped and flagged
+ * PA_DERR_BLOCK_OOB.  The result is defined when no dst repeats and no dst is
+ * also a src (pa_copy_blocks_check tests exactly that).
+ */
+pa_status pa_copy_blocks(void* k_cache, void* v_cache, const int32_t* block_mapping, int num_pairs,
+                         int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                         pa_dtype dtype, uint32_t* d_err, pa_stream_t stream);
+
+/* pa_copy_blocks_check -- optional validation of a block_mapping on the device:
+ * flags PA_DERR_MAPPING_CONFLICT when a dst appears twice or also appears as a
+ * src.  O(num_pairs^2) comparisons; meant for debugging and tests. */
+pa_status pa_copy_blocks_check(const int32_t* block_mapping, int num_pairs, uint32_t* d_err,
+                               pa_stream_t stream);
+
+/* pa_decode_partition_tokens -- tokens per split-K partition that pa_decode
+ * uses for these sizes: partition_tokens itself when it is positive, else the
+ * library's choice (a multiple of block_size).  Returns -1 for invalid sizes. */
+int pa_decode_partition_tokens(int max_blocks_per_seq, int block_size, int partition_tokens);
+
+/* pa_decode_workspace_size -- bytes of device workspace pa_decode needs for
+ * these sizes (0 when no sequence can span more than one partition). */
+size_t pa_decode_workspace_size(int num_seqs, int num_q_heads, int head_dim, int max_blocks_per_seq,
+                                int block_size, int partition_tokens);
+
+/* pa_decode -- paged decode attention.
+ *
+ * For each sequence s and query head h, with n = context_lens[s],
+ * g = num_q_heads / num_kv_heads and kv head h / g:
+ *   K_s, V_s = the rows of tokens t < n, token t read from physical block
+ *              block_tables[s][t / block_size] at offset t % block_size
+ *   out[s][h] = softmax(scale * q[s][h] . K_s^T) . V_s
+ * The kernel walks the block table block by block and the tokens of each
+ * block in order, staging each block's K and V in shared memory and taking
+ * the dot products with q there ("PagedAttention" (compassingai.com) §8;
+ * "PagedAttention 深度解析" §二 item 3).  Long sequences are split into
+ * partitions of pa_decode_partition_tokens() tokens whose partial softmax
+ * states are merged by a second kernel (log-sum-exp), which needs `workspace`
+ * of at least pa_decode_workspace_size() bytes (may be NULL when that is 0).
+ * n == 0 gives a zero row.  Accumulation is fp32; out has dtype `dtype`.
+ * Supported: head_dim 64 or 128; block_size a multiple of 16 up to 256;
+ * num_q_heads a multiple of num_kv_heads.
+ */
+pa_status pa_decode(void* out, const void* q, const void* k_cache, const void* v_cache,
+                    const int32_t* block_tables, int max_blocks_per_seq,
+                    const int32_t* context_lens, int num_seqs, int num_q_heads, int num_kv_heads,
+                    int head_dim, int block_size, int num_blocks, float scale,
+                    int partition_tokens, pa_dtype dtype, void* workspace,
+                    size_t workspace_bytes, uint32_t* d_err, pa_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* PA_H */

@@ -1,0 +1,196 @@
+"""ctypes binding of libpa (include/pa.h): argument marshalling only.
+
+Every function takes torch CUDA tensors, derives the sizes from their shapes,
+passes ``data_ptr()`` values and the current CUDA stream to the C ABI, and
+raises ``PaError`` on a non-OK status.  All compute runs in libpa's kernels;
+there is no fallback.  The shared library is built in-tree by
+``paged_kv_cache_314_gb300._build.build()``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional
+
+import torch
+
+from . import _build
+
+PA_OK = 0
+STATUS_NAMES = {0: "PA_OK", 1: "PA_ERR_INVALID_ARG", 2: "PA_ERR_UNSUPPORTED",
+                3: "PA_ERR_WORKSPACE_TOO_SMALL", 4: "PA_ERR_CUDA"}
+DERR_BLOCK_OOB = 1
+DERR_CTX_OOB = 2
+DERR_SLOT_OOB = 4
+DERR_TIMEOUT = 8
+DERR_MAPPING_CONFLICT = 16
+
+DTYPE_CODE = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}
+EXPORTED = ("pa_abi_version", "pa_status_string", "pa_kv_write", "pa_copy_blocks",
+            "pa_copy_blocks_check", "pa_decode_partition_tokens", "pa_decode_workspace_size",
+            "pa_decode")
+
+_lock = threading.Lock()
+_lib: Optional[ctypes.CDLL] = None
+
+
+class PaError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {STATUS_NAMES.get(status, status)} ({_status_string(status)})")
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def load() -> ctypes.CDLL:
+    """Load libpa.so; raise if it has not been built (there is no other path)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = library_path()
+        if not os.path.exists(path):
+            raise RuntimeError(f"libpa.so not found at {path}: build it with "
+                               "`python -c 'import __graft_entry__ as g; g.build()'`")
+        lib = ctypes.CDLL(path)
+        vp, i32, u64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+        lib.pa_abi_version.restype = i32
+        lib.pa_abi_version.argtypes = []
+        lib.pa_status_string.restype = ctypes.c_char_p
+        lib.pa_status_string.argtypes = [i32]
+        lib.pa_kv_write.restype = i32
+        lib.pa_kv_write.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, vp, vp]
+        lib.pa_copy_blocks.restype = i32
+        lib.pa_copy_blocks.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, i32, vp, vp]
+        lib.pa_copy_blocks_check.restype = i32
+        lib.pa_copy_blocks_check.argtypes = [vp, i32, vp, vp]
+        lib.pa_decode_partition_tokens.restype = i32
+        lib.pa_decode_partition_tokens.argtypes = [i32, i32, i32]
+        lib.pa_decode_workspace_size.restype = u64
+        lib.pa_decode_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32]
+        lib.pa_decode.restype = i32
+        lib.pa_decode.argtypes = [vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, i32,
+                                  ctypes.c_float, i32, i32, vp, u64, vp, vp]
+        _lib = lib
+        return lib
+
+
+def _status_string(status: int) -> str:
+    try:
+        return load().pa_status_string(status).decode()
+    except Exception:  # library missing while formatting an error
+        return "?"
+
+
+def _check(status: int, what: str) -> None:
+    if status != PA_OK:
+        raise PaError(status, what)
+
+
+def _stream(stream, device) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _cuda_contig(name: str, t: torch.Tensor) -> None:
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def abi_version() -> int:
+    return int(load().pa_abi_version())
+
+
+def kv_write(k_new: torch.Tensor, v_new: torch.Tensor, k_cache: torch.Tensor,
+             v_cache: torch.Tensor, slot_mapping: torch.Tensor,
+             d_err: Optional[torch.Tensor] = None, stream=None) -> None:
+    """k_cache[slot//B][h][slot%B] = k_new[t][h] (and V) for every token t."""
+    for n, t in (("k_new", k_new), ("v_new", v_new), ("k_cache", k_cache), ("v_cache", v_cache),
+                 ("slot_mapping", slot_mapping)):
+        _cuda_contig(n, t)
+    if slot_mapping.dtype != torch.int64:
+        raise ValueError("slot_mapping must be int64")
+    NB, Hkv, B, d = k_cache.shape
+    T = slot_mapping.shape[0]
+    st = load().pa_kv_write(_ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache),
+                            _ptr(slot_mapping), T, Hkv, d, B, NB, DTYPE_CODE[k_cache.dtype],
+                            _ptr(d_err), _stream(stream, k_cache.device))
+    _check(st, "pa_kv_write")
+
+
+def copy_blocks(k_cache: torch.Tensor, v_cache: torch.Tensor, block_mapping: torch.Tensor,
+                d_err: Optional[torch.Tensor] = None, stream=None) -> None:
+    """Copy block src -> dst (all kv heads, K and V) for each (src, dst) row."""
+    for n, t in (("k_cache", k_cache), ("v_cache", v_cache), ("block_mapping", block_mapping)):
+        _cuda_contig(n, t)
+    if block_mapping.dtype != torch.int32:
+        raise ValueError("block_mapping must be int32 [P][2]")
+    NB, Hkv, B, d = k_cache.shape
+    P = block_mapping.numel() // 2
+    st = load().pa_copy_blocks(_ptr(k_cache), _ptr(v_cache), _ptr(block_mapping), P, Hkv, d, B,
+                               NB, DTYPE_CODE[k_cache.dtype], _ptr(d_err),
+                               _stream(stream, k_cache.device))
+    _check(st, "pa_copy_blocks")
+
+
+def copy_blocks_check(block_mapping: torch.Tensor, d_err: torch.Tensor, stream=None) -> None:
+    _cuda_contig("block_mapping", block_mapping)
+    P = block_mapping.numel() // 2
+    st = load().pa_copy_blocks_check(_ptr(block_mapping), P, _ptr(d_err),
+                                     _stream(stream, block_mapping.device))
+    _check(st, "pa_copy_blocks_check")
+
+
+def decode_partition_tokens(max_blocks_per_seq: int, block_size: int,
+                            partition_tokens: int = 0) -> int:
+    return int(load().pa_decode_partition_tokens(max_blocks_per_seq, block_size, partition_tokens))
+
+
+def decode_workspace_size(num_seqs: int, num_q_heads: int, head_dim: int, max_blocks_per_seq: int,
+                          block_size: int, partition_tokens: int = 0) -> int:
+    return int(load().pa_decode_workspace_size(num_seqs, num_q_heads, head_dim,
+                                               max_blocks_per_seq, block_size, partition_tokens))
+
+
+def decode_workspace(q: torch.Tensor, k_cache: torch.Tensor, block_tables: torch.Tensor,
+                     partition_tokens: int = 0) -> Optional[torch.Tensor]:
+    """Allocate (with torch) the workspace pa_decode needs for these shapes."""
+    S, Hq, d = q.shape
+    n = decode_workspace_size(S, Hq, d, block_tables.shape[1], k_cache.shape[2], partition_tokens)
+    return torch.empty(n, dtype=torch.uint8, device=q.device) if n else None
+
+
+def decode(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+           block_tables: torch.Tensor, context_lens: torch.Tensor, scale: float,
+           partition_tokens: int = 0, workspace: Optional[torch.Tensor] = None,
+           d_err: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """out[s][h] = softmax(scale * q[s][h] . K_s^T) V_s through the block table."""
+    for n, t in (("out", out), ("q", q), ("k_cache", k_cache), ("v_cache", v_cache),
+                 ("block_tables", block_tables), ("context_lens", context_lens)):
+        _cuda_contig(n, t)
+    if block_tables.dtype != torch.int32 or context_lens.dtype != torch.int32:
+        raise ValueError("block_tables and context_lens must be int32")
+    S, Hq, d = q.shape
+    NB, Hkv, B, d2 = k_cache.shape
+    if d2 != d or out.shape != q.shape or out.dtype != q.dtype or k_cache.dtype != q.dtype:
+        raise ValueError("q, out, k_cache and v_cache must agree in head_dim and dtype")
+    MB = block_tables.shape[1]
+    if workspace is None:
+        workspace = decode_workspace(q, k_cache, block_tables, partition_tokens)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = load().pa_decode(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), MB,
+                          _ptr(context_lens), S, Hq, Hkv, d, B, NB, float(scale),
+                          int(partition_tokens), DTYPE_CODE[q.dtype], _ptr(workspace), ws_bytes,
+                          _ptr(d_err), _stream(stream, q.device))
+    _check(st, "pa_decode")
+    return out

@@ -1,0 +1,130 @@
+// decode.cu -- host side of pa_decode: argument checks, split-K planning,
+// workspace layout and dispatch to the typed kernels.
+#include <math.h>
+
+#include "decode_kernels.cuh"
+
+namespace pa {
+namespace {
+
+constexpr int kDefaultPartitionTokens = 256;
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+bool block_size_ok(int B) { return B >= 16 && B <= 256 && B % 16 == 0; }
+
+int max_parts_for(int max_blocks_per_seq, int block_size, int P) {
+    const long long max_ctx = static_cast<long long>(max_blocks_per_seq) * block_size;
+    return static_cast<int>((max_ctx + P - 1) / P);
+}
+
+struct WsLayout {
+    size_t m_off, l_off, o_off, bytes;
+};
+
+WsLayout ws_layout(int num_seqs, int num_q_heads, int head_dim, int max_parts) {
+    WsLayout w{0, 0, 0, 0};
+    if (max_parts <= 1) return w;
+    const size_t rows = static_cast<size_t>(num_seqs) * num_q_heads * max_parts;
+    w.m_off = 0;
+    w.l_off = round_up(rows * 4, 256);
+    w.o_off = w.l_off + round_up(rows * 4, 256);
+    w.bytes = w.o_off + round_up(rows * static_cast<size_t>(head_dim) * 4, 256);
+    return w;
+}
+
+// Largest power-of-two query-head tile (<= 8) that stays inside one kv head.
+int head_tile(int group) {
+    for (int gt = 8; gt > 1; gt >>= 1)
+        if (group % gt == 0) return gt;
+    return 1;
+}
+
+}  // namespace
+}  // namespace pa
+
+extern "C" int pa_decode_partition_tokens(int max_blocks_per_seq, int block_size,
+                                          int partition_tokens) {
+    using namespace pa;
+    if (max_blocks_per_seq <= 0 || !block_size_ok(block_size) || partition_tokens < 0) return -1;
+    if (partition_tokens > 0) return partition_tokens % block_size == 0 ? partition_tokens : -1;
+    const int P = kDefaultPartitionTokens;
+    return (P + block_size - 1) / block_size * block_size;
+}
+
+extern "C" size_t pa_decode_workspace_size(int num_seqs, int num_q_heads, int head_dim,
+                                           int max_blocks_per_seq, int block_size,
+                                           int partition_tokens) {
+    using namespace pa;
+    const int P = pa_decode_partition_tokens(max_blocks_per_seq, block_size, partition_tokens);
+    if (P <= 0 || num_seqs <= 0 || num_q_heads <= 0 || head_dim <= 0) return 0;
+    return ws_layout(num_seqs, num_q_heads, head_dim, max_parts_for(max_blocks_per_seq, block_size, P))
+        .bytes;
+}
+
+extern "C" pa_status pa_decode(void* out, const void* q, const void* k_cache, const void* v_cache,
+                               const int32_t* block_tables, int max_blocks_per_seq,
+                               const int32_t* context_lens, int num_seqs, int num_q_heads,
+                               int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                               float scale, int partition_tokens, pa_dtype dtype, void* workspace,
+                               size_t workspace_bytes, uint32_t* d_err, pa_stream_t stream) {
+    using namespace pa;
+    if (!valid_dtype(dtype)) return PA_ERR_INVALID_ARG;
+    if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 ||
+        block_size <= 0 || num_blocks <= 0 || max_blocks_per_seq <= 0 || partition_tokens < 0)
+        return PA_ERR_INVALID_ARG;
+    if (num_q_heads % num_kv_heads != 0 || !isfinite(scale)) return PA_ERR_INVALID_ARG;
+    if (head_dim != 64 && head_dim != 128) return PA_ERR_UNSUPPORTED;
+    if (!block_size_ok(block_size)) return PA_ERR_UNSUPPORTED;
+    if (static_cast<long long>(max_blocks_per_seq) * block_size > 0x7fffffffLL)
+        return PA_ERR_INVALID_ARG;
+    const int P = pa_decode_partition_tokens(max_blocks_per_seq, block_size, partition_tokens);
+    if (P <= 0) return PA_ERR_INVALID_ARG;
+    if (num_seqs == 0) return PA_OK;
+    if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens)
+        return PA_ERR_INVALID_ARG;
+    if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache))
+        return PA_ERR_INVALID_ARG;
+
+    const int max_parts = max_parts_for(max_blocks_per_seq, block_size, P);
+    const WsLayout ws = ws_layout(num_seqs, num_q_heads, head_dim, max_parts);
+    if (ws.bytes > 0) {
+        if (workspace == nullptr) return PA_ERR_INVALID_ARG;
+        if (workspace_bytes < ws.bytes) return PA_ERR_WORKSPACE_TOO_SMALL;
+        if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return PA_ERR_INVALID_ARG;
+    }
+    const int group = num_q_heads / num_kv_heads;
+    const int gt = head_tile(group);
+
+    DecodeParams p;
+    p.out = out;
+    p.q = q;
+    p.k_cache = static_cast<const unsigned char*>(k_cache);
+    p.v_cache = static_cast<const unsigned char*>(v_cache);
+    p.block_tables = block_tables;
+    p.context_lens = context_lens;
+    unsigned char* wsb = static_cast<unsigned char*>(workspace);
+    p.ws_m = ws.bytes ? reinterpret_cast<float*>(wsb + ws.m_off) : nullptr;
+    p.ws_l = ws.bytes ? reinterpret_cast<float*>(wsb + ws.l_off) : nullptr;
+    p.ws_o = ws.bytes ? reinterpret_cast<float*>(wsb + ws.o_off) : nullptr;
+    p.d_err = d_err;
+    p.num_seqs = num_seqs;
+    p.num_q_heads = num_q_heads;
+    p.num_kv_heads = num_kv_heads;
+    p.group = group;
+    p.head_tiles = num_q_heads / gt;
+    p.max_blocks_per_seq = max_blocks_per_seq;
+    p.block_size = block_size;
+    p.num_blocks = num_blocks;
+    p.partition_tokens = P;
+    p.max_parts = max_parts;
+    p.qk_scale_log2 = scale * 1.4426950408889634f;  // log2(e)
+
+    const cudaStream_t st = as_cuda(stream);
+    switch (dtype) {
+        case PA_F32: return launch_decode_f32(p, head_dim, gt, st);
+        case PA_F16: return launch_decode_f16(p, head_dim, gt, st);
+        case PA_BF16: return launch_decode_bf16(p, head_dim, gt, st);
+    }
+    return PA_ERR_INVALID_ARG;
+}

@@ -1,0 +1,490 @@
+// decode_kernels.cuh -- paged decode attention kernels (SIMT path).
+//
+// What is computed: for each sequence s and query head h, the softmax of the
+// scaled dot products of q[s][h] with the K rows of the sequence's first
+// context_len tokens, times their V rows.  The K/V rows are found through the
+// block table: logical block i lives in physical block table[i], token t at
+// offset t mod B ("PagedAttention" (compassingai.com) §5; "PagedAttention
+// 深度解析" §二).  The walk goes block by block in table order and token by
+// token inside a block; a block's K is staged in shared memory where many
+// threads take their dot products with q ("PagedAttention" (compassingai.com)
+// §8).
+//
+// How (GB300 design):
+//  * One CTA per (sequence, group of GT query heads sharing one kv head,
+//    partition of P tokens).  Partitions bound the work of one CTA so that
+//    skewed context lengths do not leave a long tail; a second kernel merges
+//    the partitions' softmax states (log-sum-exp).
+//  * Warp 4 is the producer: it reads the partition's slice of the block
+//    table (one entry per lane, shuffled out) and lane 0 issues bulk copies
+//    (cp.async.bulk, TMA engine) of the 16-token K and V sub-blocks into a
+//    ring of kStages shared-memory stages guarded by mbarriers.  The copies
+//    carry an L2 evict-first hint: each K/V byte is read once per step.
+//  * Warps 0-3 consume: each lane owns one 16-byte column slice of a token row
+//    (kLpt lanes per row), so a warp reads kTpp whole rows per 128-bit shared
+//    load without bank conflicts; dot products finish with xor shuffles; the
+//    softmax is online (running max m, running sum l, fp32) in the log2
+//    domain (q is pre-scaled by scale*log2(e)), updated once per stage.
+//  * Tokens past context_len and tokens of blocks whose id fails the bounds
+//    check are masked by select, never by arithmetic, so poison in unused
+//    slots (NaN) cannot leak into the result.
+//  * Every wait is bounded (mbar_wait): on timeout the CTA reports
+//    PA_DERR_TIMEOUT, stops issuing copies, waits for the copies it already
+//    issued and returns without writing its outputs.
+#pragma once
+
+#include "pa_device.cuh"
+#include "pa_host.h"
+
+namespace pa {
+
+struct DecodeParams {
+    void* out;
+    const void* q;
+    const unsigned char* k_cache;
+    const unsigned char* v_cache;
+    const int32_t* block_tables;
+    const int32_t* context_lens;
+    float* ws_m;  // [S][Hq][max_parts] running max (log2 domain) per partition
+    float* ws_l;  // [S][Hq][max_parts] running sum per partition
+    float* ws_o;  // [S][Hq][max_parts][D] unnormalised output per partition
+    uint32_t* d_err;
+    int num_seqs;
+    int num_q_heads;
+    int num_kv_heads;
+    int group;       // query heads per kv head
+    int head_tiles;  // num_q_heads / GT
+    int max_blocks_per_seq;
+    int block_size;
+    int num_blocks;
+    int partition_tokens;
+    int max_parts;
+    float qk_scale_log2;  // scale * log2(e)
+};
+
+template <typename T, int D, int GT>
+struct DecodeTile {
+    static constexpr int kElem = sizeof(T);
+    static constexpr int kVec = 16 / kElem;           // elements per 16-byte access
+    static constexpr int kLpt = D / kVec;             // lanes per token row
+    static constexpr int kTpp = 32 / kLpt;            // token rows per warp pass
+    static constexpr int kRowBytes = D * kElem;
+    static constexpr int kConsumerWarps = 4;
+    static constexpr int kThreads = 32 * (kConsumerWarps + 1);
+    static constexpr int kTps = 8192 / kRowBytes;     // tokens per stage (8 KB of K + 8 KB of V)
+    static constexpr int kPasses = kTps / (kConsumerWarps * kTpp);
+    static constexpr int kStages = 4;
+    static constexpr int kSubs = kTps / 16;           // 16-token bulk copies per tensor per stage
+    static constexpr int kStageBytes = 2 * kTps * kRowBytes;
+    static constexpr int kRingBytes = kStages * kStageBytes;
+    static constexpr int kMergeFloats = kConsumerWarps * GT * (D + 2);
+    static constexpr int kBarOffset = kRingBytes + ((kMergeFloats * 4 + 15) / 16) * 16;
+    // full[kStages], empty[kStages], mask[kStages], abort flag
+    static constexpr int kSmemBytes = kBarOffset + 3 * kStages * 8 + 16;
+    static_assert(kLpt >= 1 && kLpt <= 32 && 32 % kLpt == 0, "row must split over lanes");
+    static_assert(kTps % 16 == 0 && kTps <= 64, "stage holds whole 16-token sub-blocks");
+    static_assert(kPasses >= 1 && kPasses * kConsumerWarps * kTpp == kTps, "passes tile the stage");
+};
+
+template <typename T, int D, int GT>
+__device__ __forceinline__ void decode_produce(const DecodeParams& p, unsigned char* smem, int s,
+                                               int hk, int tok_begin, int tok_end, int nstages) {
+    using C = DecodeTile<T, D, GT>;
+    const int lane = threadIdx.x & 31;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBarOffset);
+    uint64_t* masks = bars + 2 * C::kStages;
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(masks + C::kStages);
+    const uint32_t full0 = smem_addr(bars);
+    const uint32_t empty0 = smem_addr(bars + C::kStages);
+
+    const uint64_t policy = l2_evict_first_policy();
+    const int B = p.block_size;
+    const int32_t* trow = p.block_tables + static_cast<size_t>(s) * p.max_blocks_per_seq;
+    const int blk_end = (tok_end + B - 1) / B;
+    int win = tok_begin / B;  // first logical block held in the lanes' window
+    int32_t entry = (win + lane < blk_end) ? __ldg(trow + win + lane) : -1;
+    const size_t head_bytes = static_cast<size_t>(B) * C::kRowBytes;
+    const size_t block_bytes = static_cast<size_t>(p.num_kv_heads) * head_bytes;
+    const unsigned char* kbase = p.k_cache + static_cast<size_t>(hk) * head_bytes;
+    const unsigned char* vbase = p.v_cache + static_cast<size_t>(hk) * head_bytes;
+
+    int issued = 0;
+    bool oob = false;
+    for (int c = 0; c < nstages; ++c) {
+        const int st = c % C::kStages;
+        const uint32_t round = static_cast<uint32_t>(c / C::kStages);
+        if (c >= C::kStages && !mbar_wait(empty0 + 8 * st, (round - 1) & 1)) {
+            if (lane == 0) report(p.d_err, PA_DERR_TIMEOUT);
+            *abort_flag = 1;
+            break;
+        }
+        if (*abort_flag) break;
+        const int t0 = tok_begin + c * C::kTps;
+        const int t1 = min(t0 + C::kTps, tok_end);
+        size_t src_off[C::kSubs];
+        uint32_t len_bytes[C::kSubs];
+        uint32_t bytes = 0;
+        uint64_t mask = 0;
+#pragma unroll
+        for (int r = 0; r < C::kSubs; ++r) {
+            const int t = t0 + 16 * r;
+            len_bytes[r] = 0;
+            src_off[r] = 0;
+            if (t < t1) {  // warp-uniform
+                const int lb = t / B;
+                const int off = t - lb * B;
+                const int len = min(16, t1 - t);
+                while (lb - win >= 32) {
+                    win += 32;
+                    entry = (win + lane < blk_end) ? __ldg(trow + win + lane) : -1;
+                }
+                const int pb = __shfl_sync(0xffffffffu, entry, lb - win);
+                if (static_cast<unsigned>(pb) < static_cast<unsigned>(p.num_blocks)) {
+                    src_off[r] = static_cast<size_t>(pb) * block_bytes +
+                                 static_cast<size_t>(off) * C::kRowBytes;
+                    len_bytes[r] = static_cast<uint32_t>(len) * C::kRowBytes;
+                    bytes += 2u * len_bytes[r];
+                    mask |= ((1ull << len) - 1ull) << (16 * r);
+                } else {
+                    oob = true;
+                }
+            }
+        }
+        if (lane == 0) {
+            masks[st] = mask;
+            const uint32_t full = full0 + 8 * st;
+            mbar_arrive_expect_tx(full, bytes);
+            const uint32_t sK = smem_addr(smem + st * C::kStageBytes);
+            const uint32_t sV = sK + C::kTps * C::kRowBytes;
+#pragma unroll
+            for (int r = 0; r < C::kSubs; ++r) {
+                if (len_bytes[r] != 0) {
+                    bulk_g2s(sK + 16 * r * C::kRowBytes, kbase + src_off[r], len_bytes[r], full, policy);
+                    bulk_g2s(sV + 16 * r * C::kRowBytes, vbase + src_off[r], len_bytes[r], full, policy);
+                }
+            }
+        }
+        __syncwarp();
+        issued = c + 1;
+    }
+    if (lane == 0) {
+        if (oob) report(p.d_err, PA_DERR_BLOCK_OOB);
+        // No copy may still be writing shared memory when the CTA exits.
+        for (int c = max(0, issued - C::kStages); c < issued; ++c) {
+            const int st = c % C::kStages;
+            if (!mbar_wait(full0 + 8 * st, static_cast<uint32_t>(c / C::kStages) & 1))
+                report(p.d_err, PA_DERR_TIMEOUT);
+        }
+    }
+}
+
+template <typename T, int D, int GT>
+__device__ __forceinline__ void decode_consume(const DecodeParams& p, unsigned char* smem, int s,
+                                               int hq0, int part, int nparts, int nstages) {
+    using C = DecodeTile<T, D, GT>;
+    constexpr int kVec = C::kVec, kLpt = C::kLpt, kTpp = C::kTpp, W = C::kConsumerWarps;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int grp = lane / kLpt;  // which row of a pass this lane reads
+    const int lig = lane % kLpt;  // which 16-byte slice of the row
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBarOffset);
+    const uint64_t* masks = bars + 2 * C::kStages;
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 3 * C::kStages);
+    const uint32_t full0 = smem_addr(bars);
+    const uint32_t empty0 = smem_addr(bars + C::kStages);
+
+    float qf[GT][kVec];
+#pragma unroll
+    for (int j = 0; j < GT; ++j) {
+        const uint4 raw = __ldg(reinterpret_cast<const uint4*>(
+                                    static_cast<const T*>(p.q) +
+                                    (static_cast<size_t>(s) * p.num_q_heads + hq0 + j) * D) +
+                                lig);
+        Elem<T>::unpack(raw, qf[j]);
+#pragma unroll
+        for (int v = 0; v < kVec; ++v) qf[j][v] *= p.qk_scale_log2;
+    }
+    float m[GT], l[GT], o[GT][kVec];
+#pragma unroll
+    for (int j = 0; j < GT; ++j) {
+        m[j] = -INFINITY;
+        l[j] = 0.f;
+#pragma unroll
+        for (int v = 0; v < kVec; ++v) o[j][v] = 0.f;
+    }
+
+    for (int c = 0; c < nstages; ++c) {
+        const int st = c % C::kStages;
+        const uint32_t round = static_cast<uint32_t>(c / C::kStages);
+        if (!mbar_wait(full0 + 8 * st, round & 1)) {
+            if (lane == 0) report(p.d_err, PA_DERR_TIMEOUT);
+            *abort_flag = 1;
+            break;
+        }
+        const uint64_t mask = masks[st];
+        const unsigned char* sK = smem + st * C::kStageBytes;
+        const unsigned char* sV = sK + C::kTps * C::kRowBytes;
+        float x[C::kPasses][GT];
+        bool valid[C::kPasses];
+#pragma unroll
+        for (int ps = 0; ps < C::kPasses; ++ps) {
+            const int ti = (ps * W + warp) * kTpp + grp;
+            valid[ps] = (mask >> ti) & 1ull;
+            const uint4 raw = *reinterpret_cast<const uint4*>(sK + ti * C::kRowBytes + lig * 16);
+            float kf[kVec];
+            Elem<T>::unpack(raw, kf);
+#pragma unroll
+            for (int j = 0; j < GT; ++j) {
+                float acc = 0.f;
+#pragma unroll
+                for (int v = 0; v < kVec; ++v) acc = fmaf(qf[j][v], kf[v], acc);
+                x[ps][j] = acc;
+            }
+        }
+#pragma unroll
+        for (int ps = 0; ps < C::kPasses; ++ps)
+#pragma unroll
+            for (int j = 0; j < GT; ++j)
+#pragma unroll
+                for (int off = kLpt / 2; off > 0; off >>= 1)
+                    x[ps][j] += __shfl_xor_sync(0xffffffffu, x[ps][j], off);
+#pragma unroll
+        for (int j = 0; j < GT; ++j) {
+            float mx = -INFINITY;
+#pragma unroll
+            for (int ps = 0; ps < C::kPasses; ++ps) mx = fmaxf(mx, valid[ps] ? x[ps][j] : -INFINITY);
+#pragma unroll
+            for (int off = kLpt; off < 32; off <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+            const float m_new = fmaxf(m[j], mx);
+            const float alpha = (m_new == -INFINITY) ? 1.f : exp2f(m[j] - m_new);
+            m[j] = m_new;
+            l[j] *= alpha;
+#pragma unroll
+            for (int v = 0; v < kVec; ++v) o[j][v] *= alpha;
+        }
+#pragma unroll
+        for (int ps = 0; ps < C::kPasses; ++ps) {
+            const int ti = (ps * W + warp) * kTpp + grp;
+            const uint4 raw = *reinterpret_cast<const uint4*>(sV + ti * C::kRowBytes + lig * 16);
+            float vf[kVec];
+            Elem<T>::unpack(raw, vf);
+#pragma unroll
+            for (int v = 0; v < kVec; ++v) vf[v] = valid[ps] ? vf[v] : 0.f;
+#pragma unroll
+            for (int j = 0; j < GT; ++j) {
+                const float pw = valid[ps] ? exp2f(x[ps][j] - m[j]) : 0.f;
+                l[j] += pw;
+#pragma unroll
+                for (int v = 0; v < kVec; ++v) o[j][v] = fmaf(pw, vf[v], o[j][v]);
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty0 + 8 * st);
+    }
+
+    // Rows of one pass were split over kTpp lane groups that share m: add them up.
+#pragma unroll
+    for (int j = 0; j < GT; ++j) {
+#pragma unroll
+        for (int off = kLpt; off < 32; off <<= 1) {
+            l[j] += __shfl_xor_sync(0xffffffffu, l[j], off);
+#pragma unroll
+            for (int v = 0; v < kVec; ++v) o[j][v] += __shfl_xor_sync(0xffffffffu, o[j][v], off);
+        }
+    }
+    float* merge_m = reinterpret_cast<float*>(smem + C::kRingBytes);  // [W][GT]
+    float* merge_l = merge_m + W * GT;                                // [W][GT]
+    float* merge_o = merge_l + W * GT;                                // [W][GT][D]
+    if (grp == 0) {
+#pragma unroll
+        for (int j = 0; j < GT; ++j)
+#pragma unroll
+            for (int v = 0; v < kVec; ++v) merge_o[(warp * GT + j) * D + lig * kVec + v] = o[j][v];
+    }
+    if (lane == 0) {
+#pragma unroll
+        for (int j = 0; j < GT; ++j) {
+            merge_m[warp * GT + j] = m[j];
+            merge_l[warp * GT + j] = l[j];
+        }
+    }
+    named_barrier(1, W * 32);
+    if (*abort_flag) return;
+
+    const bool direct = nparts == 1;
+    for (int idx = threadIdx.x; idx < GT * D; idx += W * 32) {
+        const int j = idx / D;
+        const int dd = idx - j * D;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < W; ++w) M = fmaxf(M, merge_m[w * GT + j]);
+        float L = 0.f, O = 0.f;
+        if (M != -INFINITY) {
+#pragma unroll
+            for (int w = 0; w < W; ++w) {
+                const float mw = merge_m[w * GT + j];
+                if (mw != -INFINITY) {
+                    const float sc = exp2f(mw - M);
+                    L = fmaf(merge_l[w * GT + j], sc, L);
+                    O = fmaf(merge_o[(w * GT + j) * D + dd], sc, O);
+                }
+            }
+        }
+        const size_t row = static_cast<size_t>(s) * p.num_q_heads + hq0 + j;
+        if (direct) {
+            static_cast<T*>(p.out)[row * D + dd] = Elem<T>::from_float(L > 0.f ? O / L : 0.f);
+        } else {
+            const size_t r = row * p.max_parts + part;
+            p.ws_o[r * D + dd] = O;
+            if (dd == 0) {
+                p.ws_m[r] = M;
+                p.ws_l[r] = L;
+            }
+        }
+    }
+}
+
+template <typename T, int D, int GT>
+__global__ void __launch_bounds__(DecodeTile<T, D, GT>::kThreads)
+    decode_partition_kernel(const DecodeParams p) {
+    using C = DecodeTile<T, D, GT>;
+    extern __shared__ __align__(128) unsigned char smem[];
+    const int warp = threadIdx.x >> 5;
+
+    const int part = static_cast<int>(blockIdx.x % static_cast<unsigned>(p.max_parts));
+    const int rest = static_cast<int>(blockIdx.x / static_cast<unsigned>(p.max_parts));
+    const int ht = rest % p.head_tiles;
+    const int s = rest / p.head_tiles;
+    const int hq0 = ht * GT;
+    const int hk = hq0 / p.group;
+
+    const int ctx = p.context_lens[s];
+    const int max_ctx = p.max_blocks_per_seq * p.block_size;
+    if (ctx < 0 || ctx > max_ctx) {
+        if (part == 0) {
+            if (threadIdx.x == 0) report(p.d_err, PA_DERR_CTX_OOB);
+            T* out = static_cast<T*>(p.out) + (static_cast<size_t>(s) * p.num_q_heads + hq0) * D;
+            for (int i = threadIdx.x; i < GT * D; i += blockDim.x) out[i] = Elem<T>::from_float(0.f);
+        }
+        return;
+    }
+    const int P = p.partition_tokens;
+    const int nparts = ctx == 0 ? 1 : (ctx + P - 1) / P;
+    if (part >= nparts) return;
+    const int tok_begin = part * P;
+    const int tok_end = min(tok_begin + P, ctx);
+    const int nstages = (tok_end - tok_begin + C::kTps - 1) / C::kTps;
+
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBarOffset);
+    if (threadIdx.x == 0) {
+#pragma unroll
+        for (int st = 0; st < C::kStages; ++st) {
+            mbar_init(smem_addr(bars + st), 1);
+            mbar_init(smem_addr(bars + C::kStages + st), C::kConsumerWarps);
+        }
+        *reinterpret_cast<volatile int*>(bars + 3 * C::kStages) = 0;
+        fence_barrier_init();
+    }
+    __syncthreads();
+
+    if (warp == C::kConsumerWarps)
+        decode_produce<T, D, GT>(p, smem, s, hk, tok_begin, tok_end, nstages);
+    else
+        decode_consume<T, D, GT>(p, smem, s, hq0, part, nparts, nstages);
+}
+
+// Merges the partitions of one (sequence, query head): M = max_i m_i,
+// out = sum_i 2^(m_i-M) o_i / sum_i 2^(m_i-M) l_i.  Four warps split the
+// partitions; each lane owns D/32 output columns.
+template <typename T, int D>
+__global__ void __launch_bounds__(128) decode_reduce_kernel(const DecodeParams p) {
+    constexpr int kCols = D / 32;
+    const int sh = blockIdx.x;
+    const int s = sh / p.num_q_heads;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int ctx = p.context_lens[s];
+    if (ctx < 0 || ctx > p.max_blocks_per_seq * p.block_size) return;
+    const int nparts = ctx == 0 ? 1 : (ctx + p.partition_tokens - 1) / p.partition_tokens;
+    if (nparts <= 1) return;
+    const size_t row = static_cast<size_t>(sh) * p.max_parts;
+
+    __shared__ float red_m[4];
+    __shared__ float red_l[4];
+    __shared__ float red_o[4][D];
+    float M = -INFINITY;
+    for (int i = threadIdx.x; i < nparts; i += 128) M = fmaxf(M, p.ws_m[row + i]);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    if (lane == 0) red_m[warp] = M;
+    __syncthreads();
+    M = fmaxf(fmaxf(red_m[0], red_m[1]), fmaxf(red_m[2], red_m[3]));
+
+    float L = 0.f, O[kCols];
+#pragma unroll
+    for (int c = 0; c < kCols; ++c) O[c] = 0.f;
+    if (M != -INFINITY) {
+#pragma unroll 4
+        for (int i = warp; i < nparts; i += 4) {
+            const float mi = p.ws_m[row + i];
+            const float sc = (mi == -INFINITY) ? 0.f : exp2f(mi - M);
+            L = fmaf(sc, p.ws_l[row + i], L);
+            const float* po = p.ws_o + (row + i) * D + lane * kCols;
+#pragma unroll
+            for (int c = 0; c < kCols; ++c) O[c] = fmaf(sc, po[c], O[c]);
+        }
+    }
+    if (lane == 0) red_l[warp] = L;
+#pragma unroll
+    for (int c = 0; c < kCols; ++c) red_o[warp][lane * kCols + c] = O[c];
+    __syncthreads();
+    const float Lt = red_l[0] + red_l[1] + red_l[2] + red_l[3];
+    T* out = static_cast<T*>(p.out) + static_cast<size_t>(sh) * D;
+    for (int dd = threadIdx.x; dd < D; dd += 128) {
+        const float Ot = red_o[0][dd] + red_o[1][dd] + red_o[2][dd] + red_o[3][dd];
+        out[dd] = Elem<T>::from_float(Lt > 0.f ? Ot / Lt : 0.f);
+    }
+}
+
+template <typename T, int D, int GT>
+inline pa_status launch_decode_tile(const DecodeParams& p, cudaStream_t stream) {
+    using C = DecodeTile<T, D, GT>;
+    static std::atomic<uint64_t> smem_configured{0};  // one per instantiation
+    auto kernel = decode_partition_kernel<T, D, GT>;
+    if (ensure_smem(kernel, C::kSmemBytes, smem_configured) != PA_OK) return PA_ERR_CUDA;
+    const long long grid = static_cast<long long>(p.num_seqs) * p.head_tiles * p.max_parts;
+    if (grid <= 0 || grid > 0x7fffffffLL) return PA_ERR_UNSUPPORTED;
+    kernel<<<static_cast<unsigned>(grid), C::kThreads, C::kSmemBytes, stream>>>(p);
+    if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
+    if (p.max_parts > 1) {
+        decode_reduce_kernel<T, D><<<p.num_seqs * p.num_q_heads, 128, 0, stream>>>(p);
+        if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
+    }
+    return PA_OK;
+}
+
+template <typename T, int D>
+inline pa_status launch_decode_dim(const DecodeParams& p, int gt, cudaStream_t stream) {
+    switch (gt) {
+        case 1: return launch_decode_tile<T, D, 1>(p, stream);
+        case 2: return launch_decode_tile<T, D, 2>(p, stream);
+        case 4: return launch_decode_tile<T, D, 4>(p, stream);
+        case 8: return launch_decode_tile<T, D, 8>(p, stream);
+    }
+    return PA_ERR_UNSUPPORTED;
+}
+
+template <typename T>
+inline pa_status launch_decode_typed(const DecodeParams& p, int head_dim, int gt,
+                                     cudaStream_t stream) {
+    switch (head_dim) {
+        case 64: return launch_decode_dim<T, 64>(p, gt, stream);
+        case 128: return launch_decode_dim<T, 128>(p, gt, stream);
+    }
+    return PA_ERR_UNSUPPORTED;
+}
+
+// One per element type, each in its own translation unit.
+pa_status launch_decode_f32(const DecodeParams& p, int head_dim, int gt, cudaStream_t stream);
+pa_status launch_decode_f16(const DecodeParams& p, int head_dim, int gt, cudaStream_t stream);
+pa_status launch_decode_bf16(const DecodeParams& p, int head_dim, int gt, cudaStream_t stream);
+
+}  // namespace pa

@@ -1,0 +1,83 @@
+// kv_write.cu -- slot-mapped write of each new token's K/V rows into the pool.
+//
+// The new token's K/V is the only K/V a decode step computes; it is written
+// into the slot of the sequence's current block (kwkr.cn "vLLM PagedAttention
+// 技术深度解析" §1.2.2 allocation flow; wmrh.cn "paged attention", KV-cache
+// part).  Pure data movement: one CTA per token, 16-byte vector copies of the
+// token's rows for every kv head.
+#include "pa_device.cuh"
+#include "pa_host.h"
+
+namespace pa {
+namespace {
+
+struct KvWriteParams {
+    const uint4* k_new;
+    const uint4* v_new;
+    uint4* k_cache;
+    uint4* v_cache;
+    const int64_t* slot_mapping;
+    uint32_t* d_err;
+    int num_kv_heads;
+    int row_vecs;  // 16-byte vectors per (token, head) row
+    int block_size;
+    int num_blocks;
+};
+
+__global__ void __launch_bounds__(256) kv_write_kernel(const KvWriteParams p) {
+    const int t = blockIdx.x;
+    const int64_t slot = p.slot_mapping[t];
+    if (slot < 0) return;  // padding token
+    if (slot >= static_cast<int64_t>(p.num_blocks) * p.block_size) {
+        if (threadIdx.x == 0) report(p.d_err, PA_DERR_SLOT_OOB);
+        return;
+    }
+    const int64_t blk = slot / p.block_size;
+    const int64_t off = slot - blk * p.block_size;
+    const int per_tensor = p.num_kv_heads * p.row_vecs;
+    for (int i = threadIdx.x; i < 2 * per_tensor; i += blockDim.x) {
+        const bool is_v = i >= per_tensor;
+        const int c = is_v ? i - per_tensor : i;
+        const int h = c / p.row_vecs;
+        const int w = c - h * p.row_vecs;
+        const size_t src = (static_cast<size_t>(t) * p.num_kv_heads + h) * p.row_vecs + w;
+        const size_t dst =
+            ((static_cast<size_t>(blk) * p.num_kv_heads + h) * p.block_size + off) * p.row_vecs + w;
+        if (is_v)
+            p.v_cache[dst] = __ldg(p.v_new + src);
+        else
+            p.k_cache[dst] = __ldg(p.k_new + src);
+    }
+}
+
+}  // namespace
+}  // namespace pa
+
+extern "C" pa_status pa_kv_write(const void* k_new, const void* v_new, void* k_cache,
+                                 void* v_cache, const int64_t* slot_mapping, int num_tokens,
+                                 int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                                 pa_dtype dtype, uint32_t* d_err, pa_stream_t stream) {
+    using namespace pa;
+    if (!valid_dtype(dtype)) return PA_ERR_INVALID_ARG;
+    if (num_tokens < 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 || num_blocks <= 0)
+        return PA_ERR_INVALID_ARG;
+    const int row_bytes = head_dim * elem_bytes(dtype);
+    if (row_bytes % 16 != 0) return PA_ERR_UNSUPPORTED;
+    if (num_tokens == 0) return PA_OK;
+    if (!k_new || !v_new || !k_cache || !v_cache || !slot_mapping) return PA_ERR_INVALID_ARG;
+    if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) || !aligned16(v_cache))
+        return PA_ERR_INVALID_ARG;
+    KvWriteParams p;
+    p.k_new = static_cast<const uint4*>(k_new);
+    p.v_new = static_cast<const uint4*>(v_new);
+    p.k_cache = static_cast<uint4*>(k_cache);
+    p.v_cache = static_cast<uint4*>(v_cache);
+    p.slot_mapping = slot_mapping;
+    p.d_err = d_err;
+    p.num_kv_heads = num_kv_heads;
+    p.row_vecs = row_bytes / 16;
+    p.block_size = block_size;
+    p.num_blocks = num_blocks;
+    kv_write_kernel<<<num_tokens, 256, 0, as_cuda(stream)>>>(p);
+    return launch_status();
+}

@@ -1,0 +1,188 @@
+"""GPU parity: libpa (through the C ABI) against the fp64 oracle on the same bytes.
+
+kv_write and copy_blocks must match bit for bit over the whole pool (untouched
+blocks and poison included); decode must be within the tolerances of
+tests/gpu_util.TOL.  Every named workload runs at full size; the long-context
+ones are checked on sampled (sequence, head) outputs, which the oracle
+computes one at a time.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_cache_314_gb300 as pa
+from paged_kv_cache_314_gb300 import _build
+from paged_kv_cache_314_gb300 import workloads as wl
+
+from gpu_util import (assert_close, gpu_step, oracle_step, out_f64, to_numpy, upload)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    _build.build()
+    pa.load()
+
+
+def _check_step(w, partition_tokens=None, pools=True):
+    d = upload(w)
+    out = gpu_step(w, d, partition_tokens=partition_tokens)
+    kc, vc, ref, err = oracle_step(w)
+    assert int(d["d_err"].item()) == err, (int(d["d_err"].item()), err)
+    if pools:
+        assert np.array_equal(to_numpy(d["k_cache"], w.dtype), kc), "k_cache differs from oracle"
+        assert np.array_equal(to_numpy(d["v_cache"], w.dtype), vc), "v_cache differs from oracle"
+    return assert_close(out_f64(out), ref, w.dtype, w.name), out, d
+
+
+# ---------------------------------------------------------------------------
+# small cases spanning several stages, partitions and ragged tails
+# ---------------------------------------------------------------------------
+
+SMALL = [
+    # dtype, Hq, Hkv, d, B, ctx
+    ("f32", 4, 4, 64, 16, [1, 17, 33, 50]),
+    ("f32", 2, 2, 128, 16, [1, 15, 16, 17, 31, 300]),
+    ("f16", 4, 4, 128, 16, [1, 15, 16, 17, 255, 256, 257, 700]),
+    ("f16", 3, 3, 64, 32, [5, 31, 32, 33, 64, 65, 511, 512, 513]),
+    ("bf16", 8, 8, 128, 128, [1, 127, 128, 129, 1000, 1111]),
+    ("bf16", 8, 2, 128, 16, [1, 16, 17, 300, 515]),   # GQA, 4 q heads per kv head
+    ("bf16", 16, 2, 128, 16, [3, 100, 257, 600]),     # GQA, 8 q heads per kv head
+    ("f16", 6, 1, 64, 64, [1, 63, 64, 65, 400]),      # 6 q heads per kv head -> tiles of 2
+    ("bf16", 4, 4, 64, 256, [1, 255, 256, 257, 900]),
+]
+
+
+@pytest.mark.parametrize("case", range(len(SMALL)))
+@pytest.mark.parametrize("partition", [0, "block", "whole"])
+def test_small_parity(case, partition):
+    dtype, Hq, Hkv, d, B, ctx = SMALL[case]
+    w = wl.custom(f"small{case}", ctx, dtype=dtype, num_q_heads=Hq, num_kv_heads=Hkv,
+                  head_dim=d, block_size=B, seed=100 + case, pool_factor=1.3)
+    P = {0: 0, "block": B, "whole": w.max_blocks_per_seq * B}[partition]
+    _check_step(w, partition_tokens=P)
+
+
+def test_tiny_workload():
+    _check_step(wl.tiny())
+
+
+# ---------------------------------------------------------------------------
+# named workloads at full size
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("name", ["llama7b", "llama13b", "gqa_share", "gqa_share_p1016"])
+def test_named_full_size(name):
+    w = wl.by_name(name)
+    stats, _, _ = _check_step(w)
+    print(name, stats)
+
+
+@pytest.mark.parametrize("name", ["long_b16", "long_b128"])
+def test_long_context_sampled(name):
+    w = wl.by_name(name)
+    d = upload(w)
+    out = out_f64(gpu_step(w, d))
+    assert int(d["d_err"].item()) == 0
+    kc = to_numpy(d["k_cache"], w.dtype)
+    vc = to_numpy(d["v_cache"], w.dtype)
+    # the write of each new token, checked where it landed
+    for t in range(w.num_tokens):
+        slot = int(w.slot_mapping[t])
+        b, o = divmod(slot, w.block_size)
+        assert np.array_equal(kc[b, :, o], w.k_new[t]) and np.array_equal(vc[b, :, o], w.v_new[t])
+    rng = np.random.default_rng(5)
+    picks = [(s, int(rng.integers(w.num_q_heads))) for s in range(w.num_seqs)]
+    picks += [(int(np.argmax(w.context_lens)), 0), (int(np.argmin(w.context_lens)), w.num_q_heads - 1)]
+    ref = np.stack([oracle.decode_head(w.q, kc, vc, w.block_tables, w.context_lens, s, h,
+                                       scale=w.scale, dtype=w.dtype)[0] for s, h in picks])
+    got = np.stack([out[s, h] for s, h in picks])
+    assert np.isfinite(out).all()
+    assert_close(got, ref, w.dtype, name)
+
+
+# ---------------------------------------------------------------------------
+# metamorphic: placement, determinism, partition size
+# ---------------------------------------------------------------------------
+
+def test_physical_permutation_is_bit_identical():
+    w = wl.custom("perm", [3, 40, 333, 1000, 2048], dtype="bf16", num_q_heads=8, num_kv_heads=8,
+                  head_dim=128, block_size=16, seed=21)
+    base = gpu_step(w, upload(w))
+    again = gpu_step(w, upload(w))
+    assert torch.equal(base, again), "two identical runs differ"
+    rng = np.random.default_rng(22)
+    for _ in range(3):
+        wp = wl.permute_physical(w, rng)
+        assert torch.equal(gpu_step(wp, upload(wp)), base)
+
+
+def test_partition_sizes_agree():
+    w = wl.custom("parts", [1, 16, 100, 511, 512, 513, 1500, 4000], dtype="f16", num_q_heads=4,
+                  num_kv_heads=4, head_dim=128, block_size=16, seed=23)
+    _, _, ref, _ = oracle_step(w)
+    for P in (16, 32, 256, 512, w.max_blocks_per_seq * 16):
+        out = gpu_step(w, upload(w), partition_tokens=P)
+        assert_close(out_f64(out), ref, "f16", f"P={P}")
+
+
+# ---------------------------------------------------------------------------
+# bounds checks and errors
+# ---------------------------------------------------------------------------
+
+def test_bad_lengths_and_block_ids_are_flagged_and_skipped():
+    w = wl.custom("bad", [20, 40, 60, 5, 0], dtype="f32", num_q_heads=2, num_kv_heads=2,
+                  head_dim=64, block_size=16, seed=24, max_blocks_per_seq=4)
+    w.context_lens[0] = -3                   # negative length
+    w.context_lens[3] = 4 * 16 + 1           # longer than the table allows
+    w.block_tables[2, 1] = w.num_blocks + 5  # block id outside the pool
+    w.block_tables[1, 0] = -7
+    d = upload(w)
+    out = gpu_step(w, d)
+    _, _, ref, err = oracle_step(w)
+    assert err == oracle.ERR_CTX_OOB | oracle.ERR_BLOCK_OOB
+    assert int(d["d_err"].item()) == err
+    assert_close(out_f64(out), ref, "f32", "bad")
+    assert (out[0] == 0).all() and (out[3] == 0).all() and (out[4] == 0).all()
+
+
+def test_slot_and_copy_bounds():
+    w = wl.custom("slots", [10, 20], dtype="f16", num_q_heads=2, num_kv_heads=2, head_dim=64,
+                  block_size=16, seed=25)
+    w.slot_mapping[0] = w.num_blocks * 16  # outside the pool
+    w.slot_mapping[1] = -1                 # padding
+    w.block_mapping = np.array([[0, w.num_blocks], [1, 2]], np.int32)
+    _check_step(w)
+
+
+def test_copy_blocks_check_flags_conflicts():
+    for mapping, want in (([[1, 2], [3, 4]], 0), ([[1, 2], [3, 2]], pa.DERR_MAPPING_CONFLICT),
+                          ([[1, 2], [2, 4]], pa.DERR_MAPPING_CONFLICT)):
+        m = torch.tensor(mapping, dtype=torch.int32, device="cuda")
+        e = torch.zeros(1, dtype=torch.int32, device="cuda")
+        pa.copy_blocks_check(m, e)
+        torch.cuda.synchronize()
+        assert int(e.item()) == want
+
+
+def test_host_checked_errors():
+    w = wl.custom("err", [300], dtype="f16", num_q_heads=2, num_kv_heads=2, head_dim=128,
+                  block_size=16, seed=26)
+    d = upload(w)
+    out = torch.empty_like(d["q"])
+    need = pa.decode_workspace_size(1, 2, 128, w.max_blocks_per_seq, 16, 16)
+    assert need > 0
+    small = torch.empty(need - 256, dtype=torch.uint8, device="cuda")
+    with pytest.raises(pa.PaError) as e:
+        pa.decode(out, d["q"], d["k_cache"], d["v_cache"], d["block_tables"], d["context_lens"],
+                  w.scale, partition_tokens=16, workspace=small)
+    assert e.value.status == 3
+    with pytest.raises(pa.PaError) as e:  # partition not a multiple of the block size
+        pa.decode(out, d["q"], d["k_cache"], d["v_cache"], d["block_tables"], d["context_lens"],
+                  w.scale, partition_tokens=24)
+    assert e.value.status == 1
