@@ -109,6 +109,12 @@ def oracle_step(w, do_copy=True, parallel=True):
     return kc, vc, out, err | e
 
 
+def same_bits(a: np.ndarray, b: np.ndarray) -> bool:
+    """Bitwise equality (NaN poison compares equal to itself)."""
+    return a.shape == b.shape and np.array_equal(np.ascontiguousarray(a).view(np.uint8),
+                                                 np.ascontiguousarray(b).view(np.uint8))
+
+
 def assert_close(got: np.ndarray, ref: np.ndarray, dtype: str, what: str = "") -> Dict[str, float]:
     atol, rtol = TOL[dtype]
     assert got.shape == ref.shape

@@ -17,7 +17,7 @@ import paged_kv_cache_314_gb300 as pa
 from paged_kv_cache_314_gb300 import _build
 from paged_kv_cache_314_gb300 import workloads as wl
 
-from gpu_util import (assert_close, gpu_step, oracle_step, out_f64, to_numpy, upload)
+from gpu_util import (assert_close, gpu_step, oracle_step, out_f64, same_bits, to_numpy, upload)
 
 pytestmark = pytest.mark.gpu
 
@@ -35,8 +35,8 @@ def _check_step(w, partition_tokens=None, pools=True):
     kc, vc, ref, err = oracle_step(w)
     assert int(d["d_err"].item()) == err, (int(d["d_err"].item()), err)
     if pools:
-        assert np.array_equal(to_numpy(d["k_cache"], w.dtype), kc), "k_cache differs from oracle"
-        assert np.array_equal(to_numpy(d["v_cache"], w.dtype), vc), "v_cache differs from oracle"
+        assert same_bits(to_numpy(d["k_cache"], w.dtype), kc), "k_cache differs from oracle"
+        assert same_bits(to_numpy(d["v_cache"], w.dtype), vc), "v_cache differs from oracle"
     return assert_close(out_f64(out), ref, w.dtype, w.name), out, d
 
 
@@ -95,7 +95,7 @@ def test_long_context_sampled(name):
     for t in range(w.num_tokens):
         slot = int(w.slot_mapping[t])
         b, o = divmod(slot, w.block_size)
-        assert np.array_equal(kc[b, :, o], w.k_new[t]) and np.array_equal(vc[b, :, o], w.v_new[t])
+        assert same_bits(kc[b, :, o], w.k_new[t]) and same_bits(vc[b, :, o], w.v_new[t])
     rng = np.random.default_rng(5)
     picks = [(s, int(rng.integers(w.num_q_heads))) for s in range(w.num_seqs)]
     picks += [(int(np.argmax(w.context_lens)), 0), (int(np.argmin(w.context_lens)), w.num_q_heads - 1)]
