@@ -97,60 +97,82 @@ def _ncu_traffic(config: str):
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+    """SM clock and clock-event (throttle) reasons sampled every ~0.5 ms during
+    the timed region through NVML (read-only queries, via ctypes)."""
 
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    # NVML clock-event reason bits
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
 
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
-        self.proc = None
+        self.samples = []
+        self.max_mhz = None
+        self.error = None
+        self._stop = False
+        self._thread = None
+        self._nvml = None
+        try:
+            import ctypes
+            nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if nv.nvmlInit_v2() != 0:
+                raise RuntimeError("nvmlInit failed")
+            h = ctypes.c_void_p()
+            bus = None
+            try:
+                import torch
+                props = torch.cuda.get_device_properties(gpu_index)
+                bus = "%08x:%02x:%02x.0" % (props.pci_domain_id, props.pci_bus_id,
+                                            props.pci_device_id)
+            except Exception:
+                bus = None
+            if bus is None or nv.nvmlDeviceGetHandleByPciBusId_v2(bus.encode(), ctypes.byref(h)) != 0:
+                if nv.nvmlDeviceGetHandleByIndex_v2(gpu_index, ctypes.byref(h)) != 0:
+                    raise RuntimeError("no NVML handle")
+            mx = ctypes.c_uint()
+            if nv.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0:
+                self.max_mhz = float(mx.value)
+            self._nvml, self._h = nv, h
+        except Exception as e:  # no NVML: report that instead of clocks
+            self.error = str(e)
+
+    def _run(self):
+        import ctypes
+        clk = ctypes.c_uint()
+        rsn = ctypes.c_ulonglong()
+        while not self._stop:
+            if self._nvml.nvmlDeviceGetClockInfo(self._h, 1, ctypes.byref(clk)) == 0:
+                r = 0
+                if self._nvml.nvmlDeviceGetCurrentClocksEventReasons(self._h, ctypes.byref(rsn)) == 0:
+                    r = rsn.value
+                self.samples.append((float(clk.value), int(r)))
+            time.sleep(0.0005)
 
     def __enter__(self):
-        try:
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
-                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-        except Exception:
-            self.proc = None
-        time.sleep(0.3)
+        import threading
+        if self._nvml is not None:
+            self._thread = threading.Thread(target=self._run, daemon=True)
+            self._thread.start()
         return self
 
     def __exit__(self, *exc):
-        self.lines = []
-        if self.proc is not None:
-            time.sleep(0.15)
-            self.proc.terminate()
-            try:
-                out, _ = self.proc.communicate(timeout=5)
-            except Exception:
-                self.proc.kill()
-                out = ""
-            self.lines = [l for l in out.splitlines() if l.strip()]
+        self._stop = True
+        if self._thread is not None:
+            self._thread.join(timeout=5)
         return False
 
     def summary(self):
-        if not getattr(self, "lines", None):
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
-        sm, smax, reasons = [], [], set()
-        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
-        for l in self.lines:
-            f = [x.strip() for x in l.split(",")]
-            if len(f) < 9:
-                continue
-            try:
-                sm.append(float(f[1]))
-                smax.append(float(f[2]))
-            except ValueError:
-                continue
-            for n, v in zip(names, f[5:9]):
-                if v.lower() == "active":
-                    reasons.add(n)
-        return {"sm_mhz": float(np.median(sm)) if sm else None,
-                "sm_max_mhz": max(smax) if smax else None,
-                "reasons": sorted(reasons), "samples": len(sm)}
+        if self._nvml is None or not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz,
+                    "reasons": [f"no samples: {self.error or 'timed region too short'}"]}
+        reasons = set()
+        for _, r in self.samples:
+            for bit, name in self.REASONS.items():
+                if r & bit:
+                    reasons.add(name)
+        return {"sm_mhz": float(np.median([c for c, _ in self.samples])),
+                "sm_max_mhz": self.max_mhz, "reasons": sorted(reasons),
+                "samples": len(self.samples), "source": "NVML, every ~0.5 ms in the timed region"}
 
 
 # ---------------------------------------------------------------------------
@@ -164,9 +186,10 @@ def _to_torch(a, dtype):
     return torch.from_numpy(np.ascontiguousarray(a))
 
 
-def _cpu_baseline(w, budget_s=20.0):
-    """The oracle, as it stands, on this workload's decode (whole sequences,
-    in order, until the budget is spent) on all host cores."""
+def _cpu_baseline(w, cpu_seconds=16.0, max_wall_s=20.0):
+    """The oracle, as it stands, on this workload's decode on all host cores:
+    whole sequences in order, passes over the batch repeated until about
+    cpu_seconds of CPU work (threads x wall time) are done."""
     import concurrent.futures as cf
     import oracle
     threads = os.cpu_count() or 1
@@ -174,8 +197,12 @@ def _cpu_baseline(w, budget_s=20.0):
     done_bytes, n_seqs, t0 = 0, 0, time.perf_counter()
     per_tok = 2 * w.num_kv_heads * w.head_dim * w.elem_bytes
     with cf.ThreadPoolExecutor(threads) as ex:
-        while n_seqs < w.num_seqs and time.perf_counter() - t0 < budget_s:
-            seqs = list(range(n_seqs, min(w.num_seqs, n_seqs + threads)))
+        while True:
+            el = time.perf_counter() - t0
+            if n_seqs > 0 and (el * threads >= cpu_seconds or el >= max_wall_s):
+                break
+            first = n_seqs % w.num_seqs
+            seqs = list(range(first, min(w.num_seqs, first + threads)))
 
             def one(s):
                 o, _ = oracle.decode(np.ascontiguousarray(w.q[s:s + 1]), kc, vc,
@@ -189,9 +216,9 @@ def _cpu_baseline(w, budget_s=20.0):
             n_seqs += len(seqs)
     dt = time.perf_counter() - t0
     return {"value": done_bytes / dt / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
-            "sample": f"decode of the first {n_seqs} of {w.num_seqs} sequences of the same "
-                      f"workload ({done_bytes / 1e6:.0f} MB of K/V), fp64 C oracle, one "
-                      f"sequence per host thread, {dt:.1f} s"}
+            "sample": f"decode of {n_seqs} sequences ({n_seqs / w.num_seqs:.2f} passes over the "
+                      f"{w.num_seqs}-sequence batch of the same workload, {done_bytes / 1e6:.0f} MB"
+                      f" of K/V), fp64 C oracle, one sequence per host thread, {dt:.1f} s wall"}
 
 
 def run_gpu(args):
