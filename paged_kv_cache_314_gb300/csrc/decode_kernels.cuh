@@ -20,11 +20,18 @@
 //    (cp.async.bulk, TMA engine) of the 16-token K and V sub-blocks into a
 //    ring of kStages shared-memory stages guarded by mbarriers.  The copies
 //    carry an L2 evict-first hint: each K/V byte is read once per step.
-//  * Warps 0-3 consume: each lane owns one 16-byte column slice of a token row
-//    (kLpt lanes per row), so a warp reads kTpp whole rows per 128-bit shared
-//    load without bank conflicts; dot products finish with xor shuffles; the
-//    softmax is online (running max m, running sum l, fp32) in the log2
-//    domain (q is pre-scaled by scale*log2(e)), updated once per stage.
+//  * Warps 0-3 consume, each one whole stage at a time (stage c belongs to
+//    warp c mod 4, so warps never wait on one another inside the loop).  A
+//    lane owns one 16-byte column slice of a token row (kLpt lanes per row),
+//    so one 128-bit shared load per lane reads kTpp whole rows without bank
+//    conflicts.  The per-lane partial dot products of a stage are finished by
+//    a reduce-scatter butterfly (each level halves the values a lane keeps),
+//    which leaves every lane with whole logits of its own tokens: one exp2 per
+//    lane per stage.  The probabilities go through shared memory to the lanes
+//    that multiply them into the V rows.  The softmax is online (running max
+//    m, running sum l, fp32) in the log2 domain (q is pre-scaled by
+//    scale*log2(e)); its max is updated once per stage.
+//  * Stages whose tokens are all valid take a path without any masking.
 //  * Tokens past context_len and tokens of blocks whose id fails the bounds
 //    check are masked by select, never by arithmetic, so poison in unused
 //    slots (NaN) cannot leak into the result.
@@ -62,28 +69,63 @@ struct DecodeParams {
     float qk_scale_log2;  // scale * log2(e)
 };
 
+constexpr int align16(int x) { return (x + 15) / 16 * 16; }
+
 template <typename T, int D, int GT>
 struct DecodeTile {
     static constexpr int kElem = sizeof(T);
     static constexpr int kVec = 16 / kElem;           // elements per 16-byte access
-    static constexpr int kLpt = D / kVec;             // lanes per token row
+    static constexpr int kLpt = D / kVec;             // lanes per token row: 8, 16 or 32
     static constexpr int kTpp = 32 / kLpt;            // token rows per warp pass
     static constexpr int kRowBytes = D * kElem;
     static constexpr int kConsumerWarps = 4;
     static constexpr int kThreads = 32 * (kConsumerWarps + 1);
-    static constexpr int kTps = 8192 / kRowBytes;     // tokens per stage (8 KB of K + 8 KB of V)
-    static constexpr int kPasses = kTps / (kConsumerWarps * kTpp);
-    static constexpr int kStages = 4;
+    // tokens per stage: 4 KB of K (and 4 KB of V), at least 16 tokens
+    static constexpr int kTps = (4096 / kRowBytes) > 16 ? (4096 / kRowBytes) : 16;
+    static constexpr int kPasses = kTps / kTpp;       // warp passes over one stage
+    static constexpr int kVals = kPasses >= kLpt ? kPasses / kLpt : 1;  // logits per lane
+    static constexpr int kDup = kPasses >= kLpt ? 1 : kLpt / kPasses;   // lanes per logit
     static constexpr int kSubs = kTps / 16;           // 16-token bulk copies per tensor per stage
     static constexpr int kStageBytes = 2 * kTps * kRowBytes;
+    static constexpr int kStages = (65536 / kStageBytes) / kConsumerWarps * kConsumerWarps;
     static constexpr int kRingBytes = kStages * kStageBytes;
+    static constexpr int kPOffset = kRingBytes;       // [W][GT][kTpp][kPasses] probabilities
+    static constexpr int kMergeOffset = kPOffset + kConsumerWarps * GT * kTps * 4;
     static constexpr int kMergeFloats = kConsumerWarps * GT * (D + 2);
-    static constexpr int kBarOffset = kRingBytes + ((kMergeFloats * 4 + 15) / 16) * 16;
+    static constexpr int kBarOffset = align16(kMergeOffset + kMergeFloats * 4);
     // full[kStages], empty[kStages], mask[kStages], abort flag
     static constexpr int kSmemBytes = kBarOffset + 3 * kStages * 8 + 16;
-    static_assert(kLpt >= 1 && kLpt <= 32 && 32 % kLpt == 0, "row must split over lanes");
+    static constexpr uint64_t kFullMask = kTps >= 64 ? ~0ull : ((1ull << kTps) - 1ull);
+    static_assert(kLpt >= 8 && kLpt <= 32 && 32 % kLpt == 0, "row must split over lanes");
     static_assert(kTps % 16 == 0 && kTps <= 64, "stage holds whole 16-token sub-blocks");
-    static_assert(kPasses >= 1 && kPasses * kConsumerWarps * kTpp == kTps, "passes tile the stage");
+    static_assert(kPasses % 4 == 0 && kPasses * kTpp == kTps, "passes tile the stage");
+    static_assert(kStages >= kConsumerWarps, "every consumer warp owns a stage");
+};
+
+// Reduce-scatter over the N values of each lane across the lanes xor-linked
+// by OFF, OFF/2, ..., 1: at each level a lane keeps one half of its values
+// (the upper half when its OFF bit is set) and adds its partner's matching
+// half.  Afterwards lane bits pick the value index: with N >= 2*OFF a lane
+// holds N/(2*OFF) whole sums, else one sum shared by 2*OFF/N lanes.
+template <int N, int OFF>
+struct ReduceScatter {
+    __device__ __forceinline__ static void run(float* x, int lane) {
+        if constexpr (OFF > 0) {
+            if constexpr (N > 1) {
+                const bool up = (lane & OFF) != 0;
+#pragma unroll
+                for (int i = 0; i < N / 2; ++i) {
+                    const float keep = up ? x[i + N / 2] : x[i];
+                    const float send = up ? x[i] : x[i + N / 2];
+                    x[i] = keep + __shfl_xor_sync(0xffffffffu, send, OFF);
+                }
+                ReduceScatter<N / 2, OFF / 2>::run(x, lane);
+            } else {
+                x[0] += __shfl_xor_sync(0xffffffffu, x[0], OFF);
+                ReduceScatter<1, OFF / 2>::run(x, lane);
+            }
+        }
+    }
 };
 
 template <typename T, int D, int GT>
@@ -178,11 +220,101 @@ __device__ __forceinline__ void decode_produce(const DecodeParams& p, unsigned c
     }
 }
 
+// One stage (kTps tokens) of one consumer warp.  kFull: every token valid.
+template <typename T, int D, int GT, bool kFull>
+__device__ __forceinline__ void decode_stage(const unsigned char* sK, const unsigned char* sV,
+                                             uint64_t mask, const float (&qf)[GT][16 / sizeof(T)],
+                                             float (&m)[GT], float (&l)[GT],
+                                             float (&o)[GT][16 / sizeof(T)], float* pw, int grp,
+                                             int lig) {
+    using C = DecodeTile<T, D, GT>;
+    constexpr int kVec = C::kVec, kLpt = C::kLpt, kTpp = C::kTpp, kPasses = C::kPasses;
+    float x[GT][kPasses];
+#pragma unroll
+    for (int ps = 0; ps < kPasses; ++ps) {
+        const uint4 raw =
+            *reinterpret_cast<const uint4*>(sK + (ps * kTpp + grp) * C::kRowBytes + lig * 16);
+        float kf[kVec];
+        Elem<T>::unpack(raw, kf);
+#pragma unroll
+        for (int j = 0; j < GT; ++j) {
+            float acc = 0.f;
+#pragma unroll
+            for (int v = 0; v < kVec; ++v) acc = fmaf(qf[j][v], kf[v], acc);
+            x[j][ps] = acc;
+        }
+    }
+#pragma unroll
+    for (int j = 0; j < GT; ++j) ReduceScatter<kPasses, kLpt / 2>::run(x[j], lig);
+
+#pragma unroll
+    for (int j = 0; j < GT; ++j) {
+        float xv[C::kVals];
+        float mx = -INFINITY;
+#pragma unroll
+        for (int i = 0; i < C::kVals; ++i) {
+            const int ps = kPasses >= kLpt ? lig * C::kVals + i : lig / C::kDup;
+            const int ti = ps * kTpp + grp;
+            xv[i] = (kFull || ((mask >> ti) & 1ull)) ? x[j][i] : -INFINITY;
+            mx = fmaxf(mx, xv[i]);
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+        const float m_new = fmaxf(m[j], mx);
+        float pv[C::kVals];
+        if (kFull || m_new != -INFINITY) {
+            const float alpha = fast_exp2(m[j] - m_new);  // 0 while m was -inf
+            m[j] = m_new;
+            l[j] *= alpha;
+#pragma unroll
+            for (int v = 0; v < kVec; ++v) o[j][v] *= alpha;
+#pragma unroll
+            for (int i = 0; i < C::kVals; ++i) {
+                pv[i] = fast_exp2(xv[i] - m_new);  // masked tokens: 2^-inf = 0
+                l[j] += pv[i];
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < C::kVals; ++i) pv[i] = 0.f;
+        }
+#pragma unroll
+        for (int i = 0; i < C::kVals; ++i) {
+            const int ps = kPasses >= kLpt ? lig * C::kVals + i : lig / C::kDup;
+            pw[(j * kTpp + grp) * kPasses + ps] = pv[i];
+        }
+    }
+    __syncwarp();
+    float pp[GT][kPasses];
+#pragma unroll
+    for (int j = 0; j < GT; ++j)
+#pragma unroll
+        for (int q4 = 0; q4 < kPasses / 4; ++q4) {
+            const float4 t = *reinterpret_cast<const float4*>(pw + (j * kTpp + grp) * kPasses + 4 * q4);
+            pp[j][4 * q4] = t.x;
+            pp[j][4 * q4 + 1] = t.y;
+            pp[j][4 * q4 + 2] = t.z;
+            pp[j][4 * q4 + 3] = t.w;
+        }
+#pragma unroll
+    for (int ps = 0; ps < kPasses; ++ps) {
+        const int ti = ps * kTpp + grp;
+        if (!kFull && !((mask >> ti) & 1ull)) continue;  // masked rows may hold anything
+        const uint4 raw = *reinterpret_cast<const uint4*>(sV + ti * C::kRowBytes + lig * 16);
+        float vf[kVec];
+        Elem<T>::unpack(raw, vf);
+#pragma unroll
+        for (int j = 0; j < GT; ++j)
+#pragma unroll
+            for (int v = 0; v < kVec; ++v) o[j][v] = fmaf(pp[j][ps], vf[v], o[j][v]);
+    }
+    __syncwarp();  // pw is rewritten by this warp's next stage
+}
+
 template <typename T, int D, int GT>
 __device__ __forceinline__ void decode_consume(const DecodeParams& p, unsigned char* smem, int s,
                                                int hq0, int part, int nparts, int nstages) {
     using C = DecodeTile<T, D, GT>;
-    constexpr int kVec = C::kVec, kLpt = C::kLpt, kTpp = C::kTpp, W = C::kConsumerWarps;
+    constexpr int kVec = C::kVec, kLpt = C::kLpt, W = C::kConsumerWarps;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int grp = lane / kLpt;  // which row of a pass this lane reads
     const int lig = lane % kLpt;  // which 16-byte slice of the row
@@ -191,6 +323,7 @@ __device__ __forceinline__ void decode_consume(const DecodeParams& p, unsigned c
     volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 3 * C::kStages);
     const uint32_t full0 = smem_addr(bars);
     const uint32_t empty0 = smem_addr(bars + C::kStages);
+    float* pw = reinterpret_cast<float*>(smem + C::kPOffset) + warp * GT * C::kTps;
 
     float qf[GT][kVec];
 #pragma unroll
@@ -212,7 +345,7 @@ __device__ __forceinline__ void decode_consume(const DecodeParams& p, unsigned c
         for (int v = 0; v < kVec; ++v) o[j][v] = 0.f;
     }
 
-    for (int c = 0; c < nstages; ++c) {
+    for (int c = warp; c < nstages; c += W) {
         const int st = c % C::kStages;
         const uint32_t round = static_cast<uint32_t>(c / C::kStages);
         if (!mbar_wait(full0 + 8 * st, round & 1)) {
@@ -223,77 +356,28 @@ __device__ __forceinline__ void decode_consume(const DecodeParams& p, unsigned c
         const uint64_t mask = masks[st];
         const unsigned char* sK = smem + st * C::kStageBytes;
         const unsigned char* sV = sK + C::kTps * C::kRowBytes;
-        float x[C::kPasses][GT];
-        bool valid[C::kPasses];
-#pragma unroll
-        for (int ps = 0; ps < C::kPasses; ++ps) {
-            const int ti = (ps * W + warp) * kTpp + grp;
-            valid[ps] = (mask >> ti) & 1ull;
-            const uint4 raw = *reinterpret_cast<const uint4*>(sK + ti * C::kRowBytes + lig * 16);
-            float kf[kVec];
-            Elem<T>::unpack(raw, kf);
-#pragma unroll
-            for (int j = 0; j < GT; ++j) {
-                float acc = 0.f;
-#pragma unroll
-                for (int v = 0; v < kVec; ++v) acc = fmaf(qf[j][v], kf[v], acc);
-                x[ps][j] = acc;
-            }
-        }
-#pragma unroll
-        for (int ps = 0; ps < C::kPasses; ++ps)
-#pragma unroll
-            for (int j = 0; j < GT; ++j)
-#pragma unroll
-                for (int off = kLpt / 2; off > 0; off >>= 1)
-                    x[ps][j] += __shfl_xor_sync(0xffffffffu, x[ps][j], off);
-#pragma unroll
-        for (int j = 0; j < GT; ++j) {
-            float mx = -INFINITY;
-#pragma unroll
-            for (int ps = 0; ps < C::kPasses; ++ps) mx = fmaxf(mx, valid[ps] ? x[ps][j] : -INFINITY);
-#pragma unroll
-            for (int off = kLpt; off < 32; off <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-            const float m_new = fmaxf(m[j], mx);
-            const float alpha = (m_new == -INFINITY) ? 1.f : exp2f(m[j] - m_new);
-            m[j] = m_new;
-            l[j] *= alpha;
-#pragma unroll
-            for (int v = 0; v < kVec; ++v) o[j][v] *= alpha;
-        }
-#pragma unroll
-        for (int ps = 0; ps < C::kPasses; ++ps) {
-            const int ti = (ps * W + warp) * kTpp + grp;
-            const uint4 raw = *reinterpret_cast<const uint4*>(sV + ti * C::kRowBytes + lig * 16);
-            float vf[kVec];
-            Elem<T>::unpack(raw, vf);
-#pragma unroll
-            for (int v = 0; v < kVec; ++v) vf[v] = valid[ps] ? vf[v] : 0.f;
-#pragma unroll
-            for (int j = 0; j < GT; ++j) {
-                const float pw = valid[ps] ? exp2f(x[ps][j] - m[j]) : 0.f;
-                l[j] += pw;
-#pragma unroll
-                for (int v = 0; v < kVec; ++v) o[j][v] = fmaf(pw, vf[v], o[j][v]);
-            }
-        }
-        __syncwarp();
+        if (mask == C::kFullMask)
+            decode_stage<T, D, GT, true>(sK, sV, mask, qf, m, l, o, pw, grp, lig);
+        else
+            decode_stage<T, D, GT, false>(sK, sV, mask, qf, m, l, o, pw, grp, lig);
         if (lane == 0) mbar_arrive(empty0 + 8 * st);
     }
 
-    // Rows of one pass were split over kTpp lane groups that share m: add them up.
+    // l: every lane summed the probabilities it computed (kDup lanes per token);
+    // o: rows were split over kTpp lane groups sharing one m.
 #pragma unroll
     for (int j = 0; j < GT; ++j) {
 #pragma unroll
-        for (int off = kLpt; off < 32; off <<= 1) {
-            l[j] += __shfl_xor_sync(0xffffffffu, l[j], off);
+        for (int off = 16; off > 0; off >>= 1) l[j] += __shfl_xor_sync(0xffffffffu, l[j], off);
+        l[j] *= 1.f / C::kDup;
+#pragma unroll
+        for (int off = kLpt; off < 32; off <<= 1)
 #pragma unroll
             for (int v = 0; v < kVec; ++v) o[j][v] += __shfl_xor_sync(0xffffffffu, o[j][v], off);
-        }
     }
-    float* merge_m = reinterpret_cast<float*>(smem + C::kRingBytes);  // [W][GT]
-    float* merge_l = merge_m + W * GT;                                // [W][GT]
-    float* merge_o = merge_l + W * GT;                                // [W][GT][D]
+    float* merge_m = reinterpret_cast<float*>(smem + C::kMergeOffset);  // [W][GT]
+    float* merge_l = merge_m + W * GT;                                  // [W][GT]
+    float* merge_o = merge_l + W * GT;                                  // [W][GT][D]
     if (grp == 0) {
 #pragma unroll
         for (int j = 0; j < GT; ++j)
@@ -323,7 +407,7 @@ __device__ __forceinline__ void decode_consume(const DecodeParams& p, unsigned c
             for (int w = 0; w < W; ++w) {
                 const float mw = merge_m[w * GT + j];
                 if (mw != -INFINITY) {
-                    const float sc = exp2f(mw - M);
+                    const float sc = fast_exp2(mw - M);
                     L = fmaf(merge_l[w * GT + j], sc, L);
                     O = fmaf(merge_o[(w * GT + j) * D + dd], sc, O);
                 }
@@ -379,7 +463,7 @@ __global__ void __launch_bounds__(DecodeTile<T, D, GT>::kThreads)
 #pragma unroll
         for (int st = 0; st < C::kStages; ++st) {
             mbar_init(smem_addr(bars + st), 1);
-            mbar_init(smem_addr(bars + C::kStages + st), C::kConsumerWarps);
+            mbar_init(smem_addr(bars + C::kStages + st), 1);  // released by its one consumer warp
         }
         *reinterpret_cast<volatile int*>(bars + 3 * C::kStages) = 0;
         fence_barrier_init();
@@ -425,7 +509,7 @@ __global__ void __launch_bounds__(128) decode_reduce_kernel(const DecodeParams p
 #pragma unroll 4
         for (int i = warp; i < nparts; i += 4) {
             const float mi = p.ws_m[row + i];
-            const float sc = (mi == -INFINITY) ? 0.f : exp2f(mi - M);
+            const float sc = fast_exp2(mi - M);  // empty partition: m = -inf -> 0
             L = fmaf(sc, p.ws_l[row + i], L);
             const float* po = p.ws_o + (row + i) * D + lane * kCols;
 #pragma unroll
