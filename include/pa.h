@@ -123,7 +123,9 @@ pa_status pa_copy_blocks_check(const int32_t* block_mapping, int num_pairs, uint
 int pa_decode_partition_tokens(int max_blocks_per_seq, int block_size, int partition_tokens);
 
 /* pa_decode_workspace_size -- bytes of device workspace pa_decode needs for
- * these sizes (0 when no sequence can span more than one partition). */
+ * these sizes: 256 bytes of work-scheduling counters, plus the partial
+ * softmax states of split sequences (num_seqs * num_q_heads * partitions *
+ * (head_dim + 2) floats) when a sequence can span more than one partition. */
 size_t pa_decode_workspace_size(int num_seqs, int num_q_heads, int head_dim, int max_blocks_per_seq,
                                 int block_size, int partition_tokens);
 
@@ -139,8 +141,13 @@ size_t pa_decode_workspace_size(int num_seqs, int num_q_heads, int head_dim, int
  * the dot products with q there ("PagedAttention" (compassingai.com) §8;
  * "PagedAttention 深度解析" §二 item 3).  Long sequences are split into
  * partitions of pa_decode_partition_tokens() tokens whose partial softmax
- * states are merged by a second kernel (log-sum-exp), which needs `workspace`
- * of at least pa_decode_workspace_size() bytes (may be NULL when that is 0).
+ * states are merged by a second kernel (log-sum-exp).
+ * workspace: device memory of at least pa_decode_workspace_size() bytes,
+ * 256-byte aligned and zero-filled once before its first use.  Its first 256
+ * bytes are work counters that every call returns to zero (a call that
+ * reported PA_DERR_TIMEOUT included), so a workspace can be reused for any
+ * number of calls without clearing it again; calls that share one must not
+ * overlap on the GPU.
  * n == 0 gives a zero row.  Accumulation is fp32; out has dtype `dtype`.
  * Supported: head_dim 64 or 128; block_size a multiple of 16 up to 256;
  * num_q_heads a multiple of num_kv_heads.

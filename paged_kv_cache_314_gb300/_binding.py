@@ -163,11 +163,12 @@ def decode_workspace_size(num_seqs: int, num_q_heads: int, head_dim: int, max_bl
 
 
 def decode_workspace(q: torch.Tensor, k_cache: torch.Tensor, block_tables: torch.Tensor,
-                     partition_tokens: int = 0) -> Optional[torch.Tensor]:
-    """Allocate (with torch) the workspace pa_decode needs for these shapes."""
+                     partition_tokens: int = 0) -> torch.Tensor:
+    """Allocate (with torch) the zero-filled workspace pa_decode needs for these
+    shapes; it can be reused by later calls with the same or smaller shapes."""
     S, Hq, d = q.shape
     n = decode_workspace_size(S, Hq, d, block_tables.shape[1], k_cache.shape[2], partition_tokens)
-    return torch.empty(n, dtype=torch.uint8, device=q.device) if n else None
+    return torch.zeros(n, dtype=torch.uint8, device=q.device)
 
 
 def decode(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,

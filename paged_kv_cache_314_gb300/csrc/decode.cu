@@ -18,16 +18,21 @@ int max_parts_for(int max_blocks_per_seq, int block_size, int P) {
     return static_cast<int>((max_ctx + P - 1) / P);
 }
 
+// Workspace: 256 bytes of scheduling counters (zero between calls), then the
+// partial softmax states of split sequences when a sequence can span more
+// than one partition.
+constexpr size_t kCounterBytes = 256;
+
 struct WsLayout {
     size_t m_off, l_off, o_off, bytes;
 };
 
 WsLayout ws_layout(int num_seqs, int num_q_heads, int head_dim, int max_parts) {
-    WsLayout w{0, 0, 0, 0};
+    WsLayout w{0, 0, 0, kCounterBytes};
     if (max_parts <= 1) return w;
     const size_t rows = static_cast<size_t>(num_seqs) * num_q_heads * max_parts;
-    w.m_off = 0;
-    w.l_off = round_up(rows * 4, 256);
+    w.m_off = kCounterBytes;
+    w.l_off = w.m_off + round_up(rows * 4, 256);
     w.o_off = w.l_off + round_up(rows * 4, 256);
     w.bytes = w.o_off + round_up(rows * static_cast<size_t>(head_dim) * 4, 256);
     return w;
@@ -57,7 +62,7 @@ extern "C" size_t pa_decode_workspace_size(int num_seqs, int num_q_heads, int he
                                            int partition_tokens) {
     using namespace pa;
     const int P = pa_decode_partition_tokens(max_blocks_per_seq, block_size, partition_tokens);
-    if (P <= 0 || num_seqs <= 0 || num_q_heads <= 0 || head_dim <= 0) return 0;
+    if (P <= 0 || num_seqs < 0 || num_q_heads <= 0 || head_dim <= 0) return 0;
     return ws_layout(num_seqs, num_q_heads, head_dim, max_parts_for(max_blocks_per_seq, block_size, P))
         .bytes;
 }
@@ -88,11 +93,9 @@ extern "C" pa_status pa_decode(void* out, const void* q, const void* k_cache, co
 
     const int max_parts = max_parts_for(max_blocks_per_seq, block_size, P);
     const WsLayout ws = ws_layout(num_seqs, num_q_heads, head_dim, max_parts);
-    if (ws.bytes > 0) {
-        if (workspace == nullptr) return PA_ERR_INVALID_ARG;
-        if (workspace_bytes < ws.bytes) return PA_ERR_WORKSPACE_TOO_SMALL;
-        if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return PA_ERR_INVALID_ARG;
-    }
+    if (workspace == nullptr) return PA_ERR_INVALID_ARG;
+    if (workspace_bytes < ws.bytes) return PA_ERR_WORKSPACE_TOO_SMALL;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return PA_ERR_INVALID_ARG;
     const int group = num_q_heads / num_kv_heads;
     const int gt = head_tile(group);
 
@@ -104,9 +107,10 @@ extern "C" pa_status pa_decode(void* out, const void* q, const void* k_cache, co
     p.block_tables = block_tables;
     p.context_lens = context_lens;
     unsigned char* wsb = static_cast<unsigned char*>(workspace);
-    p.ws_m = ws.bytes ? reinterpret_cast<float*>(wsb + ws.m_off) : nullptr;
-    p.ws_l = ws.bytes ? reinterpret_cast<float*>(wsb + ws.l_off) : nullptr;
-    p.ws_o = ws.bytes ? reinterpret_cast<float*>(wsb + ws.o_off) : nullptr;
+    p.counters = reinterpret_cast<unsigned int*>(wsb);
+    p.ws_m = max_parts > 1 ? reinterpret_cast<float*>(wsb + ws.m_off) : nullptr;
+    p.ws_l = max_parts > 1 ? reinterpret_cast<float*>(wsb + ws.l_off) : nullptr;
+    p.ws_o = max_parts > 1 ? reinterpret_cast<float*>(wsb + ws.o_off) : nullptr;
     p.d_err = d_err;
     p.num_seqs = num_seqs;
     p.num_q_heads = num_q_heads;

@@ -11,17 +11,24 @@
 // §8).
 //
 // How (GB300 design):
-//  * One CTA per (sequence, group of GT query heads sharing one kv head,
-//    partition of P tokens).  Partitions bound the work of one CTA so that
-//    skewed context lengths do not leave a long tail; a second kernel merges
-//    the partitions' softmax states (log-sum-exp).
-//  * Warp 4 is the producer: it reads the partition's slice of the block
-//    table (one entry per lane, shuffled out) and lane 0 issues bulk copies
+//  * Work items are (sequence, group of GT query heads sharing one kv head,
+//    partition of P tokens), numbered sequence by sequence.  Partitions bound
+//    an item's size so that skewed context lengths leave no long tail; a
+//    second kernel merges the partitions' softmax states (log-sum-exp).
+//  * The kernel is persistent: a few CTAs per SM take items from an atomic
+//    counter in the workspace until none is left (the last CTA to finish
+//    resets the counter).  The producer warp maps an item number to its
+//    sequence with a warp-parallel scan over context_lens and keeps the
+//    shared-memory ring full across item boundaries, so the HBM stream never
+//    drains between items.
+//  * Warp 4 is the producer: it reads the item's slice of the block table
+//    (one entry per lane, shuffled out) and lane 0 issues bulk copies
 //    (cp.async.bulk, TMA engine) of the 16-token K and V sub-blocks into a
-//    ring of kStages shared-memory stages guarded by mbarriers.  The copies
-//    carry an L2 evict-first hint: each K/V byte is read once per step.
+//    ring of kStages shared-memory stages guarded by mbarriers, plus one bulk
+//    copy of the item's query rows.  The copies carry an L2 evict-first hint:
+//    each K/V byte is read once per step.
 //  * Warps 0-3 consume, each one whole stage at a time (stage c belongs to
-//    warp c mod 4, so warps never wait on one another inside the loop).  A
+//    warp c mod 4, so warps never wait on one another inside an item).  A
 //    lane owns one 16-byte column slice of a token row (kLpt lanes per row),
 //    so one 128-bit shared load per lane reads kTpp whole rows without bank
 //    conflicts.  The per-lane partial dot products of a stage are finished by
@@ -31,13 +38,16 @@
 //    that multiply them into the V rows.  The softmax is online (running max
 //    m, running sum l, fp32) in the log2 domain (q is pre-scaled by
 //    scale*log2(e)); its max is updated once per stage.
-//  * Stages whose tokens are all valid take a path without any masking.
+//  * At the end of an item every warp that took part leaves its (m, l, o) in
+//    the item's merge slot; the last one to arrive merges them and writes the
+//    output row (or the partition's partial state) and frees the slot.
 //  * Tokens past context_len and tokens of blocks whose id fails the bounds
 //    check are masked by select, never by arithmetic, so poison in unused
-//    slots (NaN) cannot leak into the result.
+//    slots (NaN) cannot leak into the result.  Stages whose tokens are all
+//    valid take a path without any masking.
 //  * Every wait is bounded (mbar_wait): on timeout the CTA reports
 //    PA_DERR_TIMEOUT, stops issuing copies, waits for the copies it already
-//    issued and returns without writing its outputs.
+//    issued and returns; outputs of unfinished items are left unset.
 #pragma once
 
 #include "pa_device.cuh"
@@ -52,6 +62,7 @@ struct DecodeParams {
     const unsigned char* v_cache;
     const int32_t* block_tables;
     const int32_t* context_lens;
+    unsigned int* counters;  // [0] next work item, [1] CTAs finished (both zero between calls)
     float* ws_m;  // [S][Hq][max_parts] running max (log2 domain) per partition
     float* ws_l;  // [S][Hq][max_parts] running sum per partition
     float* ws_o;  // [S][Hq][max_parts][D] unnormalised output per partition
@@ -69,7 +80,29 @@ struct DecodeParams {
     float qk_scale_log2;  // scale * log2(e)
 };
 
-constexpr int align16(int x) { return (x + 15) / 16 * 16; }
+__host__ __device__ constexpr int align16(int x) { return (x + 15) / 16 * 16; }
+
+// Stage flags written by the producer next to each stage.
+constexpr uint32_t kStageFirst = 1u;  // first stage of its item for the consuming warp
+constexpr uint32_t kStageLast = 2u;   // last stage of its item for the consuming warp
+constexpr uint32_t kStageEnd = 4u;    // no more work: the consuming warp leaves
+
+struct StageMeta {
+    uint64_t mask;      // bit i: token i of the stage is valid
+    uint32_t item_seq;  // CTA-local number of the item the stage belongs to
+    uint32_t flags;
+};
+
+struct ItemRec {
+    int s;           // sequence
+    int hq0;         // first query head of the tile
+    int part;        // partition index
+    int nparts;      // partitions of the sequence; 0 = context length out of range
+    int first_warp;  // warp of the item's first stage
+    int nwarps;      // warps that take part (min(stages, 4))
+    int done;        // warps finished with the item
+    int pad;
+};
 
 template <typename T, int D, int GT>
 struct DecodeTile {
@@ -87,19 +120,26 @@ struct DecodeTile {
     static constexpr int kDup = kPasses >= kLpt ? 1 : kLpt / kPasses;   // lanes per logit
     static constexpr int kSubs = kTps / 16;           // 16-token bulk copies per tensor per stage
     static constexpr int kStageBytes = 2 * kTps * kRowBytes;
-    static constexpr int kStages = (65536 / kStageBytes) / kConsumerWarps * kConsumerWarps;
+    static constexpr int kStages = 65536 / kStageBytes;
+    static constexpr int kItems = GT >= 4 ? 2 : 3;    // item slots in flight
+    static constexpr int kQBytes = GT * D * kElem;    // query rows of one item
+    static constexpr int kMergeFloats = kConsumerWarps * GT * (D + 2);  // per item slot
     static constexpr int kRingBytes = kStages * kStageBytes;
-    static constexpr int kPOffset = kRingBytes;       // [W][GT][kTpp][kPasses] probabilities
-    static constexpr int kMergeOffset = kPOffset + kConsumerWarps * GT * kTps * 4;
-    static constexpr int kMergeFloats = kConsumerWarps * GT * (D + 2);
-    static constexpr int kBarOffset = align16(kMergeOffset + kMergeFloats * 4);
-    // full[kStages], empty[kStages], mask[kStages], abort flag
-    static constexpr int kSmemBytes = kBarOffset + 3 * kStages * 8 + 16;
+    static constexpr int kMetaOffset = kRingBytes;
+    static constexpr int kPOffset = kMetaOffset + kStages * 16;  // [W][GT][kTpp][kPasses] floats
+    static constexpr int kItemOffset = kPOffset + kConsumerWarps * GT * kTps * 4;
+    static constexpr int kQOffset = align16(kItemOffset + kItems * 32);
+    static constexpr int kMergeOffset = kQOffset + kItems * align16(kQBytes);
+    static constexpr int kBarOffset = align16(kMergeOffset + kItems * kMergeFloats * 4);
+    // full[kStages], empty[kStages], q_full[kItems], item_free[kItems]
+    static constexpr int kFlagOffset = kBarOffset + (2 * kStages + 2 * kItems) * 8;
+    static constexpr int kSmemBytes = kFlagOffset + 16;
     static constexpr uint64_t kFullMask = kTps >= 64 ? ~0ull : ((1ull << kTps) - 1ull);
     static_assert(kLpt >= 8 && kLpt <= 32 && 32 % kLpt == 0, "row must split over lanes");
     static_assert(kTps % 16 == 0 && kTps <= 64, "stage holds whole 16-token sub-blocks");
     static_assert(kPasses % 4 == 0 && kPasses * kTpp == kTps, "passes tile the stage");
     static_assert(kStages >= kConsumerWarps, "every consumer warp owns a stage");
+    static_assert(GT > 1 || 3 * (kSmemBytes + 1024) <= 228 * 1024, "three CTAs per SM");
 };
 
 // Reduce-scatter over the N values of each lane across the lanes xor-linked
@@ -128,96 +168,10 @@ struct ReduceScatter {
     }
 };
 
-template <typename T, int D, int GT>
-__device__ __forceinline__ void decode_produce(const DecodeParams& p, unsigned char* smem, int s,
-                                               int hk, int tok_begin, int tok_end, int nstages) {
-    using C = DecodeTile<T, D, GT>;
-    const int lane = threadIdx.x & 31;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBarOffset);
-    uint64_t* masks = bars + 2 * C::kStages;
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(masks + C::kStages);
-    const uint32_t full0 = smem_addr(bars);
-    const uint32_t empty0 = smem_addr(bars + C::kStages);
-
-    const uint64_t policy = l2_evict_first_policy();
-    const int B = p.block_size;
-    const int32_t* trow = p.block_tables + static_cast<size_t>(s) * p.max_blocks_per_seq;
-    const int blk_end = (tok_end + B - 1) / B;
-    int win = tok_begin / B;  // first logical block held in the lanes' window
-    int32_t entry = (win + lane < blk_end) ? __ldg(trow + win + lane) : -1;
-    const size_t head_bytes = static_cast<size_t>(B) * C::kRowBytes;
-    const size_t block_bytes = static_cast<size_t>(p.num_kv_heads) * head_bytes;
-    const unsigned char* kbase = p.k_cache + static_cast<size_t>(hk) * head_bytes;
-    const unsigned char* vbase = p.v_cache + static_cast<size_t>(hk) * head_bytes;
-
-    int issued = 0;
-    bool oob = false;
-    for (int c = 0; c < nstages; ++c) {
-        const int st = c % C::kStages;
-        const uint32_t round = static_cast<uint32_t>(c / C::kStages);
-        if (c >= C::kStages && !mbar_wait(empty0 + 8 * st, (round - 1) & 1)) {
-            if (lane == 0) report(p.d_err, PA_DERR_TIMEOUT);
-            *abort_flag = 1;
-            break;
-        }
-        if (*abort_flag) break;
-        const int t0 = tok_begin + c * C::kTps;
-        const int t1 = min(t0 + C::kTps, tok_end);
-        size_t src_off[C::kSubs];
-        uint32_t len_bytes[C::kSubs];
-        uint32_t bytes = 0;
-        uint64_t mask = 0;
-#pragma unroll
-        for (int r = 0; r < C::kSubs; ++r) {
-            const int t = t0 + 16 * r;
-            len_bytes[r] = 0;
-            src_off[r] = 0;
-            if (t < t1) {  // warp-uniform
-                const int lb = t / B;
-                const int off = t - lb * B;
-                const int len = min(16, t1 - t);
-                while (lb - win >= 32) {
-                    win += 32;
-                    entry = (win + lane < blk_end) ? __ldg(trow + win + lane) : -1;
-                }
-                const int pb = __shfl_sync(0xffffffffu, entry, lb - win);
-                if (static_cast<unsigned>(pb) < static_cast<unsigned>(p.num_blocks)) {
-                    src_off[r] = static_cast<size_t>(pb) * block_bytes +
-                                 static_cast<size_t>(off) * C::kRowBytes;
-                    len_bytes[r] = static_cast<uint32_t>(len) * C::kRowBytes;
-                    bytes += 2u * len_bytes[r];
-                    mask |= ((1ull << len) - 1ull) << (16 * r);
-                } else {
-                    oob = true;
-                }
-            }
-        }
-        if (lane == 0) {
-            masks[st] = mask;
-            const uint32_t full = full0 + 8 * st;
-            mbar_arrive_expect_tx(full, bytes);
-            const uint32_t sK = smem_addr(smem + st * C::kStageBytes);
-            const uint32_t sV = sK + C::kTps * C::kRowBytes;
-#pragma unroll
-            for (int r = 0; r < C::kSubs; ++r) {
-                if (len_bytes[r] != 0) {
-                    bulk_g2s(sK + 16 * r * C::kRowBytes, kbase + src_off[r], len_bytes[r], full, policy);
-                    bulk_g2s(sV + 16 * r * C::kRowBytes, vbase + src_off[r], len_bytes[r], full, policy);
-                }
-            }
-        }
-        __syncwarp();
-        issued = c + 1;
-    }
-    if (lane == 0) {
-        if (oob) report(p.d_err, PA_DERR_BLOCK_OOB);
-        // No copy may still be writing shared memory when the CTA exits.
-        for (int c = max(0, issued - C::kStages); c < issued; ++c) {
-            const int st = c % C::kStages;
-            if (!mbar_wait(full0 + 8 * st, static_cast<uint32_t>(c / C::kStages) & 1))
-                report(p.d_err, PA_DERR_TIMEOUT);
-        }
-    }
+// Number of work items of one sequence per query-head tile.
+__device__ __forceinline__ int items_of(int ctx, int max_ctx, int P) {
+    if (ctx < 0 || ctx > max_ctx) return 1;  // one item writes the zero rows
+    return ctx == 0 ? 1 : (ctx + P - 1) / P;
 }
 
 // One stage (kTps tokens) of one consumer warp.  kFull: every token valid.
@@ -310,50 +264,286 @@ __device__ __forceinline__ void decode_stage(const unsigned char* sK, const unsi
     __syncwarp();  // pw is rewritten by this warp's next stage
 }
 
+
 template <typename T, int D, int GT>
-__device__ __forceinline__ void decode_consume(const DecodeParams& p, unsigned char* smem, int s,
-                                               int hq0, int part, int nparts, int nstages) {
+__device__ __forceinline__ void decode_produce(const DecodeParams& p, unsigned char* smem) {
+    using C = DecodeTile<T, D, GT>;
+    constexpr int W = C::kConsumerWarps;
+    const int lane = threadIdx.x & 31;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBarOffset);
+    const uint32_t full0 = smem_addr(bars);
+    const uint32_t empty0 = smem_addr(bars + C::kStages);
+    const uint32_t qfull0 = smem_addr(bars + 2 * C::kStages);
+    const uint32_t ifree0 = smem_addr(bars + 2 * C::kStages + C::kItems);
+    StageMeta* meta = reinterpret_cast<StageMeta*>(smem + C::kMetaOffset);
+    ItemRec* items = reinterpret_cast<ItemRec*>(smem + C::kItemOffset);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kFlagOffset);
+
+    const uint64_t policy = l2_evict_first_policy();
+    const int S = p.num_seqs, HT = p.head_tiles, P = p.partition_tokens, B = p.block_size;
+    const int max_ctx = p.max_blocks_per_seq * B;
+    const size_t head_bytes = static_cast<size_t>(B) * C::kRowBytes;
+    const size_t block_bytes = static_cast<size_t>(p.num_kv_heads) * head_bytes;
+
+    // Cursor over the sequence-major item numbering: base = items of all
+    // sequences before s_cur; lanes hold context_lens[win0 + lane].
+    int s_cur = 0, base = 0, win0 = 0;
+    int ctx_lane = lane < S ? __ldg(p.context_lens + lane) : 0;
+    int c = 0;         // stages issued by this CTA
+    int item_seq = 0;  // items taken by this CTA
+    bool aborted = false;
+    bool oob = false;
+    int item_id = 0;
+    if (lane == 0) item_id = static_cast<int>(atomicAdd(p.counters, 1u));
+    item_id = __shfl_sync(0xffffffffu, item_id, 0);
+
+    while (!aborted) {
+        // ---- which sequence holds item_id?
+        bool found = false;
+        while (s_cur < S) {
+            if (s_cur - win0 >= 32) {
+                win0 = s_cur;
+                ctx_lane = win0 + lane < S ? __ldg(p.context_lens + win0 + lane) : 0;
+            }
+            const int sl = win0 + lane;
+            const int cnt = (sl >= s_cur && sl < S) ? HT * items_of(ctx_lane, max_ctx, P) : 0;
+            int incl = cnt;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, incl, off);
+                if (lane >= off) incl += y;
+            }
+            const int total = __shfl_sync(0xffffffffu, incl, 31);
+            if (base + total > item_id) {
+                const unsigned hit = __ballot_sync(0xffffffffu, base + incl > item_id);
+                const int L = __ffs(hit) - 1;
+                base += __shfl_sync(0xffffffffu, incl - cnt, L);
+                s_cur = win0 + L;
+                found = true;
+                break;
+            }
+            base += total;
+            s_cur = win0 + 32;
+        }
+        if (!found) break;
+        // take the next item now; its number is needed only after this item is issued
+        int next_id = 0;
+        if (lane == 0) next_id = static_cast<int>(atomicAdd(p.counters, 1u));
+
+        const int s = s_cur;
+        const int ctx = __shfl_sync(0xffffffffu, ctx_lane, s_cur - win0);
+        const bool valid = ctx >= 0 && ctx <= max_ctx;
+        const int np = items_of(ctx, max_ctx, P);
+        const int i_loc = item_id - base;
+        const int ht = i_loc / np;
+        const int part = i_loc - ht * np;
+        const int hq0 = ht * GT;
+        const int hk = hq0 / p.group;
+        const int tok_begin = part * P;
+        const int tok_end = valid ? min(tok_begin + P, ctx) : tok_begin;
+        const int nst = tok_end > tok_begin ? (tok_end - tok_begin + C::kTps - 1) / C::kTps : 1;
+        if (!valid && lane == 0) report(p.d_err, PA_DERR_CTX_OOB);
+
+        // ---- item slot: wait until its previous item has been merged
+        const int islot = item_seq % C::kItems;
+        if (item_seq >= C::kItems &&
+            !mbar_wait(ifree0 + 8 * islot, static_cast<uint32_t>(item_seq / C::kItems - 1) & 1)) {
+            if (lane == 0) report(p.d_err, PA_DERR_TIMEOUT);
+            *abort_flag = 1;
+            break;
+        }
+        if (lane == 0) {
+            ItemRec& r = items[islot];
+            r.s = s;
+            r.hq0 = hq0;
+            r.part = part;
+            r.nparts = valid ? np : 0;
+            r.first_warp = c % W;
+            r.nwarps = min(nst, W);
+            const uint32_t qf = qfull0 + 8 * islot;
+            mbar_arrive_expect_tx(qf, C::kQBytes);
+            bulk_g2s(smem_addr(smem + C::kQOffset + islot * align16(C::kQBytes)),
+                     static_cast<const T*>(p.q) + (static_cast<size_t>(s) * p.num_q_heads + hq0) * D,
+                     C::kQBytes, qf, policy);
+        }
+
+        // ---- this item's slice of the block table, one entry per lane
+        const int32_t* trow = p.block_tables + static_cast<size_t>(s) * p.max_blocks_per_seq;
+        const int blk_end = (tok_end + B - 1) / B;
+        int win = tok_begin / B;
+        int32_t entry = (win + lane < blk_end) ? __ldg(trow + win + lane) : -1;
+        const unsigned char* kbase = p.k_cache + static_cast<size_t>(hk) * head_bytes;
+        const unsigned char* vbase = p.v_cache + static_cast<size_t>(hk) * head_bytes;
+
+        for (int i = 0; i < nst; ++i) {
+            const int cc = c + i;
+            const int st = cc % C::kStages;
+            if (cc >= C::kStages &&
+                !mbar_wait(empty0 + 8 * st, static_cast<uint32_t>(cc / C::kStages - 1) & 1)) {
+                if (lane == 0) report(p.d_err, PA_DERR_TIMEOUT);
+                *abort_flag = 1;
+                aborted = true;
+                c = cc;
+                break;
+            }
+            const int t0 = tok_begin + i * C::kTps;
+            const int t1 = min(t0 + C::kTps, tok_end);
+            size_t src_off[C::kSubs];
+            uint32_t len_bytes[C::kSubs];
+            uint32_t bytes = 0;
+            uint64_t mask = 0;
+#pragma unroll
+            for (int r = 0; r < C::kSubs; ++r) {
+                const int t = t0 + 16 * r;
+                len_bytes[r] = 0;
+                src_off[r] = 0;
+                if (t < t1) {  // warp-uniform
+                    const int lb = t / B;
+                    const int off = t - lb * B;
+                    const int len = min(16, t1 - t);
+                    while (lb - win >= 32) {
+                        win += 32;
+                        entry = (win + lane < blk_end) ? __ldg(trow + win + lane) : -1;
+                    }
+                    const int pb = __shfl_sync(0xffffffffu, entry, lb - win);
+                    if (static_cast<unsigned>(pb) < static_cast<unsigned>(p.num_blocks)) {
+                        src_off[r] = static_cast<size_t>(pb) * block_bytes +
+                                     static_cast<size_t>(off) * C::kRowBytes;
+                        len_bytes[r] = static_cast<uint32_t>(len) * C::kRowBytes;
+                        bytes += 2u * len_bytes[r];
+                        mask |= ((1ull << len) - 1ull) << (16 * r);
+                    } else {
+                        oob = true;
+                    }
+                }
+            }
+            if (lane == 0) {
+                uint32_t flags = 0;
+                if (i < W) flags |= kStageFirst;
+                if (i + W >= nst) flags |= kStageLast;
+                meta[st].mask = mask;
+                meta[st].item_seq = static_cast<uint32_t>(item_seq);
+                meta[st].flags = flags;
+                const uint32_t full = full0 + 8 * st;
+                mbar_arrive_expect_tx(full, bytes);
+                const uint32_t sK = smem_addr(smem + st * C::kStageBytes);
+                const uint32_t sV = sK + C::kTps * C::kRowBytes;
+#pragma unroll
+                for (int r = 0; r < C::kSubs; ++r) {
+                    if (len_bytes[r] != 0) {
+                        bulk_g2s(sK + 16 * r * C::kRowBytes, kbase + src_off[r], len_bytes[r], full, policy);
+                        bulk_g2s(sV + 16 * r * C::kRowBytes, vbase + src_off[r], len_bytes[r], full, policy);
+                    }
+                }
+            }
+            __syncwarp();
+        }
+        if (aborted) break;
+        c += nst;
+        ++item_seq;
+        item_id = __shfl_sync(0xffffffffu, next_id, 0);
+        if (*abort_flag) aborted = true;
+    }
+
+    // ---- one end marker per consumer warp (the next W stages, one per warp)
+    if (!aborted) {
+        for (int i = 0; i < W; ++i) {
+            const int cc = c + i;
+            const int st = cc % C::kStages;
+            if (cc >= C::kStages &&
+                !mbar_wait(empty0 + 8 * st, static_cast<uint32_t>(cc / C::kStages - 1) & 1)) {
+                if (lane == 0) report(p.d_err, PA_DERR_TIMEOUT);
+                *abort_flag = 1;
+                break;
+            }
+            if (lane == 0) {
+                meta[st].mask = 0;
+                meta[st].flags = kStageEnd;
+                mbar_arrive(full0 + 8 * st);
+            }
+            c = cc + 1;
+        }
+    }
+    if (lane == 0) {
+        if (oob) report(p.d_err, PA_DERR_BLOCK_OOB);
+        // No bulk copy may still be writing shared memory when the CTA exits.
+        for (int cc = max(0, c - C::kStages); cc < c; ++cc) {
+            const int st = cc % C::kStages;
+            if (!mbar_wait(full0 + 8 * st, static_cast<uint32_t>(cc / C::kStages) & 1))
+                report(p.d_err, PA_DERR_TIMEOUT);
+        }
+        for (int k = max(0, item_seq - C::kItems); k < item_seq; ++k) {
+            const int sl = k % C::kItems;
+            if (!mbar_wait(qfull0 + 8 * sl, static_cast<uint32_t>(k / C::kItems) & 1))
+                report(p.d_err, PA_DERR_TIMEOUT);
+        }
+        __threadfence();  // this CTA's last counter update precedes its exit count
+    }
+}
+
+
+template <typename T, int D, int GT>
+__device__ __forceinline__ void decode_consume(const DecodeParams& p, unsigned char* smem) {
     using C = DecodeTile<T, D, GT>;
     constexpr int kVec = C::kVec, kLpt = C::kLpt, W = C::kConsumerWarps;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int grp = lane / kLpt;  // which row of a pass this lane reads
     const int lig = lane % kLpt;  // which 16-byte slice of the row
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBarOffset);
-    const uint64_t* masks = bars + 2 * C::kStages;
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 3 * C::kStages);
     const uint32_t full0 = smem_addr(bars);
     const uint32_t empty0 = smem_addr(bars + C::kStages);
+    const uint32_t qfull0 = smem_addr(bars + 2 * C::kStages);
+    const uint32_t ifree0 = smem_addr(bars + 2 * C::kStages + C::kItems);
+    const StageMeta* meta = reinterpret_cast<const StageMeta*>(smem + C::kMetaOffset);
+    ItemRec* items = reinterpret_cast<ItemRec*>(smem + C::kItemOffset);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kFlagOffset);
     float* pw = reinterpret_cast<float*>(smem + C::kPOffset) + warp * GT * C::kTps;
 
     float qf[GT][kVec];
-#pragma unroll
-    for (int j = 0; j < GT; ++j) {
-        const uint4 raw = __ldg(reinterpret_cast<const uint4*>(
-                                    static_cast<const T*>(p.q) +
-                                    (static_cast<size_t>(s) * p.num_q_heads + hq0 + j) * D) +
-                                lig);
-        Elem<T>::unpack(raw, qf[j]);
-#pragma unroll
-        for (int v = 0; v < kVec; ++v) qf[j][v] *= p.qk_scale_log2;
-    }
     float m[GT], l[GT], o[GT][kVec];
 #pragma unroll
     for (int j = 0; j < GT; ++j) {
         m[j] = -INFINITY;
         l[j] = 0.f;
 #pragma unroll
-        for (int v = 0; v < kVec; ++v) o[j][v] = 0.f;
+        for (int v = 0; v < kVec; ++v) {
+            o[j][v] = 0.f;
+            qf[j][v] = 0.f;
+        }
     }
 
-    for (int c = warp; c < nstages; c += W) {
-        const int st = c % C::kStages;
-        const uint32_t round = static_cast<uint32_t>(c / C::kStages);
-        if (!mbar_wait(full0 + 8 * st, round & 1)) {
+    for (int cc = warp;; cc += W) {
+        const int st = cc % C::kStages;
+        if (!mbar_wait(full0 + 8 * st, static_cast<uint32_t>(cc / C::kStages) & 1)) {
             if (lane == 0) report(p.d_err, PA_DERR_TIMEOUT);
             *abort_flag = 1;
             break;
         }
-        const uint64_t mask = masks[st];
+        const uint32_t flags = meta[st].flags;
+        if (flags & kStageEnd) break;
+        const uint64_t mask = meta[st].mask;
+        const int item_seq = static_cast<int>(meta[st].item_seq);
+        const int islot = item_seq % C::kItems;
+        if (flags & kStageFirst) {
+            if (!mbar_wait(qfull0 + 8 * islot, static_cast<uint32_t>(item_seq / C::kItems) & 1)) {
+                if (lane == 0) report(p.d_err, PA_DERR_TIMEOUT);
+                *abort_flag = 1;
+                break;
+            }
+            const T* qs = reinterpret_cast<const T*>(smem + C::kQOffset + islot * align16(C::kQBytes));
+#pragma unroll
+            for (int j = 0; j < GT; ++j) {
+                const uint4 raw = *reinterpret_cast<const uint4*>(qs + j * D + lig * kVec);
+                Elem<T>::unpack(raw, qf[j]);
+#pragma unroll
+                for (int v = 0; v < kVec; ++v) {
+                    qf[j][v] *= p.qk_scale_log2;
+                    o[j][v] = 0.f;
+                }
+                m[j] = -INFINITY;
+                l[j] = 0.f;
+            }
+        }
         const unsigned char* sK = smem + st * C::kStageBytes;
         const unsigned char* sV = sK + C::kTps * C::kRowBytes;
         if (mask == C::kFullMask)
@@ -361,119 +551,116 @@ __device__ __forceinline__ void decode_consume(const DecodeParams& p, unsigned c
         else
             decode_stage<T, D, GT, false>(sK, sV, mask, qf, m, l, o, pw, grp, lig);
         if (lane == 0) mbar_arrive(empty0 + 8 * st);
-    }
+        if (!(flags & kStageLast)) continue;
 
-    // l: every lane summed the probabilities it computed (kDup lanes per token);
-    // o: rows were split over kTpp lane groups sharing one m.
-#pragma unroll
-    for (int j = 0; j < GT; ++j) {
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) l[j] += __shfl_xor_sync(0xffffffffu, l[j], off);
-        l[j] *= 1.f / C::kDup;
-#pragma unroll
-        for (int off = kLpt; off < 32; off <<= 1)
-#pragma unroll
-            for (int v = 0; v < kVec; ++v) o[j][v] += __shfl_xor_sync(0xffffffffu, o[j][v], off);
-    }
-    float* merge_m = reinterpret_cast<float*>(smem + C::kMergeOffset);  // [W][GT]
-    float* merge_l = merge_m + W * GT;                                  // [W][GT]
-    float* merge_o = merge_l + W * GT;                                  // [W][GT][D]
-    if (grp == 0) {
-#pragma unroll
-        for (int j = 0; j < GT; ++j)
-#pragma unroll
-            for (int v = 0; v < kVec; ++v) merge_o[(warp * GT + j) * D + lig * kVec + v] = o[j][v];
-    }
-    if (lane == 0) {
+        // ---- this warp is done with the item: leave (m, l, o) in the merge slot
+        float* slot = reinterpret_cast<float*>(smem + C::kMergeOffset) + islot * C::kMergeFloats;
+        float* sm_m = slot;                // [W][GT]
+        float* sm_l = slot + W * GT;       // [W][GT]
+        float* sm_o = slot + 2 * W * GT;   // [W][GT][D]
 #pragma unroll
         for (int j = 0; j < GT; ++j) {
-            merge_m[warp * GT + j] = m[j];
-            merge_l[warp * GT + j] = l[j];
+            float lj = l[j];
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) lj += __shfl_xor_sync(0xffffffffu, lj, off);
+            float oj[kVec];
+#pragma unroll
+            for (int v = 0; v < kVec; ++v) {
+                oj[v] = o[j][v];
+#pragma unroll
+                for (int off = kLpt; off < 32; off <<= 1)
+                    oj[v] += __shfl_xor_sync(0xffffffffu, oj[v], off);
+            }
+            if (grp == 0) {
+#pragma unroll
+                for (int v = 0; v < kVec; ++v) sm_o[(warp * GT + j) * D + lig * kVec + v] = oj[v];
+            }
+            if (lane == 0) {
+                sm_m[warp * GT + j] = m[j];
+                sm_l[warp * GT + j] = lj * (1.f / C::kDup);  // kDup lanes counted each token
+            }
         }
-    }
-    named_barrier(1, W * 32);
-    if (*abort_flag) return;
+        __syncwarp();
+        __threadfence_block();
+        ItemRec& rec = items[islot];
+        int prev = 0;
+        if (lane == 0) prev = atomicAdd(&rec.done, 1);
+        prev = __shfl_sync(0xffffffffu, prev, 0);
+        if (prev != rec.nwarps - 1) continue;
 
-    const bool direct = nparts == 1;
-    for (int idx = threadIdx.x; idx < GT * D; idx += W * 32) {
-        const int j = idx / D;
-        const int dd = idx - j * D;
-        float M = -INFINITY;
-#pragma unroll
-        for (int w = 0; w < W; ++w) M = fmaxf(M, merge_m[w * GT + j]);
-        float L = 0.f, O = 0.f;
-        if (M != -INFINITY) {
-#pragma unroll
-            for (int w = 0; w < W; ++w) {
-                const float mw = merge_m[w * GT + j];
-                if (mw != -INFINITY) {
-                    const float sc = fast_exp2(mw - M);
-                    L = fmaf(merge_l[w * GT + j], sc, L);
-                    O = fmaf(merge_o[(w * GT + j) * D + dd], sc, O);
+        // ---- last warp of the item: merge the warps' states and write the result
+        __threadfence_block();
+        const int s = rec.s, hq0 = rec.hq0, part = rec.part, nparts = rec.nparts;
+        const int w0 = rec.first_warp, nw = rec.nwarps;
+        for (int idx = lane; idx < GT * D; idx += 32) {
+            const int j = idx / D;
+            const int dd = idx - j * D;
+            float M = -INFINITY;
+            for (int k = 0; k < nw; ++k) M = fmaxf(M, sm_m[((w0 + k) % W) * GT + j]);
+            float L = 0.f, O = 0.f;
+            if (M != -INFINITY) {
+                for (int k = 0; k < nw; ++k) {
+                    const int w = (w0 + k) % W;
+                    const float sc = fast_exp2(sm_m[w * GT + j] - M);  // empty warp: 2^-inf = 0
+                    L = fmaf(sm_l[w * GT + j], sc, L);
+                    O = fmaf(sm_o[(w * GT + j) * D + dd], sc, O);
+                }
+            }
+            const size_t row = static_cast<size_t>(s) * p.num_q_heads + hq0 + j;
+            if (nparts <= 1) {  // whole sequence in one item, or a zero row
+                static_cast<T*>(p.out)[row * D + dd] =
+                    Elem<T>::from_float(nparts == 1 && L > 0.f ? O / L : 0.f);
+            } else {
+                const size_t r = row * p.max_parts + part;
+                p.ws_o[r * D + dd] = O;
+                if (dd == 0) {
+                    p.ws_m[r] = M;
+                    p.ws_l[r] = L;
                 }
             }
         }
-        const size_t row = static_cast<size_t>(s) * p.num_q_heads + hq0 + j;
-        if (direct) {
-            static_cast<T*>(p.out)[row * D + dd] = Elem<T>::from_float(L > 0.f ? O / L : 0.f);
-        } else {
-            const size_t r = row * p.max_parts + part;
-            p.ws_o[r * D + dd] = O;
-            if (dd == 0) {
-                p.ws_m[r] = M;
-                p.ws_l[r] = L;
-            }
+        __syncwarp();
+        if (lane == 0) {
+            rec.done = 0;
+            mbar_arrive(ifree0 + 8 * islot);
         }
     }
 }
 
 template <typename T, int D, int GT>
 __global__ void __launch_bounds__(DecodeTile<T, D, GT>::kThreads)
-    decode_partition_kernel(const DecodeParams p) {
+    decode_persistent_kernel(const DecodeParams p) {
     using C = DecodeTile<T, D, GT>;
     extern __shared__ __align__(128) unsigned char smem[];
-    const int warp = threadIdx.x >> 5;
-
-    const int part = static_cast<int>(blockIdx.x % static_cast<unsigned>(p.max_parts));
-    const int rest = static_cast<int>(blockIdx.x / static_cast<unsigned>(p.max_parts));
-    const int ht = rest % p.head_tiles;
-    const int s = rest / p.head_tiles;
-    const int hq0 = ht * GT;
-    const int hk = hq0 / p.group;
-
-    const int ctx = p.context_lens[s];
-    const int max_ctx = p.max_blocks_per_seq * p.block_size;
-    if (ctx < 0 || ctx > max_ctx) {
-        if (part == 0) {
-            if (threadIdx.x == 0) report(p.d_err, PA_DERR_CTX_OOB);
-            T* out = static_cast<T*>(p.out) + (static_cast<size_t>(s) * p.num_q_heads + hq0) * D;
-            for (int i = threadIdx.x; i < GT * D; i += blockDim.x) out[i] = Elem<T>::from_float(0.f);
-        }
-        return;
-    }
-    const int P = p.partition_tokens;
-    const int nparts = ctx == 0 ? 1 : (ctx + P - 1) / P;
-    if (part >= nparts) return;
-    const int tok_begin = part * P;
-    const int tok_end = min(tok_begin + P, ctx);
-    const int nstages = (tok_end - tok_begin + C::kTps - 1) / C::kTps;
-
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBarOffset);
     if (threadIdx.x == 0) {
-#pragma unroll
         for (int st = 0; st < C::kStages; ++st) {
-            mbar_init(smem_addr(bars + st), 1);
-            mbar_init(smem_addr(bars + C::kStages + st), 1);  // released by its one consumer warp
+            mbar_init(smem_addr(bars + st), 1);                // producer's arrive + bytes
+            mbar_init(smem_addr(bars + C::kStages + st), 1);   // released by its consumer warp
         }
-        *reinterpret_cast<volatile int*>(bars + 3 * C::kStages) = 0;
+        for (int k = 0; k < C::kItems; ++k) {
+            mbar_init(smem_addr(bars + 2 * C::kStages + k), 1);            // query rows landed
+            mbar_init(smem_addr(bars + 2 * C::kStages + C::kItems + k), 1);  // item merged
+            reinterpret_cast<ItemRec*>(smem + C::kItemOffset)[k].done = 0;
+        }
+        *reinterpret_cast<volatile int*>(smem + C::kFlagOffset) = 0;
         fence_barrier_init();
     }
     __syncthreads();
-
-    if (warp == C::kConsumerWarps)
-        decode_produce<T, D, GT>(p, smem, s, hk, tok_begin, tok_end, nstages);
+    if ((threadIdx.x >> 5) == C::kConsumerWarps)
+        decode_produce<T, D, GT>(p, smem);
     else
-        decode_consume<T, D, GT>(p, smem, s, hq0, part, nparts, nstages);
+        decode_consume<T, D, GT>(p, smem);
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        // The last CTA out returns both counters to zero for the next call.
+        __threadfence();
+        const unsigned prev = atomicAdd(p.counters + 1, 1u);
+        if (prev == gridDim.x - 1) {
+            atomicExch(p.counters, 0u);
+            atomicExch(p.counters + 1, 0u);
+        }
+    }
 }
 
 // Merges the partitions of one (sequence, query head): M = max_i m_i,
@@ -532,10 +719,25 @@ template <typename T, int D, int GT>
 inline pa_status launch_decode_tile(const DecodeParams& p, cudaStream_t stream) {
     using C = DecodeTile<T, D, GT>;
     static std::atomic<uint64_t> smem_configured{0};  // one per instantiation
-    auto kernel = decode_partition_kernel<T, D, GT>;
+    static std::atomic<int> ctas_per_sm{0};
+    auto kernel = decode_persistent_kernel<T, D, GT>;
     if (ensure_smem(kernel, C::kSmemBytes, smem_configured) != PA_OK) return PA_ERR_CUDA;
-    const long long grid = static_cast<long long>(p.num_seqs) * p.head_tiles * p.max_parts;
-    if (grid <= 0 || grid > 0x7fffffffLL) return PA_ERR_UNSUPPORTED;
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return PA_ERR_CUDA;
+    int per_sm = ctas_per_sm.load(std::memory_order_relaxed);
+    if (per_sm == 0) {
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, C::kThreads,
+                                                          C::kSmemBytes) != cudaSuccess)
+            return PA_ERR_CUDA;
+        per_sm = per_sm < 1 ? 1 : per_sm;
+        ctas_per_sm.store(per_sm, std::memory_order_relaxed);
+    }
+    const long long work = static_cast<long long>(p.num_seqs) * p.head_tiles * p.max_parts;
+    if (work > 0x7fffffffLL) return PA_ERR_UNSUPPORTED;
+    long long grid = static_cast<long long>(sms) * per_sm;
+    if (grid > work) grid = work;
     kernel<<<static_cast<unsigned>(grid), C::kThreads, C::kSmemBytes, stream>>>(p);
     if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
     if (p.max_parts > 1) {

@@ -42,10 +42,11 @@ def test_host_only_entry_points(lib):
     assert pa.decode_partition_tokens(128, 16, 0) % 16 == 0
     assert pa.decode_partition_tokens(128, 16, 24) == -1  # not a multiple of the block size
     assert pa.decode_partition_tokens(128, 24, 0) == -1   # block size not a multiple of 16
-    assert pa.decode_workspace_size(4, 8, 128, 4, 16, 64) == 0  # one partition: no workspace
+    # one partition: only the 256 bytes of work counters
+    assert pa.decode_workspace_size(4, 8, 128, 4, 16, 64) == 256
     n = pa.decode_workspace_size(64, 32, 128, 128, 16, 256)
     rows = 64 * 32 * 8
-    assert n >= rows * (128 + 2) * 4
+    assert n >= 256 + rows * (128 + 2) * 4
 
 
 def test_invalid_arguments_are_rejected_before_any_launch(lib):

@@ -72,6 +72,35 @@ def test_tiny_workload():
     _check_step(wl.tiny())
 
 
+def test_many_short_sequences_and_bad_lengths():
+    """Work scheduling: hundreds of sequences (the item cursor crosses many
+    32-sequence windows), lengths 0, 1, tiny and a few thousand, two lengths
+    out of range; run twice on the same workspace (its counters must return
+    to zero)."""
+    rng = np.random.default_rng(31)
+    ctx = rng.choice([0, 1, 2, 15, 16, 17, 33, 250, 257, 700, 3000], size=700)
+    w = wl.custom("many", list(ctx), dtype="bf16", num_q_heads=4, num_kv_heads=2, head_dim=128,
+                  block_size=16, seed=32, pool_factor=1.2)
+    w.context_lens[[5, 600]] = [-1, w.max_blocks_per_seq * 16 + 16]
+    d = upload(w)
+    _, _, ref, err = oracle_step(w)
+    assert err == oracle.ERR_CTX_OOB
+    ws = pa.decode_workspace(d["q"], d["k_cache"], d["block_tables"], 256)
+    outs = []
+    pa.kv_write(d["k_new"], d["v_new"], d["k_cache"], d["v_cache"], d["slot_mapping"],
+                d_err=d["d_err"])
+    for _ in range(2):
+        out = torch.empty_like(d["q"])
+        pa.decode(out, d["q"], d["k_cache"], d["v_cache"], d["block_tables"], d["context_lens"],
+                  w.scale, partition_tokens=256, workspace=ws, d_err=d["d_err"])
+        torch.cuda.synchronize()
+        outs.append(out)
+        assert int(ws[:8].view(torch.int32).abs().sum().item()) == 0, "work counters not reset"
+    assert int(d["d_err"].item()) == err
+    assert torch.equal(outs[0], outs[1])
+    assert_close(out_f64(outs[0]), ref, "bf16", "many")
+
+
 # ---------------------------------------------------------------------------
 # named workloads at full size
 # ---------------------------------------------------------------------------
