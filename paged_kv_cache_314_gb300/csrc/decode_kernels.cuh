@@ -447,8 +447,9 @@ __device__ __forceinline__ void decode_produce(const DecodeParams& p, unsigned c
 
     // ---- one end marker per consumer warp (the next W stages, one per warp)
     if (!aborted) {
+        const int c_end = c;
         for (int i = 0; i < W; ++i) {
-            const int cc = c + i;
+            const int cc = c_end + i;
             const int st = cc % C::kStages;
             if (cc >= C::kStages &&
                 !mbar_wait(empty0 + 8 * st, static_cast<uint32_t>(cc / C::kStages - 1) & 1)) {
