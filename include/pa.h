@@ -159,6 +159,38 @@ pa_status pa_decode(void* out, const void* q, const void* k_cache, const void* v
                     int partition_tokens, pa_dtype dtype, void* workspace,
                     size_t workspace_bytes, uint32_t* d_err, pa_stream_t stream);
 
+/* pa_decode_static_workspace -- pa_decode for callers that cannot allocate.
+ *
+ * The pages have no counterpart to this call: it exists for callers that must
+ * not allocate device memory while they run, e.g. code executing inside
+ * another framework's memory pool or allocator hook, a real-time serving loop
+ * that forbids cudaMalloc (it can synchronise the device), or an embedding
+ * that has no allocator at all.  It computes exactly what pa_decode computes,
+ * with the same arguments except the workspace: the scratch lives in a
+ * static device array of PA_DECODE_STATIC_SCRATCH_BYTES that this library
+ * holds on every GPU that loads it, until the process exits.  The call
+ * allocates nothing (no cudaMalloc, no library allocator).
+ *   - Sizes: when pa_decode_workspace_size() for these sizes exceeds
+ *     PA_DECODE_STATIC_SCRATCH_BYTES, it returns PA_ERR_WORKSPACE_TOO_SMALL
+ *     and enqueues nothing; use pa_decode with your own workspace then.
+ *   - Set-up: the first call on a device, with that device current, looks up
+ *     the array's device address once; make that first call before capturing
+ *     the stream into a graph.
+ *   - Sharing: every call uses the same array and it keeps the last call's
+ *     contents; each call clears the part that must start at zero (the work
+ *     counters) on `stream` first.  Calls whose work overlaps on the GPU (other
+ *     streams, other host threads on the same device) race on the array and
+ *     must be serialised by the caller.
+ */
+#define PA_DECODE_STATIC_SCRATCH_BYTES (64u << 20)
+pa_status pa_decode_static_workspace(void* out, const void* q, const void* k_cache,
+                                     const void* v_cache, const int32_t* block_tables,
+                                     int max_blocks_per_seq, const int32_t* context_lens,
+                                     int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                                     int block_size, int num_blocks, float scale,
+                                     int partition_tokens, pa_dtype dtype, uint32_t* d_err,
+                                     pa_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif
