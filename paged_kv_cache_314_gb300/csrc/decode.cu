@@ -7,7 +7,7 @@
 namespace pa {
 namespace {
 
-constexpr int kDefaultPartitionTokens = 256;
+constexpr int kDefaultPartitionTokens = 512;
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
