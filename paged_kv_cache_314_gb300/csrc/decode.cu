@@ -1,8 +1,12 @@
 // decode.cu -- host side of pa_decode: argument checks, split-K planning,
 // workspace layout and dispatch to the typed kernels.
+#include <cudaTypedefs.h>
 #include <math.h>
 
+#include <mutex>
+
 #include "decode_kernels.cuh"
+#include "decode_tc.cuh"
 
 namespace pa {
 namespace {
@@ -43,6 +47,36 @@ int head_tile(int group) {
     for (int gt = 8; gt > 1; gt >>= 1)
         if (group % gt == 0) return gt;
     return 1;
+}
+
+// cuTensorMapEncodeTiled from the driver, looked up once.
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static std::once_flag once;
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    std::call_once(once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    });
+    return fn;
+}
+
+// The K or V pool as a [rows = NB*Hkv*B][128] matrix of 16-bit elements, read
+// in [16 rows x 64 columns] boxes with 128-byte swizzle.
+bool make_pool_map(CUtensorMap* map, const void* pool, long long rows, pa_dtype dtype) {
+    PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
+    if (encode == nullptr) return false;
+    const cuuint64_t dims[2] = {128, static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {128 * 2};
+    const cuuint32_t box[2] = {64, 16};
+    const cuuint32_t elem_strides[2] = {1, 1};
+    return encode(map, dtype == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                  2, const_cast<void*>(pool), dims, strides, box, elem_strides,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 }  // namespace
@@ -125,6 +159,18 @@ extern "C" pa_status pa_decode(void* out, const void* q, const void* k_cache, co
     p.qk_scale_log2 = scale * 1.4426950408889634f;  // log2(e)
 
     const cudaStream_t st = as_cuda(stream);
+    // Grouped-query heads with 16-bit K/V and head_dim 128: the tensor-core path.
+    const long long pool_rows = static_cast<long long>(num_blocks) * num_kv_heads * block_size;
+    if ((dtype == PA_F16 || dtype == PA_BF16) && head_dim == 128 && group >= 4 && group <= 16 &&
+        P % 128 == 0 && pool_rows < 0x7fffffffLL) {
+        CUtensorMap map_k, map_v;
+        if (make_pool_map(&map_k, k_cache, pool_rows, dtype) &&
+            make_pool_map(&map_v, v_cache, pool_rows, dtype)) {
+            p.head_tiles = num_kv_heads;
+            return dtype == PA_BF16 ? launch_decode_tc_bf16(p, map_k, map_v, st)
+                                    : launch_decode_tc_f16(p, map_k, map_v, st);
+        }
+    }
     switch (dtype) {
         case PA_F32: return launch_decode_f32(p, head_dim, gt, st);
         case PA_F16: return launch_decode_f16(p, head_dim, gt, st);

@@ -1,8 +1,14 @@
-// decode_f16.cu -- decode kernel instantiations for __half elements.
+// decode_f16.cu -- decode kernel instantiations for __half elements
+// (SIMT path and the grouped-query tensor-core path).
 #include "decode_kernels.cuh"
+#include "decode_tc.cuh"
 
 namespace pa {
 pa_status launch_decode_f16(const DecodeParams& p, int head_dim, int gt, cudaStream_t stream) {
     return launch_decode_typed<__half>(p, head_dim, gt, stream);
+}
+pa_status launch_decode_tc_f16(const DecodeParams& p, const CUtensorMap& mapK,
+                               const CUtensorMap& mapV, cudaStream_t stream) {
+    return launch_decode_tc_typed<__half>(p, mapK, mapV, stream);
 }
 }  // namespace pa

@@ -1,0 +1,605 @@
+// decode_tc.cuh -- paged decode attention for grouped-query heads on the
+// sm_103a tensor cores (tcgen05 + TMA tensor copies).
+//
+// When g = Hq/Hkv query heads share one kv head, q.K^T for a block of tokens
+// is a real dense tile ([tokens x d] x [d x g]) and so is P.V; the SIMT path
+// would spend g times the FMAs per byte.  Here one work item is (sequence,
+// kv head, partition of P tokens) with all g query heads, processed in stages
+// of 128 tokens:
+//   S  [128 tokens x 16]  = K_stage [128 x 128] . Q^T      (tcgen05.mma, M=128, N=16)
+//   softmax over the stage's rows, online across stages (fp32, log2 domain)
+//   O^T[128 dims x 16]    = V_stage^T [128 x 128] . P^T    (tcgen05.mma, M=128, N=16)
+// with both accumulators in tensor memory (32 columns).  The query heads are
+// padded to N = 16 (g <= 16; padding rows are zero).
+//
+// The paging is unchanged: the block table is walked block by block in
+// order, every 16-token block of a stage is fetched through its table entry
+// ("PagedAttention" (compassingai.com) §5, §8) by a 2-D TMA tensor copy of a
+// [16 rows x 64 columns] box with 128-byte swizzle (the K/V pools are viewed
+// as [NB*Hkv*B rows x d columns]); the swizzled tiles are the MMA operands as
+// they land.
+//
+// Warp roles (192 threads, persistent, one CTA per SM):
+//   warp 0   producer: item cursor over context_lens (as in the SIMT path),
+//            block-table slice, TMA loads into a 3-stage ring (64 KB/stage),
+//            bulk copy of the item's query rows into a staging slot
+//   warp 1   allocates tensor memory, issues the MMAs (one thread)
+//   warps 2-5 the "team": thread = row (token for S, head dimension for O),
+//            reading the accumulator lanes of its warp's quadrant
+// Rows of invalid tokens (past context_len, or in a block whose id fails the
+// bounds check) get -inf logits and their V rows are zeroed before P.V, so
+// NaN poison cannot reach the products.  P is rounded to the element type
+// before P.V and the softmax sum uses the same rounded values.
+#pragma once
+
+#include <type_traits>
+
+#include "decode_kernels.cuh"
+#include "tc_ptx.cuh"
+
+namespace pa {
+
+template <typename T>
+struct TcTile {
+    static constexpr int D = 128;
+    static constexpr int kStageTok = 128;                         // MMA M (tokens)
+    static constexpr int kN = 16;                                 // query heads, padded
+    static constexpr int kHalfBytes = kStageTok * 128;            // 64 columns x 128 rows
+    static constexpr int kTileBytes = 2 * kHalfBytes;             // K or V of a stage: 32 KB
+    static constexpr int kStageBytes = 2 * kTileBytes;            // 64 KB
+    static constexpr int kStages = 3;
+    static constexpr int kQSlots = 2;
+    static constexpr int kQBytes = kN * D * 2;                    // staged query rows (linear)
+    static constexpr int kOpBytes = 2 * kN * 128;                 // Q or P operand, swizzled: 4 KB
+    static constexpr int kRingOff = 0;
+    static constexpr int kQsOff = kStages * kStageBytes;
+    static constexpr int kQopOff = kQsOff + kQSlots * kQBytes;
+    static constexpr int kPopOff = kQopOff + kOpBytes;
+    static constexpr int kRedOff = kPopOff + kOpBytes;            // [2][4][16] floats
+    static constexpr int kRecOff = kRedOff + 2 * 4 * kN * 4;      // item records [kQSlots]
+    static constexpr int kMetaOff = kRecOff + kQSlots * 16;       // stage meta [kStages]
+    static constexpr int kBarOff = kMetaOff + kStages * 16;
+    // full[S], empty[S], qfull[Q], qempty[Q], q_ready, s_full, p_full, o_full, drain
+    static constexpr int kNumBars = 2 * kStages + 2 * kQSlots + 5;
+    static constexpr int kMiscOff = kBarOff + kNumBars * 8;       // tmem base, abort, team flags
+    static constexpr int kSmemBytes = kMiscOff + 32 + 1024;       // + alignment slack
+    static constexpr int kThreads = 192;
+    static constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
+    static_assert(kBf16 || std::is_same<T, __half>::value, "16-bit operands only");
+    static constexpr uint32_t kIdescS = tc::instr_desc_f16(kBf16, 128, kN, false, false);
+    static constexpr uint32_t kIdescO = tc::instr_desc_f16(kBf16, 128, kN, true, false);
+};
+
+struct TcStageMeta {
+    uint32_t item_seq;
+    int nvalid;       // tokens of the stage before the partition end
+    uint32_t groups;  // bit r: 16-token group r was loaded (its block id passed the check)
+    uint32_t flags;   // kStageFirst / kStageLast / kStageEnd
+};
+
+struct TcItemRec {
+    int s, hq0, part, nparts;  // nparts 0: context length out of range (zero rows)
+};
+
+template <typename T>
+__device__ __forceinline__ void tc_produce(const DecodeParams& p, const CUtensorMap* mapK,
+                                           const CUtensorMap* mapV, unsigned char* sm,
+                                           uint32_t base) {
+    using C = TcTile<T>;
+    const int lane = threadIdx.x & 31;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::kBarOff);
+    const uint32_t full0 = smem_addr(bars), empty0 = smem_addr(bars + C::kStages);
+    const uint32_t qfull0 = smem_addr(bars + 2 * C::kStages);
+    const uint32_t qempty0 = smem_addr(bars + 2 * C::kStages + C::kQSlots);
+    TcStageMeta* meta = reinterpret_cast<TcStageMeta*>(sm + C::kMetaOff);
+    TcItemRec* recs = reinterpret_cast<TcItemRec*>(sm + C::kRecOff);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + C::kMiscOff + 4);
+
+    const uint64_t policy = l2_evict_first_policy();
+    const int S = p.num_seqs, HT = p.head_tiles, P = p.partition_tokens, B = p.block_size;
+    const int g = p.group;
+    const int max_ctx = p.max_blocks_per_seq * B;
+    const uint32_t qbytes = static_cast<uint32_t>(g * C::D * 2);
+
+    int s_cur = 0, base_items = 0, win0 = 0;
+    int ctx_lane = lane < S ? __ldg(p.context_lens + lane) : 0;
+    int c = 0, item_seq = 0;
+    bool aborted = false, oob = false;
+    int item_id = 0;
+    if (lane == 0) item_id = static_cast<int>(atomicAdd(p.counters, 1u));
+    item_id = __shfl_sync(0xffffffffu, item_id, 0);
+
+    while (!aborted) {
+        bool found = false;
+        while (s_cur < S) {
+            if (s_cur - win0 >= 32) {
+                win0 = s_cur;
+                ctx_lane = win0 + lane < S ? __ldg(p.context_lens + win0 + lane) : 0;
+            }
+            const int sl = win0 + lane;
+            const int cnt = (sl >= s_cur && sl < S) ? HT * items_of(ctx_lane, max_ctx, P) : 0;
+            int incl = cnt;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, incl, off);
+                if (lane >= off) incl += y;
+            }
+            const int total = __shfl_sync(0xffffffffu, incl, 31);
+            if (base_items + total > item_id) {
+                const unsigned hit = __ballot_sync(0xffffffffu, base_items + incl > item_id);
+                const int L = __ffs(hit) - 1;
+                base_items += __shfl_sync(0xffffffffu, incl - cnt, L);
+                s_cur = win0 + L;
+                found = true;
+                break;
+            }
+            base_items += total;
+            s_cur = win0 + 32;
+        }
+        if (!found) break;
+        int next_id = 0;
+        if (lane == 0) next_id = static_cast<int>(atomicAdd(p.counters, 1u));
+
+        const int s = s_cur;
+        const int ctx = __shfl_sync(0xffffffffu, ctx_lane, s_cur - win0);
+        const bool valid = ctx >= 0 && ctx <= max_ctx;
+        const int np = items_of(ctx, max_ctx, P);
+        const int i_loc = item_id - base_items;
+        const int hk = i_loc / np;  // one item per kv head: all g query heads
+        const int part = i_loc - hk * np;
+        const int hq0 = hk * g;
+        const int tok_begin = part * P;
+        const int tok_end = valid ? min(tok_begin + P, ctx) : tok_begin;
+        const int nst = tok_end > tok_begin ? (tok_end - tok_begin + C::kStageTok - 1) / C::kStageTok : 1;
+        if (!valid && lane == 0) report(p.d_err, PA_DERR_CTX_OOB);
+
+        const int qs = item_seq % C::kQSlots;
+        if (item_seq >= C::kQSlots &&
+            !mbar_wait_warp(qempty0 + 8 * qs, static_cast<uint32_t>(item_seq / C::kQSlots - 1) & 1)) {
+            if (lane == 0) report(p.d_err, PA_DERR_TIMEOUT);
+            *abort_flag = 1;
+            break;
+        }
+        if (lane == 0) {
+            recs[qs].s = s;
+            recs[qs].hq0 = hq0;
+            recs[qs].part = part;
+            recs[qs].nparts = valid ? np : 0;
+            const uint32_t qf = qfull0 + 8 * qs;
+            mbar_arrive_expect_tx(qf, qbytes);
+            bulk_g2s(base + C::kQsOff + qs * C::kQBytes,
+                     static_cast<const T*>(p.q) + (static_cast<size_t>(s) * p.num_q_heads + hq0) * C::D,
+                     qbytes, qf, policy);
+        }
+
+        const int32_t* trow = p.block_tables + static_cast<size_t>(s) * p.max_blocks_per_seq;
+        const int blk_end = (tok_end + B - 1) / B;
+        int win = tok_begin / B;
+        int32_t entry = (win + lane < blk_end) ? __ldg(trow + win + lane) : -1;
+
+        for (int i = 0; i < nst; ++i) {
+            const int cc = c + i;
+            const int st = cc % C::kStages;
+            if (cc >= C::kStages &&
+                !mbar_wait_warp(empty0 + 8 * st, static_cast<uint32_t>(cc / C::kStages - 1) & 1)) {
+                if (lane == 0) report(p.d_err, PA_DERR_TIMEOUT);
+                *abort_flag = 1;
+                aborted = true;
+                c = cc;
+                break;
+            }
+            const int t0 = tok_begin + i * C::kStageTok;
+            const int t1 = min(t0 + C::kStageTok, tok_end);
+            int rows[8];
+            uint32_t groups = 0;
+#pragma unroll
+            for (int r = 0; r < 8; ++r) {
+                const int t = t0 + 16 * r;
+                rows[r] = 0;
+                if (t < t1) {  // warp-uniform
+                    const int lb = t / B;
+                    const int off = t - lb * B;
+                    while (lb - win >= 32) {
+                        win += 32;
+                        entry = (win + lane < blk_end) ? __ldg(trow + win + lane) : -1;
+                    }
+                    const int pb = __shfl_sync(0xffffffffu, entry, lb - win);
+                    if (static_cast<unsigned>(pb) < static_cast<unsigned>(p.num_blocks)) {
+                        rows[r] = (pb * p.num_kv_heads + hk) * B + off;
+                        groups |= 1u << r;
+                    } else {
+                        oob = true;
+                    }
+                }
+            }
+            if (lane == 0) {
+                uint32_t flags = 0;
+                if (i == 0) flags |= kStageFirst;
+                if (i == nst - 1) flags |= kStageLast;
+                meta[st].item_seq = static_cast<uint32_t>(item_seq);
+                meta[st].nvalid = max(0, t1 - t0);
+                meta[st].groups = groups;
+                meta[st].flags = flags;
+                const uint32_t full = full0 + 8 * st;
+                mbar_arrive_expect_tx(full, static_cast<uint32_t>(__popc(groups)) * 4u * 2048u);
+                const uint32_t sK = base + C::kRingOff + st * C::kStageBytes;
+                const uint32_t sV = sK + C::kTileBytes;
+#pragma unroll
+                for (int r = 0; r < 8; ++r) {
+                    if (groups & (1u << r)) {
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            tc::tma_load_2d(sK + h * C::kHalfBytes + r * 2048, mapK, 64 * h, rows[r], full, policy);
+                            tc::tma_load_2d(sV + h * C::kHalfBytes + r * 2048, mapV, 64 * h, rows[r], full, policy);
+                        }
+                    }
+                }
+            }
+            __syncwarp();
+        }
+        if (aborted) break;
+        c += nst;
+        ++item_seq;
+        item_id = __shfl_sync(0xffffffffu, next_id, 0);
+        if (*abort_flag) aborted = true;
+    }
+    if (!aborted) {  // one end marker: the MMA warp and the team read stages in order
+        const int st = c % C::kStages;
+        if (c >= C::kStages &&
+            !mbar_wait_warp(empty0 + 8 * st, static_cast<uint32_t>(c / C::kStages - 1) & 1)) {
+            if (lane == 0) report(p.d_err, PA_DERR_TIMEOUT);
+            *abort_flag = 1;
+        } else {
+            if (lane == 0) {
+                meta[st].flags = kStageEnd;
+                meta[st].nvalid = 0;
+                meta[st].groups = 0;
+                mbar_arrive(full0 + 8 * st);
+            }
+            ++c;
+        }
+    }
+    if (lane == 0) {
+        if (oob) report(p.d_err, PA_DERR_BLOCK_OOB);
+        for (int cc = max(0, c - C::kStages); cc < c; ++cc)
+            if (!mbar_wait(full0 + 8 * (cc % C::kStages), static_cast<uint32_t>(cc / C::kStages) & 1))
+                report(p.d_err, PA_DERR_TIMEOUT);
+        for (int k = max(0, item_seq - C::kQSlots); k < item_seq; ++k)
+            if (!mbar_wait(qfull0 + 8 * (k % C::kQSlots), static_cast<uint32_t>(k / C::kQSlots) & 1))
+                report(p.d_err, PA_DERR_TIMEOUT);
+        __threadfence();
+    }
+}
+
+template <typename T>
+__device__ __forceinline__ void tc_mma(const DecodeParams& p, unsigned char* sm, uint32_t base,
+                                       uint32_t tmem) {
+    using C = TcTile<T>;
+    const int lane = threadIdx.x & 31;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::kBarOff);
+    const uint32_t full0 = smem_addr(bars), empty0 = smem_addr(bars + C::kStages);
+    const uint32_t qready = smem_addr(bars + 2 * C::kStages + 2 * C::kQSlots);
+    const uint32_t sfull = qready + 8, pfull = qready + 16, ofull = qready + 24, drain = qready + 32;
+    const TcStageMeta* meta = reinterpret_cast<const TcStageMeta*>(sm + C::kMetaOff);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + C::kMiscOff + 4);
+    const uint32_t tS = tmem, tO = tmem + C::kN;
+    const uint32_t qop = base + C::kQopOff, pop = base + C::kPopOff;
+
+    int nitems = 0;
+    for (int c = 0;; ++c) {
+        const int st = c % C::kStages;
+        if (!mbar_wait_warp(full0 + 8 * st, static_cast<uint32_t>(c / C::kStages) & 1)) {
+            if (lane == 0) report(p.d_err, PA_DERR_TIMEOUT);
+            *abort_flag = 1;
+            break;
+        }
+        const uint32_t flags = meta[st].flags;
+        if (flags & kStageEnd) break;
+        if (flags & kStageFirst) {
+            if (!mbar_wait_warp(qready, static_cast<uint32_t>(nitems) & 1)) {
+                if (lane == 0) report(p.d_err, PA_DERR_TIMEOUT);
+                *abort_flag = 1;
+                break;
+            }
+            ++nitems;
+        }
+        tc::fence_after_sync();
+        const uint32_t sK = base + C::kRingOff + st * C::kStageBytes;
+        const uint32_t sV = sK + C::kTileBytes;
+        if (lane == 0) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {  // 16 head dims per step
+                const uint64_t a = tc::smem_desc_sw128(sK + (j / 4) * C::kHalfBytes + (j % 4) * 32, 16, 1024);
+                const uint64_t b = tc::smem_desc_sw128(qop + (j / 4) * 2048 + (j % 4) * 32, 16, 1024);
+                tc::mma_f16(tS, a, b, C::kIdescS, j > 0);
+            }
+            tc::mma_commit(sfull);
+        }
+        __syncwarp();
+        if (!mbar_wait_warp(pfull, static_cast<uint32_t>(c) & 1)) {
+            if (lane == 0) report(p.d_err, PA_DERR_TIMEOUT);
+            *abort_flag = 1;
+            break;
+        }
+        tc::fence_after_sync();
+        if (lane == 0) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {  // 16 tokens per step
+                const uint64_t a = tc::smem_desc_sw128(sV + j * 2048, C::kHalfBytes, 1024);
+                const uint64_t b = tc::smem_desc_sw128(pop + (j / 4) * 2048 + (j % 4) * 32, 16, 1024);
+                tc::mma_f16(tO, a, b, C::kIdescO, j > 0);
+            }
+            tc::mma_commit(ofull);
+            tc::mma_commit(empty0 + 8 * st);  // the stage's K and V are free once both MMAs are done
+        }
+        __syncwarp();
+    }
+    if (lane == 0) {  // every MMA issued here has completed before tensor memory is freed
+        tc::mma_commit(drain);
+        if (!mbar_wait(drain, 0)) report(p.d_err, PA_DERR_TIMEOUT);
+    }
+    __syncwarp();
+}
+
+// The four team warps agree on every wait: thread 0 waits (bounded), the
+// outcome goes through one of two alternating shared flags and a named
+// barrier, so no team thread can stay behind at a later barrier.
+struct TeamSync {
+    volatile int* flags;  // [2]
+    int tid;
+    int k = 0;
+    __device__ __forceinline__ bool wait(uint32_t bar, uint32_t parity, uint32_t* d_err,
+                                         volatile int* abort_flag) {
+        const int slot = k++ & 1;
+        if (tid == 0) {
+            const bool ok = mbar_wait(bar, parity);
+            if (!ok) {
+                report(d_err, PA_DERR_TIMEOUT);
+                *abort_flag = 1;
+            }
+            flags[slot] = ok ? 1 : 0;
+        }
+        named_barrier(1, 128);
+        return flags[slot] != 0;
+    }
+};
+
+template <typename T>
+__device__ __forceinline__ void tc_team(const DecodeParams& p, unsigned char* sm, uint32_t base,
+                                        uint32_t tmem) {
+    using C = TcTile<T>;
+    constexpr int N = C::kN;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int tid = threadIdx.x - 64;  // 0..127
+    const int quad = warp & 3;         // accumulator lanes 32*quad .. +31
+    const int row = 32 * quad + lane;  // token of S, head dimension of O
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::kBarOff);
+    const uint32_t full0 = smem_addr(bars);
+    const uint32_t qfull0 = smem_addr(bars + 2 * C::kStages);
+    const uint32_t qempty0 = smem_addr(bars + 2 * C::kStages + C::kQSlots);
+    const uint32_t qready = smem_addr(bars + 2 * C::kStages + 2 * C::kQSlots);
+    const uint32_t sfull = qready + 8, pfull = qready + 16, ofull = qready + 24;
+    const TcStageMeta* meta = reinterpret_cast<const TcStageMeta*>(sm + C::kMetaOff);
+    const TcItemRec* recs = reinterpret_cast<const TcItemRec*>(sm + C::kRecOff);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + C::kMiscOff + 4);
+    float* red_max = reinterpret_cast<float*>(sm + C::kRedOff);  // [4][16]
+    float* red_sum = red_max + 4 * N;                            // [4][16]
+    TeamSync team{reinterpret_cast<volatile int*>(sm + C::kMiscOff + 8), tid};
+    const uint32_t lane_off = static_cast<uint32_t>(32 * quad) << 16;
+    const int g = p.group;
+
+    float m[N], l[N], o[N];
+#pragma unroll
+    for (int h = 0; h < N; ++h) {
+        m[h] = -INFINITY;
+        l[h] = 0.f;
+        o[h] = 0.f;
+    }
+    TcItemRec rec{0, 0, 0, 0};
+    for (int c = 0;; ++c) {
+        const int st = c % C::kStages;
+        if (!team.wait(full0 + 8 * st, static_cast<uint32_t>(c / C::kStages) & 1, p.d_err, abort_flag)) break;
+        const uint32_t flags = meta[st].flags;
+        if (flags & kStageEnd) break;
+        const int item_seq = static_cast<int>(meta[st].item_seq);
+        const int nvalid = meta[st].nvalid;
+        const uint32_t groups = meta[st].groups;
+        const int qs = item_seq % C::kQSlots;
+
+        if (flags & kStageFirst) {
+            if (!team.wait(qfull0 + 8 * qs, static_cast<uint32_t>(item_seq / C::kQSlots) & 1, p.d_err, abort_flag))
+                break;
+            rec = recs[qs];  // the slot is reused once qempty is released below
+            // query rows -> the swizzled K-major Q operand (rows >= g stay zero)
+            const unsigned char* src = sm + C::kQsOff + qs * C::kQBytes;
+            for (int idx = tid; idx < g * 16; idx += 128) {
+                const int h = idx >> 4, ch = idx & 15;
+                const uint4 v = *reinterpret_cast<const uint4*>(src + (h * C::D + ch * 8) * 2);
+                *reinterpret_cast<uint4*>(sm + C::kQopOff + (ch >> 3) * 2048 + (h >> 3) * 1024 +
+                                          (h & 7) * 128 + (((ch & 7) ^ (h & 7)) << 4)) = v;
+            }
+            tc::fence_async_smem();
+            named_barrier(1, 128);
+            if (tid == 0) {
+                mbar_arrive(qempty0 + 8 * qs);
+                mbar_arrive(qready);
+            }
+#pragma unroll
+            for (int h = 0; h < N; ++h) {
+                m[h] = -INFINITY;
+                l[h] = 0.f;
+                o[h] = 0.f;
+            }
+        }
+
+        // ---- S row of this thread's token: mask, stage max per head
+        if (!team.wait(sfull, static_cast<uint32_t>(c) & 1, p.d_err, abort_flag)) break;
+        tc::fence_after_sync();
+        float x[N];
+        tc::tmem_ld16(tmem + lane_off, x);
+        const bool valid = row < nvalid && ((groups >> (row >> 4)) & 1u);
+#pragma unroll
+        for (int h = 0; h < N; ++h) {
+            x[h] = (valid && h < g) ? x[h] * p.qk_scale_log2 : -INFINITY;
+            float mx = x[h];
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+            if (lane == 0) red_max[quad * N + h] = mx;
+        }
+        named_barrier(1, 128);
+        float alpha[N];
+        unsigned char* pop = sm + C::kPopOff;
+#pragma unroll
+        for (int h = 0; h < N; ++h) {
+            const float mt = fmaxf(fmaxf(red_max[h], red_max[N + h]), fmaxf(red_max[2 * N + h], red_max[3 * N + h]));
+            const float m_new = fmaxf(m[h], mt);
+            float pr = 0.f;
+            alpha[h] = 1.f;
+            if (m_new != -INFINITY) {
+                alpha[h] = fast_exp2(m[h] - m_new);  // 0 while m was -inf
+                m[h] = m_new;
+                pr = Elem<T>::to_float(Elem<T>::from_float(fast_exp2(x[h] - m_new)));
+            }
+            l[h] = l[h] * alpha[h] + pr;
+            if (h < g) {  // P[h][row] in the swizzled K-major P operand
+                const int col = row & 63;
+                *reinterpret_cast<T*>(pop + (row >> 6) * 2048 + (h >> 3) * 1024 + (h & 7) * 128 +
+                                      ((((col >> 3) ^ (h & 7))) << 4) + (col & 7) * 2) = Elem<T>::from_float(pr);
+            }
+        }
+        if (!valid) {  // zero this token's V row (both 64-column halves)
+            unsigned char* vrow = sm + C::kRingOff + st * C::kStageBytes + C::kTileBytes +
+                                  (row >> 3) * 1024 + (row & 7) * 128;
+#pragma unroll
+            for (int h2 = 0; h2 < 2; ++h2)
+#pragma unroll
+                for (int k = 0; k < 8; ++k)
+                    *reinterpret_cast<uint4*>(vrow + h2 * C::kHalfBytes + k * 16) = make_uint4(0, 0, 0, 0);
+        }
+        tc::fence_async_smem();
+        tc::fence_before_sync();
+        named_barrier(1, 128);
+        if (tid == 0) mbar_arrive(pfull);
+
+        // ---- O^T row of this thread's head dimension: rescale and add
+        if (!team.wait(ofull, static_cast<uint32_t>(c) & 1, p.d_err, abort_flag)) break;
+        tc::fence_after_sync();
+        float ov[N];
+        tc::tmem_ld16(tmem + C::kN + lane_off, ov);
+#pragma unroll
+        for (int h = 0; h < N; ++h) o[h] = o[h] * alpha[h] + ov[h];
+        tc::fence_before_sync();
+
+        if (flags & kStageLast) {
+#pragma unroll
+            for (int h = 0; h < N; ++h) {
+                float lt = l[h];
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) lt += __shfl_xor_sync(0xffffffffu, lt, off);
+                if (lane == 0) red_sum[quad * N + h] = lt;
+            }
+            named_barrier(1, 128);
+            for (int h = 0; h < g; ++h) {
+                const float L = red_sum[h] + red_sum[N + h] + red_sum[2 * N + h] + red_sum[3 * N + h];
+                const size_t r = static_cast<size_t>(rec.s) * p.num_q_heads + rec.hq0 + h;
+                if (rec.nparts <= 1) {
+                    static_cast<T*>(p.out)[r * C::D + row] =
+                        Elem<T>::from_float(rec.nparts == 1 && L > 0.f ? o[h] / L : 0.f);
+                } else {
+                    const size_t w = r * p.max_parts + rec.part;
+                    p.ws_o[w * C::D + row] = o[h];
+                    if (row == 0) {
+                        p.ws_m[w] = m[h];
+                        p.ws_l[w] = L;
+                    }
+                }
+            }
+            named_barrier(1, 128);  // red_sum is reused by the next item
+        }
+    }
+    tc::fence_before_sync();
+}
+
+template <typename T>
+__global__ void __launch_bounds__(TcTile<T>::kThreads, 1)
+    decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap mapK,
+                     const __grid_constant__ CUtensorMap mapV) {
+    using C = TcTile<T>;
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    const uint32_t raw = smem_addr(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;  // 128-byte swizzle atoms need 1 KB alignment
+    unsigned char* sm = smem_raw + (base - raw);
+    const int warp = threadIdx.x >> 5;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::kBarOff);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + C::kMiscOff);
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < C::kNumBars; ++i) mbar_init(smem_addr(bars + i), 1);
+        *reinterpret_cast<volatile int*>(sm + C::kMiscOff + 4) = 0;
+        fence_barrier_init();
+        tc::prefetch_tensormap(&mapK);
+        tc::prefetch_tensormap(&mapV);
+    }
+    // zero the Q and P operands once: padding rows (heads >= g) stay zero
+    for (int i = threadIdx.x; i < 2 * C::kOpBytes / 16; i += blockDim.x)
+        reinterpret_cast<uint4*>(sm + C::kQopOff)[i] = make_uint4(0, 0, 0, 0);
+    tc::fence_async_smem();
+    if (warp == 1) tc::tmem_alloc(smem_addr(tmem_slot), 32);
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
+
+    if (warp == 0)
+        tc_produce<T>(p, &mapK, &mapV, sm, base);
+    else if (warp == 1)
+        tc_mma<T>(p, sm, base, tmem);
+    else
+        tc_team<T>(p, sm, base, tmem);
+
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        tc::fence_after_sync();
+        tc::tmem_free(tmem, 32);
+    }
+    if (threadIdx.x == 0) {
+        __threadfence();
+        const unsigned prev = atomicAdd(p.counters + 1, 1u);
+        if (prev == gridDim.x - 1) {
+            atomicExch(p.counters, 0u);
+            atomicExch(p.counters + 1, 0u);
+        }
+    }
+}
+
+template <typename T>
+inline pa_status launch_decode_tc_typed(const DecodeParams& p, const CUtensorMap& mapK,
+                                        const CUtensorMap& mapV, cudaStream_t stream) {
+    using C = TcTile<T>;
+    static std::atomic<uint64_t> smem_configured{0};
+    auto kernel = decode_tc_kernel<T>;
+    if (ensure_smem(kernel, C::kSmemBytes, smem_configured) != PA_OK) return PA_ERR_CUDA;
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return PA_ERR_CUDA;
+    const long long work = static_cast<long long>(p.num_seqs) * p.head_tiles * p.max_parts;
+    if (work > 0x7fffffffLL) return PA_ERR_UNSUPPORTED;
+    long long grid = sms;
+    if (grid > work) grid = work;
+    kernel<<<static_cast<unsigned>(grid), C::kThreads, C::kSmemBytes, stream>>>(p, mapK, mapV);
+    if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
+    if (p.max_parts > 1) {
+        decode_reduce_kernel<T, C::D><<<p.num_seqs * p.num_q_heads, 128, 0, stream>>>(p);
+        if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
+    }
+    return PA_OK;
+}
+
+pa_status launch_decode_tc_f16(const DecodeParams& p, const CUtensorMap& mapK,
+                               const CUtensorMap& mapV, cudaStream_t stream);
+pa_status launch_decode_tc_bf16(const DecodeParams& p, const CUtensorMap& mapK,
+                                const CUtensorMap& mapV, cudaStream_t stream);
+
+}  // namespace pa

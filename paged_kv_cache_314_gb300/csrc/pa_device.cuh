@@ -76,6 +76,14 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
     }
 }
 
+// Bounded wait by every lane of a warp; the lanes agree on the outcome, so a
+// warp never splits into lanes that go on and lanes that give up (which would
+// leave the others stuck in a later shuffle or barrier).
+__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity) {
+    const bool ok = mbar_wait(bar, parity);
+    return __all_sync(0xffffffffu, ok);
+}
+
 // ---- bulk copies (TMA, non-tensor) ------------------------------------------
 
 // L2 policy for data read exactly once per step: evict it first.

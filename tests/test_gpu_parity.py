@@ -68,6 +68,42 @@ def test_small_parity(case, partition):
     _check_step(w, partition_tokens=P)
 
 
+# Grouped-query heads with 16-bit K/V, head_dim 128 and partitions that are a
+# multiple of 128 tokens run on the tensor-core path (TMA + tcgen05).
+GQA_TC = [
+    # dtype, Hq, Hkv, B, P, ctx
+    ("bf16", 8, 2, 16, 512, [1, 15, 16, 17, 127, 128, 129, 300, 515, 1100]),
+    ("f16", 16, 2, 16, 128, [3, 100, 128, 257, 600, 2049]),
+    ("bf16", 64, 4, 32, 256, [1, 31, 256, 257, 777]),
+    ("bf16", 16, 4, 128, 512, [1, 127, 128, 129, 1000, 1111]),
+    ("f16", 32, 2, 16, 512, [0, 5, 512, 513, 1024, 3000]),
+]
+
+
+@pytest.mark.parametrize("case", range(len(GQA_TC)))
+def test_gqa_tensor_core_parity(case):
+    dtype, Hq, Hkv, B, P, ctx = GQA_TC[case]
+    w = wl.custom(f"gqa_tc{case}", ctx, dtype=dtype, num_q_heads=Hq, num_kv_heads=Hkv,
+                  head_dim=128, block_size=B, seed=200 + case, pool_factor=1.3)
+    _check_step(w, partition_tokens=P)
+
+
+def test_gqa_tensor_core_bad_entries():
+    w = wl.custom("gqa_bad", [40, 300, 600, 5, 0, 260], dtype="bf16", num_q_heads=16,
+                  num_kv_heads=2, head_dim=128, block_size=16, seed=210, max_blocks_per_seq=40)
+    w.context_lens[0] = -3
+    w.context_lens[3] = 40 * 16 + 1
+    w.block_tables[2, 7] = w.num_blocks + 5
+    w.block_tables[5, 0] = -7
+    d = upload(w)
+    out = gpu_step(w, d, partition_tokens=256)
+    _, _, ref, err = oracle_step(w)
+    assert err == oracle.ERR_CTX_OOB | oracle.ERR_BLOCK_OOB
+    assert int(d["d_err"].item()) == err
+    assert_close(out_f64(out), ref, "bf16", "gqa_bad")
+    assert (out[0] == 0).all() and (out[3] == 0).all() and (out[4] == 0).all()
+
+
 def test_tiny_workload():
     _check_step(wl.tiny())
 
