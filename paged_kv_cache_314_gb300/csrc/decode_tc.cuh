@@ -55,12 +55,12 @@ struct TcTile {
     static constexpr int kQsOff = kStages * kStageBytes;
     static constexpr int kQopOff = kQsOff + kQSlots * kQBytes;
     static constexpr int kPopOff = kQopOff + kOpBytes;
-    static constexpr int kRedOff = kPopOff + kOpBytes;            // [2][4][16] floats
-    static constexpr int kRecOff = kRedOff + 2 * 4 * kN * 4;      // item records [kQSlots]
+    static constexpr int kRedOff = kPopOff + 2 * kOpBytes;        // P double-buffered; [4][16] floats
+    static constexpr int kRecOff = kRedOff + 4 * kN * 4;          // item records [kQSlots]
     static constexpr int kMetaOff = kRecOff + kQSlots * 16;       // stage meta [kStages]
     static constexpr int kBarOff = kMetaOff + kStages * 16;
-    // full[S], empty[S], qfull[Q], qempty[Q], q_ready, s_full, p_full, o_full, drain
-    static constexpr int kNumBars = 2 * kStages + 2 * kQSlots + 5;
+    // full[S], empty[S], qfull[Q], qempty[Q], q_ready, s_full[2], p_full[2], o_full[2], drain
+    static constexpr int kNumBars = 2 * kStages + 2 * kQSlots + 8;
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;       // tmem base, abort, team flags
     static constexpr int kSmemBytes = kMiscOff + 32 + 1024;       // + alignment slack
     static constexpr int kThreads = 192;
@@ -271,68 +271,121 @@ __device__ __forceinline__ void tc_produce(const DecodeParams& p, const CUtensor
     }
 }
 
+// Barrier indices after full[S], empty[S], qfull[Q], qempty[Q].
+template <typename T>
+struct TcBars {
+    using C = TcTile<T>;
+    static constexpr int kQReady = 2 * C::kStages + 2 * C::kQSlots;
+    static constexpr int kSFull = kQReady + 1;  // [2]
+    static constexpr int kPFull = kSFull + 2;   // [2]
+    static constexpr int kOFull = kPFull + 2;   // [2]
+    static constexpr int kDrain = kOFull + 2;
+};
+
+template <typename T>
+__device__ __forceinline__ void tc_mma1(uint32_t sK, uint32_t qop, uint32_t tS) {
+    using C = TcTile<T>;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {  // 16 head dimensions per step
+        const uint64_t a = tc::smem_desc_sw128(sK + (j / 4) * C::kHalfBytes + (j % 4) * 32, 16, 1024);
+        const uint64_t b = tc::smem_desc_sw128(qop + (j / 4) * 2048 + (j % 4) * 32, 16, 1024);
+        tc::mma_f16(tS, a, b, C::kIdescS, j > 0);
+    }
+}
+
+template <typename T>
+__device__ __forceinline__ void tc_mma2(uint32_t sV, uint32_t pop, uint32_t tO) {
+    using C = TcTile<T>;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {  // 16 tokens per step
+        const uint64_t a = tc::smem_desc_sw128(sV + j * 2048, C::kHalfBytes, 1024);
+        const uint64_t b = tc::smem_desc_sw128(pop + (j / 4) * 2048 + (j % 4) * 32, 16, 1024);
+        tc::mma_f16(tO, a, b, C::kIdescO, j > 0);
+    }
+}
+
+// MMA issuer.  Stage c: S[c%2] = K_c.Q^T (MMA1), then O[c%2] = V_c^T.P_c^T
+// (MMA2) once the team has written P_c.  MMA1 of the next stage is issued
+// before MMA2 of this one when the next stage has already landed and belongs
+// to the same item, so the team's softmax of stage c+1 overlaps MMA2 of c.
 template <typename T>
 __device__ __forceinline__ void tc_mma(const DecodeParams& p, unsigned char* sm, uint32_t base,
                                        uint32_t tmem) {
     using C = TcTile<T>;
+    using Bi = TcBars<T>;
     const int lane = threadIdx.x & 31;
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::kBarOff);
     const uint32_t full0 = smem_addr(bars), empty0 = smem_addr(bars + C::kStages);
-    const uint32_t qready = smem_addr(bars + 2 * C::kStages + 2 * C::kQSlots);
-    const uint32_t sfull = qready + 8, pfull = qready + 16, ofull = qready + 24, drain = qready + 32;
+    const uint32_t qready = smem_addr(bars + Bi::kQReady);
+    const uint32_t sfull0 = smem_addr(bars + Bi::kSFull), pfull0 = smem_addr(bars + Bi::kPFull);
+    const uint32_t ofull0 = smem_addr(bars + Bi::kOFull), drain = smem_addr(bars + Bi::kDrain);
     const TcStageMeta* meta = reinterpret_cast<const TcStageMeta*>(sm + C::kMetaOff);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + C::kMiscOff + 4);
-    const uint32_t tS = tmem, tO = tmem + C::kN;
-    const uint32_t qop = base + C::kQopOff, pop = base + C::kPopOff;
+    const uint32_t qop = base + C::kQopOff, pop0 = base + C::kPopOff;
+    auto stage_k = [&](int c) { return base + C::kRingOff + (c % C::kStages) * C::kStageBytes; };
+    auto fail = [&]() {
+        if (lane == 0) report(p.d_err, PA_DERR_TIMEOUT);
+        *abort_flag = 1;
+    };
 
     int nitems = 0;
-    for (int c = 0;; ++c) {
+    // MMA1 of stage c (waiting for its data, and for its query rows at an item start).
+    // Returns 0 = issued, 1 = end marker, -1 = gave up.
+    auto issue_mma1 = [&](int c) -> int {
         const int st = c % C::kStages;
-        if (!mbar_wait_warp(full0 + 8 * st, static_cast<uint32_t>(c / C::kStages) & 1)) {
-            if (lane == 0) report(p.d_err, PA_DERR_TIMEOUT);
-            *abort_flag = 1;
-            break;
-        }
+        if (!mbar_wait_warp(full0 + 8 * st, static_cast<uint32_t>(c / C::kStages) & 1)) return -1;
         const uint32_t flags = meta[st].flags;
-        if (flags & kStageEnd) break;
+        if (flags & kStageEnd) return 1;
         if (flags & kStageFirst) {
-            if (!mbar_wait_warp(qready, static_cast<uint32_t>(nitems) & 1)) {
-                if (lane == 0) report(p.d_err, PA_DERR_TIMEOUT);
-                *abort_flag = 1;
-                break;
-            }
+            if (!mbar_wait_warp(qready, static_cast<uint32_t>(nitems) & 1)) return -1;
             ++nitems;
         }
         tc::fence_after_sync();
-        const uint32_t sK = base + C::kRingOff + st * C::kStageBytes;
-        const uint32_t sV = sK + C::kTileBytes;
         if (lane == 0) {
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {  // 16 head dims per step
-                const uint64_t a = tc::smem_desc_sw128(sK + (j / 4) * C::kHalfBytes + (j % 4) * 32, 16, 1024);
-                const uint64_t b = tc::smem_desc_sw128(qop + (j / 4) * 2048 + (j % 4) * 32, 16, 1024);
-                tc::mma_f16(tS, a, b, C::kIdescS, j > 0);
-            }
-            tc::mma_commit(sfull);
+            tc_mma1<T>(stage_k(c), qop, tmem + (c & 1) * C::kN);
+            tc::mma_commit(sfull0 + 8 * (c & 1));
         }
         __syncwarp();
-        if (!mbar_wait_warp(pfull, static_cast<uint32_t>(c) & 1)) {
-            if (lane == 0) report(p.d_err, PA_DERR_TIMEOUT);
-            *abort_flag = 1;
+        return 0;
+    };
+
+    int r = issue_mma1(0);
+    if (r < 0) fail();
+    for (int c = 0; r == 0; ++c) {
+        // MMA1 of stage c+1 early, when it has landed and continues the same item
+        bool next_done = false;
+        {
+            const int st1 = (c + 1) % C::kStages;
+            int early = 0;
+            if (lane == 0 &&
+                mbar_try_wait(full0 + 8 * st1, static_cast<uint32_t>((c + 1) / C::kStages) & 1))
+                early = !(meta[st1].flags & (kStageEnd | kStageFirst));
+            if (__shfl_sync(0xffffffffu, early, 0)) {
+                r = issue_mma1(c + 1);
+                next_done = true;
+            }
+        }
+        if (r < 0) {
+            fail();
+            break;
+        }
+        if (!mbar_wait_warp(pfull0 + 8 * (c & 1), static_cast<uint32_t>(c / 2) & 1)) {
+            fail();
             break;
         }
         tc::fence_after_sync();
         if (lane == 0) {
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {  // 16 tokens per step
-                const uint64_t a = tc::smem_desc_sw128(sV + j * 2048, C::kHalfBytes, 1024);
-                const uint64_t b = tc::smem_desc_sw128(pop + (j / 4) * 2048 + (j % 4) * 32, 16, 1024);
-                tc::mma_f16(tO, a, b, C::kIdescO, j > 0);
-            }
-            tc::mma_commit(ofull);
-            tc::mma_commit(empty0 + 8 * st);  // the stage's K and V are free once both MMAs are done
+            tc_mma2<T>(stage_k(c) + C::kTileBytes, pop0 + (c & 1) * C::kOpBytes,
+                       tmem + 2 * C::kN + (c & 1) * C::kN);
+            tc::mma_commit(ofull0 + 8 * (c & 1));
+            tc::mma_commit(empty0 + 8 * (c % C::kStages));  // K_c and V_c are free
         }
         __syncwarp();
+        if (!next_done) r = issue_mma1(c + 1);
+        if (r < 0) {
+            fail();
+            break;
+        }
     }
     if (lane == 0) {  // every MMA issued here has completed before tensor memory is freed
         tc::mma_commit(drain);
@@ -364,11 +417,44 @@ struct TeamSync {
     }
 };
 
-template <typename T>
+// Max (or sum) over the 32 lanes of G per-lane values by a reduce-scatter:
+// afterwards lane l holds the result for value index l / (32 / G).
+template <int G, bool kMax>
+__device__ __forceinline__ float warp_reduce_scatter(float (&v)[G], int lane) {
+    float x[G];
+#pragma unroll
+    for (int i = 0; i < G; ++i) x[i] = v[i];
+    int n = G;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        if (n > 1) {
+            const bool up = (lane & off) != 0;
+#pragma unroll
+            for (int i = 0; i < G / 2; ++i) {
+                if (i < n / 2) {
+                    const float keep = up ? x[i + n / 2] : x[i];
+                    const float send = up ? x[i] : x[i + n / 2];
+                    const float other = __shfl_xor_sync(0xffffffffu, send, off);
+                    x[i] = kMax ? fmaxf(keep, other) : keep + other;
+                }
+            }
+            n >>= 1;
+        } else {
+            const float other = __shfl_xor_sync(0xffffffffu, x[0], off);
+            x[0] = kMax ? fmaxf(x[0], other) : x[0] + other;
+        }
+    }
+    return x[0];
+}
+
+// Team: softmax of stage c (thread = token row of S), then the deferred
+// O-accumulate of stage c-1 of the same item (thread = head dimension of O^T);
+// at an item's last stage its own O-accumulate and the output.
+template <typename T, int G>
 __device__ __forceinline__ void tc_team(const DecodeParams& p, unsigned char* sm, uint32_t base,
                                         uint32_t tmem) {
     using C = TcTile<T>;
-    constexpr int N = C::kN;
+    using Bi = TcBars<T>;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int tid = threadIdx.x - 64;  // 0..127
     const int quad = warp & 3;         // accumulator lanes 32*quad .. +31
@@ -377,25 +463,41 @@ __device__ __forceinline__ void tc_team(const DecodeParams& p, unsigned char* sm
     const uint32_t full0 = smem_addr(bars);
     const uint32_t qfull0 = smem_addr(bars + 2 * C::kStages);
     const uint32_t qempty0 = smem_addr(bars + 2 * C::kStages + C::kQSlots);
-    const uint32_t qready = smem_addr(bars + 2 * C::kStages + 2 * C::kQSlots);
-    const uint32_t sfull = qready + 8, pfull = qready + 16, ofull = qready + 24;
+    const uint32_t qready = smem_addr(bars + Bi::kQReady);
+    const uint32_t sfull0 = smem_addr(bars + Bi::kSFull), pfull0 = smem_addr(bars + Bi::kPFull);
+    const uint32_t ofull0 = smem_addr(bars + Bi::kOFull);
     const TcStageMeta* meta = reinterpret_cast<const TcStageMeta*>(sm + C::kMetaOff);
     const TcItemRec* recs = reinterpret_cast<const TcItemRec*>(sm + C::kRecOff);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + C::kMiscOff + 4);
-    float* red_max = reinterpret_cast<float*>(sm + C::kRedOff);  // [4][16]
-    float* red_sum = red_max + 4 * N;                            // [4][16]
+    float* red = reinterpret_cast<float*>(sm + C::kRedOff);  // [4][16]
     TeamSync team{reinterpret_cast<volatile int*>(sm + C::kMiscOff + 8), tid};
     const uint32_t lane_off = static_cast<uint32_t>(32 * quad) << 16;
     const int g = p.group;
+    constexpr int kSpan = 32 / G;  // lanes holding one head's reduction
 
-    float m[N], l[N], o[N];
+    float m[G], l[G], o[G], alpha_prev[G];
 #pragma unroll
-    for (int h = 0; h < N; ++h) {
+    for (int h = 0; h < G; ++h) {
         m[h] = -INFINITY;
         l[h] = 0.f;
         o[h] = 0.f;
+        alpha_prev[h] = 1.f;
     }
     TcItemRec rec{0, 0, 0, 0};
+    int deferred = -1;  // stage whose O-accumulate is still to do
+
+    auto o_accumulate = [&](int cs, const float (&alpha)[G]) -> bool {
+        if (!team.wait(ofull0 + 8 * (cs & 1), static_cast<uint32_t>(cs / 2) & 1, p.d_err, abort_flag))
+            return false;
+        tc::fence_after_sync();
+        float ov[16];
+        tc::tmem_ld16(tmem + 2 * C::kN + (cs & 1) * C::kN + lane_off, ov);
+#pragma unroll
+        for (int h = 0; h < G; ++h) o[h] = o[h] * alpha[h] + ov[h];
+        tc::fence_before_sync();
+        return true;
+    };
+
     for (int c = 0;; ++c) {
         const int st = c % C::kStages;
         if (!team.wait(full0 + 8 * st, static_cast<uint32_t>(c / C::kStages) & 1, p.d_err, abort_flag)) break;
@@ -425,33 +527,33 @@ __device__ __forceinline__ void tc_team(const DecodeParams& p, unsigned char* sm
                 mbar_arrive(qready);
             }
 #pragma unroll
-            for (int h = 0; h < N; ++h) {
+            for (int h = 0; h < G; ++h) {
                 m[h] = -INFINITY;
                 l[h] = 0.f;
                 o[h] = 0.f;
             }
         }
 
-        // ---- S row of this thread's token: mask, stage max per head
-        if (!team.wait(sfull, static_cast<uint32_t>(c) & 1, p.d_err, abort_flag)) break;
+        // ---- softmax of stage c: S row of this thread's token
+        if (!team.wait(sfull0 + 8 * (c & 1), static_cast<uint32_t>(c / 2) & 1, p.d_err, abort_flag)) break;
         tc::fence_after_sync();
-        float x[N];
-        tc::tmem_ld16(tmem + lane_off, x);
+        float sv[16];
+        tc::tmem_ld16(tmem + (c & 1) * C::kN + lane_off, sv);
         const bool valid = row < nvalid && ((groups >> (row >> 4)) & 1u);
+        float x[G];
 #pragma unroll
-        for (int h = 0; h < N; ++h) {
-            x[h] = (valid && h < g) ? x[h] * p.qk_scale_log2 : -INFINITY;
-            float mx = x[h];
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-            if (lane == 0) red_max[quad * N + h] = mx;
+        for (int h = 0; h < G; ++h) x[h] = (valid && h < g) ? sv[h] * p.qk_scale_log2 : -INFINITY;
+        {
+            const float mx = warp_reduce_scatter<G, true>(x, lane);
+            if (lane % kSpan == 0) red[quad * 16 + lane / kSpan] = mx;
         }
         named_barrier(1, 128);
-        float alpha[N];
-        unsigned char* pop = sm + C::kPopOff;
+        float alpha[G];
+        unsigned char* pop = sm + C::kPopOff + (c & 1) * C::kOpBytes;
+        const int col = row & 63;
 #pragma unroll
-        for (int h = 0; h < N; ++h) {
-            const float mt = fmaxf(fmaxf(red_max[h], red_max[N + h]), fmaxf(red_max[2 * N + h], red_max[3 * N + h]));
+        for (int h = 0; h < G; ++h) {
+            const float mt = fmaxf(fmaxf(red[h], red[16 + h]), fmaxf(red[32 + h], red[48 + h]));
             const float m_new = fmaxf(m[h], mt);
             float pr = 0.f;
             alpha[h] = 1.f;
@@ -461,11 +563,10 @@ __device__ __forceinline__ void tc_team(const DecodeParams& p, unsigned char* sm
                 pr = Elem<T>::to_float(Elem<T>::from_float(fast_exp2(x[h] - m_new)));
             }
             l[h] = l[h] * alpha[h] + pr;
-            if (h < g) {  // P[h][row] in the swizzled K-major P operand
-                const int col = row & 63;
+            // P[h][row] in the swizzled K-major P operand (rows >= g stay zero)
+            if (h < g)
                 *reinterpret_cast<T*>(pop + (row >> 6) * 2048 + (h >> 3) * 1024 + (h & 7) * 128 +
                                       ((((col >> 3) ^ (h & 7))) << 4) + (col & 7) * 2) = Elem<T>::from_float(pr);
-            }
         }
         if (!valid) {  // zero this token's V row (both 64-column halves)
             unsigned char* vrow = sm + C::kRingOff + st * C::kStageBytes + C::kTileBytes +
@@ -478,49 +579,49 @@ __device__ __forceinline__ void tc_team(const DecodeParams& p, unsigned char* sm
         }
         tc::fence_async_smem();
         tc::fence_before_sync();
+        named_barrier(1, 128);  // also: every thread has read red before it is rewritten
+        if (tid == 0) mbar_arrive(pfull0 + 8 * (c & 1));
+
+        // ---- O-accumulates: the deferred previous stage, then (at an item end) this one
+        if (deferred >= 0) {
+            if (!o_accumulate(deferred, alpha_prev)) break;
+            deferred = -1;
+        }
+        if (!(flags & kStageLast)) {
+            deferred = c;
+#pragma unroll
+            for (int h = 0; h < G; ++h) alpha_prev[h] = alpha[h];
+            continue;
+        }
+        if (!o_accumulate(c, alpha)) break;
+
+        // ---- output of the item: softmax sums over the 128 token rows
+        {
+            const float ls = warp_reduce_scatter<G, false>(l, lane);
+            if (lane % kSpan == 0) red[quad * 16 + lane / kSpan] = ls;
+        }
         named_barrier(1, 128);
-        if (tid == 0) mbar_arrive(pfull);
-
-        // ---- O^T row of this thread's head dimension: rescale and add
-        if (!team.wait(ofull, static_cast<uint32_t>(c) & 1, p.d_err, abort_flag)) break;
-        tc::fence_after_sync();
-        float ov[N];
-        tc::tmem_ld16(tmem + C::kN + lane_off, ov);
-#pragma unroll
-        for (int h = 0; h < N; ++h) o[h] = o[h] * alpha[h] + ov[h];
-        tc::fence_before_sync();
-
-        if (flags & kStageLast) {
-#pragma unroll
-            for (int h = 0; h < N; ++h) {
-                float lt = l[h];
-#pragma unroll
-                for (int off = 16; off > 0; off >>= 1) lt += __shfl_xor_sync(0xffffffffu, lt, off);
-                if (lane == 0) red_sum[quad * N + h] = lt;
-            }
-            named_barrier(1, 128);
-            for (int h = 0; h < g; ++h) {
-                const float L = red_sum[h] + red_sum[N + h] + red_sum[2 * N + h] + red_sum[3 * N + h];
-                const size_t r = static_cast<size_t>(rec.s) * p.num_q_heads + rec.hq0 + h;
-                if (rec.nparts <= 1) {
-                    static_cast<T*>(p.out)[r * C::D + row] =
-                        Elem<T>::from_float(rec.nparts == 1 && L > 0.f ? o[h] / L : 0.f);
-                } else {
-                    const size_t w = r * p.max_parts + rec.part;
-                    p.ws_o[w * C::D + row] = o[h];
-                    if (row == 0) {
-                        p.ws_m[w] = m[h];
-                        p.ws_l[w] = L;
-                    }
+        for (int h = 0; h < g && h < G; ++h) {
+            const float L = red[h] + red[16 + h] + red[32 + h] + red[48 + h];
+            const size_t rr = static_cast<size_t>(rec.s) * p.num_q_heads + rec.hq0 + h;
+            if (rec.nparts <= 1) {
+                static_cast<T*>(p.out)[rr * C::D + row] =
+                    Elem<T>::from_float(rec.nparts == 1 && L > 0.f ? o[h] / L : 0.f);
+            } else {
+                const size_t w = rr * p.max_parts + rec.part;
+                p.ws_o[w * C::D + row] = o[h];
+                if (row == 0) {
+                    p.ws_m[w] = m[h];
+                    p.ws_l[w] = L;
                 }
             }
-            named_barrier(1, 128);  // red_sum is reused by the next item
         }
+        named_barrier(1, 128);  // red is reused by the next stage
     }
     tc::fence_before_sync();
 }
 
-template <typename T>
+template <typename T, int G>
 __global__ void __launch_bounds__(TcTile<T>::kThreads, 1)
     decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap mapK,
                      const __grid_constant__ CUtensorMap mapV) {
@@ -540,11 +641,11 @@ __global__ void __launch_bounds__(TcTile<T>::kThreads, 1)
         tc::prefetch_tensormap(&mapK);
         tc::prefetch_tensormap(&mapV);
     }
-    // zero the Q and P operands once: padding rows (heads >= g) stay zero
-    for (int i = threadIdx.x; i < 2 * C::kOpBytes / 16; i += blockDim.x)
+    // zero the Q and both P operands once: padding rows (heads >= g) stay zero
+    for (int i = threadIdx.x; i < 3 * C::kOpBytes / 16; i += blockDim.x)
         reinterpret_cast<uint4*>(sm + C::kQopOff)[i] = make_uint4(0, 0, 0, 0);
     tc::fence_async_smem();
-    if (warp == 1) tc::tmem_alloc(smem_addr(tmem_slot), 32);
+    if (warp == 1) tc::tmem_alloc(smem_addr(tmem_slot), 64);  // S[2], O^T[2]: 16 columns each
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
@@ -555,13 +656,13 @@ __global__ void __launch_bounds__(TcTile<T>::kThreads, 1)
     else if (warp == 1)
         tc_mma<T>(p, sm, base, tmem);
     else
-        tc_team<T>(p, sm, base, tmem);
+        tc_team<T, G>(p, sm, base, tmem);
 
     tc::fence_before_sync();
     __syncthreads();
     if (warp == 1) {
         tc::fence_after_sync();
-        tc::tmem_free(tmem, 32);
+        tc::tmem_free(tmem, 64);
     }
     if (threadIdx.x == 0) {
         __threadfence();
@@ -577,9 +678,11 @@ template <typename T>
 inline pa_status launch_decode_tc_typed(const DecodeParams& p, const CUtensorMap& mapK,
                                         const CUtensorMap& mapV, cudaStream_t stream) {
     using C = TcTile<T>;
-    static std::atomic<uint64_t> smem_configured{0};
-    auto kernel = decode_tc_kernel<T>;
-    if (ensure_smem(kernel, C::kSmemBytes, smem_configured) != PA_OK) return PA_ERR_CUDA;
+    static std::atomic<uint64_t> smem_configured[3];
+    const int G = p.group <= 4 ? 4 : p.group <= 8 ? 8 : 16;
+    auto kernel = G == 4 ? decode_tc_kernel<T, 4> : G == 8 ? decode_tc_kernel<T, 8> : decode_tc_kernel<T, 16>;
+    if (ensure_smem(kernel, C::kSmemBytes, smem_configured[G == 4 ? 0 : G == 8 ? 1 : 2]) != PA_OK)
+        return PA_ERR_CUDA;
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
