@@ -19,13 +19,16 @@
 // as [NB*Hkv*B rows x d columns]); the swizzled tiles are the MMA operands as
 // they land.
 //
-// Warp roles (192 threads, persistent, one CTA per SM):
+// Warp roles (320 threads, persistent, one CTA per SM):
 //   warp 0   producer: item cursor over context_lens (as in the SIMT path),
-//            block-table slice, TMA loads into a 3-stage ring (64 KB/stage),
-//            bulk copy of the item's query rows into a staging slot
-//   warp 1   allocates tensor memory, issues the MMAs (one thread)
-//   warps 2-5 the "team": thread = row (token for S, head dimension for O),
-//            reading the accumulator lanes of its warp's quadrant
+//            block-table slice, TMA loads into a 3-stage ring (64 KB/stage;
+//            one [16 x 64] box per lane), bulk copy of the item's query rows
+//            into a staging slot
+//   warp 1   allocates tensor memory, issues the MMAs (one thread); S and
+//            O^T are double-buffered in tensor memory (64 columns)
+//   warps 2-9 two "teams" of four warps, each owning half of the heads:
+//            thread = row (token for S, head dimension for O), reading the
+//            accumulator lanes of its warp's quadrant
 // Rows of invalid tokens (past context_len, or in a block whose id fails the
 // bounds check) get -inf logits and their V rows are zeroed before P.V, so
 // NaN poison cannot reach the products.  P is rounded to the element type
@@ -63,7 +66,7 @@ struct TcTile {
     static constexpr int kNumBars = 2 * kStages + 2 * kQSlots + 8;
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;       // tmem base, abort, team flags
     static constexpr int kSmemBytes = kMiscOff + 32 + 1024;       // + alignment slack
-    static constexpr int kThreads = 192;
+    static constexpr int kThreads = 320;  // producer, MMA, two teams of 4 warps
     static constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
     static_assert(kBf16 || std::is_same<T, __half>::value, "16-bit operands only");
     static constexpr uint32_t kIdescS = tc::instr_desc_f16(kBf16, 128, kN, false, false);
@@ -190,28 +193,33 @@ __device__ __forceinline__ void tc_produce(const DecodeParams& p, const CUtensor
             }
             const int t0 = tok_begin + i * C::kStageTok;
             const int t1 = min(t0 + C::kStageTok, tok_end);
-            int rows[8];
-            uint32_t groups = 0;
-#pragma unroll
-            for (int r = 0; r < 8; ++r) {
-                const int t = t0 + 16 * r;
-                rows[r] = 0;
-                if (t < t1) {  // warp-uniform
-                    const int lb = t / B;
-                    const int off = t - lb * B;
-                    while (lb - win >= 32) {
-                        win += 32;
-                        entry = (win + lane < blk_end) ? __ldg(trow + win + lane) : -1;
-                    }
-                    const int pb = __shfl_sync(0xffffffffu, entry, lb - win);
+            // One TMA box per lane: lane = 4*group + 2*half + (0: K, 1: V).
+            if (t1 > t0 && (t1 - 1) / B - win >= 32) {  // window must hold the stage's blocks
+                win = t0 / B;
+                entry = (win + lane < blk_end) ? __ldg(trow + win + lane) : -1;
+            }
+            const int r = lane >> 2;
+            const int t = t0 + 16 * r;
+            int row = 0;
+            bool mine = false, bad = false;
+            {
+                const int lb = t < t1 ? t / B : win;
+                const int pb = __shfl_sync(0xffffffffu, entry, lb - win);
+                if (t < t1) {
                     if (static_cast<unsigned>(pb) < static_cast<unsigned>(p.num_blocks)) {
-                        rows[r] = (pb * p.num_kv_heads + hk) * B + off;
-                        groups |= 1u << r;
+                        row = (pb * p.num_kv_heads + hk) * B + (t - lb * B);
+                        mine = true;
                     } else {
-                        oob = true;
+                        bad = true;
                     }
                 }
             }
+            const unsigned loaded = __ballot_sync(0xffffffffu, mine && (lane & 3) == 0);
+            if (__any_sync(0xffffffffu, bad)) oob = true;
+            uint32_t groups = 0;
+#pragma unroll
+            for (int g8 = 0; g8 < 8; ++g8) groups |= ((loaded >> (4 * g8)) & 1u) << g8;
+            const uint32_t full = full0 + 8 * st;
             if (lane == 0) {
                 uint32_t flags = 0;
                 if (i == 0) flags |= kStageFirst;
@@ -220,20 +228,14 @@ __device__ __forceinline__ void tc_produce(const DecodeParams& p, const CUtensor
                 meta[st].nvalid = max(0, t1 - t0);
                 meta[st].groups = groups;
                 meta[st].flags = flags;
-                const uint32_t full = full0 + 8 * st;
                 mbar_arrive_expect_tx(full, static_cast<uint32_t>(__popc(groups)) * 4u * 2048u);
-                const uint32_t sK = base + C::kRingOff + st * C::kStageBytes;
-                const uint32_t sV = sK + C::kTileBytes;
-#pragma unroll
-                for (int r = 0; r < 8; ++r) {
-                    if (groups & (1u << r)) {
-#pragma unroll
-                        for (int h = 0; h < 2; ++h) {
-                            tc::tma_load_2d(sK + h * C::kHalfBytes + r * 2048, mapK, 64 * h, rows[r], full, policy);
-                            tc::tma_load_2d(sV + h * C::kHalfBytes + r * 2048, mapV, 64 * h, rows[r], full, policy);
-                        }
-                    }
-                }
+            }
+            __syncwarp();
+            if (mine) {
+                const int h = (lane >> 1) & 1;
+                const uint32_t dst = base + C::kRingOff + st * C::kStageBytes + (lane & 1) * C::kTileBytes +
+                                     h * C::kHalfBytes + r * 2048;
+                tc::tma_load_2d(dst, (lane & 1) ? mapV : mapK, 64 * h, row, full, policy);
             }
             __syncwarp();
         }
@@ -394,13 +396,15 @@ __device__ __forceinline__ void tc_mma(const DecodeParams& p, unsigned char* sm,
     __syncwarp();
 }
 
-// The four team warps agree on every wait: thread 0 waits (bounded), the
-// outcome goes through one of two alternating shared flags and a named
-// barrier, so no team thread can stay behind at a later barrier.
+// The four warps of a team agree on every wait: thread 0 waits (bounded),
+// the outcome goes through one of two alternating shared flags and the team's
+// named barrier, so no team thread can stay behind at a later barrier.
 struct TeamSync {
     volatile int* flags;  // [2]
     int tid;
+    int barrier_id;
     int k = 0;
+    __device__ __forceinline__ void sync() const { named_barrier(barrier_id, 128); }
     __device__ __forceinline__ bool wait(uint32_t bar, uint32_t parity, uint32_t* d_err,
                                          volatile int* abort_flag) {
         const int slot = k++ & 1;
@@ -412,25 +416,25 @@ struct TeamSync {
             }
             flags[slot] = ok ? 1 : 0;
         }
-        named_barrier(1, 128);
+        sync();
         return flags[slot] != 0;
     }
 };
 
-// Max (or sum) over the 32 lanes of G per-lane values by a reduce-scatter:
-// afterwards lane l holds the result for value index l / (32 / G).
-template <int G, bool kMax>
-__device__ __forceinline__ float warp_reduce_scatter(float (&v)[G], int lane) {
-    float x[G];
+// Max (or sum) over the 32 lanes of N per-lane values by a reduce-scatter:
+// afterwards lane l holds the result for value index l / (32 / N).
+template <int N, bool kMax>
+__device__ __forceinline__ float warp_reduce_scatter(const float (&v)[N], int lane) {
+    float x[N];
 #pragma unroll
-    for (int i = 0; i < G; ++i) x[i] = v[i];
-    int n = G;
+    for (int i = 0; i < N; ++i) x[i] = v[i];
+    int n = N;
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) {
         if (n > 1) {
             const bool up = (lane & off) != 0;
 #pragma unroll
-            for (int i = 0; i < G / 2; ++i) {
+            for (int i = 0; i < N / 2; ++i) {
                 if (i < n / 2) {
                     const float keep = up ? x[i + n / 2] : x[i];
                     const float send = up ? x[i] : x[i + n / 2];
@@ -447,18 +451,25 @@ __device__ __forceinline__ float warp_reduce_scatter(float (&v)[G], int lane) {
     return x[0];
 }
 
-// Team: softmax of stage c (thread = token row of S), then the deferred
-// O-accumulate of stage c-1 of the same item (thread = head dimension of O^T);
-// at an item's last stage its own O-accumulate and the output.
+// A team (4 warps, one per accumulator lane quadrant) owns heads
+// [h0, h0 + H) of the G padded query heads.  Per stage: softmax of stage c
+// (thread = token row of S), then the deferred O-accumulate of stage c-1 of
+// the same item (thread = head dimension of O^T); at an item's last stage its
+// own O-accumulate and the output rows of the team's heads.  Team 0 also
+// zeroes the V rows of invalid tokens.  Each team signals p_full, q_ready and
+// qempty once (those barriers count two arrivals).
 template <typename T, int G>
-__device__ __forceinline__ void tc_team(const DecodeParams& p, unsigned char* sm, uint32_t base,
-                                        uint32_t tmem) {
+__device__ __forceinline__ void tc_team(const DecodeParams& p, unsigned char* sm, uint32_t tmem,
+                                        int team_id) {
     using C = TcTile<T>;
     using Bi = TcBars<T>;
+    constexpr int H = G / 2;         // heads of this team
+    constexpr int kSpan = 32 / H;    // lanes holding one head's reduction
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int tid = threadIdx.x - 64;  // 0..127
-    const int quad = warp & 3;         // accumulator lanes 32*quad .. +31
-    const int row = 32 * quad + lane;  // token of S, head dimension of O
+    const int tid = threadIdx.x - 64 - 128 * team_id;  // 0..127 within the team
+    const int quad = warp & 3;                          // accumulator lanes 32*quad .. +31
+    const int row = 32 * quad + lane;                   // token of S, head dimension of O
+    const int h0 = team_id * H;
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::kBarOff);
     const uint32_t full0 = smem_addr(bars);
     const uint32_t qfull0 = smem_addr(bars + 2 * C::kStages);
@@ -469,15 +480,15 @@ __device__ __forceinline__ void tc_team(const DecodeParams& p, unsigned char* sm
     const TcStageMeta* meta = reinterpret_cast<const TcStageMeta*>(sm + C::kMetaOff);
     const TcItemRec* recs = reinterpret_cast<const TcItemRec*>(sm + C::kRecOff);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + C::kMiscOff + 4);
-    float* red = reinterpret_cast<float*>(sm + C::kRedOff);  // [4][16]
-    TeamSync team{reinterpret_cast<volatile int*>(sm + C::kMiscOff + 8), tid};
+    float* red = reinterpret_cast<float*>(sm + C::kRedOff);  // [4][16]: [quadrant][head]
+    TeamSync team{reinterpret_cast<volatile int*>(sm + C::kMiscOff + 8 + 8 * team_id), tid,
+                  1 + team_id};
     const uint32_t lane_off = static_cast<uint32_t>(32 * quad) << 16;
     const int g = p.group;
-    constexpr int kSpan = 32 / G;  // lanes holding one head's reduction
 
-    float m[G], l[G], o[G], alpha_prev[G];
+    float m[H], l[H], o[H], alpha_prev[H];
 #pragma unroll
-    for (int h = 0; h < G; ++h) {
+    for (int h = 0; h < H; ++h) {
         m[h] = -INFINITY;
         l[h] = 0.f;
         o[h] = 0.f;
@@ -486,14 +497,14 @@ __device__ __forceinline__ void tc_team(const DecodeParams& p, unsigned char* sm
     TcItemRec rec{0, 0, 0, 0};
     int deferred = -1;  // stage whose O-accumulate is still to do
 
-    auto o_accumulate = [&](int cs, const float (&alpha)[G]) -> bool {
+    auto o_accumulate = [&](int cs, const float (&alpha)[H]) -> bool {
         if (!team.wait(ofull0 + 8 * (cs & 1), static_cast<uint32_t>(cs / 2) & 1, p.d_err, abort_flag))
             return false;
         tc::fence_after_sync();
-        float ov[16];
-        tc::tmem_ld16(tmem + 2 * C::kN + (cs & 1) * C::kN + lane_off, ov);
+        float ov[H];
+        tc::tmem_ld<H>(tmem + 2 * C::kN + (cs & 1) * C::kN + h0 + lane_off, ov);
 #pragma unroll
-        for (int h = 0; h < G; ++h) o[h] = o[h] * alpha[h] + ov[h];
+        for (int h = 0; h < H; ++h) o[h] = o[h] * alpha[h] + ov[h];
         tc::fence_before_sync();
         return true;
     };
@@ -512,48 +523,50 @@ __device__ __forceinline__ void tc_team(const DecodeParams& p, unsigned char* sm
             if (!team.wait(qfull0 + 8 * qs, static_cast<uint32_t>(item_seq / C::kQSlots) & 1, p.d_err, abort_flag))
                 break;
             rec = recs[qs];  // the slot is reused once qempty is released below
-            // query rows -> the swizzled K-major Q operand (rows >= g stay zero)
+            // query rows of this team's heads -> the swizzled K-major Q operand
             const unsigned char* src = sm + C::kQsOff + qs * C::kQBytes;
-            for (int idx = tid; idx < g * 16; idx += 128) {
-                const int h = idx >> 4, ch = idx & 15;
-                const uint4 v = *reinterpret_cast<const uint4*>(src + (h * C::D + ch * 8) * 2);
-                *reinterpret_cast<uint4*>(sm + C::kQopOff + (ch >> 3) * 2048 + (h >> 3) * 1024 +
-                                          (h & 7) * 128 + (((ch & 7) ^ (h & 7)) << 4)) = v;
+            for (int idx = tid; idx < H * 16; idx += 128) {
+                const int h = h0 + (idx >> 4), ch = idx & 15;
+                if (h < g) {
+                    const uint4 v = *reinterpret_cast<const uint4*>(src + (h * C::D + ch * 8) * 2);
+                    *reinterpret_cast<uint4*>(sm + C::kQopOff + (ch >> 3) * 2048 + (h >> 3) * 1024 +
+                                              (h & 7) * 128 + (((ch & 7) ^ (h & 7)) << 4)) = v;
+                }
             }
             tc::fence_async_smem();
-            named_barrier(1, 128);
+            team.sync();
             if (tid == 0) {
                 mbar_arrive(qempty0 + 8 * qs);
                 mbar_arrive(qready);
             }
 #pragma unroll
-            for (int h = 0; h < G; ++h) {
+            for (int h = 0; h < H; ++h) {
                 m[h] = -INFINITY;
                 l[h] = 0.f;
                 o[h] = 0.f;
             }
         }
 
-        // ---- softmax of stage c: S row of this thread's token
+        // ---- softmax of stage c: S row of this thread's token, this team's heads
         if (!team.wait(sfull0 + 8 * (c & 1), static_cast<uint32_t>(c / 2) & 1, p.d_err, abort_flag)) break;
         tc::fence_after_sync();
-        float sv[16];
-        tc::tmem_ld16(tmem + (c & 1) * C::kN + lane_off, sv);
+        float x[H];
+        tc::tmem_ld<H>(tmem + (c & 1) * C::kN + h0 + lane_off, x);
         const bool valid = row < nvalid && ((groups >> (row >> 4)) & 1u);
-        float x[G];
 #pragma unroll
-        for (int h = 0; h < G; ++h) x[h] = (valid && h < g) ? sv[h] * p.qk_scale_log2 : -INFINITY;
+        for (int h = 0; h < H; ++h) x[h] = (valid && h0 + h < g) ? x[h] * p.qk_scale_log2 : -INFINITY;
         {
-            const float mx = warp_reduce_scatter<G, true>(x, lane);
-            if (lane % kSpan == 0) red[quad * 16 + lane / kSpan] = mx;
+            const float mx = warp_reduce_scatter<H, true>(x, lane);
+            if (lane % kSpan == 0) red[quad * 16 + h0 + lane / kSpan] = mx;
         }
-        named_barrier(1, 128);
-        float alpha[G];
+        team.sync();
+        float alpha[H];
         unsigned char* pop = sm + C::kPopOff + (c & 1) * C::kOpBytes;
         const int col = row & 63;
 #pragma unroll
-        for (int h = 0; h < G; ++h) {
-            const float mt = fmaxf(fmaxf(red[h], red[16 + h]), fmaxf(red[32 + h], red[48 + h]));
+        for (int h = 0; h < H; ++h) {
+            const int hh = h0 + h;
+            const float mt = fmaxf(fmaxf(red[hh], red[16 + hh]), fmaxf(red[32 + hh], red[48 + hh]));
             const float m_new = fmaxf(m[h], mt);
             float pr = 0.f;
             alpha[h] = 1.f;
@@ -563,12 +576,12 @@ __device__ __forceinline__ void tc_team(const DecodeParams& p, unsigned char* sm
                 pr = Elem<T>::to_float(Elem<T>::from_float(fast_exp2(x[h] - m_new)));
             }
             l[h] = l[h] * alpha[h] + pr;
-            // P[h][row] in the swizzled K-major P operand (rows >= g stay zero)
-            if (h < g)
-                *reinterpret_cast<T*>(pop + (row >> 6) * 2048 + (h >> 3) * 1024 + (h & 7) * 128 +
-                                      ((((col >> 3) ^ (h & 7))) << 4) + (col & 7) * 2) = Elem<T>::from_float(pr);
+            // P[hh][row] in the swizzled K-major P operand (rows >= g stay zero)
+            if (hh < g)
+                *reinterpret_cast<T*>(pop + (row >> 6) * 2048 + (hh >> 3) * 1024 + (hh & 7) * 128 +
+                                      ((((col >> 3) ^ (hh & 7))) << 4) + (col & 7) * 2) = Elem<T>::from_float(pr);
         }
-        if (!valid) {  // zero this token's V row (both 64-column halves)
+        if (!valid && team_id == 0) {  // zero this token's V row (both 64-column halves)
             unsigned char* vrow = sm + C::kRingOff + st * C::kStageBytes + C::kTileBytes +
                                   (row >> 3) * 1024 + (row & 7) * 128;
 #pragma unroll
@@ -579,7 +592,7 @@ __device__ __forceinline__ void tc_team(const DecodeParams& p, unsigned char* sm
         }
         tc::fence_async_smem();
         tc::fence_before_sync();
-        named_barrier(1, 128);  // also: every thread has read red before it is rewritten
+        team.sync();  // also: the team has read its red entries before they are rewritten
         if (tid == 0) mbar_arrive(pfull0 + 8 * (c & 1));
 
         // ---- O-accumulates: the deferred previous stage, then (at an item end) this one
@@ -590,20 +603,23 @@ __device__ __forceinline__ void tc_team(const DecodeParams& p, unsigned char* sm
         if (!(flags & kStageLast)) {
             deferred = c;
 #pragma unroll
-            for (int h = 0; h < G; ++h) alpha_prev[h] = alpha[h];
+            for (int h = 0; h < H; ++h) alpha_prev[h] = alpha[h];
             continue;
         }
         if (!o_accumulate(c, alpha)) break;
 
-        // ---- output of the item: softmax sums over the 128 token rows
+        // ---- output rows of the team's heads: softmax sums over the 128 token rows
         {
-            const float ls = warp_reduce_scatter<G, false>(l, lane);
-            if (lane % kSpan == 0) red[quad * 16 + lane / kSpan] = ls;
+            const float ls = warp_reduce_scatter<H, false>(l, lane);
+            if (lane % kSpan == 0) red[quad * 16 + h0 + lane / kSpan] = ls;
         }
-        named_barrier(1, 128);
-        for (int h = 0; h < g && h < G; ++h) {
-            const float L = red[h] + red[16 + h] + red[32 + h] + red[48 + h];
-            const size_t rr = static_cast<size_t>(rec.s) * p.num_q_heads + rec.hq0 + h;
+        team.sync();
+#pragma unroll
+        for (int h = 0; h < H; ++h) {
+            const int hh = h0 + h;
+            if (hh >= g) break;
+            const float L = red[hh] + red[16 + hh] + red[32 + hh] + red[48 + hh];
+            const size_t rr = static_cast<size_t>(rec.s) * p.num_q_heads + rec.hq0 + hh;
             if (rec.nparts <= 1) {
                 static_cast<T*>(p.out)[rr * C::D + row] =
                     Elem<T>::from_float(rec.nparts == 1 && L > 0.f ? o[h] / L : 0.f);
@@ -616,7 +632,7 @@ __device__ __forceinline__ void tc_team(const DecodeParams& p, unsigned char* sm
                 }
             }
         }
-        named_barrier(1, 128);  // red is reused by the next stage
+        team.sync();  // red is reused by the next stage
     }
     tc::fence_before_sync();
 }
@@ -635,7 +651,12 @@ __global__ void __launch_bounds__(TcTile<T>::kThreads, 1)
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + C::kMiscOff);
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < C::kNumBars; ++i) mbar_init(smem_addr(bars + i), 1);
+        for (int i = 0; i < C::kNumBars; ++i) {
+            // qempty, q_ready and p_full are signalled once by each of the two teams
+            const bool two = (i >= 2 * C::kStages + C::kQSlots && i <= TcBars<T>::kQReady) ||
+                             i == TcBars<T>::kPFull || i == TcBars<T>::kPFull + 1;
+            mbar_init(smem_addr(bars + i), two ? 2 : 1);
+        }
         *reinterpret_cast<volatile int*>(sm + C::kMiscOff + 4) = 0;
         fence_barrier_init();
         tc::prefetch_tensormap(&mapK);
@@ -656,7 +677,7 @@ __global__ void __launch_bounds__(TcTile<T>::kThreads, 1)
     else if (warp == 1)
         tc_mma<T>(p, sm, base, tmem);
     else
-        tc_team<T, G>(p, sm, base, tmem);
+        tc_team<T, G>(p, sm, tmem, (warp - 2) >> 2);
 
     tc::fence_before_sync();
     __syncthreads();
