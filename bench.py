@@ -241,7 +241,8 @@ def run_gpu(args):
 
     w = wl.by_name(args.config, poison=False, **({"partition_tokens": args.partition}
                                                    if args.partition is not None else {}))
-    P = pa.decode_partition_tokens(w.max_blocks_per_seq, w.block_size, w.partition_tokens)
+    P = pa.decode_partition_tokens(w.num_q_heads, w.num_kv_heads, w.head_dim, w.max_blocks_per_seq,
+                                   w.block_size, w.dtype, w.partition_tokens)
     dt = w.dtype
     d = {k: v.to(dev) for k, v in {
         "q": _to_torch(w.q, dt), "k_cache": _to_torch(w.k_cache, dt),

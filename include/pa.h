@@ -118,16 +118,22 @@ pa_status pa_copy_blocks_check(const int32_t* block_mapping, int num_pairs, uint
                                pa_stream_t stream);
 
 /* pa_decode_partition_tokens -- tokens per split-K partition that pa_decode
- * uses for these sizes: partition_tokens itself when it is positive, else the
- * library's choice (a multiple of block_size).  Returns -1 for invalid sizes. */
-int pa_decode_partition_tokens(int max_blocks_per_seq, int block_size, int partition_tokens);
+ * uses for these sizes: partition_tokens itself when it is positive (it must
+ * be a multiple of block_size), else the library's choice, a multiple of
+ * block_size: 512 tokens, or 2048 when the query heads are grouped (4 to 16
+ * per kv head) over 16-bit K/V with head_dim 128, the shapes decoded on the
+ * tensor cores.  Returns -1 for invalid sizes. */
+int pa_decode_partition_tokens(int num_q_heads, int num_kv_heads, int head_dim,
+                               int max_blocks_per_seq, int block_size, pa_dtype dtype,
+                               int partition_tokens);
 
 /* pa_decode_workspace_size -- bytes of device workspace pa_decode needs for
  * these sizes: 256 bytes of work-scheduling counters, plus the partial
  * softmax states of split sequences (num_seqs * num_q_heads * partitions *
  * (head_dim + 2) floats) when a sequence can span more than one partition. */
-size_t pa_decode_workspace_size(int num_seqs, int num_q_heads, int head_dim, int max_blocks_per_seq,
-                                int block_size, int partition_tokens);
+size_t pa_decode_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                                int max_blocks_per_seq, int block_size, pa_dtype dtype,
+                                int partition_tokens);
 
 /* pa_decode -- paged decode attention.
  *
@@ -139,7 +145,10 @@ size_t pa_decode_workspace_size(int num_seqs, int num_q_heads, int head_dim, int
  * The kernel walks the block table block by block and the tokens of each
  * block in order, staging each block's K and V in shared memory and taking
  * the dot products with q there ("PagedAttention" (compassingai.com) §8;
- * "PagedAttention 深度解析" §二 item 3).  Long sequences are split into
+ * "PagedAttention 深度解析" §二 item 3).  When 4 to 16 query heads share a kv
+ * head (16-bit K/V, head_dim 128, partitions a multiple of 128 tokens), q.K^T
+ * and P.V of a 128-token stage are dense tiles computed on the tensor cores
+ * (tcgen05) from tiles fetched by TMA tensor copies.  Long sequences are split into
  * partitions of pa_decode_partition_tokens() tokens whose partial softmax
  * states are merged by a second kernel (log-sum-exp).
  * workspace: device memory of at least pa_decode_workspace_size() bytes,

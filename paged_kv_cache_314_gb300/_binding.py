@@ -68,9 +68,9 @@ def load() -> ctypes.CDLL:
         lib.pa_copy_blocks_check.restype = i32
         lib.pa_copy_blocks_check.argtypes = [vp, i32, vp, vp]
         lib.pa_decode_partition_tokens.restype = i32
-        lib.pa_decode_partition_tokens.argtypes = [i32, i32, i32]
+        lib.pa_decode_partition_tokens.argtypes = [i32, i32, i32, i32, i32, i32, i32]
         lib.pa_decode_workspace_size.restype = u64
-        lib.pa_decode_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32]
+        lib.pa_decode_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32, i32, i32]
         lib.pa_decode.restype = i32
         lib.pa_decode.argtypes = [vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, i32,
                                   ctypes.c_float, i32, i32, vp, u64, vp, vp]
@@ -151,15 +151,28 @@ def copy_blocks_check(block_mapping: torch.Tensor, d_err: torch.Tensor, stream=N
     _check(st, "pa_copy_blocks_check")
 
 
-def decode_partition_tokens(max_blocks_per_seq: int, block_size: int,
+DTYPE_NAME_CODE = {"f32": 0, "f16": 1, "bf16": 2}
+
+
+def _dtype_code(dtype) -> int:
+    return DTYPE_NAME_CODE[dtype] if isinstance(dtype, str) else DTYPE_CODE[dtype]
+
+
+def decode_partition_tokens(num_q_heads: int, num_kv_heads: int, head_dim: int,
+                            max_blocks_per_seq: int, block_size: int, dtype,
                             partition_tokens: int = 0) -> int:
-    return int(load().pa_decode_partition_tokens(max_blocks_per_seq, block_size, partition_tokens))
+    """Tokens per split-K partition pa_decode uses (dtype: torch dtype or 'f16' ...)."""
+    return int(load().pa_decode_partition_tokens(num_q_heads, num_kv_heads, head_dim,
+                                                 max_blocks_per_seq, block_size,
+                                                 _dtype_code(dtype), partition_tokens))
 
 
-def decode_workspace_size(num_seqs: int, num_q_heads: int, head_dim: int, max_blocks_per_seq: int,
-                          block_size: int, partition_tokens: int = 0) -> int:
-    return int(load().pa_decode_workspace_size(num_seqs, num_q_heads, head_dim,
-                                               max_blocks_per_seq, block_size, partition_tokens))
+def decode_workspace_size(num_seqs: int, num_q_heads: int, num_kv_heads: int, head_dim: int,
+                          max_blocks_per_seq: int, block_size: int, dtype,
+                          partition_tokens: int = 0) -> int:
+    return int(load().pa_decode_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim,
+                                               max_blocks_per_seq, block_size,
+                                               _dtype_code(dtype), partition_tokens))
 
 
 def decode_workspace(q: torch.Tensor, k_cache: torch.Tensor, block_tables: torch.Tensor,
@@ -167,7 +180,8 @@ def decode_workspace(q: torch.Tensor, k_cache: torch.Tensor, block_tables: torch
     """Allocate (with torch) the zero-filled workspace pa_decode needs for these
     shapes; it can be reused by later calls with the same or smaller shapes."""
     S, Hq, d = q.shape
-    n = decode_workspace_size(S, Hq, d, block_tables.shape[1], k_cache.shape[2], partition_tokens)
+    n = decode_workspace_size(S, Hq, k_cache.shape[1], d, block_tables.shape[1],
+                              k_cache.shape[2], q.dtype, partition_tokens)
     return torch.zeros(n, dtype=torch.uint8, device=q.device)
 
 

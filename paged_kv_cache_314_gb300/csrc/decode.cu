@@ -11,7 +11,18 @@
 namespace pa {
 namespace {
 
+// Default split-K partitions: 512 tokens for the SIMT path (one query head per
+// kv head or few), 2048 for the grouped-query tensor-core path, whose per-item
+// start-up (query rows, first MMA) costs more and whose items are 16 stages.
 constexpr int kDefaultPartitionTokens = 512;
+constexpr int kDefaultPartitionTokensTc = 2048;
+
+// Grouped-query heads with 16-bit K/V and head_dim 128 run on the tensor cores.
+bool tc_shape(int num_q_heads, int num_kv_heads, int head_dim, pa_dtype dtype) {
+    if (num_kv_heads <= 0 || num_q_heads % num_kv_heads != 0) return false;
+    const int g = num_q_heads / num_kv_heads;
+    return (dtype == PA_F16 || dtype == PA_BF16) && head_dim == 128 && g >= 4 && g <= 16;
+}
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -82,20 +93,23 @@ bool make_pool_map(CUtensorMap* map, const void* pool, long long rows, pa_dtype 
 }  // namespace
 }  // namespace pa
 
-extern "C" int pa_decode_partition_tokens(int max_blocks_per_seq, int block_size,
+extern "C" int pa_decode_partition_tokens(int num_q_heads, int num_kv_heads, int head_dim,
+                                          int max_blocks_per_seq, int block_size, pa_dtype dtype,
                                           int partition_tokens) {
     using namespace pa;
     if (max_blocks_per_seq <= 0 || !block_size_ok(block_size) || partition_tokens < 0) return -1;
     if (partition_tokens > 0) return partition_tokens % block_size == 0 ? partition_tokens : -1;
-    const int P = kDefaultPartitionTokens;
+    const int P = tc_shape(num_q_heads, num_kv_heads, head_dim, dtype) ? kDefaultPartitionTokensTc
+                                                                        : kDefaultPartitionTokens;
     return (P + block_size - 1) / block_size * block_size;
 }
 
-extern "C" size_t pa_decode_workspace_size(int num_seqs, int num_q_heads, int head_dim,
-                                           int max_blocks_per_seq, int block_size,
-                                           int partition_tokens) {
+extern "C" size_t pa_decode_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads,
+                                           int head_dim, int max_blocks_per_seq, int block_size,
+                                           pa_dtype dtype, int partition_tokens) {
     using namespace pa;
-    const int P = pa_decode_partition_tokens(max_blocks_per_seq, block_size, partition_tokens);
+    const int P = pa_decode_partition_tokens(num_q_heads, num_kv_heads, head_dim,
+                                             max_blocks_per_seq, block_size, dtype, partition_tokens);
     if (P <= 0 || num_seqs < 0 || num_q_heads <= 0 || head_dim <= 0) return 0;
     return ws_layout(num_seqs, num_q_heads, head_dim, max_parts_for(max_blocks_per_seq, block_size, P))
         .bytes;
@@ -117,7 +131,8 @@ extern "C" pa_status pa_decode(void* out, const void* q, const void* k_cache, co
     if (!block_size_ok(block_size)) return PA_ERR_UNSUPPORTED;
     if (static_cast<long long>(max_blocks_per_seq) * block_size > 0x7fffffffLL)
         return PA_ERR_INVALID_ARG;
-    const int P = pa_decode_partition_tokens(max_blocks_per_seq, block_size, partition_tokens);
+    const int P = pa_decode_partition_tokens(num_q_heads, num_kv_heads, head_dim,
+                                             max_blocks_per_seq, block_size, dtype, partition_tokens);
     if (P <= 0) return PA_ERR_INVALID_ARG;
     if (num_seqs == 0) return PA_OK;
     if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens)
@@ -161,8 +176,8 @@ extern "C" pa_status pa_decode(void* out, const void* q, const void* k_cache, co
     const cudaStream_t st = as_cuda(stream);
     // Grouped-query heads with 16-bit K/V and head_dim 128: the tensor-core path.
     const long long pool_rows = static_cast<long long>(num_blocks) * num_kv_heads * block_size;
-    if ((dtype == PA_F16 || dtype == PA_BF16) && head_dim == 128 && group >= 4 && group <= 16 &&
-        P % 128 == 0 && pool_rows < 0x7fffffffLL) {
+    if (tc_shape(num_q_heads, num_kv_heads, head_dim, dtype) && P % 128 == 0 &&
+        pool_rows < 0x7fffffffLL) {
         CUtensorMap map_k, map_v;
         if (make_pool_map(&map_k, k_cache, pool_rows, dtype) &&
             make_pool_map(&map_v, v_cache, pool_rows, dtype)) {

@@ -347,7 +347,7 @@ __device__ __forceinline__ void decode_produce(const DecodeParams& p, unsigned c
         // ---- item slot: wait until its previous item has been merged
         const int islot = item_seq % C::kItems;
         if (item_seq >= C::kItems &&
-            !mbar_wait_warp(ifree0 + 8 * islot, static_cast<uint32_t>(item_seq / C::kItems - 1) & 1)) {
+            !mbar_wait_lane0(ifree0 + 8 * islot, static_cast<uint32_t>(item_seq / C::kItems - 1) & 1)) {
             if (lane == 0) report(p.d_err, PA_DERR_TIMEOUT);
             *abort_flag = 1;
             break;
@@ -379,7 +379,7 @@ __device__ __forceinline__ void decode_produce(const DecodeParams& p, unsigned c
             const int cc = c + i;
             const int st = cc % C::kStages;
             if (cc >= C::kStages &&
-                !mbar_wait_warp(empty0 + 8 * st, static_cast<uint32_t>(cc / C::kStages - 1) & 1)) {
+                !mbar_wait_lane0(empty0 + 8 * st, static_cast<uint32_t>(cc / C::kStages - 1) & 1)) {
                 if (lane == 0) report(p.d_err, PA_DERR_TIMEOUT);
                 *abort_flag = 1;
                 aborted = true;
@@ -452,7 +452,7 @@ __device__ __forceinline__ void decode_produce(const DecodeParams& p, unsigned c
             const int cc = c_end + i;
             const int st = cc % C::kStages;
             if (cc >= C::kStages &&
-                !mbar_wait_warp(empty0 + 8 * st, static_cast<uint32_t>(cc / C::kStages - 1) & 1)) {
+                !mbar_wait_lane0(empty0 + 8 * st, static_cast<uint32_t>(cc / C::kStages - 1) & 1)) {
                 if (lane == 0) report(p.d_err, PA_DERR_TIMEOUT);
                 *abort_flag = 1;
                 break;

@@ -54,10 +54,12 @@ extern "C" pa_status pa_decode_static_workspace(
     if (dtype != PA_F32 && dtype != PA_F16 && dtype != PA_BF16) return PA_ERR_INVALID_ARG;
     if (head_dim != 64 && head_dim != 128) return PA_ERR_UNSUPPORTED;
     if (block_size % 16 != 0 || block_size > 256) return PA_ERR_UNSUPPORTED;
-    if (pa_decode_partition_tokens(max_blocks_per_seq, block_size, partition_tokens) <= 0)
+    if (pa_decode_partition_tokens(num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq,
+                                   block_size, dtype, partition_tokens) <= 0)
         return PA_ERR_INVALID_ARG;
-    const size_t need = pa_decode_workspace_size(num_seqs, num_q_heads, head_dim,
-                                                 max_blocks_per_seq, block_size, partition_tokens);
+    const size_t need = pa_decode_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim,
+                                                 max_blocks_per_seq, block_size, dtype,
+                                                 partition_tokens);
     if (need > kStaticScratchBytes) return PA_ERR_WORKSPACE_TOO_SMALL;
     if (num_seqs == 0) return PA_OK;
     const void* ptrs[] = {out, q, k_cache, v_cache, block_tables, context_lens};

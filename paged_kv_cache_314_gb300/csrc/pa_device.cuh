@@ -84,6 +84,18 @@ __device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity) {
     return __all_sync(0xffffffffu, ok);
 }
 
+// Bounded wait decided by lane 0 alone: lane 0 waits, the outcome is
+// broadcast and the warp synchronises, so the lanes cannot disagree.  For
+// warps whose other lanes only need to be ordered after the wait (producers,
+// the MMA issuer), not to read data the barrier guards on their own.
+__device__ __forceinline__ bool mbar_wait_lane0(uint32_t bar, uint32_t parity) {
+    int ok = 0;
+    if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity) ? 1 : 0;
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    __syncwarp();
+    return ok != 0;
+}
+
 // ---- bulk copies (TMA, non-tensor) ------------------------------------------
 
 // L2 policy for data read exactly once per step: evict it first.

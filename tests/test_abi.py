@@ -39,12 +39,14 @@ def test_every_declared_symbol_is_exported(lib):
 def test_host_only_entry_points(lib):
     assert pa.abi_version() == 1
     assert lib.pa_status_string(0) == b"ok"
-    assert pa.decode_partition_tokens(128, 16, 0) % 16 == 0
-    assert pa.decode_partition_tokens(128, 16, 24) == -1  # not a multiple of the block size
-    assert pa.decode_partition_tokens(128, 24, 0) == -1   # block size not a multiple of 16
+    assert pa.decode_partition_tokens(32, 32, 128, 128, 16, "f16") == 512
+    assert pa.decode_partition_tokens(64, 8, 128, 128, 16, "bf16") == 2048  # tensor-core shapes
+    assert pa.decode_partition_tokens(64, 8, 128, 128, 16, "f32") == 512
+    assert pa.decode_partition_tokens(32, 32, 128, 128, 16, "f16", 24) == -1  # not a multiple of B
+    assert pa.decode_partition_tokens(32, 32, 128, 128, 24, "f16") == -1      # B not a multiple of 16
     # one partition: only the 256 bytes of work counters
-    assert pa.decode_workspace_size(4, 8, 128, 4, 16, 64) == 256
-    n = pa.decode_workspace_size(64, 32, 128, 128, 16, 256)
+    assert pa.decode_workspace_size(4, 8, 8, 128, 4, 16, "f16", 64) == 256
+    n = pa.decode_workspace_size(64, 32, 32, 128, 128, 16, "f16", 256)
     rows = 64 * 32 * 8
     assert n >= 256 + rows * (128 + 2) * 4
 

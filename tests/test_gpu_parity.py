@@ -240,7 +240,7 @@ def test_host_checked_errors():
                   block_size=16, seed=26)
     d = upload(w)
     out = torch.empty_like(d["q"])
-    need = pa.decode_workspace_size(1, 2, 128, w.max_blocks_per_seq, 16, 16)
+    need = pa.decode_workspace_size(1, 2, 2, 128, w.max_blocks_per_seq, 16, "f16", 16)
     assert need > 0
     small = torch.empty(need - 256, dtype=torch.uint8, device="cuda")
     with pytest.raises(pa.PaError) as e:

@@ -60,8 +60,8 @@ def test_static_workspace_matches_pa_decode(lib, case):
         w = wl.custom("static1", [5, 60, 64], dtype="f16", num_q_heads=4, num_kv_heads=4,
                       head_dim=64, block_size=16, seed=42)
         P = 0
-    need = pa.decode_workspace_size(w.num_seqs, w.num_q_heads, w.head_dim, w.max_blocks_per_seq,
-                                    w.block_size, P)
+    need = pa.decode_workspace_size(w.num_seqs, w.num_q_heads, w.num_kv_heads, w.head_dim,
+                                    w.max_blocks_per_seq, w.block_size, w.dtype, P)
     assert need <= STATIC_BYTES
     d = upload(w)
     pa.kv_write(d["k_new"], d["v_new"], d["k_cache"], d["v_cache"], d["slot_mapping"])
@@ -79,7 +79,7 @@ def test_static_workspace_matches_pa_decode(lib, case):
 
 def test_sizes_beyond_the_static_array_are_rejected(lib):
     # 4096 sequences x 64 heads x 128-token partitions of 64k tokens: far beyond 64 MiB.
-    need = pa.decode_workspace_size(4096, 64, 128, 4096, 16, 128)
+    need = pa.decode_workspace_size(4096, 64, 8, 128, 4096, 16, "bf16", 128)
     assert need > STATIC_BYTES
     vp = ctypes.c_void_p
     st = lib.pa_decode_static_workspace(vp(256), vp(256), vp(256), vp(256), vp(256), 4096,
