@@ -130,7 +130,8 @@ struct DecodeTile {
     static constexpr int kItemOffset = kPOffset + kConsumerWarps * GT * kTps * 4;
     static constexpr int kQOffset = align16(kItemOffset + kItems * 32);
     static constexpr int kMergeOffset = kQOffset + kItems * align16(kQBytes);
-    static constexpr int kBarOffset = align16(kMergeOffset + kItems * kMergeFloats * 4);
+    static constexpr int kTableOffset = align16(kMergeOffset + kItems * kMergeFloats * 4);  // [32]
+    static constexpr int kBarOffset = kTableOffset + 32 * 4;
     // full[kStages], empty[kStages], q_full[kItems], item_free[kItems]
     static constexpr int kFlagOffset = kBarOffset + (2 * kStages + 2 * kItems) * 8;
     static constexpr int kSmemBytes = kFlagOffset + 16;
@@ -367,57 +368,57 @@ __device__ __forceinline__ void decode_produce(const DecodeParams& p, unsigned c
                      C::kQBytes, qf, policy);
         }
 
-        // ---- this item's slice of the block table, one entry per lane
+        // ---- this item's slice of the block table goes to shared memory (one
+        //      entry per lane); lane 0 alone then runs the stage loop, so its
+        //      bounded waits need no agreement with the other lanes
         const int32_t* trow = p.block_tables + static_cast<size_t>(s) * p.max_blocks_per_seq;
         const int blk_end = (tok_end + B - 1) / B;
-        int win = tok_begin / B;
-        int32_t entry = (win + lane < blk_end) ? __ldg(trow + win + lane) : -1;
+        const int win = tok_begin / B;
+        int32_t* twin = reinterpret_cast<int32_t*>(smem + C::kTableOffset);
+        twin[lane] = (win + lane < blk_end) ? __ldg(trow + win + lane) : -1;
+        __syncwarp();
         const unsigned char* kbase = p.k_cache + static_cast<size_t>(hk) * head_bytes;
         const unsigned char* vbase = p.v_cache + static_cast<size_t>(hk) * head_bytes;
 
-        for (int i = 0; i < nst; ++i) {
-            const int cc = c + i;
-            const int st = cc % C::kStages;
-            if (cc >= C::kStages &&
-                !mbar_wait_lane0(empty0 + 8 * st, static_cast<uint32_t>(cc / C::kStages - 1) & 1)) {
-                if (lane == 0) report(p.d_err, PA_DERR_TIMEOUT);
-                *abort_flag = 1;
-                aborted = true;
-                c = cc;
-                break;
-            }
-            const int t0 = tok_begin + i * C::kTps;
-            const int t1 = min(t0 + C::kTps, tok_end);
-            size_t src_off[C::kSubs];
-            uint32_t len_bytes[C::kSubs];
-            uint32_t bytes = 0;
-            uint64_t mask = 0;
+        if (lane == 0) {
+            for (int i = 0; i < nst; ++i) {
+                const int cc = c + i;
+                const int st = cc % C::kStages;
+                if (cc >= C::kStages &&
+                    !mbar_wait(empty0 + 8 * st, static_cast<uint32_t>(cc / C::kStages - 1) & 1)) {
+                    report(p.d_err, PA_DERR_TIMEOUT);
+                    *abort_flag = 1;
+                    aborted = true;
+                    c = cc;
+                    break;
+                }
+                const int t0 = tok_begin + i * C::kTps;
+                const int t1 = min(t0 + C::kTps, tok_end);
+                size_t src_off[C::kSubs];
+                uint32_t len_bytes[C::kSubs];
+                uint32_t bytes = 0;
+                uint64_t mask = 0;
 #pragma unroll
-            for (int r = 0; r < C::kSubs; ++r) {
-                const int t = t0 + 16 * r;
-                len_bytes[r] = 0;
-                src_off[r] = 0;
-                if (t < t1) {  // warp-uniform
-                    const int lb = t / B;
-                    const int off = t - lb * B;
-                    const int len = min(16, t1 - t);
-                    while (lb - win >= 32) {
-                        win += 32;
-                        entry = (win + lane < blk_end) ? __ldg(trow + win + lane) : -1;
-                    }
-                    const int pb = __shfl_sync(0xffffffffu, entry, lb - win);
-                    if (static_cast<unsigned>(pb) < static_cast<unsigned>(p.num_blocks)) {
-                        src_off[r] = static_cast<size_t>(pb) * block_bytes +
-                                     static_cast<size_t>(off) * C::kRowBytes;
-                        len_bytes[r] = static_cast<uint32_t>(len) * C::kRowBytes;
-                        bytes += 2u * len_bytes[r];
-                        mask |= ((1ull << len) - 1ull) << (16 * r);
-                    } else {
-                        oob = true;
+                for (int r = 0; r < C::kSubs; ++r) {
+                    const int t = t0 + 16 * r;
+                    len_bytes[r] = 0;
+                    src_off[r] = 0;
+                    if (t < t1) {
+                        const int lb = t / B;
+                        const int off = t - lb * B;
+                        const int len = min(16, t1 - t);
+                        const int pb = lb - win < 32 ? twin[lb - win] : __ldg(trow + lb);
+                        if (static_cast<unsigned>(pb) < static_cast<unsigned>(p.num_blocks)) {
+                            src_off[r] = static_cast<size_t>(pb) * block_bytes +
+                                         static_cast<size_t>(off) * C::kRowBytes;
+                            len_bytes[r] = static_cast<uint32_t>(len) * C::kRowBytes;
+                            bytes += 2u * len_bytes[r];
+                            mask |= ((1ull << len) - 1ull) << (16 * r);
+                        } else {
+                            oob = true;
+                        }
                     }
                 }
-            }
-            if (lane == 0) {
                 uint32_t flags = 0;
                 if (i < W) flags |= kStageFirst;
                 if (i + W >= nst) flags |= kStageLast;
@@ -436,8 +437,8 @@ __device__ __forceinline__ void decode_produce(const DecodeParams& p, unsigned c
                     }
                 }
             }
-            __syncwarp();
         }
+        aborted = __shfl_sync(0xffffffffu, aborted ? 1 : 0, 0) != 0;
         if (aborted) break;
         c += nst;
         ++item_seq;
@@ -446,22 +447,20 @@ __device__ __forceinline__ void decode_produce(const DecodeParams& p, unsigned c
     }
 
     // ---- one end marker per consumer warp (the next W stages, one per warp)
-    if (!aborted) {
+    if (!aborted && lane == 0) {
         const int c_end = c;
         for (int i = 0; i < W; ++i) {
             const int cc = c_end + i;
             const int st = cc % C::kStages;
             if (cc >= C::kStages &&
-                !mbar_wait_lane0(empty0 + 8 * st, static_cast<uint32_t>(cc / C::kStages - 1) & 1)) {
-                if (lane == 0) report(p.d_err, PA_DERR_TIMEOUT);
+                !mbar_wait(empty0 + 8 * st, static_cast<uint32_t>(cc / C::kStages - 1) & 1)) {
+                report(p.d_err, PA_DERR_TIMEOUT);
                 *abort_flag = 1;
                 break;
             }
-            if (lane == 0) {
-                meta[st].mask = 0;
-                meta[st].flags = kStageEnd;
-                mbar_arrive(full0 + 8 * st);
-            }
+            meta[st].mask = 0;
+            meta[st].flags = kStageEnd;
+            mbar_arrive(full0 + 8 * st);
             c = cc + 1;
         }
     }

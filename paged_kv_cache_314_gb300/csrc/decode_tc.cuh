@@ -158,7 +158,7 @@ __device__ __forceinline__ void tc_produce(const DecodeParams& p, const CUtensor
 
         const int qs = item_seq % C::kQSlots;
         if (item_seq >= C::kQSlots &&
-            !mbar_wait_lane0(qempty0 + 8 * qs, static_cast<uint32_t>(item_seq / C::kQSlots - 1) & 1)) {
+            !mbar_wait_warp(qempty0 + 8 * qs, static_cast<uint32_t>(item_seq / C::kQSlots - 1) & 1)) {
             if (lane == 0) report(p.d_err, PA_DERR_TIMEOUT);
             *abort_flag = 1;
             break;
@@ -184,7 +184,7 @@ __device__ __forceinline__ void tc_produce(const DecodeParams& p, const CUtensor
             const int cc = c + i;
             const int st = cc % C::kStages;
             if (cc >= C::kStages &&
-                !mbar_wait_lane0(empty0 + 8 * st, static_cast<uint32_t>(cc / C::kStages - 1) & 1)) {
+                !mbar_wait_warp(empty0 + 8 * st, static_cast<uint32_t>(cc / C::kStages - 1) & 1)) {
                 if (lane == 0) report(p.d_err, PA_DERR_TIMEOUT);
                 *abort_flag = 1;
                 aborted = true;
@@ -248,7 +248,7 @@ __device__ __forceinline__ void tc_produce(const DecodeParams& p, const CUtensor
     if (!aborted) {  // one end marker: the MMA warp and the team read stages in order
         const int st = c % C::kStages;
         if (c >= C::kStages &&
-            !mbar_wait_lane0(empty0 + 8 * st, static_cast<uint32_t>(c / C::kStages - 1) & 1)) {
+            !mbar_wait_warp(empty0 + 8 * st, static_cast<uint32_t>(c / C::kStages - 1) & 1)) {
             if (lane == 0) report(p.d_err, PA_DERR_TIMEOUT);
             *abort_flag = 1;
         } else {
@@ -335,11 +335,11 @@ __device__ __forceinline__ void tc_mma(const DecodeParams& p, unsigned char* sm,
     // Returns 0 = issued, 1 = end marker, -1 = gave up.
     auto issue_mma1 = [&](int c) -> int {
         const int st = c % C::kStages;
-        if (!mbar_wait_lane0(full0 + 8 * st, static_cast<uint32_t>(c / C::kStages) & 1)) return -1;
+        if (!mbar_wait_warp(full0 + 8 * st, static_cast<uint32_t>(c / C::kStages) & 1)) return -1;
         const uint32_t flags = meta[st].flags;
         if (flags & kStageEnd) return 1;
         if (flags & kStageFirst) {
-            if (!mbar_wait_lane0(qready, static_cast<uint32_t>(nitems) & 1)) return -1;
+            if (!mbar_wait_warp(qready, static_cast<uint32_t>(nitems) & 1)) return -1;
             ++nitems;
         }
         tc::fence_after_sync();
@@ -371,7 +371,7 @@ __device__ __forceinline__ void tc_mma(const DecodeParams& p, unsigned char* sm,
             fail();
             break;
         }
-        if (!mbar_wait_lane0(pfull0 + 8 * (c & 1), static_cast<uint32_t>(c / 2) & 1)) {
+        if (!mbar_wait_warp(pfull0 + 8 * (c & 1), static_cast<uint32_t>(c / 2) & 1)) {
             fail();
             break;
         }
