@@ -130,8 +130,7 @@ struct DecodeTile {
     static constexpr int kItemOffset = kPOffset + kConsumerWarps * GT * kTps * 4;
     static constexpr int kQOffset = align16(kItemOffset + kItems * 32);
     static constexpr int kMergeOffset = kQOffset + kItems * align16(kQBytes);
-    static constexpr int kTableOffset = align16(kMergeOffset + kItems * kMergeFloats * 4);  // [32]
-    static constexpr int kBarOffset = kTableOffset + 32 * 4;
+    static constexpr int kBarOffset = align16(kMergeOffset + kItems * kMergeFloats * 4);
     // full[kStages], empty[kStages], q_full[kItems], item_free[kItems]
     static constexpr int kFlagOffset = kBarOffset + (2 * kStages + 2 * kItems) * 8;
     static constexpr int kSmemBytes = kFlagOffset + 16;
@@ -292,6 +291,7 @@ __device__ __forceinline__ void decode_produce(const DecodeParams& p, unsigned c
     int ctx_lane = lane < S ? __ldg(p.context_lens + lane) : 0;
     int c = 0;         // stages issued by this CTA
     int item_seq = 0;  // items taken by this CTA
+    int q_issued = 0;  // items whose query rows were requested
     bool aborted = false;
     bool oob = false;
     int item_id = 0;
@@ -367,58 +367,56 @@ __device__ __forceinline__ void decode_produce(const DecodeParams& p, unsigned c
                      static_cast<const T*>(p.q) + (static_cast<size_t>(s) * p.num_q_heads + hq0) * D,
                      C::kQBytes, qf, policy);
         }
+        q_issued = item_seq + 1;
 
-        // ---- this item's slice of the block table goes to shared memory (one
-        //      entry per lane); lane 0 alone then runs the stage loop, so its
-        //      bounded waits need no agreement with the other lanes
+        // ---- this item's slice of the block table, one entry per lane
         const int32_t* trow = p.block_tables + static_cast<size_t>(s) * p.max_blocks_per_seq;
         const int blk_end = (tok_end + B - 1) / B;
-        const int win = tok_begin / B;
-        int32_t* twin = reinterpret_cast<int32_t*>(smem + C::kTableOffset);
-        twin[lane] = (win + lane < blk_end) ? __ldg(trow + win + lane) : -1;
-        __syncwarp();
+        int win = tok_begin / B;
+        int32_t entry = (win + lane < blk_end) ? __ldg(trow + win + lane) : -1;
         const unsigned char* kbase = p.k_cache + static_cast<size_t>(hk) * head_bytes;
         const unsigned char* vbase = p.v_cache + static_cast<size_t>(hk) * head_bytes;
 
-        if (lane == 0) {
-            for (int i = 0; i < nst; ++i) {
-                const int cc = c + i;
-                const int st = cc % C::kStages;
-                if (cc >= C::kStages &&
-                    !mbar_wait(empty0 + 8 * st, static_cast<uint32_t>(cc / C::kStages - 1) & 1)) {
-                    report(p.d_err, PA_DERR_TIMEOUT);
-                    *abort_flag = 1;
-                    aborted = true;
-                    c = cc;
-                    break;
-                }
-                const int t0 = tok_begin + i * C::kTps;
-                const int t1 = min(t0 + C::kTps, tok_end);
-                size_t src_off[C::kSubs];
-                uint32_t len_bytes[C::kSubs];
-                uint32_t bytes = 0;
-                uint64_t mask = 0;
+        for (int i = 0; i < nst; ++i) {
+            const int cc = c + i;
+            const int st = cc % C::kStages;
+            // Every lane waits; only lane 0's outcome decides whether the stage is
+            // issued.  A lane that gave up still runs this stage's warp-wide code,
+            // and the vote at its end makes all lanes leave together.
+            const bool ok = cc < C::kStages ||
+                            mbar_wait(empty0 + 8 * st, static_cast<uint32_t>(cc / C::kStages - 1) & 1);
+            const int t0 = tok_begin + i * C::kTps;
+            const int t1 = min(t0 + C::kTps, tok_end);
+            size_t src_off[C::kSubs];
+            uint32_t len_bytes[C::kSubs];
+            uint32_t bytes = 0;
+            uint64_t mask = 0;
 #pragma unroll
-                for (int r = 0; r < C::kSubs; ++r) {
-                    const int t = t0 + 16 * r;
-                    len_bytes[r] = 0;
-                    src_off[r] = 0;
-                    if (t < t1) {
-                        const int lb = t / B;
-                        const int off = t - lb * B;
-                        const int len = min(16, t1 - t);
-                        const int pb = lb - win < 32 ? twin[lb - win] : __ldg(trow + lb);
-                        if (static_cast<unsigned>(pb) < static_cast<unsigned>(p.num_blocks)) {
-                            src_off[r] = static_cast<size_t>(pb) * block_bytes +
-                                         static_cast<size_t>(off) * C::kRowBytes;
-                            len_bytes[r] = static_cast<uint32_t>(len) * C::kRowBytes;
-                            bytes += 2u * len_bytes[r];
-                            mask |= ((1ull << len) - 1ull) << (16 * r);
-                        } else {
-                            oob = true;
-                        }
+            for (int r = 0; r < C::kSubs; ++r) {
+                const int t = t0 + 16 * r;
+                len_bytes[r] = 0;
+                src_off[r] = 0;
+                if (t < t1) {  // warp-uniform
+                    const int lb = t / B;
+                    const int off = t - lb * B;
+                    const int len = min(16, t1 - t);
+                    while (lb - win >= 32) {
+                        win += 32;
+                        entry = (win + lane < blk_end) ? __ldg(trow + win + lane) : -1;
+                    }
+                    const int pb = __shfl_sync(0xffffffffu, entry, lb - win);
+                    if (static_cast<unsigned>(pb) < static_cast<unsigned>(p.num_blocks)) {
+                        src_off[r] = static_cast<size_t>(pb) * block_bytes +
+                                     static_cast<size_t>(off) * C::kRowBytes;
+                        len_bytes[r] = static_cast<uint32_t>(len) * C::kRowBytes;
+                        bytes += 2u * len_bytes[r];
+                        mask |= ((1ull << len) - 1ull) << (16 * r);
+                    } else {
+                        oob = true;
                     }
                 }
+            }
+            if (lane == 0 && ok) {
                 uint32_t flags = 0;
                 if (i < W) flags |= kStageFirst;
                 if (i + W >= nst) flags |= kStageLast;
@@ -437,8 +435,15 @@ __device__ __forceinline__ void decode_produce(const DecodeParams& p, unsigned c
                     }
                 }
             }
+            if (__any_sync(0xffffffffu, !ok)) {
+                if (lane == 0) report(p.d_err, PA_DERR_TIMEOUT);
+                *abort_flag = 1;
+                aborted = true;
+                // stages up to cc-1 were issued, and cc as well when lane 0 saw its slot free
+                c = __shfl_sync(0xffffffffu, ok ? cc + 1 : cc, 0);
+                break;
+            }
         }
-        aborted = __shfl_sync(0xffffffffu, aborted ? 1 : 0, 0) != 0;
         if (aborted) break;
         c += nst;
         ++item_seq;
@@ -472,7 +477,7 @@ __device__ __forceinline__ void decode_produce(const DecodeParams& p, unsigned c
             if (!mbar_wait(full0 + 8 * st, static_cast<uint32_t>(cc / C::kStages) & 1))
                 report(p.d_err, PA_DERR_TIMEOUT);
         }
-        for (int k = max(0, item_seq - C::kItems); k < item_seq; ++k) {
+        for (int k = max(0, q_issued - C::kItems); k < q_issued; ++k) {
             const int sl = k % C::kItems;
             if (!mbar_wait(qfull0 + 8 * sl, static_cast<uint32_t>(k / C::kItems) & 1))
                 report(p.d_err, PA_DERR_TIMEOUT);

@@ -106,7 +106,7 @@ __device__ __forceinline__ void tc_produce(const DecodeParams& p, const CUtensor
 
     int s_cur = 0, base_items = 0, win0 = 0;
     int ctx_lane = lane < S ? __ldg(p.context_lens + lane) : 0;
-    int c = 0, item_seq = 0;
+    int c = 0, item_seq = 0, q_issued = 0;
     bool aborted = false, oob = false;
     int item_id = 0;
     if (lane == 0) item_id = static_cast<int>(atomicAdd(p.counters, 1u));
@@ -174,6 +174,7 @@ __device__ __forceinline__ void tc_produce(const DecodeParams& p, const CUtensor
                      static_cast<const T*>(p.q) + (static_cast<size_t>(s) * p.num_q_heads + hq0) * C::D,
                      qbytes, qf, policy);
         }
+        q_issued = item_seq + 1;
 
         const int32_t* trow = p.block_tables + static_cast<size_t>(s) * p.max_blocks_per_seq;
         const int blk_end = (tok_end + B - 1) / B;
@@ -266,7 +267,7 @@ __device__ __forceinline__ void tc_produce(const DecodeParams& p, const CUtensor
         for (int cc = max(0, c - C::kStages); cc < c; ++cc)
             if (!mbar_wait(full0 + 8 * (cc % C::kStages), static_cast<uint32_t>(cc / C::kStages) & 1))
                 report(p.d_err, PA_DERR_TIMEOUT);
-        for (int k = max(0, item_seq - C::kQSlots); k < item_seq; ++k)
+        for (int k = max(0, q_issued - C::kQSlots); k < q_issued; ++k)
             if (!mbar_wait(qfull0 + 8 * (k % C::kQSlots), static_cast<uint32_t>(k / C::kQSlots) & 1))
                 report(p.d_err, PA_DERR_TIMEOUT);
         __threadfence();
