@@ -4,6 +4,7 @@
  *
  *   pa_kv_write     write each new token's K and V rows into its slot
  *   pa_copy_blocks  copy whole blocks (copy-on-write of shared blocks)
+ *   pa_swap_blocks  copy whole blocks between two pools (swap to / from host)
  *   pa_decode       one query per sequence attends to its cached tokens,
  *                   walking the sequence's block table
  *
@@ -24,7 +25,8 @@
  *   block_mapping    int32 [num_pairs][2] = (src, dst)
  *
  * Conventions shared by every call:
- *   - Ownership: every pointer is device memory owned by the caller.  The
+ *   - Ownership: every pointer is device memory owned by the caller (for
+ *     pa_swap_blocks, one pool may be device-addressable host memory).  The
  *     library allocates nothing, keeps no state between calls and never
  *     synchronises the stream.  Device pointers must be 16-byte aligned.
  *   - Asynchrony: work is enqueued on `stream` (NULL = the legacy default
@@ -109,6 +111,27 @@ pa_status pa_kv_write(const void* k_new, const void* v_new, void* k_cache, void*
  */
 pa_status pa_copy_blocks(void* k_cache, void* v_cache, const int32_t* block_mapping, int num_pairs,
                          int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                         pa_dtype dtype, uint32_t* d_err, pa_stream_t stream);
+
+/* pa_swap_blocks -- copy whole blocks from one pool to another.
+ *
+ * For each pair i, block block_mapping[i][0] of the source pool (all kv heads,
+ * all block_size slots, K and V) is copied to block block_mapping[i][1] of the
+ * destination pool.  Under memory pressure the blocks of a preempted sequence
+ * are swapped out to CPU memory and swapped back in when it resumes
+ * ("PagedAttention" (compassingai.com) §6 and §11; kwkr.cn "vLLM PagedAttention
+ * 技术深度解析" §1.5).  Either pool may be pinned host memory the GPU can
+ * address (cudaHostAlloc / cudaHostRegister; on GB300 read and written
+ * directly over NVLink-C2C by the copy kernel): swap-out is device -> host,
+ * swap-in host -> device.  block_mapping must be device-accessible.  Both
+ * pools have the layout [num_blocks][num_kv_heads][block_size][head_dim];
+ * ids outside [0, src_num_blocks) / [0, dst_num_blocks) are skipped and
+ * flagged PA_DERR_BLOCK_OOB.  Two pairs with the same dst leave one of the
+ * two blocks (unspecified which).
+ */
+pa_status pa_swap_blocks(const void* src_k, const void* src_v, void* dst_k, void* dst_v,
+                         const int32_t* block_mapping, int num_pairs, int num_kv_heads,
+                         int head_dim, int block_size, int src_num_blocks, int dst_num_blocks,
                          pa_dtype dtype, uint32_t* d_err, pa_stream_t stream);
 
 /* pa_copy_blocks_check -- optional validation of a block_mapping on the device:
@@ -199,6 +222,13 @@ pa_status pa_decode_static_workspace(void* out, const void* q, const void* k_cac
                                      int block_size, int num_blocks, float scale,
                                      int partition_tokens, pa_dtype dtype, uint32_t* d_err,
                                      pa_stream_t stream);
+
+/* pa_selftest_wait_timeout -- exercises the bounded waits the kernels use.
+ * One warp waits on a barrier nothing ever arrives at; after the wait limit
+ * (about one second) it gives up, ORs PA_DERR_TIMEOUT into *d_err (required)
+ * and the kernel ends normally, leaving the context usable.  Stands for
+ * every wait in the library: each gives up the same way instead of hanging. */
+pa_status pa_selftest_wait_timeout(uint32_t* d_err, pa_stream_t stream);
 
 #ifdef __cplusplus
 }

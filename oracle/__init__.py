@@ -66,6 +66,9 @@ def _load() -> ctypes.CDLL:
             lib.oracle_kv_write.restype = c_uint
             lib.oracle_kv_write.argtypes = [vp, vp, vp, vp, vp, c_int, c_int, c_int, c_int, c_int,
                                             c_int]
+            lib.oracle_swap_blocks.restype = c_uint
+            lib.oracle_swap_blocks.argtypes = [vp, vp, vp, vp, vp, c_int, c_int, c_int, c_int,
+                                               c_int, c_int, c_int]
             lib.oracle_copy_blocks.restype = c_uint
             lib.oracle_copy_blocks.argtypes = [vp, vp, vp, c_int, c_int, c_int, c_int, c_int,
                                                c_int]
@@ -144,6 +147,16 @@ def copy_blocks(k_cache, v_cache, block_mapping, *, dtype: str):
     bm = np.ascontiguousarray(block_mapping, dtype=np.int32).reshape(-1, 2)
     return int(lib.oracle_copy_blocks(_ptr(k_cache), _ptr(v_cache), _ptr(bm), bm.shape[0], Hkv, d,
                                       B, NB, ELEM_BYTES[dtype]))
+
+
+def swap_blocks(src_k, src_v, dst_k, dst_v, block_mapping, *, dtype: str):
+    """In-place on host copies of the destination pools.  Returns error bits."""
+    lib = _load()
+    NBs, Hkv, B, d = src_k.shape
+    NBd = dst_k.shape[0]
+    bm = np.ascontiguousarray(block_mapping, dtype=np.int32).reshape(-1, 2)
+    return int(lib.oracle_swap_blocks(_ptr(src_k), _ptr(src_v), _ptr(dst_k), _ptr(dst_v), _ptr(bm),
+                                      bm.shape[0], Hkv, d, B, NBs, NBd, ELEM_BYTES[dtype]))
 
 
 def step(w, *, do_copy: bool = True):

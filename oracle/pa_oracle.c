@@ -21,6 +21,9 @@
  *    wmrh.cn "paged attention": only the new token's K/V is computed).
  *  - copy_blocks: copy-on-write of a shared block copies its whole content
  *    to a fresh block ("PagedAttention" (compassingai.com) §6).
+ *  - swap_blocks: whole blocks move between the GPU pool and a CPU pool when
+ *    a sequence is preempted and resumed ("PagedAttention" (compassingai.com)
+ *    §6, §11).
  *  - bounds checks: a bad block id, slot or length is skipped and reported,
  *    never followed ("PagedAttention" (compassingai.com) §13).
  */
@@ -186,6 +189,24 @@ unsigned oracle_copy_blocks(void* k_cache, void* v_cache, const int32_t* block_m
         }
         memmove((char*)k_cache + (size_t)dst * blk_bytes, (const char*)k_cache + (size_t)src * blk_bytes, blk_bytes);
         memmove((char*)v_cache + (size_t)dst * blk_bytes, (const char*)v_cache + (size_t)src * blk_bytes, blk_bytes);
+    }
+    return err;
+}
+
+unsigned oracle_swap_blocks(const void* src_k, const void* src_v, void* dst_k, void* dst_v,
+                            const int32_t* block_mapping, int num_pairs, int num_kv_heads,
+                            int head_dim, int block_size, int src_num_blocks, int dst_num_blocks,
+                            int elem_bytes) {
+    unsigned err = 0;
+    const size_t blk_bytes = (size_t)num_kv_heads * block_size * head_dim * elem_bytes;
+    for (int i = 0; i < num_pairs; ++i) {
+        int src = block_mapping[2 * i], dst = block_mapping[2 * i + 1];
+        if (src < 0 || src >= src_num_blocks || dst < 0 || dst >= dst_num_blocks) {
+            err |= OR_BLOCK_OOB;
+            continue;
+        }
+        memcpy((char*)dst_k + (size_t)dst * blk_bytes, (const char*)src_k + (size_t)src * blk_bytes, blk_bytes);
+        memcpy((char*)dst_v + (size_t)dst * blk_bytes, (const char*)src_v + (size_t)src * blk_bytes, blk_bytes);
     }
     return err;
 }

@@ -55,6 +55,12 @@ unsigned oracle_copy_blocks(void* k_cache, void* v_cache, const int32_t* block_m
                             int num_pairs, int num_kv_heads, int head_dim, int block_size,
                             int num_blocks, int elem_bytes);
 
+/* Copy whole blocks from a source pool to a destination pool for each pair. */
+unsigned oracle_swap_blocks(const void* src_k, const void* src_v, void* dst_k, void* dst_v,
+                            const int32_t* block_mapping, int num_pairs, int num_kv_heads,
+                            int head_dim, int block_size, int src_num_blocks, int dst_num_blocks,
+                            int elem_bytes);
+
 #ifdef __cplusplus
 }
 #endif

@@ -27,9 +27,9 @@ DERR_TIMEOUT = 8
 DERR_MAPPING_CONFLICT = 16
 
 DTYPE_CODE = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}
-EXPORTED = ("pa_abi_version", "pa_status_string", "pa_kv_write", "pa_copy_blocks",
+EXPORTED = ("pa_abi_version", "pa_status_string", "pa_kv_write", "pa_copy_blocks", "pa_swap_blocks",
             "pa_copy_blocks_check", "pa_decode_partition_tokens", "pa_decode_workspace_size",
-            "pa_decode")
+            "pa_decode", "pa_decode_static_workspace", "pa_selftest_wait_timeout")
 
 _lock = threading.Lock()
 _lib: Optional[ctypes.CDLL] = None
@@ -65,12 +65,16 @@ def load() -> ctypes.CDLL:
         lib.pa_kv_write.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, vp, vp]
         lib.pa_copy_blocks.restype = i32
         lib.pa_copy_blocks.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, i32, vp, vp]
+        lib.pa_swap_blocks.restype = i32
+        lib.pa_swap_blocks.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, vp, vp]
         lib.pa_copy_blocks_check.restype = i32
         lib.pa_copy_blocks_check.argtypes = [vp, i32, vp, vp]
         lib.pa_decode_partition_tokens.restype = i32
         lib.pa_decode_partition_tokens.argtypes = [i32, i32, i32, i32, i32, i32, i32]
         lib.pa_decode_workspace_size.restype = u64
         lib.pa_decode_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32, i32, i32]
+        lib.pa_selftest_wait_timeout.restype = i32
+        lib.pa_selftest_wait_timeout.argtypes = [vp, vp]
         lib.pa_decode.restype = i32
         lib.pa_decode.argtypes = [vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, i32,
                                   ctypes.c_float, i32, i32, vp, u64, vp, vp]
@@ -107,6 +111,13 @@ def _cuda_contig(name: str, t: torch.Tensor) -> None:
         raise ValueError(f"{name} must be contiguous")
 
 
+def selftest_wait_timeout(d_err: torch.Tensor, stream=None) -> None:
+    """Run the bounded-wait self-test (about one second); expect DERR_TIMEOUT in d_err."""
+    _cuda_contig("d_err", d_err)
+    _check(load().pa_selftest_wait_timeout(_ptr(d_err), _stream(stream, d_err.device)),
+           "pa_selftest_wait_timeout")
+
+
 def abi_version() -> int:
     return int(load().pa_abi_version())
 
@@ -141,6 +152,34 @@ def copy_blocks(k_cache: torch.Tensor, v_cache: torch.Tensor, block_mapping: tor
                                NB, DTYPE_CODE[k_cache.dtype], _ptr(d_err),
                                _stream(stream, k_cache.device))
     _check(st, "pa_copy_blocks")
+
+
+def _pool(name: str, t: torch.Tensor) -> None:
+    if not (t.is_cuda or t.is_pinned()):
+        raise ValueError(f"{name} must be a CUDA tensor or pinned host memory")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def swap_blocks(src_k: torch.Tensor, src_v: torch.Tensor, dst_k: torch.Tensor,
+                dst_v: torch.Tensor, block_mapping: torch.Tensor,
+                d_err: Optional[torch.Tensor] = None, stream=None) -> None:
+    """Copy block src of the source pool to block dst of the destination pool for each
+    (src, dst) row; either pool may be pinned host memory (swap out / swap in)."""
+    for n, t in (("src_k", src_k), ("src_v", src_v), ("dst_k", dst_k), ("dst_v", dst_v)):
+        _pool(n, t)
+    _cuda_contig("block_mapping", block_mapping)
+    if block_mapping.dtype != torch.int32:
+        raise ValueError("block_mapping must be int32 [P][2]")
+    if src_k.shape[1:] != dst_k.shape[1:] or src_k.dtype != dst_k.dtype:
+        raise ValueError("pools must agree in kv heads, block size, head_dim and dtype")
+    NBs, Hkv, B, d = src_k.shape
+    P = block_mapping.numel() // 2
+    st = load().pa_swap_blocks(_ptr(src_k), _ptr(src_v), _ptr(dst_k), _ptr(dst_v),
+                               _ptr(block_mapping), P, Hkv, d, B, NBs, dst_k.shape[0],
+                               DTYPE_CODE[src_k.dtype], _ptr(d_err),
+                               _stream(stream, block_mapping.device))
+    _check(st, "pa_swap_blocks")
 
 
 def copy_blocks_check(block_mapping: torch.Tensor, d_err: torch.Tensor, stream=None) -> None:

@@ -1,11 +1,17 @@
-// copy_blocks.cu -- copy-on-write block copies, plus an optional check of the
-// (src, dst) mapping.
+// copy_blocks.cu -- whole-block copies: copy-on-write inside one pool
+// (pa_copy_blocks), swap between two pools (pa_swap_blocks), and an optional
+// check of a copy-on-write mapping.
 //
 // A write to a block shared by several sequences first takes a fresh block
 // and copies the shared content there ("PagedAttention" (compassingai.com)
-// §6; kwkr.cn "vLLM PagedAttention 技术深度解析" §1.3.2).  A block holds every
-// kv head's K (and V) for block_size tokens, so one pair moves
-// 2 * num_kv_heads * block_size * head_dim elements.
+// §6; kwkr.cn "vLLM PagedAttention 技术深度解析" §1.3.2).  Under memory
+// pressure whole blocks are swapped out to CPU memory and back in later
+// ("PagedAttention" (compassingai.com) §6, §11; kwkr.cn §1.5 moves inactive
+// blocks to CPU memory over NVLink).  On GB300 the GPU addresses pinned host
+// memory directly over NVLink-C2C, so the swap is the same copy kernel with a
+// source and a destination pool, either of which may live in host memory.
+// A block holds every kv head's K (and V) for block_size tokens, so one pair
+// moves 2 * num_kv_heads * block_size * head_dim elements.
 #include "pa_device.cuh"
 #include "pa_host.h"
 
@@ -16,12 +22,15 @@ constexpr int kCopyThreads = 256;
 constexpr int kCopyUnroll = 4;  // 16-byte vectors in flight per thread
 
 struct CopyParams {
-    uint4* k_cache;
-    uint4* v_cache;
+    const uint4* src_k;
+    const uint4* src_v;
+    uint4* dst_k;
+    uint4* dst_v;
     const int32_t* block_mapping;
     uint32_t* d_err;
     int num_pairs;
-    int num_blocks;
+    int src_blocks;
+    int dst_blocks;
     int64_t block_vecs;  // 16-byte vectors per block of one tensor
 };
 
@@ -29,7 +38,7 @@ __global__ void __launch_bounds__(kCopyThreads) copy_blocks_kernel(const CopyPar
     for (int pair = blockIdx.y; pair < p.num_pairs; pair += gridDim.y) {
         const int src = p.block_mapping[2 * pair];
         const int dst = p.block_mapping[2 * pair + 1];
-        if (src < 0 || src >= p.num_blocks || dst < 0 || dst >= p.num_blocks) {
+        if (src < 0 || src >= p.src_blocks || dst < 0 || dst >= p.dst_blocks) {
             if (blockIdx.x == 0 && threadIdx.x == 0) report(p.d_err, PA_DERR_BLOCK_OOB);
             continue;
         }
@@ -44,7 +53,7 @@ __global__ void __launch_bounds__(kCopyThreads) copy_blocks_kernel(const CopyPar
             if (i < total) {
                 const bool is_v = i >= p.block_vecs;
                 const int64_t w = is_v ? i - p.block_vecs : i;
-                const uint4* from = (is_v ? p.v_cache : p.k_cache) + src * p.block_vecs + w;
+                const uint4* from = (is_v ? p.src_v : p.src_k) + src * p.block_vecs + w;
                 buf[u] = *from;
             }
         }
@@ -54,7 +63,7 @@ __global__ void __launch_bounds__(kCopyThreads) copy_blocks_kernel(const CopyPar
             if (i < total) {
                 const bool is_v = i >= p.block_vecs;
                 const int64_t w = is_v ? i - p.block_vecs : i;
-                uint4* to = (is_v ? p.v_cache : p.k_cache) + dst * p.block_vecs + w;
+                uint4* to = (is_v ? p.dst_v : p.dst_k) + dst * p.block_vecs + w;
                 *to = buf[u];
             }
         }
@@ -79,27 +88,57 @@ __global__ void __launch_bounds__(256)
 }  // namespace
 }  // namespace pa
 
-extern "C" pa_status pa_copy_blocks(void* k_cache, void* v_cache, const int32_t* block_mapping,
-                                    int num_pairs, int num_kv_heads, int head_dim, int block_size,
-                                    int num_blocks, pa_dtype dtype, uint32_t* d_err,
-                                    pa_stream_t stream) {
-    using namespace pa;
+namespace pa {
+namespace {
+
+// Device-side address of a pool: device and managed memory as they are,
+// pinned (page-locked, registered) host memory through its mapped device
+// address; anything else (pageable host memory) is rejected.
+pa_status device_view(const void* ptr, const void** out) {
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, ptr) != cudaSuccess) {
+        cudaGetLastError();  // clear the error the query left behind
+        return PA_ERR_INVALID_ARG;
+    }
+    switch (a.type) {
+        case cudaMemoryTypeDevice:
+        case cudaMemoryTypeManaged:
+            *out = ptr;
+            return PA_OK;
+        case cudaMemoryTypeHost:
+            if (a.devicePointer == nullptr) return PA_ERR_INVALID_ARG;
+            *out = a.devicePointer;
+            return PA_OK;
+        default:
+            return PA_ERR_INVALID_ARG;
+    }
+}
+
+pa_status launch_copy(const void* src_k, const void* src_v, void* dst_k, void* dst_v,
+                      const int32_t* block_mapping, int num_pairs, int num_kv_heads, int head_dim,
+                      int block_size, int src_blocks, int dst_blocks, pa_dtype dtype,
+                      uint32_t* d_err, pa_stream_t stream) {
     if (!valid_dtype(dtype)) return PA_ERR_INVALID_ARG;
-    if (num_pairs < 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 || num_blocks <= 0)
+    if (num_pairs < 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 ||
+        src_blocks <= 0 || dst_blocks <= 0)
         return PA_ERR_INVALID_ARG;
     const int64_t block_bytes =
         static_cast<int64_t>(num_kv_heads) * block_size * head_dim * elem_bytes(dtype);
     if (block_bytes % 16 != 0) return PA_ERR_UNSUPPORTED;
     if (num_pairs == 0) return PA_OK;
-    if (!k_cache || !v_cache || !block_mapping) return PA_ERR_INVALID_ARG;
-    if (!aligned16(k_cache) || !aligned16(v_cache)) return PA_ERR_INVALID_ARG;
+    if (!src_k || !src_v || !dst_k || !dst_v || !block_mapping) return PA_ERR_INVALID_ARG;
+    if (!aligned16(src_k) || !aligned16(src_v) || !aligned16(dst_k) || !aligned16(dst_v))
+        return PA_ERR_INVALID_ARG;
     CopyParams p;
-    p.k_cache = static_cast<uint4*>(k_cache);
-    p.v_cache = static_cast<uint4*>(v_cache);
+    p.src_k = static_cast<const uint4*>(src_k);
+    p.src_v = static_cast<const uint4*>(src_v);
+    p.dst_k = static_cast<uint4*>(dst_k);
+    p.dst_v = static_cast<uint4*>(dst_v);
     p.block_mapping = block_mapping;
     p.d_err = d_err;
     p.num_pairs = num_pairs;
-    p.num_blocks = num_blocks;
+    p.src_blocks = src_blocks;
+    p.dst_blocks = dst_blocks;
     p.block_vecs = block_bytes / 16;
     const int64_t per_cta = static_cast<int64_t>(kCopyThreads) * kCopyUnroll;
     const int64_t gx = (2 * p.block_vecs + per_cta - 1) / per_cta;
@@ -107,6 +146,40 @@ extern "C" pa_status pa_copy_blocks(void* k_cache, void* v_cache, const int32_t*
     const dim3 grid(static_cast<unsigned>(gx), static_cast<unsigned>(num_pairs < 65535 ? num_pairs : 65535));
     copy_blocks_kernel<<<grid, kCopyThreads, 0, as_cuda(stream)>>>(p);
     return launch_status();
+}
+
+}  // namespace
+}  // namespace pa
+
+extern "C" pa_status pa_copy_blocks(void* k_cache, void* v_cache, const int32_t* block_mapping,
+                                    int num_pairs, int num_kv_heads, int head_dim, int block_size,
+                                    int num_blocks, pa_dtype dtype, uint32_t* d_err,
+                                    pa_stream_t stream) {
+    return pa::launch_copy(k_cache, v_cache, k_cache, v_cache, block_mapping, num_pairs,
+                           num_kv_heads, head_dim, block_size, num_blocks, num_blocks, dtype, d_err,
+                           stream);
+}
+
+extern "C" pa_status pa_swap_blocks(const void* src_k, const void* src_v, void* dst_k, void* dst_v,
+                                    const int32_t* block_mapping, int num_pairs, int num_kv_heads,
+                                    int head_dim, int block_size, int src_num_blocks,
+                                    int dst_num_blocks, pa_dtype dtype, uint32_t* d_err,
+                                    pa_stream_t stream) {
+    if (num_pairs > 0) {  // either pool may be pinned host memory: use its device address
+        const void* ptrs[4] = {src_k, src_v, dst_k, dst_v};
+        for (const void*& q : ptrs) {
+            if (q == nullptr) return PA_ERR_INVALID_ARG;
+            const pa_status st = pa::device_view(q, &q);
+            if (st != PA_OK) return st;
+        }
+        src_k = ptrs[0];
+        src_v = ptrs[1];
+        dst_k = const_cast<void*>(ptrs[2]);
+        dst_v = const_cast<void*>(ptrs[3]);
+    }
+    return pa::launch_copy(src_k, src_v, dst_k, dst_v, block_mapping, num_pairs, num_kv_heads,
+                           head_dim, block_size, src_num_blocks, dst_num_blocks, dtype, d_err,
+                           stream);
 }
 
 extern "C" pa_status pa_copy_blocks_check(const int32_t* block_mapping, int num_pairs,

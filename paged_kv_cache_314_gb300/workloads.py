@@ -259,11 +259,19 @@ def build_workload(name: str, plan: _Plan, *, dtype: str, num_q_heads: int, num_
 
 
 def plan_independent(ctx: Sequence[int], block_size: int, max_blocks_per_seq: int,
-                     num_blocks: int, rng: np.random.Generator) -> _Plan:
-    """Sequences with private blocks; each step writes the token at ctx-1."""
+                     num_blocks: int, rng: np.random.Generator, layout: str = "paged") -> _Plan:
+    """Sequences with private blocks; each step writes the token at ctx-1.
+
+    layout "paged": blocks handed out from a seeded permutation of the pool
+    (scattered); "contiguous": in pool order, so each sequence's blocks are
+    consecutive in memory -- the same cache without the scatter, the
+    comparison the PagedAttention pages make against contiguous KV."""
     ctx = np.asarray(ctx, dtype=np.int64)
     S, B = len(ctx), block_size
-    alloc = BlockAllocator(num_blocks, rng.permutation(num_blocks))
+    if layout not in ("paged", "contiguous"):
+        raise ValueError(layout)
+    order = rng.permutation(num_blocks) if layout == "paged" else np.arange(num_blocks)
+    alloc = BlockAllocator(num_blocks, order)
     tables = np.full((S, max_blocks_per_seq), -1, dtype=np.int32)
     data = np.zeros((num_blocks, B), dtype=bool)
     writes = []
@@ -346,15 +354,15 @@ CONFIG_NAMES = ("tiny", "llama7b", "llama13b", "gqa_share", "long")
 
 
 def _independent(name, ctx, *, dtype, Hq, Hkv, d, B, pool_factor, MB, seed, scale=None,
-                 partition_tokens=0, poison=True, min_pool=0, meta=None):
+                 partition_tokens=0, poison=True, min_pool=0, meta=None, layout="paged"):
     rng = np.random.default_rng(seed)
     needed = int(sum((int(n) + B - 1) // B for n in ctx))
     NB = max(min_pool, pool_size(needed, pool_factor))
-    plan = plan_independent(ctx, B, MB, NB, rng)
+    plan = plan_independent(ctx, B, MB, NB, rng, layout)
     return build_workload(name, plan, dtype=dtype, num_q_heads=Hq, num_kv_heads=Hkv, head_dim=d,
                           block_size=B, num_blocks=NB, scale=scale,
                           partition_tokens=partition_tokens, seed=seed + 1_000_003,
-                          poison=poison, meta=meta)
+                          poison=poison, meta=dict(meta or {}, layout=layout))
 
 
 def tiny(seed: int = 314, poison: bool = True) -> Workload:
@@ -364,24 +372,24 @@ def tiny(seed: int = 314, poison: bool = True) -> Workload:
 
 
 def llama7b(seed: int = 315, poison: bool = True, num_seqs: int = 64, num_heads: int = 32,
-            ctx_range=(128, 2048), partition_tokens: int = 0) -> Workload:
+            ctx_range=(128, 2048), partition_tokens: int = 0, layout: str = "paged") -> Workload:
     """LLaMA-7B-shaped decode: 64 seqs, 32 heads, d=128, fp16, B=16, ctx U[128,2048]."""
     rng = np.random.default_rng(seed)
     ctx = rng.integers(ctx_range[0], ctx_range[1] + 1, size=num_seqs)
     return _independent("llama7b", ctx, dtype="f16", Hq=num_heads, Hkv=num_heads, d=128, B=16,
                         pool_factor=1.1, MB=(ctx_range[1] + 15) // 16, seed=seed,
-                        partition_tokens=partition_tokens, poison=poison)
+                        partition_tokens=partition_tokens, poison=poison, layout=layout)
 
 
 def llama13b(seed: int = 316, poison: bool = True, num_seqs: int = 256, num_heads: int = 40,
-             partition_tokens: int = 0) -> Workload:
+             partition_tokens: int = 0, layout: str = "paged") -> Workload:
     """LLaMA-13B-shaped decode: 256 seqs, 40 heads, d=128, bf16, B=16,
     ctx log-normal with median 400 (sigma 1.0), clipped to [1, 4096]."""
     rng = np.random.default_rng(seed)
     ctx = np.clip(np.rint(np.exp(rng.normal(math.log(400.0), 1.0, size=num_seqs))), 1, 4096)
     return _independent("llama13b", ctx.astype(np.int64), dtype="bf16", Hq=num_heads,
                         Hkv=num_heads, d=128, B=16, pool_factor=1.1, MB=4096 // 16, seed=seed,
-                        partition_tokens=partition_tokens, poison=poison)
+                        partition_tokens=partition_tokens, poison=poison, layout=layout)
 
 
 def gqa_share(seed: int = 317, poison: bool = True, groups: int = 32, samples: int = 8,
@@ -408,14 +416,14 @@ def gqa_share(seed: int = 317, poison: bool = True, groups: int = 32, samples: i
 
 def long_context(seed: int = 318, poison: bool = True, block_size: int = 16, num_seqs: int = 8,
                  num_heads: int = 32, ctx_range=(32768, 131072),
-                 partition_tokens: int = 512) -> Workload:
+                 partition_tokens: int = 512, layout: str = "paged") -> Workload:
     """Long context: 8 seqs, 32 heads, d=128, bf16, ctx U[32768,131072], 512-token partitions."""
     rng = np.random.default_rng(seed)
     ctx = rng.integers(ctx_range[0], ctx_range[1] + 1, size=num_seqs)
     return _independent(f"long_b{block_size}", ctx, dtype="bf16", Hq=num_heads, Hkv=num_heads,
                         d=128, B=block_size, pool_factor=1.05,
                         MB=(ctx_range[1] + block_size - 1) // block_size, seed=seed,
-                        partition_tokens=partition_tokens, poison=poison)
+                        partition_tokens=partition_tokens, poison=poison, layout=layout)
 
 
 def custom(name: str, ctx: Sequence[int], *, dtype: str, num_q_heads: int, num_kv_heads: int,

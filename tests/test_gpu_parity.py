@@ -251,3 +251,42 @@ def test_host_checked_errors():
         pa.decode(out, d["q"], d["k_cache"], d["v_cache"], d["block_tables"], d["context_lens"],
                   w.scale, partition_tokens=24)
     assert e.value.status == 1
+
+
+# ---------------------------------------------------------------------------
+# swap to / from pinned host memory, and the bounded waits
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_swap_blocks_device_host_round_trip(dtype):
+    rng = np.random.default_rng(33)
+    NB, Hkv, B, d, NH = 40, 4, 16, 128 if dtype == "bf16" else 64, 24
+    from gpu_util import to_torch
+    gk = wl._to_storage(rng.standard_normal((NB, Hkv, B, d)).astype(np.float32), dtype)
+    gv = wl._to_storage(rng.standard_normal((NB, Hkv, B, d)).astype(np.float32), dtype)
+    hk = wl._poison_fill((NH, Hkv, B, d), dtype, True)
+    hv = wl._poison_fill((NH, Hkv, B, d), dtype, True)
+    dk, dv = to_torch(gk, dtype).cuda(), to_torch(gv, dtype).cuda()
+    pk, pv = to_torch(hk, dtype).pin_memory(), to_torch(hv, dtype).pin_memory()
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out_pairs = np.array([[3, 0], [17, 5], [39, 23], [8, NH]], np.int32)  # last: dst outside
+    pa.swap_blocks(dk, dv, pk, pv, torch.from_numpy(out_pairs).cuda(), d_err=err)  # swap out
+    torch.cuda.synchronize()
+    ref_err = oracle.swap_blocks(gk, gv, hk, hv, out_pairs, dtype=dtype)
+    assert int(err.item()) == ref_err == oracle.ERR_BLOCK_OOB
+    assert same_bits(to_numpy(pk, dtype), hk) and same_bits(to_numpy(pv, dtype), hv)
+    in_pairs = np.array([[0, 1], [5, 2], [23, 30]], np.int32)  # swap back in elsewhere
+    err.zero_()
+    pa.swap_blocks(pk, pv, dk, dv, torch.from_numpy(in_pairs).cuda(), d_err=err)
+    torch.cuda.synchronize()
+    assert oracle.swap_blocks(hk, hv, gk, gv, in_pairs, dtype=dtype) == 0 == int(err.item())
+    assert same_bits(to_numpy(dk, dtype), gk) and same_bits(to_numpy(dv, dtype), gv)
+
+
+def test_bounded_wait_gives_up_and_reports():
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    pa.selftest_wait_timeout(err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == pa.DERR_TIMEOUT
+    # the context is still usable afterwards
+    _check_step(wl.tiny())

@@ -358,3 +358,23 @@ def test_copy_blocks_copies_whole_blocks_only():
         assert np.array_equal(kc[t], k0[s]) and np.array_equal(vc[t], v0[s])
     for p in (0, 1, 2, 3, 4, 7):
         assert np.array_equal(kc[p], k0[p]) and np.array_equal(vc[p], v0[p])
+
+
+def test_swap_blocks_moves_whole_blocks_between_pools():
+    rng = np.random.default_rng(12)
+    Hkv, B, d = 2, 16, 64
+    gk = _store(rng.standard_normal((6, Hkv, B, d)), "bf16")
+    gv = _store(rng.standard_normal((6, Hkv, B, d)), "bf16")
+    hk = wl._poison_fill((4, Hkv, B, d), "bf16", True)
+    hv = wl._poison_fill((4, Hkv, B, d), "bf16", True)
+    h0k, h0v = hk.copy(), hv.copy()
+    out_pairs = np.array([[5, 0], [2, 3], [1, 9]], np.int32)  # last one: dst outside the host pool
+    err = oracle.swap_blocks(gk, gv, hk, hv, out_pairs, dtype="bf16")
+    assert err == oracle.ERR_BLOCK_OOB
+    assert np.array_equal(hk[0], gk[5]) and np.array_equal(hv[3], gv[2])
+    for b in (1, 2):
+        assert np.array_equal(hk[b].view(np.uint8), h0k[b].view(np.uint8))
+    # and back into other device blocks: the round trip preserves every byte
+    gk2, gv2 = gk.copy(), gv.copy()
+    assert oracle.swap_blocks(hk, hv, gk2, gv2, np.array([[0, 1], [3, 4]], np.int32), dtype="bf16") == 0
+    assert np.array_equal(gk2[1], gk[5]) and np.array_equal(gv2[4], gv[2])
