@@ -262,19 +262,20 @@ def run_gpu(args):
     launches_per_step = (1 if w.num_pairs else 0) + (1 if w.num_tokens else 0) + 1 + (
         1 if max_parts > 1 else 0)
 
-    def step(dd, ev_dec=None):
+    def step(dd, ev_mid=None):
+        """copy_blocks, kv_write, decode; ev_mid: events after copy_blocks and after kv_write."""
         if w.num_pairs:
             pa.copy_blocks(dd["k_cache"], dd["v_cache"], dd["block_mapping"], d_err=d_err)
+        if ev_mid is not None:
+            ev_mid[0].record(stream)
         if w.num_tokens:
             pa.kv_write(dd["k_new"], dd["v_new"], dd["k_cache"], dd["v_cache"],
                         dd["slot_mapping"], d_err=d_err)
-        if ev_dec is not None:
-            ev_dec[0].record(stream)
+        if ev_mid is not None:
+            ev_mid[1].record(stream)
         pa.decode(out, dd["q"], dd["k_cache"], dd["v_cache"], dd["block_tables"],
                   dd["context_lens"], w.scale, partition_tokens=w.partition_tokens,
                   workspace=workspace, d_err=d_err)
-        if ev_dec is not None:
-            ev_dec[1].record(stream)
 
     for _ in range(args.warmup):
         flush.zero_()
@@ -299,7 +300,9 @@ def run_gpu(args):
         torch.cuda.synchronize()
         t_wall = time.perf_counter() - t_wall
     step_ms = [a.elapsed_time(b) for a, _, _, b in ev]
-    dec_ms = [a.elapsed_time(b) for _, a, b, _ in ev]
+    dec_ms = [a.elapsed_time(b) for _, _, a, b in ev]
+    copy_ms = float(np.mean([a.elapsed_time(b) for a, b, _, _ in ev]))
+    kvw_ms = float(np.mean([a.elapsed_time(b) for _, a, b, _ in ev]))
     ms_per_step = float(np.mean(step_ms))
     dec_ms_avg = float(np.mean(dec_ms))
     if dist is not None:
@@ -381,6 +384,17 @@ def run_gpu(args):
         "e2e": {"value": round(ws * kv_bytes / (e2e_avg * 1e-3) / 1e9, 2), "unit": "GB/s",
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                 "ms_per_step": round(e2e_avg, 5)},
+        "components": {
+            "kv_write": {"ms": round(kvw_ms, 5), "tokens": w.num_tokens,
+                         "gb_per_s": round(4 * w.num_tokens * w.num_kv_heads * w.head_dim *
+                                           w.elem_bytes / max(kvw_ms, 1e-9) / 1e6, 2),
+                         "bytes": "K and V rows read + written"},
+            "copy_blocks": {"ms": round(copy_ms, 5), "pairs": w.num_pairs,
+                            "gb_per_s": round(4 * w.num_pairs * w.num_kv_heads * w.block_size *
+                                              w.head_dim * w.elem_bytes / max(copy_ms, 1e-9) / 1e6, 2)
+                            if w.num_pairs else None,
+                            "bytes": "K and V blocks read + written"},
+            "decode": {"ms": round(dec_ms_avg, 5)}},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk.summary(),
         "wall_s_timed_region": round(t_wall, 4),
@@ -451,6 +465,49 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def run_swap(args):
+    """Swap-out (device pool -> pinned host pool) and swap-in bandwidth of pa_swap_blocks."""
+    import torch
+    import paged_kv_cache_314_gb300 as pa
+    from paged_kv_cache_314_gb300 import _build, workloads as wl
+    _build.build()
+    pa.load()
+    dev = torch.device("cuda", 0)
+    w = wl.by_name(args.config, poison=False)
+    d_k = _to_torch(w.k_cache, w.dtype).to(dev)
+    d_v = _to_torch(w.v_cache, w.dtype).to(dev)
+    n = min(w.num_blocks, args.swap_blocks)
+    h_k = torch.empty((n,) + tuple(d_k.shape[1:]), dtype=d_k.dtype).pin_memory()
+    h_v = torch.empty_like(h_k).pin_memory()
+    rng = np.random.default_rng(7)
+    src = rng.choice(w.num_blocks, size=n, replace=False).astype(np.int32)
+    out_map = torch.from_numpy(np.stack([src, np.arange(n, dtype=np.int32)], 1)).to(dev)
+    in_map = torch.from_numpy(np.stack([np.arange(n, dtype=np.int32), src], 1)).to(dev)
+    stream = torch.cuda.current_stream(dev)
+    res = {}
+    for name, args_ in (("swap_out", (d_k, d_v, h_k, h_v, out_map)),
+                        ("swap_in", (h_k, h_v, d_k, d_v, in_map))):
+        for _ in range(args.warmup):
+            pa.swap_blocks(*args_)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(args.steps):
+            pa.swap_blocks(*args_)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / args.steps
+        nbytes = 2 * n * d_k[0].numel() * d_k.element_size()
+        res[name] = {"ms": round(ms, 4), "gb_per_s": round(nbytes / (ms * 1e-3) / 1e9, 2),
+                     "bytes": nbytes}
+    print(json.dumps({"metric": "pa_swap_blocks GB/s (K+V blocks, device <-> pinned host)",
+                      "value": res["swap_out"]["gb_per_s"], "unit": "GB/s", "n_gpus": 1,
+                      "steps": args.steps, "warmup": args.warmup, "higher_is_better": True,
+                      "dtype": w.dtype, "data": "synthetic",
+                      "config": {"workload": WORKLOAD_TEXT.get(args.config, args.config),
+                                 "blocks": n}, **res}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -465,10 +522,15 @@ def main():
                     help="contiguous: identity-like block tables (each sequence's blocks adjacent), "
                          "the contiguous-KV comparison")
     ap.add_argument("--reference-sample-bytes", type=int, default=400 << 20)
+    ap.add_argument("--op", choices=("step", "swap"), default="step",
+                    help="swap: pa_swap_blocks bandwidth device <-> pinned host")
+    ap.add_argument("--swap-blocks", type=int, default=2048)
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)  # at least three untimed warm-up steps
     if args.impl == "reference":
         run_reference(args)
+    elif args.op == "swap":
+        run_swap(args)
     else:
         run_gpu(args)
 
