@@ -63,6 +63,9 @@ def _load() -> ctypes.CDLL:
             lib.oracle_decode.restype = c_uint
             lib.oracle_decode.argtypes = [vp, vp, vp, vp, vp, c_int, vp, c_int, c_int, c_int,
                                           c_int, c_int, c_int, c_double, c_int]
+            lib.oracle_multi_query.restype = c_uint
+            lib.oracle_multi_query.argtypes = [vp, vp, c_int, vp, vp, vp, vp, c_int, vp, c_int,
+                                               c_int, c_int, c_int, c_int, c_int, c_double, c_int]
             lib.oracle_kv_write.restype = c_uint
             lib.oracle_kv_write.argtypes = [vp, vp, vp, vp, vp, c_int, c_int, c_int, c_int, c_int,
                                             c_int]
@@ -128,6 +131,32 @@ def decode_head(q, k_cache, v_cache, block_tables, context_lens, s: int, h: int,
     return out, int(err)
 
 
+def multi_query(q, query_start, k_cache, v_cache, block_tables, context_lens, *, scale: float,
+                dtype: str):
+    """Causal attention of several query tokens per sequence: row
+    query_start[s] + i attends to the first context_lens[s] - L_s + i + 1
+    tokens of sequence s (L_s its number of queries); fp64 [Tq][Hq][d].
+    Returns (out, error bits)."""
+    lib = _load()
+    Tq, Hq, d = q.shape
+    NB, Hkv, B, d2 = k_cache.shape
+    assert d2 == d and v_cache.shape == k_cache.shape
+    S = context_lens.shape[0]
+    qs = np.ascontiguousarray(query_start, dtype=np.int32)
+    assert qs.shape == (S + 1,)
+    MB = block_tables.shape[1]
+    bt = np.ascontiguousarray(block_tables, dtype=np.int32)
+    cl = np.ascontiguousarray(context_lens, dtype=np.int32)
+    out = np.zeros((Tq, Hq, d), dtype=np.float64)
+    q = np.ascontiguousarray(q)
+    kc = np.ascontiguousarray(k_cache)
+    vc = np.ascontiguousarray(v_cache)
+    err = lib.oracle_multi_query(_ptr(out), _ptr(q), Tq, _ptr(qs), _ptr(kc), _ptr(vc), _ptr(bt),
+                                 MB, _ptr(cl), S, Hq, Hkv, d, B, NB, float(scale),
+                                 ELEM_TYPE[dtype])
+    return out, int(err)
+
+
 def kv_write(k_cache, v_cache, k_new, v_new, slot_mapping, *, dtype: str):
     """In-place on the host pool copies k_cache / v_cache.  Returns error bits."""
     lib = _load()
@@ -160,13 +189,18 @@ def swap_blocks(src_k, src_v, dst_k, dst_v, block_mapping, *, dtype: str):
 
 
 def step(w, *, do_copy: bool = True):
-    """One decode step of a workload on host copies: copy_blocks, kv_write,
-    decode.  Returns (k_cache, v_cache, out, error bits)."""
+    """One step of a workload on host copies: copy_blocks, kv_write, then
+    decode (or multi-query attention when the workload has query_start).
+    Returns (k_cache, v_cache, out, error bits)."""
     kc = w.k_cache.copy()
     vc = w.v_cache.copy()
     err = 0
     if do_copy and w.block_mapping.size:
         err |= copy_blocks(kc, vc, w.block_mapping, dtype=w.dtype)
     err |= kv_write(kc, vc, w.k_new, w.v_new, w.slot_mapping, dtype=w.dtype)
-    out, e = decode(w.q, kc, vc, w.block_tables, w.context_lens, scale=w.scale, dtype=w.dtype)
+    if getattr(w, "query_start", None) is not None:
+        out, e = multi_query(w.q, w.query_start, kc, vc, w.block_tables, w.context_lens,
+                             scale=w.scale, dtype=w.dtype)
+    else:
+        out, e = decode(w.q, kc, vc, w.block_tables, w.context_lens, scale=w.scale, dtype=w.dtype)
     return kc, vc, out, err | e

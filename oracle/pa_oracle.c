@@ -16,6 +16,8 @@
  *    lookup by the kernel, model sees a contiguous cache).
  *  - only the last block is partly filled: tokens at or after context_len
  *    are never read ("PagedAttention" (compassingai.com) §7).
+ *  - multi-query: several query tokens per sequence, each attending to the
+ *    tokens up to and including its own position (causal), the same walk.
  *  - kv_write: the new token's K/V goes into its slot of the current block
  *    (kwkr.cn "vLLM PagedAttention 技术深度解析" §1.2.2 allocation flow;
  *    wmrh.cn "paged attention": only the new token's K/V is computed).
@@ -148,6 +150,53 @@ unsigned oracle_decode(double* out, const void* q, const void* k_cache, const vo
                                       max_blocks_per_seq, context_lens[s], h / group,
                                       num_kv_heads, head_dim, block_size, num_blocks, scale,
                                       elem_type);
+        }
+    }
+    return err;
+}
+
+/* Several query tokens per sequence (chunked prefill, speculative-decoding
+ * verification): the sequence's last L = query_start[s+1] - query_start[s]
+ * cached tokens are its queries, written to the cache before attention, so
+ * query i sits at position ctx - L + i and attends to positions 0 .. ctx-L+i
+ * (itself and everything before it, nothing after).  Each (query, head) is
+ * then plain decode attention over its own prefix of the sequence.
+ * "PagedAttention 深度解析" §六 item 5 (chunked prefill and speculative
+ * decoding named as the optimisations beside paged decode); kwkr.cn "vLLM PagedAttention 技术深度解析" §1.2.2
+ * (new tokens' K/V go into the sequence's blocks first). */
+unsigned oracle_multi_query(double* out, const void* q, int num_query_tokens,
+                            const int32_t* query_start, const void* k_cache, const void* v_cache,
+                            const int32_t* block_tables, int max_blocks_per_seq,
+                            const int32_t* context_lens, int num_seqs, int num_q_heads,
+                            int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                            double scale, int elem_type) {
+    unsigned err = 0;
+    const int group = num_q_heads / num_kv_heads;
+    const size_t es = elem_type == 0 ? 4 : 2;
+    for (int s = 0; s < num_seqs; ++s) {
+        const int q0 = query_start[s], q1 = query_start[s + 1];
+        if (q0 < 0 || q1 < q0 || q1 > num_query_tokens) { /* rows cannot be placed */
+            err |= OR_CTX_OOB;
+            continue;
+        }
+        const int L = q1 - q0, ctx = context_lens[s];
+        const int ok = ctx >= 0 && (long long)ctx <= (long long)max_blocks_per_seq * block_size &&
+                       L <= ctx;
+        if (!ok && L > 0) err |= OR_CTX_OOB;
+        for (int i = 0; i < L; ++i) {
+            for (int h = 0; h < num_q_heads; ++h) {
+                double* o = out + ((size_t)(q0 + i) * num_q_heads + h) * head_dim;
+                if (!ok) {
+                    for (int j = 0; j < head_dim; ++j) o[j] = 0.0;
+                    continue;
+                }
+                const char* q_row = (const char*)q + ((size_t)(q0 + i) * num_q_heads + h) * head_dim * es;
+                err |= oracle_decode_head(o, q_row, k_cache, v_cache,
+                                          block_tables + (size_t)s * max_blocks_per_seq,
+                                          max_blocks_per_seq, ctx - L + i + 1, h / group,
+                                          num_kv_heads, head_dim, block_size, num_blocks, scale,
+                                          elem_type);
+            }
         }
     }
     return err;

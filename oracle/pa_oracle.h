@@ -45,6 +45,22 @@ unsigned oracle_decode(double* out, const void* q, const void* k_cache, const vo
                        int num_kv_heads, int head_dim, int block_size, int num_blocks,
                        double scale, int elem_type);
 
+/* Attention for several query tokens per sequence (causal over the cache).
+ *   q, out         [num_query_tokens][Hq][d] (out in doubles)
+ *   query_start    [num_seqs + 1]: the queries of sequence s are rows
+ *                  query_start[s] .. query_start[s+1]-1, the last
+ *                  L = query_start[s+1]-query_start[s] of its context_lens[s]
+ *                  cached tokens; query i attends to tokens 0 .. ctx-L+i.
+ * A sequence with L > context_len or a context length out of range gets zero
+ * rows and error bit 2; so does a query range outside [0, num_query_tokens]
+ * (its rows are then left untouched). */
+unsigned oracle_multi_query(double* out, const void* q, int num_query_tokens,
+                            const int32_t* query_start, const void* k_cache, const void* v_cache,
+                            const int32_t* block_tables, int max_blocks_per_seq,
+                            const int32_t* context_lens, int num_seqs, int num_q_heads,
+                            int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                            double scale, int elem_type);
+
 /* Write each new token's K and V rows into its slot of the pool. */
 unsigned oracle_kv_write(void* k_cache, void* v_cache, const void* k_new, const void* v_new,
                          const int64_t* slot_mapping, int num_tokens, int num_kv_heads,

@@ -19,7 +19,10 @@ Memory model followed here (all from the PagedAttention pages):
     ("PagedAttention" (compassingai.com) §13).
 
 Layouts (row-major):
-  q, out        [S][Hq][d]
+  q, out        [S][Hq][d]     (one query per sequence: decode)
+                [Tq][Hq][d]    (several per sequence: query_start below)
+  query_start   int32 [S+1]    (queries of sequence s: rows query_start[s] ..
+                                query_start[s+1]-1, its last L_s tokens)
   k/v_cache     [NB][Hkv][B][d]
   k/v_new       [T][Hkv][d]
   block_tables  int32 [S][MB]  (entries past a sequence's last block are -1)
@@ -133,6 +136,11 @@ class Workload:
     block_mapping: np.ndarray
     refcount: np.ndarray
     meta: Dict[str, object] = dataclasses.field(default_factory=dict)
+    query_start: Optional[np.ndarray] = None  # None: one query per sequence
+
+    @property
+    def num_query_tokens(self) -> int:
+        return int(self.q.shape[0])
 
     @property
     def num_tokens(self) -> int:
@@ -204,6 +212,7 @@ class _Plan:
     write_tokens: List[Tuple[int, int]]  # (seq, position) written by kv_write this step
     pairs: List[Tuple[int, int]]
     refcount: np.ndarray
+    query_lens: Optional[np.ndarray] = None  # [S] queries per sequence; None: decode
 
 
 def _fill_pool(rng, NB, Hkv, B, d, dtype, data_slots, poison, chunk_blocks):
@@ -241,7 +250,13 @@ def build_workload(name: str, plan: _Plan, *, dtype: str, num_q_heads: int, num_
     chunk = max(1, (1 << 26) // row_elems)
     k_cache = _fill_pool(rng, NB, Hkv, B, d, dtype, plan.data_slots, poison, chunk)
     v_cache = _fill_pool(rng, NB, Hkv, B, d, dtype, plan.data_slots, poison, chunk)
-    q = _normals(rng, (S, Hq, d), dtype)
+    query_start = None
+    if plan.query_lens is None:
+        q = _normals(rng, (S, Hq, d), dtype)
+    else:
+        query_start = np.zeros(S + 1, dtype=np.int32)
+        query_start[1:] = np.cumsum(plan.query_lens)
+        q = _normals(rng, (int(query_start[-1]), Hq, d), dtype)
     T = len(plan.write_tokens)
     k_new = _normals(rng, (T, Hkv, d), dtype)
     v_new = _normals(rng, (T, Hkv, d), dtype)
@@ -255,12 +270,14 @@ def build_workload(name: str, plan: _Plan, *, dtype: str, num_q_heads: int, num_
         context_lens=np.ascontiguousarray(plan.ctx, dtype=np.int32),
         slot_mapping=_slots_for(plan, B), k_new=k_new, v_new=v_new,
         block_mapping=np.ascontiguousarray(pairs), refcount=plan.refcount.copy(),
-        meta=dict(meta or {}))
+        meta=dict(meta or {}), query_start=query_start)
 
 
 def plan_independent(ctx: Sequence[int], block_size: int, max_blocks_per_seq: int,
-                     num_blocks: int, rng: np.random.Generator, layout: str = "paged") -> _Plan:
-    """Sequences with private blocks; each step writes the token at ctx-1.
+                     num_blocks: int, rng: np.random.Generator, layout: str = "paged",
+                     query_lens: Optional[Sequence[int]] = None) -> _Plan:
+    """Sequences with private blocks; each step writes the token at ctx-1
+    (with ``query_lens``: the last L_s tokens, the step's queries).
 
     layout "paged": blocks handed out from a seeded permutation of the pool
     (scattered); "contiguous": in pool order, so each sequence's blocks are
@@ -275,18 +292,22 @@ def plan_independent(ctx: Sequence[int], block_size: int, max_blocks_per_seq: in
     tables = np.full((S, max_blocks_per_seq), -1, dtype=np.int32)
     data = np.zeros((num_blocks, B), dtype=bool)
     writes = []
+    ql = None if query_lens is None else np.asarray(query_lens, dtype=np.int64)
     for s in range(S):
         n = int(ctx[s])
+        L = min(1, n) if ql is None else int(ql[s])
+        if L > n:
+            raise ValueError("more queries than context tokens")
         nblk = (n + B - 1) // B
         if nblk > max_blocks_per_seq:
             raise ValueError("context longer than max_blocks_per_seq * block_size")
         for i in range(nblk):
             tables[s, i] = alloc.allocate()
-        for t in range(max(0, n - 1)):
+        for t in range(n - L):
             data[tables[s, t // B], t % B] = True
-        if n > 0:
-            writes.append((s, n - 1))
-    return _Plan(tables, ctx, data, writes, [], alloc.refcount.copy())
+        for t in range(n - L, n):
+            writes.append((s, t))
+    return _Plan(tables, ctx, data, writes, [], alloc.refcount.copy(), ql)
 
 
 def plan_shared_prefix(groups: int, samples: int, prefix_len: int, suffix: Sequence[int],
@@ -354,11 +375,12 @@ CONFIG_NAMES = ("tiny", "llama7b", "llama13b", "gqa_share", "long")
 
 
 def _independent(name, ctx, *, dtype, Hq, Hkv, d, B, pool_factor, MB, seed, scale=None,
-                 partition_tokens=0, poison=True, min_pool=0, meta=None, layout="paged"):
+                 partition_tokens=0, poison=True, min_pool=0, meta=None, layout="paged",
+                 query_lens=None):
     rng = np.random.default_rng(seed)
     needed = int(sum((int(n) + B - 1) // B for n in ctx))
     NB = max(min_pool, pool_size(needed, pool_factor))
-    plan = plan_independent(ctx, B, MB, NB, rng, layout)
+    plan = plan_independent(ctx, B, MB, NB, rng, layout, query_lens)
     return build_workload(name, plan, dtype=dtype, num_q_heads=Hq, num_kv_heads=Hkv, head_dim=d,
                           block_size=B, num_blocks=NB, scale=scale,
                           partition_tokens=partition_tokens, seed=seed + 1_000_003,
@@ -426,17 +448,48 @@ def long_context(seed: int = 318, poison: bool = True, block_size: int = 16, num
                         partition_tokens=partition_tokens, poison=poison, layout=layout)
 
 
+def spec_verify(seed: int = 319, poison: bool = True, num_seqs: int = 64, num_heads: int = 32,
+                draft: int = 4, ctx_range=(128, 2048), partition_tokens: int = 0) -> Workload:
+    """Speculative-decoding verification, LLaMA-7B-shaped: 64 seqs, 32 heads,
+    d=128, fp16, B=16; each sequence appends ``draft`` tokens this step and
+    all of them are queries (causal); ctx U[128,2048] counts them."""
+    rng = np.random.default_rng(seed)
+    ctx = rng.integers(ctx_range[0], ctx_range[1] + 1, size=num_seqs)
+    return _independent("spec_verify", ctx, dtype="f16", Hq=num_heads, Hkv=num_heads, d=128,
+                        B=16, pool_factor=1.1, MB=(ctx_range[1] + 15) // 16, seed=seed,
+                        partition_tokens=partition_tokens, poison=poison,
+                        query_lens=[draft] * num_seqs, meta={"draft": draft})
+
+
+def chunked_prefill(seed: int = 320, poison: bool = True, num_seqs: int = 8, num_q_heads: int = 32,
+                    num_kv_heads: int = 8, chunk: int = 512, prior_range=(0, 3584),
+                    dtype: str = "bf16", partition_tokens: int = 0) -> Workload:
+    """Chunked prefill: 8 seqs each append a ``chunk``-token slice of their
+    prompt to U[0,3584] tokens already cached; GQA 32 q / 8 kv heads, d=128,
+    bf16, B=16; every token of the chunk is a query (causal)."""
+    rng = np.random.default_rng(seed)
+    prior = rng.integers(prior_range[0], prior_range[1] + 1, size=num_seqs)
+    ctx = prior + chunk
+    return _independent("chunked_prefill", ctx, dtype=dtype, Hq=num_q_heads, Hkv=num_kv_heads,
+                        d=128, B=16, pool_factor=1.1,
+                        MB=(prior_range[1] + chunk + 15) // 16, seed=seed,
+                        partition_tokens=partition_tokens, poison=poison,
+                        query_lens=[chunk] * num_seqs, meta={"chunk": chunk})
+
+
 def custom(name: str, ctx: Sequence[int], *, dtype: str, num_q_heads: int, num_kv_heads: int,
            head_dim: int, block_size: int, seed: int, pool_factor: float = 1.25,
            max_blocks_per_seq: Optional[int] = None, partition_tokens: int = 0,
-           scale: Optional[float] = None, poison: bool = True, min_pool: int = 0) -> Workload:
+           scale: Optional[float] = None, poison: bool = True, min_pool: int = 0,
+           query_lens: Optional[Sequence[int]] = None) -> Workload:
     B = block_size
     mb = max_blocks_per_seq
     if mb is None:
         mb = max(1, max((int(n) + B - 1) // B for n in ctx) if len(ctx) else 1)
     return _independent(name, ctx, dtype=dtype, Hq=num_q_heads, Hkv=num_kv_heads, d=head_dim, B=B,
                         pool_factor=pool_factor, MB=mb, seed=seed, scale=scale,
-                        partition_tokens=partition_tokens, poison=poison, min_pool=min_pool)
+                        partition_tokens=partition_tokens, poison=poison, min_pool=min_pool,
+                        query_lens=query_lens)
 
 
 def by_name(name: str, poison: bool = True, **kw) -> Workload:
@@ -454,6 +507,10 @@ def by_name(name: str, poison: bool = True, **kw) -> Workload:
         return long_context(poison=poison, block_size=16, **kw)
     if name == "long_b128":
         return long_context(poison=poison, block_size=128, **kw)
+    if name == "spec_verify":
+        return spec_verify(poison=poison, **kw)
+    if name == "chunked_prefill":
+        return chunked_prefill(poison=poison, **kw)
     raise KeyError(name)
 
 

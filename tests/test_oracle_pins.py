@@ -378,3 +378,113 @@ def test_swap_blocks_moves_whole_blocks_between_pools():
     gk2, gv2 = gk.copy(), gv.copy()
     assert oracle.swap_blocks(hk, hv, gk2, gv2, np.array([[0, 1], [3, 4]], np.int32), dtype="bf16") == 0
     assert np.array_equal(gk2[1], gk[5]) and np.array_equal(gv2[4], gv[2])
+
+
+# ---------------------------------------------------------------------------
+# several query tokens per sequence (chunked prefill, speculative verification)
+# ---------------------------------------------------------------------------
+
+def _sdpa_masked(q64, K64, V64, scale, allowed):
+    """torch SDPA in float64 with an explicit boolean mask [Lq][n] (True = attend)."""
+    Hq, Hkv = q64.shape[1], K64.shape[0]
+    g = Hq // Hkv
+    Kt = torch.from_numpy(K64).repeat_interleave(g, dim=0)          # [Hq][n][d]
+    Vt = torch.from_numpy(V64).repeat_interleave(g, dim=0)
+    qt = torch.from_numpy(np.ascontiguousarray(q64.transpose(1, 0, 2)))  # [Hq][Lq][d]
+    m = torch.from_numpy(allowed)[None]
+    o = torch.nn.functional.scaled_dot_product_attention(qt, Kt, Vt, attn_mask=m, scale=scale)
+    return o.numpy().transpose(1, 0, 2)                             # [Lq][Hq][d]
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("Hq,Hkv", [(4, 4), (8, 2)])
+@pytest.mark.parametrize("B", [4, 16])
+def test_multi_query_equals_library_causal_attention(dtype, Hq, Hkv, B):
+    rng = np.random.default_rng(50 + B + Hq)
+    d = 32
+    # (context, queries): decode, full prefill from nothing, chunks, a chunk past a block edge
+    cases = [(1, 1), (7, 7), (B + 1, 3), (3 * B + 2, B), (2 * B, 1), (40, 16)]
+    ctx = [c for c, _ in cases]
+    L = np.array([l for _, l in cases])
+    S = len(cases)
+    _, Kc, Vc, kp, vp, tables = _contiguous_case(rng, S, Hq, Hkv, d, B, ctx, dtype)
+    qs = np.zeros(S + 1, np.int32)
+    qs[1:] = np.cumsum(L)
+    q = _store(rng.standard_normal((int(qs[-1]), Hq, d)), dtype)
+    scale = 1.0 / math.sqrt(d)
+    out, err = oracle.multi_query(q, qs, kp, vp, tables, np.array(ctx, np.int32), scale=scale,
+                                  dtype=dtype)
+    assert err == 0
+    for s, (n, l) in enumerate(cases):
+        # query i sits at position n - l + i and sees positions 0 .. n - l + i
+        allowed = np.arange(n)[None, :] <= (n - l + np.arange(l))[:, None]
+        want = _sdpa_masked(_f64(q[qs[s]:qs[s + 1]], dtype), _f64(Kc[s, :, :n], dtype),
+                            _f64(Vc[s, :, :n], dtype), scale, allowed)
+        np.testing.assert_allclose(out[qs[s]:qs[s + 1]], want, rtol=1e-12, atol=1e-12)
+
+
+def test_multi_query_full_prefill_first_query_returns_first_value():
+    """A prompt prefilled from nothing: its first token sees only itself."""
+    rng = np.random.default_rng(5)
+    n, Hkv, d = 37, 2, 16
+    K = rng.standard_normal((n, Hkv, d)).astype(np.float32)
+    V = rng.standard_normal((n, Hkv, d)).astype(np.float32)
+    q1, kp, vp, table = _one_seq(K, V, rng.standard_normal((Hkv, d)).astype(np.float32))
+    q = rng.standard_normal((n, 2 * Hkv, d)).astype(np.float32)
+    out, err = oracle.multi_query(q, np.array([0, n], np.int32), kp, vp, table,
+                                  np.array([n], np.int32), scale=0.3, dtype="f32")
+    assert err == 0
+    for h in range(2 * Hkv):
+        assert np.array_equal(out[0, h], V[0, h // 2].astype(np.float64))
+
+
+def test_multi_query_rows_match_decode_of_their_prefix():
+    """Row i of a chunk equals one-query decode of the same sequence cut at its position."""
+    w = wl.custom("mqpin", [50, 23, 16], dtype="f16", num_q_heads=4, num_kv_heads=2, head_dim=32,
+                  block_size=16, seed=8, query_lens=[5, 23, 1])
+    kc, vc, out, err = oracle.step(w, do_copy=False)
+    assert err == 0 and np.isfinite(out).all()
+    qs = w.query_start
+    for s in range(w.num_seqs):
+        n, l = int(w.context_lens[s]), int(qs[s + 1] - qs[s])
+        for i in range(l):
+            want, e = oracle.decode(w.q[qs[s] + i][None], kc, vc, w.block_tables[s:s + 1],
+                                    np.array([n - l + i + 1], np.int32), scale=w.scale,
+                                    dtype=w.dtype)
+            assert e == 0
+            assert np.array_equal(out[qs[s] + i], want[0])
+
+
+def test_multi_query_never_reads_later_tokens():
+    """Changing the K/V of positions after a query's own leaves its row unchanged."""
+    w = wl.custom("mqfut", [40], dtype="f32", num_q_heads=2, num_kv_heads=2, head_dim=16,
+                  block_size=16, seed=9, query_lens=[8])
+    kc, vc, base, err = oracle.step(w, do_copy=False)
+    assert err == 0
+    pos = 40 - 8 + 3  # query 3's position
+    for t in range(pos + 1, 40):
+        blk, off = int(w.block_tables[0, t // 16]), t % 16
+        kc[blk, :, off] = np.float32(1e3)
+        vc[blk, :, off] = np.float32(-1e3)
+    out, err = oracle.multi_query(w.q, w.query_start, kc, vc, w.block_tables, w.context_lens,
+                                  scale=w.scale, dtype=w.dtype)
+    assert err == 0
+    assert np.array_equal(out[:4], base[:4])
+    assert not np.allclose(out[4:], base[4:])
+
+
+def test_multi_query_bad_lengths_are_reported():
+    w = wl.custom("mqbad", [20, 10], dtype="f32", num_q_heads=2, num_kv_heads=1, head_dim=16,
+                  block_size=16, seed=10, query_lens=[3, 2])
+    kc, vc, _, err = oracle.step(w, do_copy=False)
+    assert err == 0
+    ctx = w.context_lens.copy()
+    ctx[1] = 1  # 2 queries but 1 cached token
+    out, err = oracle.multi_query(w.q, w.query_start, kc, vc, w.block_tables, ctx,
+                                  scale=w.scale, dtype=w.dtype)
+    assert err == oracle.ERR_CTX_OOB
+    assert np.all(out[3:5] == 0.0) and np.isfinite(out[:3]).all()
+    qs = np.array([0, 3, 2], np.int32)  # decreasing: the second sequence has no rows
+    out, err = oracle.multi_query(w.q, qs, kc, vc, w.block_tables, w.context_lens,
+                                  scale=w.scale, dtype=w.dtype)
+    assert err == oracle.ERR_CTX_OOB

@@ -119,3 +119,29 @@ def test_permute_physical_keeps_the_logical_cache():
             a = w.k_cache[w.block_tables[s, t // 16], :, t % 16]
             b = wp.k_cache[wp.block_tables[s, t // 16], :, t % 16]
             assert np.array_equal(a, b)
+
+
+@pytest.mark.parametrize("make", [lambda: wl.spec_verify(num_seqs=6, ctx_range=(20, 90)),
+                                  lambda: wl.chunked_prefill(num_seqs=3, chunk=40,
+                                                             prior_range=(0, 70))])
+def test_multi_query_plans_write_every_query_token(make):
+    w = make()
+    qs = w.query_start
+    S, B = w.num_seqs, w.block_size
+    assert qs.shape == (S + 1,) and qs[0] == 0 and np.all(np.diff(qs) >= 1)
+    assert w.q.shape == (int(qs[-1]), w.num_q_heads, w.head_dim)
+    assert w.num_tokens == int(qs[-1])  # kv_write stores every query token first
+    slots = w.slot_mapping.reshape(-1)
+    k = 0
+    for s in range(S):
+        n, L = int(w.context_lens[s]), int(qs[s + 1] - qs[s])
+        assert 1 <= L <= n
+        for t in range(n - L, n):  # the last L positions, in order
+            assert slots[k] == int(w.block_tables[s, t // B]) * B + t % B
+            k += 1
+        # positions before the queries hold data, the queries' own slots are poison
+        for t in (0, n - L - 1, n - L):
+            if 0 <= t < n:
+                v = w.k_cache[int(w.block_tables[s, t // B]), 0, t % B]
+                bits = v.view(np.uint32 if w.dtype == "f32" else np.uint16)
+                assert np.all(bits == wl.POISON_BITS[w.dtype]) == (t >= n - L)
