@@ -61,6 +61,39 @@ unsigned oracle_multi_query(double* out, const void* q, int num_query_tokens,
                             int num_kv_heads, int head_dim, int block_size, int num_blocks,
                             double scale, int elem_type);
 
+/* FP8 E4M3 ("E4M3FN": bias 7, 3 fraction bits, no infinities, S.1111.111 =
+ * NaN, largest finite 448).  Decoding of a code, and rounding of a float to
+ * the nearest code (ties to the even code, saturating at 448, NaN -> 0x7F,
+ * sign kept). */
+double oracle_e4m3_to_double(uint8_t code);
+uint8_t oracle_e4m3_from_float(float y);
+
+/* Decode attention over an E4M3 cache: k_cache / v_cache hold codes
+ * [NB][Hkv][B][d], k_scale / v_scale fp32 [NB][Hkv]; the value of an element
+ * is its code's value times the scale of its (block, kv head).  q (and the
+ * double output) as in oracle_decode, q of element type q_type (0, 1 or 2). */
+unsigned oracle_decode_fp8(double* out, const void* q, int q_type, const void* k_cache,
+                           const void* v_cache, const float* k_scale, const float* v_scale,
+                           const int32_t* block_tables, int max_blocks_per_seq,
+                           const int32_t* context_lens, int num_seqs, int num_q_heads,
+                           int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                           double scale);
+
+/* kv_write into an E4M3 cache: code = e4m3(float(x) / scale of the slot's
+ * (block, kv head)), the division in fp32.  k_new / v_new of type new_type. */
+unsigned oracle_kv_write_fp8(void* k_cache, void* v_cache, const float* k_scale,
+                             const float* v_scale, const void* k_new, const void* v_new,
+                             int new_type, const int64_t* slot_mapping, int num_tokens,
+                             int num_kv_heads, int head_dim, int block_size, int num_blocks);
+
+/* Whole-block copies of an E4M3 cache between two pools (the same pool for
+ * copy-on-write): codes and the block's K and V scales. */
+unsigned oracle_swap_blocks_fp8(const void* src_k, const void* src_v, const float* src_ks,
+                                const float* src_vs, void* dst_k, void* dst_v, float* dst_ks,
+                                float* dst_vs, const int32_t* block_mapping, int num_pairs,
+                                int num_kv_heads, int head_dim, int block_size,
+                                int src_num_blocks, int dst_num_blocks);
+
 /* Write each new token's K and V rows into its slot of the pool. */
 unsigned oracle_kv_write(void* k_cache, void* v_cache, const void* k_new, const void* v_new,
                          const int64_t* slot_mapping, int num_tokens, int num_kv_heads,

@@ -29,6 +29,7 @@ Layouts (row-major):
   context_lens  int32 [S]      (counts the new token written this step)
   slot_mapping  int64 [T]      (slot = block*B + offset; <0 means skip)
   block_mapping int32 [P][2]   ((src, dst) pairs for copy-on-write)
+  k/v_scale     fp32 [NB][Hkv] (E4M3 caches only: value = code value x scale)
 
 Element storage: f32 -> np.float32, f16 -> np.float16, bf16 -> np.uint16
 holding the bfloat16 bit pattern (round-to-nearest-even from float32).
@@ -137,6 +138,11 @@ class Workload:
     refcount: np.ndarray
     meta: Dict[str, object] = dataclasses.field(default_factory=dict)
     query_start: Optional[np.ndarray] = None  # None: one query per sequence
+    # E4M3 caches: k_cache / v_cache hold uint8 codes and these fp32 [NB][Hkv]
+    # scales; q, out and the new tokens keep ``dtype``.
+    kv_dtype: Optional[str] = None
+    k_scale: Optional[np.ndarray] = None
+    v_scale: Optional[np.ndarray] = None
 
     @property
     def num_query_tokens(self) -> int:
@@ -154,10 +160,14 @@ class Workload:
     def elem_bytes(self) -> int:
         return ELEM_BYTES[self.dtype]
 
+    @property
+    def kv_elem_bytes(self) -> int:
+        return 1 if self.kv_dtype == "e4m3" else ELEM_BYTES[self.dtype]
+
     def kv_read_bytes(self) -> int:
         """K+V bytes one decode step must read: ctx tokens per (seq, kv head)."""
         ctx = np.clip(self.context_lens.astype(np.int64), 0, None)
-        return int(ctx.sum()) * 2 * self.num_kv_heads * self.head_dim * self.elem_bytes
+        return int(ctx.sum()) * 2 * self.num_kv_heads * self.head_dim * self.kv_elem_bytes
 
     def kv_unique_read_bytes(self) -> int:
         """K+V bytes of the distinct physical slots decode reads (shared blocks once)."""
@@ -172,7 +182,7 @@ class Workload:
         for blk, rows in seen:
             per_blk[blk] = max(per_blk.get(blk, 0), rows)
         rows = sum(per_blk.values())
-        return rows * 2 * self.num_kv_heads * self.head_dim * self.elem_bytes
+        return rows * 2 * self.num_kv_heads * self.head_dim * self.kv_elem_bytes
 
 
 def _to_storage(x32: np.ndarray, dtype: str) -> np.ndarray:
@@ -492,7 +502,37 @@ def custom(name: str, ctx: Sequence[int], *, dtype: str, num_q_heads: int, num_k
                         query_lens=query_lens)
 
 
+E4M3_NAN = 0x7F  # poison code of E4M3 pools
+
+
+def to_fp8(w: Workload, seed: int = 0) -> Workload:
+    """The same workload over an E4M3 cache: one fp32 scale per (physical
+    block, kv head) for K and one for V, 2^-6 * exp(N(0, 0.3^2)), and the pool
+    codes = the existing values divided by their block's scale, converted to
+    float8_e4m3fn by torch (input data; poison slots become the NaN code).
+    q, the new tokens and the output keep the workload's dtype."""
+    import torch
+    rng = np.random.default_rng(seed)
+    NB, Hkv = w.num_blocks, w.num_kv_heads
+    ks = (2.0 ** -6 * np.exp(rng.normal(0.0, 0.3, size=(NB, Hkv)))).astype(np.float32)
+    vs = (2.0 ** -6 * np.exp(rng.normal(0.0, 0.3, size=(NB, Hkv)))).astype(np.float32)
+
+    def codes(pool, sc):
+        if w.dtype == "bf16":
+            x = torch.from_numpy(pool.view(np.int16)).view(torch.bfloat16).float()
+        else:
+            x = torch.from_numpy(np.ascontiguousarray(pool)).float()
+        x = x / torch.from_numpy(sc)[:, :, None, None]
+        return x.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+
+    return dataclasses.replace(w, name=w.name + "_fp8", k_cache=codes(w.k_cache, ks),
+                               v_cache=codes(w.v_cache, vs), kv_dtype="e4m3", k_scale=ks,
+                               v_scale=vs)
+
+
 def by_name(name: str, poison: bool = True, **kw) -> Workload:
+    if name.endswith("_fp8"):
+        return to_fp8(by_name(name[:-4], poison=poison, **kw), seed=321)
     if name == "tiny":
         return tiny(poison=poison, **kw)
     if name == "llama7b":
@@ -536,5 +576,7 @@ def permute_physical(w: Workload, rng: np.random.Generator) -> Workload:
         pairs = perm[pairs].astype(np.int32)
     rc = np.zeros_like(w.refcount)
     rc[perm] = w.refcount
+    if w.k_scale is not None:
+        w = dataclasses.replace(w, k_scale=w.k_scale[inv], v_scale=w.v_scale[inv])
     return dataclasses.replace(w, k_cache=k, v_cache=v, block_tables=tables.astype(np.int32),
                                slot_mapping=slots, block_mapping=pairs, refcount=rc)

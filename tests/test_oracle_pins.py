@@ -488,3 +488,158 @@ def test_multi_query_bad_lengths_are_reported():
     out, err = oracle.multi_query(w.q, qs, kc, vc, w.block_tables, w.context_lens,
                                   scale=w.scale, dtype=w.dtype)
     assert err == oracle.ERR_CTX_OOB
+
+
+# ---------------------------------------------------------------------------
+# E4M3 caches: quantised historical blocks with one scale per (block, kv head)
+# ---------------------------------------------------------------------------
+
+def test_e4m3_decoder_exhaustive():
+    codes = np.arange(256, dtype=np.uint8)
+    got = oracle.e4m3_to_f64(codes)
+    want = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    nan = np.isnan(want)
+    assert nan.sum() == 2 and np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], want[~nan])
+    # values fixed by the format: largest finite, smallest normal and subnormal, one
+    assert oracle.e4m3_to_f64(np.array([0x7E, 0x08, 0x01, 0x38, 0xB8], np.uint8)).tolist() == \
+        [448.0, 2.0 ** -6, 2.0 ** -9, 1.0, -1.0]
+
+
+def test_e4m3_encoder_rounds_to_nearest_even_and_saturates():
+    rng = np.random.default_rng(31)
+    y = (rng.standard_normal(100000) * np.exp(rng.uniform(-14, 7, 100000))).astype(np.float32)
+    y = y[np.abs(y) < 448]
+    want = torch.from_numpy(y).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(oracle.e4m3_from_f32(y), want)
+    # every code's value maps back to the code (NaN codes aside)
+    vals = oracle.e4m3_to_f64(np.arange(256, dtype=np.uint8))
+    ok = ~np.isnan(vals)
+    assert np.array_equal(oracle.e4m3_from_f32(vals[ok].astype(np.float32)),
+                          np.arange(256)[ok].astype(np.uint8))
+    # ties go to the even code; saturation; NaN; the sign of zero
+    ties = np.array([1.0625, 1.1875, 2.0 ** -10, 3 * 2.0 ** -10, 464.0 - 1, 464.0, 1e9,
+                     np.inf, -np.inf, np.nan, -1e-30, 0.0], np.float32)
+    assert oracle.e4m3_from_f32(ties).tolist() == \
+        [0x38, 0x3A, 0x00, 0x02, 0x7E, 0x7E, 0x7E, 0x7E, 0xFE, 0x7F, 0x80, 0x00]
+
+
+def _fp8_contiguous_case(rng, S, Hq, Hkv, d, B, ctx, q_dtype):
+    MB = max(1, max((n + B - 1) // B for n in ctx))
+    NB = S * MB
+    kc = rng.integers(0, 256, size=(NB, Hkv, B, d), dtype=np.uint8)
+    vc = rng.integers(0, 256, size=(NB, Hkv, B, d), dtype=np.uint8)
+    for c in (kc, vc):  # no NaN codes in the data
+        c[(c & 0x7F) == 0x7F] = 0x3F
+    ks = np.exp(rng.normal(-4.0, 0.5, size=(NB, Hkv))).astype(np.float32)
+    vs = np.exp(rng.normal(-4.0, 0.5, size=(NB, Hkv))).astype(np.float32)
+    q = _store(rng.standard_normal((S, Hq, d)), q_dtype)
+    tables = np.arange(NB, dtype=np.int32).reshape(S, MB)
+    return q, kc, vc, ks, vs, tables
+
+
+def _dequant(codes, sc):
+    vals = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    return vals * sc.astype(np.float64)[:, :, None, None]
+
+
+@pytest.mark.parametrize("q_dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("Hq,Hkv", [(4, 4), (8, 2)])
+def test_fp8_decode_equals_library_attention_on_dequantised_values(q_dtype, Hq, Hkv):
+    rng = np.random.default_rng(60 + Hq)
+    d, B = 32, 16
+    ctx = [1, 15, 16, 17, 50]
+    S = len(ctx)
+    q, kc, vc, ks, vs, tables = _fp8_contiguous_case(rng, S, Hq, Hkv, d, B, ctx, q_dtype)
+    scale = 1.0 / math.sqrt(d)
+    out, err = oracle.decode_fp8(q, kc, vc, ks, vs, tables, np.array(ctx, np.int32), scale=scale,
+                                 q_dtype=q_dtype)
+    assert err == 0
+    K, V = _dequant(kc, ks), _dequant(vc, vs)  # [NB][Hkv][B][d]
+    MB = tables.shape[1]
+    for s, n in enumerate(ctx):
+        Ks = K[s * MB:(s + 1) * MB].transpose(1, 0, 2, 3).reshape(Hkv, MB * B, d)[:, :n]
+        Vs = V[s * MB:(s + 1) * MB].transpose(1, 0, 2, 3).reshape(Hkv, MB * B, d)[:, :n]
+        want = _sdpa(_f64(q[s], q_dtype), Ks, Vs, scale)
+        np.testing.assert_allclose(out[s], want, rtol=1e-12, atol=1e-12)
+
+
+def test_fp8_decode_with_power_of_two_scales_is_f32_decode_bitwise():
+    """Code x 2^k is exact in fp32, so the E4M3 cache and the fp32 cache of its
+    values give the same arithmetic."""
+    w = _small(dtype="f32", Hq=4, Hkv=2, d=32, ctx=(1, 16, 17, 40))
+    kc, vc, _, err = oracle.step(w, do_copy=False)
+    assert err == 0
+    rng = np.random.default_rng(61)
+    NB, Hkv = w.num_blocks, w.num_kv_heads
+    codes_k = rng.integers(0, 0x7E, size=kc.shape, dtype=np.uint8) | \
+        (rng.integers(0, 2, size=kc.shape, dtype=np.uint8) << 7)
+    codes_v = rng.integers(0, 0x7E, size=vc.shape, dtype=np.uint8)
+    ks = (2.0 ** rng.integers(-8, 3, size=(NB, Hkv))).astype(np.float32)
+    vs = (2.0 ** rng.integers(-8, 3, size=(NB, Hkv))).astype(np.float32)
+    k32 = _dequant(codes_k, ks).astype(np.float32)
+    v32 = _dequant(codes_v, vs).astype(np.float32)
+    assert np.array_equal(k32.astype(np.float64), _dequant(codes_k, ks))  # exact
+    want, e1 = oracle.decode(w.q, k32, v32, w.block_tables, w.context_lens, scale=w.scale,
+                             dtype="f32")
+    got, e2 = oracle.decode_fp8(w.q, codes_k, codes_v, ks, vs, w.block_tables, w.context_lens,
+                                scale=w.scale, q_dtype="f32")
+    assert e1 == e2 == 0 and np.array_equal(got, want)
+
+
+@pytest.mark.parametrize("new_dtype", ["f16", "bf16", "f32"])
+def test_fp8_kv_write_quantises_like_the_library(new_dtype):
+    rng = np.random.default_rng(62)
+    NB, Hkv, B, d, T = 6, 2, 16, 32, 9
+    kc = np.full((NB, Hkv, B, d), 0x7F, np.uint8)
+    vc = kc.copy()
+    ks = np.exp(rng.normal(-3.0, 1.0, size=(NB, Hkv))).astype(np.float32)
+    vs = np.exp(rng.normal(-3.0, 1.0, size=(NB, Hkv))).astype(np.float32)
+    kn = _store(rng.standard_normal((T, Hkv, d)) * 3, new_dtype)
+    vn = _store(rng.standard_normal((T, Hkv, d)) * 3, new_dtype)
+    kn.reshape(-1)[:4] = _store(np.array([1e4, -1e4, 0.0, -0.0]), new_dtype)  # saturate, zeros
+    slots = rng.permutation(NB * B)[:T].astype(np.int64)
+    slots[3] = -1  # padding
+    err = oracle.kv_write_fp8(kc, vc, ks, vs, kn, vn, slots, new_dtype=new_dtype)
+    assert err == 0
+    for t in range(T):
+        blk, off = divmod(int(slots[t]), B)
+        if slots[t] < 0:
+            continue
+        for (cache, new, sc) in ((kc, kn, ks), (vc, vn, vs)):
+            y = (torch.from_numpy(_f64(new[t], new_dtype)).float()
+                 / torch.from_numpy(sc[blk])[:, None])
+            want = y.clamp(-448, 448).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+            assert np.array_equal(cache[blk, :, off], want)
+    untouched = np.ones((NB, B), bool)
+    for sl in slots[slots >= 0]:
+        untouched[sl // B, sl % B] = False
+    assert np.all(kc.transpose(0, 2, 1, 3)[untouched] == 0x7F)
+
+
+def test_fp8_block_copies_move_codes_and_scales():
+    rng = np.random.default_rng(63)
+    NB, Hkv, B, d = 8, 2, 16, 32
+    kc = rng.integers(0, 256, size=(NB, Hkv, B, d), dtype=np.uint8)
+    vc = rng.integers(0, 256, size=(NB, Hkv, B, d), dtype=np.uint8)
+    ks = rng.random((NB, Hkv)).astype(np.float32)
+    vs = rng.random((NB, Hkv)).astype(np.float32)
+    k0, v0, ks0, vs0 = kc.copy(), vc.copy(), ks.copy(), vs.copy()
+    pairs = np.array([[1, 5], [2, 6], [9, 0]], np.int32)  # the last one is out of the pool
+    err = oracle.swap_blocks_fp8(kc, vc, ks, vs, kc, vc, ks, vs, pairs)
+    assert err == oracle.ERR_BLOCK_OOB
+    for src, dst in ((1, 5), (2, 6)):
+        assert np.array_equal(kc[dst], k0[src]) and np.array_equal(vc[dst], v0[src])
+        assert np.array_equal(ks[dst], ks0[src]) and np.array_equal(vs[dst], vs0[src])
+    for b in (0, 1, 2, 3, 4, 7):
+        assert np.array_equal(kc[b], k0[b]) and np.array_equal(ks[b], ks0[b])
+
+
+def test_fp8_workload_step_is_finite_and_permutation_invariant():
+    w = wl.to_fp8(_small(dtype="bf16", Hq=4, Hkv=2, d=32, ctx=(1, 16, 17, 40, 77)), seed=5)
+    assert w.kv_dtype == "e4m3" and w.k_cache.dtype == np.uint8
+    _, _, base, err = oracle.step(w)
+    assert err == 0 and np.isfinite(base).all()
+    wp = wl.permute_physical(w, np.random.default_rng(64))
+    _, _, out, err = oracle.step(wp)
+    assert err == 0 and np.array_equal(out, base)
