@@ -53,7 +53,54 @@ WORKLOAD_TEXT = {
     "long_b128": "long context as long_b16 with 128-token blocks",
     "tiny": "tiny: 4 seqs, 4 heads, head_dim 64, fp32, block 16, context {1,17,33,50}, "
             "64-block pool",
+    "spec_verify": "speculative-decoding verification, LLaMA-7B-shaped: 64 seqs x 4 causal "
+                   "query tokens (kv_write of all 4, then attention of each over its prefix), "
+                   "32 q/kv heads, head_dim 128, fp16, block 16, context U[128,2048]",
+    "chunked_prefill": "chunked prefill: 8 seqs each append a 512-token prompt chunk (kv_write "
+                       "of 512 tokens, then causal attention of each) to U[0,3584] cached "
+                       "tokens; GQA 32 q / 8 kv heads, head_dim 128, bf16, block 16",
 }
+
+# fp32 FMA lanes per SM (sm_100 family): the SIMT path's arithmetic roofline is
+# SMs x 128 lanes x 2 flop x the maximum SM clock.
+FP32_LANES_PER_SM = 128
+
+
+def _alu_peak_tflops(sm_count):
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            mhz = float(json.load(f).get("sm_max_mhz", 2070.0))
+    except (OSError, ValueError):
+        mhz = 2070.0
+    return sm_count * FP32_LANES_PER_SM * 2 * mhz * 1e6 / 1e12
+
+
+def _rows(w):
+    """(sequence, row, tokens attended) for every query row of the step."""
+    out = []
+    if w.query_start is None:
+        for s in range(w.num_seqs):
+            out.append((s, s, max(0, int(w.context_lens[s]))))
+    else:
+        for s in range(w.num_seqs):
+            q0, q1 = int(w.query_start[s]), int(w.query_start[s + 1])
+            n = int(w.context_lens[s])
+            for i in range(q1 - q0):
+                out.append((s, q0 + i, n - (q1 - q0) + i + 1))
+    return out
+
+
+def _oracle_row(w, kc, vc, s, r, n):
+    """The oracle on one query row (all heads) of the step."""
+    import oracle
+    if w.query_start is None:
+        return oracle.decode(np.ascontiguousarray(w.q[r:r + 1]), kc, vc,
+                             np.ascontiguousarray(w.block_tables[s:s + 1]),
+                             np.ascontiguousarray(w.context_lens[s:s + 1]), scale=w.scale,
+                             dtype=w.dtype)
+    return oracle.multi_query(np.ascontiguousarray(w.q[r:r + 1]), np.array([0, 1], np.int32), kc,
+                              vc, np.ascontiguousarray(w.block_tables[s:s + 1]),
+                              np.array([n], np.int32), scale=w.scale, dtype=w.dtype)
 
 
 def _dist_env():
@@ -187,38 +234,35 @@ def _to_torch(a, dtype):
 
 
 def _cpu_baseline(w, cpu_seconds=16.0, max_wall_s=20.0):
-    """The oracle, as it stands, on this workload's decode on all host cores:
-    whole sequences in order, passes over the batch repeated until about
-    cpu_seconds of CPU work (threads x wall time) are done."""
+    """The oracle, as it stands, on this workload's attention on all host cores:
+    query rows (all heads) in order, passes repeated until about cpu_seconds
+    of CPU work (threads x wall time) are done.  GB/s-equivalent: the step's
+    K/V bytes x (tokens attended by the rows done / by all rows) / time."""
     import concurrent.futures as cf
-    import oracle
     threads = os.cpu_count() or 1
     kc, vc = w.k_cache, w.v_cache
-    done_bytes, n_seqs, t0 = 0, 0, time.perf_counter()
-    per_tok = 2 * w.num_kv_heads * w.head_dim * w.elem_bytes
+    rows = _rows(w)
+    total = max(1, sum(n for _, _, n in rows))
+    kv_bytes = w.kv_read_bytes()
+    done, n_rows, t0 = 0, 0, time.perf_counter()
     with cf.ThreadPoolExecutor(threads) as ex:
         while True:
             el = time.perf_counter() - t0
-            if n_seqs > 0 and (el * threads >= cpu_seconds or el >= max_wall_s):
+            if n_rows > 0 and (el * threads >= cpu_seconds or el >= max_wall_s):
                 break
-            first = n_seqs % w.num_seqs
-            seqs = list(range(first, min(w.num_seqs, first + threads)))
-
-            def one(s):
-                o, _ = oracle.decode(np.ascontiguousarray(w.q[s:s + 1]), kc, vc,
-                                     np.ascontiguousarray(w.block_tables[s:s + 1]),
-                                     np.ascontiguousarray(w.context_lens[s:s + 1]),
-                                     scale=w.scale, dtype=w.dtype)
-                return o
-
-            list(ex.map(one, seqs))
-            done_bytes += int(w.context_lens[seqs].clip(0).sum()) * per_tok
-            n_seqs += len(seqs)
+            first = n_rows % len(rows)
+            batch = rows[first:first + threads]
+            list(ex.map(lambda x: _oracle_row(w, kc, vc, *x), batch))
+            done += sum(n for _, _, n in batch)
+            n_rows += len(batch)
     dt = time.perf_counter() - t0
-    return {"value": done_bytes / dt / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
-            "sample": f"decode of {n_seqs} sequences ({n_seqs / w.num_seqs:.2f} passes over the "
-                      f"{w.num_seqs}-sequence batch of the same workload, {done_bytes / 1e6:.0f} MB"
-                      f" of K/V), fp64 C oracle, one sequence per host thread, {dt:.1f} s wall"}
+    eq = kv_bytes * done / total
+    unit = "sequences" if w.query_start is None else "query rows"
+    return {"value": eq / dt / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "sample": f"attention of {n_rows} {unit} ({n_rows / len(rows):.3f} passes over the "
+                      f"step's {len(rows)}; {eq / 1e6:.0f} MB of the step's K/V bytes in "
+                      f"proportion to the tokens attended), fp64 C oracle, one row per host "
+                      f"thread, {dt:.1f} s wall"}
 
 
 def run_gpu(args):
@@ -243,8 +287,15 @@ def run_gpu(args):
     if args.layout != "paged":
         kw["layout"] = args.layout
     w = wl.by_name(args.config, poison=False, **kw)
-    P = pa.decode_partition_tokens(w.num_q_heads, w.num_kv_heads, w.head_dim, w.max_blocks_per_seq,
-                                   w.block_size, w.dtype, w.partition_tokens)
+    mq = w.query_start is not None
+    if mq:
+        P = pa.multi_query_partition_tokens(w.num_query_tokens, w.num_q_heads, w.num_kv_heads,
+                                            w.head_dim, w.max_blocks_per_seq, w.block_size,
+                                            w.dtype, w.partition_tokens)
+    else:
+        P = pa.decode_partition_tokens(w.num_q_heads, w.num_kv_heads, w.head_dim,
+                                       w.max_blocks_per_seq, w.block_size, w.dtype,
+                                       w.partition_tokens)
     dt = w.dtype
     d = {k: v.to(dev) for k, v in {
         "q": _to_torch(w.q, dt), "k_cache": _to_torch(w.k_cache, dt),
@@ -252,9 +303,15 @@ def run_gpu(args):
         "v_new": _to_torch(w.v_new, dt), "block_tables": torch.from_numpy(w.block_tables),
         "context_lens": torch.from_numpy(w.context_lens),
         "slot_mapping": torch.from_numpy(w.slot_mapping),
-        "block_mapping": torch.from_numpy(w.block_mapping.reshape(-1, 2))}.items()}
+        "block_mapping": torch.from_numpy(w.block_mapping.reshape(-1, 2)),
+        **({"query_start": torch.from_numpy(w.query_start)} if mq else {})}.items()}
     out = torch.empty_like(d["q"])
-    workspace = pa.decode_workspace(d["q"], d["k_cache"], d["block_tables"], w.partition_tokens)
+    if mq:
+        workspace = pa.multi_query_workspace(d["q"], d["k_cache"], d["block_tables"],
+                                             w.partition_tokens)
+    else:
+        workspace = pa.decode_workspace(d["q"], d["k_cache"], d["block_tables"],
+                                        w.partition_tokens)
     d_err = torch.zeros(1, dtype=torch.int32, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
@@ -273,9 +330,14 @@ def run_gpu(args):
                         dd["slot_mapping"], d_err=d_err)
         if ev_mid is not None:
             ev_mid[1].record(stream)
-        pa.decode(out, dd["q"], dd["k_cache"], dd["v_cache"], dd["block_tables"],
-                  dd["context_lens"], w.scale, partition_tokens=w.partition_tokens,
-                  workspace=workspace, d_err=d_err)
+        if mq:
+            pa.multi_query(out, dd["q"], dd["query_start"], dd["k_cache"], dd["v_cache"],
+                           dd["block_tables"], dd["context_lens"], w.scale,
+                           partition_tokens=w.partition_tokens, workspace=workspace, d_err=d_err)
+        else:
+            pa.decode(out, dd["q"], dd["k_cache"], dd["v_cache"], dd["block_tables"],
+                      dd["context_lens"], w.scale, partition_tokens=w.partition_tokens,
+                      workspace=workspace, d_err=d_err)
 
     for _ in range(args.warmup):
         flush.zero_()
@@ -314,7 +376,7 @@ def run_gpu(args):
     # the output back to pinned host memory, every step.
     host_in = {k: d[k].cpu().pin_memory() for k in
                ("q", "k_new", "v_new", "slot_mapping", "block_tables", "context_lens",
-                "block_mapping")}
+                "block_mapping") + (("query_start",) if mq else ())}
     host_out = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
     h2d = sum(t.numel() * t.element_size() for t in host_in.values())
     d2h = host_out.numel() * host_out.element_size()
@@ -348,6 +410,41 @@ def run_gpu(args):
     peak, peak_kind = _peaks()
     achieved = kv_bytes / (dec_ms_avg * 1e-3) / 1e9
     seq_heads = w.num_seqs * w.num_q_heads
+    # attention flops: 2 d (q.K) + 2 d (P.V) per (query row, head, token attended)
+    flops = 4 * w.head_dim * w.num_q_heads * sum(n for _, _, n in _rows(w))
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    alu_peak = _alu_peak_tflops(sms)
+    kernel = "pa_multi_query (partition kernel + split-K merge)" if mq else \
+        "pa_decode (partition kernel + split-K merge)"
+    # The binding roofline: HBM for the K/V stream unless the SIMT arithmetic
+    # needs longer at its peak (many query rows per K/V byte).
+    tc_path = (not mq and w.dtype in ("f16", "bf16") and w.head_dim == 128
+               and 4 <= w.num_q_heads // w.num_kv_heads <= 16 and P % 128 == 0)
+    alu_bound = not tc_path and flops / (alu_peak * 1e12) > unique_bytes / (peak * 1e9)
+    if alu_bound:
+        ach = flops / (dec_ms_avg * 1e-3) / 1e12
+        roof = {"bound": "alu", "kernel": kernel, "achieved": round(ach, 3),
+                "peak": round(alu_peak, 1), "unit": "TFLOP/s", "frac": round(ach / alu_peak, 4),
+                "peak_source": f"derived: {sms} SMs x {FP32_LANES_PER_SM} fp32 FMA lanes x 2 "
+                               "flop x maximum SM clock (MEASURED_PEAKS sm_max_mhz)",
+                "flops": "4 x head_dim per (query row, head, token attended)",
+                "traffic": None, "algorithmic_flops_per_launch": int(flops),
+                "hbm_achieved_gbs": round(unique_bytes / (dec_ms_avg * 1e-3) / 1e9, 2),
+                "avg_launch_ms": round(dec_ms_avg, 5)}
+    else:
+        roof = {"bound": "hbm", "kernel": kernel,
+                "achieved": round(unique_bytes / (dec_ms_avg * 1e-3) / 1e9, 2), "peak": peak,
+                "unit": "GB/s",
+                "frac": round(unique_bytes / (dec_ms_avg * 1e-3) / 1e9 / peak, 4),
+                "peak_source": f"{peak_kind} hbm_gbs",
+                "bytes": "distinct K/V bytes read (shared prefix blocks once)"
+                         if unique_bytes != kv_bytes else "K/V bytes of the cached tokens",
+                "logical_achieved": round(achieved, 2),
+                "traffic": _ncu_traffic(args.config),
+                "algorithmic_bytes_per_launch": unique_bytes,
+                "logical_bytes_per_launch": kv_bytes,
+                "attn_tflops": round(flops / (dec_ms_avg * 1e-3) / 1e12, 3),
+                "avg_launch_ms": round(dec_ms_avg, 5)}
     if rank != 0:
         if dist is not None:
             dist.destroy_process_group()
@@ -363,24 +460,16 @@ def run_gpu(args):
                    "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim,
                    "block_size": w.block_size, "num_blocks": w.num_blocks,
                    "partition_tokens": P, "kv_read_bytes_per_step": kv_bytes,
+                   **({"query_tokens": w.num_query_tokens} if mq else {}),
                    "layout": w.meta.get("layout", "paged"),
                    "l2": "KV pool larger than L2 and a 256 MB L2 flush before every step "
                          "(outside the timed events)",
                    "parallelism": f"weak: {ws} independent replicas of the batch, one per GPU"},
         "seq_heads_per_s": round(ws * seq_heads / (ms_per_step * 1e-3), 1),
         "hbm_frac": round(value / ws / peak, 4),
-        "roofline": {"bound": "hbm", "kernel": "pa_decode (partition kernel + split-K merge)",
-                     "achieved": round(unique_bytes / (dec_ms_avg * 1e-3) / 1e9, 2), "peak": peak,
-                     "unit": "GB/s",
-                     "frac": round(unique_bytes / (dec_ms_avg * 1e-3) / 1e9 / peak, 4),
-                     "peak_source": f"{peak_kind} hbm_gbs",
-                     "bytes": "distinct K/V bytes read (shared prefix blocks once)"
-                              if unique_bytes != kv_bytes else "K/V bytes of the cached tokens",
-                     "logical_achieved": round(achieved, 2),
-                     "traffic": _ncu_traffic(args.config),
-                     "algorithmic_bytes_per_launch": unique_bytes,
-                     "logical_bytes_per_launch": kv_bytes,
-                     "avg_launch_ms": round(dec_ms_avg, 5)},
+        "roofline": roof,
+        **({"query_tokens_per_s": round(ws * w.num_query_tokens / (ms_per_step * 1e-3), 1)}
+           if mq else {}),
         "e2e": {"value": round(ws * kv_bytes / (e2e_avg * 1e-3) / 1e9, 2), "unit": "GB/s",
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                 "ms_per_step": round(e2e_avg, 5)},
@@ -421,19 +510,21 @@ def run_reference(args):
     w = wl.by_name(args.config, poison=False, **({"partition_tokens": args.partition}
                                                    if args.partition is not None else {}))
     threads = os.cpu_count() or 1
-    # each step: the oracle's copy_blocks and kv_write, then decode of a bounded
-    # sample of sequences (whole sequences, in order) spread over host threads
-    per_tok = 2 * w.num_kv_heads * w.head_dim * w.elem_bytes
-    cum = np.cumsum(np.clip(w.context_lens, 0, None).astype(np.int64) * per_tok)
+    # each step: the oracle's copy_blocks and kv_write, then attention of a
+    # bounded sample of query rows (all heads; whole sequences for decode), in
+    # order, spread over host threads.  Bytes: the step's K/V bytes in
+    # proportion to the tokens the sampled rows attend to.
+    rows = _rows(w)
+    total = max(1, sum(r[2] for r in rows))
+    kv_bytes = w.kv_read_bytes()
+    cum = np.cumsum([r[2] for r in rows]).astype(np.float64) * kv_bytes / total
     n = int(np.searchsorted(cum, args.reference_sample_bytes)) + 1
-    n = max(1, min(w.num_seqs, n))
+    n = max(1, min(len(rows), n))
     sample_bytes = int(cum[n - 1])
     kc, vc = w.k_cache, w.v_cache
 
-    def one(s):
-        oracle.decode(np.ascontiguousarray(w.q[s:s + 1]), kc, vc,
-                      np.ascontiguousarray(w.block_tables[s:s + 1]),
-                      np.ascontiguousarray(w.context_lens[s:s + 1]), scale=w.scale, dtype=w.dtype)
+    def one(i):
+        _oracle_row(w, kc, vc, *rows[i])
 
     times = []
     with cf.ThreadPoolExecutor(threads) as ex:
@@ -453,12 +544,13 @@ def run_reference(args):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
         "data": "synthetic (same seeded workload as the GPU arm)",
         "config": {"workload": WORKLOAD_TEXT.get(args.config, args.config), "name": args.config,
-                   "sample_seqs": n, "sample_kv_bytes": sample_bytes},
+                   "sample_rows": n, "sample_kv_bytes": sample_bytes},
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads,
                          "kind": "oracle",
-                         "sample": f"per step: oracle copy_blocks + kv_write + decode of the "
-                                   f"first {n} of {w.num_seqs} sequences ({sample_bytes / 1e6:.0f}"
-                                   f" MB of K/V), fp64 C oracle, {threads} host threads"},
+                         "sample": f"per step: oracle copy_blocks + kv_write + attention of the "
+                                   f"first {n} of {len(rows)} query rows ({sample_bytes / 1e6:.0f}"
+                                   f" MB of the step's K/V bytes in proportion to the tokens "
+                                   f"attended), fp64 C oracle, {threads} host threads"},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }

@@ -191,6 +191,49 @@ pa_status pa_decode(void* out, const void* q, const void* k_cache, const void* v
                     int partition_tokens, pa_dtype dtype, void* workspace,
                     size_t workspace_bytes, uint32_t* d_err, pa_stream_t stream);
 
+/* pa_multi_query -- paged attention for several query tokens per sequence
+ * (chunked prefill, speculative-decoding verification).
+ *
+ * Chunked prefill and speculative decoding are the steps beside paged decode
+ * ("PagedAttention 深度解析" §六 item 5).  Their new tokens' K/V are written
+ * into the sequence's blocks first (pa_kv_write with one slot per token;
+ * kwkr.cn "vLLM PagedAttention 技术深度解析" §1.2.2), so context_lens[s] counts
+ * them, and then each new token is a query over the same block table:
+ *   L_s = query_start[s+1] - query_start[s]   queries of sequence s, the last
+ *                                             L_s of its n = context_lens[s] tokens
+ *   row r = query_start[s] + i (i < L_s) sits at position n - L_s + i and
+ *   out[r][h] = softmax(scale * q[r][h] . K^T) . V over tokens 0 .. n-L_s+i
+ *   (causal: itself and everything before it), K/V gathered as in pa_decode.
+ * q, out: [num_query_tokens][num_q_heads][head_dim], dtype `dtype`, 16-byte
+ * aligned.  query_start: device int32 [num_seqs + 1], ascending, within
+ * [0, num_query_tokens]; rows no sequence claims are not written.  A
+ * sequence with L_s > n, or n outside [0, max_blocks_per_seq*block_size],
+ * gets zero rows and PA_DERR_CTX_OOB; a descending query_start is flagged
+ * PA_DERR_CTX_OOB and the rows it would place are skipped.  Bad block ids:
+ * as pa_decode.  The work is tiled as (kv head, up to 8 query rows of one or
+ * more consecutive query tokens, partition), so the K/V of a tile is read
+ * once for all its rows.  Partitions: pa_multi_query_partition_tokens();
+ * workspace: pa_multi_query_workspace_size() bytes, with the same rules as
+ * pa_decode's.  Supported sizes and accumulation: as pa_decode.
+ */
+int pa_multi_query_partition_tokens(int num_query_tokens, int num_q_heads, int num_kv_heads,
+                                    int head_dim, int max_blocks_per_seq, int block_size,
+                                    pa_dtype dtype, int partition_tokens);
+/* 256 bytes of counters plus num_query_tokens * num_q_heads * partitions *
+ * (head_dim + 2) floats when a sequence can span more than one partition.
+ * The default partitions (partition_tokens = 0) are 512 tokens, doubled
+ * until those partial states fit in 256 MiB. */
+size_t pa_multi_query_workspace_size(int num_query_tokens, int num_q_heads, int num_kv_heads,
+                                     int head_dim, int max_blocks_per_seq, int block_size,
+                                     pa_dtype dtype, int partition_tokens);
+pa_status pa_multi_query(void* out, const void* q, int num_query_tokens,
+                         const int32_t* query_start, const void* k_cache, const void* v_cache,
+                         const int32_t* block_tables, int max_blocks_per_seq,
+                         const int32_t* context_lens, int num_seqs, int num_q_heads,
+                         int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                         float scale, int partition_tokens, pa_dtype dtype, void* workspace,
+                         size_t workspace_bytes, uint32_t* d_err, pa_stream_t stream);
+
 /* pa_decode_static_workspace -- pa_decode for callers that cannot allocate.
  *
  * The pages have no counterpart to this call: it exists for callers that must

@@ -29,7 +29,8 @@ DERR_MAPPING_CONFLICT = 16
 DTYPE_CODE = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}
 EXPORTED = ("pa_abi_version", "pa_status_string", "pa_kv_write", "pa_copy_blocks", "pa_swap_blocks",
             "pa_copy_blocks_check", "pa_decode_partition_tokens", "pa_decode_workspace_size",
-            "pa_decode", "pa_decode_static_workspace", "pa_selftest_wait_timeout")
+            "pa_decode", "pa_decode_static_workspace", "pa_multi_query_partition_tokens",
+            "pa_multi_query_workspace_size", "pa_multi_query", "pa_selftest_wait_timeout")
 
 _lock = threading.Lock()
 _lib: Optional[ctypes.CDLL] = None
@@ -78,6 +79,13 @@ def load() -> ctypes.CDLL:
         lib.pa_decode.restype = i32
         lib.pa_decode.argtypes = [vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, i32,
                                   ctypes.c_float, i32, i32, vp, u64, vp, vp]
+        lib.pa_multi_query_partition_tokens.restype = i32
+        lib.pa_multi_query_partition_tokens.argtypes = [i32, i32, i32, i32, i32, i32, i32, i32]
+        lib.pa_multi_query_workspace_size.restype = u64
+        lib.pa_multi_query_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32, i32, i32]
+        lib.pa_multi_query.restype = i32
+        lib.pa_multi_query.argtypes = [vp, vp, i32, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32,
+                                       i32, i32, ctypes.c_float, i32, i32, vp, u64, vp, vp]
         _lib = lib
         return lib
 
@@ -247,4 +255,64 @@ def decode(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor, v_cache: t
                           int(partition_tokens), DTYPE_CODE[q.dtype], _ptr(workspace), ws_bytes,
                           _ptr(d_err), _stream(stream, q.device))
     _check(st, "pa_decode")
+    return out
+
+
+def multi_query_partition_tokens(num_query_tokens: int, num_q_heads: int, num_kv_heads: int,
+                                 head_dim: int, max_blocks_per_seq: int, block_size: int, dtype,
+                                 partition_tokens: int = 0) -> int:
+    """Tokens per split-K partition pa_multi_query uses."""
+    return int(load().pa_multi_query_partition_tokens(num_query_tokens, num_q_heads, num_kv_heads,
+                                                      head_dim, max_blocks_per_seq, block_size,
+                                                      _dtype_code(dtype), partition_tokens))
+
+
+def multi_query_workspace_size(num_query_tokens: int, num_q_heads: int, num_kv_heads: int,
+                               head_dim: int, max_blocks_per_seq: int, block_size: int, dtype,
+                               partition_tokens: int = 0) -> int:
+    return int(load().pa_multi_query_workspace_size(num_query_tokens, num_q_heads, num_kv_heads,
+                                                    head_dim, max_blocks_per_seq, block_size,
+                                                    _dtype_code(dtype), partition_tokens))
+
+
+def multi_query_workspace(q: torch.Tensor, k_cache: torch.Tensor, block_tables: torch.Tensor,
+                          partition_tokens: int = 0) -> torch.Tensor:
+    """Zero-filled workspace (allocated with torch) for pa_multi_query at these shapes."""
+    Tq, Hq, d = q.shape
+    n = multi_query_workspace_size(Tq, Hq, k_cache.shape[1], d, block_tables.shape[1],
+                                   k_cache.shape[2], q.dtype, partition_tokens)
+    return torch.zeros(n, dtype=torch.uint8, device=q.device)
+
+
+def multi_query(out: torch.Tensor, q: torch.Tensor, query_start: torch.Tensor,
+                k_cache: torch.Tensor, v_cache: torch.Tensor, block_tables: torch.Tensor,
+                context_lens: torch.Tensor, scale: float, partition_tokens: int = 0,
+                workspace: Optional[torch.Tensor] = None, d_err: Optional[torch.Tensor] = None,
+                stream=None) -> torch.Tensor:
+    """Causal paged attention of several query tokens per sequence: row
+    query_start[s] + i attends to tokens 0 .. context_lens[s] - L_s + i."""
+    for n, t in (("out", out), ("q", q), ("query_start", query_start), ("k_cache", k_cache),
+                 ("v_cache", v_cache), ("block_tables", block_tables),
+                 ("context_lens", context_lens)):
+        _cuda_contig(n, t)
+    if (block_tables.dtype != torch.int32 or context_lens.dtype != torch.int32
+            or query_start.dtype != torch.int32):
+        raise ValueError("block_tables, context_lens and query_start must be int32")
+    Tq, Hq, d = q.shape
+    NB, Hkv, B, d2 = k_cache.shape
+    S = context_lens.shape[0]
+    if query_start.shape != (S + 1,):
+        raise ValueError("query_start must have num_seqs + 1 entries")
+    if d2 != d or out.shape != q.shape or out.dtype != q.dtype or k_cache.dtype != q.dtype:
+        raise ValueError("q, out, k_cache and v_cache must agree in head_dim and dtype")
+    MB = block_tables.shape[1]
+    if workspace is None:
+        workspace = multi_query_workspace(q, k_cache, block_tables, partition_tokens)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    st = load().pa_multi_query(_ptr(out), _ptr(q), Tq, _ptr(query_start), _ptr(k_cache),
+                               _ptr(v_cache), _ptr(block_tables), MB, _ptr(context_lens), S, Hq,
+                               Hkv, d, B, NB, float(scale), int(partition_tokens),
+                               DTYPE_CODE[q.dtype], _ptr(workspace), ws_bytes, _ptr(d_err),
+                               _stream(stream, q.device))
+    _check(st, "pa_multi_query")
     return out

@@ -115,13 +115,138 @@ extern "C" size_t pa_decode_workspace_size(int num_seqs, int num_q_heads, int nu
         .bytes;
 }
 
-extern "C" pa_status pa_decode(void* out, const void* q, const void* k_cache, const void* v_cache,
-                               const int32_t* block_tables, int max_blocks_per_seq,
-                               const int32_t* context_lens, int num_seqs, int num_q_heads,
-                               int num_kv_heads, int head_dim, int block_size, int num_blocks,
-                               float scale, int partition_tokens, pa_dtype dtype, void* workspace,
-                               size_t workspace_bytes, uint32_t* d_err, pa_stream_t stream) {
-    using namespace pa;
+namespace pa {
+namespace {
+
+// Default partitions of the multi-query call: 512 tokens, doubled while the
+// partial states of all query rows would exceed 256 MiB.
+constexpr size_t kMultiQueryPartialBudget = 256u << 20;
+
+int multi_query_partition_tokens(int num_query_tokens, int num_q_heads, int head_dim,
+                                 int max_blocks_per_seq, int block_size, int partition_tokens) {
+    if (max_blocks_per_seq <= 0 || !block_size_ok(block_size) || partition_tokens < 0 ||
+        num_query_tokens < 0 || num_q_heads <= 0 || head_dim <= 0)
+        return -1;
+    if (partition_tokens > 0) return partition_tokens % block_size == 0 ? partition_tokens : -1;
+    const long long max_ctx = static_cast<long long>(max_blocks_per_seq) * block_size;
+    long long P = (kDefaultPartitionTokens + block_size - 1) / block_size * block_size;
+    while (P < max_ctx) {
+        const long long parts = (max_ctx + P - 1) / P;
+        const double bytes = static_cast<double>(num_query_tokens) * num_q_heads * parts * (head_dim + 2) * 4.0;
+        if (bytes <= static_cast<double>(kMultiQueryPartialBudget)) break;
+        P = (2 * P + block_size - 1) / block_size * block_size;
+    }
+    return static_cast<int>(P < 0x7fffffffLL ? P : 0x7fffffffLL / block_size * block_size);
+}
+
+struct AttnCall {
+    void* out;
+    const void* q;
+    const int32_t* query_start;  // null: one query per sequence
+    int num_query_tokens;
+    const void* k_cache;
+    const void* v_cache;
+    const int32_t* block_tables;
+    int max_blocks_per_seq;
+    const int32_t* context_lens;
+    int num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks;
+    float scale;
+    int partition_tokens;  // resolved, > 0
+    pa_dtype dtype;
+    void* workspace;
+    size_t workspace_bytes;
+    uint32_t* d_err;
+    pa_stream_t stream;
+};
+
+int log2_exact(int x) {
+    int r = 0;
+    while ((1 << r) < x) ++r;
+    return r;
+}
+
+// Shared by pa_decode and pa_multi_query once the arguments are checked.
+pa_status run_attention(const AttnCall& a) {
+    const int P = a.partition_tokens;
+    const int max_parts = max_parts_for(a.max_blocks_per_seq, a.block_size, P);
+    const WsLayout ws = ws_layout(a.num_query_tokens, a.num_q_heads, a.head_dim, max_parts);
+    if (a.workspace == nullptr) return PA_ERR_INVALID_ARG;
+    if (a.workspace_bytes < ws.bytes) return PA_ERR_WORKSPACE_TOO_SMALL;
+    if ((reinterpret_cast<uintptr_t>(a.workspace) & 255u) != 0) return PA_ERR_INVALID_ARG;
+    const int group = a.num_q_heads / a.num_kv_heads;
+    const int heads = head_tile(group);
+    int tokens = 1;  // query tokens per work item: fill a tile of up to 8 rows
+    if (a.query_start != nullptr && a.num_seqs > 0) {
+        const long long avg = (static_cast<long long>(a.num_query_tokens) + a.num_seqs - 1) / a.num_seqs;
+        while (tokens * 2 * heads <= 8 && tokens < avg) tokens *= 2;
+    }
+
+    DecodeParams p;
+    p.out = a.out;
+    p.q = a.q;
+    p.k_cache = static_cast<const unsigned char*>(a.k_cache);
+    p.v_cache = static_cast<const unsigned char*>(a.v_cache);
+    p.block_tables = a.block_tables;
+    p.context_lens = a.context_lens;
+    p.query_start = a.query_start;
+    unsigned char* wsb = static_cast<unsigned char*>(a.workspace);
+    p.counters = reinterpret_cast<unsigned int*>(wsb);
+    p.ws_m = max_parts > 1 ? reinterpret_cast<float*>(wsb + ws.m_off) : nullptr;
+    p.ws_l = max_parts > 1 ? reinterpret_cast<float*>(wsb + ws.l_off) : nullptr;
+    p.ws_o = max_parts > 1 ? reinterpret_cast<float*>(wsb + ws.o_off) : nullptr;
+    p.d_err = a.d_err;
+    p.num_seqs = a.num_seqs;
+    p.num_q_heads = a.num_q_heads;
+    p.num_kv_heads = a.num_kv_heads;
+    p.num_query_tokens = a.num_query_tokens;
+    p.group = group;
+    p.tile_heads = heads;
+    p.tile_heads_log2 = log2_exact(heads);
+    p.tile_tokens = tokens;
+    p.head_tiles = a.num_q_heads / heads;
+    p.max_blocks_per_seq = a.max_blocks_per_seq;
+    p.block_size = a.block_size;
+    p.num_blocks = a.num_blocks;
+    p.partition_tokens = P;
+    p.max_parts = max_parts;
+    p.qk_scale_log2 = a.scale * 1.4426950408889634f;  // log2(e)
+
+    const cudaStream_t st = as_cuda(a.stream);
+    // Grouped-query decode with 16-bit K/V and head_dim 128: the tensor-core path.
+    const long long pool_rows = static_cast<long long>(a.num_blocks) * a.num_kv_heads * a.block_size;
+    if (a.query_start == nullptr && tc_shape(a.num_q_heads, a.num_kv_heads, a.head_dim, a.dtype) &&
+        P % 128 == 0 && pool_rows < 0x7fffffffLL) {
+        CUtensorMap map_k, map_v;
+        if (make_pool_map(&map_k, a.k_cache, pool_rows, a.dtype) &&
+            make_pool_map(&map_v, a.v_cache, pool_rows, a.dtype)) {
+            p.head_tiles = a.num_kv_heads;
+            return a.dtype == PA_BF16 ? launch_decode_tc_bf16(p, map_k, map_v, st)
+                                      : launch_decode_tc_f16(p, map_k, map_v, st);
+        }
+    }
+    const int gt = heads * tokens;
+    if (a.query_start != nullptr) {
+        switch (a.dtype) {
+            case PA_F32: return launch_multi_query_f32(p, a.head_dim, gt, st);
+            case PA_F16: return launch_multi_query_f16(p, a.head_dim, gt, st);
+            case PA_BF16: return launch_multi_query_bf16(p, a.head_dim, gt, st);
+        }
+        return PA_ERR_INVALID_ARG;
+    }
+    switch (a.dtype) {
+        case PA_F32: return launch_decode_f32(p, a.head_dim, gt, st);
+        case PA_F16: return launch_decode_f16(p, a.head_dim, gt, st);
+        case PA_BF16: return launch_decode_bf16(p, a.head_dim, gt, st);
+    }
+    return PA_ERR_INVALID_ARG;
+}
+
+// Checks shared by both calls; returns PA_OK or the error to report.
+pa_status check_attention(const void* out, const void* q, const void* k_cache, const void* v_cache,
+                          const int32_t* block_tables, int max_blocks_per_seq,
+                          const int32_t* context_lens, int num_seqs, int num_q_heads,
+                          int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                          float scale, int partition_tokens, pa_dtype dtype) {
     if (!valid_dtype(dtype)) return PA_ERR_INVALID_ARG;
     if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 ||
         block_size <= 0 || num_blocks <= 0 || max_blocks_per_seq <= 0 || partition_tokens < 0)
@@ -131,65 +256,90 @@ extern "C" pa_status pa_decode(void* out, const void* q, const void* k_cache, co
     if (!block_size_ok(block_size)) return PA_ERR_UNSUPPORTED;
     if (static_cast<long long>(max_blocks_per_seq) * block_size > 0x7fffffffLL)
         return PA_ERR_INVALID_ARG;
-    const int P = pa_decode_partition_tokens(num_q_heads, num_kv_heads, head_dim,
-                                             max_blocks_per_seq, block_size, dtype, partition_tokens);
-    if (P <= 0) return PA_ERR_INVALID_ARG;
     if (num_seqs == 0) return PA_OK;
     if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens)
         return PA_ERR_INVALID_ARG;
     if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache))
         return PA_ERR_INVALID_ARG;
+    return PA_OK;
+}
 
-    const int max_parts = max_parts_for(max_blocks_per_seq, block_size, P);
-    const WsLayout ws = ws_layout(num_seqs, num_q_heads, head_dim, max_parts);
-    if (workspace == nullptr) return PA_ERR_INVALID_ARG;
-    if (workspace_bytes < ws.bytes) return PA_ERR_WORKSPACE_TOO_SMALL;
-    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return PA_ERR_INVALID_ARG;
-    const int group = num_q_heads / num_kv_heads;
-    const int gt = head_tile(group);
+}  // namespace
+}  // namespace pa
 
-    DecodeParams p;
-    p.out = out;
-    p.q = q;
-    p.k_cache = static_cast<const unsigned char*>(k_cache);
-    p.v_cache = static_cast<const unsigned char*>(v_cache);
-    p.block_tables = block_tables;
-    p.context_lens = context_lens;
-    unsigned char* wsb = static_cast<unsigned char*>(workspace);
-    p.counters = reinterpret_cast<unsigned int*>(wsb);
-    p.ws_m = max_parts > 1 ? reinterpret_cast<float*>(wsb + ws.m_off) : nullptr;
-    p.ws_l = max_parts > 1 ? reinterpret_cast<float*>(wsb + ws.l_off) : nullptr;
-    p.ws_o = max_parts > 1 ? reinterpret_cast<float*>(wsb + ws.o_off) : nullptr;
-    p.d_err = d_err;
-    p.num_seqs = num_seqs;
-    p.num_q_heads = num_q_heads;
-    p.num_kv_heads = num_kv_heads;
-    p.group = group;
-    p.head_tiles = num_q_heads / gt;
-    p.max_blocks_per_seq = max_blocks_per_seq;
-    p.block_size = block_size;
-    p.num_blocks = num_blocks;
-    p.partition_tokens = P;
-    p.max_parts = max_parts;
-    p.qk_scale_log2 = scale * 1.4426950408889634f;  // log2(e)
+extern "C" pa_status pa_decode(void* out, const void* q, const void* k_cache, const void* v_cache,
+                               const int32_t* block_tables, int max_blocks_per_seq,
+                               const int32_t* context_lens, int num_seqs, int num_q_heads,
+                               int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                               float scale, int partition_tokens, pa_dtype dtype, void* workspace,
+                               size_t workspace_bytes, uint32_t* d_err, pa_stream_t stream) {
+    using namespace pa;
+    const pa_status c = check_attention(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq,
+                                        context_lens, num_seqs, num_q_heads, num_kv_heads,
+                                        head_dim, block_size, num_blocks, scale, partition_tokens,
+                                        dtype);
+    if (c != PA_OK) return c;
+    const int P = pa_decode_partition_tokens(num_q_heads, num_kv_heads, head_dim,
+                                             max_blocks_per_seq, block_size, dtype, partition_tokens);
+    if (P <= 0) return PA_ERR_INVALID_ARG;
+    if (num_seqs == 0) return PA_OK;
+    if (static_cast<long long>(num_seqs) * num_q_heads > 0x7fffffffLL) return PA_ERR_UNSUPPORTED;
+    const AttnCall a{out, q, nullptr, num_seqs, k_cache, v_cache, block_tables, max_blocks_per_seq,
+                     context_lens, num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                     num_blocks, scale, P, dtype, workspace, workspace_bytes, d_err, stream};
+    return run_attention(a);
+}
 
-    const cudaStream_t st = as_cuda(stream);
-    // Grouped-query heads with 16-bit K/V and head_dim 128: the tensor-core path.
-    const long long pool_rows = static_cast<long long>(num_blocks) * num_kv_heads * block_size;
-    if (tc_shape(num_q_heads, num_kv_heads, head_dim, dtype) && P % 128 == 0 &&
-        pool_rows < 0x7fffffffLL) {
-        CUtensorMap map_k, map_v;
-        if (make_pool_map(&map_k, k_cache, pool_rows, dtype) &&
-            make_pool_map(&map_v, v_cache, pool_rows, dtype)) {
-            p.head_tiles = num_kv_heads;
-            return dtype == PA_BF16 ? launch_decode_tc_bf16(p, map_k, map_v, st)
-                                    : launch_decode_tc_f16(p, map_k, map_v, st);
-        }
-    }
-    switch (dtype) {
-        case PA_F32: return launch_decode_f32(p, head_dim, gt, st);
-        case PA_F16: return launch_decode_f16(p, head_dim, gt, st);
-        case PA_BF16: return launch_decode_bf16(p, head_dim, gt, st);
-    }
-    return PA_ERR_INVALID_ARG;
+extern "C" int pa_multi_query_partition_tokens(int num_query_tokens, int num_q_heads,
+                                               int num_kv_heads, int head_dim,
+                                               int max_blocks_per_seq, int block_size,
+                                               pa_dtype dtype, int partition_tokens) {
+    (void)num_kv_heads;
+    (void)dtype;
+    return pa::multi_query_partition_tokens(num_query_tokens, num_q_heads, head_dim,
+                                            max_blocks_per_seq, block_size, partition_tokens);
+}
+
+extern "C" size_t pa_multi_query_workspace_size(int num_query_tokens, int num_q_heads,
+                                                int num_kv_heads, int head_dim,
+                                                int max_blocks_per_seq, int block_size,
+                                                pa_dtype dtype, int partition_tokens) {
+    using namespace pa;
+    const int P = pa_multi_query_partition_tokens(num_query_tokens, num_q_heads, num_kv_heads,
+                                                  head_dim, max_blocks_per_seq, block_size, dtype,
+                                                  partition_tokens);
+    if (P <= 0) return 0;
+    return ws_layout(num_query_tokens, num_q_heads, head_dim,
+                     max_parts_for(max_blocks_per_seq, block_size, P))
+        .bytes;
+}
+
+extern "C" pa_status pa_multi_query(void* out, const void* q, int num_query_tokens,
+                                    const int32_t* query_start, const void* k_cache,
+                                    const void* v_cache, const int32_t* block_tables,
+                                    int max_blocks_per_seq, const int32_t* context_lens,
+                                    int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                                    int block_size, int num_blocks, float scale,
+                                    int partition_tokens, pa_dtype dtype, void* workspace,
+                                    size_t workspace_bytes, uint32_t* d_err, pa_stream_t stream) {
+    using namespace pa;
+    if (num_query_tokens < 0) return PA_ERR_INVALID_ARG;
+    const pa_status c = check_attention(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq,
+                                        context_lens, num_seqs, num_q_heads, num_kv_heads,
+                                        head_dim, block_size, num_blocks, scale, partition_tokens,
+                                        dtype);
+    if (c != PA_OK) return c;
+    const int P = pa_multi_query_partition_tokens(num_query_tokens, num_q_heads, num_kv_heads,
+                                                  head_dim, max_blocks_per_seq, block_size, dtype,
+                                                  partition_tokens);
+    if (P <= 0) return PA_ERR_INVALID_ARG;
+    if (num_seqs == 0 || num_query_tokens == 0) return PA_OK;
+    if (query_start == nullptr) return PA_ERR_INVALID_ARG;
+    if (static_cast<long long>(num_query_tokens) * num_q_heads > 0x7fffffffLL)
+        return PA_ERR_UNSUPPORTED;
+    const AttnCall a{out, q, query_start, num_query_tokens, k_cache, v_cache, block_tables,
+                     max_blocks_per_seq, context_lens, num_seqs, num_q_heads, num_kv_heads,
+                     head_dim, block_size, num_blocks, scale, P, dtype, workspace,
+                     workspace_bytes, d_err, stream};
+    return run_attention(a);
 }

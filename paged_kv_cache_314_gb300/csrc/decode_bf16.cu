@@ -5,7 +5,7 @@
 
 namespace pa {
 pa_status launch_decode_bf16(const DecodeParams& p, int head_dim, int gt, cudaStream_t stream) {
-    return launch_decode_typed<__nv_bfloat16>(p, head_dim, gt, stream);
+    return launch_decode_typed<__nv_bfloat16, false>(p, head_dim, gt, stream);
 }
 pa_status launch_decode_tc_bf16(const DecodeParams& p, const CUtensorMap& mapK,
                                const CUtensorMap& mapV, cudaStream_t stream) {

@@ -5,7 +5,7 @@
 
 namespace pa {
 pa_status launch_decode_f16(const DecodeParams& p, int head_dim, int gt, cudaStream_t stream) {
-    return launch_decode_typed<__half>(p, head_dim, gt, stream);
+    return launch_decode_typed<__half, false>(p, head_dim, gt, stream);
 }
 pa_status launch_decode_tc_f16(const DecodeParams& p, const CUtensorMap& mapK,
                                const CUtensorMap& mapV, cudaStream_t stream) {

@@ -62,16 +62,22 @@ struct DecodeParams {
     const unsigned char* v_cache;
     const int32_t* block_tables;
     const int32_t* context_lens;
+    const int32_t* query_start;  // [S+1] queries of sequence s: rows query_start[s] ..
+                                 // query_start[s+1]-1; null: one query per sequence (row s)
     unsigned int* counters;  // [0] next work item, [1] CTAs finished (both zero between calls)
-    float* ws_m;  // [S][Hq][max_parts] running max (log2 domain) per partition
-    float* ws_l;  // [S][Hq][max_parts] running sum per partition
-    float* ws_o;  // [S][Hq][max_parts][D] unnormalised output per partition
+    float* ws_m;  // [rows][Hq][max_parts] running max (log2 domain) per partition
+    float* ws_l;  // [rows][Hq][max_parts] running sum per partition
+    float* ws_o;  // [rows][Hq][max_parts][D] unnormalised output per partition
     uint32_t* d_err;
     int num_seqs;
     int num_q_heads;
     int num_kv_heads;
-    int group;       // query heads per kv head
-    int head_tiles;  // num_q_heads / GT
+    int num_query_tokens;  // rows of q and out (num_seqs when query_start is null)
+    int group;             // query heads per kv head
+    int head_tiles;        // num_q_heads / tile_heads
+    int tile_heads;        // query heads of one kv head in a work item (power of two)
+    int tile_heads_log2;
+    int tile_tokens;       // query tokens in a work item; tile_heads * tile_tokens = GT
     int max_blocks_per_seq;
     int block_size;
     int num_blocks;
@@ -86,6 +92,9 @@ __host__ __device__ constexpr int align16(int x) { return (x + 15) / 16 * 16; }
 constexpr uint32_t kStageFirst = 1u;  // first stage of its item for the consuming warp
 constexpr uint32_t kStageLast = 2u;   // last stage of its item for the consuming warp
 constexpr uint32_t kStageEnd = 4u;    // no more work: the consuming warp leaves
+constexpr uint32_t kStageCausal = 8u;  // some query row's causal limit ends inside the stage;
+                                       // bits 8..15: that limit of the item's first query
+                                       // token minus the stage's first token (int8, clamped)
 
 struct StageMeta {
     uint64_t mask;      // bit i: token i of the stage is valid
@@ -94,14 +103,14 @@ struct StageMeta {
 };
 
 struct ItemRec {
-    int s;           // sequence
+    int row0;        // q / out row of the item's first query token
     int hq0;         // first query head of the tile
     int part;        // partition index
     int nparts;      // partitions of the sequence; 0 = context length out of range
     int first_warp;  // warp of the item's first stage
     int nwarps;      // warps that take part (min(stages, 4))
     int done;        // warps finished with the item
-    int pad;
+    int ntok;        // query tokens of the item (<= tile_tokens)
 };
 
 template <typename T, int D, int GT>
@@ -174,10 +183,50 @@ __device__ __forceinline__ int items_of(int ctx, int max_ctx, int P) {
     return ctx == 0 ? 1 : (ctx + P - 1) / P;
 }
 
-// One stage (kTps tokens) of one consumer warp.  kFull: every token valid.
+// A sequence's queries and how many work items it has.  One query per
+// sequence: row s, context tokens 0..ctx-1.  Several: rows q0..q1-1 are the
+// last L = q1-q0 of the ctx tokens, query i seeing tokens 0..ctx-L+i.
+struct SeqQueries {
+    int ctx, q0, q1;
+    bool multi;  // several queries per sequence: they must fit in the context
+    __device__ __forceinline__ bool rows_ok(int num_rows) const {
+        return q0 >= 0 && q1 >= q0 && q1 <= num_rows;
+    }
+    __device__ __forceinline__ bool ctx_ok(int max_ctx) const {
+        return ctx >= 0 && ctx <= max_ctx && (!multi || q1 - q0 <= ctx);
+    }
+};
+
+__device__ __forceinline__ SeqQueries seq_queries(const DecodeParams& p, int s) {
+    SeqQueries r;
+    r.ctx = __ldg(p.context_lens + s);
+    r.multi = p.query_start != nullptr;
+    if (!r.multi) {
+        r.q0 = s;
+        r.q1 = s + 1;
+    } else {
+        r.q0 = __ldg(p.query_start + s);
+        r.q1 = __ldg(p.query_start + s + 1);
+    }
+    return r;
+}
+
+// Items of one sequence: head tiles x query-token tiles x partitions.  A
+// sequence whose context is out of range (or shorter than its queries) has
+// one item per tile, which writes zero rows.
+__device__ __forceinline__ int seq_items(const SeqQueries& q, const DecodeParams& p, int max_ctx) {
+    if (!q.rows_ok(p.num_query_tokens) || q.q1 == q.q0) return 0;
+    const int ntt = (q.q1 - q.q0 + p.tile_tokens - 1) / p.tile_tokens;
+    const int np = q.ctx_ok(max_ctx) ? items_of(q.ctx, max_ctx, p.partition_tokens) : 1;
+    return p.head_tiles * ntt * np;
+}
+
+// One stage (kTps tokens) of one consumer warp.  kFull: every token valid
+// for every row.  mask: tokens holding data; rmask[j]: tokens row j attends to.
 template <typename T, int D, int GT, bool kFull>
 __device__ __forceinline__ void decode_stage(const unsigned char* sK, const unsigned char* sV,
-                                             uint64_t mask, const float (&qf)[GT][16 / sizeof(T)],
+                                             uint64_t mask, const uint64_t (&rmask)[GT],
+                                             const float (&qf)[GT][16 / sizeof(T)],
                                              float (&m)[GT], float (&l)[GT],
                                              float (&o)[GT][16 / sizeof(T)], float* pw, int grp,
                                              int lig) {
@@ -209,7 +258,7 @@ __device__ __forceinline__ void decode_stage(const unsigned char* sK, const unsi
         for (int i = 0; i < C::kVals; ++i) {
             const int ps = kPasses >= kLpt ? lig * C::kVals + i : lig / C::kDup;
             const int ti = ps * kTpp + grp;
-            xv[i] = (kFull || ((mask >> ti) & 1ull)) ? x[j][i] : -INFINITY;
+            xv[i] = (kFull || ((rmask[j] >> ti) & 1ull)) ? x[j][i] : -INFINITY;
             mx = fmaxf(mx, xv[i]);
         }
 #pragma unroll
@@ -265,7 +314,9 @@ __device__ __forceinline__ void decode_stage(const unsigned char* sK, const unsi
 }
 
 
-template <typename T, int D, int GT>
+// kMulti: several query tokens per sequence (query_start given); false
+// compiles the one-query-per-sequence decode without any of that logic.
+template <typename T, int D, int GT, bool kMulti>
 __device__ __forceinline__ void decode_produce(const DecodeParams& p, unsigned char* smem) {
     using C = DecodeTile<T, D, GT>;
     constexpr int W = C::kConsumerWarps;
@@ -286,9 +337,22 @@ __device__ __forceinline__ void decode_produce(const DecodeParams& p, unsigned c
     const size_t block_bytes = static_cast<size_t>(p.num_kv_heads) * head_bytes;
 
     // Cursor over the sequence-major item numbering: base = items of all
-    // sequences before s_cur; lanes hold context_lens[win0 + lane].
+    // sequences before s_cur; lane l holds sequence win0 + l and its item count.
     int s_cur = 0, base = 0, win0 = 0;
-    int ctx_lane = lane < S ? __ldg(p.context_lens + lane) : 0;
+    SeqQueries sq_lane{0, 0, 0, kMulti};
+    int items_lane = 0;
+    auto load_window = [&]() {
+        const int sl = win0 + lane;
+        if constexpr (kMulti) {
+            sq_lane = sl < S ? seq_queries(p, sl) : SeqQueries{0, 0, 0, true};
+            items_lane = sl < S ? seq_items(sq_lane, p, max_ctx) : 0;
+            if (sl < S && !sq_lane.rows_ok(p.num_query_tokens)) report(p.d_err, PA_DERR_CTX_OOB);
+        } else {
+            sq_lane.ctx = sl < S ? __ldg(p.context_lens + sl) : 0;
+            items_lane = sl < S ? HT * items_of(sq_lane.ctx, max_ctx, P) : 0;
+        }
+    };
+    load_window();
     int c = 0;         // stages issued by this CTA
     int item_seq = 0;  // items taken by this CTA
     int q_issued = 0;  // items whose query rows were requested
@@ -304,10 +368,10 @@ __device__ __forceinline__ void decode_produce(const DecodeParams& p, unsigned c
         while (s_cur < S) {
             if (s_cur - win0 >= 32) {
                 win0 = s_cur;
-                ctx_lane = win0 + lane < S ? __ldg(p.context_lens + win0 + lane) : 0;
+                load_window();
             }
             const int sl = win0 + lane;
-            const int cnt = (sl >= s_cur && sl < S) ? HT * items_of(ctx_lane, max_ctx, P) : 0;
+            const int cnt = (sl >= s_cur && sl < S) ? items_lane : 0;
             int incl = cnt;
 #pragma unroll
             for (int off = 1; off < 32; off <<= 1) {
@@ -332,16 +396,40 @@ __device__ __forceinline__ void decode_produce(const DecodeParams& p, unsigned c
         if (lane == 0) next_id = static_cast<int>(atomicAdd(p.counters, 1u));
 
         const int s = s_cur;
-        const int ctx = __shfl_sync(0xffffffffu, ctx_lane, s_cur - win0);
-        const bool valid = ctx >= 0 && ctx <= max_ctx;
-        const int np = items_of(ctx, max_ctx, P);
+        SeqQueries sq;
+        sq.ctx = __shfl_sync(0xffffffffu, sq_lane.ctx, s_cur - win0);
+        sq.multi = kMulti;
+        if constexpr (kMulti) {
+            sq.q0 = __shfl_sync(0xffffffffu, sq_lane.q0, s_cur - win0);
+            sq.q1 = __shfl_sync(0xffffffffu, sq_lane.q1, s_cur - win0);
+        } else {
+            sq.q0 = s;
+            sq.q1 = s + 1;
+        }
+        const int ctx = sq.ctx;
+        const bool valid = sq.ctx_ok(max_ctx);
+        const int tile_tokens = kMulti ? p.tile_tokens : 1;
+        const int qlen = sq.q1 - sq.q0;
+        const int np = valid ? items_of(ctx, max_ctx, P) : 1;
+        const int ntt = kMulti ? (qlen + tile_tokens - 1) / tile_tokens : 1;
         const int i_loc = item_id - base;
-        const int ht = i_loc / np;
-        const int part = i_loc - ht * np;
-        const int hq0 = ht * GT;
+        if (kMulti && (i_loc < 0 || i_loc >= __shfl_sync(0xffffffffu, items_lane, s_cur - win0))) {
+            // only reachable when query_start is not ascending (item counts can overflow)
+            if (lane == 0) report(p.d_err, PA_DERR_CTX_OOB);
+            break;
+        }
+        const int tile = i_loc / np;
+        const int part = i_loc - tile * np;
+        const int ht = kMulti ? tile / ntt : tile;
+        const int it = tile - ht * ntt;
+        const int hq0 = ht * (kMulti ? p.tile_heads : GT);
         const int hk = hq0 / p.group;
+        const int i0 = it * tile_tokens;                   // first query token of the tile
+        const int ntok = kMulti ? min(tile_tokens, qlen - i0) : 1;
+        const int lim_first = ctx - qlen + i0 + 1;         // tokens seen by query i0
+        const int lim_last = lim_first + ntok - 1;         // ... and by the tile's last query
         const int tok_begin = part * P;
-        const int tok_end = valid ? min(tok_begin + P, ctx) : tok_begin;
+        const int tok_end = valid ? max(tok_begin, min(tok_begin + P, lim_last)) : tok_begin;
         const int nst = tok_end > tok_begin ? (tok_end - tok_begin + C::kTps - 1) / C::kTps : 1;
         if (!valid && lane == 0) report(p.d_err, PA_DERR_CTX_OOB);
 
@@ -355,17 +443,24 @@ __device__ __forceinline__ void decode_produce(const DecodeParams& p, unsigned c
         }
         if (lane == 0) {
             ItemRec& r = items[islot];
-            r.s = s;
+            r.row0 = sq.q0 + i0;
             r.hq0 = hq0;
             r.part = part;
             r.nparts = valid ? np : 0;
             r.first_warp = c % W;
             r.nwarps = min(nst, W);
+            r.ntok = ntok;
+            // query rows: tile_heads consecutive heads of each of the tile's tokens
             const uint32_t qf = qfull0 + 8 * islot;
-            mbar_arrive_expect_tx(qf, C::kQBytes);
-            bulk_g2s(smem_addr(smem + C::kQOffset + islot * align16(C::kQBytes)),
-                     static_cast<const T*>(p.q) + (static_cast<size_t>(s) * p.num_q_heads + hq0) * D,
-                     C::kQBytes, qf, policy);
+            const uint32_t row_bytes =
+                kMulti ? static_cast<uint32_t>(p.tile_heads * D * C::kElem) : C::kQBytes;
+            mbar_arrive_expect_tx(qf, row_bytes * ntok);
+            const uint32_t dst = smem_addr(smem + C::kQOffset + islot * align16(C::kQBytes));
+            for (int ti = 0; ti < ntok; ++ti)
+                bulk_g2s(dst + ti * row_bytes,
+                         static_cast<const T*>(p.q) +
+                             (static_cast<size_t>(sq.q0 + i0 + ti) * p.num_q_heads + hq0) * D,
+                         row_bytes, qf, policy);
         }
         q_issued = item_seq + 1;
 
@@ -420,6 +515,10 @@ __device__ __forceinline__ void decode_produce(const DecodeParams& p, unsigned c
                 uint32_t flags = 0;
                 if (i < W) flags |= kStageFirst;
                 if (i + W >= nst) flags |= kStageLast;
+                if (kMulti && t1 > lim_first) {  // a query row stops attending inside this stage
+                    const int rel = max(-128, min(127, lim_first - t0));
+                    flags |= kStageCausal | (static_cast<uint32_t>(rel & 0xff) << 8);
+                }
                 meta[st].mask = mask;
                 meta[st].item_seq = static_cast<uint32_t>(item_seq);
                 meta[st].flags = flags;
@@ -487,7 +586,7 @@ __device__ __forceinline__ void decode_produce(const DecodeParams& p, unsigned c
 }
 
 
-template <typename T, int D, int GT>
+template <typename T, int D, int GT, bool kMulti>
 __device__ __forceinline__ void decode_consume(const DecodeParams& p, unsigned char* smem) {
     using C = DecodeTile<T, D, GT>;
     constexpr int kVec = C::kVec, kLpt = C::kLpt, W = C::kConsumerWarps;
@@ -551,10 +650,25 @@ __device__ __forceinline__ void decode_consume(const DecodeParams& p, unsigned c
         }
         const unsigned char* sK = smem + st * C::kStageBytes;
         const unsigned char* sV = sK + C::kTps * C::kRowBytes;
-        if (mask == C::kFullMask)
-            decode_stage<T, D, GT, true>(sK, sV, mask, qf, m, l, o, pw, grp, lig);
+        uint64_t rmask[GT];
+        if (kMulti && (flags & kStageCausal)) {
+            // row j (query token j / tile_heads of the item) attends to the stage's
+            // first rel0 + j / tile_heads tokens
+            const int rel0 = static_cast<int>(static_cast<int8_t>((flags >> 8) & 0xffu));
+#pragma unroll
+            for (int j = 0; j < GT; ++j) {
+                const int rel = rel0 + (j >> p.tile_heads_log2);
+                const uint64_t lim = rel <= 0 ? 0ull : rel >= 64 ? ~0ull : ((1ull << rel) - 1ull);
+                rmask[j] = mask & lim;
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < GT; ++j) rmask[j] = mask;
+        }
+        if (mask == C::kFullMask && !(kMulti && (flags & kStageCausal)))
+            decode_stage<T, D, GT, true>(sK, sV, mask, rmask, qf, m, l, o, pw, grp, lig);
         else
-            decode_stage<T, D, GT, false>(sK, sV, mask, qf, m, l, o, pw, grp, lig);
+            decode_stage<T, D, GT, false>(sK, sV, mask, rmask, qf, m, l, o, pw, grp, lig);
         if (lane == 0) mbar_arrive(empty0 + 8 * st);
         if (!(flags & kStageLast)) continue;
 
@@ -595,11 +709,13 @@ __device__ __forceinline__ void decode_consume(const DecodeParams& p, unsigned c
 
         // ---- last warp of the item: merge the warps' states and write the result
         __threadfence_block();
-        const int s = rec.s, hq0 = rec.hq0, part = rec.part, nparts = rec.nparts;
-        const int w0 = rec.first_warp, nw = rec.nwarps;
+        const int row0 = rec.row0, hq0 = rec.hq0, part = rec.part, nparts = rec.nparts;
+        const int w0 = rec.first_warp, nw = rec.nwarps, ntok = rec.ntok;
         for (int idx = lane; idx < GT * D; idx += 32) {
             const int j = idx / D;
             const int dd = idx - j * D;
+            const int tj = kMulti ? j >> p.tile_heads_log2 : 0;  // query token of row j
+            if (kMulti && tj >= ntok) break;                     // rows past the last query
             float M = -INFINITY;
             for (int k = 0; k < nw; ++k) M = fmaxf(M, sm_m[((w0 + k) % W) * GT + j]);
             float L = 0.f, O = 0.f;
@@ -611,7 +727,8 @@ __device__ __forceinline__ void decode_consume(const DecodeParams& p, unsigned c
                     O = fmaf(sm_o[(w * GT + j) * D + dd], sc, O);
                 }
             }
-            const size_t row = static_cast<size_t>(s) * p.num_q_heads + hq0 + j;
+            const size_t row = static_cast<size_t>(row0 + tj) * p.num_q_heads + hq0 +
+                               (kMulti ? (j & (p.tile_heads - 1)) : j);
             if (nparts <= 1) {  // whole sequence in one item, or a zero row
                 static_cast<T*>(p.out)[row * D + dd] =
                     Elem<T>::from_float(nparts == 1 && L > 0.f ? O / L : 0.f);
@@ -632,7 +749,7 @@ __device__ __forceinline__ void decode_consume(const DecodeParams& p, unsigned c
     }
 }
 
-template <typename T, int D, int GT>
+template <typename T, int D, int GT, bool kMulti>
 __global__ void __launch_bounds__(DecodeTile<T, D, GT>::kThreads)
     decode_persistent_kernel(const DecodeParams p) {
     using C = DecodeTile<T, D, GT>;
@@ -653,9 +770,9 @@ __global__ void __launch_bounds__(DecodeTile<T, D, GT>::kThreads)
     }
     __syncthreads();
     if ((threadIdx.x >> 5) == C::kConsumerWarps)
-        decode_produce<T, D, GT>(p, smem);
+        decode_produce<T, D, GT, kMulti>(p, smem);
     else
-        decode_consume<T, D, GT>(p, smem);
+        decode_consume<T, D, GT, kMulti>(p, smem);
     __syncthreads();
     if (threadIdx.x == 0) {
         // The last CTA out returns both counters to zero for the next call.
@@ -674,12 +791,25 @@ __global__ void __launch_bounds__(DecodeTile<T, D, GT>::kThreads)
 template <typename T, int D>
 __global__ void __launch_bounds__(128) decode_reduce_kernel(const DecodeParams p) {
     constexpr int kCols = D / 32;
-    const int sh = blockIdx.x;
-    const int s = sh / p.num_q_heads;
+    const int sh = blockIdx.x;  // q / out row x query head
+    const int tok = sh / p.num_q_heads;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int ctx = p.context_lens[s];
-    if (ctx < 0 || ctx > p.max_blocks_per_seq * p.block_size) return;
-    const int nparts = ctx == 0 ? 1 : (ctx + p.partition_tokens - 1) / p.partition_tokens;
+    int s = tok;
+    if (p.query_start != nullptr) {  // the sequence whose queries hold row tok
+        int lo = 0, hi = p.num_seqs;  // first k in [lo, hi) with query_start[k + 1] > tok
+        while (lo < hi) {
+            const int mid = (lo + hi) >> 1;
+            if (p.query_start[mid + 1] > tok) hi = mid;
+            else lo = mid + 1;
+        }
+        if (lo >= p.num_seqs) return;
+        s = lo;
+    }
+    const SeqQueries sq = seq_queries(p, s);
+    const int max_ctx = p.max_blocks_per_seq * p.block_size;
+    if (!sq.rows_ok(p.num_query_tokens) || tok < sq.q0 || tok >= sq.q1 || !sq.ctx_ok(max_ctx))
+        return;
+    const int nparts = items_of(sq.ctx, max_ctx, p.partition_tokens);
     if (nparts <= 1) return;
     const size_t row = static_cast<size_t>(sh) * p.max_parts;
 
@@ -720,12 +850,12 @@ __global__ void __launch_bounds__(128) decode_reduce_kernel(const DecodeParams p
     }
 }
 
-template <typename T, int D, int GT>
+template <typename T, int D, int GT, bool kMulti>
 inline pa_status launch_decode_tile(const DecodeParams& p, cudaStream_t stream) {
     using C = DecodeTile<T, D, GT>;
     static std::atomic<uint64_t> smem_configured{0};  // one per instantiation
     static std::atomic<int> ctas_per_sm{0};
-    auto kernel = decode_persistent_kernel<T, D, GT>;
+    auto kernel = decode_persistent_kernel<T, D, GT, kMulti>;
     if (ensure_smem(kernel, C::kSmemBytes, smem_configured) != PA_OK) return PA_ERR_CUDA;
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
@@ -739,43 +869,52 @@ inline pa_status launch_decode_tile(const DecodeParams& p, cudaStream_t stream) 
         per_sm = per_sm < 1 ? 1 : per_sm;
         ctas_per_sm.store(per_sm, std::memory_order_relaxed);
     }
-    const long long work = static_cast<long long>(p.num_seqs) * p.head_tiles * p.max_parts;
+    // upper bound of the work items: query-token tiles are at most
+    // rows / tile_tokens plus one ragged tile per sequence
+    const long long tiles = p.query_start == nullptr
+                                ? p.num_seqs
+                                : p.num_query_tokens / p.tile_tokens + p.num_seqs;
+    const long long work = tiles * p.head_tiles * p.max_parts;
     if (work > 0x7fffffffLL) return PA_ERR_UNSUPPORTED;
     long long grid = static_cast<long long>(sms) * per_sm;
     if (grid > work) grid = work;
     kernel<<<static_cast<unsigned>(grid), C::kThreads, C::kSmemBytes, stream>>>(p);
     if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
     if (p.max_parts > 1) {
-        decode_reduce_kernel<T, D><<<p.num_seqs * p.num_q_heads, 128, 0, stream>>>(p);
+        decode_reduce_kernel<T, D><<<p.num_query_tokens * p.num_q_heads, 128, 0, stream>>>(p);
         if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
     }
     return PA_OK;
 }
 
-template <typename T, int D>
+template <typename T, int D, bool kMulti>
 inline pa_status launch_decode_dim(const DecodeParams& p, int gt, cudaStream_t stream) {
     switch (gt) {
-        case 1: return launch_decode_tile<T, D, 1>(p, stream);
-        case 2: return launch_decode_tile<T, D, 2>(p, stream);
-        case 4: return launch_decode_tile<T, D, 4>(p, stream);
-        case 8: return launch_decode_tile<T, D, 8>(p, stream);
+        case 1: return launch_decode_tile<T, D, 1, kMulti>(p, stream);
+        case 2: return launch_decode_tile<T, D, 2, kMulti>(p, stream);
+        case 4: return launch_decode_tile<T, D, 4, kMulti>(p, stream);
+        case 8: return launch_decode_tile<T, D, 8, kMulti>(p, stream);
     }
     return PA_ERR_UNSUPPORTED;
 }
 
-template <typename T>
+template <typename T, bool kMulti>
 inline pa_status launch_decode_typed(const DecodeParams& p, int head_dim, int gt,
                                      cudaStream_t stream) {
     switch (head_dim) {
-        case 64: return launch_decode_dim<T, 64>(p, gt, stream);
-        case 128: return launch_decode_dim<T, 128>(p, gt, stream);
+        case 64: return launch_decode_dim<T, 64, kMulti>(p, gt, stream);
+        case 128: return launch_decode_dim<T, 128, kMulti>(p, gt, stream);
     }
     return PA_ERR_UNSUPPORTED;
 }
 
-// One per element type, each in its own translation unit.
+// One per element type and query form, each in its own translation unit.
 pa_status launch_decode_f32(const DecodeParams& p, int head_dim, int gt, cudaStream_t stream);
 pa_status launch_decode_f16(const DecodeParams& p, int head_dim, int gt, cudaStream_t stream);
 pa_status launch_decode_bf16(const DecodeParams& p, int head_dim, int gt, cudaStream_t stream);
+pa_status launch_multi_query_f32(const DecodeParams& p, int head_dim, int gt, cudaStream_t stream);
+pa_status launch_multi_query_f16(const DecodeParams& p, int head_dim, int gt, cudaStream_t stream);
+pa_status launch_multi_query_bf16(const DecodeParams& p, int head_dim, int gt,
+                                  cudaStream_t stream);
 
 }  // namespace pa

@@ -49,6 +49,8 @@ def upload(w, device="cuda") -> Dict[str, torch.Tensor]:
         "slot_mapping": torch.from_numpy(w.slot_mapping).to(device),
         "block_mapping": torch.from_numpy(w.block_mapping.reshape(-1, 2)).to(device),
         "d_err": torch.zeros(1, dtype=torch.int32, device=device),
+        **({"query_start": torch.from_numpy(w.query_start).to(device)}
+           if w.query_start is not None else {}),
     }
 
 
@@ -62,8 +64,13 @@ def gpu_step(w, d: Dict[str, torch.Tensor], partition_tokens: Optional[int] = No
         pa.kv_write(d["k_new"], d["v_new"], d["k_cache"], d["v_cache"], d["slot_mapping"],
                     d_err=d["d_err"])
     out = torch.empty_like(d["q"])
-    pa.decode(out, d["q"], d["k_cache"], d["v_cache"], d["block_tables"], d["context_lens"],
-              w.scale, partition_tokens=P, d_err=d["d_err"])
+    if w.query_start is not None:
+        pa.multi_query(out, d["q"], d["query_start"], d["k_cache"], d["v_cache"],
+                       d["block_tables"], d["context_lens"], w.scale, partition_tokens=P,
+                       d_err=d["d_err"])
+    else:
+        pa.decode(out, d["q"], d["k_cache"], d["v_cache"], d["block_tables"], d["context_lens"],
+                  w.scale, partition_tokens=P, d_err=d["d_err"])
     torch.cuda.synchronize()
     return out
 
@@ -92,6 +99,34 @@ def oracle_decode_parallel(q, kc, vc, tables, ctx, *, scale, dtype, threads=None
     return out, e
 
 
+def oracle_multi_query_parallel(q, query_start, kc, vc, tables, ctx, *, scale, dtype,
+                                threads=None):
+    """The oracle's multi-query attention, sequences split over host threads."""
+    S = ctx.shape[0]
+    threads = max(1, min(S, threads or os.cpu_count() or 4))
+    bounds = np.linspace(0, S, threads + 1).astype(int)
+    out = np.zeros(q.shape, np.float64)
+
+    def run(i):
+        a, b = bounds[i], bounds[i + 1]
+        if a == b:
+            return 0
+        r0, r1 = int(query_start[a]), int(query_start[b])
+        o, e = oracle.multi_query(np.ascontiguousarray(q[r0:r1]),
+                                  np.ascontiguousarray(query_start[a:b + 1] - r0), kc, vc,
+                                  np.ascontiguousarray(tables[a:b]),
+                                  np.ascontiguousarray(ctx[a:b]), scale=scale, dtype=dtype)
+        out[r0:r1] = o
+        return e
+
+    with cf.ThreadPoolExecutor(threads) as ex:
+        errs = list(ex.map(run, range(threads)))
+    e = 0
+    for x in errs:
+        e |= x
+    return out, e
+
+
 def oracle_step(w, do_copy=True, parallel=True):
     kc = w.k_cache.copy()
     vc = w.v_cache.copy()
@@ -100,7 +135,14 @@ def oracle_step(w, do_copy=True, parallel=True):
         err |= oracle.copy_blocks(kc, vc, w.block_mapping, dtype=w.dtype)
     if w.num_tokens:
         err |= oracle.kv_write(kc, vc, w.k_new, w.v_new, w.slot_mapping, dtype=w.dtype)
-    if parallel:
+    if w.query_start is not None:
+        if parallel:
+            out, e = oracle_multi_query_parallel(w.q, w.query_start, kc, vc, w.block_tables,
+                                                 w.context_lens, scale=w.scale, dtype=w.dtype)
+        else:
+            out, e = oracle.multi_query(w.q, w.query_start, kc, vc, w.block_tables,
+                                        w.context_lens, scale=w.scale, dtype=w.dtype)
+    elif parallel:
         out, e = oracle_decode_parallel(w.q, kc, vc, w.block_tables, w.context_lens, scale=w.scale,
                                         dtype=w.dtype)
     else:
