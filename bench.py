@@ -56,6 +56,10 @@ WORKLOAD_TEXT = {
     "spec_verify": "speculative-decoding verification, LLaMA-7B-shaped: 64 seqs x 4 causal "
                    "query tokens (kv_write of all 4, then attention of each over its prefix), "
                    "32 q/kv heads, head_dim 128, fp16, block 16, context U[128,2048]",
+    "llama13b_fp8": "LLaMA-13B-shaped decode as llama13b over an FP8 E4M3 KV cache (q/out bf16)",
+    "llama7b_fp8": "LLaMA-7B-shaped decode as llama7b over an FP8 E4M3 KV cache (one fp32 scale "
+                   "per block and kv head; q/out fp16; quantising kv_write of 1 token/seq)",
+    "gqa_share_fp8": "gqa_share over an FP8 E4M3 KV cache (scales copied with each CoW block)",
     "chunked_prefill": "chunked prefill: 8 seqs each append a 512-token prompt chunk (kv_write "
                        "of 512 tokens, then causal attention of each) to U[0,3584] cached "
                        "tokens; GQA 32 q / 8 kv heads, head_dim 128, bf16, block 16",
@@ -93,6 +97,11 @@ def _rows(w):
 def _oracle_row(w, kc, vc, s, r, n):
     """The oracle on one query row (all heads) of the step."""
     import oracle
+    if w.kv_dtype == "e4m3":
+        return oracle.decode_fp8(np.ascontiguousarray(w.q[r:r + 1]), kc, vc, w.k_scale, w.v_scale,
+                                 np.ascontiguousarray(w.block_tables[s:s + 1]),
+                                 np.ascontiguousarray(w.context_lens[s:s + 1]), scale=w.scale,
+                                 q_dtype=w.dtype)
     if w.query_start is None:
         return oracle.decode(np.ascontiguousarray(w.q[r:r + 1]), kc, vc,
                              np.ascontiguousarray(w.block_tables[s:s + 1]),
@@ -288,7 +297,12 @@ def run_gpu(args):
         kw["layout"] = args.layout
     w = wl.by_name(args.config, poison=False, **kw)
     mq = w.query_start is not None
-    if mq:
+    fp8 = w.kv_dtype == "e4m3"
+    if fp8:
+        P = pa.decode_partition_tokens(w.num_q_heads, w.num_kv_heads, w.head_dim,
+                                       w.max_blocks_per_seq, w.block_size, "e4m3",
+                                       w.partition_tokens)
+    elif mq:
         P = pa.multi_query_partition_tokens(w.num_query_tokens, w.num_q_heads, w.num_kv_heads,
                                             w.head_dim, w.max_blocks_per_seq, w.block_size,
                                             w.dtype, w.partition_tokens)
@@ -297,16 +311,23 @@ def run_gpu(args):
                                        w.max_blocks_per_seq, w.block_size, w.dtype,
                                        w.partition_tokens)
     dt = w.dtype
+    pool = (lambda a: torch.from_numpy(a)) if fp8 else (lambda a: _to_torch(a, dt))
     d = {k: v.to(dev) for k, v in {
-        "q": _to_torch(w.q, dt), "k_cache": _to_torch(w.k_cache, dt),
-        "v_cache": _to_torch(w.v_cache, dt), "k_new": _to_torch(w.k_new, dt),
+        "q": _to_torch(w.q, dt), "k_cache": pool(w.k_cache),
+        "v_cache": pool(w.v_cache), "k_new": _to_torch(w.k_new, dt),
         "v_new": _to_torch(w.v_new, dt), "block_tables": torch.from_numpy(w.block_tables),
         "context_lens": torch.from_numpy(w.context_lens),
         "slot_mapping": torch.from_numpy(w.slot_mapping),
         "block_mapping": torch.from_numpy(w.block_mapping.reshape(-1, 2)),
-        **({"query_start": torch.from_numpy(w.query_start)} if mq else {})}.items()}
+        **({"query_start": torch.from_numpy(w.query_start)} if mq else {}),
+        **({"k_scale": torch.from_numpy(w.k_scale), "v_scale": torch.from_numpy(w.v_scale)}
+           if fp8 else {})}.items()}
     out = torch.empty_like(d["q"])
-    if mq:
+    if fp8:
+        workspace = torch.zeros(pa.decode_workspace_size(
+            w.num_seqs, w.num_q_heads, w.num_kv_heads, w.head_dim, w.max_blocks_per_seq,
+            w.block_size, "e4m3", w.partition_tokens), dtype=torch.uint8, device=dev)
+    elif mq:
         workspace = pa.multi_query_workspace(d["q"], d["k_cache"], d["block_tables"],
                                              w.partition_tokens)
     else:
@@ -321,16 +342,26 @@ def run_gpu(args):
 
     def step(dd, ev_mid=None):
         """copy_blocks, kv_write, decode; ev_mid: events after copy_blocks and after kv_write."""
-        if w.num_pairs:
+        if w.num_pairs and fp8:
+            pa.copy_blocks_fp8(dd["k_cache"], dd["v_cache"], dd["k_scale"], dd["v_scale"],
+                               dd["block_mapping"], d_err=d_err)
+        elif w.num_pairs:
             pa.copy_blocks(dd["k_cache"], dd["v_cache"], dd["block_mapping"], d_err=d_err)
         if ev_mid is not None:
             ev_mid[0].record(stream)
-        if w.num_tokens:
+        if w.num_tokens and fp8:
+            pa.kv_write_fp8(dd["k_new"], dd["v_new"], dd["k_cache"], dd["v_cache"],
+                            dd["k_scale"], dd["v_scale"], dd["slot_mapping"], d_err=d_err)
+        elif w.num_tokens:
             pa.kv_write(dd["k_new"], dd["v_new"], dd["k_cache"], dd["v_cache"],
                         dd["slot_mapping"], d_err=d_err)
         if ev_mid is not None:
             ev_mid[1].record(stream)
-        if mq:
+        if fp8:
+            pa.decode_fp8(out, dd["q"], dd["k_cache"], dd["v_cache"], dd["k_scale"],
+                          dd["v_scale"], dd["block_tables"], dd["context_lens"], w.scale,
+                          partition_tokens=w.partition_tokens, workspace=workspace, d_err=d_err)
+        elif mq:
             pa.multi_query(out, dd["q"], dd["query_start"], dd["k_cache"], dd["v_cache"],
                            dd["block_tables"], dd["context_lens"], w.scale,
                            partition_tokens=w.partition_tokens, workspace=workspace, d_err=d_err)
@@ -452,7 +483,8 @@ def run_gpu(args):
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": dt,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "e4m3" if fp8 else dt,
         "data": "synthetic (seeded PCG64 N(0,1) K/V/q; block tables from a seeded random "
                 "permutation of the pool)",
         "config": {"workload": WORKLOAD_TEXT.get(args.config, args.config), "name": args.config,
@@ -530,9 +562,16 @@ def run_reference(args):
     with cf.ThreadPoolExecutor(threads) as ex:
         for i in range(args.warmup + args.steps):
             t0 = time.perf_counter()
-            if w.num_pairs:
-                oracle.copy_blocks(kc, vc, w.block_mapping, dtype=w.dtype)
-            oracle.kv_write(kc, vc, w.k_new, w.v_new, w.slot_mapping, dtype=w.dtype)
+            if w.kv_dtype == "e4m3":
+                ks, vs = w.k_scale, w.v_scale
+                if w.num_pairs:
+                    oracle.swap_blocks_fp8(kc, vc, ks, vs, kc, vc, ks, vs, w.block_mapping)
+                oracle.kv_write_fp8(kc, vc, ks, vs, w.k_new, w.v_new, w.slot_mapping,
+                                    new_dtype=w.dtype)
+            else:
+                if w.num_pairs:
+                    oracle.copy_blocks(kc, vc, w.block_mapping, dtype=w.dtype)
+                oracle.kv_write(kc, vc, w.k_new, w.v_new, w.slot_mapping, dtype=w.dtype)
             list(ex.map(one, range(n)))
             if i >= args.warmup:
                 times.append(time.perf_counter() - t0)
@@ -541,7 +580,8 @@ def run_reference(args):
     line = {
         "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
         "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "e4m3" if w.kv_dtype == "e4m3" else w.dtype,
         "data": "synthetic (same seeded workload as the GPU arm)",
         "config": {"workload": WORKLOAD_TEXT.get(args.config, args.config), "name": args.config,
                    "sample_rows": n, "sample_kv_bytes": sample_bytes},

@@ -64,7 +64,9 @@ typedef enum pa_status {
 typedef enum pa_dtype {
     PA_F32 = 0,  /* IEEE binary32 */
     PA_F16 = 1,  /* IEEE binary16 */
-    PA_BF16 = 2  /* bfloat16      */
+    PA_BF16 = 2, /* bfloat16      */
+    PA_E4M3 = 3  /* FP8 E4M3 cache codes with per-(block, kv head) scales: the *_fp8 calls,
+                    and pa_decode_partition_tokens / pa_decode_workspace_size for them */
 } pa_dtype;
 
 /* Bits OR-ed into *d_err by the kernels. */
@@ -265,6 +267,63 @@ pa_status pa_decode_static_workspace(void* out, const void* q, const void* k_cac
                                      int block_size, int num_blocks, float scale,
                                      int partition_tokens, pa_dtype dtype, uint32_t* d_err,
                                      pa_stream_t stream);
+
+/* ---- FP8 E4M3 caches ----------------------------------------------------
+ *
+ * Quantised storage of historical blocks raises the cache's effective capacity
+ * (kwkr.cn "vLLM PagedAttention 技术深度解析" §1.5: quantised compression of
+ * history blocks; "PagedAttention" (compassingai.com) §15: lossy compression
+ * of physical blocks).  Here each K and V element is one E4M3 byte (the OCP
+ * "E4M3FN" format: bias 7, 3 fraction bits, no infinities, largest finite
+ * 448) and each (physical block, kv head) has one fp32 scale for K and one
+ * for V:  value = code value x scale.
+ *   k_cache, v_cache  uint8 codes [num_blocks][num_kv_heads][block_size][head_dim]
+ *   k_scale, v_scale  fp32 [num_blocks][num_kv_heads], device memory; a
+ *                     block's scales are set by the caller when it allocates
+ *                     the block, before its first token is written.
+ * head_dim must be 128 for pa_decode_fp8 (a multiple of 16 for the others).
+ */
+
+/* pa_kv_write_fp8 -- pa_kv_write into an E4M3 cache.  k_new / v_new have
+ * type new_dtype (PA_F32, PA_F16 or PA_BF16); each element x is stored as the
+ * E4M3 code nearest to fp32(x) / scale of its slot's (block, kv head), the
+ * division IEEE round-to-nearest, ties to the even code, magnitudes at or
+ * above 448 saturating to +-448.  Slots: as pa_kv_write. */
+pa_status pa_kv_write_fp8(const void* k_new, const void* v_new, pa_dtype new_dtype,
+                          void* k_cache, void* v_cache, const float* k_scale,
+                          const float* v_scale, const int64_t* slot_mapping, int num_tokens,
+                          int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                          uint32_t* d_err, pa_stream_t stream);
+
+/* pa_copy_blocks_fp8 / pa_swap_blocks_fp8 -- pa_copy_blocks / pa_swap_blocks
+ * for E4M3 caches: the codes of each block and its K and V scales are copied
+ * together (either side of a swap may be pinned host memory, scales
+ * included). */
+pa_status pa_copy_blocks_fp8(void* k_cache, void* v_cache, float* k_scale, float* v_scale,
+                             const int32_t* block_mapping, int num_pairs, int num_kv_heads,
+                             int head_dim, int block_size, int num_blocks, uint32_t* d_err,
+                             pa_stream_t stream);
+pa_status pa_swap_blocks_fp8(const void* src_k, const void* src_v, const float* src_k_scale,
+                             const float* src_v_scale, void* dst_k, void* dst_v,
+                             float* dst_k_scale, float* dst_v_scale,
+                             const int32_t* block_mapping, int num_pairs, int num_kv_heads,
+                             int head_dim, int block_size, int src_num_blocks,
+                             int dst_num_blocks, uint32_t* d_err, pa_stream_t stream);
+
+/* pa_decode_fp8 -- pa_decode over an E4M3 cache: K/V element = code value x
+ * the scale of its (block, kv head); q and out have type q_dtype (PA_F16 or
+ * PA_BF16).  The logit of a token is (q . K codes) x its K scale x scale, and
+ * its softmax weight is multiplied by its V scale before it weights the V
+ * codes; accumulation fp32.  Partitions and workspace: pa_decode_partition_tokens
+ * and pa_decode_workspace_size with dtype PA_E4M3.  Runs on the SIMT kernel
+ * for every head grouping (head_dim 128). */
+pa_status pa_decode_fp8(void* out, const void* q, pa_dtype q_dtype, const void* k_cache,
+                        const void* v_cache, const float* k_scale, const float* v_scale,
+                        const int32_t* block_tables, int max_blocks_per_seq,
+                        const int32_t* context_lens, int num_seqs, int num_q_heads,
+                        int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                        float scale, int partition_tokens, void* workspace,
+                        size_t workspace_bytes, uint32_t* d_err, pa_stream_t stream);
 
 /* pa_selftest_wait_timeout -- exercises the bounded waits the kernels use.
  * One warp waits on a barrier nothing ever arrives at; after the wait limit

@@ -30,7 +30,10 @@ DTYPE_CODE = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}
 EXPORTED = ("pa_abi_version", "pa_status_string", "pa_kv_write", "pa_copy_blocks", "pa_swap_blocks",
             "pa_copy_blocks_check", "pa_decode_partition_tokens", "pa_decode_workspace_size",
             "pa_decode", "pa_decode_static_workspace", "pa_multi_query_partition_tokens",
-            "pa_multi_query_workspace_size", "pa_multi_query", "pa_selftest_wait_timeout")
+            "pa_multi_query_workspace_size", "pa_multi_query", "pa_kv_write_fp8",
+            "pa_copy_blocks_fp8", "pa_swap_blocks_fp8", "pa_decode_fp8",
+            "pa_selftest_wait_timeout")
+PA_E4M3 = 3
 
 _lock = threading.Lock()
 _lib: Optional[ctypes.CDLL] = None
@@ -86,6 +89,17 @@ def load() -> ctypes.CDLL:
         lib.pa_multi_query.restype = i32
         lib.pa_multi_query.argtypes = [vp, vp, i32, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32,
                                        i32, i32, ctypes.c_float, i32, i32, vp, u64, vp, vp]
+        lib.pa_kv_write_fp8.restype = i32
+        lib.pa_kv_write_fp8.argtypes = [vp, vp, i32, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32,
+                                        vp, vp]
+        lib.pa_copy_blocks_fp8.restype = i32
+        lib.pa_copy_blocks_fp8.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp, vp]
+        lib.pa_swap_blocks_fp8.restype = i32
+        lib.pa_swap_blocks_fp8.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32,
+                                           i32, i32, vp, vp]
+        lib.pa_decode_fp8.restype = i32
+        lib.pa_decode_fp8.argtypes = [vp, vp, i32, vp, vp, vp, vp, vp, i32, vp, i32, i32, i32,
+                                      i32, i32, i32, ctypes.c_float, i32, vp, u64, vp, vp]
         _lib = lib
         return lib
 
@@ -198,7 +212,7 @@ def copy_blocks_check(block_mapping: torch.Tensor, d_err: torch.Tensor, stream=N
     _check(st, "pa_copy_blocks_check")
 
 
-DTYPE_NAME_CODE = {"f32": 0, "f16": 1, "bf16": 2}
+DTYPE_NAME_CODE = {"f32": 0, "f16": 1, "bf16": 2, "e4m3": 3}
 
 
 def _dtype_code(dtype) -> int:
@@ -315,4 +329,98 @@ def multi_query(out: torch.Tensor, q: torch.Tensor, query_start: torch.Tensor,
                                DTYPE_CODE[q.dtype], _ptr(workspace), ws_bytes, _ptr(d_err),
                                _stream(stream, q.device))
     _check(st, "pa_multi_query")
+    return out
+
+
+# ---- E4M3 caches: uint8 (or torch.float8_e4m3fn) codes + fp32 [NB][Hkv] scales ----
+
+def _fp8_pool(name: str, t: torch.Tensor) -> None:
+    if t.element_size() != 1:
+        raise ValueError(f"{name} must hold one-byte E4M3 codes")
+
+
+def kv_write_fp8(k_new: torch.Tensor, v_new: torch.Tensor, k_cache: torch.Tensor,
+                 v_cache: torch.Tensor, k_scale: torch.Tensor, v_scale: torch.Tensor,
+                 slot_mapping: torch.Tensor, d_err: Optional[torch.Tensor] = None,
+                 stream=None) -> None:
+    """Quantising kv_write: k_cache[slot] = e4m3(k_new / k_scale[block][h]) (and V)."""
+    for n, t in (("k_new", k_new), ("v_new", v_new), ("k_cache", k_cache), ("v_cache", v_cache),
+                 ("k_scale", k_scale), ("v_scale", v_scale), ("slot_mapping", slot_mapping)):
+        _cuda_contig(n, t)
+    _fp8_pool("k_cache", k_cache)
+    _fp8_pool("v_cache", v_cache)
+    if slot_mapping.dtype != torch.int64 or k_scale.dtype != torch.float32:
+        raise ValueError("slot_mapping must be int64 and the scales float32")
+    T, Hkv, d = k_new.shape
+    NB, Hkv2, B, d2 = k_cache.shape
+    if (Hkv2, d2) != (Hkv, d) or k_scale.shape != (NB, Hkv) or v_scale.shape != (NB, Hkv):
+        raise ValueError("shape mismatch between new rows, cache and scales")
+    st = load().pa_kv_write_fp8(_ptr(k_new), _ptr(v_new), DTYPE_CODE[k_new.dtype], _ptr(k_cache),
+                                _ptr(v_cache), _ptr(k_scale), _ptr(v_scale), _ptr(slot_mapping), T,
+                                Hkv, d, B, NB, _ptr(d_err), _stream(stream, k_new.device))
+    _check(st, "pa_kv_write_fp8")
+
+
+def copy_blocks_fp8(k_cache: torch.Tensor, v_cache: torch.Tensor, k_scale: torch.Tensor,
+                    v_scale: torch.Tensor, block_mapping: torch.Tensor,
+                    d_err: Optional[torch.Tensor] = None, stream=None) -> None:
+    """Copy-on-write block copies of an E4M3 cache, scales included."""
+    for n, t in (("k_cache", k_cache), ("v_cache", v_cache), ("k_scale", k_scale),
+                 ("v_scale", v_scale), ("block_mapping", block_mapping)):
+        _cuda_contig(n, t)
+    _fp8_pool("k_cache", k_cache)
+    NB, Hkv, B, d = k_cache.shape
+    P = block_mapping.shape[0]
+    st = load().pa_copy_blocks_fp8(_ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale),
+                                   _ptr(block_mapping), P, Hkv, d, B, NB, _ptr(d_err),
+                                   _stream(stream, k_cache.device))
+    _check(st, "pa_copy_blocks_fp8")
+
+
+def swap_blocks_fp8(src_k: torch.Tensor, src_v: torch.Tensor, src_ks: torch.Tensor,
+                    src_vs: torch.Tensor, dst_k: torch.Tensor, dst_v: torch.Tensor,
+                    dst_ks: torch.Tensor, dst_vs: torch.Tensor, block_mapping: torch.Tensor,
+                    d_err: Optional[torch.Tensor] = None, stream=None) -> None:
+    """Block copies between two E4M3 pools (either may be pinned host memory), scales included."""
+    for n, t in (("src_k", src_k), ("src_v", src_v), ("dst_k", dst_k), ("dst_v", dst_v),
+                 ("src_ks", src_ks), ("src_vs", src_vs), ("dst_ks", dst_ks), ("dst_vs", dst_vs)):
+        if not t.is_contiguous():
+            raise ValueError(f"{n} must be contiguous")
+    _cuda_contig("block_mapping", block_mapping)
+    NBs, Hkv, B, d = src_k.shape
+    dev = block_mapping.device
+    st = load().pa_swap_blocks_fp8(_ptr(src_k), _ptr(src_v), _ptr(src_ks), _ptr(src_vs),
+                                   _ptr(dst_k), _ptr(dst_v), _ptr(dst_ks), _ptr(dst_vs),
+                                   _ptr(block_mapping), block_mapping.shape[0], Hkv, d, B, NBs,
+                                   dst_k.shape[0], _ptr(d_err), _stream(stream, dev))
+    _check(st, "pa_swap_blocks_fp8")
+
+
+def decode_fp8(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+               k_scale: torch.Tensor, v_scale: torch.Tensor, block_tables: torch.Tensor,
+               context_lens: torch.Tensor, scale: float, partition_tokens: int = 0,
+               workspace: Optional[torch.Tensor] = None, d_err: Optional[torch.Tensor] = None,
+               stream=None) -> torch.Tensor:
+    """Decode over an E4M3 cache: K/V element = code x scale of its (block, kv head)."""
+    for n, t in (("out", out), ("q", q), ("k_cache", k_cache), ("v_cache", v_cache),
+                 ("k_scale", k_scale), ("v_scale", v_scale), ("block_tables", block_tables),
+                 ("context_lens", context_lens)):
+        _cuda_contig(n, t)
+    _fp8_pool("k_cache", k_cache)
+    _fp8_pool("v_cache", v_cache)
+    S, Hq, d = q.shape
+    NB, Hkv, B, d2 = k_cache.shape
+    if d2 != d or out.shape != q.shape or out.dtype != q.dtype:
+        raise ValueError("q, out and the cache must agree in head_dim; out has q's dtype")
+    MB = block_tables.shape[1]
+    if workspace is None:
+        n = int(load().pa_decode_workspace_size(S, Hq, Hkv, d, MB, B, PA_E4M3, partition_tokens))
+        workspace = torch.zeros(n, dtype=torch.uint8, device=q.device)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    st = load().pa_decode_fp8(_ptr(out), _ptr(q), DTYPE_CODE[q.dtype], _ptr(k_cache),
+                              _ptr(v_cache), _ptr(k_scale), _ptr(v_scale), _ptr(block_tables), MB,
+                              _ptr(context_lens), S, Hq, Hkv, d, B, NB, float(scale),
+                              int(partition_tokens), _ptr(workspace), ws_bytes, _ptr(d_err),
+                              _stream(stream, q.device))
+    _check(st, "pa_decode_fp8")
     return out

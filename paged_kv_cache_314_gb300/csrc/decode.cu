@@ -3,6 +3,7 @@
 #include <cudaTypedefs.h>
 #include <math.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "decode_kernels.cuh"
@@ -146,6 +147,8 @@ struct AttnCall {
     int num_query_tokens;
     const void* k_cache;
     const void* v_cache;
+    const float* k_scale;  // E4M3 caches: [NB][Hkv]; else null
+    const float* v_scale;
     const int32_t* block_tables;
     int max_blocks_per_seq;
     const int32_t* context_lens;
@@ -174,7 +177,9 @@ pa_status run_attention(const AttnCall& a) {
     if (a.workspace_bytes < ws.bytes) return PA_ERR_WORKSPACE_TOO_SMALL;
     if ((reinterpret_cast<uintptr_t>(a.workspace) & 255u) != 0) return PA_ERR_INVALID_ARG;
     const int group = a.num_q_heads / a.num_kv_heads;
-    const int heads = head_tile(group);
+    // E4M3 caches widen 16 elements per lane: at most 4 rows per tile keep the
+    // query slices and accumulators in registers.
+    const int heads = a.k_scale != nullptr ? std::min(head_tile(group), 4) : head_tile(group);
     int tokens = 1;  // query tokens per work item: fill a tile of up to 8 rows
     if (a.query_start != nullptr && a.num_seqs > 0) {
         const long long avg = (static_cast<long long>(a.num_query_tokens) + a.num_seqs - 1) / a.num_seqs;
@@ -186,6 +191,8 @@ pa_status run_attention(const AttnCall& a) {
     p.q = a.q;
     p.k_cache = static_cast<const unsigned char*>(a.k_cache);
     p.v_cache = static_cast<const unsigned char*>(a.v_cache);
+    p.k_scale = a.k_scale;
+    p.v_scale = a.v_scale;
     p.block_tables = a.block_tables;
     p.context_lens = a.context_lens;
     p.query_start = a.query_start;
@@ -212,6 +219,12 @@ pa_status run_attention(const AttnCall& a) {
     p.qk_scale_log2 = a.scale * 1.4426950408889634f;  // log2(e)
 
     const cudaStream_t st = as_cuda(a.stream);
+    if (a.k_scale != nullptr) {  // E4M3 cache: the SIMT kernel, head_dim 128
+        const int gt = heads * tokens;
+        if (a.query_start != nullptr) return PA_ERR_UNSUPPORTED;
+        return a.dtype == PA_BF16 ? launch_decode_fp8_bf16(p, gt, st)
+                                  : launch_decode_fp8_f16(p, gt, st);
+    }
     // Grouped-query decode with 16-bit K/V and head_dim 128: the tensor-core path.
     const long long pool_rows = static_cast<long long>(a.num_blocks) * a.num_kv_heads * a.block_size;
     if (a.query_start == nullptr && tc_shape(a.num_q_heads, a.num_kv_heads, a.head_dim, a.dtype) &&
@@ -284,9 +297,39 @@ extern "C" pa_status pa_decode(void* out, const void* q, const void* k_cache, co
     if (P <= 0) return PA_ERR_INVALID_ARG;
     if (num_seqs == 0) return PA_OK;
     if (static_cast<long long>(num_seqs) * num_q_heads > 0x7fffffffLL) return PA_ERR_UNSUPPORTED;
-    const AttnCall a{out, q, nullptr, num_seqs, k_cache, v_cache, block_tables, max_blocks_per_seq,
-                     context_lens, num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
-                     num_blocks, scale, P, dtype, workspace, workspace_bytes, d_err, stream};
+    const AttnCall a{out, q, nullptr, num_seqs, k_cache, v_cache, nullptr, nullptr, block_tables,
+                     max_blocks_per_seq, context_lens, num_seqs, num_q_heads, num_kv_heads,
+                     head_dim, block_size, num_blocks, scale, P, dtype, workspace,
+                     workspace_bytes, d_err, stream};
+    return run_attention(a);
+}
+
+extern "C" pa_status pa_decode_fp8(void* out, const void* q, pa_dtype q_dtype, const void* k_cache,
+                                   const void* v_cache, const float* k_scale, const float* v_scale,
+                                   const int32_t* block_tables, int max_blocks_per_seq,
+                                   const int32_t* context_lens, int num_seqs, int num_q_heads,
+                                   int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                                   float scale, int partition_tokens, void* workspace,
+                                   size_t workspace_bytes, uint32_t* d_err, pa_stream_t stream) {
+    using namespace pa;
+    if (q_dtype != PA_F16 && q_dtype != PA_BF16) return PA_ERR_UNSUPPORTED;
+    const pa_status c = check_attention(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq,
+                                        context_lens, num_seqs, num_q_heads, num_kv_heads,
+                                        head_dim, block_size, num_blocks, scale, partition_tokens,
+                                        q_dtype);
+    if (c != PA_OK) return c;
+    if (head_dim != 128) return PA_ERR_UNSUPPORTED;
+    const int P = pa_decode_partition_tokens(num_q_heads, num_kv_heads, head_dim,
+                                             max_blocks_per_seq, block_size, PA_E4M3,
+                                             partition_tokens);
+    if (P <= 0) return PA_ERR_INVALID_ARG;
+    if (num_seqs == 0) return PA_OK;
+    if (k_scale == nullptr || v_scale == nullptr) return PA_ERR_INVALID_ARG;
+    if (static_cast<long long>(num_seqs) * num_q_heads > 0x7fffffffLL) return PA_ERR_UNSUPPORTED;
+    const AttnCall a{out, q, nullptr, num_seqs, k_cache, v_cache, k_scale, v_scale, block_tables,
+                     max_blocks_per_seq, context_lens, num_seqs, num_q_heads, num_kv_heads,
+                     head_dim, block_size, num_blocks, scale, P, q_dtype, workspace,
+                     workspace_bytes, d_err, stream};
     return run_attention(a);
 }
 
@@ -337,7 +380,8 @@ extern "C" pa_status pa_multi_query(void* out, const void* q, int num_query_toke
     if (query_start == nullptr) return PA_ERR_INVALID_ARG;
     if (static_cast<long long>(num_query_tokens) * num_q_heads > 0x7fffffffLL)
         return PA_ERR_UNSUPPORTED;
-    const AttnCall a{out, q, query_start, num_query_tokens, k_cache, v_cache, block_tables,
+    const AttnCall a{out, q, query_start, num_query_tokens, k_cache, v_cache, nullptr, nullptr,
+                     block_tables,
                      max_blocks_per_seq, context_lens, num_seqs, num_q_heads, num_kv_heads,
                      head_dim, block_size, num_blocks, scale, P, dtype, workspace,
                      workspace_bytes, d_err, stream};

@@ -68,6 +68,8 @@ struct DecodeParams {
     float* ws_m;  // [rows][Hq][max_parts] running max (log2 domain) per partition
     float* ws_l;  // [rows][Hq][max_parts] running sum per partition
     float* ws_o;  // [rows][Hq][max_parts][D] unnormalised output per partition
+    const float* k_scale;  // [NB][Hkv] E4M3 caches: value = code x scale; else null
+    const float* v_scale;
     uint32_t* d_err;
     int num_seqs;
     int num_q_heads;
@@ -113,9 +115,12 @@ struct ItemRec {
     int ntok;        // query tokens of the item (<= tile_tokens)
 };
 
-template <typename T, int D, int GT>
+// T: element type of q and out; TC: of the K/V cache (T, or E4M3 codes with
+// one fp32 scale per (block, kv head)).
+template <typename T, int D, int GT, typename TC = T>
 struct DecodeTile {
-    static constexpr int kElem = sizeof(T);
+    static constexpr int kElem = sizeof(TC);          // cache element bytes
+    static constexpr bool kFp8 = sizeof(TC) == 1;
     static constexpr int kVec = 16 / kElem;           // elements per 16-byte access
     static constexpr int kLpt = D / kVec;             // lanes per token row: 8, 16 or 32
     static constexpr int kTpp = 32 / kLpt;            // token rows per warp pass
@@ -131,7 +136,7 @@ struct DecodeTile {
     static constexpr int kStageBytes = 2 * kTps * kRowBytes;
     static constexpr int kStages = 65536 / kStageBytes;
     static constexpr int kItems = GT >= 4 ? 2 : 3;    // item slots in flight
-    static constexpr int kQBytes = GT * D * kElem;    // query rows of one item
+    static constexpr int kQBytes = GT * D * sizeof(T);  // query rows of one item
     static constexpr int kMergeFloats = kConsumerWarps * GT * (D + 2);  // per item slot
     static constexpr int kRingBytes = kStages * kStageBytes;
     static constexpr int kMetaOffset = kRingBytes;
@@ -139,7 +144,9 @@ struct DecodeTile {
     static constexpr int kItemOffset = kPOffset + kConsumerWarps * GT * kTps * 4;
     static constexpr int kQOffset = align16(kItemOffset + kItems * 32);
     static constexpr int kMergeOffset = kQOffset + kItems * align16(kQBytes);
-    static constexpr int kBarOffset = align16(kMergeOffset + kItems * kMergeFloats * 4);
+    // E4M3: the K and V scales of each stage's 16-token sub-blocks [kStages][2][kSubs]
+    static constexpr int kScaleOffset = align16(kMergeOffset + kItems * kMergeFloats * 4);
+    static constexpr int kBarOffset = kScaleOffset + (kFp8 ? kStages * 2 * kSubs * 4 : 0);
     // full[kStages], empty[kStages], q_full[kItems], item_free[kItems]
     static constexpr int kFlagOffset = kBarOffset + (2 * kStages + 2 * kItems) * 8;
     static constexpr int kSmemBytes = kFlagOffset + 16;
@@ -149,6 +156,7 @@ struct DecodeTile {
     static_assert(kPasses % 4 == 0 && kPasses * kTpp == kTps, "passes tile the stage");
     static_assert(kStages >= kConsumerWarps, "every consumer warp owns a stage");
     static_assert(GT > 1 || 3 * (kSmemBytes + 1024) <= 228 * 1024, "three CTAs per SM");
+    static_assert((kVec * sizeof(T)) % 16 == 0, "a lane's query slice is whole 16-byte loads");
 };
 
 // Reduce-scatter over the N values of each lane across the lanes xor-linked
@@ -223,14 +231,19 @@ __device__ __forceinline__ int seq_items(const SeqQueries& q, const DecodeParams
 
 // One stage (kTps tokens) of one consumer warp.  kFull: every token valid
 // for every row.  mask: tokens holding data; rmask[j]: tokens row j attends to.
-template <typename T, int D, int GT, bool kFull>
+// E4M3 caches: scl = the stage's K scales then V scales, one per 16-token
+// sub-block; a logit is (q . codes) x its K scale, and a probability is
+// multiplied by its V scale before it weights the V codes (the softmax sum
+// uses the probability itself).
+template <typename T, int D, int GT, typename TC, bool kFull>
 __device__ __forceinline__ void decode_stage(const unsigned char* sK, const unsigned char* sV,
                                              uint64_t mask, const uint64_t (&rmask)[GT],
-                                             const float (&qf)[GT][16 / sizeof(T)],
+                                             const float* scl,
+                                             const float (&qf)[GT][DecodeTile<T, D, GT, TC>::kVec],
                                              float (&m)[GT], float (&l)[GT],
-                                             float (&o)[GT][16 / sizeof(T)], float* pw, int grp,
-                                             int lig) {
-    using C = DecodeTile<T, D, GT>;
+                                             float (&o)[GT][DecodeTile<T, D, GT, TC>::kVec],
+                                             float* pw, int grp, int lig) {
+    using C = DecodeTile<T, D, GT, TC>;
     constexpr int kVec = C::kVec, kLpt = C::kLpt, kTpp = C::kTpp, kPasses = C::kPasses;
     float x[GT][kPasses];
 #pragma unroll
@@ -238,7 +251,7 @@ __device__ __forceinline__ void decode_stage(const unsigned char* sK, const unsi
         const uint4 raw =
             *reinterpret_cast<const uint4*>(sK + (ps * kTpp + grp) * C::kRowBytes + lig * 16);
         float kf[kVec];
-        Elem<T>::unpack(raw, kf);
+        Elem<TC>::unpack(raw, kf);
 #pragma unroll
         for (int j = 0; j < GT; ++j) {
             float acc = 0.f;
@@ -258,7 +271,9 @@ __device__ __forceinline__ void decode_stage(const unsigned char* sK, const unsi
         for (int i = 0; i < C::kVals; ++i) {
             const int ps = kPasses >= kLpt ? lig * C::kVals + i : lig / C::kDup;
             const int ti = ps * kTpp + grp;
-            xv[i] = (kFull || ((rmask[j] >> ti) & 1ull)) ? x[j][i] : -INFINITY;
+            float xi = x[j][i];
+            if constexpr (C::kFp8) xi *= scl[ti >> 4];
+            xv[i] = (kFull || ((rmask[j] >> ti) & 1ull)) ? xi : -INFINITY;
             mx = fmaxf(mx, xv[i]);
         }
 #pragma unroll
@@ -283,7 +298,9 @@ __device__ __forceinline__ void decode_stage(const unsigned char* sK, const unsi
 #pragma unroll
         for (int i = 0; i < C::kVals; ++i) {
             const int ps = kPasses >= kLpt ? lig * C::kVals + i : lig / C::kDup;
-            pw[(j * kTpp + grp) * kPasses + ps] = pv[i];
+            float pvi = pv[i];
+            if constexpr (C::kFp8) pvi *= scl[C::kSubs + ((ps * kTpp + grp) >> 4)];
+            pw[(j * kTpp + grp) * kPasses + ps] = pvi;
         }
     }
     __syncwarp();
@@ -304,7 +321,7 @@ __device__ __forceinline__ void decode_stage(const unsigned char* sK, const unsi
         if (!kFull && !((mask >> ti) & 1ull)) continue;  // masked rows may hold anything
         const uint4 raw = *reinterpret_cast<const uint4*>(sV + ti * C::kRowBytes + lig * 16);
         float vf[kVec];
-        Elem<T>::unpack(raw, vf);
+        Elem<TC>::unpack(raw, vf);
 #pragma unroll
         for (int j = 0; j < GT; ++j)
 #pragma unroll
@@ -316,9 +333,9 @@ __device__ __forceinline__ void decode_stage(const unsigned char* sK, const unsi
 
 // kMulti: several query tokens per sequence (query_start given); false
 // compiles the one-query-per-sequence decode without any of that logic.
-template <typename T, int D, int GT, bool kMulti>
+template <typename T, int D, int GT, bool kMulti, typename TC>
 __device__ __forceinline__ void decode_produce(const DecodeParams& p, unsigned char* smem) {
-    using C = DecodeTile<T, D, GT>;
+    using C = DecodeTile<T, D, GT, TC>;
     constexpr int W = C::kConsumerWarps;
     const int lane = threadIdx.x & 31;
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBarOffset);
@@ -453,7 +470,7 @@ __device__ __forceinline__ void decode_produce(const DecodeParams& p, unsigned c
             // query rows: tile_heads consecutive heads of each of the tile's tokens
             const uint32_t qf = qfull0 + 8 * islot;
             const uint32_t row_bytes =
-                kMulti ? static_cast<uint32_t>(p.tile_heads * D * C::kElem) : C::kQBytes;
+                kMulti ? static_cast<uint32_t>(p.tile_heads * D * sizeof(T)) : C::kQBytes;
             mbar_arrive_expect_tx(qf, row_bytes * ntok);
             const uint32_t dst = smem_addr(smem + C::kQOffset + islot * align16(C::kQBytes));
             for (int ti = 0; ti < ntok; ++ti)
@@ -469,6 +486,16 @@ __device__ __forceinline__ void decode_produce(const DecodeParams& p, unsigned c
         const int blk_end = (tok_end + B - 1) / B;
         int win = tok_begin / B;
         int32_t entry = (win + lane < blk_end) ? __ldg(trow + win + lane) : -1;
+        float ks_lane = 0.f, vs_lane = 0.f;  // E4M3: the scales of this lane's block
+        auto load_scales = [&]() {
+            if constexpr (C::kFp8) {
+                const bool in = static_cast<unsigned>(entry) < static_cast<unsigned>(p.num_blocks);
+                const size_t si = static_cast<size_t>(in ? entry : 0) * p.num_kv_heads + hk;
+                ks_lane = in ? __ldg(p.k_scale + si) : 0.f;
+                vs_lane = in ? __ldg(p.v_scale + si) : 0.f;
+            }
+        };
+        load_scales();
         const unsigned char* kbase = p.k_cache + static_cast<size_t>(hk) * head_bytes;
         const unsigned char* vbase = p.v_cache + static_cast<size_t>(hk) * head_bytes;
 
@@ -484,6 +511,7 @@ __device__ __forceinline__ void decode_produce(const DecodeParams& p, unsigned c
             const int t1 = min(t0 + C::kTps, tok_end);
             size_t src_off[C::kSubs];
             uint32_t len_bytes[C::kSubs];
+            float sub_scale[2 * C::kSubs];
             uint32_t bytes = 0;
             uint64_t mask = 0;
 #pragma unroll
@@ -491,6 +519,8 @@ __device__ __forceinline__ void decode_produce(const DecodeParams& p, unsigned c
                 const int t = t0 + 16 * r;
                 len_bytes[r] = 0;
                 src_off[r] = 0;
+                sub_scale[r] = 0.f;
+                sub_scale[C::kSubs + r] = 0.f;
                 if (t < t1) {  // warp-uniform
                     const int lb = t / B;
                     const int off = t - lb * B;
@@ -498,8 +528,13 @@ __device__ __forceinline__ void decode_produce(const DecodeParams& p, unsigned c
                     while (lb - win >= 32) {
                         win += 32;
                         entry = (win + lane < blk_end) ? __ldg(trow + win + lane) : -1;
+                        load_scales();
                     }
                     const int pb = __shfl_sync(0xffffffffu, entry, lb - win);
+                    if constexpr (C::kFp8) {
+                        sub_scale[r] = __shfl_sync(0xffffffffu, ks_lane, lb - win);
+                        sub_scale[C::kSubs + r] = __shfl_sync(0xffffffffu, vs_lane, lb - win);
+                    }
                     if (static_cast<unsigned>(pb) < static_cast<unsigned>(p.num_blocks)) {
                         src_off[r] = static_cast<size_t>(pb) * block_bytes +
                                      static_cast<size_t>(off) * C::kRowBytes;
@@ -522,6 +557,11 @@ __device__ __forceinline__ void decode_produce(const DecodeParams& p, unsigned c
                 meta[st].mask = mask;
                 meta[st].item_seq = static_cast<uint32_t>(item_seq);
                 meta[st].flags = flags;
+                if constexpr (C::kFp8) {
+                    float* sc = reinterpret_cast<float*>(smem + C::kScaleOffset) + st * 2 * C::kSubs;
+#pragma unroll
+                    for (int r = 0; r < 2 * C::kSubs; ++r) sc[r] = sub_scale[r];
+                }
                 const uint32_t full = full0 + 8 * st;
                 mbar_arrive_expect_tx(full, bytes);
                 const uint32_t sK = smem_addr(smem + st * C::kStageBytes);
@@ -586,9 +626,9 @@ __device__ __forceinline__ void decode_produce(const DecodeParams& p, unsigned c
 }
 
 
-template <typename T, int D, int GT, bool kMulti>
+template <typename T, int D, int GT, bool kMulti, typename TC>
 __device__ __forceinline__ void decode_consume(const DecodeParams& p, unsigned char* smem) {
-    using C = DecodeTile<T, D, GT>;
+    using C = DecodeTile<T, D, GT, TC>;
     constexpr int kVec = C::kVec, kLpt = C::kLpt, W = C::kConsumerWarps;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int grp = lane / kLpt;  // which row of a pass this lane reads
@@ -637,8 +677,13 @@ __device__ __forceinline__ void decode_consume(const DecodeParams& p, unsigned c
             const T* qs = reinterpret_cast<const T*>(smem + C::kQOffset + islot * align16(C::kQBytes));
 #pragma unroll
             for (int j = 0; j < GT; ++j) {
-                const uint4 raw = *reinterpret_cast<const uint4*>(qs + j * D + lig * kVec);
-                Elem<T>::unpack(raw, qf[j]);
+                // this lane's kVec query elements: one or two 16-byte loads
+#pragma unroll
+                for (int c16 = 0; c16 < kVec / Elem<T>::kVec; ++c16) {
+                    const uint4 raw = *reinterpret_cast<const uint4*>(qs + j * D + lig * kVec +
+                                                                      c16 * Elem<T>::kVec);
+                    Elem<T>::unpack(raw, qf[j] + c16 * Elem<T>::kVec);
+                }
 #pragma unroll
                 for (int v = 0; v < kVec; ++v) {
                     qf[j][v] *= p.qk_scale_log2;
@@ -665,10 +710,11 @@ __device__ __forceinline__ void decode_consume(const DecodeParams& p, unsigned c
 #pragma unroll
             for (int j = 0; j < GT; ++j) rmask[j] = mask;
         }
+        const float* scl = reinterpret_cast<const float*>(smem + C::kScaleOffset) + st * 2 * C::kSubs;
         if (mask == C::kFullMask && !(kMulti && (flags & kStageCausal)))
-            decode_stage<T, D, GT, true>(sK, sV, mask, rmask, qf, m, l, o, pw, grp, lig);
+            decode_stage<T, D, GT, TC, true>(sK, sV, mask, rmask, scl, qf, m, l, o, pw, grp, lig);
         else
-            decode_stage<T, D, GT, false>(sK, sV, mask, rmask, qf, m, l, o, pw, grp, lig);
+            decode_stage<T, D, GT, TC, false>(sK, sV, mask, rmask, scl, qf, m, l, o, pw, grp, lig);
         if (lane == 0) mbar_arrive(empty0 + 8 * st);
         if (!(flags & kStageLast)) continue;
 
@@ -749,10 +795,10 @@ __device__ __forceinline__ void decode_consume(const DecodeParams& p, unsigned c
     }
 }
 
-template <typename T, int D, int GT, bool kMulti>
-__global__ void __launch_bounds__(DecodeTile<T, D, GT>::kThreads)
+template <typename T, int D, int GT, bool kMulti, typename TC>
+__global__ void __launch_bounds__(DecodeTile<T, D, GT, TC>::kThreads)
     decode_persistent_kernel(const DecodeParams p) {
-    using C = DecodeTile<T, D, GT>;
+    using C = DecodeTile<T, D, GT, TC>;
     extern __shared__ __align__(128) unsigned char smem[];
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBarOffset);
     if (threadIdx.x == 0) {
@@ -770,9 +816,9 @@ __global__ void __launch_bounds__(DecodeTile<T, D, GT>::kThreads)
     }
     __syncthreads();
     if ((threadIdx.x >> 5) == C::kConsumerWarps)
-        decode_produce<T, D, GT, kMulti>(p, smem);
+        decode_produce<T, D, GT, kMulti, TC>(p, smem);
     else
-        decode_consume<T, D, GT, kMulti>(p, smem);
+        decode_consume<T, D, GT, kMulti, TC>(p, smem);
     __syncthreads();
     if (threadIdx.x == 0) {
         // The last CTA out returns both counters to zero for the next call.
@@ -850,12 +896,12 @@ __global__ void __launch_bounds__(128) decode_reduce_kernel(const DecodeParams p
     }
 }
 
-template <typename T, int D, int GT, bool kMulti>
+template <typename T, int D, int GT, bool kMulti, typename TC = T>
 inline pa_status launch_decode_tile(const DecodeParams& p, cudaStream_t stream) {
-    using C = DecodeTile<T, D, GT>;
+    using C = DecodeTile<T, D, GT, TC>;
     static std::atomic<uint64_t> smem_configured{0};  // one per instantiation
     static std::atomic<int> ctas_per_sm{0};
-    auto kernel = decode_persistent_kernel<T, D, GT, kMulti>;
+    auto kernel = decode_persistent_kernel<T, D, GT, kMulti, TC>;
     if (ensure_smem(kernel, C::kSmemBytes, smem_configured) != PA_OK) return PA_ERR_CUDA;
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
@@ -908,6 +954,17 @@ inline pa_status launch_decode_typed(const DecodeParams& p, int head_dim, int gt
     return PA_ERR_UNSUPPORTED;
 }
 
+// E4M3 caches (head_dim 128), q / out of type T.
+template <typename T, bool kMulti>
+inline pa_status launch_decode_fp8_typed(const DecodeParams& p, int gt, cudaStream_t stream) {
+    switch (gt) {
+        case 1: return launch_decode_tile<T, 128, 1, kMulti, __nv_fp8_e4m3>(p, stream);
+        case 2: return launch_decode_tile<T, 128, 2, kMulti, __nv_fp8_e4m3>(p, stream);
+        case 4: return launch_decode_tile<T, 128, 4, kMulti, __nv_fp8_e4m3>(p, stream);
+    }
+    return PA_ERR_UNSUPPORTED;
+}
+
 // One per element type and query form, each in its own translation unit.
 pa_status launch_decode_f32(const DecodeParams& p, int head_dim, int gt, cudaStream_t stream);
 pa_status launch_decode_f16(const DecodeParams& p, int head_dim, int gt, cudaStream_t stream);
@@ -916,5 +973,7 @@ pa_status launch_multi_query_f32(const DecodeParams& p, int head_dim, int gt, cu
 pa_status launch_multi_query_f16(const DecodeParams& p, int head_dim, int gt, cudaStream_t stream);
 pa_status launch_multi_query_bf16(const DecodeParams& p, int head_dim, int gt,
                                   cudaStream_t stream);
+pa_status launch_decode_fp8_f16(const DecodeParams& p, int gt, cudaStream_t stream);
+pa_status launch_decode_fp8_bf16(const DecodeParams& p, int gt, cudaStream_t stream);
 
 }  // namespace pa

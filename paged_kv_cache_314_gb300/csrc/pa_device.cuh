@@ -5,6 +5,7 @@
 
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <stdint.h>
 
 #include "pa.h"
@@ -178,6 +179,28 @@ struct Elem<__nv_bfloat16> {
     }
     __device__ __forceinline__ static float to_float(__nv_bfloat16 x) { return __bfloat162float(x); }
     __device__ __forceinline__ static __nv_bfloat16 from_float(float x) { return __float2bfloat16_rn(x); }
+};
+
+// FP8 E4M3 cache elements (codes; the per-block scale is applied by the
+// caller).  Every E4M3 value is exact in binary16, so each pair of codes is
+// widened by the hardware conversion to a half2 and then to two floats.
+template <>
+struct Elem<__nv_fp8_e4m3> {
+    static constexpr int kVec = 16;
+    __device__ __forceinline__ static void unpack(const uint4& u, float* f) {
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+                const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(
+                    static_cast<__nv_fp8x2_storage_t>(w[i] >> (16 * k)), __NV_E4M3);
+                const float2 v = __half22float2(*reinterpret_cast<const __half2*>(&hr));
+                f[4 * i + 2 * k] = v.x;
+                f[4 * i + 2 * k + 1] = v.y;
+            }
+        }
+    }
 };
 
 }  // namespace pa

@@ -508,8 +508,9 @@ E4M3_NAN = 0x7F  # poison code of E4M3 pools
 def to_fp8(w: Workload, seed: int = 0) -> Workload:
     """The same workload over an E4M3 cache: one fp32 scale per (physical
     block, kv head) for K and one for V, 2^-6 * exp(N(0, 0.3^2)), and the pool
-    codes = the existing values divided by their block's scale, converted to
-    float8_e4m3fn by torch (input data; poison slots become the NaN code).
+    codes = the existing values divided by their block's scale, clamped to
+    +-448 and converted to float8_e4m3fn by torch (input data; poison slots
+    become the NaN code).
     q, the new tokens and the output keep the workload's dtype."""
     import torch
     rng = np.random.default_rng(seed)
@@ -522,7 +523,7 @@ def to_fp8(w: Workload, seed: int = 0) -> Workload:
             x = torch.from_numpy(pool.view(np.int16)).view(torch.bfloat16).float()
         else:
             x = torch.from_numpy(np.ascontiguousarray(pool)).float()
-        x = x / torch.from_numpy(sc)[:, :, None, None]
+        x = (x / torch.from_numpy(sc)[:, :, None, None]).clamp(-448.0, 448.0)  # NaN stays NaN
         return x.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
 
     return dataclasses.replace(w, name=w.name + "_fp8", k_cache=codes(w.k_cache, ks),

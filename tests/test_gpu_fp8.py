@@ -1,0 +1,150 @@
+"""GPU parity of the E4M3 cache path against the fp64 oracle.
+
+kv_write_fp8 (the quantisation of the new tokens) and copy_blocks_fp8 /
+swap_blocks_fp8 must match the oracle bit for bit over the whole pool, codes
+and scales; decode_fp8 within the 16-bit tolerances of tests/gpu_util.TOL
+(both sides read the same codes and scales; the oracle in fp64).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_cache_314_gb300 as pa
+from paged_kv_cache_314_gb300 import _build
+from paged_kv_cache_314_gb300 import workloads as wl
+
+from gpu_util import assert_close, out_f64, same_bits, to_torch
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    _build.build()
+    pa.load()
+
+
+def _upload(w):
+    dt = w.dtype
+    return {
+        "q": to_torch(w.q, dt).cuda(), "k_new": to_torch(w.k_new, dt).cuda(),
+        "v_new": to_torch(w.v_new, dt).cuda(),
+        "k_cache": torch.from_numpy(w.k_cache).cuda(), "v_cache": torch.from_numpy(w.v_cache).cuda(),
+        "k_scale": torch.from_numpy(w.k_scale).cuda(), "v_scale": torch.from_numpy(w.v_scale).cuda(),
+        "block_tables": torch.from_numpy(w.block_tables).cuda(),
+        "context_lens": torch.from_numpy(w.context_lens).cuda(),
+        "slot_mapping": torch.from_numpy(w.slot_mapping).cuda(),
+        "block_mapping": torch.from_numpy(w.block_mapping.reshape(-1, 2)).cuda(),
+        "d_err": torch.zeros(1, dtype=torch.int32, device="cuda"),
+    }
+
+
+def _gpu_step(w, d, partition_tokens=None):
+    P = w.partition_tokens if partition_tokens is None else partition_tokens
+    if w.num_pairs:
+        pa.copy_blocks_fp8(d["k_cache"], d["v_cache"], d["k_scale"], d["v_scale"],
+                           d["block_mapping"], d_err=d["d_err"])
+    if w.num_tokens:
+        pa.kv_write_fp8(d["k_new"], d["v_new"], d["k_cache"], d["v_cache"], d["k_scale"],
+                        d["v_scale"], d["slot_mapping"], d_err=d["d_err"])
+    out = torch.empty_like(d["q"])
+    pa.decode_fp8(out, d["q"], d["k_cache"], d["v_cache"], d["k_scale"], d["v_scale"],
+                  d["block_tables"], d["context_lens"], w.scale, partition_tokens=P,
+                  d_err=d["d_err"])
+    torch.cuda.synchronize()
+    return out
+
+
+def _check(w, partition_tokens=None):
+    d = _upload(w)
+    out = _gpu_step(w, d, partition_tokens)
+    (kc, ks), (vc, vs), ref, err = oracle.step(w)
+    assert int(d["d_err"].item()) == err, (int(d["d_err"].item()), err)
+    assert same_bits(d["k_cache"].cpu().numpy(), kc), "K codes differ from the oracle"
+    assert same_bits(d["v_cache"].cpu().numpy(), vc), "V codes differ from the oracle"
+    assert same_bits(d["k_scale"].cpu().numpy(), ks) and same_bits(d["v_scale"].cpu().numpy(), vs)
+    return assert_close(out_f64(out), ref, w.dtype, w.name), out, d
+
+
+FP8_SMALL = [
+    # q dtype, Hq, Hkv, B, ctx
+    ("f16", 4, 4, 16, [1, 15, 16, 17, 31, 32, 33, 300, 700]),
+    ("bf16", 8, 2, 16, [1, 16, 17, 300, 515]),      # 4 q heads per kv head
+    ("bf16", 16, 2, 32, [3, 100, 257, 600]),        # 8 per kv head: tiles of 4
+    ("f16", 6, 1, 64, [1, 63, 64, 65, 400]),        # 6 per kv head: tiles of 2
+    ("bf16", 4, 4, 128, [1, 127, 128, 129, 1000]),
+]
+
+
+@pytest.mark.parametrize("case", range(len(FP8_SMALL)))
+@pytest.mark.parametrize("partition", [0, "block", "whole"])
+def test_fp8_small_parity(case, partition):
+    dtype, Hq, Hkv, B, ctx = FP8_SMALL[case]
+    w = wl.to_fp8(wl.custom(f"fp8_{case}", ctx, dtype=dtype, num_q_heads=Hq, num_kv_heads=Hkv,
+                            head_dim=128, block_size=B, seed=500 + case, pool_factor=1.3),
+                  seed=510 + case)
+    P = {0: 0, "block": B, "whole": w.max_blocks_per_seq * B}[partition]
+    _check(w, partition_tokens=P)
+
+
+@pytest.mark.parametrize("name", ["llama7b_fp8", "gqa_share_fp8"])
+def test_fp8_named_full_size(name):
+    stats, _, _ = _check(wl.by_name(name))
+    print(name, stats)
+
+
+def test_fp8_kv_write_saturates_and_keeps_signed_zeros():
+    w = wl.to_fp8(wl.custom("fp8_sat", [5, 40, 17], dtype="bf16", num_q_heads=2, num_kv_heads=2,
+                            head_dim=128, block_size=16, seed=520), seed=521)
+    k = w.k_new.reshape(-1)
+    k[:6] = wl._to_storage(np.array([1e4, -1e4, 0.0, -0.0, 3e-7, -3e-7], np.float32), "bf16")
+    _check(w)
+
+
+def test_fp8_bad_entries_are_flagged_and_skipped():
+    w = wl.to_fp8(wl.custom("fp8_bad", [40, 300, 600, 5, 0, 260], dtype="f16", num_q_heads=8,
+                            num_kv_heads=2, head_dim=128, block_size=16, seed=530,
+                            max_blocks_per_seq=40), seed=531)
+    w.context_lens[0] = -3
+    w.context_lens[3] = 40 * 16 + 1
+    w.block_tables[2, 7] = w.num_blocks + 5
+    w.block_tables[5, 0] = -7
+    d = _upload(w)
+    out = _gpu_step(w, d, partition_tokens=256)
+    _, _, ref, err = oracle.step(w)
+    assert err == oracle.ERR_CTX_OOB | oracle.ERR_BLOCK_OOB
+    assert int(d["d_err"].item()) == err
+    assert_close(out_f64(out), ref, "f16", "fp8_bad")
+    assert (out[0] == 0).all() and (out[3] == 0).all() and (out[4] == 0).all()
+
+
+def test_fp8_swap_round_trip_through_pinned_host_memory():
+    w = wl.to_fp8(wl.custom("fp8_swap", [100, 333, 64], dtype="bf16", num_q_heads=4,
+                            num_kv_heads=4, head_dim=128, block_size=16, seed=540), seed=541)
+    d = _upload(w)
+    NB = w.num_blocks
+    host = [torch.zeros(t.shape, dtype=t.dtype).pin_memory()
+            for t in (d["k_cache"], d["v_cache"], d["k_scale"], d["v_scale"])]
+    blocks = [int(b) for b in w.block_tables[1, :21]]
+    out_map = torch.tensor([[b, i] for i, b in enumerate(blocks)], dtype=torch.int32, device="cuda")
+    pa.swap_blocks_fp8(d["k_cache"], d["v_cache"], d["k_scale"], d["v_scale"], host[0], host[1],
+                       host[2], host[3], out_map, d_err=d["d_err"])
+    torch.cuda.synchronize()
+    kc, vc = w.k_cache, w.v_cache
+    hk, hv, hks, hvs = (t.numpy() for t in host)
+    for i, b in enumerate(blocks):
+        assert same_bits(hk[i], kc[b]) and same_bits(hv[i], vc[b])
+        assert hks[i].tolist() == w.k_scale[b].tolist() and hvs[i].tolist() == w.v_scale[b].tolist()
+    # swap back into other blocks of a fresh device pool
+    dst = [torch.zeros_like(t) for t in (d["k_cache"], d["v_cache"], d["k_scale"], d["v_scale"])]
+    in_map = torch.tensor([[i, NB - 1 - i] for i in range(len(blocks))], dtype=torch.int32,
+                          device="cuda")
+    pa.swap_blocks_fp8(host[0], host[1], host[2], host[3], dst[0], dst[1], dst[2], dst[3], in_map,
+                       d_err=d["d_err"])
+    torch.cuda.synchronize()
+    assert int(d["d_err"].item()) == 0
+    for i, b in enumerate(blocks):
+        assert same_bits(dst[0][NB - 1 - i].cpu().numpy(), kc[b])
+        assert same_bits(dst[3][NB - 1 - i].cpu().numpy(), w.v_scale[b])

@@ -145,3 +145,14 @@ def test_multi_query_plans_write_every_query_token(make):
                 v = w.k_cache[int(w.block_tables[s, t // B]), 0, t % B]
                 bits = v.view(np.uint32 if w.dtype == "f32" else np.uint16)
                 assert np.all(bits == wl.POISON_BITS[w.dtype]) == (t >= n - L)
+
+
+def test_fp8_workload_codes_are_finite_where_data_lives():
+    w = wl.to_fp8(wl.llama7b(num_seqs=4, ctx_range=(100, 400)), seed=3)
+    B = w.block_size
+    for s in range(w.num_seqs):
+        n = int(w.context_lens[s])
+        for t in range(n - 1):  # cached tokens (the last one is written by the step)
+            b = int(w.block_tables[s, t // B])
+            assert np.all((w.k_cache[b, :, t % B] & 0x7F) != 0x7F)
+            assert np.all((w.v_cache[b, :, t % B] & 0x7F) != 0x7F)
