@@ -254,10 +254,10 @@ __device__ __forceinline__ void decode_stage(const unsigned char* sK, const unsi
         Elem<TC>::unpack(raw, kf);
 #pragma unroll
         for (int j = 0; j < GT; ++j) {
-            float acc = 0.f;
+            float a0 = 0.f, a1 = 0.f;  // even and odd elements, packed multiply-adds
 #pragma unroll
-            for (int v = 0; v < kVec; ++v) acc = fmaf(qf[j][v], kf[v], acc);
-            x[j][ps] = acc;
+            for (int v = 0; v < kVec; v += 2) fma2(a0, a1, qf[j][v], qf[j][v + 1], kf[v], kf[v + 1]);
+            x[j][ps] = a0 + a1;
         }
     }
 #pragma unroll
@@ -325,7 +325,8 @@ __device__ __forceinline__ void decode_stage(const unsigned char* sK, const unsi
 #pragma unroll
         for (int j = 0; j < GT; ++j)
 #pragma unroll
-            for (int v = 0; v < kVec; ++v) o[j][v] = fmaf(pp[j][ps], vf[v], o[j][v]);
+            for (int v = 0; v < kVec; v += 2)
+                fma2(o[j][v], o[j][v + 1], pp[j][ps], pp[j][ps], vf[v], vf[v + 1]);
     }
     __syncwarp();  // pw is rewritten by this warp's next stage
 }

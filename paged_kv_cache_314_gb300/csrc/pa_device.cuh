@@ -132,6 +132,17 @@ __device__ __forceinline__ void named_barrier(int id, int threads) {
 
 // ---- element conversions ----------------------------------------------------
 
+// Packed fp32 multiply-add on two lanes of a register pair (sm_100 family):
+// (d0, d1) = (a0 * b0 + d0, a1 * b1 + d1), each rounded to nearest as fmaf.
+__device__ __forceinline__ void fma2(float& d0, float& d1, float a0, float a1, float b0, float b1) {
+    uint64_t d, a, b;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(a) : "f"(a0), "f"(a1));
+    asm("mov.b64 %0, {%1, %2};" : "=l"(b) : "f"(b0), "f"(b1));
+    asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "f"(d0), "f"(d1));
+    asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(d) : "l"(a), "l"(b));
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(d0), "=f"(d1) : "l"(d));
+}
+
 template <typename T>
 struct Elem;
 
