@@ -29,9 +29,10 @@
 //    each K/V byte is read once per step.
 //  * Warps 0-3 consume, each one whole stage at a time (stage c belongs to
 //    warp c mod 4, so warps never wait on one another inside an item).  A
-//    lane owns one 16-byte column slice of a token row (kLpt lanes per row),
-//    so one 128-bit shared load per lane reads kTpp whole rows without bank
-//    conflicts.  The per-lane partial dot products of a stage are finished by
+//    lane owns one 16-byte column slice of a token row (8 bytes for E4M3
+//    caches; kLpt lanes per row), so one shared load per lane reads kTpp
+//    whole rows without bank conflicts.  Multiply-adds are packed two to an
+//    instruction (fma.rn.f32x2).  The per-lane partial dot products of a stage are finished by
 //    a reduce-scatter butterfly (each level halves the values a lane keeps),
 //    which leaves every lane with whole logits of its own tokens: one exp2 per
 //    lane per stage.  The probabilities go through shared memory to the lanes
@@ -45,10 +46,19 @@
 //    check are masked by select, never by arithmetic, so poison in unused
 //    slots (NaN) cannot leak into the result.  Stages whose tokens are all
 //    valid take a path without any masking.
+//  * Several query tokens per sequence (kMulti): an item covers up to GT
+//    rows = query tokens x heads of one kv head, all reading the same
+//    stages; a stage in which some row's causal limit ends carries that limit
+//    and the rows are masked one by one.
+//  * E4M3 caches (TC = __nv_fp8_e4m3): the producer stages the K and V scale
+//    of every 16-token sub-block beside the stage; logits are scaled by the
+//    K scale and probabilities by the V scale before they weight V.
 //  * Every wait is bounded (mbar_wait): on timeout the CTA reports
 //    PA_DERR_TIMEOUT, stops issuing copies, waits for the copies it already
 //    issued and returns; outputs of unfinished items are left unset.
 #pragma once
+
+#include <type_traits>
 
 #include "pa_device.cuh"
 #include "pa_host.h"
@@ -121,7 +131,10 @@ template <typename T, int D, int GT, typename TC = T>
 struct DecodeTile {
     static constexpr int kElem = sizeof(TC);          // cache element bytes
     static constexpr bool kFp8 = sizeof(TC) == 1;
-    static constexpr int kVec = 16 / kElem;           // elements per 16-byte access
+    // bytes of a token row one lane reads: 16, or 8 for E4M3 (so a lane holds
+    // 8 elements either way and the query slices and accumulators stay small)
+    static constexpr int kSlice = kFp8 ? 8 : 16;
+    static constexpr int kVec = kSlice / kElem;       // elements per lane slice
     static constexpr int kLpt = D / kVec;             // lanes per token row: 8, 16 or 32
     static constexpr int kTpp = 32 / kLpt;            // token rows per warp pass
     static constexpr int kRowBytes = D * kElem;
@@ -157,6 +170,7 @@ struct DecodeTile {
     static_assert(kStages >= kConsumerWarps, "every consumer warp owns a stage");
     static_assert(GT > 1 || 3 * (kSmemBytes + 1024) <= 228 * 1024, "three CTAs per SM");
     static_assert((kVec * sizeof(T)) % 16 == 0, "a lane's query slice is whole 16-byte loads");
+    using Slice = typename std::conditional<kFp8, uint2, uint4>::type;
 };
 
 // Reduce-scatter over the N values of each lane across the lanes xor-linked
@@ -248,8 +262,8 @@ __device__ __forceinline__ void decode_stage(const unsigned char* sK, const unsi
     float x[GT][kPasses];
 #pragma unroll
     for (int ps = 0; ps < kPasses; ++ps) {
-        const uint4 raw =
-            *reinterpret_cast<const uint4*>(sK + (ps * kTpp + grp) * C::kRowBytes + lig * 16);
+        const typename C::Slice raw = *reinterpret_cast<const typename C::Slice*>(
+            sK + (ps * kTpp + grp) * C::kRowBytes + lig * C::kSlice);
         float kf[kVec];
         Elem<TC>::unpack(raw, kf);
 #pragma unroll
@@ -319,7 +333,8 @@ __device__ __forceinline__ void decode_stage(const unsigned char* sK, const unsi
     for (int ps = 0; ps < kPasses; ++ps) {
         const int ti = ps * kTpp + grp;
         if (!kFull && !((mask >> ti) & 1ull)) continue;  // masked rows may hold anything
-        const uint4 raw = *reinterpret_cast<const uint4*>(sV + ti * C::kRowBytes + lig * 16);
+        const typename C::Slice raw =
+            *reinterpret_cast<const typename C::Slice*>(sV + ti * C::kRowBytes + lig * C::kSlice);
         float vf[kVec];
         Elem<TC>::unpack(raw, vf);
 #pragma unroll

@@ -193,15 +193,16 @@ struct Elem<__nv_bfloat16> {
 };
 
 // FP8 E4M3 cache elements (codes; the per-block scale is applied by the
-// caller).  Every E4M3 value is exact in binary16, so each pair of codes is
-// widened by the hardware conversion to a half2 and then to two floats.
+// caller), read 8 bytes at a time.  Every E4M3 value is exact in binary16, so
+// each pair of codes is widened by the hardware conversion to a half2 and
+// then to two floats.
 template <>
 struct Elem<__nv_fp8_e4m3> {
-    static constexpr int kVec = 16;
-    __device__ __forceinline__ static void unpack(const uint4& u, float* f) {
-        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+    static constexpr int kVec = 8;  // elements per 8-byte slice
+    __device__ __forceinline__ static void unpack(const uint2& u, float* f) {
+        const uint32_t w[2] = {u.x, u.y};
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
+        for (int i = 0; i < 2; ++i) {
 #pragma unroll
             for (int k = 0; k < 2; ++k) {
                 const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(
