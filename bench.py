@@ -70,6 +70,16 @@ WORKLOAD_TEXT = {
 FP32_LANES_PER_SM = 128
 
 
+def _tensor_peak():
+    """Dense bf16 tensor peak: the measured burst figure (the attention call is
+    timed on its own, well under a second)."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except (OSError, ValueError, KeyError):
+        return 1900.0, "fallback"
+
+
 def _alu_peak_tflops(sm_count):
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -447,12 +457,32 @@ def run_gpu(args):
     alu_peak = _alu_peak_tflops(sms)
     kernel = "pa_multi_query (partition kernel + split-K merge)" if mq else \
         "pa_decode (partition kernel + split-K merge)"
-    # The binding roofline: HBM for the K/V stream unless the SIMT arithmetic
-    # needs longer at its peak (many query rows per K/V byte).
-    tc_path = (not mq and w.dtype in ("f16", "bf16") and w.head_dim == 128
-               and 4 <= w.num_q_heads // w.num_kv_heads <= 16 and P % 128 == 0)
+    # The binding roofline: HBM for the K/V stream unless the arithmetic needs
+    # longer at its peak (many query rows per K/V byte): fp32 FMA on the SIMT
+    # path, bf16/fp16 tensor cores on the tensor-core path (the library's
+    # dispatch rule: 16-bit K/V, head_dim 128, partitions of 128k tokens, and
+    # at least 4 query rows per kv head in an item).
+    g = w.num_q_heads // w.num_kv_heads
+    tc_tokens = 1
+    if mq:
+        avg = -(-w.num_query_tokens // w.num_seqs)
+        while tc_tokens * 2 * g <= 16 and tc_tokens < avg:
+            tc_tokens *= 2
+    tc_path = (not fp8 and w.dtype in ("f16", "bf16") and w.head_dim == 128 and g <= 16
+               and P % 128 == 0 and (tc_tokens * g >= 4 if mq else g >= 4))
+    tensor_peak, tensor_kind = _tensor_peak()
+    tensor_bound = tc_path and flops / (tensor_peak * 1e12) > unique_bytes / (peak * 1e9)
     alu_bound = not tc_path and flops / (alu_peak * 1e12) > unique_bytes / (peak * 1e9)
-    if alu_bound:
+    if tensor_bound:
+        ach = flops / (dec_ms_avg * 1e-3) / 1e12
+        roof = {"bound": "tensor", "kernel": kernel, "achieved": round(ach, 3),
+                "peak": tensor_peak, "unit": "TFLOP/s", "frac": round(ach / tensor_peak, 4),
+                "peak_source": f"{tensor_kind} bf16_tflops (fp16 MMA runs at the bf16 rate)",
+                "flops": "4 x head_dim per (query row, head, token attended)",
+                "traffic": None, "algorithmic_flops_per_launch": int(flops),
+                "hbm_achieved_gbs": round(unique_bytes / (dec_ms_avg * 1e-3) / 1e9, 2),
+                "avg_launch_ms": round(dec_ms_avg, 5)}
+    elif alu_bound:
         ach = flops / (dec_ms_avg * 1e-3) / 1e12
         roof = {"bound": "alu", "kernel": kernel, "achieved": round(ach, 3),
                 "peak": round(alu_peak, 1), "unit": "TFLOP/s", "frac": round(ach / alu_peak, 4),

@@ -225,14 +225,30 @@ pa_status run_attention(const AttnCall& a) {
         return a.dtype == PA_BF16 ? launch_decode_fp8_bf16(p, gt, st)
                                   : launch_decode_fp8_f16(p, gt, st);
     }
-    // Grouped-query decode with 16-bit K/V and head_dim 128: the tensor-core path.
+    // 16-bit K/V with head_dim 128 and at least 4 query rows per kv head in a
+    // work item (grouped heads, or several query tokens x heads): the
+    // tensor-core path, items of all g heads of one kv head.
     const long long pool_rows = static_cast<long long>(a.num_blocks) * a.num_kv_heads * a.block_size;
-    if (a.query_start == nullptr && tc_shape(a.num_q_heads, a.num_kv_heads, a.head_dim, a.dtype) &&
-        P % 128 == 0 && pool_rows < 0x7fffffffLL) {
+    const bool tc_ok = (a.dtype == PA_F16 || a.dtype == PA_BF16) && a.head_dim == 128 &&
+                       P % 128 == 0 && pool_rows < 0x7fffffffLL && group <= 16;
+    int tc_tokens = 1;  // query tokens per tensor-core item: up to 16 rows
+    if (a.query_start != nullptr && a.num_seqs > 0) {
+        const long long avg = (static_cast<long long>(a.num_query_tokens) + a.num_seqs - 1) / a.num_seqs;
+        while (tc_tokens * 2 * group <= 16 && tc_tokens < avg) tc_tokens *= 2;
+    }
+    const bool tc_rows = a.query_start == nullptr
+                             ? tc_shape(a.num_q_heads, a.num_kv_heads, a.head_dim, a.dtype)
+                             : tc_tokens * group >= 4;
+    if (tc_ok && tc_rows) {
         CUtensorMap map_k, map_v;
         if (make_pool_map(&map_k, a.k_cache, pool_rows, a.dtype) &&
             make_pool_map(&map_v, a.v_cache, pool_rows, a.dtype)) {
             p.head_tiles = a.num_kv_heads;
+            p.tile_heads = group;
+            p.tile_tokens = tc_tokens;
+            if (a.query_start != nullptr)
+                return a.dtype == PA_BF16 ? launch_multi_query_tc_bf16(p, map_k, map_v, st)
+                                          : launch_multi_query_tc_f16(p, map_k, map_v, st);
             return a.dtype == PA_BF16 ? launch_decode_tc_bf16(p, map_k, map_v, st)
                                       : launch_decode_tc_f16(p, map_k, map_v, st);
         }

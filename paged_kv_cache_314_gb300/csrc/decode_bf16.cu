@@ -9,6 +9,6 @@ pa_status launch_decode_bf16(const DecodeParams& p, int head_dim, int gt, cudaSt
 }
 pa_status launch_decode_tc_bf16(const DecodeParams& p, const CUtensorMap& mapK,
                                const CUtensorMap& mapV, cudaStream_t stream) {
-    return launch_decode_tc_typed<__nv_bfloat16>(p, mapK, mapV, stream);
+    return launch_decode_tc_typed<__nv_bfloat16, false>(p, mapK, mapV, stream);
 }
 }  // namespace pa

@@ -9,6 +9,6 @@ pa_status launch_decode_f16(const DecodeParams& p, int head_dim, int gt, cudaStr
 }
 pa_status launch_decode_tc_f16(const DecodeParams& p, const CUtensorMap& mapK,
                                const CUtensorMap& mapV, cudaStream_t stream) {
-    return launch_decode_tc_typed<__half>(p, mapK, mapV, stream);
+    return launch_decode_tc_typed<__half, false>(p, mapK, mapV, stream);
 }
 }  // namespace pa

@@ -60,8 +60,8 @@ struct TcTile {
     static constexpr int kPopOff = kQopOff + kOpBytes;
     static constexpr int kRedOff = kPopOff + 2 * kOpBytes;        // P double-buffered; [4][16] floats
     static constexpr int kRecOff = kRedOff + 4 * kN * 4;          // item records [kQSlots]
-    static constexpr int kMetaOff = kRecOff + kQSlots * 16;       // stage meta [kStages]
-    static constexpr int kBarOff = kMetaOff + kStages * 16;
+    static constexpr int kMetaOff = kRecOff + kQSlots * 32;       // stage meta [kStages]
+    static constexpr int kBarOff = kMetaOff + kStages * 32;
     // full[S], empty[S], qfull[Q], qempty[Q], q_ready, s_full[2], p_full[2], o_full[2], drain
     static constexpr int kNumBars = 2 * kStages + 2 * kQSlots + 8;
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;       // tmem base, abort, team flags
@@ -78,13 +78,20 @@ struct TcStageMeta {
     int nvalid;       // tokens of the stage before the partition end
     uint32_t groups;  // bit r: 16-token group r was loaded (its block id passed the check)
     uint32_t flags;   // kStageFirst / kStageLast / kStageEnd
+    int lim_rel;      // several queries: tokens of this stage the item's first query sees
+    int pad[3];
 };
 
 struct TcItemRec {
-    int s, hq0, part, nparts;  // nparts 0: context length out of range (zero rows)
+    int row0;    // q / out row of the item's first query token
+    int hq0;     // first query head (all g heads of one kv head)
+    int part;    // partition index
+    int nparts;  // 0: context length out of range (zero rows)
+    int nrows;   // valid rows: query tokens x g (g for one query per sequence)
+    int pad[3];
 };
 
-template <typename T>
+template <typename T, bool kMulti>
 __device__ __forceinline__ void tc_produce(const DecodeParams& p, const CUtensorMap* mapK,
                                            const CUtensorMap* mapV, unsigned char* sm,
                                            uint32_t base) {
@@ -102,10 +109,25 @@ __device__ __forceinline__ void tc_produce(const DecodeParams& p, const CUtensor
     const int S = p.num_seqs, HT = p.head_tiles, P = p.partition_tokens, B = p.block_size;
     const int g = p.group;
     const int max_ctx = p.max_blocks_per_seq * B;
-    const uint32_t qbytes = static_cast<uint32_t>(g * C::D * 2);
+    const uint32_t row_bytes = static_cast<uint32_t>(g * C::D * 2);  // one token's g query rows
 
+    // Cursor over the sequence-major item numbering (as in the SIMT path):
+    // lane l holds sequence win0 + l and its number of items.
     int s_cur = 0, base_items = 0, win0 = 0;
-    int ctx_lane = lane < S ? __ldg(p.context_lens + lane) : 0;
+    SeqQueries sq_lane{0, 0, 0, kMulti};
+    int items_lane = 0;
+    auto load_window = [&]() {
+        const int sl = win0 + lane;
+        if constexpr (kMulti) {
+            sq_lane = sl < S ? seq_queries(p, sl) : SeqQueries{0, 0, 0, true};
+            items_lane = sl < S ? seq_items(sq_lane, p, max_ctx) : 0;
+            if (sl < S && !sq_lane.rows_ok(p.num_query_tokens)) report(p.d_err, PA_DERR_CTX_OOB);
+        } else {
+            sq_lane.ctx = sl < S ? __ldg(p.context_lens + sl) : 0;
+            items_lane = sl < S ? HT * items_of(sq_lane.ctx, max_ctx, P) : 0;
+        }
+    };
+    load_window();
     int c = 0, item_seq = 0, q_issued = 0;
     bool aborted = false, oob = false;
     int item_id = 0;
@@ -117,10 +139,10 @@ __device__ __forceinline__ void tc_produce(const DecodeParams& p, const CUtensor
         while (s_cur < S) {
             if (s_cur - win0 >= 32) {
                 win0 = s_cur;
-                ctx_lane = win0 + lane < S ? __ldg(p.context_lens + win0 + lane) : 0;
+                load_window();
             }
             const int sl = win0 + lane;
-            const int cnt = (sl >= s_cur && sl < S) ? HT * items_of(ctx_lane, max_ctx, P) : 0;
+            const int cnt = (sl >= s_cur && sl < S) ? items_lane : 0;
             int incl = cnt;
 #pragma unroll
             for (int off = 1; off < 32; off <<= 1) {
@@ -144,15 +166,39 @@ __device__ __forceinline__ void tc_produce(const DecodeParams& p, const CUtensor
         if (lane == 0) next_id = static_cast<int>(atomicAdd(p.counters, 1u));
 
         const int s = s_cur;
-        const int ctx = __shfl_sync(0xffffffffu, ctx_lane, s_cur - win0);
-        const bool valid = ctx >= 0 && ctx <= max_ctx;
-        const int np = items_of(ctx, max_ctx, P);
+        SeqQueries sq;
+        sq.ctx = __shfl_sync(0xffffffffu, sq_lane.ctx, s_cur - win0);
+        sq.multi = kMulti;
+        if constexpr (kMulti) {
+            sq.q0 = __shfl_sync(0xffffffffu, sq_lane.q0, s_cur - win0);
+            sq.q1 = __shfl_sync(0xffffffffu, sq_lane.q1, s_cur - win0);
+        } else {
+            sq.q0 = s;
+            sq.q1 = s + 1;
+        }
+        const int ctx = sq.ctx;
+        const bool valid = sq.ctx_ok(max_ctx);
+        const int tile_tokens = kMulti ? p.tile_tokens : 1;
+        const int qlen = sq.q1 - sq.q0;
+        const int np = valid ? items_of(ctx, max_ctx, P) : 1;
+        const int ntt = kMulti ? (qlen + tile_tokens - 1) / tile_tokens : 1;
         const int i_loc = item_id - base_items;
-        const int hk = i_loc / np;  // one item per kv head: all g query heads
-        const int part = i_loc - hk * np;
+        if (kMulti && (i_loc < 0 || i_loc >= __shfl_sync(0xffffffffu, items_lane, s_cur - win0))) {
+            // only reachable when query_start is not ascending (item counts can overflow)
+            if (lane == 0) report(p.d_err, PA_DERR_CTX_OOB);
+            break;
+        }
+        const int tile = i_loc / np;  // (kv head, query-token tile); all g query heads
+        const int part = i_loc - tile * np;
+        const int hk = kMulti ? tile / ntt : tile;
+        const int it = tile - hk * ntt;
         const int hq0 = hk * g;
+        const int i0 = it * tile_tokens;
+        const int ntok = kMulti ? min(tile_tokens, qlen - i0) : 1;
+        const int lim_first = ctx - qlen + i0 + 1;  // tokens the item's first query sees
+        const int lim_last = lim_first + ntok - 1;
         const int tok_begin = part * P;
-        const int tok_end = valid ? min(tok_begin + P, ctx) : tok_begin;
+        const int tok_end = valid ? max(tok_begin, min(tok_begin + P, lim_last)) : tok_begin;
         const int nst = tok_end > tok_begin ? (tok_end - tok_begin + C::kStageTok - 1) / C::kStageTok : 1;
         if (!valid && lane == 0) report(p.d_err, PA_DERR_CTX_OOB);
 
@@ -164,15 +210,18 @@ __device__ __forceinline__ void tc_produce(const DecodeParams& p, const CUtensor
             break;
         }
         if (lane == 0) {
-            recs[qs].s = s;
+            recs[qs].row0 = sq.q0 + i0;
             recs[qs].hq0 = hq0;
             recs[qs].part = part;
             recs[qs].nparts = valid ? np : 0;
+            recs[qs].nrows = ntok * g;
             const uint32_t qf = qfull0 + 8 * qs;
-            mbar_arrive_expect_tx(qf, qbytes);
-            bulk_g2s(base + C::kQsOff + qs * C::kQBytes,
-                     static_cast<const T*>(p.q) + (static_cast<size_t>(s) * p.num_q_heads + hq0) * C::D,
-                     qbytes, qf, policy);
+            mbar_arrive_expect_tx(qf, row_bytes * ntok);
+            for (int ti = 0; ti < ntok; ++ti)
+                bulk_g2s(base + C::kQsOff + qs * C::kQBytes + ti * row_bytes,
+                         static_cast<const T*>(p.q) +
+                             (static_cast<size_t>(sq.q0 + i0 + ti) * p.num_q_heads + hq0) * C::D,
+                         row_bytes, qf, policy);
         }
         q_issued = item_seq + 1;
 
@@ -229,6 +278,8 @@ __device__ __forceinline__ void tc_produce(const DecodeParams& p, const CUtensor
                 meta[st].nvalid = max(0, t1 - t0);
                 meta[st].groups = groups;
                 meta[st].flags = flags;
+                meta[st].lim_rel = kMulti ? max(-C::kN, min(C::kStageTok, lim_first - t0))
+                                          : C::kStageTok;
                 mbar_arrive_expect_tx(full, static_cast<uint32_t>(__popc(groups)) * 4u * 2048u);
             }
             __syncwarp();
@@ -452,14 +503,15 @@ __device__ __forceinline__ float warp_reduce_scatter(const float (&v)[N], int la
     return x[0];
 }
 
-// A team (4 warps, one per accumulator lane quadrant) owns heads
-// [h0, h0 + H) of the G padded query heads.  Per stage: softmax of stage c
+// A team (4 warps, one per accumulator lane quadrant) owns rows
+// [h0, h0 + H) of the G padded query rows (the g heads of one kv head, or for
+// several queries per sequence: query token r / g, head r % g).  Per stage: softmax of stage c
 // (thread = token row of S), then the deferred O-accumulate of stage c-1 of
 // the same item (thread = head dimension of O^T); at an item's last stage its
 // own O-accumulate and the output rows of the team's heads.  Team 0 also
 // zeroes the V rows of invalid tokens.  Each team signals p_full, q_ready and
 // qempty once (those barriers count two arrivals).
-template <typename T, int G>
+template <typename T, int G, bool kMulti>
 __device__ __forceinline__ void tc_team(const DecodeParams& p, unsigned char* sm, uint32_t tmem,
                                         int team_id) {
     using C = TcTile<T>;
@@ -495,8 +547,11 @@ __device__ __forceinline__ void tc_team(const DecodeParams& p, unsigned char* sm
         o[h] = 0.f;
         alpha_prev[h] = 1.f;
     }
-    TcItemRec rec{0, 0, 0, 0};
+    TcItemRec rec{0, 0, 0, 0, 0, {0, 0, 0}};
     int deferred = -1;  // stage whose O-accumulate is still to do
+    int qtok[H];        // several queries: query token of each of the team's rows
+#pragma unroll
+    for (int h = 0; h < H; ++h) qtok[h] = kMulti ? (h0 + h) / g : 0;
 
     auto o_accumulate = [&](int cs, const float (&alpha)[H]) -> bool {
         if (!team.wait(ofull0 + 8 * (cs & 1), static_cast<uint32_t>(cs / 2) & 1, p.d_err, abort_flag))
@@ -528,7 +583,7 @@ __device__ __forceinline__ void tc_team(const DecodeParams& p, unsigned char* sm
             const unsigned char* src = sm + C::kQsOff + qs * C::kQBytes;
             for (int idx = tid; idx < H * 16; idx += 128) {
                 const int h = h0 + (idx >> 4), ch = idx & 15;
-                if (h < g) {
+                if (h < rec.nrows) {
                     const uint4 v = *reinterpret_cast<const uint4*>(src + (h * C::D + ch * 8) * 2);
                     *reinterpret_cast<uint4*>(sm + C::kQopOff + (ch >> 3) * 2048 + (h >> 3) * 1024 +
                                               (h & 7) * 128 + (((ch & 7) ^ (h & 7)) << 4)) = v;
@@ -554,8 +609,12 @@ __device__ __forceinline__ void tc_team(const DecodeParams& p, unsigned char* sm
         float x[H];
         tc::tmem_ld<H>(tmem + (c & 1) * C::kN + h0 + lane_off, x);
         const bool valid = row < nvalid && ((groups >> (row >> 4)) & 1u);
+        const int lim_rel = kMulti ? meta[st].lim_rel : C::kStageTok;
 #pragma unroll
-        for (int h = 0; h < H; ++h) x[h] = (valid && h0 + h < g) ? x[h] * p.qk_scale_log2 : -INFINITY;
+        for (int h = 0; h < H; ++h)  // several queries: row h sees the first lim_rel + qtok[h] tokens
+            x[h] = (valid && h0 + h < rec.nrows && (!kMulti || row < lim_rel + qtok[h]))
+                       ? x[h] * p.qk_scale_log2
+                       : -INFINITY;
         {
             const float mx = warp_reduce_scatter<H, true>(x, lane);
             if (lane % kSpan == 0) red[quad * 16 + h0 + lane / kSpan] = mx;
@@ -577,8 +636,9 @@ __device__ __forceinline__ void tc_team(const DecodeParams& p, unsigned char* sm
                 pr = Elem<T>::to_float(Elem<T>::from_float(fast_exp2(x[h] - m_new)));
             }
             l[h] = l[h] * alpha[h] + pr;
-            // P[hh][row] in the swizzled K-major P operand (rows >= g stay zero)
-            if (hh < g)
+            // P[hh][row] in the swizzled K-major P operand (rows >= g stay zero;
+            // several queries: every row is written, 0 past the item's rows)
+            if (kMulti || hh < g)
                 *reinterpret_cast<T*>(pop + (row >> 6) * 2048 + (hh >> 3) * 1024 + (hh & 7) * 128 +
                                       ((((col >> 3) ^ (hh & 7))) << 4) + (col & 7) * 2) = Elem<T>::from_float(pr);
         }
@@ -618,9 +678,10 @@ __device__ __forceinline__ void tc_team(const DecodeParams& p, unsigned char* sm
 #pragma unroll
         for (int h = 0; h < H; ++h) {
             const int hh = h0 + h;
-            if (hh >= g) break;
+            if (hh >= rec.nrows) break;
             const float L = red[hh] + red[16 + hh] + red[32 + hh] + red[48 + hh];
-            const size_t rr = static_cast<size_t>(rec.s) * p.num_q_heads + rec.hq0 + hh;
+            const size_t rr = static_cast<size_t>(rec.row0 + qtok[h]) * p.num_q_heads + rec.hq0 +
+                              (hh - qtok[h] * g);
             if (rec.nparts <= 1) {
                 static_cast<T*>(p.out)[rr * C::D + row] =
                     Elem<T>::from_float(rec.nparts == 1 && L > 0.f ? o[h] / L : 0.f);
@@ -638,7 +699,7 @@ __device__ __forceinline__ void tc_team(const DecodeParams& p, unsigned char* sm
     tc::fence_before_sync();
 }
 
-template <typename T, int G>
+template <typename T, int G, bool kMulti>
 __global__ void __launch_bounds__(TcTile<T>::kThreads, 1)
     decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap mapK,
                      const __grid_constant__ CUtensorMap mapV) {
@@ -674,11 +735,11 @@ __global__ void __launch_bounds__(TcTile<T>::kThreads, 1)
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
 
     if (warp == 0)
-        tc_produce<T>(p, &mapK, &mapV, sm, base);
+        tc_produce<T, kMulti>(p, &mapK, &mapV, sm, base);
     else if (warp == 1)
         tc_mma<T>(p, sm, base, tmem);
     else
-        tc_team<T, G>(p, sm, tmem, (warp - 2) >> 2);
+        tc_team<T, G, kMulti>(p, sm, tmem, (warp - 2) >> 2);
 
     tc::fence_before_sync();
     __syncthreads();
@@ -696,27 +757,34 @@ __global__ void __launch_bounds__(TcTile<T>::kThreads, 1)
     }
 }
 
-template <typename T>
+template <typename T, bool kMulti>
 inline pa_status launch_decode_tc_typed(const DecodeParams& p, const CUtensorMap& mapK,
                                         const CUtensorMap& mapV, cudaStream_t stream) {
     using C = TcTile<T>;
     static std::atomic<uint64_t> smem_configured[3];
-    const int G = p.group <= 4 ? 4 : p.group <= 8 ? 8 : 16;
-    auto kernel = G == 4 ? decode_tc_kernel<T, 4> : G == 8 ? decode_tc_kernel<T, 8> : decode_tc_kernel<T, 16>;
+    const int rows = kMulti ? p.tile_tokens * p.group : p.group;
+    if (rows > C::kN) return PA_ERR_UNSUPPORTED;
+    const int G = rows <= 4 ? 4 : rows <= 8 ? 8 : 16;
+    auto kernel = G == 4   ? decode_tc_kernel<T, 4, kMulti>
+                  : G == 8 ? decode_tc_kernel<T, 8, kMulti>
+                           : decode_tc_kernel<T, 16, kMulti>;
     if (ensure_smem(kernel, C::kSmemBytes, smem_configured[G == 4 ? 0 : G == 8 ? 1 : 2]) != PA_OK)
         return PA_ERR_CUDA;
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
         return PA_ERR_CUDA;
-    const long long work = static_cast<long long>(p.num_seqs) * p.head_tiles * p.max_parts;
+    // upper bound of the work items (query-token tiles: rows / tile_tokens + one ragged per sequence)
+    const long long tiles =
+        kMulti ? p.num_query_tokens / p.tile_tokens + p.num_seqs : p.num_seqs;
+    const long long work = tiles * p.head_tiles * p.max_parts;
     if (work > 0x7fffffffLL) return PA_ERR_UNSUPPORTED;
     long long grid = sms;
     if (grid > work) grid = work;
     kernel<<<static_cast<unsigned>(grid), C::kThreads, C::kSmemBytes, stream>>>(p, mapK, mapV);
     if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
     if (p.max_parts > 1) {
-        decode_reduce_kernel<T, C::D><<<p.num_seqs * p.num_q_heads, 128, 0, stream>>>(p);
+        decode_reduce_kernel<T, C::D><<<p.num_query_tokens * p.num_q_heads, 128, 0, stream>>>(p);
         if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
     }
     return PA_OK;
@@ -726,5 +794,9 @@ pa_status launch_decode_tc_f16(const DecodeParams& p, const CUtensorMap& mapK,
                                const CUtensorMap& mapV, cudaStream_t stream);
 pa_status launch_decode_tc_bf16(const DecodeParams& p, const CUtensorMap& mapK,
                                 const CUtensorMap& mapV, cudaStream_t stream);
+pa_status launch_multi_query_tc_f16(const DecodeParams& p, const CUtensorMap& mapK,
+                                    const CUtensorMap& mapV, cudaStream_t stream);
+pa_status launch_multi_query_tc_bf16(const DecodeParams& p, const CUtensorMap& mapK,
+                                     const CUtensorMap& mapV, cudaStream_t stream);
 
 }  // namespace pa

@@ -1,4 +1,4 @@
-// multi_query_f32.cu -- SIMT kernel instantiations for several query tokens
+// multi_query_f32.cu -- kernel instantiations for several query tokens
 // per sequence (causal), float elements.
 #include "decode_kernels.cuh"
 

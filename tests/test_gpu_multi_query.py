@@ -171,3 +171,24 @@ def test_multi_query_host_checked_errors():
         pa.multi_query(out, d["q"], d["query_start"], d["k_cache"], d["v_cache"],
                        d["block_tables"], d["context_lens"], w.scale, partition_tokens=40)
     assert e.value.status == 1
+
+
+# 16-bit K/V, head_dim 128, partitions a multiple of 128 tokens and at least
+# 4 rows (query tokens x heads of one kv head) per item: the tensor-core path.
+MQ_TC = [
+    # dtype, Hq, Hkv, B, P, ctx, queries per sequence
+    ("f16", 4, 4, 16, 512, [16, 40, 300, 700, 129], [16, 5, 33, 16, 3]),     # MHA: 16 tokens/item
+    ("bf16", 8, 4, 16, 128, [20, 513, 1500, 64], [20, 17, 64, 64]),         # 2 per kv head
+    ("bf16", 32, 2, 32, 256, [1, 100, 257, 900], [1, 2, 3, 7]),             # 16 per kv head
+    ("f16", 24, 4, 128, 1024, [128, 129, 1000, 2100], [128, 1, 9, 40]),     # 6 per kv head
+]
+
+
+@pytest.mark.parametrize("case", range(len(MQ_TC)))
+def test_multi_query_tensor_core_parity(case):
+    dtype, Hq, Hkv, B, P, ctx, ql = MQ_TC[case]
+    w = wl.custom(f"mq_tc{case}", ctx, dtype=dtype, num_q_heads=Hq, num_kv_heads=Hkv,
+                  head_dim=128, block_size=B, seed=420 + case, pool_factor=1.3, query_lens=ql)
+    _, out, d = _check(w, partition_tokens=P)
+    again = gpu_step(w, upload(w), partition_tokens=P)
+    assert torch.equal(out, again), "two identical runs differ"
