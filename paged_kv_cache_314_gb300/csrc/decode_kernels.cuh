@@ -141,9 +141,10 @@ struct DecodeTile {
     static constexpr int kConsumerWarps = 4;
     static constexpr int kThreads = 32 * (kConsumerWarps + 1);
     // tokens per stage: 4 KB of K (and 4 KB of V), at least 16 tokens; E4M3
-    // stages hold 16 tokens (2 KB each) so a consumer warp's chain per stage
-    // is as long as with 16-bit elements
-    static constexpr int kTps = kFp8 ? 16 : (4096 / kRowBytes) > 16 ? (4096 / kRowBytes) : 16;
+    // tiles of several rows hold 16 tokens (2 KB) per stage, which halves the
+    // passes a consumer warp keeps in registers
+    static constexpr int kTps = (kFp8 && GT > 1) ? 16
+                                : (4096 / kRowBytes) > 16 ? (4096 / kRowBytes) : 16;
     static constexpr int kPasses = kTps / kTpp;       // warp passes over one stage
     static constexpr int kVals = kPasses >= kLpt ? kPasses / kLpt : 1;  // logits per lane
     static constexpr int kDup = kPasses >= kLpt ? 1 : kLpt / kPasses;   // lanes per logit
