@@ -62,8 +62,12 @@ struct TcTile {
     static constexpr int kRecOff = kRedOff + 4 * kN * 4;          // item records [kQSlots]
     static constexpr int kMetaOff = kRecOff + kQSlots * 32;       // stage meta [kStages]
     static constexpr int kBarOff = kMetaOff + kStages * 32;
-    // full[S], empty[S], qfull[Q], qempty[Q], q_ready, s_full[2], p_full[2], o_full[2], drain
-    static constexpr int kNumBars = 2 * kStages + 2 * kQSlots + 8;
+    // fullK[S], emptyK[S], qfull[Q], qempty[Q], q_ready, s_full[2], p_full[2], o_full[2],
+    // drain, fullV[S], emptyV[S]: the K and V halves of a ring slot land and are
+    // released separately (K after MMA1 of its stage, V after MMA2)
+    static constexpr int kFullVBar = 2 * kStages + 2 * kQSlots + 8;
+    static constexpr int kEmptyVBar = kFullVBar + kStages;
+    static constexpr int kNumBars = kEmptyVBar + kStages;
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;       // tmem base, abort, team flags
     static constexpr int kSmemBytes = kMiscOff + 32 + 1024;       // + alignment slack
     static constexpr int kThreads = 320;  // producer, MMA, two teams of 4 warps
@@ -98,11 +102,13 @@ __device__ __forceinline__ void tc_produce(const DecodeParams& p, const CUtensor
     using C = TcTile<T>;
     const int lane = threadIdx.x & 31;
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::kBarOff);
-    const uint32_t full0 = smem_addr(bars), empty0 = smem_addr(bars + C::kStages);
+    const uint32_t fullK0 = smem_addr(bars), emptyK0 = smem_addr(bars + C::kStages);
+    const uint32_t fullV0 = smem_addr(bars + C::kFullVBar), emptyV0 = smem_addr(bars + C::kEmptyVBar);
     const uint32_t qfull0 = smem_addr(bars + 2 * C::kStages);
     const uint32_t qempty0 = smem_addr(bars + 2 * C::kStages + C::kQSlots);
     TcStageMeta* meta = reinterpret_cast<TcStageMeta*>(sm + C::kMetaOff);
     TcItemRec* recs = reinterpret_cast<TcItemRec*>(sm + C::kRecOff);
+    int k_only = -1;  // a stage whose K copies were issued but not its V copies (abort)
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + C::kMiscOff + 4);
 
     const uint64_t policy = l2_evict_first_policy();
@@ -233,8 +239,9 @@ __device__ __forceinline__ void tc_produce(const DecodeParams& p, const CUtensor
         for (int i = 0; i < nst; ++i) {
             const int cc = c + i;
             const int st = cc % C::kStages;
-            if (cc >= C::kStages &&
-                !mbar_wait_warp(empty0 + 8 * st, static_cast<uint32_t>(cc / C::kStages - 1) & 1)) {
+            const uint32_t reuse = static_cast<uint32_t>(cc / C::kStages - 1) & 1;
+            // the K half of the slot is free once MMA1 of its previous stage completed
+            if (cc >= C::kStages && !mbar_wait_warp(emptyK0 + 8 * st, reuse)) {
                 if (lane == 0) report(p.d_err, PA_DERR_TIMEOUT);
                 *abort_flag = 1;
                 aborted = true;
@@ -269,7 +276,27 @@ __device__ __forceinline__ void tc_produce(const DecodeParams& p, const CUtensor
             uint32_t groups = 0;
 #pragma unroll
             for (int g8 = 0; g8 < 8; ++g8) groups |= ((loaded >> (4 * g8)) & 1u) << g8;
-            const uint32_t full = full0 + 8 * st;
+            const uint32_t fullK = fullK0 + 8 * st, fullV = fullV0 + 8 * st;
+            const uint32_t half_bytes = static_cast<uint32_t>(__popc(groups)) * 2u * 2048u;  // K or V
+            const uint32_t stage_base = base + C::kRingOff + st * C::kStageBytes;
+            const int h = (lane >> 1) & 1;
+            // K boxes first (their bytes complete on fullK before its arrival is posted)
+            if (mine && (lane & 1) == 0)
+                tc::tma_load_2d(stage_base + h * C::kHalfBytes + r * 2048, mapK, 64 * h, row, fullK,
+                                policy);
+            __syncwarp();
+            // the V half is free once MMA2 of the slot's previous stage completed
+            if (cc >= C::kStages && !mbar_wait_warp(emptyV0 + 8 * st, reuse)) {
+                if (lane == 0) {
+                    report(p.d_err, PA_DERR_TIMEOUT);
+                    mbar_arrive_expect_tx(fullK, half_bytes);  // so the drain can see K land
+                }
+                *abort_flag = 1;
+                aborted = true;
+                k_only = cc;
+                c = cc + 1;
+                break;
+            }
             if (lane == 0) {
                 uint32_t flags = 0;
                 if (i == 0) flags |= kStageFirst;
@@ -280,15 +307,15 @@ __device__ __forceinline__ void tc_produce(const DecodeParams& p, const CUtensor
                 meta[st].flags = flags;
                 meta[st].lim_rel = kMulti ? max(-C::kN, min(C::kStageTok, lim_first - t0))
                                           : C::kStageTok;
-                mbar_arrive_expect_tx(full, static_cast<uint32_t>(__popc(groups)) * 4u * 2048u);
+                // meta is written before either arrival: the MMA warp reads it after
+                // fullK, the team after fullV
+                mbar_arrive_expect_tx(fullK, half_bytes);
+                mbar_arrive_expect_tx(fullV, half_bytes);
             }
             __syncwarp();
-            if (mine) {
-                const int h = (lane >> 1) & 1;
-                const uint32_t dst = base + C::kRingOff + st * C::kStageBytes + (lane & 1) * C::kTileBytes +
-                                     h * C::kHalfBytes + r * 2048;
-                tc::tma_load_2d(dst, (lane & 1) ? mapV : mapK, 64 * h, row, full, policy);
-            }
+            if (mine && (lane & 1) != 0)
+                tc::tma_load_2d(stage_base + C::kTileBytes + h * C::kHalfBytes + r * 2048, mapV, 64 * h,
+                                row, fullV, policy);
             __syncwarp();
         }
         if (aborted) break;
@@ -299,8 +326,9 @@ __device__ __forceinline__ void tc_produce(const DecodeParams& p, const CUtensor
     }
     if (!aborted) {  // one end marker: the MMA warp and the team read stages in order
         const int st = c % C::kStages;
-        if (c >= C::kStages &&
-            !mbar_wait_warp(empty0 + 8 * st, static_cast<uint32_t>(c / C::kStages - 1) & 1)) {
+        const uint32_t reuse = static_cast<uint32_t>(c / C::kStages - 1) & 1;
+        if (c >= C::kStages && (!mbar_wait_warp(emptyK0 + 8 * st, reuse) ||
+                                !mbar_wait_warp(emptyV0 + 8 * st, reuse))) {
             if (lane == 0) report(p.d_err, PA_DERR_TIMEOUT);
             *abort_flag = 1;
         } else {
@@ -308,16 +336,20 @@ __device__ __forceinline__ void tc_produce(const DecodeParams& p, const CUtensor
                 meta[st].flags = kStageEnd;
                 meta[st].nvalid = 0;
                 meta[st].groups = 0;
-                mbar_arrive(full0 + 8 * st);
+                mbar_arrive(fullK0 + 8 * st);
+                mbar_arrive(fullV0 + 8 * st);
             }
             ++c;
         }
     }
     if (lane == 0) {
         if (oob) report(p.d_err, PA_DERR_BLOCK_OOB);
-        for (int cc = max(0, c - C::kStages); cc < c; ++cc)
-            if (!mbar_wait(full0 + 8 * (cc % C::kStages), static_cast<uint32_t>(cc / C::kStages) & 1))
+        for (int cc = max(0, c - C::kStages); cc < c; ++cc) {
+            const uint32_t par = static_cast<uint32_t>(cc / C::kStages) & 1;
+            if (!mbar_wait(fullK0 + 8 * (cc % C::kStages), par)) report(p.d_err, PA_DERR_TIMEOUT);
+            if (cc != k_only && !mbar_wait(fullV0 + 8 * (cc % C::kStages), par))
                 report(p.d_err, PA_DERR_TIMEOUT);
+        }
         for (int k = max(0, q_issued - C::kQSlots); k < q_issued; ++k)
             if (!mbar_wait(qfull0 + 8 * (k % C::kQSlots), static_cast<uint32_t>(k / C::kQSlots) & 1))
                 report(p.d_err, PA_DERR_TIMEOUT);
@@ -369,7 +401,8 @@ __device__ __forceinline__ void tc_mma(const DecodeParams& p, unsigned char* sm,
     using Bi = TcBars<T>;
     const int lane = threadIdx.x & 31;
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::kBarOff);
-    const uint32_t full0 = smem_addr(bars), empty0 = smem_addr(bars + C::kStages);
+    const uint32_t fullK0 = smem_addr(bars), emptyK0 = smem_addr(bars + C::kStages);
+    const uint32_t emptyV0 = smem_addr(bars + C::kEmptyVBar);
     const uint32_t qready = smem_addr(bars + Bi::kQReady);
     const uint32_t sfull0 = smem_addr(bars + Bi::kSFull), pfull0 = smem_addr(bars + Bi::kPFull);
     const uint32_t ofull0 = smem_addr(bars + Bi::kOFull), drain = smem_addr(bars + Bi::kDrain);
@@ -387,7 +420,7 @@ __device__ __forceinline__ void tc_mma(const DecodeParams& p, unsigned char* sm,
     // Returns 0 = issued, 1 = end marker, -1 = gave up.
     auto issue_mma1 = [&](int c) -> int {
         const int st = c % C::kStages;
-        if (!mbar_wait_warp(full0 + 8 * st, static_cast<uint32_t>(c / C::kStages) & 1)) return -1;
+        if (!mbar_wait_warp(fullK0 + 8 * st, static_cast<uint32_t>(c / C::kStages) & 1)) return -1;
         const uint32_t flags = meta[st].flags;
         if (flags & kStageEnd) return 1;
         if (flags & kStageFirst) {
@@ -398,6 +431,7 @@ __device__ __forceinline__ void tc_mma(const DecodeParams& p, unsigned char* sm,
         if (lane == 0) {
             tc_mma1<T>(stage_k(c), qop, tmem + (c & 1) * C::kN);
             tc::mma_commit(sfull0 + 8 * (c & 1));
+            tc::mma_commit(emptyK0 + 8 * st);  // K_c is free once MMA1 completed
         }
         __syncwarp();
         return 0;
@@ -412,7 +446,7 @@ __device__ __forceinline__ void tc_mma(const DecodeParams& p, unsigned char* sm,
             const int st1 = (c + 1) % C::kStages;
             int early = 0;
             if (lane == 0 &&
-                mbar_try_wait(full0 + 8 * st1, static_cast<uint32_t>((c + 1) / C::kStages) & 1))
+                mbar_try_wait(fullK0 + 8 * st1, static_cast<uint32_t>((c + 1) / C::kStages) & 1))
                 early = !(meta[st1].flags & (kStageEnd | kStageFirst));
             if (__shfl_sync(0xffffffffu, early, 0)) {
                 r = issue_mma1(c + 1);
@@ -432,7 +466,7 @@ __device__ __forceinline__ void tc_mma(const DecodeParams& p, unsigned char* sm,
             tc_mma2<T>(stage_k(c) + C::kTileBytes, pop0 + (c & 1) * C::kOpBytes,
                        tmem + 2 * C::kN + (c & 1) * C::kN);
             tc::mma_commit(ofull0 + 8 * (c & 1));
-            tc::mma_commit(empty0 + 8 * (c % C::kStages));  // K_c and V_c are free
+            tc::mma_commit(emptyV0 + 8 * (c % C::kStages));  // V_c is free
         }
         __syncwarp();
         if (!next_done) r = issue_mma1(c + 1);
@@ -524,7 +558,7 @@ __device__ __forceinline__ void tc_team(const DecodeParams& p, unsigned char* sm
     const int row = 32 * quad + lane;                   // token of S, head dimension of O
     const int h0 = team_id * H;
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::kBarOff);
-    const uint32_t full0 = smem_addr(bars);
+    const uint32_t fullV0 = smem_addr(bars + C::kFullVBar);  // V landed (and the stage's meta)
     const uint32_t qfull0 = smem_addr(bars + 2 * C::kStages);
     const uint32_t qempty0 = smem_addr(bars + 2 * C::kStages + C::kQSlots);
     const uint32_t qready = smem_addr(bars + Bi::kQReady);
@@ -567,7 +601,7 @@ __device__ __forceinline__ void tc_team(const DecodeParams& p, unsigned char* sm
 
     for (int c = 0;; ++c) {
         const int st = c % C::kStages;
-        if (!team.wait(full0 + 8 * st, static_cast<uint32_t>(c / C::kStages) & 1, p.d_err, abort_flag)) break;
+        if (!team.wait(fullV0 + 8 * st, static_cast<uint32_t>(c / C::kStages) & 1, p.d_err, abort_flag)) break;
         const uint32_t flags = meta[st].flags;
         if (flags & kStageEnd) break;
         const int item_seq = static_cast<int>(meta[st].item_seq);
