@@ -19,13 +19,15 @@
 // as [NB*Hkv*B rows x d columns]); the swizzled tiles are the MMA operands as
 // they land.
 //
-// Warp roles (320 threads, persistent, one CTA per SM):
+// Warp roles (352 threads, persistent, one CTA per SM):
 //   warp 0   producer: item cursor over context_lens (as in the SIMT path),
 //            block-table slice, TMA loads into a 3-stage ring (64 KB/stage;
 //            one [16 x 64] box per lane), bulk copy of the item's query rows
 //            into a staging slot
 //   warp 1   allocates tensor memory, issues the MMAs (one thread); S and
 //            O^T are double-buffered in tensor memory (64 columns)
+//   warp 10  issues the V boxes of each stage from the producer's plan (the
+//            TMA issue rate of one warp bounds the stage rate)
 //   warps 2-9 two "teams" of four warps, each owning half of the heads:
 //            thread = row (token for S, head dimension for O), reading the
 //            accumulator lanes of its warp's quadrant
@@ -61,16 +63,21 @@ struct TcTile {
     static constexpr int kRedOff = kPopOff + 2 * kOpBytes;        // P double-buffered; [4][16] floats
     static constexpr int kRecOff = kRedOff + 4 * kN * 4;          // item records [kQSlots]
     static constexpr int kMetaOff = kRecOff + kQSlots * 32;       // stage meta [kStages]
-    static constexpr int kBarOff = kMetaOff + kStages * 32;
+    // V copy plan of each stage for the V-issuing warp: 16 box rows (-1: none) + a stop word
+    static constexpr int kPlanOff = kMetaOff + kStages * 32;
+    static constexpr int kPlanInts = 20;
+    static constexpr int kBarOff = kPlanOff + kStages * kPlanInts * 4;
     // fullK[S], emptyK[S], qfull[Q], qempty[Q], q_ready, s_full[2], p_full[2], o_full[2],
-    // drain, fullV[S], emptyV[S]: the K and V halves of a ring slot land and are
-    // released separately (K after MMA1 of its stage, V after MMA2)
+    // drain, fullV[S], emptyV[S], vplan[S]: the K and V halves of a ring slot land and
+    // are released separately (K after MMA1 of its stage, V after MMA2); a stage's V
+    // copies are issued by their own warp from the plan the producer leaves
     static constexpr int kFullVBar = 2 * kStages + 2 * kQSlots + 8;
     static constexpr int kEmptyVBar = kFullVBar + kStages;
-    static constexpr int kNumBars = kEmptyVBar + kStages;
+    static constexpr int kVPlanBar = kEmptyVBar + kStages;
+    static constexpr int kNumBars = kVPlanBar + kStages;
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;       // tmem base, abort, team flags
     static constexpr int kSmemBytes = kMiscOff + 32 + 1024;       // + alignment slack
-    static constexpr int kThreads = 320;  // producer, MMA, two teams of 4 warps
+    static constexpr int kThreads = 352;  // producer, MMA, two teams of 4 warps, V copies
     static constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
     static_assert(kBf16 || std::is_same<T, __half>::value, "16-bit operands only");
     static constexpr uint32_t kIdescS = tc::instr_desc_f16(kBf16, 128, kN, false, false);
@@ -104,6 +111,8 @@ __device__ __forceinline__ void tc_produce(const DecodeParams& p, const CUtensor
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::kBarOff);
     const uint32_t fullK0 = smem_addr(bars), emptyK0 = smem_addr(bars + C::kStages);
     const uint32_t fullV0 = smem_addr(bars + C::kFullVBar), emptyV0 = smem_addr(bars + C::kEmptyVBar);
+    const uint32_t vplan0 = smem_addr(bars + C::kVPlanBar);
+    int* plan = reinterpret_cast<int*>(sm + C::kPlanOff);
     const uint32_t qfull0 = smem_addr(bars + 2 * C::kStages);
     const uint32_t qempty0 = smem_addr(bars + 2 * C::kStages + C::kQSlots);
     TcStageMeta* meta = reinterpret_cast<TcStageMeta*>(sm + C::kMetaOff);
@@ -311,12 +320,12 @@ __device__ __forceinline__ void tc_produce(const DecodeParams& p, const CUtensor
                 // fullK, the team after fullV
                 mbar_arrive_expect_tx(fullK, half_bytes);
                 mbar_arrive_expect_tx(fullV, half_bytes);
+                plan[st * C::kPlanInts + 16] = 0;  // not the last stage
             }
+            // the V boxes: their rows go to the V-issuing warp (lane 2j+1 -> entry j)
+            if ((lane & 1) != 0) plan[st * C::kPlanInts + (lane >> 1)] = mine ? row : -1;
             __syncwarp();
-            if (mine && (lane & 1) != 0)
-                tc::tma_load_2d(stage_base + C::kTileBytes + h * C::kHalfBytes + r * 2048, mapV, 64 * h,
-                                row, fullV, policy);
-            __syncwarp();
+            if (lane == 0) mbar_arrive(vplan0 + 8 * st);
         }
         if (aborted) break;
         c += nst;
@@ -336,8 +345,10 @@ __device__ __forceinline__ void tc_produce(const DecodeParams& p, const CUtensor
                 meta[st].flags = kStageEnd;
                 meta[st].nvalid = 0;
                 meta[st].groups = 0;
+                plan[st * C::kPlanInts + 16] = 1;  // the V-issuing warp leaves
                 mbar_arrive(fullK0 + 8 * st);
                 mbar_arrive(fullV0 + 8 * st);
+                mbar_arrive(vplan0 + 8 * st);
             }
             ++c;
         }
@@ -354,6 +365,40 @@ __device__ __forceinline__ void tc_produce(const DecodeParams& p, const CUtensor
             if (!mbar_wait(qfull0 + 8 * (k % C::kQSlots), static_cast<uint32_t>(k / C::kQSlots) & 1))
                 report(p.d_err, PA_DERR_TIMEOUT);
         __threadfence();
+    }
+}
+
+// The V-issuing warp: for each stage, in ring order, it waits for the plan the
+// producer leaves once the slot's V half is free, and issues the stage's V boxes
+// (one per lane, lanes 0-15); they complete on fullV, whose arrival the producer
+// has already posted with the expected bytes.
+template <typename T>
+__device__ __forceinline__ void tc_issue_v(const DecodeParams& p, const CUtensorMap* mapV,
+                                           unsigned char* sm, uint32_t base) {
+    using C = TcTile<T>;
+    const int lane = threadIdx.x & 31;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::kBarOff);
+    const uint32_t fullV0 = smem_addr(bars + C::kFullVBar);
+    const uint32_t vplan0 = smem_addr(bars + C::kVPlanBar);
+    const int* plan = reinterpret_cast<const int*>(sm + C::kPlanOff);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + C::kMiscOff + 4);
+    const uint64_t policy = l2_evict_first_policy();
+    for (int c = 0;; ++c) {
+        const int st = c % C::kStages;
+        if (!mbar_wait_warp(vplan0 + 8 * st, static_cast<uint32_t>(c / C::kStages) & 1)) {
+            if (lane == 0) report(p.d_err, PA_DERR_TIMEOUT);
+            *abort_flag = 1;
+            break;
+        }
+        if (plan[st * C::kPlanInts + 16] != 0) break;
+        const int row = lane < 16 ? plan[st * C::kPlanInts + lane] : -1;
+        if (row >= 0) {
+            const int r = lane >> 1, h = lane & 1;
+            tc::tma_load_2d(base + C::kRingOff + st * C::kStageBytes + C::kTileBytes + h * C::kHalfBytes +
+                                r * 2048,
+                            mapV, 64 * h, row, fullV0 + 8 * st, policy);
+        }
+        __syncwarp();
     }
 }
 
@@ -772,8 +817,10 @@ __global__ void __launch_bounds__(TcTile<T>::kThreads, 1)
         tc_produce<T, kMulti>(p, &mapK, &mapV, sm, base);
     else if (warp == 1)
         tc_mma<T>(p, sm, base, tmem);
-    else
+    else if (warp < 10)
         tc_team<T, G, kMulti>(p, sm, tmem, (warp - 2) >> 2);
+    else
+        tc_issue_v<T>(p, &mapV, sm, base);
 
     tc::fence_before_sync();
     __syncthreads();
