@@ -19,15 +19,16 @@
 // as [NB*Hkv*B rows x d columns]); the swizzled tiles are the MMA operands as
 // they land.
 //
-// Warp roles (352 threads, persistent, one CTA per SM):
+// Warp roles (416 threads, persistent, one CTA per SM):
 //   warp 0   producer: item cursor over context_lens (as in the SIMT path),
 //            block-table slice, TMA loads into a 3-stage ring (64 KB/stage;
 //            one [16 x 64] box per lane), bulk copy of the item's query rows
 //            into a staging slot
 //   warp 1   allocates tensor memory, issues the MMAs (one thread); S and
 //            O^T are double-buffered in tensor memory (64 columns)
-//   warp 10  issues the V boxes of each stage from the producer's plan (the
-//            TMA issue rate of one warp bounds the stage rate)
+//   warps 10-12 issue the other three quarters of each stage's TMA boxes (V
+//            half 0, K half 1, V half 1) from the producer's plan: one warp's
+//            TMA issue rate would bound the stage rate
 //   warps 2-9 two "teams" of four warps, each owning half of the heads:
 //            thread = row (token for S, head dimension for O), reading the
 //            accumulator lanes of its warp's quadrant
@@ -63,9 +64,11 @@ struct TcTile {
     static constexpr int kRedOff = kPopOff + 2 * kOpBytes;        // P double-buffered; [4][16] floats
     static constexpr int kRecOff = kRedOff + 4 * kN * 4;          // item records [kQSlots]
     static constexpr int kMetaOff = kRecOff + kQSlots * 32;       // stage meta [kStages]
-    // V copy plan of each stage for the V-issuing warp: 16 box rows (-1: none) + a stop word
+    // copy plan of each stage for the issuing warps: 16 K box rows, 16 V box rows
+    // (entry 2*group + half; -1: none) and a stop word
     static constexpr int kPlanOff = kMetaOff + kStages * 32;
-    static constexpr int kPlanInts = 20;
+    static constexpr int kPlanInts = 36;
+    static constexpr int kPlanStop = 32;
     static constexpr int kBarOff = kPlanOff + kStages * kPlanInts * 4;
     // fullK[S], emptyK[S], qfull[Q], qempty[Q], q_ready, s_full[2], p_full[2], o_full[2],
     // drain, fullV[S], emptyV[S], vplan[S]: the K and V halves of a ring slot land and
@@ -74,10 +77,14 @@ struct TcTile {
     static constexpr int kFullVBar = 2 * kStages + 2 * kQSlots + 8;
     static constexpr int kEmptyVBar = kFullVBar + kStages;
     static constexpr int kVPlanBar = kEmptyVBar + kStages;
-    static constexpr int kNumBars = kVPlanBar + kStages;
+    static constexpr int kKPlanBar = kVPlanBar + kStages;
+    static constexpr int kNumBars = kKPlanBar + kStages;
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;       // tmem base, abort, team flags
     static constexpr int kSmemBytes = kMiscOff + 32 + 1024;       // + alignment slack
-    static constexpr int kThreads = 352;  // producer, MMA, two teams of 4 warps, V copies
+    // producer, MMA, two teams of 4 warps, three copy warps: the 32 TMA boxes of a
+    // stage are issued by four warps (the producer and warps 10-12, 8 boxes each),
+    // since one warp's TMA issue rate would bound the stage rate
+    static constexpr int kThreads = 416;
     static constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
     static_assert(kBf16 || std::is_same<T, __half>::value, "16-bit operands only");
     static constexpr uint32_t kIdescS = tc::instr_desc_f16(kBf16, 128, kN, false, false);
@@ -111,7 +118,7 @@ __device__ __forceinline__ void tc_produce(const DecodeParams& p, const CUtensor
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::kBarOff);
     const uint32_t fullK0 = smem_addr(bars), emptyK0 = smem_addr(bars + C::kStages);
     const uint32_t fullV0 = smem_addr(bars + C::kFullVBar), emptyV0 = smem_addr(bars + C::kEmptyVBar);
-    const uint32_t vplan0 = smem_addr(bars + C::kVPlanBar);
+    const uint32_t vplan0 = smem_addr(bars + C::kVPlanBar), kplan0 = smem_addr(bars + C::kKPlanBar);
     int* plan = reinterpret_cast<int*>(sm + C::kPlanOff);
     const uint32_t qfull0 = smem_addr(bars + 2 * C::kStages);
     const uint32_t qempty0 = smem_addr(bars + 2 * C::kStages + C::kQSlots);
@@ -289,10 +296,14 @@ __device__ __forceinline__ void tc_produce(const DecodeParams& p, const CUtensor
             const uint32_t half_bytes = static_cast<uint32_t>(__popc(groups)) * 2u * 2048u;  // K or V
             const uint32_t stage_base = base + C::kRingOff + st * C::kStageBytes;
             const int h = (lane >> 1) & 1;
-            // K boxes first (their bytes complete on fullK before its arrival is posted)
-            if (mine && (lane & 1) == 0)
-                tc::tma_load_2d(stage_base + h * C::kHalfBytes + r * 2048, mapK, 64 * h, row, fullK,
-                                policy);
+            // K boxes first (their bytes complete on fullK before its arrival is posted):
+            // the second 64-column half goes to warp 11 through the plan
+            if ((lane & 1) == 0) plan[st * C::kPlanInts + (lane >> 1)] = mine ? row : -1;
+            if (lane == 0) plan[st * C::kPlanInts + C::kPlanStop] = 0;  // not the last stage
+            __syncwarp();
+            if (lane == 0) mbar_arrive(kplan0 + 8 * st);
+            if (mine && (lane & 3) == 0)
+                tc::tma_load_2d(stage_base + r * 2048, mapK, 0, row, fullK, policy);
             __syncwarp();
             // the V half is free once MMA2 of the slot's previous stage completed
             if (cc >= C::kStages && !mbar_wait_warp(emptyV0 + 8 * st, reuse)) {
@@ -320,10 +331,9 @@ __device__ __forceinline__ void tc_produce(const DecodeParams& p, const CUtensor
                 // fullK, the team after fullV
                 mbar_arrive_expect_tx(fullK, half_bytes);
                 mbar_arrive_expect_tx(fullV, half_bytes);
-                plan[st * C::kPlanInts + 16] = 0;  // not the last stage
             }
-            // the V boxes: their rows go to the V-issuing warp (lane 2j+1 -> entry j)
-            if ((lane & 1) != 0) plan[st * C::kPlanInts + (lane >> 1)] = mine ? row : -1;
+            // the V boxes: their rows go to warps 10 and 12 (lane 4g+2h+1 -> entry 16+2g+h)
+            if ((lane & 1) != 0) plan[st * C::kPlanInts + 16 + (lane >> 1)] = mine ? row : -1;
             __syncwarp();
             if (lane == 0) mbar_arrive(vplan0 + 8 * st);
         }
@@ -345,9 +355,10 @@ __device__ __forceinline__ void tc_produce(const DecodeParams& p, const CUtensor
                 meta[st].flags = kStageEnd;
                 meta[st].nvalid = 0;
                 meta[st].groups = 0;
-                plan[st * C::kPlanInts + 16] = 1;  // the V-issuing warp leaves
+                plan[st * C::kPlanInts + C::kPlanStop] = 1;  // the copy warps leave
                 mbar_arrive(fullK0 + 8 * st);
                 mbar_arrive(fullV0 + 8 * st);
+                mbar_arrive(kplan0 + 8 * st);
                 mbar_arrive(vplan0 + 8 * st);
             }
             ++c;
@@ -368,36 +379,35 @@ __device__ __forceinline__ void tc_produce(const DecodeParams& p, const CUtensor
     }
 }
 
-// The V-issuing warp: for each stage, in ring order, it waits for the plan the
-// producer leaves once the slot's V half is free, and issues the stage's V boxes
-// (one per lane, lanes 0-15); they complete on fullV, whose arrival the producer
-// has already posted with the expected bytes.
+// A copy warp: for each stage, in ring order, it waits for the plan the
+// producer leaves once the slot's K (or V) half is free, and issues that
+// tensor's boxes of one 64-column half (one per lane, lanes 0-7 = the stage's
+// eight 16-token groups); they complete on fullK / fullV, whose arrivals the
+// producer posts with the expected bytes.
 template <typename T>
-__device__ __forceinline__ void tc_issue_v(const DecodeParams& p, const CUtensorMap* mapV,
-                                           unsigned char* sm, uint32_t base) {
+__device__ __forceinline__ void tc_copy(const DecodeParams& p, const CUtensorMap* map,
+                                        unsigned char* sm, uint32_t base, bool is_v, int half) {
     using C = TcTile<T>;
     const int lane = threadIdx.x & 31;
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::kBarOff);
-    const uint32_t fullV0 = smem_addr(bars + C::kFullVBar);
-    const uint32_t vplan0 = smem_addr(bars + C::kVPlanBar);
+    const uint32_t full0 = smem_addr(bars + (is_v ? C::kFullVBar : 0));
+    const uint32_t plan0 = smem_addr(bars + (is_v ? C::kVPlanBar : C::kKPlanBar));
     const int* plan = reinterpret_cast<const int*>(sm + C::kPlanOff);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + C::kMiscOff + 4);
     const uint64_t policy = l2_evict_first_policy();
     for (int c = 0;; ++c) {
         const int st = c % C::kStages;
-        if (!mbar_wait_warp(vplan0 + 8 * st, static_cast<uint32_t>(c / C::kStages) & 1)) {
+        if (!mbar_wait_warp(plan0 + 8 * st, static_cast<uint32_t>(c / C::kStages) & 1)) {
             if (lane == 0) report(p.d_err, PA_DERR_TIMEOUT);
             *abort_flag = 1;
             break;
         }
-        if (plan[st * C::kPlanInts + 16] != 0) break;
-        const int row = lane < 16 ? plan[st * C::kPlanInts + lane] : -1;
-        if (row >= 0) {
-            const int r = lane >> 1, h = lane & 1;
-            tc::tma_load_2d(base + C::kRingOff + st * C::kStageBytes + C::kTileBytes + h * C::kHalfBytes +
-                                r * 2048,
-                            mapV, 64 * h, row, fullV0 + 8 * st, policy);
-        }
+        if (plan[st * C::kPlanInts + C::kPlanStop] != 0) break;
+        const int row = lane < 8 ? plan[st * C::kPlanInts + (is_v ? 16 : 0) + 2 * lane + half] : -1;
+        if (row >= 0)
+            tc::tma_load_2d(base + C::kRingOff + st * C::kStageBytes + (is_v ? C::kTileBytes : 0) +
+                                half * C::kHalfBytes + lane * 2048,
+                            map, 64 * half, row, full0 + 8 * st, policy);
         __syncwarp();
     }
 }
@@ -420,7 +430,7 @@ __device__ __forceinline__ void tc_mma1(uint32_t sK, uint32_t qop, uint32_t tS) 
     for (int j = 0; j < 8; ++j) {  // 16 head dimensions per step
         const uint64_t a = tc::smem_desc_sw128(sK + (j / 4) * C::kHalfBytes + (j % 4) * 32, 16, 1024);
         const uint64_t b = tc::smem_desc_sw128(qop + (j / 4) * 2048 + (j % 4) * 32, 16, 1024);
-        tc::mma_f16(tS, a, b, C::kIdescS, j > 0);
+        tc::mma_f16_warp(tS, a, b, C::kIdescS, j > 0);
     }
 }
 
@@ -431,7 +441,7 @@ __device__ __forceinline__ void tc_mma2(uint32_t sV, uint32_t pop, uint32_t tO) 
     for (int j = 0; j < 8; ++j) {  // 16 tokens per step
         const uint64_t a = tc::smem_desc_sw128(sV + j * 2048, C::kHalfBytes, 1024);
         const uint64_t b = tc::smem_desc_sw128(pop + (j / 4) * 2048 + (j % 4) * 32, 16, 1024);
-        tc::mma_f16(tO, a, b, C::kIdescO, j > 0);
+        tc::mma_f16_warp(tO, a, b, C::kIdescO, j > 0);
     }
 }
 
@@ -473,11 +483,10 @@ __device__ __forceinline__ void tc_mma(const DecodeParams& p, unsigned char* sm,
             ++nitems;
         }
         tc::fence_after_sync();
-        if (lane == 0) {
-            tc_mma1<T>(stage_k(c), qop, tmem + (c & 1) * C::kN);
-            tc::mma_commit(sfull0 + 8 * (c & 1));
-            tc::mma_commit(emptyK0 + 8 * st);  // K_c is free once MMA1 completed
-        }
+        // the whole warp runs the issue code, one elected lane (lane 0) issues
+        tc_mma1<T>(stage_k(c), qop, tmem + (c & 1) * C::kN);
+        tc::mma_commit_warp(sfull0 + 8 * (c & 1));
+        tc::mma_commit_warp(emptyK0 + 8 * st);  // K_c is free once MMA1 completed
         __syncwarp();
         return 0;
     };
@@ -507,12 +516,10 @@ __device__ __forceinline__ void tc_mma(const DecodeParams& p, unsigned char* sm,
             break;
         }
         tc::fence_after_sync();
-        if (lane == 0) {
-            tc_mma2<T>(stage_k(c) + C::kTileBytes, pop0 + (c & 1) * C::kOpBytes,
-                       tmem + 2 * C::kN + (c & 1) * C::kN);
-            tc::mma_commit(ofull0 + 8 * (c & 1));
-            tc::mma_commit(emptyV0 + 8 * (c % C::kStages));  // V_c is free
-        }
+        tc_mma2<T>(stage_k(c) + C::kTileBytes, pop0 + (c & 1) * C::kOpBytes,
+                   tmem + 2 * C::kN + (c & 1) * C::kN);
+        tc::mma_commit_warp(ofull0 + 8 * (c & 1));
+        tc::mma_commit_warp(emptyV0 + 8 * (c % C::kStages));  // V_c is free
         __syncwarp();
         if (!next_done) r = issue_mma1(c + 1);
         if (r < 0) {
@@ -520,10 +527,11 @@ __device__ __forceinline__ void tc_mma(const DecodeParams& p, unsigned char* sm,
             break;
         }
     }
-    if (lane == 0) {  // every MMA issued here has completed before tensor memory is freed
-        tc::mma_commit(drain);
-        if (!mbar_wait(drain, 0)) report(p.d_err, PA_DERR_TIMEOUT);
-    }
+    // every MMA issued here has completed before tensor memory is freed (the commit
+    // is elected like the MMAs, so it is made by the lane that issued them)
+    __syncwarp();
+    tc::mma_commit_warp(drain);
+    if (lane == 0 && !mbar_wait(drain, 0)) report(p.d_err, PA_DERR_TIMEOUT);
     __syncwarp();
 }
 
@@ -819,8 +827,12 @@ __global__ void __launch_bounds__(TcTile<T>::kThreads, 1)
         tc_mma<T>(p, sm, base, tmem);
     else if (warp < 10)
         tc_team<T, G, kMulti>(p, sm, tmem, (warp - 2) >> 2);
+    else if (warp == 10)
+        tc_copy<T>(p, &mapV, sm, base, true, 0);
+    else if (warp == 11)
+        tc_copy<T>(p, &mapK, sm, base, false, 1);
     else
-        tc_issue_v<T>(p, &mapV, sm, base);
+        tc_copy<T>(p, &mapV, sm, base, true, 1);
 
     tc::fence_before_sync();
     __syncthreads();
