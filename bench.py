@@ -122,6 +122,23 @@ def _oracle_row(w, kc, vc, s, r, n):
                               np.array([n], np.int32), scale=w.scale, dtype=w.dtype)
 
 
+def _max_over_ranks(values, dist, device):
+    """Element-wise maximum over the ranks of per-rank timings: the slowest
+    rank sets the step time (no collective on the data path; this one runs
+    after the timed region)."""
+    if dist is None:
+        return [float(v) for v in values]
+    import torch
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t]
+
+
+def _weak_value(world_size, bytes_per_rank, ms_per_step):
+    """Whole-job GB/s of weak scaling: every rank processes its own replica."""
+    return world_size * bytes_per_rank / (ms_per_step * 1e-3) / 1e9
+
+
 def _dist_env():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -408,10 +425,7 @@ def run_gpu(args):
     kvw_ms = float(np.mean([a.elapsed_time(b) for _, a, b, _ in ev]))
     ms_per_step = float(np.mean(step_ms))
     dec_ms_avg = float(np.mean(dec_ms))
-    if dist is not None:
-        t = torch.tensor([ms_per_step, dec_ms_avg], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_per_step, dec_ms_avg = float(t[0]), float(t[1])
+    ms_per_step, dec_ms_avg = _max_over_ranks([ms_per_step, dec_ms_avg], dist, dev)
 
     # end to end through the public API: the step's inputs from pinned host memory,
     # the output back to pinned host memory, every step.
@@ -436,18 +450,14 @@ def run_gpu(args):
         torch.cuda.synchronize()
         if i >= args.warmup:
             e2e_ms.append(e0.elapsed_time(e1))
-    e2e_avg = float(np.mean(e2e_ms))
-    if dist is not None:
-        t = torch.tensor([e2e_avg], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_avg = float(t[0])
+    e2e_avg = _max_over_ranks([float(np.mean(e2e_ms))], dist, dev)[0]
     torch.cuda.synchronize()
     if int(d_err.item()) != 0:
         raise RuntimeError(f"device error word {int(d_err.item())} during timing")
 
     kv_bytes = w.kv_read_bytes()
     unique_bytes = w.kv_unique_read_bytes() if w.num_pairs or "gqa" in w.name else kv_bytes
-    value = ws * kv_bytes / (ms_per_step * 1e-3) / 1e9
+    value = _weak_value(ws, kv_bytes, ms_per_step)
     peak, peak_kind = _peaks()
     achieved = kv_bytes / (dec_ms_avg * 1e-3) / 1e9
     seq_heads = w.num_seqs * w.num_q_heads
@@ -532,7 +542,7 @@ def run_gpu(args):
         "roofline": roof,
         **({"query_tokens_per_s": round(ws * w.num_query_tokens / (ms_per_step * 1e-3), 1)}
            if mq else {}),
-        "e2e": {"value": round(ws * kv_bytes / (e2e_avg * 1e-3) / 1e9, 2), "unit": "GB/s",
+        "e2e": {"value": round(_weak_value(ws, kv_bytes, e2e_avg), 2), "unit": "GB/s",
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                 "ms_per_step": round(e2e_avg, 5)},
         "components": {
