@@ -489,7 +489,7 @@ def run_gpu(args):
                 "peak": tensor_peak, "unit": "TFLOP/s", "frac": round(ach / tensor_peak, 4),
                 "peak_source": f"{tensor_kind} bf16_tflops (fp16 MMA runs at the bf16 rate)",
                 "flops": "4 x head_dim per (query row, head, token attended)",
-                "traffic": None, "algorithmic_flops_per_launch": int(flops),
+                "traffic": _ncu_traffic(args.config), "algorithmic_flops_per_launch": int(flops),
                 "hbm_achieved_gbs": round(unique_bytes / (dec_ms_avg * 1e-3) / 1e9, 2),
                 "avg_launch_ms": round(dec_ms_avg, 5)}
     elif alu_bound:
@@ -499,7 +499,7 @@ def run_gpu(args):
                 "peak_source": f"derived: {sms} SMs x {FP32_LANES_PER_SM} fp32 FMA lanes x 2 "
                                "flop x maximum SM clock (MEASURED_PEAKS sm_max_mhz)",
                 "flops": "4 x head_dim per (query row, head, token attended)",
-                "traffic": None, "algorithmic_flops_per_launch": int(flops),
+                "traffic": _ncu_traffic(args.config), "algorithmic_flops_per_launch": int(flops),
                 "hbm_achieved_gbs": round(unique_bytes / (dec_ms_avg * 1e-3) / 1e9, 2),
                 "avg_launch_ms": round(dec_ms_avg, 5)}
     else:
