@@ -37,6 +37,7 @@ if ROOT not in sys.path:
 
 METRIC = "paged decode attn KV-read GB/s (fraction of GB300 HBM peak); seq-heads/s"
 L2_FLUSH_BYTES = 256 << 20
+L2_BYTES = 129 << 20  # GB300 L2
 
 WORKLOAD_TEXT = {
     "llama7b": "LLaMA-7B-shaped single-layer decode: 64 seqs, 32 q/kv heads, head_dim 128, fp16 "
@@ -534,8 +535,11 @@ def run_gpu(args):
                    "partition_tokens": P, "kv_read_bytes_per_step": kv_bytes,
                    **({"query_tokens": w.num_query_tokens} if mq else {}),
                    "layout": w.meta.get("layout", "paged"),
-                   "l2": "KV pool larger than L2 and a 256 MB L2 flush before every step "
-                         "(outside the timed events)",
+                   "l2": ("KV pool larger than L2 and a 256 MB L2 flush before every step "
+                          "(outside the timed events)")
+                         if 2 * w.k_cache.nbytes > L2_BYTES else
+                         "a 256 MB L2 flush before every step (outside the timed events); the "
+                         "KV pool itself fits in L2",
                    "parallelism": f"weak: {ws} independent replicas of the batch, one per GPU"},
         "seq_heads_per_s": round(ws * seq_heads / (ms_per_step * 1e-3), 1),
         "hbm_frac": round(value / ws / peak, 4),
