@@ -479,8 +479,10 @@ def run_gpu(args):
         avg = -(-w.num_query_tokens // w.num_seqs)
         while tc_tokens * 2 * g <= 16 and tc_tokens < avg:
             tc_tokens *= 2
-    tc_path = (not fp8 and w.dtype in ("f16", "bf16") and w.head_dim == 128 and g <= 16
-               and P % 128 == 0 and (tc_tokens * g >= 4 if mq else g >= 4))
+    # (E4M3 caches: grouped-head decode, its codes widened to 16 bits in shared memory)
+    tc_path = (w.head_dim == 128 and g <= 16 and P % 128 == 0 and
+               ((fp8 and not mq and g >= 4) or
+                (not fp8 and w.dtype in ("f16", "bf16") and (tc_tokens * g >= 4 if mq else g >= 4))))
     tensor_peak, tensor_kind = _tensor_peak()
     tensor_bound = tc_path and flops / (tensor_peak * 1e12) > unique_bytes / (peak * 1e9)
     alu_bound = not tc_path and flops / (alu_peak * 1e12) > unique_bytes / (peak * 1e9)

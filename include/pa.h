@@ -315,8 +315,11 @@ pa_status pa_swap_blocks_fp8(const void* src_k, const void* src_v, const float* 
  * PA_BF16).  The logit of a token is (q . K codes) x its K scale x scale, and
  * its softmax weight is multiplied by its V scale before it weights the V
  * codes; accumulation fp32.  Partitions and workspace: pa_decode_partition_tokens
- * and pa_decode_workspace_size with dtype PA_E4M3.  Runs on the SIMT kernel
- * for every head grouping (head_dim 128). */
+ * and pa_decode_workspace_size with dtype PA_E4M3 (head_dim 128).  Grouped
+ * heads (4 to 16 query heads per kv head, partitions a multiple of 128 tokens)
+ * run on the tensor-core kernel (the codes widened exactly to q_dtype for
+ * the products, the V-scaled softmax weights rounded to q_dtype for P.V), the
+ * other groupings on the SIMT kernel. */
 pa_status pa_decode_fp8(void* out, const void* q, pa_dtype q_dtype, const void* k_cache,
                         const void* v_cache, const float* k_scale, const float* v_scale,
                         const int32_t* block_tables, int max_blocks_per_seq,

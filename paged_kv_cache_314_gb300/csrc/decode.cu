@@ -18,11 +18,12 @@ namespace {
 constexpr int kDefaultPartitionTokens = 512;
 constexpr int kDefaultPartitionTokensTc = 2048;
 
-// Grouped-query heads with 16-bit K/V and head_dim 128 run on the tensor cores.
+// Grouped-query heads with 16-bit or E4M3 K/V and head_dim 128 run on the tensor cores.
 bool tc_shape(int num_q_heads, int num_kv_heads, int head_dim, pa_dtype dtype) {
     if (num_kv_heads <= 0 || num_q_heads % num_kv_heads != 0) return false;
     const int g = num_q_heads / num_kv_heads;
-    return (dtype == PA_F16 || dtype == PA_BF16) && head_dim == 128 && g >= 4 && g <= 16;
+    return (dtype == PA_F16 || dtype == PA_BF16 || dtype == PA_E4M3) && head_dim == 128 && g >= 4 &&
+           g <= 16;
 }
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -88,6 +89,20 @@ bool make_pool_map(CUtensorMap* map, const void* pool, long long rows, pa_dtype 
     return encode(map, dtype == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
                   2, const_cast<void*>(pool), dims, strides, box, elem_strides,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// An E4M3 pool as a [rows][128] byte matrix, read in [16 rows x 128 bytes]
+// boxes without swizzle (the kernel widens them in shared memory).
+bool make_pool_map_fp8(CUtensorMap* map, const void* pool, long long rows) {
+    PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
+    if (encode == nullptr) return false;
+    const cuuint64_t dims[2] = {128, static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {128};
+    const cuuint32_t box[2] = {128, 16};
+    const cuuint32_t elem_strides[2] = {1, 1};
+    return encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(pool), dims, strides, box,
+                  elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -219,16 +234,29 @@ pa_status run_attention(const AttnCall& a) {
     p.qk_scale_log2 = a.scale * 1.4426950408889634f;  // log2(e)
 
     const cudaStream_t st = as_cuda(a.stream);
-    if (a.k_scale != nullptr) {  // E4M3 cache: the SIMT kernel, head_dim 128
-        const int gt = heads * tokens;
+    const long long pool_rows = static_cast<long long>(a.num_blocks) * a.num_kv_heads * a.block_size;
+    if (a.k_scale != nullptr) {  // E4M3 cache, head_dim 128
         if (a.query_start != nullptr) return PA_ERR_UNSUPPORTED;
+        // grouped heads: the tensor-core kernel, which widens the codes in shared memory
+        if (tc_shape(a.num_q_heads, a.num_kv_heads, a.head_dim, PA_E4M3) && P % 128 == 0 &&
+            pool_rows < 0x7fffffffLL) {
+            CUtensorMap map_k, map_v;
+            if (make_pool_map_fp8(&map_k, a.k_cache, pool_rows) &&
+                make_pool_map_fp8(&map_v, a.v_cache, pool_rows)) {
+                p.head_tiles = a.num_kv_heads;
+                p.tile_heads = group;
+                p.tile_tokens = 1;
+                return a.dtype == PA_BF16 ? launch_decode_tc_fp8_bf16(p, map_k, map_v, st)
+                                          : launch_decode_tc_fp8_f16(p, map_k, map_v, st);
+            }
+        }
+        const int gt = heads * tokens;
         return a.dtype == PA_BF16 ? launch_decode_fp8_bf16(p, gt, st)
                                   : launch_decode_fp8_f16(p, gt, st);
     }
     // 16-bit K/V with head_dim 128 and at least 4 query rows per kv head in a
     // work item (grouped heads, or several query tokens x heads): the
     // tensor-core path, items of all g heads of one kv head.
-    const long long pool_rows = static_cast<long long>(a.num_blocks) * a.num_kv_heads * a.block_size;
     const bool tc_ok = (a.dtype == PA_F16 || a.dtype == PA_BF16) && a.head_dim == 128 &&
                        P % 128 == 0 && pool_rows < 0x7fffffffLL && group <= 16;
     int tc_tokens = 1;  // query tokens per tensor-core item: up to 16 rows

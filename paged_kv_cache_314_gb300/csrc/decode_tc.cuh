@@ -69,7 +69,9 @@ struct TcTile {
     static constexpr int kPlanOff = kMetaOff + kStages * 32;
     static constexpr int kPlanInts = 36;
     static constexpr int kPlanStop = 32;
-    static constexpr int kBarOff = kPlanOff + kStages * kPlanInts * 4;
+    // E4M3 caches: the K and V scales of each stage's eight 16-token groups [kStages][16]
+    static constexpr int kScaleOff = kPlanOff + kStages * kPlanInts * 4;
+    static constexpr int kBarOff = kScaleOff + kStages * 16 * 4;
     // fullK[S], emptyK[S], qfull[Q], qempty[Q], q_ready, s_full[2], p_full[2], o_full[2],
     // drain, fullV[S], emptyV[S], vplan[S]: the K and V halves of a ring slot land and
     // are released separately (K after MMA1 of its stage, V after MMA2); a stage's V
@@ -78,7 +80,10 @@ struct TcTile {
     static constexpr int kEmptyVBar = kFullVBar + kStages;
     static constexpr int kVPlanBar = kEmptyVBar + kStages;
     static constexpr int kKPlanBar = kVPlanBar + kStages;
-    static constexpr int kNumBars = kKPlanBar + kStages;
+    // E4M3 caches: a stage's K and V, widened to 16 bits in place by the two teams
+    // (one arrival each), are ready for the MMAs
+    static constexpr int kConvBar = kKPlanBar + kStages;
+    static constexpr int kNumBars = kConvBar + kStages;
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;       // tmem base, abort, team flags
     static constexpr int kSmemBytes = kMiscOff + 32 + 1024;       // + alignment slack
     // producer, MMA, two teams of 4 warps, three copy warps: the 32 TMA boxes of a
@@ -109,7 +114,10 @@ struct TcItemRec {
     int pad[3];
 };
 
-template <typename T, bool kMulti>
+// kFp8: the cache holds E4M3 codes; each 16-token block is one [16 x 128-byte]
+// box per tensor, landing row-major in the upper half of the stage's 32 KB
+// tile (the teams widen it in place); the blocks' scales go beside the stage.
+template <typename T, bool kMulti, bool kFp8>
 __device__ __forceinline__ void tc_produce(const DecodeParams& p, const CUtensorMap* mapK,
                                            const CUtensorMap* mapV, unsigned char* sm,
                                            uint32_t base) {
@@ -251,6 +259,16 @@ __device__ __forceinline__ void tc_produce(const DecodeParams& p, const CUtensor
         const int blk_end = (tok_end + B - 1) / B;
         int win = tok_begin / B;
         int32_t entry = (win + lane < blk_end) ? __ldg(trow + win + lane) : -1;
+        float ks_lane = 0.f, vs_lane = 0.f;  // E4M3: the scales of this lane's block
+        auto load_scales = [&]() {
+            if constexpr (kFp8) {
+                const bool in = static_cast<unsigned>(entry) < static_cast<unsigned>(p.num_blocks);
+                const size_t si = static_cast<size_t>(in ? entry : 0) * p.num_kv_heads + hk;
+                ks_lane = in ? __ldg(p.k_scale + si) : 0.f;
+                vs_lane = in ? __ldg(p.v_scale + si) : 0.f;
+            }
+        };
+        load_scales();
 
         for (int i = 0; i < nst; ++i) {
             const int cc = c + i;
@@ -270,14 +288,20 @@ __device__ __forceinline__ void tc_produce(const DecodeParams& p, const CUtensor
             if (t1 > t0 && (t1 - 1) / B - win >= 32) {  // window must hold the stage's blocks
                 win = t0 / B;
                 entry = (win + lane < blk_end) ? __ldg(trow + win + lane) : -1;
+                load_scales();
             }
             const int r = lane >> 2;
             const int t = t0 + 16 * r;
             int row = 0;
             bool mine = false, bad = false;
+            float ks_r = 0.f, vs_r = 0.f;  // E4M3: the scales of this lane's block
             {
                 const int lb = t < t1 ? t / B : win;
                 const int pb = __shfl_sync(0xffffffffu, entry, lb - win);
+                if constexpr (kFp8) {
+                    ks_r = __shfl_sync(0xffffffffu, ks_lane, lb - win);
+                    vs_r = __shfl_sync(0xffffffffu, vs_lane, lb - win);
+                }
                 if (t < t1) {
                     if (static_cast<unsigned>(pb) < static_cast<unsigned>(p.num_blocks)) {
                         row = (pb * p.num_kv_heads + hk) * B + (t - lb * B);
@@ -293,17 +317,21 @@ __device__ __forceinline__ void tc_produce(const DecodeParams& p, const CUtensor
 #pragma unroll
             for (int g8 = 0; g8 < 8; ++g8) groups |= ((loaded >> (4 * g8)) & 1u) << g8;
             const uint32_t fullK = fullK0 + 8 * st, fullV = fullV0 + 8 * st;
-            const uint32_t half_bytes = static_cast<uint32_t>(__popc(groups)) * 2u * 2048u;  // K or V
+            // bytes of K (or of V) the stage's loaded groups carry
+            const uint32_t half_bytes = static_cast<uint32_t>(__popc(groups)) * (kFp8 ? 1u : 2u) * 2048u;
             const uint32_t stage_base = base + C::kRingOff + st * C::kStageBytes;
             const int h = (lane >> 1) & 1;
             // K boxes first (their bytes complete on fullK before its arrival is posted):
             // the second 64-column half goes to warp 11 through the plan
-            if ((lane & 1) == 0) plan[st * C::kPlanInts + (lane >> 1)] = mine ? row : -1;
+            // (E4M3: one box holds a block's whole rows; the second half has none)
+            if ((lane & 1) == 0)
+                plan[st * C::kPlanInts + (lane >> 1)] = (mine && !(kFp8 && h == 1)) ? row : -1;
             if (lane == 0) plan[st * C::kPlanInts + C::kPlanStop] = 0;  // not the last stage
             __syncwarp();
             if (lane == 0) mbar_arrive(kplan0 + 8 * st);
             if (mine && (lane & 3) == 0)
-                tc::tma_load_2d(stage_base + r * 2048, mapK, 0, row, fullK, policy);
+                tc::tma_load_2d(stage_base + (kFp8 ? C::kHalfBytes : 0) + r * 2048, mapK, 0, row, fullK,
+                                policy);
             __syncwarp();
             // the V half is free once MMA2 of the slot's previous stage completed
             if (cc >= C::kStages && !mbar_wait_warp(emptyV0 + 8 * st, reuse)) {
@@ -316,6 +344,14 @@ __device__ __forceinline__ void tc_produce(const DecodeParams& p, const CUtensor
                 k_only = cc;
                 c = cc + 1;
                 break;
+            }
+            if constexpr (kFp8) {  // the groups' scales, K then V, beside the stage
+                if ((lane & 3) == 0) {
+                    float* sc = reinterpret_cast<float*>(sm + C::kScaleOff) + st * 16;
+                    sc[r] = ks_r;
+                    sc[8 + r] = vs_r;
+                }
+                __syncwarp();  // before lane 0 posts the arrivals
             }
             if (lane == 0) {
                 uint32_t flags = 0;
@@ -333,7 +369,8 @@ __device__ __forceinline__ void tc_produce(const DecodeParams& p, const CUtensor
                 mbar_arrive_expect_tx(fullV, half_bytes);
             }
             // the V boxes: their rows go to warps 10 and 12 (lane 4g+2h+1 -> entry 16+2g+h)
-            if ((lane & 1) != 0) plan[st * C::kPlanInts + 16 + (lane >> 1)] = mine ? row : -1;
+            if ((lane & 1) != 0)
+                plan[st * C::kPlanInts + 16 + (lane >> 1)] = (mine && !(kFp8 && h == 1)) ? row : -1;
             __syncwarp();
             if (lane == 0) mbar_arrive(vplan0 + 8 * st);
         }
@@ -384,7 +421,7 @@ __device__ __forceinline__ void tc_produce(const DecodeParams& p, const CUtensor
 // tensor's boxes of one 64-column half (one per lane, lanes 0-7 = the stage's
 // eight 16-token groups); they complete on fullK / fullV, whose arrivals the
 // producer posts with the expected bytes.
-template <typename T>
+template <typename T, bool kFp8>
 __device__ __forceinline__ void tc_copy(const DecodeParams& p, const CUtensorMap* map,
                                         unsigned char* sm, uint32_t base, bool is_v, int half) {
     using C = TcTile<T>;
@@ -404,11 +441,27 @@ __device__ __forceinline__ void tc_copy(const DecodeParams& p, const CUtensorMap
         }
         if (plan[st * C::kPlanInts + C::kPlanStop] != 0) break;
         const int row = lane < 8 ? plan[st * C::kPlanInts + (is_v ? 16 : 0) + 2 * lane + half] : -1;
-        if (row >= 0)
+        if (row >= 0)  // (E4M3: whole 128-byte rows into the tile's upper half)
             tc::tma_load_2d(base + C::kRingOff + st * C::kStageBytes + (is_v ? C::kTileBytes : 0) +
-                                half * C::kHalfBytes + lane * 2048,
-                            map, 64 * half, row, full0 + 8 * st, policy);
+                                (kFp8 ? 1 : half) * C::kHalfBytes + lane * 2048,
+                            map, kFp8 ? 0 : 64 * half, row, full0 + 8 * st, policy);
         __syncwarp();
+    }
+}
+
+// Two E4M3 codes (the low 16 bits, lower address first) widened to a pair of
+// T.  Every E4M3 value is exact in binary16 and in bfloat16, so the widening
+// loses nothing: the hardware conversion to half2, then (bfloat16) through fp32.
+template <typename T>
+__device__ __forceinline__ uint32_t widen_e4m3x2(uint32_t two_codes) {
+    const __half2_raw hr =
+        __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two_codes & 0xffffu), __NV_E4M3);
+    if constexpr (std::is_same<T, __half>::value) {
+        return static_cast<uint32_t>(hr.x) | (static_cast<uint32_t>(hr.y) << 16);
+    } else {
+        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&hr));
+        const __nv_bfloat162 h = __floats2bfloat162_rn(f.x, f.y);
+        return *reinterpret_cast<const uint32_t*>(&h);
     }
 }
 
@@ -449,14 +502,16 @@ __device__ __forceinline__ void tc_mma2(uint32_t sV, uint32_t pop, uint32_t tO) 
 // (MMA2) once the team has written P_c.  MMA1 of the next stage is issued
 // before MMA2 of this one when the next stage has already landed and belongs
 // to the same item, so the team's softmax of stage c+1 overlaps MMA2 of c.
-template <typename T>
+template <typename T, bool kFp8>
 __device__ __forceinline__ void tc_mma(const DecodeParams& p, unsigned char* sm, uint32_t base,
                                        uint32_t tmem) {
     using C = TcTile<T>;
     using Bi = TcBars<T>;
     const int lane = threadIdx.x & 31;
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::kBarOff);
-    const uint32_t fullK0 = smem_addr(bars), emptyK0 = smem_addr(bars + C::kStages);
+    // the K operand of a stage is ready when it landed (16-bit) or was widened (E4M3)
+    const uint32_t fullK0 = smem_addr(bars + (kFp8 ? C::kConvBar : 0));
+    const uint32_t emptyK0 = smem_addr(bars + C::kStages);
     const uint32_t emptyV0 = smem_addr(bars + C::kEmptyVBar);
     const uint32_t qready = smem_addr(bars + Bi::kQReady);
     const uint32_t sfull0 = smem_addr(bars + Bi::kSFull), pfull0 = smem_addr(bars + Bi::kPFull);
@@ -598,7 +653,15 @@ __device__ __forceinline__ float warp_reduce_scatter(const float (&v)[N], int la
 // own O-accumulate and the output rows of the team's heads.  Team 0 also
 // zeroes the V rows of invalid tokens.  Each team signals p_full, q_ready and
 // qempty once (those barriers count two arrivals).
-template <typename T, int G, bool kMulti>
+// E4M3 caches (kFp8): at the start of each stage team 0 widens the K tile and
+// team 1 the V tile in place, one token row per thread: the row's 128 codes
+// (landed row-major in the tile's upper half), exact in T, stored in the
+// 128-byte-swizzled layout the MMAs read (rows of invalid tokens become zero).
+// A row's second 64 columns land in the same 128 bytes its codes occupied, so
+// each thread only overwrites what it has read.  The scales stay in fp32: the
+// K scale of a token's block multiplies its logits, the V scale its softmax
+// weight before that is rounded to T for the P.V product.
+template <typename T, int G, bool kMulti, bool kFp8>
 __device__ __forceinline__ void tc_team(const DecodeParams& p, unsigned char* sm, uint32_t tmem,
                                         int team_id) {
     using C = TcTile<T>;
@@ -612,6 +675,7 @@ __device__ __forceinline__ void tc_team(const DecodeParams& p, unsigned char* sm
     const int h0 = team_id * H;
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::kBarOff);
     const uint32_t fullV0 = smem_addr(bars + C::kFullVBar);  // V landed (and the stage's meta)
+    const uint32_t fullK0 = smem_addr(bars), conv0 = smem_addr(bars + C::kConvBar);
     const uint32_t qfull0 = smem_addr(bars + 2 * C::kStages);
     const uint32_t qempty0 = smem_addr(bars + 2 * C::kStages + C::kQSlots);
     const uint32_t qready = smem_addr(bars + Bi::kQReady);
@@ -656,7 +720,36 @@ __device__ __forceinline__ void tc_team(const DecodeParams& p, unsigned char* sm
         const int st = c % C::kStages;
         if (!team.wait(fullV0 + 8 * st, static_cast<uint32_t>(c / C::kStages) & 1, p.d_err, abort_flag)) break;
         const uint32_t flags = meta[st].flags;
-        if (flags & kStageEnd) break;
+        if (flags & kStageEnd) {
+            if (kFp8 && tid == 0) mbar_arrive(conv0 + 8 * st);  // the MMA warp reads the end there
+            break;
+        }
+        if constexpr (kFp8) {
+            if (team_id == 0 &&  // (team 1 widens V, which fullV already covers)
+                !team.wait(fullK0 + 8 * st, static_cast<uint32_t>(c / C::kStages) & 1, p.d_err, abort_flag))
+                break;
+            const int nv = meta[st].nvalid;
+            const uint32_t grp = meta[st].groups;
+            const bool ok = row < nv && ((grp >> (row >> 4)) & 1u);
+            unsigned char* tile = sm + C::kRingOff + st * C::kStageBytes + team_id * C::kTileBytes;
+            uint4 codes[8];
+            const uint4* src = reinterpret_cast<const uint4*>(tile + C::kHalfBytes + row * 128);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) codes[k] = ok ? src[k] : make_uint4(0, 0, 0, 0);
+            unsigned char* dst_row = tile + (row >> 3) * 1024 + (row & 7) * 128;
+#pragma unroll
+            for (int ch = 0; ch < 16; ++ch) {  // 8 codes -> one 16-byte chunk of the row
+                const uint4& u = codes[ch >> 1];
+                const uint32_t a = (ch & 1) ? u.z : u.x, b = (ch & 1) ? u.w : u.y;
+                *reinterpret_cast<uint4*>(dst_row + (ch >> 3) * C::kHalfBytes +
+                                          (((ch & 7) ^ (row & 7)) << 4)) =
+                    make_uint4(widen_e4m3x2<T>(a), widen_e4m3x2<T>(a >> 16), widen_e4m3x2<T>(b),
+                               widen_e4m3x2<T>(b >> 16));
+            }
+            tc::fence_async_smem();  // the widened tiles are read by the MMAs
+            team.sync();
+            if (tid == 0) mbar_arrive(conv0 + 8 * st);
+        }
         const int item_seq = static_cast<int>(meta[st].item_seq);
         const int nvalid = meta[st].nvalid;
         const uint32_t groups = meta[st].groups;
@@ -697,10 +790,16 @@ __device__ __forceinline__ void tc_team(const DecodeParams& p, unsigned char* sm
         tc::tmem_ld<H>(tmem + (c & 1) * C::kN + h0 + lane_off, x);
         const bool valid = row < nvalid && ((groups >> (row >> 4)) & 1u);
         const int lim_rel = kMulti ? meta[st].lim_rel : C::kStageTok;
+        float kq = p.qk_scale_log2, vsc = 1.f;  // E4M3: this token's block scales folded in
+        if constexpr (kFp8) {
+            const float* sc = reinterpret_cast<const float*>(sm + C::kScaleOff) + st * 16;
+            kq *= sc[row >> 4];
+            vsc = sc[8 + (row >> 4)];
+        }
 #pragma unroll
         for (int h = 0; h < H; ++h)  // several queries: row h sees the first lim_rel + qtok[h] tokens
             x[h] = (valid && h0 + h < rec.nrows && (!kMulti || row < lim_rel + qtok[h]))
-                       ? x[h] * p.qk_scale_log2
+                       ? x[h] * kq
                        : -INFINITY;
         {
             const float mx = warp_reduce_scatter<H, true>(x, lane);
@@ -727,9 +826,10 @@ __device__ __forceinline__ void tc_team(const DecodeParams& p, unsigned char* sm
             // several queries: every row is written, 0 past the item's rows)
             if (kMulti || hh < g)
                 *reinterpret_cast<T*>(pop + (row >> 6) * 2048 + (hh >> 3) * 1024 + (hh & 7) * 128 +
-                                      ((((col >> 3) ^ (hh & 7))) << 4) + (col & 7) * 2) = Elem<T>::from_float(pr);
+                                      ((((col >> 3) ^ (hh & 7))) << 4) + (col & 7) * 2) =
+                    Elem<T>::from_float(kFp8 ? pr * vsc : pr);
         }
-        if (!valid && team_id == 0) {  // zero this token's V row (both 64-column halves)
+        if (!kFp8 && !valid && team_id == 0) {  // zero this token's V row (both 64-column halves)
             unsigned char* vrow = sm + C::kRingOff + st * C::kStageBytes + C::kTileBytes +
                                   (row >> 3) * 1024 + (row & 7) * 128;
 #pragma unroll
@@ -786,7 +886,7 @@ __device__ __forceinline__ void tc_team(const DecodeParams& p, unsigned char* sm
     tc::fence_before_sync();
 }
 
-template <typename T, int G, bool kMulti>
+template <typename T, int G, bool kMulti, bool kFp8>
 __global__ void __launch_bounds__(TcTile<T>::kThreads, 1)
     decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap mapK,
                      const __grid_constant__ CUtensorMap mapV) {
@@ -802,8 +902,10 @@ __global__ void __launch_bounds__(TcTile<T>::kThreads, 1)
     if (threadIdx.x == 0) {
         for (int i = 0; i < C::kNumBars; ++i) {
             // qempty, q_ready and p_full are signalled once by each of the two teams
+            // (and so is conv, E4M3 only: K by team 0, V by team 1)
             const bool two = (i >= 2 * C::kStages + C::kQSlots && i <= TcBars<T>::kQReady) ||
-                             i == TcBars<T>::kPFull || i == TcBars<T>::kPFull + 1;
+                             i == TcBars<T>::kPFull || i == TcBars<T>::kPFull + 1 ||
+                             i >= C::kConvBar;
             mbar_init(smem_addr(bars + i), two ? 2 : 1);
         }
         *reinterpret_cast<volatile int*>(sm + C::kMiscOff + 4) = 0;
@@ -822,17 +924,17 @@ __global__ void __launch_bounds__(TcTile<T>::kThreads, 1)
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
 
     if (warp == 0)
-        tc_produce<T, kMulti>(p, &mapK, &mapV, sm, base);
+        tc_produce<T, kMulti, kFp8>(p, &mapK, &mapV, sm, base);
     else if (warp == 1)
-        tc_mma<T>(p, sm, base, tmem);
+        tc_mma<T, kFp8>(p, sm, base, tmem);
     else if (warp < 10)
-        tc_team<T, G, kMulti>(p, sm, tmem, (warp - 2) >> 2);
+        tc_team<T, G, kMulti, kFp8>(p, sm, tmem, (warp - 2) >> 2);
     else if (warp == 10)
-        tc_copy<T>(p, &mapV, sm, base, true, 0);
+        tc_copy<T, kFp8>(p, &mapV, sm, base, true, 0);
     else if (warp == 11)
-        tc_copy<T>(p, &mapK, sm, base, false, 1);
+        tc_copy<T, kFp8>(p, &mapK, sm, base, false, 1);
     else
-        tc_copy<T>(p, &mapV, sm, base, true, 1);
+        tc_copy<T, kFp8>(p, &mapV, sm, base, true, 1);
 
     tc::fence_before_sync();
     __syncthreads();
@@ -850,7 +952,7 @@ __global__ void __launch_bounds__(TcTile<T>::kThreads, 1)
     }
 }
 
-template <typename T, bool kMulti>
+template <typename T, bool kMulti, bool kFp8 = false>
 inline pa_status launch_decode_tc_typed(const DecodeParams& p, const CUtensorMap& mapK,
                                         const CUtensorMap& mapV, cudaStream_t stream) {
     using C = TcTile<T>;
@@ -858,9 +960,9 @@ inline pa_status launch_decode_tc_typed(const DecodeParams& p, const CUtensorMap
     const int rows = kMulti ? p.tile_tokens * p.group : p.group;
     if (rows > C::kN) return PA_ERR_UNSUPPORTED;
     const int G = rows <= 4 ? 4 : rows <= 8 ? 8 : 16;
-    auto kernel = G == 4   ? decode_tc_kernel<T, 4, kMulti>
-                  : G == 8 ? decode_tc_kernel<T, 8, kMulti>
-                           : decode_tc_kernel<T, 16, kMulti>;
+    auto kernel = G == 4   ? decode_tc_kernel<T, 4, kMulti, kFp8>
+                  : G == 8 ? decode_tc_kernel<T, 8, kMulti, kFp8>
+                           : decode_tc_kernel<T, 16, kMulti, kFp8>;
     if (ensure_smem(kernel, C::kSmemBytes, smem_configured[G == 4 ? 0 : G == 8 ? 1 : 2]) != PA_OK)
         return PA_ERR_CUDA;
     int dev = 0, sms = 0;
@@ -891,5 +993,10 @@ pa_status launch_multi_query_tc_f16(const DecodeParams& p, const CUtensorMap& ma
                                     const CUtensorMap& mapV, cudaStream_t stream);
 pa_status launch_multi_query_tc_bf16(const DecodeParams& p, const CUtensorMap& mapK,
                                      const CUtensorMap& mapV, cudaStream_t stream);
+// E4M3 K/V, 16-bit queries (maps over the 8-bit pools: 128-byte rows, 16-row boxes)
+pa_status launch_decode_tc_fp8_f16(const DecodeParams& p, const CUtensorMap& mapK,
+                                   const CUtensorMap& mapV, cudaStream_t stream);
+pa_status launch_decode_tc_fp8_bf16(const DecodeParams& p, const CUtensorMap& mapK,
+                                    const CUtensorMap& mapV, cudaStream_t stream);
 
 }  // namespace pa

@@ -148,3 +148,31 @@ def test_fp8_swap_round_trip_through_pinned_host_memory():
     for i, b in enumerate(blocks):
         assert same_bits(dst[0][NB - 1 - i].cpu().numpy(), kc[b])
         assert same_bits(dst[3][NB - 1 - i].cpu().numpy(), w.v_scale[b])
+
+
+# Grouped heads (4 to 16 query heads per kv head) with partitions a multiple of
+# 128 tokens: the tensor-core kernel, which widens the codes in shared memory.
+FP8_TC = [
+    # q dtype, Hq, Hkv, B, P, ctx
+    ("bf16", 8, 2, 16, 128, [1, 15, 16, 17, 127, 128, 129, 300, 1000]),   # 4 per kv head
+    ("f16", 32, 4, 32, 512, [3, 100, 257, 600, 2049]),                     # 8 per kv head
+    ("bf16", 32, 2, 128, 0, [128, 129, 1000, 2100, 4097]),                 # 16 per kv head
+    ("f16", 24, 4, 64, 256, [1, 63, 64, 65, 400, 777]),                    # 6: padded to 8 rows
+]
+
+
+@pytest.mark.parametrize("case", range(len(FP8_TC)))
+def test_fp8_tensor_core_parity(case):
+    dtype, Hq, Hkv, B, P, ctx = FP8_TC[case]
+    w = wl.to_fp8(wl.custom(f"fp8_tc{case}", ctx, dtype=dtype, num_q_heads=Hq, num_kv_heads=Hkv,
+                            head_dim=128, block_size=B, seed=550 + case, pool_factor=1.3),
+                  seed=560 + case)
+    _, out, _ = _check(w, partition_tokens=P)
+    again = _gpu_step(w, _upload(w), partition_tokens=P)
+    assert torch.equal(out, again), "two identical runs differ"
+
+
+def test_fp8_tensor_core_default_partition():
+    # grouped E4M3 heads default to the tensor-core partition length
+    assert pa.decode_partition_tokens(32, 4, 128, 256, 16, "e4m3") == 2048
+    assert pa.decode_partition_tokens(32, 32, 128, 256, 16, "e4m3") == 512
