@@ -80,8 +80,8 @@ struct TcTile {
     static constexpr int kEmptyVBar = kFullVBar + kStages;
     static constexpr int kVPlanBar = kEmptyVBar + kStages;
     static constexpr int kKPlanBar = kVPlanBar + kStages;
-    // E4M3 caches: a stage's K and V, widened to 16 bits in place by the two teams
-    // (one arrival each), are ready for the MMAs
+    // E4M3 caches: a stage's K, widened to 16 bits in place by team 0, is ready for
+    // MMA1 (its V, widened by team 1, is covered by that team's p_full)
     static constexpr int kConvBar = kKPlanBar + kStages;
     static constexpr int kNumBars = kConvBar + kStages;
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;       // tmem base, abort, team flags
@@ -449,20 +449,25 @@ __device__ __forceinline__ void tc_copy(const DecodeParams& p, const CUtensorMap
     }
 }
 
-// Two E4M3 codes (the low 16 bits, lower address first) widened to a pair of
-// T.  Every E4M3 value is exact in binary16 and in bfloat16, so the widening
-// loses nothing: the hardware conversion to half2, then (bfloat16) through fp32.
+// Four E4M3 codes (lower address in the low byte) widened to four T, two per
+// word.  Every E4M3 value is exact in binary16 and in bfloat16: the hardware
+// conversion of a code pair to half2, then (bfloat16) through fp32.
 template <typename T>
-__device__ __forceinline__ uint32_t widen_e4m3x2(uint32_t two_codes) {
-    const __half2_raw hr =
-        __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two_codes & 0xffffu), __NV_E4M3);
-    if constexpr (std::is_same<T, __half>::value) {
-        return static_cast<uint32_t>(hr.x) | (static_cast<uint32_t>(hr.y) << 16);
-    } else {
-        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&hr));
-        const __nv_bfloat162 h = __floats2bfloat162_rn(f.x, f.y);
-        return *reinterpret_cast<const uint32_t*>(&h);
+__device__ __forceinline__ uint2 widen_e4m3x4(uint32_t four_codes) {
+    uint32_t w[2];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(
+            static_cast<__nv_fp8x2_storage_t>((four_codes >> (16 * i)) & 0xffffu), __NV_E4M3);
+        if constexpr (std::is_same<T, __half>::value) {
+            w[i] = static_cast<uint32_t>(hr.x) | (static_cast<uint32_t>(hr.y) << 16);
+        } else {
+            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&hr));
+            const __nv_bfloat162 h = __floats2bfloat162_rn(f.x, f.y);
+            w[i] = *reinterpret_cast<const uint32_t*>(&h);
+        }
     }
+    return make_uint2(w[0], w[1]);
 }
 
 // Barrier indices after full[S], empty[S], qfull[Q], qempty[Q].
@@ -653,8 +658,9 @@ __device__ __forceinline__ float warp_reduce_scatter(const float (&v)[N], int la
 // own O-accumulate and the output rows of the team's heads.  Team 0 also
 // zeroes the V rows of invalid tokens.  Each team signals p_full, q_ready and
 // qempty once (those barriers count two arrivals).
-// E4M3 caches (kFp8): at the start of each stage team 0 widens the K tile and
-// team 1 the V tile in place, one token row per thread: the row's 128 codes
+// E4M3 caches (kFp8): team 1 widens the stage's V tile at the start of each
+// stage, team 0 the next stage's K tile once it has posted this stage's P (the
+// first stage's at its start), in place, one token row per thread: the row's 128 codes
 // (landed row-major in the tile's upper half), exact in T, stored in the
 // 128-byte-swizzled layout the MMAs read (rows of invalid tokens become zero).
 // A row's second 64 columns land in the same 128 bytes its codes occupied, so
@@ -704,6 +710,39 @@ __device__ __forceinline__ void tc_team(const DecodeParams& p, unsigned char* sm
 #pragma unroll
     for (int h = 0; h < H; ++h) qtok[h] = kMulti ? (h0 + h) / g : 0;
 
+    // E4M3: widen this team's tile of ring slot sl (team 0: K, team 1: V).
+    int kconv_next = 0;  // team 0: first stage whose K has not been widened
+    auto widen = [&](int sl) {
+        const int nv = meta[sl].nvalid;
+        const uint32_t grp = meta[sl].groups;
+        const bool ok = row < nv && ((grp >> (row >> 4)) & 1u);
+        unsigned char* tile = sm + C::kRingOff + sl * C::kStageBytes + team_id * C::kTileBytes;
+        const uint4* src = reinterpret_cast<const uint4*>(tile + C::kHalfBytes + row * 128);
+        unsigned char* dst_row = tile + (row >> 3) * 1024 + (row & 7) * 128;
+        // All 16-byte pieces of the row are read before any is written: the row's
+        // second 64 columns overwrite its codes.  Each thread starts at piece
+        // (row & 7), so the 8 rows of a shared-memory wavefront touch 8 distinct
+        // bank groups on the reads and, through the swizzle, on the writes too.
+        uint4 codes[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) codes[k] = ok ? src[(k + row) & 7] : make_uint4(0, 0, 0, 0);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {  // 16 codes (piece kk) -> chunks 2kk, 2kk + 1 of the row
+            const int kk = (k + row) & 7;
+            const uint4& u = codes[k];
+#pragma unroll
+            for (int hlf = 0; hlf < 2; ++hlf) {
+                const int ch = 2 * kk + hlf;
+                const uint2 a = widen_e4m3x4<T>(hlf ? u.z : u.x);
+                const uint2 b = widen_e4m3x4<T>(hlf ? u.w : u.y);
+                *reinterpret_cast<uint4*>(dst_row + (ch >> 3) * C::kHalfBytes +
+                                          (((ch & 7) ^ (row & 7)) << 4)) = make_uint4(a.x, a.y, b.x, b.y);
+            }
+        }
+        tc::fence_async_smem();  // the widened tile is read by the MMAs
+        team.sync();
+    };
+
     auto o_accumulate = [&](int cs, const float (&alpha)[H]) -> bool {
         if (!team.wait(ofull0 + 8 * (cs & 1), static_cast<uint32_t>(cs / 2) & 1, p.d_err, abort_flag))
             return false;
@@ -721,34 +760,20 @@ __device__ __forceinline__ void tc_team(const DecodeParams& p, unsigned char* sm
         if (!team.wait(fullV0 + 8 * st, static_cast<uint32_t>(c / C::kStages) & 1, p.d_err, abort_flag)) break;
         const uint32_t flags = meta[st].flags;
         if (flags & kStageEnd) {
-            if (kFp8 && tid == 0) mbar_arrive(conv0 + 8 * st);  // the MMA warp reads the end there
+            // the MMA warp reads the end after conv (unless team 0 already passed it)
+            if (kFp8 && team_id == 0 && kconv_next == c && tid == 0) mbar_arrive(conv0 + 8 * st);
             break;
         }
         if constexpr (kFp8) {
-            if (team_id == 0 &&  // (team 1 widens V, which fullV already covers)
-                !team.wait(fullK0 + 8 * st, static_cast<uint32_t>(c / C::kStages) & 1, p.d_err, abort_flag))
-                break;
-            const int nv = meta[st].nvalid;
-            const uint32_t grp = meta[st].groups;
-            const bool ok = row < nv && ((grp >> (row >> 4)) & 1u);
-            unsigned char* tile = sm + C::kRingOff + st * C::kStageBytes + team_id * C::kTileBytes;
-            uint4 codes[8];
-            const uint4* src = reinterpret_cast<const uint4*>(tile + C::kHalfBytes + row * 128);
-#pragma unroll
-            for (int k = 0; k < 8; ++k) codes[k] = ok ? src[k] : make_uint4(0, 0, 0, 0);
-            unsigned char* dst_row = tile + (row >> 3) * 1024 + (row & 7) * 128;
-#pragma unroll
-            for (int ch = 0; ch < 16; ++ch) {  // 8 codes -> one 16-byte chunk of the row
-                const uint4& u = codes[ch >> 1];
-                const uint32_t a = (ch & 1) ? u.z : u.x, b = (ch & 1) ? u.w : u.y;
-                *reinterpret_cast<uint4*>(dst_row + (ch >> 3) * C::kHalfBytes +
-                                          (((ch & 7) ^ (row & 7)) << 4)) =
-                    make_uint4(widen_e4m3x2<T>(a), widen_e4m3x2<T>(a >> 16), widen_e4m3x2<T>(b),
-                               widen_e4m3x2<T>(b >> 16));
+            if (team_id == 0 && kconv_next == c) {  // only the first stage: later ones early
+                if (!team.wait(fullK0 + 8 * st, static_cast<uint32_t>(c / C::kStages) & 1, p.d_err,
+                               abort_flag))
+                    break;
+                widen(st);
+                if (tid == 0) mbar_arrive(conv0 + 8 * st);
+                kconv_next = c + 1;
             }
-            tc::fence_async_smem();  // the widened tiles are read by the MMAs
-            team.sync();
-            if (tid == 0) mbar_arrive(conv0 + 8 * st);
+            if (team_id == 1) widen(st);  // V: MMA2 waits for this team's p_full
         }
         const int item_seq = static_cast<int>(meta[st].item_seq);
         const int nvalid = meta[st].nvalid;
@@ -843,6 +868,18 @@ __device__ __forceinline__ void tc_team(const DecodeParams& p, unsigned char* sm
         team.sync();  // also: the team has read its red entries before they are rewritten
         if (tid == 0) mbar_arrive(pfull0 + 8 * (c & 1));
 
+        // ---- E4M3, team 0: widen the next stage's K now, so that its MMA1 runs
+        // beside this stage's MMA2 and O-accumulates (an end marker is passed on)
+        if (kFp8 && team_id == 0) {
+            const int c1 = c + 1, st1 = c1 % C::kStages;
+            if (!team.wait(fullK0 + 8 * st1, static_cast<uint32_t>(c1 / C::kStages) & 1, p.d_err,
+                           abort_flag))
+                break;
+            if (!(meta[st1].flags & kStageEnd)) widen(st1);
+            if (tid == 0) mbar_arrive(conv0 + 8 * st1);
+            kconv_next = c1 + 1;
+        }
+
         // ---- O-accumulates: the deferred previous stage, then (at an item end) this one
         if (deferred >= 0) {
             if (!o_accumulate(deferred, alpha_prev)) break;
@@ -902,10 +939,8 @@ __global__ void __launch_bounds__(TcTile<T>::kThreads, 1)
     if (threadIdx.x == 0) {
         for (int i = 0; i < C::kNumBars; ++i) {
             // qempty, q_ready and p_full are signalled once by each of the two teams
-            // (and so is conv, E4M3 only: K by team 0, V by team 1)
             const bool two = (i >= 2 * C::kStages + C::kQSlots && i <= TcBars<T>::kQReady) ||
-                             i == TcBars<T>::kPFull || i == TcBars<T>::kPFull + 1 ||
-                             i >= C::kConvBar;
+                             i == TcBars<T>::kPFull || i == TcBars<T>::kPFull + 1;
             mbar_init(smem_addr(bars + i), two ? 2 : 1);
         }
         *reinterpret_cast<volatile int*>(sm + C::kMiscOff + 4) = 0;

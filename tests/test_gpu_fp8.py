@@ -176,3 +176,44 @@ def test_fp8_tensor_core_default_partition():
     # grouped E4M3 heads default to the tensor-core partition length
     assert pa.decode_partition_tokens(32, 4, 128, 256, 16, "e4m3") == 2048
     assert pa.decode_partition_tokens(32, 32, 128, 256, 16, "e4m3") == 512
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_fp8_tensor_core_widening_covers_every_code(dtype):
+    """One cached token per sequence: the output row is that token's V row,
+    code value x V scale.  Two sequences hold every finite E4M3 code (NaN codes
+    0x7f / 0xff replaced by their neighbours) across their 128 columns, so a
+    wrong bit placement, a lost sign or subnormal codes flushed to zero in the
+    widening show up (the scale 1/8 keeps every value exact in q's type)."""
+    tdt = {"f16": torch.float16, "bf16": torch.bfloat16}[dtype]
+    NB, Hkv, Hq, B, D = 4, 1, 4, 16, 128
+    codes = np.arange(256, dtype=np.uint8)
+    codes[0x7F], codes[0xFF] = 0x7E, 0xFE
+    kc = torch.zeros((NB, Hkv, B, D), dtype=torch.uint8)
+    vc = torch.zeros((NB, Hkv, B, D), dtype=torch.uint8)
+    vc[0, 0, 0] = torch.from_numpy(codes[:128].copy())
+    vc[1, 0, 0] = torch.from_numpy(codes[128:].copy())
+    vc[:2, 0, 1:] = 0x7E   # tokens past the context: must not leak into the output
+    scales = torch.full((NB, Hkv), 0.125, dtype=torch.float32)
+    tables = torch.tensor([[0], [1]], dtype=torch.int32)
+    ctx = torch.tensor([1, 1], dtype=torch.int32)
+    q = torch.randn((2, Hq, D), generator=torch.Generator().manual_seed(570)).to(tdt)
+    dev = {k: v.cuda() for k, v in dict(q=q, kc=kc, vc=vc, s=scales, t=tables, c=ctx).items()}
+    out = torch.full_like(dev["q"], float("nan"))
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    assert pa.decode_partition_tokens(Hq, Hkv, D, 1, B, "e4m3") % 128 == 0  # tensor-core path
+    pa.decode_fp8(out, dev["q"], dev["kc"], dev["vc"], dev["s"], dev["s"], dev["t"], dev["c"],
+                  0.088, d_err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    want = oracle.e4m3_to_f64(codes) * 0.125
+    got = out.double().cpu().numpy()
+    for s in range(2):
+        ref = want[128 * s:128 * (s + 1)]
+        for h in range(Hq):
+            row = got[s, h]
+            assert ((row == 0) == (ref == 0)).all(), (s, h)
+            assert (np.signbit(row[ref != 0]) == np.signbit(ref[ref != 0])).all(), (s, h)
+            nz = ref != 0
+            rel = np.abs(row[nz] - ref[nz]) / np.abs(ref[nz])
+            assert rel.max() <= 2.0 ** -8, (s, h, float(rel.max()))
