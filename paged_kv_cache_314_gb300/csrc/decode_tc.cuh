@@ -80,16 +80,20 @@ struct TcTile {
     static constexpr int kEmptyVBar = kFullVBar + kStages;
     static constexpr int kVPlanBar = kEmptyVBar + kStages;
     static constexpr int kKPlanBar = kVPlanBar + kStages;
-    // E4M3 caches: a stage's K, widened to 16 bits in place by team 0, is ready for
-    // MMA1 (its V, widened by team 1, is covered by that team's p_full)
+    // E4M3 caches: a stage's K (conv) and V (convV), widened to 16 bits in place by
+    // the converter warps, are ready for MMA1 and MMA2
     static constexpr int kConvBar = kKPlanBar + kStages;
-    static constexpr int kNumBars = kConvBar + kStages;
-    static constexpr int kMiscOff = kBarOff + kNumBars * 8;       // tmem base, abort, team flags
+    static constexpr int kConvVBar = kConvBar + kStages;
+    static constexpr int kNumBars = kConvVBar + kStages;
+    static constexpr int kMiscOff = kBarOff + kNumBars * 8;  // tmem base, abort, team and converter flags
     static constexpr int kSmemBytes = kMiscOff + 32 + 1024;       // + alignment slack
     // producer, MMA, two teams of 4 warps, three copy warps: the 32 TMA boxes of a
     // stage are issued by four warps (the producer and warps 10-12, 8 boxes each),
     // since one warp's TMA issue rate would bound the stage rate
     static constexpr int kThreads = 416;
+    // E4M3 caches: the producer and warp 10 issue the stage's 16 boxes (warps 11
+    // and 12 have none), and warps 11-14 widen the codes
+    static constexpr int kThreadsFp8 = 480;
     static constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
     static_assert(kBf16 || std::is_same<T, __half>::value, "16-bit operands only");
     static constexpr uint32_t kIdescS = tc::instr_desc_f16(kBf16, 128, kN, false, false);
@@ -518,6 +522,7 @@ __device__ __forceinline__ void tc_mma(const DecodeParams& p, unsigned char* sm,
     const uint32_t fullK0 = smem_addr(bars + (kFp8 ? C::kConvBar : 0));
     const uint32_t emptyK0 = smem_addr(bars + C::kStages);
     const uint32_t emptyV0 = smem_addr(bars + C::kEmptyVBar);
+    const uint32_t convV0 = smem_addr(bars + C::kConvVBar);  // E4M3: V widened
     const uint32_t qready = smem_addr(bars + Bi::kQReady);
     const uint32_t sfull0 = smem_addr(bars + Bi::kSFull), pfull0 = smem_addr(bars + Bi::kPFull);
     const uint32_t ofull0 = smem_addr(bars + Bi::kOFull), drain = smem_addr(bars + Bi::kDrain);
@@ -571,7 +576,9 @@ __device__ __forceinline__ void tc_mma(const DecodeParams& p, unsigned char* sm,
             fail();
             break;
         }
-        if (!mbar_wait_warp(pfull0 + 8 * (c & 1), static_cast<uint32_t>(c / 2) & 1)) {
+        if (!mbar_wait_warp(pfull0 + 8 * (c & 1), static_cast<uint32_t>(c / 2) & 1) ||
+            (kFp8 && !mbar_wait_warp(convV0 + 8 * (c % C::kStages),
+                                     static_cast<uint32_t>(c / C::kStages) & 1))) {
             fail();
             break;
         }
@@ -658,15 +665,10 @@ __device__ __forceinline__ float warp_reduce_scatter(const float (&v)[N], int la
 // own O-accumulate and the output rows of the team's heads.  Team 0 also
 // zeroes the V rows of invalid tokens.  Each team signals p_full, q_ready and
 // qempty once (those barriers count two arrivals).
-// E4M3 caches (kFp8): team 1 widens the stage's V tile at the start of each
-// stage, team 0 the next stage's K tile once it has posted this stage's P (the
-// first stage's at its start), in place, one token row per thread: the row's 128 codes
-// (landed row-major in the tile's upper half), exact in T, stored in the
-// 128-byte-swizzled layout the MMAs read (rows of invalid tokens become zero).
-// A row's second 64 columns land in the same 128 bytes its codes occupied, so
-// each thread only overwrites what it has read.  The scales stay in fp32: the
-// K scale of a token's block multiplies its logits, the V scale its softmax
-// weight before that is rounded to T for the P.V product.
+// E4M3 caches (kFp8): the tiles hold the codes widened exactly to T (by the
+// converter warps); the scales stay in fp32: the K scale of a token's block
+// multiplies its logits, the V scale its softmax weight before that is rounded
+// to T for the P.V product.
 template <typename T, int G, bool kMulti, bool kFp8>
 __device__ __forceinline__ void tc_team(const DecodeParams& p, unsigned char* sm, uint32_t tmem,
                                         int team_id) {
@@ -681,7 +683,6 @@ __device__ __forceinline__ void tc_team(const DecodeParams& p, unsigned char* sm
     const int h0 = team_id * H;
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::kBarOff);
     const uint32_t fullV0 = smem_addr(bars + C::kFullVBar);  // V landed (and the stage's meta)
-    const uint32_t fullK0 = smem_addr(bars), conv0 = smem_addr(bars + C::kConvBar);
     const uint32_t qfull0 = smem_addr(bars + 2 * C::kStages);
     const uint32_t qempty0 = smem_addr(bars + 2 * C::kStages + C::kQSlots);
     const uint32_t qready = smem_addr(bars + Bi::kQReady);
@@ -710,39 +711,6 @@ __device__ __forceinline__ void tc_team(const DecodeParams& p, unsigned char* sm
 #pragma unroll
     for (int h = 0; h < H; ++h) qtok[h] = kMulti ? (h0 + h) / g : 0;
 
-    // E4M3: widen this team's tile of ring slot sl (team 0: K, team 1: V).
-    int kconv_next = 0;  // team 0: first stage whose K has not been widened
-    auto widen = [&](int sl) {
-        const int nv = meta[sl].nvalid;
-        const uint32_t grp = meta[sl].groups;
-        const bool ok = row < nv && ((grp >> (row >> 4)) & 1u);
-        unsigned char* tile = sm + C::kRingOff + sl * C::kStageBytes + team_id * C::kTileBytes;
-        const uint4* src = reinterpret_cast<const uint4*>(tile + C::kHalfBytes + row * 128);
-        unsigned char* dst_row = tile + (row >> 3) * 1024 + (row & 7) * 128;
-        // All 16-byte pieces of the row are read before any is written: the row's
-        // second 64 columns overwrite its codes.  Each thread starts at piece
-        // (row & 7), so the 8 rows of a shared-memory wavefront touch 8 distinct
-        // bank groups on the reads and, through the swizzle, on the writes too.
-        uint4 codes[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) codes[k] = ok ? src[(k + row) & 7] : make_uint4(0, 0, 0, 0);
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {  // 16 codes (piece kk) -> chunks 2kk, 2kk + 1 of the row
-            const int kk = (k + row) & 7;
-            const uint4& u = codes[k];
-#pragma unroll
-            for (int hlf = 0; hlf < 2; ++hlf) {
-                const int ch = 2 * kk + hlf;
-                const uint2 a = widen_e4m3x4<T>(hlf ? u.z : u.x);
-                const uint2 b = widen_e4m3x4<T>(hlf ? u.w : u.y);
-                *reinterpret_cast<uint4*>(dst_row + (ch >> 3) * C::kHalfBytes +
-                                          (((ch & 7) ^ (row & 7)) << 4)) = make_uint4(a.x, a.y, b.x, b.y);
-            }
-        }
-        tc::fence_async_smem();  // the widened tile is read by the MMAs
-        team.sync();
-    };
-
     auto o_accumulate = [&](int cs, const float (&alpha)[H]) -> bool {
         if (!team.wait(ofull0 + 8 * (cs & 1), static_cast<uint32_t>(cs / 2) & 1, p.d_err, abort_flag))
             return false;
@@ -759,22 +727,7 @@ __device__ __forceinline__ void tc_team(const DecodeParams& p, unsigned char* sm
         const int st = c % C::kStages;
         if (!team.wait(fullV0 + 8 * st, static_cast<uint32_t>(c / C::kStages) & 1, p.d_err, abort_flag)) break;
         const uint32_t flags = meta[st].flags;
-        if (flags & kStageEnd) {
-            // the MMA warp reads the end after conv (unless team 0 already passed it)
-            if (kFp8 && team_id == 0 && kconv_next == c && tid == 0) mbar_arrive(conv0 + 8 * st);
-            break;
-        }
-        if constexpr (kFp8) {
-            if (team_id == 0 && kconv_next == c) {  // only the first stage: later ones early
-                if (!team.wait(fullK0 + 8 * st, static_cast<uint32_t>(c / C::kStages) & 1, p.d_err,
-                               abort_flag))
-                    break;
-                widen(st);
-                if (tid == 0) mbar_arrive(conv0 + 8 * st);
-                kconv_next = c + 1;
-            }
-            if (team_id == 1) widen(st);  // V: MMA2 waits for this team's p_full
-        }
+        if (flags & kStageEnd) break;
         const int item_seq = static_cast<int>(meta[st].item_seq);
         const int nvalid = meta[st].nvalid;
         const uint32_t groups = meta[st].groups;
@@ -868,17 +821,6 @@ __device__ __forceinline__ void tc_team(const DecodeParams& p, unsigned char* sm
         team.sync();  // also: the team has read its red entries before they are rewritten
         if (tid == 0) mbar_arrive(pfull0 + 8 * (c & 1));
 
-        // ---- E4M3, team 0: widen the next stage's K now, so that its MMA1 runs
-        // beside this stage's MMA2 and O-accumulates (an end marker is passed on)
-        if (kFp8 && team_id == 0) {
-            const int c1 = c + 1, st1 = c1 % C::kStages;
-            if (!team.wait(fullK0 + 8 * st1, static_cast<uint32_t>(c1 / C::kStages) & 1, p.d_err,
-                           abort_flag))
-                break;
-            if (!(meta[st1].flags & kStageEnd)) widen(st1);
-            if (tid == 0) mbar_arrive(conv0 + 8 * st1);
-            kconv_next = c1 + 1;
-        }
 
         // ---- O-accumulates: the deferred previous stage, then (at an item end) this one
         if (deferred >= 0) {
@@ -923,8 +865,72 @@ __device__ __forceinline__ void tc_team(const DecodeParams& p, unsigned char* sm
     tc::fence_before_sync();
 }
 
+// E4M3 caches: the converter warps (4, one token row per thread) widen each
+// stage's K tile, then its V tile, in place and in ring order, as they land:
+// a row's 128 codes (landed row-major in the tile's upper half), exact in T,
+// are stored in the 128-byte-swizzled layout the MMAs read (rows of invalid
+// tokens become zero).  A row's second 64 columns land in the same 128 bytes
+// its codes occupied, so each thread only overwrites what it has read.  They
+// run ahead of the MMA warp and the teams by up to the ring's depth.
+template <typename T>
+__device__ __forceinline__ void tc_convert(const DecodeParams& p, unsigned char* sm, int row) {
+    using C = TcTile<T>;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::kBarOff);
+    const uint32_t fullK0 = smem_addr(bars), fullV0 = smem_addr(bars + C::kFullVBar);
+    const uint32_t conv0 = smem_addr(bars + C::kConvBar), convV0 = smem_addr(bars + C::kConvVBar);
+    const TcStageMeta* meta = reinterpret_cast<const TcStageMeta*>(sm + C::kMetaOff);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + C::kMiscOff + 4);
+    TeamSync grp{reinterpret_cast<volatile int*>(sm + C::kMiscOff + 24), row, 3};
+
+    auto widen = [&](int sl, int which) {  // which: 0 = K, 1 = V
+        const int nv = meta[sl].nvalid;
+        const uint32_t groups = meta[sl].groups;
+        const bool ok = row < nv && ((groups >> (row >> 4)) & 1u);
+        unsigned char* tile = sm + C::kRingOff + sl * C::kStageBytes + which * C::kTileBytes;
+        const uint4* src = reinterpret_cast<const uint4*>(tile + C::kHalfBytes + row * 128);
+        unsigned char* dst_row = tile + (row >> 3) * 1024 + (row & 7) * 128;
+        // All 16-byte pieces of the row are read before any is written: the row's
+        // second 64 columns overwrite its codes.  Each thread starts at piece
+        // (row & 7), so the 8 rows of a shared-memory wavefront touch 8 distinct
+        // bank groups on the reads and, through the swizzle, on the writes too.
+        uint4 codes[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) codes[k] = ok ? src[(k + row) & 7] : make_uint4(0, 0, 0, 0);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {  // 16 codes (piece kk) -> chunks 2kk, 2kk + 1 of the row
+            const int kk = (k + row) & 7;
+            const uint4& u = codes[k];
+#pragma unroll
+            for (int hlf = 0; hlf < 2; ++hlf) {
+                const int ch = 2 * kk + hlf;
+                const uint2 a = widen_e4m3x4<T>(hlf ? u.z : u.x);
+                const uint2 b = widen_e4m3x4<T>(hlf ? u.w : u.y);
+                *reinterpret_cast<uint4*>(dst_row + (ch >> 3) * C::kHalfBytes +
+                                          (((ch & 7) ^ (row & 7)) << 4)) = make_uint4(a.x, a.y, b.x, b.y);
+            }
+        }
+        tc::fence_async_smem();  // the widened tile is read by the MMAs
+        grp.sync();
+    };
+
+    for (int c = 0;; ++c) {
+        const int st = c % C::kStages;
+        const uint32_t par = static_cast<uint32_t>(c / C::kStages) & 1;
+        if (!grp.wait(fullK0 + 8 * st, par, p.d_err, abort_flag)) break;
+        if (meta[st].flags & kStageEnd) {  // passed on: the MMA warp reads the end after conv
+            if (row == 0) mbar_arrive(conv0 + 8 * st);
+            break;
+        }
+        widen(st, 0);
+        if (row == 0) mbar_arrive(conv0 + 8 * st);
+        if (!grp.wait(fullV0 + 8 * st, par, p.d_err, abort_flag)) break;
+        widen(st, 1);
+        if (row == 0) mbar_arrive(convV0 + 8 * st);
+    }
+}
+
 template <typename T, int G, bool kMulti, bool kFp8>
-__global__ void __launch_bounds__(TcTile<T>::kThreads, 1)
+__global__ void __launch_bounds__(kFp8 ? TcTile<T>::kThreadsFp8 : TcTile<T>::kThreads, 1)
     decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap mapK,
                      const __grid_constant__ CUtensorMap mapV) {
     using C = TcTile<T>;
@@ -966,6 +972,8 @@ __global__ void __launch_bounds__(TcTile<T>::kThreads, 1)
         tc_team<T, G, kMulti, kFp8>(p, sm, tmem, (warp - 2) >> 2);
     else if (warp == 10)
         tc_copy<T, kFp8>(p, &mapV, sm, base, true, 0);
+    else if (kFp8)
+        tc_convert<T>(p, sm, threadIdx.x - 352);
     else if (warp == 11)
         tc_copy<T, kFp8>(p, &mapK, sm, base, false, 1);
     else
@@ -1011,7 +1019,8 @@ inline pa_status launch_decode_tc_typed(const DecodeParams& p, const CUtensorMap
     if (work > 0x7fffffffLL) return PA_ERR_UNSUPPORTED;
     long long grid = sms;
     if (grid > work) grid = work;
-    kernel<<<static_cast<unsigned>(grid), C::kThreads, C::kSmemBytes, stream>>>(p, mapK, mapV);
+    kernel<<<static_cast<unsigned>(grid), kFp8 ? C::kThreadsFp8 : C::kThreads, C::kSmemBytes, stream>>>(
+        p, mapK, mapV);
     if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
     if (p.max_parts > 1) {
         decode_reduce_kernel<T, C::D><<<p.num_query_tokens * p.num_q_heads, 128, 0, stream>>>(p);
