@@ -77,17 +77,20 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     return fn;
 }
 
-// The K or V pool as a [rows = NB*Hkv*B][128] matrix of 16-bit elements, read
-// in [16 rows x 64 columns] boxes with 128-byte swizzle.
+// The K or V pool (rows = NB*Hkv*B token rows of 128 16-bit elements) as a
+// 4-D tensor {64 columns, 8 rows, 2 halves, rows / 8} with strides {256 B,
+// 128 B, 2048 B}: one [64 x 8 x 2 x 2] box with 128-byte swizzle carries a
+// 16-token group as two 8-row blocks of [half][row][64 columns], the layout
+// the tensor-core kernel's operand descriptors read.
 bool make_pool_map(CUtensorMap* map, const void* pool, long long rows, pa_dtype dtype) {
     PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
-    if (encode == nullptr) return false;
-    const cuuint64_t dims[2] = {128, static_cast<cuuint64_t>(rows)};
-    const cuuint64_t strides[1] = {128 * 2};
-    const cuuint32_t box[2] = {64, 16};
-    const cuuint32_t elem_strides[2] = {1, 1};
+    if (encode == nullptr || rows % 8 != 0) return false;
+    const cuuint64_t dims[4] = {64, 8, 2, static_cast<cuuint64_t>(rows / 8)};
+    const cuuint64_t strides[3] = {128 * 2, 64 * 2, 8 * 128 * 2};
+    const cuuint32_t box[4] = {64, 8, 2, 2};
+    const cuuint32_t elem_strides[4] = {1, 1, 1, 1};
     return encode(map, dtype == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
-                  2, const_cast<void*>(pool), dims, strides, box, elem_strides,
+                  4, const_cast<void*>(pool), dims, strides, box, elem_strides,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }

@@ -328,14 +328,21 @@ __device__ __forceinline__ void tc_produce(const DecodeParams& p, const CUtensor
             // K boxes first (their bytes complete on fullK before its arrival is posted):
             // the second 64-column half goes to warp 11 through the plan
             // (E4M3: one box holds a block's whole rows; the second half has none)
+            // (16-bit: one 4 KB box per group holds both halves, see tc_copy; the
+            // producer issues groups 0-3 and warp 11 groups 4-7, through entry 2g+1)
             if ((lane & 1) == 0)
-                plan[st * C::kPlanInts + (lane >> 1)] = (mine && !(kFp8 && h == 1)) ? row : -1;
+                plan[st * C::kPlanInts + (lane >> 1)] =
+                    (mine && (kFp8 ? h == 0 : (h == 1 && r >= 4))) ? row : -1;
             if (lane == 0) plan[st * C::kPlanInts + C::kPlanStop] = 0;  // not the last stage
             __syncwarp();
             if (lane == 0) mbar_arrive(kplan0 + 8 * st);
-            if (mine && (lane & 3) == 0)
-                tc::tma_load_2d(stage_base + (kFp8 ? C::kHalfBytes : 0) + r * 2048, mapK, 0, row, fullK,
-                                policy);
+            if constexpr (kFp8) {
+                if (mine && (lane & 3) == 0)
+                    tc::tma_load_2d(stage_base + C::kHalfBytes + r * 2048, mapK, 0, row, fullK, policy);
+            } else {
+                if (mine && (lane & 3) == 0 && r < 4)
+                    tc::tma_load_4d(stage_base + r * 4096, mapK, 0, 0, 0, row >> 3, fullK, policy);
+            }
             __syncwarp();
             // the V half is free once MMA2 of the slot's previous stage completed
             if (cc >= C::kStages && !mbar_wait_warp(emptyV0 + 8 * st, reuse)) {
@@ -372,9 +379,11 @@ __device__ __forceinline__ void tc_produce(const DecodeParams& p, const CUtensor
                 mbar_arrive_expect_tx(fullK, half_bytes);
                 mbar_arrive_expect_tx(fullV, half_bytes);
             }
-            // the V boxes: their rows go to warps 10 and 12 (lane 4g+2h+1 -> entry 16+2g+h)
+            // the V boxes: their rows go to warps 10 and 12 (lane 4g+2h+1 -> entry 16+2g+h;
+            // 16-bit: warp 10 takes groups 0-3, warp 12 groups 4-7, one box each)
             if ((lane & 1) != 0)
-                plan[st * C::kPlanInts + 16 + (lane >> 1)] = (mine && !(kFp8 && h == 1)) ? row : -1;
+                plan[st * C::kPlanInts + 16 + (lane >> 1)] =
+                    (mine && (kFp8 ? h == 0 : h == (r >= 4 ? 1 : 0))) ? row : -1;
             __syncwarp();
             if (lane == 0) mbar_arrive(vplan0 + 8 * st);
         }
@@ -445,10 +454,13 @@ __device__ __forceinline__ void tc_copy(const DecodeParams& p, const CUtensorMap
         }
         if (plan[st * C::kPlanInts + C::kPlanStop] != 0) break;
         const int row = lane < 8 ? plan[st * C::kPlanInts + (is_v ? 16 : 0) + 2 * lane + half] : -1;
-        if (row >= 0)  // (E4M3: whole 128-byte rows into the tile's upper half)
-            tc::tma_load_2d(base + C::kRingOff + st * C::kStageBytes + (is_v ? C::kTileBytes : 0) +
-                                (kFp8 ? 1 : half) * C::kHalfBytes + lane * 2048,
-                            map, kFp8 ? 0 : 64 * half, row, full0 + 8 * st, policy);
+        const uint32_t tile = base + C::kRingOff + st * C::kStageBytes + (is_v ? C::kTileBytes : 0);
+        if (row >= 0) {
+            if constexpr (kFp8)  // whole 128-byte rows of codes into the tile's upper half
+                tc::tma_load_2d(tile + C::kHalfBytes + lane * 2048, map, 0, row, full0 + 8 * st, policy);
+            else  // group `lane`: both 64-column halves of its 16 rows
+                tc::tma_load_4d(tile + lane * 4096, map, 0, 0, 0, row >> 3, full0 + 8 * st, policy);
+        }
         __syncwarp();
     }
 }
@@ -485,23 +497,30 @@ struct TcBars {
     static constexpr int kDrain = kOFull + 2;
 };
 
-template <typename T>
+// Tile layouts.  16-bit K/V: 8-token row blocks of 2 KB, each [2 halves of 64
+// columns][8 rows][128 B] (the 4-D TMA box of a 16-token group is two such
+// blocks), so one 64-column half of consecutive 8-row groups lies 2048 B
+// apart and the other half 1024 B after it.  E4M3 (kFp8): [2 halves][128
+// rows][128 B], 8-row groups 1024 B apart, the halves 16 KB apart.
+template <typename T, bool kFp8>
 __device__ __forceinline__ void tc_mma1(uint32_t sK, uint32_t qop, uint32_t tS) {
     using C = TcTile<T>;
+    constexpr uint32_t kHalfStep = kFp8 ? C::kHalfBytes : 1024, kGroupStep = kFp8 ? 1024 : 2048;
 #pragma unroll
     for (int j = 0; j < 8; ++j) {  // 16 head dimensions per step
-        const uint64_t a = tc::smem_desc_sw128(sK + (j / 4) * C::kHalfBytes + (j % 4) * 32, 16, 1024);
+        const uint64_t a = tc::smem_desc_sw128(sK + (j / 4) * kHalfStep + (j % 4) * 32, 16, kGroupStep);
         const uint64_t b = tc::smem_desc_sw128(qop + (j / 4) * 2048 + (j % 4) * 32, 16, 1024);
         tc::mma_f16_warp(tS, a, b, C::kIdescS, j > 0);
     }
 }
 
-template <typename T>
+template <typename T, bool kFp8>
 __device__ __forceinline__ void tc_mma2(uint32_t sV, uint32_t pop, uint32_t tO) {
     using C = TcTile<T>;
+    constexpr uint32_t kHalfStep = kFp8 ? C::kHalfBytes : 1024, kGroupStep = kFp8 ? 1024 : 2048;
 #pragma unroll
     for (int j = 0; j < 8; ++j) {  // 16 tokens per step
-        const uint64_t a = tc::smem_desc_sw128(sV + j * 2048, C::kHalfBytes, 1024);
+        const uint64_t a = tc::smem_desc_sw128(sV + j * 2 * kGroupStep, kHalfStep, kGroupStep);
         const uint64_t b = tc::smem_desc_sw128(pop + (j / 4) * 2048 + (j % 4) * 32, 16, 1024);
         tc::mma_f16_warp(tO, a, b, C::kIdescO, j > 0);
     }
@@ -549,7 +568,7 @@ __device__ __forceinline__ void tc_mma(const DecodeParams& p, unsigned char* sm,
         }
         tc::fence_after_sync();
         // the whole warp runs the issue code, one elected lane (lane 0) issues
-        tc_mma1<T>(stage_k(c), qop, tmem + (c & 1) * C::kN);
+        tc_mma1<T, kFp8>(stage_k(c), qop, tmem + (c & 1) * C::kN);
         tc::mma_commit_warp(sfull0 + 8 * (c & 1));
         tc::mma_commit_warp(emptyK0 + 8 * st);  // K_c is free once MMA1 completed
         __syncwarp();
@@ -583,7 +602,7 @@ __device__ __forceinline__ void tc_mma(const DecodeParams& p, unsigned char* sm,
             break;
         }
         tc::fence_after_sync();
-        tc_mma2<T>(stage_k(c) + C::kTileBytes, pop0 + (c & 1) * C::kOpBytes,
+        tc_mma2<T, kFp8>(stage_k(c) + C::kTileBytes, pop0 + (c & 1) * C::kOpBytes,
                    tmem + 2 * C::kN + (c & 1) * C::kN);
         tc::mma_commit_warp(ofull0 + 8 * (c & 1));
         tc::mma_commit_warp(emptyV0 + 8 * (c % C::kStages));  // V_c is free
@@ -809,12 +828,12 @@ __device__ __forceinline__ void tc_team(const DecodeParams& p, unsigned char* sm
         }
         if (!kFp8 && !valid && team_id == 0) {  // zero this token's V row (both 64-column halves)
             unsigned char* vrow = sm + C::kRingOff + st * C::kStageBytes + C::kTileBytes +
-                                  (row >> 3) * 1024 + (row & 7) * 128;
+                                  (row >> 3) * 2048 + (row & 7) * 128;
 #pragma unroll
             for (int h2 = 0; h2 < 2; ++h2)
 #pragma unroll
                 for (int k = 0; k < 8; ++k)
-                    *reinterpret_cast<uint4*>(vrow + h2 * C::kHalfBytes + k * 16) = make_uint4(0, 0, 0, 0);
+                    *reinterpret_cast<uint4*>(vrow + h2 * 1024 + k * 16) = make_uint4(0, 0, 0, 0);
         }
         tc::fence_async_smem();
         tc::fence_before_sync();
