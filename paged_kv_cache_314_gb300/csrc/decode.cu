@@ -8,6 +8,7 @@
 
 #include "decode_kernels.cuh"
 #include "decode_tc.cuh"
+#include "prefill_tc.cuh"
 
 namespace pa {
 namespace {
@@ -91,6 +92,25 @@ bool make_pool_map(CUtensorMap* map, const void* pool, long long rows, pa_dtype 
     const cuuint32_t elem_strides[4] = {1, 1, 1, 1};
     return encode(map, dtype == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
                   4, const_cast<void*>(pool), dims, strides, box, elem_strides,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// The query rows [tokens][Hq][128] of 16-bit elements as a 3-D tensor
+// {128 columns, Hq heads, tokens}: one [64 x g x 128/g] box with 128-byte
+// swizzle holds one 64-column half of the 128 rows (token-major, then head) of
+// a multi-query item of the 128-row kernel.
+bool make_q_map(CUtensorMap* map, const void* q, int num_tokens, int num_q_heads, int group,
+                pa_dtype dtype) {
+    PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
+    if (encode == nullptr || group <= 0 || 128 % group != 0) return false;
+    const cuuint64_t dims[3] = {128, static_cast<cuuint64_t>(num_q_heads),
+                                static_cast<cuuint64_t>(num_tokens)};
+    const cuuint64_t strides[2] = {128 * 2, static_cast<cuuint64_t>(num_q_heads) * 128 * 2};
+    const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(group), static_cast<cuuint32_t>(128 / group)};
+    const cuuint32_t elem_strides[3] = {1, 1, 1};
+    return encode(map, dtype == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                  3, const_cast<void*>(q), dims, strides, box, elem_strides,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -270,6 +290,22 @@ pa_status run_attention(const AttnCall& a) {
     const bool tc_rows = a.query_start == nullptr
                              ? tc_shape(a.num_q_heads, a.num_kv_heads, a.head_dim, a.dtype)
                              : tc_tokens * group >= 4;
+    // Many query tokens per sequence (chunked prefill): items of 128 query rows
+    // (128/g tokens x g heads), when a sequence's queries fill at least half
+    // such a tile on average.
+    if (tc_ok && a.query_start != nullptr && a.num_seqs > 0 && (group & (group - 1)) == 0) {
+        const long long avg = (static_cast<long long>(a.num_query_tokens) + a.num_seqs - 1) / a.num_seqs;
+        CUtensorMap map_k, map_v, map_q;
+        if (avg * group >= 64 && make_pool_map(&map_k, a.k_cache, pool_rows, a.dtype) &&
+            make_pool_map(&map_v, a.v_cache, pool_rows, a.dtype) &&
+            make_q_map(&map_q, a.q, a.num_query_tokens, a.num_q_heads, group, a.dtype)) {
+            p.head_tiles = a.num_kv_heads;
+            p.tile_heads = group;
+            p.tile_tokens = 128 / group;
+            return a.dtype == PA_BF16 ? launch_prefill_tc_bf16(p, map_k, map_v, map_q, st)
+                                      : launch_prefill_tc_f16(p, map_k, map_v, map_q, st);
+        }
+    }
     if (tc_ok && tc_rows) {
         CUtensorMap map_k, map_v;
         if (make_pool_map(&map_k, a.k_cache, pool_rows, a.dtype) &&

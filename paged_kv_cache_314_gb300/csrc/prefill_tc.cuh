@@ -1,0 +1,762 @@
+// prefill_tc.cuh -- causal multi-query paged attention with 128 query rows per
+// tensor-core tile, for runs of many query tokens per sequence (chunked
+// prefill).
+//
+// PagedAttention (block tables, P4 §5 / §8) applied to the steps beside
+// decode that the pages name as vLLM features, chunked prefill and
+// speculative decoding (P3 §6.5): each new token of a sequence attends to its
+// own prefix of the block table.  The grouped-decode kernel of decode_tc.cuh
+// tiles the query side by at most 16 rows, so a chunk of hundreds of query
+// tokens reads every K/V tile once per 16 rows.  Here a work item is 128 query
+// rows (128/g consecutive query tokens x the g heads of one kv head) against
+// its causal span of the table, one 128-token K/V stage at a time:
+//
+//   S = Q . K^T   (tcgen05.mma, M = 128 rows, N = 128 tokens, fp32 in TMEM)
+//   P = 2^(S * scale * log2 e - m)     one thread per row, from TMEM
+//   O += P . V    (M = 128 rows, N = 128 head dimensions, fp32 in TMEM)
+//
+// with a running row maximum m that is raised only when a stage's maximum
+// exceeds it by more than 2^8 (then O in TMEM and the row sum are rescaled;
+// the weights stay <= 2^8, exact in fp32 and far inside the 16-bit range).
+//
+// Warps: 0 walks the work items and issues the Q and K copies, 1 issues the
+// MMAs (one elected lane) and owns TMEM, 2-5 are the softmax warpgroup
+// (thread = query row, warp w reading TMEM lanes 32*(w%4)..), 6 issues the V
+// copies from a per-stage plan.  Shared memory: a 2-stage K/V ring (the K and
+// V halves of a slot released separately), two Q slots, one P tile.
+#pragma once
+
+#include <stdint.h>
+
+#include <type_traits>
+
+#include "decode_kernels.cuh"
+#include "decode_tc.cuh"  // TeamSync
+#include "tc_ptx.cuh"
+
+namespace pa {
+
+template <typename T>
+struct PfTile {
+    static constexpr int D = 128;
+    static constexpr int kRows = 128;                    // query rows per item (MMA M)
+    static constexpr int kStageTok = 128;                // K/V tokens per stage
+    static constexpr int kStages = 2;
+    static constexpr int kTileBytes = kStageTok * D * 2;  // K or V of a stage: 32 KB
+    static constexpr int kStageBytes = 2 * kTileBytes;
+    static constexpr int kOpBytes = kRows * D * 2;       // Q or P: [2 halves][128 rows][128 B]
+    static constexpr int kHalf = kOpBytes / 2;
+    static constexpr int kRingOff = 0;
+    static constexpr int kQOff = kStages * kStageBytes;  // Q slots [2]
+    static constexpr int kPOff = kQOff + 2 * kOpBytes;
+    static constexpr int kMetaOff = kPOff + kOpBytes;    // stage meta [kStages], 64 B each
+    static constexpr int kPlanOff = kMetaOff + kStages * 64;  // V box rows of a stage [8] + stop word
+    static constexpr int kPlanInts = 12;
+    static constexpr int kPlanStop = 8;
+    static constexpr int kBarOff = kPlanOff + kStages * kPlanInts * 4;
+    // barriers (indices)
+    static constexpr int kFullK = 0, kEmptyK = 2, kFullV = 4, kEmptyV = 6, kVPlan = 8;
+    static constexpr int kQFull = 10, kQEmpty = 12, kSFull = 14, kSFree = 16;
+    static constexpr int kPFull = 18, kPFree = 19, kDrain = 20, kNumBars = 21;
+    static constexpr int kMiscOff = kBarOff + kNumBars * 8;  // tmem base, abort, team flags [2]
+    static constexpr int kSmemBytes = kMiscOff + 32 + 1024;  // + alignment slack
+    static constexpr int kThreads = 224;
+    static constexpr uint32_t kTmemCols = 512;  // S [2] x 128, O 128
+    static constexpr uint32_t kOCol = 256;
+    static constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
+    static_assert(kBf16 || std::is_same<T, __half>::value, "16-bit operands only");
+    static_assert(kSmemBytes <= 232448, "shared memory per CTA");
+    // S = Q.K^T: A = Q (K-major), B = K tile (K-major); O += P.V: A = P (K-major),
+    // B = V tile (N = head dimension contiguous: MN-major)
+    static constexpr uint32_t kIdescS = tc::instr_desc_f16(kBf16, 128, 128, false, false);
+    static constexpr uint32_t kIdescO = tc::instr_desc_f16(kBf16, 128, 128, false, true);
+};
+
+// Written by the producer before the stage's arrivals; the ring protects it
+// until MMA2 of the stage completed, so the softmax warps copy what they need
+// of it before they post the stage's P.
+struct PfStageMeta {
+    uint32_t item_seq;
+    int nvalid;       // tokens of the stage before the item's span end
+    uint32_t groups;  // bit r: 16-token group r was loaded (its block id passed the check)
+    uint32_t flags;   // kStageFirst / kStageLast / kStageEnd
+    int lim_rel;      // tokens of this stage the item's first query token sees
+    int row0;         // the item: q / out row of its first query token
+    int hq0;          // first query head (the g heads of one kv head)
+    int part;         // partition index
+    int nparts;       // 0: context length out of range (zero rows)
+    int ntok;         // query tokens
+    int pad[6];
+};
+static_assert(sizeof(PfStageMeta) == 64, "stage meta slot");
+
+namespace pf {
+
+__device__ __forceinline__ void tma_load_3d(uint32_t dst_smem, const CUtensorMap* map, int c0, int c1,
+                                            int c2, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst_smem),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_load_4d(uint32_t dst_smem, const CUtensorMap* map, int c3,
+                                            uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %2, %2, %3}], [%4];" ::"r"(dst_smem),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(c3), "r"(bar)
+        : "memory");
+}
+
+// 32 consecutive TMEM columns of this thread's lane.  The load and its wait
+// are one asm statement, so no use of the registers can be scheduled before
+// the data has arrived.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
+        "%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+          "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+          "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float* v) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+        "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+        "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+        "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+        "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
+        "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+        "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
+        "r"(__float_as_uint(v[15])), "r"(__float_as_uint(v[16])), "r"(__float_as_uint(v[17])),
+        "r"(__float_as_uint(v[18])), "r"(__float_as_uint(v[19])), "r"(__float_as_uint(v[20])),
+        "r"(__float_as_uint(v[21])), "r"(__float_as_uint(v[22])), "r"(__float_as_uint(v[23])),
+        "r"(__float_as_uint(v[24])), "r"(__float_as_uint(v[25])), "r"(__float_as_uint(v[26])),
+        "r"(__float_as_uint(v[27])), "r"(__float_as_uint(v[28])), "r"(__float_as_uint(v[29])),
+        "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// Two floats rounded to T, packed (lower address first).
+template <typename T>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+    if constexpr (std::is_same<T, __half>::value) {
+        const __half2 h = __floats2half2_rn(lo, hi);
+        return *reinterpret_cast<const uint32_t*>(&h);
+    } else {
+        const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+        return *reinterpret_cast<const uint32_t*>(&h);
+    }
+}
+
+}  // namespace pf
+
+// ---- warp 0: work items, Q and K copies, stage meta, V plan ------------------
+template <typename T>
+__device__ __forceinline__ void pf_produce(const DecodeParams& p, const CUtensorMap* mapK,
+                                           const CUtensorMap* mapQ, unsigned char* sm, uint32_t base) {
+    using C = PfTile<T>;
+    const int lane = threadIdx.x & 31;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::kBarOff);
+    auto bar = [&](int i) { return smem_addr(bars + i); };
+    int* plan = reinterpret_cast<int*>(sm + C::kPlanOff);
+    PfStageMeta* meta = reinterpret_cast<PfStageMeta*>(sm + C::kMetaOff);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + C::kMiscOff + 4);
+    int k_only = -1;  // a stage whose K copies were issued but not its V copies (abort)
+
+    const int S = p.num_seqs, P = p.partition_tokens, B = p.block_size, g = p.group;
+    const int Tq = p.tile_tokens;  // query tokens per item: 128 / g
+    const int max_ctx = p.max_blocks_per_seq * B;
+
+    // Cursor over the sequence-major item numbering: lane l holds sequence
+    // win0 + l and its number of items.
+    int s_cur = 0, base_items = 0, win0 = 0;
+    SeqQueries sq_lane{0, 0, 0, true};
+    int items_lane = 0;
+    auto load_window = [&]() {
+        const int sl = win0 + lane;
+        sq_lane = sl < S ? seq_queries(p, sl) : SeqQueries{0, 0, 0, true};
+        items_lane = sl < S ? seq_items(sq_lane, p, max_ctx) : 0;
+        if (sl < S && !sq_lane.rows_ok(p.num_query_tokens)) report(p.d_err, PA_DERR_CTX_OOB);
+    };
+    load_window();
+    int c = 0, item_seq = 0, q_issued = 0;
+    bool aborted = false, oob = false;
+    int item_id = 0;
+    if (lane == 0) item_id = static_cast<int>(atomicAdd(p.counters, 1u));
+    item_id = __shfl_sync(0xffffffffu, item_id, 0);
+
+    while (!aborted) {
+        bool found = false;
+        while (s_cur < S) {
+            if (s_cur - win0 >= 32) {
+                win0 = s_cur;
+                load_window();
+            }
+            const int sl = win0 + lane;
+            const int cnt = (sl >= s_cur && sl < S) ? items_lane : 0;
+            int incl = cnt;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, incl, off);
+                if (lane >= off) incl += y;
+            }
+            const int total = __shfl_sync(0xffffffffu, incl, 31);
+            if (base_items + total > item_id) {
+                const unsigned hit = __ballot_sync(0xffffffffu, base_items + incl > item_id);
+                const int L = __ffs(hit) - 1;
+                base_items += __shfl_sync(0xffffffffu, incl - cnt, L);
+                s_cur = win0 + L;
+                found = true;
+                break;
+            }
+            base_items += total;
+            s_cur = win0 + 32;
+        }
+        if (!found) break;
+        int next_id = 0;
+        if (lane == 0) next_id = static_cast<int>(atomicAdd(p.counters, 1u));
+
+        const int s = s_cur;
+        SeqQueries sq;
+        sq.ctx = __shfl_sync(0xffffffffu, sq_lane.ctx, s_cur - win0);
+        sq.q0 = __shfl_sync(0xffffffffu, sq_lane.q0, s_cur - win0);
+        sq.q1 = __shfl_sync(0xffffffffu, sq_lane.q1, s_cur - win0);
+        sq.multi = true;
+        const int ctx = sq.ctx;
+        const bool valid = sq.ctx_ok(max_ctx);
+        const int qlen = sq.q1 - sq.q0;
+        const int np = valid ? items_of(ctx, max_ctx, P) : 1;
+        const int ntt = (qlen + Tq - 1) / Tq;
+        const int i_loc = item_id - base_items;
+        if (i_loc < 0 || i_loc >= __shfl_sync(0xffffffffu, items_lane, s_cur - win0)) {
+            // only reachable when query_start is not ascending (item counts can overflow)
+            if (lane == 0) report(p.d_err, PA_DERR_CTX_OOB);
+            break;
+        }
+        const int tile = i_loc / np;  // (kv head, query-token tile)
+        const int part = i_loc - tile * np;
+        const int hk = tile / ntt;
+        const int it = tile - hk * ntt;
+        const int hq0 = hk * g;
+        const int i0 = it * Tq;
+        const int ntok = min(Tq, qlen - i0);
+        const int lim_first = ctx - qlen + i0 + 1;  // tokens the item's first query sees
+        const int lim_last = lim_first + ntok - 1;
+        const int tok_begin = part * P;
+        const int tok_end = valid ? max(tok_begin, min(tok_begin + P, lim_last)) : tok_begin;
+        const int nst = tok_end > tok_begin ? (tok_end - tok_begin + C::kStageTok - 1) / C::kStageTok : 1;
+        if (!valid && lane == 0) report(p.d_err, PA_DERR_CTX_OOB);
+
+        const int qs = item_seq & 1;
+        if (item_seq >= 2 && !mbar_wait_warp(bar(C::kQEmpty + qs), static_cast<uint32_t>((item_seq >> 1) - 1) & 1)) {
+            if (lane == 0) report(p.d_err, PA_DERR_TIMEOUT);
+            *abort_flag = 1;
+            break;
+        }
+        if (lane == 0) {
+            // the item's query rows: [token][head][64 columns] boxes, one per half
+            // (rows past the sequence's queries are loaded too, never stored)
+            const uint32_t qf = bar(C::kQFull + qs);
+            mbar_arrive_expect_tx(qf, C::kOpBytes);
+            for (int h = 0; h < 2; ++h)
+                pf::tma_load_3d(base + C::kQOff + qs * C::kOpBytes + h * C::kHalf, mapQ, 64 * h, hq0,
+                                sq.q0 + i0, qf);
+        }
+        q_issued = item_seq + 1;
+
+        const int32_t* trow = p.block_tables + static_cast<size_t>(s) * p.max_blocks_per_seq;
+        const int blk_end = (tok_end + B - 1) / B;
+        int win = tok_begin / B;
+        int32_t entry = (win + lane < blk_end) ? __ldg(trow + win + lane) : -1;
+
+        for (int i = 0; i < nst; ++i) {
+            const int cc = c + i;
+            const int st = cc & 1;
+            const uint32_t reuse = static_cast<uint32_t>((cc >> 1) - 1) & 1;
+            if (cc >= C::kStages && !mbar_wait_warp(bar(C::kEmptyK + st), reuse)) {
+                if (lane == 0) report(p.d_err, PA_DERR_TIMEOUT);
+                *abort_flag = 1;
+                aborted = true;
+                c = cc;
+                break;
+            }
+            const int t0 = tok_begin + i * C::kStageTok;
+            const int t1 = min(t0 + C::kStageTok, tok_end);
+            if (t1 > t0 && (t1 - 1) / B - win >= 32) {  // window must hold the stage's blocks
+                win = t0 / B;
+                entry = (win + lane < blk_end) ? __ldg(trow + win + lane) : -1;
+            }
+            // lane r < 8: the stage's 16-token group r
+            const int r = lane & 7;
+            const int t = t0 + 16 * r;
+            int row = 0;
+            bool mine = false, bad = false;
+            {
+                const int lb = t < t1 ? t / B : win;
+                const int pb = __shfl_sync(0xffffffffu, entry, lb - win);
+                if (lane < 8 && t < t1) {
+                    if (static_cast<unsigned>(pb) < static_cast<unsigned>(p.num_blocks)) {
+                        row = (pb * p.num_kv_heads + hk) * B + (t - lb * B);
+                        mine = true;
+                    } else {
+                        bad = true;
+                    }
+                }
+            }
+            const uint32_t groups = __ballot_sync(0xffffffffu, mine) & 0xffu;
+            if (__any_sync(0xffffffffu, bad)) oob = true;
+            const uint32_t tile_bytes = static_cast<uint32_t>(__popc(groups)) * 4096u;
+            const uint32_t stage_base = base + C::kRingOff + st * C::kStageBytes;
+            if (mine) pf::tma_load_4d(stage_base + r * 4096, mapK, row >> 3, bar(C::kFullK + st));
+            __syncwarp();
+            // the V half is free once MMA2 of the slot's previous stage completed
+            if (cc >= C::kStages && !mbar_wait_warp(bar(C::kEmptyV + st), reuse)) {
+                if (lane == 0) {
+                    report(p.d_err, PA_DERR_TIMEOUT);
+                    mbar_arrive_expect_tx(bar(C::kFullK + st), tile_bytes);  // so the drain sees K land
+                }
+                *abort_flag = 1;
+                aborted = true;
+                k_only = cc;
+                c = cc + 1;
+                break;
+            }
+            if (lane < 8) plan[st * C::kPlanInts + lane] = mine ? row : -1;
+            if (lane == 0) {
+                uint32_t flags = 0;
+                if (i == 0) flags |= kStageFirst;
+                if (i == nst - 1) flags |= kStageLast;
+                meta[st].item_seq = static_cast<uint32_t>(item_seq);
+                meta[st].nvalid = max(0, t1 - t0);
+                meta[st].groups = groups;
+                meta[st].flags = flags;
+                meta[st].lim_rel = max(-C::kRows, min(C::kStageTok, lim_first - t0));
+                meta[st].row0 = sq.q0 + i0;
+                meta[st].hq0 = hq0;
+                meta[st].part = part;
+                meta[st].nparts = valid ? np : 0;
+                meta[st].ntok = ntok;
+                plan[st * C::kPlanInts + C::kPlanStop] = 0;
+            }
+            __syncwarp();
+            if (lane == 0) {
+                // meta is written before either arrival: the MMA warp reads it after
+                // fullK, the softmax warps after fullV
+                mbar_arrive_expect_tx(bar(C::kFullK + st), tile_bytes);
+                mbar_arrive_expect_tx(bar(C::kFullV + st), tile_bytes);
+                mbar_arrive(bar(C::kVPlan + st));
+            }
+        }
+        if (aborted) break;
+        c += nst;
+        ++item_seq;
+        item_id = __shfl_sync(0xffffffffu, next_id, 0);
+        if (*abort_flag) aborted = true;
+    }
+    if (!aborted) {  // one end marker: the other warps read stages in order
+        const int st = c & 1;
+        const uint32_t reuse = static_cast<uint32_t>((c >> 1) - 1) & 1;
+        if (c >= C::kStages && (!mbar_wait_warp(bar(C::kEmptyK + st), reuse) ||
+                                !mbar_wait_warp(bar(C::kEmptyV + st), reuse))) {
+            if (lane == 0) report(p.d_err, PA_DERR_TIMEOUT);
+            *abort_flag = 1;
+        } else {
+            if (lane == 0) {
+                meta[st].flags = kStageEnd;
+                meta[st].nvalid = 0;
+                meta[st].groups = 0;
+                plan[st * C::kPlanInts + C::kPlanStop] = 1;  // the copy warp leaves
+                mbar_arrive(bar(C::kFullK + st));
+                mbar_arrive(bar(C::kFullV + st));
+                mbar_arrive(bar(C::kVPlan + st));
+            }
+            ++c;
+        }
+    }
+    if (lane == 0) {
+        if (oob) report(p.d_err, PA_DERR_BLOCK_OOB);
+        // every copy issued here has landed before the CTA may exit
+        for (int cc = max(0, c - C::kStages); cc < c; ++cc) {
+            const uint32_t par = static_cast<uint32_t>(cc >> 1) & 1;
+            if (!mbar_wait(bar(C::kFullK + (cc & 1)), par)) report(p.d_err, PA_DERR_TIMEOUT);
+            if (cc != k_only && !mbar_wait(bar(C::kFullV + (cc & 1)), par)) report(p.d_err, PA_DERR_TIMEOUT);
+        }
+        for (int k = max(0, q_issued - 2); k < q_issued; ++k)
+            if (!mbar_wait(bar(C::kQFull + (k & 1)), static_cast<uint32_t>(k >> 1) & 1))
+                report(p.d_err, PA_DERR_TIMEOUT);
+        __threadfence();
+    }
+}
+
+// ---- warp 6: the V boxes of each stage, from the producer's plan -------------
+template <typename T>
+__device__ __forceinline__ void pf_copy_v(const DecodeParams& p, const CUtensorMap* mapV,
+                                          unsigned char* sm, uint32_t base) {
+    using C = PfTile<T>;
+    const int lane = threadIdx.x & 31;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::kBarOff);
+    const int* plan = reinterpret_cast<const int*>(sm + C::kPlanOff);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + C::kMiscOff + 4);
+    for (int c = 0;; ++c) {
+        const int st = c & 1;
+        if (!mbar_wait_warp(smem_addr(bars + C::kVPlan + st), static_cast<uint32_t>(c >> 1) & 1)) {
+            if (lane == 0) report(p.d_err, PA_DERR_TIMEOUT);
+            *abort_flag = 1;
+            break;
+        }
+        if (plan[st * C::kPlanInts + C::kPlanStop] != 0) break;
+        const int row = lane < 8 ? plan[st * C::kPlanInts + lane] : -1;
+        if (row >= 0)
+            pf::tma_load_4d(base + C::kRingOff + st * C::kStageBytes + C::kTileBytes + lane * 4096, mapV,
+                            row >> 3, smem_addr(bars + C::kFullV + st));
+        __syncwarp();
+    }
+}
+
+// ---- warp 1: MMA issue -------------------------------------------------------
+// Stage c: S[c%2] = Q.K_c^T (MMA1), then O (+)= P_c.V_c (MMA2) once the
+// softmax warps have written P_c.  MMA1 of the next stage goes first when its
+// K has landed and its S buffer is free.
+template <typename T>
+__device__ __forceinline__ void pf_mma(const DecodeParams& p, unsigned char* sm, uint32_t base,
+                                       uint32_t tmem) {
+    using C = PfTile<T>;
+    const int lane = threadIdx.x & 31;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::kBarOff);
+    auto bar = [&](int i) { return smem_addr(bars + i); };
+    const PfStageMeta* meta = reinterpret_cast<const PfStageMeta*>(sm + C::kMetaOff);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + C::kMiscOff + 4);
+    auto fail = [&]() {
+        if (lane == 0) report(p.d_err, PA_DERR_TIMEOUT);
+        *abort_flag = 1;
+    };
+    auto stage_k = [&](int c) { return base + C::kRingOff + (c & 1) * C::kStageBytes; };
+
+    // Returns 0 = issued, 1 = end marker, -1 = gave up.
+    auto issue_mma1 = [&](int c) -> int {
+        const int st = c & 1;
+        if (!mbar_wait_warp(bar(C::kFullK + st), static_cast<uint32_t>(c >> 1) & 1)) return -1;
+        const uint32_t flags = meta[st].flags;
+        if (flags & kStageEnd) return 1;
+        const int item_seq = static_cast<int>(meta[st].item_seq);
+        const int qs = item_seq & 1;
+        if ((flags & kStageFirst) &&
+            !mbar_wait_warp(bar(C::kQFull + qs), static_cast<uint32_t>(item_seq >> 1) & 1))
+            return -1;
+        if (c >= 2 && !mbar_wait_warp(bar(C::kSFree + st), static_cast<uint32_t>((c >> 1) - 1) & 1))
+            return -1;
+        tc::fence_after_sync();
+        const uint32_t q = base + C::kQOff + qs * C::kOpBytes, k = stage_k(c);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {  // 16 head dimensions per step
+            const uint64_t a = tc::smem_desc_sw128(q + (j / 4) * C::kHalf + (j % 4) * 32, 16, 1024);
+            const uint64_t b = tc::smem_desc_sw128(k + (j / 4) * 1024 + (j % 4) * 32, 16, 2048);
+            tc::mma_f16_warp(tmem + st * 128, a, b, C::kIdescS, j > 0);
+        }
+        tc::mma_commit_warp(bar(C::kSFull + st));
+        tc::mma_commit_warp(bar(C::kEmptyK + st));              // K_c is free once MMA1 completed
+        if (flags & kStageLast) tc::mma_commit_warp(bar(C::kQEmpty + qs));  // so is the Q slot
+        __syncwarp();
+        return 0;
+    };
+
+    int r = issue_mma1(0);
+    if (r < 0) fail();
+    for (int c = 0; r == 0; ++c) {
+        bool next_done = false;
+        {
+            const int c1 = c + 1, st1 = c1 & 1;
+            int early = 0;
+            if (lane == 0 && mbar_try_wait(bar(C::kFullK + st1), static_cast<uint32_t>(c1 >> 1) & 1) &&
+                !(meta[st1].flags & kStageEnd) &&
+                (c1 < 2 || mbar_try_wait(bar(C::kSFree + st1), static_cast<uint32_t>((c1 >> 1) - 1) & 1)))
+                early = !(meta[st1].flags & kStageFirst) ||
+                        mbar_try_wait(bar(C::kQFull + (meta[st1].item_seq & 1)),
+                                      (meta[st1].item_seq >> 1) & 1);
+            if (__shfl_sync(0xffffffffu, early, 0)) {
+                r = issue_mma1(c1);
+                next_done = true;
+            }
+        }
+        if (r < 0) {
+            fail();
+            break;
+        }
+        if (!mbar_wait_warp(bar(C::kPFull), static_cast<uint32_t>(c) & 1)) {
+            fail();
+            break;
+        }
+        tc::fence_after_sync();
+        const bool first = (meta[c & 1].flags & kStageFirst) != 0;
+        const uint32_t pop = base + C::kPOff, v = stage_k(c) + C::kTileBytes;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {  // 16 tokens per step
+            const uint64_t a = tc::smem_desc_sw128(pop + (j / 4) * C::kHalf + (j % 4) * 32, 16, 1024);
+            const uint64_t b = tc::smem_desc_sw128(v + j * 4096, 1024, 2048);
+            tc::mma_f16_warp(tmem + C::kOCol, a, b, C::kIdescO, (j > 0 || !first) ? 1u : 0u);
+        }
+        tc::mma_commit_warp(bar(C::kPFree));             // P may be rewritten, O is complete
+        tc::mma_commit_warp(bar(C::kEmptyV + (c & 1)));  // V_c is free
+        __syncwarp();
+        if (!next_done) r = issue_mma1(c + 1);
+        if (r < 0) {
+            fail();
+            break;
+        }
+    }
+    __syncwarp();
+    tc::mma_commit_warp(bar(C::kDrain));
+    if (lane == 0 && !mbar_wait(bar(C::kDrain), 0)) report(p.d_err, PA_DERR_TIMEOUT);
+    __syncwarp();
+}
+
+// ---- warps 2-5: softmax, one thread per query row ----------------------------
+// Per stage: the row of S from TMEM, the causal and validity mask, the running
+// maximum (raised only past +8 in the log2 domain, then O and l rescaled), P
+// (rounded to T) into the K-major swizzled P tile; at an item's last stage the
+// row of O divided by the row sum (or the partition's partial state).  Thread
+// r also zeroes V row r of a stage when token r holds no data, so 0 x garbage
+// never reaches O.
+template <typename T>
+__device__ __forceinline__ void pf_softmax(const DecodeParams& p, unsigned char* sm, uint32_t tmem) {
+    using C = PfTile<T>;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int tid = threadIdx.x - 64;  // 0..127
+    const int row = 32 * (warp & 3) + lane;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::kBarOff);
+    auto bar = [&](int i) { return smem_addr(bars + i); };
+    const PfStageMeta* meta = reinterpret_cast<const PfStageMeta*>(sm + C::kMetaOff);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + C::kMiscOff + 4);
+    TeamSync team{reinterpret_cast<volatile int*>(sm + C::kMiscOff + 8), tid, 1};
+    const uint32_t lane_off = static_cast<uint32_t>(32 * (warp & 3)) << 16;
+    const int g = p.group;
+    const int ti = row / g;  // query token of this row within the item
+    const float kq = p.qk_scale_log2;
+
+    float m_ref = -INFINITY, l = 0.f;
+    int row0 = 0, hq0 = 0, part = 0, nparts = 0, ntok = 0;  // the current item
+    for (int c = 0;; ++c) {
+        const int st = c & 1;
+        if (!team.wait(bar(C::kFullV + st), static_cast<uint32_t>(c >> 1) & 1, p.d_err, abort_flag)) break;
+        const uint32_t flags = meta[st].flags;
+        if (flags & kStageEnd) break;
+        const int nvalid = meta[st].nvalid;
+        const uint32_t groups = meta[st].groups;
+        const int lim = meta[st].lim_rel + ti;  // tokens of this stage the row sees
+        if (flags & kStageFirst) {
+            row0 = meta[st].row0;
+            hq0 = meta[st].hq0;
+            part = meta[st].part;
+            nparts = meta[st].nparts;
+            ntok = meta[st].ntok;
+            m_ref = -INFINITY;
+            l = 0.f;
+        }
+        if (!(row < nvalid && ((groups >> (row >> 4)) & 1u))) {  // token `row` holds no data
+            unsigned char* vrow = sm + C::kRingOff + st * C::kStageBytes + C::kTileBytes +
+                                  (row >> 3) * 2048 + (row & 7) * 128;
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+#pragma unroll
+                for (int k = 0; k < 8; ++k)
+                    *reinterpret_cast<uint4*>(vrow + h * 1024 + k * 16) = make_uint4(0, 0, 0, 0);
+        }
+
+        // ---- S row
+        if (!team.wait(bar(C::kSFull + st), static_cast<uint32_t>(c >> 1) & 1, p.d_err, abort_flag)) break;
+        tc::fence_after_sync();
+        float x[128];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) pf::tmem_ld32(tmem + st * 128 + 32 * k + lane_off, x + 32 * k);
+        tc::fence_before_sync();
+        mbar_arrive(bar(C::kSFree + st));  // every thread of the group (count 128)
+        float mx = -INFINITY;
+#pragma unroll
+        for (int j = 0; j < 128; ++j) {
+            const bool ok = j < nvalid && ((groups >> (j >> 4)) & 1u) && j < lim;
+            x[j] = ok ? x[j] * kq : -INFINITY;
+            mx = fmaxf(mx, x[j]);
+        }
+        const float m_new = fmaxf(m_ref, mx);
+        const bool resc = m_new > m_ref + 8.f;  // also from -inf to a first finite maximum
+        float alpha = 1.f;
+        if (resc) {
+            alpha = fast_exp2(m_ref - m_new);  // 0 from -inf
+            m_ref = m_new;
+            l *= alpha;
+        }
+
+        // ---- P may be rewritten once MMA2 of the previous stage completed
+        if (c > 0 && !team.wait(bar(C::kPFree), static_cast<uint32_t>(c - 1) & 1, p.d_err, abort_flag))
+            break;
+        tc::fence_after_sync();
+        if (!(flags & kStageFirst) && __any_sync(0xffffffffu, resc)) {  // rescale this warp's O rows
+            float ov[32];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const uint32_t ta = tmem + C::kOCol + 32 * k + lane_off;
+                pf::tmem_ld32(ta, ov);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) ov[i] *= alpha;
+                pf::tmem_st32(ta, ov);
+            }
+            pf::tmem_wait_st();
+        }
+        unsigned char* prow = sm + C::kPOff + (row >> 3) * 1024 + (row & 7) * 128;
+        const bool any_valid = m_ref != -INFINITY;
+#pragma unroll
+        for (int ch = 0; ch < 16; ++ch) {  // 8 tokens per 16-byte chunk
+            uint32_t w[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int j = 8 * ch + 2 * i;
+                const float p0 = any_valid ? fast_exp2(x[j] - m_ref) : 0.f;  // masked: 2^-inf = 0
+                const float p1 = any_valid ? fast_exp2(x[j + 1] - m_ref) : 0.f;
+                w[i] = pf::pack2<T>(p0, p1);
+                const T* hp = reinterpret_cast<const T*>(&w[i]);
+                l += Elem<T>::to_float(hp[0]) + Elem<T>::to_float(hp[1]);
+            }
+            *reinterpret_cast<uint4*>(prow + (ch >> 3) * C::kHalf + (((ch & 7) ^ (row & 7)) << 4)) =
+                make_uint4(w[0], w[1], w[2], w[3]);
+        }
+        tc::fence_async_smem();
+        tc::fence_before_sync();
+        team.sync();
+        if (tid == 0) mbar_arrive(bar(C::kPFull));
+        if (!(flags & kStageLast)) continue;
+
+        // ---- item end: O of this row, once MMA2 of this stage completed
+        if (!team.wait(bar(C::kPFree), static_cast<uint32_t>(c) & 1, p.d_err, abort_flag)) break;
+        tc::fence_after_sync();
+        float o[128];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) pf::tmem_ld32(tmem + C::kOCol + 32 * k + lane_off, o + 32 * k);
+        tc::fence_before_sync();
+        if (row < ntok * g) {
+            const size_t rr = static_cast<size_t>(row0 + ti) * p.num_q_heads + hq0 + (row - ti * g);
+            if (nparts <= 1) {
+                const float inv = (nparts == 1 && l > 0.f) ? 1.f / l : 0.f;
+                uint4* dst = reinterpret_cast<uint4*>(static_cast<T*>(p.out) + rr * C::D);
+#pragma unroll
+                for (int k = 0; k < 16; ++k)
+                    dst[k] = make_uint4(pf::pack2<T>(o[8 * k] * inv, o[8 * k + 1] * inv),
+                                        pf::pack2<T>(o[8 * k + 2] * inv, o[8 * k + 3] * inv),
+                                        pf::pack2<T>(o[8 * k + 4] * inv, o[8 * k + 5] * inv),
+                                        pf::pack2<T>(o[8 * k + 6] * inv, o[8 * k + 7] * inv));
+            } else {
+                const size_t w = rr * p.max_parts + part;
+                float4* dst = reinterpret_cast<float4*>(p.ws_o + w * C::D);
+#pragma unroll
+                for (int k = 0; k < 32; ++k) dst[k] = make_float4(o[4 * k], o[4 * k + 1], o[4 * k + 2], o[4 * k + 3]);
+                p.ws_m[w] = m_ref;
+                p.ws_l[w] = l;
+            }
+        }
+    }
+    tc::fence_before_sync();
+}
+
+template <typename T>
+__global__ void __launch_bounds__(PfTile<T>::kThreads, 1)
+    prefill_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap mapK,
+                      const __grid_constant__ CUtensorMap mapV, const __grid_constant__ CUtensorMap mapQ) {
+    using C = PfTile<T>;
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    const uint32_t raw = smem_addr(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;  // 128-byte swizzle atoms need 1 KB alignment
+    unsigned char* sm = smem_raw + (base - raw);
+    const int warp = threadIdx.x >> 5;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::kBarOff);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + C::kMiscOff);
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < C::kNumBars; ++i) {
+            // s_free is signalled by every softmax thread
+            const bool all = i == C::kSFree || i == C::kSFree + 1;
+            mbar_init(smem_addr(bars + i), all ? 128 : 1);
+        }
+        *reinterpret_cast<volatile int*>(sm + C::kMiscOff + 4) = 0;
+        fence_barrier_init();
+        tc::prefetch_tensormap(&mapK);
+        tc::prefetch_tensormap(&mapV);
+        tc::prefetch_tensormap(&mapQ);
+    }
+    if (warp == 1) tc::tmem_alloc(smem_addr(tmem_slot), C::kTmemCols);
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
+
+    if (warp == 0)
+        pf_produce<T>(p, &mapK, &mapQ, sm, base);
+    else if (warp == 1)
+        pf_mma<T>(p, sm, base, tmem);
+    else if (warp < 6)
+        pf_softmax<T>(p, sm, tmem);
+    else
+        pf_copy_v<T>(p, &mapV, sm, base);
+
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        tc::fence_after_sync();
+        tc::tmem_free(tmem, C::kTmemCols);
+    }
+    if (threadIdx.x == 0) {
+        __threadfence();
+        const unsigned prev = atomicAdd(p.counters + 1, 1u);
+        if (prev == gridDim.x - 1) {
+            atomicExch(p.counters, 0u);
+            atomicExch(p.counters + 1, 0u);
+        }
+    }
+}
+
+template <typename T>
+inline pa_status launch_prefill_tc_typed(const DecodeParams& p, const CUtensorMap& mapK,
+                                         const CUtensorMap& mapV, const CUtensorMap& mapQ,
+                                         cudaStream_t stream) {
+    using C = PfTile<T>;
+    static std::atomic<uint64_t> smem_configured{0};
+    if (p.group * p.tile_tokens != C::kRows) return PA_ERR_UNSUPPORTED;
+    auto kernel = prefill_tc_kernel<T>;
+    if (ensure_smem(kernel, C::kSmemBytes, smem_configured) != PA_OK) return PA_ERR_CUDA;
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return PA_ERR_CUDA;
+    // upper bound of the work items (query-token tiles: rows / tile_tokens + one ragged per sequence)
+    const long long tiles = p.num_query_tokens / p.tile_tokens + p.num_seqs;
+    const long long work = tiles * p.head_tiles * p.max_parts;
+    if (work > 0x7fffffffLL) return PA_ERR_UNSUPPORTED;
+    long long grid = sms;
+    if (grid > work) grid = work;
+    kernel<<<static_cast<unsigned>(grid), C::kThreads, C::kSmemBytes, stream>>>(p, mapK, mapV, mapQ);
+    if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
+    if (p.max_parts > 1) {
+        decode_reduce_kernel<T, C::D><<<p.num_query_tokens * p.num_q_heads, 128, 0, stream>>>(p);
+        if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
+    }
+    return PA_OK;
+}
+
+pa_status launch_prefill_tc_f16(const DecodeParams& p, const CUtensorMap& mapK, const CUtensorMap& mapV,
+                                const CUtensorMap& mapQ, cudaStream_t stream);
+pa_status launch_prefill_tc_bf16(const DecodeParams& p, const CUtensorMap& mapK, const CUtensorMap& mapV,
+                                 const CUtensorMap& mapQ, cudaStream_t stream);
+
+}  // namespace pa

@@ -192,3 +192,50 @@ def test_multi_query_tensor_core_parity(case):
     _, out, d = _check(w, partition_tokens=P)
     again = gpu_step(w, upload(w), partition_tokens=P)
     assert torch.equal(out, again), "two identical runs differ"
+
+
+# Sequences whose queries fill 128-row tiles (query tokens x g heads, g a power
+# of two): the 128-row tensor-core kernel of chunked prefill.
+MQ_PF = [
+    # dtype, Hq, Hkv, B, P, ctx, queries per sequence
+    ("bf16", 8, 2, 16, 0, [300, 1000, 77, 2100], [300, 129, 77, 64]),     # 4 per kv head: 32 tokens/item
+    ("f16", 4, 4, 16, 256, [700, 200, 1500], [200, 200, 130]),            # MHA: 128 tokens/item
+    ("bf16", 16, 2, 32, 512, [900, 64, 2500], [100, 64, 33]),             # 8 per kv head: 16 tokens
+    ("f16", 32, 2, 128, 128, [1000, 300, 129], [20, 300, 9]),             # 16 per kv head: 8 tokens
+    ("bf16", 8, 4, 16, 0, [4096, 513, 1], [512, 513, 1]),                 # 2 per kv head; whole-context chunks
+]
+
+
+@pytest.mark.parametrize("case", range(len(MQ_PF)))
+def test_multi_query_128_row_tiles_parity(case):
+    dtype, Hq, Hkv, B, P, ctx, ql = MQ_PF[case]
+    w = wl.custom(f"mq_pf{case}", ctx, dtype=dtype, num_q_heads=Hq, num_kv_heads=Hkv,
+                  head_dim=128, block_size=B, seed=430 + case, pool_factor=1.3, query_lens=ql)
+    _, out, d = _check(w, partition_tokens=P)
+    again = gpu_step(w, upload(w), partition_tokens=P)
+    assert torch.equal(out, again), "two identical runs differ"
+
+
+def test_multi_query_128_row_tiles_bad_entries():
+    w = wl.custom("mq_pf_bad", [600, 300, 900, 200], dtype="bf16", num_q_heads=8, num_kv_heads=2,
+                  head_dim=128, block_size=16, seed=440, max_blocks_per_seq=60,
+                  query_lens=[200, 100, 150, 90])
+    d = upload(w)
+    gpu_step(w, d)  # writes the new tokens
+    kc, vc, _, err = oracle_step(w)
+    assert err == 0 and int(d["d_err"].item()) == 0
+    ctx = w.context_lens.copy()
+    ctx[0] = 150                               # fewer tokens than its 200 queries
+    tables = w.block_tables.copy()
+    tables[2, 30] = w.num_blocks + 3           # block id outside the pool
+    ref, err = oracle.multi_query(w.q, w.query_start, kc, vc, tables, ctx, scale=w.scale,
+                                  dtype=w.dtype)
+    assert err == oracle.ERR_CTX_OOB | oracle.ERR_BLOCK_OOB
+    e = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = torch.full_like(d["q"], float("nan"))
+    pa.multi_query(out, d["q"], d["query_start"], d["k_cache"], d["v_cache"],
+                   torch.from_numpy(tables).cuda(), torch.from_numpy(ctx).cuda(), w.scale, d_err=e)
+    torch.cuda.synchronize()
+    assert int(e.item()) == err
+    assert_close(out_f64(out), ref, "bf16", "mq_pf_bad")
+    assert (out[:200] == 0).all()
