@@ -12,7 +12,7 @@
 // its causal span of the table, one 128-token K/V stage at a time:
 //
 //   S = Q . K^T   (tcgen05.mma, M = 128 rows, N = 128 tokens, fp32 in TMEM)
-//   P = 2^(S * scale * log2 e - m)     one thread per row, from TMEM
+//   P = 2^(S * scale * log2 e - m)     two threads per row, from TMEM
 //   O += P . V    (M = 128 rows, N = 128 head dimensions, fp32 in TMEM)
 //
 // with a running row maximum m that is raised only when a stage's maximum
@@ -20,9 +20,9 @@
 // the weights stay <= 2^8, exact in fp32 and far inside the 16-bit range).
 //
 // Warps: 0 walks the work items and issues the Q and K copies, 1 issues the
-// MMAs (one elected lane) and owns TMEM, 2-5 are the softmax warpgroup
-// (thread = query row, warp w reading TMEM lanes 32*(w%4)..), 6 issues the V
-// copies from a per-stage plan.  Shared memory: a 2-stage K/V ring (the K and
+// MMAs (one elected lane) and owns TMEM, 2-9 are the softmax warps (two
+// threads per query row, one per 64-column half; warp w reads TMEM lanes
+// 32*(w%4)..), 10 issues the V copies from a per-stage plan.  Shared memory: a 2-stage K/V ring (the K and
 // V halves of a slot released separately), two Q slots, one P tile.
 #pragma once
 
@@ -31,7 +31,6 @@
 #include <type_traits>
 
 #include "decode_kernels.cuh"
-#include "decode_tc.cuh"  // TeamSync
 #include "tc_ptx.cuh"
 
 namespace pa {
@@ -58,9 +57,10 @@ struct PfTile {
     static constexpr int kFullK = 0, kEmptyK = 2, kFullV = 4, kEmptyV = 6, kVPlan = 8;
     static constexpr int kQFull = 10, kQEmpty = 12, kSFull = 14, kSFree = 16;
     static constexpr int kPFull = 18, kPFree = 19, kDrain = 20, kNumBars = 21;
-    static constexpr int kMiscOff = kBarOff + kNumBars * 8;  // tmem base, abort, team flags [2]
+    static constexpr int kRedOff = kBarOff + kNumBars * 8;    // row maxima / sums of the halves [2][128]
+    static constexpr int kMiscOff = kRedOff + 2 * 128 * 4;    // tmem base, abort, group flags [2]
     static constexpr int kSmemBytes = kMiscOff + 32 + 1024;  // + alignment slack
-    static constexpr int kThreads = 224;
+    static constexpr int kThreads = 352;
     static constexpr uint32_t kTmemCols = 512;  // S [2] x 128, O 128
     static constexpr uint32_t kOCol = 256;
     static constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
@@ -402,7 +402,7 @@ __device__ __forceinline__ void pf_produce(const DecodeParams& p, const CUtensor
     }
 }
 
-// ---- warp 6: the V boxes of each stage, from the producer's plan -------------
+// ---- warp 10: the V boxes of each stage, from the producer's plan ------------
 template <typename T>
 __device__ __forceinline__ void pf_copy_v(const DecodeParams& p, const CUtensorMap* mapV,
                                           unsigned char* sm, uint32_t base) {
@@ -524,39 +524,70 @@ __device__ __forceinline__ void pf_mma(const DecodeParams& p, unsigned char* sm,
     __syncwarp();
 }
 
-// ---- warps 2-5: softmax, one thread per query row ----------------------------
-// Per stage: the row of S from TMEM, the causal and validity mask, the running
-// maximum (raised only past +8 in the log2 domain, then O and l rescaled), P
-// (rounded to T) into the K-major swizzled P tile; at an item's last stage the
-// row of O divided by the row sum (or the partition's partial state).  Thread
-// r also zeroes V row r of a stage when token r holds no data, so 0 x garbage
-// never reaches O.
+// The softmax warps agree on every wait: thread 0 waits (bounded), the
+// outcome goes through one of two alternating shared flags and the group's
+// named barrier, so no thread can stay behind at a later barrier.
+struct PfGroup {
+    volatile int* flags;  // [2]
+    int tid;
+    int k = 0;
+    __device__ __forceinline__ void sync() const { named_barrier(1, 256); }
+    __device__ __forceinline__ bool wait(uint32_t bar, uint32_t parity, uint32_t* d_err,
+                                         volatile int* abort_flag) {
+        const int slot = k++ & 1;
+        if (tid == 0) {
+            const bool ok = mbar_wait(bar, parity);
+            if (!ok) {
+                report(d_err, PA_DERR_TIMEOUT);
+                *abort_flag = 1;
+            }
+            flags[slot] = ok ? 1 : 0;
+        }
+        sync();
+        return flags[slot] != 0;
+    }
+};
+
+// ---- warps 2-9: softmax, two threads per query row ---------------------------
+// Warp w handles rows 32*(w%4).. (its TMEM lane quadrant) and the 64 columns
+// (K/V tokens of the stage; head dimensions of O) of half (w-2)/4.  Per
+// stage: its half of the row of S from TMEM, the causal and validity mask,
+// the row maximum (the two halves exchange theirs through shared memory), the
+// running maximum (raised only past +8 in the log2 domain, then its half of O
+// and the row sum rescaled), P (rounded to T) into its 64-token half of the
+// swizzled P tile; at an item's last stage its half of the row of O divided by
+// the row sum (or the partition's partial state).  The thread also zeroes its
+// half of V row `row` when token `row` holds no data, so 0 x garbage never
+// reaches O.
 template <typename T>
 __device__ __forceinline__ void pf_softmax(const DecodeParams& p, unsigned char* sm, uint32_t tmem) {
     using C = PfTile<T>;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int tid = threadIdx.x - 64;  // 0..127
+    const int tid = threadIdx.x - 64;  // 0..255
+    const int half = (warp - 2) >> 2;  // columns 64*half ..
     const int row = 32 * (warp & 3) + lane;
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::kBarOff);
     auto bar = [&](int i) { return smem_addr(bars + i); };
     const PfStageMeta* meta = reinterpret_cast<const PfStageMeta*>(sm + C::kMetaOff);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + C::kMiscOff + 4);
-    TeamSync team{reinterpret_cast<volatile int*>(sm + C::kMiscOff + 8), tid, 1};
+    float* red = reinterpret_cast<float*>(sm + C::kRedOff);  // [2 halves][128 rows]
+    PfGroup grp{reinterpret_cast<volatile int*>(sm + C::kMiscOff + 8), tid};
     const uint32_t lane_off = static_cast<uint32_t>(32 * (warp & 3)) << 16;
+    const uint32_t col0 = 64u * half;
     const int g = p.group;
     const int ti = row / g;  // query token of this row within the item
     const float kq = p.qk_scale_log2;
 
-    float m_ref = -INFINITY, l = 0.f;
+    float m_ref = -INFINITY, l = 0.f;  // l: this half's share of the row sum
     int row0 = 0, hq0 = 0, part = 0, nparts = 0, ntok = 0;  // the current item
     for (int c = 0;; ++c) {
         const int st = c & 1;
-        if (!team.wait(bar(C::kFullV + st), static_cast<uint32_t>(c >> 1) & 1, p.d_err, abort_flag)) break;
+        if (!grp.wait(bar(C::kFullV + st), static_cast<uint32_t>(c >> 1) & 1, p.d_err, abort_flag)) break;
         const uint32_t flags = meta[st].flags;
         if (flags & kStageEnd) break;
         const int nvalid = meta[st].nvalid;
         const uint32_t groups = meta[st].groups;
-        const int lim = meta[st].lim_rel + ti;  // tokens of this stage the row sees
+        const int lim = min(nvalid, meta[st].lim_rel + ti);  // tokens of this stage the row sees
         if (flags & kStageFirst) {
             row0 = meta[st].row0;
             hq0 = meta[st].hq0;
@@ -568,29 +599,38 @@ __device__ __forceinline__ void pf_softmax(const DecodeParams& p, unsigned char*
         }
         if (!(row < nvalid && ((groups >> (row >> 4)) & 1u))) {  // token `row` holds no data
             unsigned char* vrow = sm + C::kRingOff + st * C::kStageBytes + C::kTileBytes +
-                                  (row >> 3) * 2048 + (row & 7) * 128;
+                                  (row >> 3) * 2048 + half * 1024 + (row & 7) * 128;
 #pragma unroll
-            for (int h = 0; h < 2; ++h)
-#pragma unroll
-                for (int k = 0; k < 8; ++k)
-                    *reinterpret_cast<uint4*>(vrow + h * 1024 + k * 16) = make_uint4(0, 0, 0, 0);
+            for (int k = 0; k < 8; ++k) *reinterpret_cast<uint4*>(vrow + k * 16) = make_uint4(0, 0, 0, 0);
         }
 
-        // ---- S row
-        if (!team.wait(bar(C::kSFull + st), static_cast<uint32_t>(c >> 1) & 1, p.d_err, abort_flag)) break;
+        // ---- this half of the S row
+        if (!grp.wait(bar(C::kSFull + st), static_cast<uint32_t>(c >> 1) & 1, p.d_err, abort_flag)) break;
         tc::fence_after_sync();
-        float x[128];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) pf::tmem_ld32(tmem + st * 128 + 32 * k + lane_off, x + 32 * k);
+        float x[64];
+        pf::tmem_ld32(tmem + st * 128 + col0 + lane_off, x);
+        pf::tmem_ld32(tmem + st * 128 + col0 + 32 + lane_off, x + 32);
         tc::fence_before_sync();
-        mbar_arrive(bar(C::kSFree + st));  // every thread of the group (count 128)
-        float mx = -INFINITY;
+        mbar_arrive(bar(C::kSFree + st));  // every thread of the group (count 256)
+        float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+        if (groups == 0xffu && lim >= 128) {  // every token valid for every row: no mask
 #pragma unroll
-        for (int j = 0; j < 128; ++j) {
-            const bool ok = j < nvalid && ((groups >> (j >> 4)) & 1u) && j < lim;
-            x[j] = ok ? x[j] * kq : -INFINITY;
-            mx = fmaxf(mx, x[j]);
+            for (int j = 0; j < 64; ++j) {
+                x[j] *= kq;
+                mx4[j & 3] = fmaxf(mx4[j & 3], x[j]);
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < 64; ++j) {
+                const int t = static_cast<int>(col0) + j;
+                const bool ok = t < lim && ((groups >> (t >> 4)) & 1u);
+                x[j] = ok ? x[j] * kq : -INFINITY;
+                mx4[j & 3] = fmaxf(mx4[j & 3], x[j]);
+            }
         }
+        red[half * 128 + row] = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+        grp.sync();
+        const float mx = fmaxf(red[row], red[128 + row]);
         const float m_new = fmaxf(m_ref, mx);
         const bool resc = m_new > m_ref + 8.f;  // also from -inf to a first finite maximum
         float alpha = 1.f;
@@ -601,14 +641,14 @@ __device__ __forceinline__ void pf_softmax(const DecodeParams& p, unsigned char*
         }
 
         // ---- P may be rewritten once MMA2 of the previous stage completed
-        if (c > 0 && !team.wait(bar(C::kPFree), static_cast<uint32_t>(c - 1) & 1, p.d_err, abort_flag))
+        if (c > 0 && !grp.wait(bar(C::kPFree), static_cast<uint32_t>(c - 1) & 1, p.d_err, abort_flag))
             break;
         tc::fence_after_sync();
-        if (!(flags & kStageFirst) && __any_sync(0xffffffffu, resc)) {  // rescale this warp's O rows
+        if (!(flags & kStageFirst) && __any_sync(0xffffffffu, resc)) {  // rescale this warp's O
             float ov[32];
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const uint32_t ta = tmem + C::kOCol + 32 * k + lane_off;
+            for (int k = 0; k < 2; ++k) {
+                const uint32_t ta = tmem + C::kOCol + col0 + 32 * k + lane_off;
                 pf::tmem_ld32(ta, ov);
 #pragma unroll
                 for (int i = 0; i < 32; ++i) ov[i] *= alpha;
@@ -616,10 +656,11 @@ __device__ __forceinline__ void pf_softmax(const DecodeParams& p, unsigned char*
             }
             pf::tmem_wait_st();
         }
-        unsigned char* prow = sm + C::kPOff + (row >> 3) * 1024 + (row & 7) * 128;
+        unsigned char* prow = sm + C::kPOff + half * C::kHalf + (row >> 3) * 1024 + (row & 7) * 128;
         const bool any_valid = m_ref != -INFINITY;
+        float l4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int ch = 0; ch < 16; ++ch) {  // 8 tokens per 16-byte chunk
+        for (int ch = 0; ch < 8; ++ch) {  // 8 tokens per 16-byte chunk
             uint32_t w[4];
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
@@ -628,42 +669,47 @@ __device__ __forceinline__ void pf_softmax(const DecodeParams& p, unsigned char*
                 const float p1 = any_valid ? fast_exp2(x[j + 1] - m_ref) : 0.f;
                 w[i] = pf::pack2<T>(p0, p1);
                 const T* hp = reinterpret_cast<const T*>(&w[i]);
-                l += Elem<T>::to_float(hp[0]) + Elem<T>::to_float(hp[1]);
+                l4[i] += Elem<T>::to_float(hp[0]) + Elem<T>::to_float(hp[1]);
             }
-            *reinterpret_cast<uint4*>(prow + (ch >> 3) * C::kHalf + (((ch & 7) ^ (row & 7)) << 4)) =
-                make_uint4(w[0], w[1], w[2], w[3]);
+            *reinterpret_cast<uint4*>(prow + (((ch & 7) ^ (row & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
         }
+        l += (l4[0] + l4[1]) + (l4[2] + l4[3]);
         tc::fence_async_smem();
         tc::fence_before_sync();
-        team.sync();
+        grp.sync();
         if (tid == 0) mbar_arrive(bar(C::kPFull));
         if (!(flags & kStageLast)) continue;
 
-        // ---- item end: O of this row, once MMA2 of this stage completed
-        if (!team.wait(bar(C::kPFree), static_cast<uint32_t>(c) & 1, p.d_err, abort_flag)) break;
+        // ---- item end: this half of the row of O, once MMA2 of this stage completed
+        if (!grp.wait(bar(C::kPFree), static_cast<uint32_t>(c) & 1, p.d_err, abort_flag)) break;
         tc::fence_after_sync();
-        float o[128];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) pf::tmem_ld32(tmem + C::kOCol + 32 * k + lane_off, o + 32 * k);
+        float o[64];
+        pf::tmem_ld32(tmem + C::kOCol + col0 + lane_off, o);
+        pf::tmem_ld32(tmem + C::kOCol + col0 + 32 + lane_off, o + 32);
         tc::fence_before_sync();
+        red[half * 128 + row] = l;
+        grp.sync();
+        const float L = red[row] + red[128 + row];
         if (row < ntok * g) {
             const size_t rr = static_cast<size_t>(row0 + ti) * p.num_q_heads + hq0 + (row - ti * g);
             if (nparts <= 1) {
-                const float inv = (nparts == 1 && l > 0.f) ? 1.f / l : 0.f;
-                uint4* dst = reinterpret_cast<uint4*>(static_cast<T*>(p.out) + rr * C::D);
+                const float inv = (nparts == 1 && L > 0.f) ? 1.f / L : 0.f;
+                uint4* dst = reinterpret_cast<uint4*>(static_cast<T*>(p.out) + rr * C::D + col0);
 #pragma unroll
-                for (int k = 0; k < 16; ++k)
+                for (int k = 0; k < 8; ++k)
                     dst[k] = make_uint4(pf::pack2<T>(o[8 * k] * inv, o[8 * k + 1] * inv),
                                         pf::pack2<T>(o[8 * k + 2] * inv, o[8 * k + 3] * inv),
                                         pf::pack2<T>(o[8 * k + 4] * inv, o[8 * k + 5] * inv),
                                         pf::pack2<T>(o[8 * k + 6] * inv, o[8 * k + 7] * inv));
             } else {
                 const size_t w = rr * p.max_parts + part;
-                float4* dst = reinterpret_cast<float4*>(p.ws_o + w * C::D);
+                float4* dst = reinterpret_cast<float4*>(p.ws_o + w * C::D + col0);
 #pragma unroll
-                for (int k = 0; k < 32; ++k) dst[k] = make_float4(o[4 * k], o[4 * k + 1], o[4 * k + 2], o[4 * k + 3]);
-                p.ws_m[w] = m_ref;
-                p.ws_l[w] = l;
+                for (int k = 0; k < 16; ++k) dst[k] = make_float4(o[4 * k], o[4 * k + 1], o[4 * k + 2], o[4 * k + 3]);
+                if (half == 0) {
+                    p.ws_m[w] = m_ref;
+                    p.ws_l[w] = L;
+                }
             }
         }
     }
@@ -687,7 +733,7 @@ __global__ void __launch_bounds__(PfTile<T>::kThreads, 1)
         for (int i = 0; i < C::kNumBars; ++i) {
             // s_free is signalled by every softmax thread
             const bool all = i == C::kSFree || i == C::kSFree + 1;
-            mbar_init(smem_addr(bars + i), all ? 128 : 1);
+            mbar_init(smem_addr(bars + i), all ? 256 : 1);
         }
         *reinterpret_cast<volatile int*>(sm + C::kMiscOff + 4) = 0;
         fence_barrier_init();
@@ -705,7 +751,7 @@ __global__ void __launch_bounds__(PfTile<T>::kThreads, 1)
         pf_produce<T>(p, &mapK, &mapQ, sm, base);
     else if (warp == 1)
         pf_mma<T>(p, sm, base, tmem);
-    else if (warp < 6)
+    else if (warp < 10)
         pf_softmax<T>(p, sm, tmem);
     else
         pf_copy_v<T>(p, &mapV, sm, base);
