@@ -212,11 +212,17 @@ pa_status pa_decode(void* out, const void* q, const void* k_cache, const void* v
  * sequence with L_s > n, or n outside [0, max_blocks_per_seq*block_size],
  * gets zero rows and PA_DERR_CTX_OOB; a descending query_start is flagged
  * PA_DERR_CTX_OOB and the rows it would place are skipped.  Bad block ids:
- * as pa_decode.  The work is tiled as (kv head, up to 8 query rows of one or
- * more consecutive query tokens, partition), so the K/V of a tile is read
- * once for all its rows.  Partitions: pa_multi_query_partition_tokens();
- * workspace: pa_multi_query_workspace_size() bytes, with the same rules as
- * pa_decode's.  Supported sizes and accumulation: as pa_decode.
+ * as pa_decode.  The work is tiled as (kv head, query rows of one or more
+ * consecutive query tokens x the kv head's query heads, partition), so the
+ * K/V of a tile is read once for all its rows: up to 8 rows on the SIMT
+ * kernel, up to 16 on the grouped tensor-core kernel, and 128 (128/g tokens x
+ * g heads) for 16-bit K/V with head_dim 128, g a power of two <= 16 and on
+ * average at least 64 query rows per sequence and kv head (chunked prefill).
+ * Partitions: pa_multi_query_partition_tokens(); with partition_tokens = 0
+ * the 128-row kernel may use longer ones (down to the whole context) when its
+ * query tiles alone give two work items per SM.  Workspace:
+ * pa_multi_query_workspace_size() bytes, with the same rules as pa_decode's.
+ * Supported sizes and accumulation: as pa_decode.
  */
 int pa_multi_query_partition_tokens(int num_query_tokens, int num_q_heads, int num_kv_heads,
                                     int head_dim, int max_blocks_per_seq, int block_size,

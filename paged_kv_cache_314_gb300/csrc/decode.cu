@@ -193,12 +193,22 @@ struct AttnCall {
     int num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks;
     float scale;
     int partition_tokens;  // resolved, > 0
+    bool partition_default;  // the caller passed 0: the library may lengthen it
     pa_dtype dtype;
     void* workspace;
     size_t workspace_bytes;
     uint32_t* d_err;
     pa_stream_t stream;
 };
+
+int gcd_int(int a, int b) {
+    while (b != 0) {
+        const int t = a % b;
+        a = b;
+        b = t;
+    }
+    return a;
+}
 
 int log2_exact(int x) {
     int r = 0;
@@ -302,6 +312,34 @@ pa_status run_attention(const AttnCall& a) {
             p.head_tiles = a.num_kv_heads;
             p.tile_heads = group;
             p.tile_tokens = 128 / group;
+            if (a.partition_default) {
+                // A chunk's query tiles already give many work items: split the
+                // context only as far as two items per SM need (each split costs
+                // partial states and a merge).  Never shorter than the default,
+                // so the workspace sized for it suffices.
+                int dev = 0, sms = 0;
+                if (cudaGetDevice(&dev) != cudaSuccess ||
+                    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+                    return PA_ERR_CUDA;
+                const long long step = a.block_size % 128 == 0 ? a.block_size
+                                       : 128 % a.block_size == 0 ? 128
+                                                                 : 128LL * a.block_size / gcd_int(128, a.block_size);
+                const long long max_ctx = static_cast<long long>(a.max_blocks_per_seq) * a.block_size;
+                const long long tiles = (a.num_query_tokens + p.tile_tokens - 1) / p.tile_tokens *
+                                        static_cast<long long>(a.num_kv_heads);
+                long long P2 = (max_ctx + step - 1) / step * step;
+                while (P2 > P && tiles * ((max_ctx + P2 - 1) / P2) < 2LL * sms)
+                    P2 = ((P2 / 2) + step - 1) / step * step;
+                if (P2 > P && P2 <= 0x7fffffffLL) {
+                    const int mp = max_parts_for(a.max_blocks_per_seq, a.block_size, static_cast<int>(P2));
+                    const WsLayout w2 = ws_layout(a.num_query_tokens, a.num_q_heads, a.head_dim, mp);
+                    p.partition_tokens = static_cast<int>(P2);
+                    p.max_parts = mp;
+                    p.ws_m = mp > 1 ? reinterpret_cast<float*>(wsb + w2.m_off) : nullptr;
+                    p.ws_l = mp > 1 ? reinterpret_cast<float*>(wsb + w2.l_off) : nullptr;
+                    p.ws_o = mp > 1 ? reinterpret_cast<float*>(wsb + w2.o_off) : nullptr;
+                }
+            }
             return a.dtype == PA_BF16 ? launch_prefill_tc_bf16(p, map_k, map_v, map_q, st)
                                       : launch_prefill_tc_f16(p, map_k, map_v, map_q, st);
         }
@@ -382,7 +420,7 @@ extern "C" pa_status pa_decode(void* out, const void* q, const void* k_cache, co
     if (static_cast<long long>(num_seqs) * num_q_heads > 0x7fffffffLL) return PA_ERR_UNSUPPORTED;
     const AttnCall a{out, q, nullptr, num_seqs, k_cache, v_cache, nullptr, nullptr, block_tables,
                      max_blocks_per_seq, context_lens, num_seqs, num_q_heads, num_kv_heads,
-                     head_dim, block_size, num_blocks, scale, P, dtype, workspace,
+                     head_dim, block_size, num_blocks, scale, P, false, dtype, workspace,
                      workspace_bytes, d_err, stream};
     return run_attention(a);
 }
@@ -411,7 +449,7 @@ extern "C" pa_status pa_decode_fp8(void* out, const void* q, pa_dtype q_dtype, c
     if (static_cast<long long>(num_seqs) * num_q_heads > 0x7fffffffLL) return PA_ERR_UNSUPPORTED;
     const AttnCall a{out, q, nullptr, num_seqs, k_cache, v_cache, k_scale, v_scale, block_tables,
                      max_blocks_per_seq, context_lens, num_seqs, num_q_heads, num_kv_heads,
-                     head_dim, block_size, num_blocks, scale, P, q_dtype, workspace,
+                     head_dim, block_size, num_blocks, scale, P, false, q_dtype, workspace,
                      workspace_bytes, d_err, stream};
     return run_attention(a);
 }
@@ -466,7 +504,7 @@ extern "C" pa_status pa_multi_query(void* out, const void* q, int num_query_toke
     const AttnCall a{out, q, query_start, num_query_tokens, k_cache, v_cache, nullptr, nullptr,
                      block_tables,
                      max_blocks_per_seq, context_lens, num_seqs, num_q_heads, num_kv_heads,
-                     head_dim, block_size, num_blocks, scale, P, dtype, workspace,
-                     workspace_bytes, d_err, stream};
+                     head_dim, block_size, num_blocks, scale, P, partition_tokens == 0, dtype,
+                     workspace, workspace_bytes, d_err, stream};
     return run_attention(a);
 }
