@@ -48,8 +48,11 @@ struct PfTile {
     static constexpr int kRingOff = 0;
     static constexpr int kQOff = kStages * kStageBytes;  // Q slots [2]
     static constexpr int kPOff = kQOff + 2 * kOpBytes;
-    static constexpr int kMetaOff = kPOff + kOpBytes;    // stage meta [kStages], 64 B each
-    static constexpr int kPlanOff = kMetaOff + kStages * 64;  // V box rows of a stage [8] + stop word
+    // stage meta, 64 B each, in 4 slots (stage c in slot c % 4): stage c+2's is
+    // written as soon as its K copies are issued, while stage c's is still read
+    static constexpr int kMetaSlots = 4;
+    static constexpr int kMetaOff = kPOff + kOpBytes;
+    static constexpr int kPlanOff = kMetaOff + kMetaSlots * 64;  // V box rows of a stage [8] + stop word
     static constexpr int kPlanInts = 12;
     static constexpr int kPlanStop = 8;
     static constexpr int kBarOff = kPlanOff + kStages * kPlanInts * 4;
@@ -72,9 +75,10 @@ struct PfTile {
     static constexpr uint32_t kIdescO = tc::instr_desc_f16(kBf16, 128, 128, false, true);
 };
 
-// Written by the producer before the stage's arrivals; the ring protects it
-// until MMA2 of the stage completed, so the softmax warps copy what they need
-// of it before they post the stage's P.
+// Written by the producer before the stage's arrivals on fullK and fullV.
+// Slot c % 4 is rewritten for stage c+4, whose K copies wait for MMA1 of
+// stage c+2, which the MMA warp issues after MMA2 of stage c and only once
+// the softmax warps have read S of stage c (so both are done with the slot).
 struct PfStageMeta {
     uint32_t item_seq;
     int nvalid;       // tokens of the stage before the item's span end
@@ -322,13 +326,29 @@ __device__ __forceinline__ void pf_produce(const DecodeParams& p, const CUtensor
             const uint32_t tile_bytes = static_cast<uint32_t>(__popc(groups)) * 4096u;
             const uint32_t stage_base = base + C::kRingOff + st * C::kStageBytes;
             if (mine) pf::tma_load_4d(stage_base + r * 4096, mapK, row >> 3, bar(C::kFullK + st));
+            if (lane == 0) {
+                PfStageMeta& m = meta[cc & (C::kMetaSlots - 1)];
+                uint32_t flags = 0;
+                if (i == 0) flags |= kStageFirst;
+                if (i == nst - 1) flags |= kStageLast;
+                m.item_seq = static_cast<uint32_t>(item_seq);
+                m.nvalid = max(0, t1 - t0);
+                m.groups = groups;
+                m.flags = flags;
+                m.lim_rel = max(-C::kRows, min(C::kStageTok, lim_first - t0));
+                m.row0 = sq.q0 + i0;
+                m.hq0 = hq0;
+                m.part = part;
+                m.nparts = valid ? np : 0;
+                m.ntok = ntok;
+                // the meta is written before either arrival: the MMA warp reads it
+                // after fullK, the softmax warps after fullV
+                mbar_arrive_expect_tx(bar(C::kFullK + st), tile_bytes);
+            }
             __syncwarp();
             // the V half is free once MMA2 of the slot's previous stage completed
             if (cc >= C::kStages && !mbar_wait_warp(bar(C::kEmptyV + st), reuse)) {
-                if (lane == 0) {
-                    report(p.d_err, PA_DERR_TIMEOUT);
-                    mbar_arrive_expect_tx(bar(C::kFullK + st), tile_bytes);  // so the drain sees K land
-                }
+                if (lane == 0) report(p.d_err, PA_DERR_TIMEOUT);
                 *abort_flag = 1;
                 aborted = true;
                 k_only = cc;
@@ -336,27 +356,9 @@ __device__ __forceinline__ void pf_produce(const DecodeParams& p, const CUtensor
                 break;
             }
             if (lane < 8) plan[st * C::kPlanInts + lane] = mine ? row : -1;
-            if (lane == 0) {
-                uint32_t flags = 0;
-                if (i == 0) flags |= kStageFirst;
-                if (i == nst - 1) flags |= kStageLast;
-                meta[st].item_seq = static_cast<uint32_t>(item_seq);
-                meta[st].nvalid = max(0, t1 - t0);
-                meta[st].groups = groups;
-                meta[st].flags = flags;
-                meta[st].lim_rel = max(-C::kRows, min(C::kStageTok, lim_first - t0));
-                meta[st].row0 = sq.q0 + i0;
-                meta[st].hq0 = hq0;
-                meta[st].part = part;
-                meta[st].nparts = valid ? np : 0;
-                meta[st].ntok = ntok;
-                plan[st * C::kPlanInts + C::kPlanStop] = 0;
-            }
+            if (lane == 0) plan[st * C::kPlanInts + C::kPlanStop] = 0;
             __syncwarp();
             if (lane == 0) {
-                // meta is written before either arrival: the MMA warp reads it after
-                // fullK, the softmax warps after fullV
-                mbar_arrive_expect_tx(bar(C::kFullK + st), tile_bytes);
                 mbar_arrive_expect_tx(bar(C::kFullV + st), tile_bytes);
                 mbar_arrive(bar(C::kVPlan + st));
             }
@@ -376,9 +378,10 @@ __device__ __forceinline__ void pf_produce(const DecodeParams& p, const CUtensor
             *abort_flag = 1;
         } else {
             if (lane == 0) {
-                meta[st].flags = kStageEnd;
-                meta[st].nvalid = 0;
-                meta[st].groups = 0;
+                PfStageMeta& m = meta[c & (C::kMetaSlots - 1)];
+                m.flags = kStageEnd;
+                m.nvalid = 0;
+                m.groups = 0;
                 plan[st * C::kPlanInts + C::kPlanStop] = 1;  // the copy warp leaves
                 mbar_arrive(bar(C::kFullK + st));
                 mbar_arrive(bar(C::kFullV + st));
@@ -450,9 +453,10 @@ __device__ __forceinline__ void pf_mma(const DecodeParams& p, unsigned char* sm,
     auto issue_mma1 = [&](int c) -> int {
         const int st = c & 1;
         if (!mbar_wait_warp(bar(C::kFullK + st), static_cast<uint32_t>(c >> 1) & 1)) return -1;
-        const uint32_t flags = meta[st].flags;
+        const PfStageMeta& m = meta[c & (C::kMetaSlots - 1)];
+        const uint32_t flags = m.flags;
         if (flags & kStageEnd) return 1;
-        const int item_seq = static_cast<int>(meta[st].item_seq);
+        const int item_seq = static_cast<int>(m.item_seq);
         const int qs = item_seq & 1;
         if ((flags & kStageFirst) &&
             !mbar_wait_warp(bar(C::kQFull + qs), static_cast<uint32_t>(item_seq >> 1) & 1))
@@ -482,11 +486,12 @@ __device__ __forceinline__ void pf_mma(const DecodeParams& p, unsigned char* sm,
             const int c1 = c + 1, st1 = c1 & 1;
             int early = 0;
             if (lane == 0 && mbar_try_wait(bar(C::kFullK + st1), static_cast<uint32_t>(c1 >> 1) & 1) &&
-                !(meta[st1].flags & kStageEnd) &&
-                (c1 < 2 || mbar_try_wait(bar(C::kSFree + st1), static_cast<uint32_t>((c1 >> 1) - 1) & 1)))
-                early = !(meta[st1].flags & kStageFirst) ||
-                        mbar_try_wait(bar(C::kQFull + (meta[st1].item_seq & 1)),
-                                      (meta[st1].item_seq >> 1) & 1);
+                !(meta[c1 & (C::kMetaSlots - 1)].flags & kStageEnd) &&
+                (c1 < 2 || mbar_try_wait(bar(C::kSFree + st1), static_cast<uint32_t>((c1 >> 1) - 1) & 1))) {
+                const PfStageMeta& m1 = meta[c1 & (C::kMetaSlots - 1)];
+                early = !(m1.flags & kStageFirst) ||
+                        mbar_try_wait(bar(C::kQFull + (m1.item_seq & 1)), (m1.item_seq >> 1) & 1);
+            }
             if (__shfl_sync(0xffffffffu, early, 0)) {
                 r = issue_mma1(c1);
                 next_done = true;
@@ -501,7 +506,7 @@ __device__ __forceinline__ void pf_mma(const DecodeParams& p, unsigned char* sm,
             break;
         }
         tc::fence_after_sync();
-        const bool first = (meta[c & 1].flags & kStageFirst) != 0;
+        const bool first = (meta[c & (C::kMetaSlots - 1)].flags & kStageFirst) != 0;
         const uint32_t pop = base + C::kPOff, v = stage_k(c) + C::kTileBytes;
 #pragma unroll
         for (int j = 0; j < 8; ++j) {  // 16 tokens per step
@@ -583,17 +588,18 @@ __device__ __forceinline__ void pf_softmax(const DecodeParams& p, unsigned char*
     for (int c = 0;; ++c) {
         const int st = c & 1;
         if (!grp.wait(bar(C::kFullV + st), static_cast<uint32_t>(c >> 1) & 1, p.d_err, abort_flag)) break;
-        const uint32_t flags = meta[st].flags;
+        const PfStageMeta& m = meta[c & (C::kMetaSlots - 1)];
+        const uint32_t flags = m.flags;
         if (flags & kStageEnd) break;
-        const int nvalid = meta[st].nvalid;
-        const uint32_t groups = meta[st].groups;
-        const int lim = min(nvalid, meta[st].lim_rel + ti);  // tokens of this stage the row sees
+        const int nvalid = m.nvalid;
+        const uint32_t groups = m.groups;
+        const int lim = min(nvalid, m.lim_rel + ti);  // tokens of this stage the row sees
         if (flags & kStageFirst) {
-            row0 = meta[st].row0;
-            hq0 = meta[st].hq0;
-            part = meta[st].part;
-            nparts = meta[st].nparts;
-            ntok = meta[st].ntok;
+            row0 = m.row0;
+            hq0 = m.hq0;
+            part = m.part;
+            nparts = m.nparts;
+            ntok = m.ntok;
             m_ref = -INFINITY;
             l = 0.f;
         }
