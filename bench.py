@@ -160,7 +160,7 @@ def _peaks():
 def _kernel_source_hash():
     csrc = os.path.join(ROOT, "paged_kv_cache_314_gb300", "csrc")
     h = hashlib.sha256()
-    for name in ("decode_kernels.cuh", "decode_tc.cuh", "tc_ptx.cuh", "pa_device.cuh"):
+    for name in ("decode_kernels.cuh", "decode_tc.cuh", "prefill_tc.cuh", "tc_ptx.cuh", "pa_device.cuh"):
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
