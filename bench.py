@@ -466,14 +466,32 @@ def run_gpu(args):
     flops = 4 * w.head_dim * w.num_q_heads * sum(n for _, _, n in _rows(w))
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     alu_peak = _alu_peak_tflops(sms)
-    kernel = "pa_multi_query (partition kernel + split-K merge)" if mq else \
-        "pa_decode (partition kernel + split-K merge)"
+    g = w.num_q_heads // w.num_kv_heads
+    # the library's 128-row multi-query kernel (16-bit K/V, d = 128, g a power of
+    # two <= 16, >= 64 query rows per sequence and kv head on average); with the
+    # default partition it splits a context only as far as two items per SM need
+    rows128 = (mq and not fp8 and w.dtype in ("f16", "bf16") and w.head_dim == 128 and
+               g <= 16 and (g & (g - 1)) == 0 and P % 128 == 0 and
+               -(-w.num_query_tokens // w.num_seqs) * g >= 64)
+    P_eff = P
+    if rows128 and w.partition_tokens == 0:
+        B = w.block_size
+        step = B if B % 128 == 0 else (128 if 128 % B == 0 else 128 * B // math.gcd(128, B))
+        max_ctx = w.max_blocks_per_seq * B
+        tiles = -(-w.num_query_tokens // (128 // g)) * w.num_kv_heads
+        P2 = -(-max_ctx // step) * step
+        while P2 > P and tiles * -(-max_ctx // P2) < 2 * sms:
+            P2 = -(-(P2 // 2) // step) * step
+        P_eff = max(P, P2)
+    n_parts = -(-w.max_blocks_per_seq * w.block_size // P_eff)
+    kernel = ("pa_multi_query, 128-row tensor-core kernel" if rows128 else "pa_multi_query") if mq \
+        else "pa_decode"
+    kernel += " (partitions + split-K merge)" if n_parts > 1 else " (one partition per context)"
     # The binding roofline: HBM for the K/V stream unless the arithmetic needs
     # longer at its peak (many query rows per K/V byte): fp32 FMA on the SIMT
     # path, bf16/fp16 tensor cores on the tensor-core path (the library's
     # dispatch rule: 16-bit K/V, head_dim 128, partitions of 128k tokens, and
     # at least 4 query rows per kv head in an item).
-    g = w.num_q_heads // w.num_kv_heads
     tc_tokens = 1
     if mq:
         avg = -(-w.num_query_tokens // w.num_seqs)
@@ -534,7 +552,7 @@ def run_gpu(args):
                    "num_seqs": w.num_seqs, "num_q_heads": w.num_q_heads,
                    "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim,
                    "block_size": w.block_size, "num_blocks": w.num_blocks,
-                   "partition_tokens": P, "kv_read_bytes_per_step": kv_bytes,
+                   "partition_tokens": P_eff, "kv_read_bytes_per_step": kv_bytes,
                    **({"query_tokens": w.num_query_tokens} if mq else {}),
                    "layout": w.meta.get("layout", "paged"),
                    "l2": ("KV pool larger than L2 and a 256 MB L2 flush before every step "
