@@ -150,7 +150,8 @@ struct DecodeTile {
     static constexpr int kDup = kPasses >= kLpt ? 1 : kLpt / kPasses;   // lanes per logit
     static constexpr int kSubs = kTps / 16;           // 16-token bulk copies per tensor per stage
     static constexpr int kStageBytes = 2 * kTps * kRowBytes;
-    static constexpr int kStages = 65536 / kStageBytes;
+    // (E4M3 with one row per tile: a 32 KB ring, so that five CTAs fit on an SM)
+    static constexpr int kStages = (kFp8 && GT == 1) ? 32768 / kStageBytes : 65536 / kStageBytes;
     static constexpr int kItems = GT >= 4 ? 2 : 3;    // item slots in flight
     static constexpr int kQBytes = GT * D * sizeof(T);  // query rows of one item
     static constexpr int kMergeFloats = kConsumerWarps * GT * (D + 2);  // per item slot
@@ -171,6 +172,10 @@ struct DecodeTile {
     static_assert(kTps % 16 == 0 && kTps <= 64, "stage holds whole 16-token sub-blocks");
     static_assert(kPasses % 4 == 0 && kPasses * kTpp == kTps, "passes tile the stage");
     static_assert(kStages >= kConsumerWarps, "every consumer warp owns a stage");
+    // consumer warp w takes stages w, w + W, ...: a ring slot must always belong to
+    // the same warp, or a warp running ahead could take a parity wait on a slot one
+    // phase early
+    static_assert(kStages % kConsumerWarps == 0, "ring slots map to consumer warps");
     static_assert(GT > 1 || 3 * (kSmemBytes + 1024) <= 228 * 1024, "three CTAs per SM");
     static_assert((kVec * sizeof(T)) % 16 == 0, "a lane's query slice is whole 16-byte loads");
     using Slice = typename std::conditional<kFp8, uint2, uint4>::type;
