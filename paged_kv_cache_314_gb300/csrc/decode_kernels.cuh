@@ -150,8 +150,9 @@ struct DecodeTile {
     static constexpr int kDup = kPasses >= kLpt ? 1 : kLpt / kPasses;   // lanes per logit
     static constexpr int kSubs = kTps / 16;           // 16-token bulk copies per tensor per stage
     static constexpr int kStageBytes = 2 * kTps * kRowBytes;
-    // (E4M3 with one row per tile: a 32 KB ring, so that five CTAs fit on an SM)
-    static constexpr int kStages = (kFp8 && GT == 1) ? 32768 / kStageBytes : 65536 / kStageBytes;
+    // (one row per tile with 8- or 16-bit elements: a 32 KB ring, so that five CTAs
+    // -- twenty consumer warps -- share an SM, 160 KB of copies still in flight)
+    static constexpr int kStages = (kElem <= 2 && GT == 1) ? 32768 / kStageBytes : 65536 / kStageBytes;
     static constexpr int kItems = GT >= 4 ? 2 : 3;    // item slots in flight
     static constexpr int kQBytes = GT * D * sizeof(T);  // query rows of one item
     static constexpr int kMergeFloats = kConsumerWarps * GT * (D + 2);  // per item slot
