@@ -145,9 +145,12 @@ pa_status pa_copy_blocks_check(const int32_t* block_mapping, int num_pairs, uint
 /* pa_decode_partition_tokens -- tokens per split-K partition that pa_decode
  * uses for these sizes: partition_tokens itself when it is positive (it must
  * be a multiple of block_size), else the library's choice, a multiple of
- * block_size: 512 tokens, or 2048 when the query heads are grouped (4 to 16
- * per kv head) over 16-bit K/V with head_dim 128, the shapes decoded on the
- * tensor cores.  Returns -1 for invalid sizes. */
+ * block_size: 2048 tokens when the query heads are grouped (4 to 16 per kv
+ * head) over 16-bit or E4M3 K/V with head_dim 128, the shapes decoded on the
+ * tensor cores; otherwise 256 when max_blocks_per_seq * block_size <= 2048
+ * for 32- or 16-bit K/V (short contexts split into few partitions, so the
+ * last items of the persistent grid are a large share of the run: shorter
+ * items even it out), else 512.  Returns -1 for invalid sizes. */
 int pa_decode_partition_tokens(int num_q_heads, int num_kv_heads, int head_dim,
                                int max_blocks_per_seq, int block_size, pa_dtype dtype,
                                int partition_tokens);

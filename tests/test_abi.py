@@ -39,9 +39,12 @@ def test_every_declared_symbol_is_exported(lib):
 def test_host_only_entry_points(lib):
     assert pa.abi_version() == 1
     assert lib.pa_status_string(0) == b"ok"
-    assert pa.decode_partition_tokens(32, 32, 128, 128, 16, "f16") == 512
+    assert pa.decode_partition_tokens(32, 32, 128, 128, 16, "f16") == 256   # contexts <= 2048
+    assert pa.decode_partition_tokens(32, 32, 128, 129, 16, "f16") == 512
+    assert pa.decode_partition_tokens(32, 32, 128, 128, 16, "e4m3") == 512
     assert pa.decode_partition_tokens(64, 8, 128, 128, 16, "bf16") == 2048  # tensor-core shapes
-    assert pa.decode_partition_tokens(64, 8, 128, 128, 16, "f32") == 512
+    assert pa.decode_partition_tokens(64, 8, 128, 128, 16, "f32") == 256
+    assert pa.decode_partition_tokens(64, 8, 128, 256, 16, "f32") == 512
     assert pa.decode_partition_tokens(32, 32, 128, 128, 16, "f16", 24) == -1  # not a multiple of B
     assert pa.decode_partition_tokens(32, 32, 128, 128, 24, "f16") == -1      # B not a multiple of 16
     # one partition: only the 256 bytes of work counters
