@@ -203,6 +203,8 @@ MQ_PF = [
     ("bf16", 16, 2, 32, 512, [900, 64, 2500], [100, 64, 33]),             # 8 per kv head: 16 tokens
     ("f16", 32, 2, 128, 128, [1000, 300, 129], [20, 300, 9]),             # 16 per kv head: 8 tokens
     ("bf16", 8, 4, 16, 0, [4096, 513, 1], [512, 513, 1]),                 # 2 per kv head; whole-context chunks
+    ("bf16", 8, 2, 48, 768, [700, 1500, 97], [160, 90, 97]),              # 48-token blocks: 3 groups each
+    ("f16", 16, 4, 256, 0, [2000, 600, 257], [300, 64, 257]),             # 256-token blocks
 ]
 
 
