@@ -473,12 +473,19 @@ def run_gpu(args):
     rows128 = (mq and not fp8 and w.dtype in ("f16", "bf16") and w.head_dim == 128 and
                g <= 16 and (g & (g - 1)) == 0 and P % 128 == 0 and
                -(-w.num_query_tokens // w.num_seqs) * g >= 64)
+    tc_tokens = 1  # query tokens per item of the 16-row tensor-core kernel
+    if mq:
+        avg = -(-w.num_query_tokens // w.num_seqs)
+        while tc_tokens * 2 * g <= 16 and tc_tokens < avg:
+            tc_tokens *= 2
+    tc_mq = (mq and not fp8 and w.dtype in ("f16", "bf16") and w.head_dim == 128 and g <= 16 and
+             P % 128 == 0 and tc_tokens * g >= 4)
     P_eff = P
-    if rows128 and w.partition_tokens == 0:
+    if (rows128 or tc_mq) and w.partition_tokens == 0:
         B = w.block_size
         step = B if B % 128 == 0 else (128 if 128 % B == 0 else 128 * B // math.gcd(128, B))
         max_ctx = w.max_blocks_per_seq * B
-        tiles = -(-w.num_query_tokens // (128 // g)) * w.num_kv_heads
+        tiles = -(-w.num_query_tokens // (128 // g if rows128 else tc_tokens)) * w.num_kv_heads
         P2 = -(-max_ctx // step) * step
         while P2 > P and tiles * -(-max_ctx // P2) < 2 * sms:
             P2 = -(-(P2 // 2) // step) * step
@@ -492,11 +499,6 @@ def run_gpu(args):
     # path, bf16/fp16 tensor cores on the tensor-core path (the library's
     # dispatch rule: 16-bit K/V, head_dim 128, partitions of 128k tokens, and
     # at least 4 query rows per kv head in an item).
-    tc_tokens = 1
-    if mq:
-        avg = -(-w.num_query_tokens // w.num_seqs)
-        while tc_tokens * 2 * g <= 16 and tc_tokens < avg:
-            tc_tokens *= 2
     # (E4M3 caches: grouped-head decode, its codes widened to 16 bits in shared memory)
     tc_path = (w.head_dim == 128 and g <= 16 and P % 128 == 0 and
                ((fp8 and not mq and g >= 4) or

@@ -222,8 +222,8 @@ pa_status pa_decode(void* out, const void* q, const void* k_cache, const void* v
  * g heads) for 16-bit K/V with head_dim 128, g a power of two <= 16 and on
  * average at least 64 query rows per sequence and kv head (chunked prefill).
  * Partitions: pa_multi_query_partition_tokens(); with partition_tokens = 0
- * the 128-row kernel may use longer ones (down to the whole context) when its
- * query tiles alone give two work items per SM.  Workspace:
+ * the two tensor-core kernels use longer ones (up to the whole context) as
+ * long as their query tiles alone give two work items per SM.  Workspace:
  * pa_multi_query_workspace_size() bytes, with the same rules as pa_decode's.
  * Supported sizes and accumulation: as pa_decode.
  */

@@ -224,6 +224,41 @@ int log2_exact(int x) {
     return r;
 }
 
+// Multi-query calls on the tensor-core kernels with the default partitions:
+// a run of query tokens already gives many work items (p.tile_tokens tokens x
+// one kv head each), and an item's start-up (query rows, first MMAs) costs
+// more than on the SIMT kernel, so the context is split only as far as two
+// items per SM need (each split also costs partial states and their merge):
+// the partitions are lengthened, up to the whole context, never below the
+// default (so the workspace sized for it suffices).  Updates p's partition
+// length, partition count and partial-state pointers.
+pa_status lengthen_partitions(const AttnCall& a, DecodeParams& p, unsigned char* wsb) {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return PA_ERR_CUDA;
+    const long long P = a.partition_tokens;
+    const long long step = a.block_size % 128 == 0 ? a.block_size
+                           : 128 % a.block_size == 0 ? 128
+                                                     : 128LL * a.block_size / gcd_int(128, a.block_size);
+    const long long max_ctx = static_cast<long long>(a.max_blocks_per_seq) * a.block_size;
+    const long long tiles = (a.num_query_tokens + p.tile_tokens - 1) / p.tile_tokens *
+                            static_cast<long long>(a.num_kv_heads);
+    long long P2 = (max_ctx + step - 1) / step * step;
+    while (P2 > P && tiles * ((max_ctx + P2 - 1) / P2) < 2LL * sms)
+        P2 = ((P2 / 2) + step - 1) / step * step;
+    if (P2 > P && P2 <= 0x7fffffffLL) {
+        const int mp = max_parts_for(a.max_blocks_per_seq, a.block_size, static_cast<int>(P2));
+        const WsLayout w2 = ws_layout(a.num_query_tokens, a.num_q_heads, a.head_dim, mp);
+        p.partition_tokens = static_cast<int>(P2);
+        p.max_parts = mp;
+        p.ws_m = mp > 1 ? reinterpret_cast<float*>(wsb + w2.m_off) : nullptr;
+        p.ws_l = mp > 1 ? reinterpret_cast<float*>(wsb + w2.l_off) : nullptr;
+        p.ws_o = mp > 1 ? reinterpret_cast<float*>(wsb + w2.o_off) : nullptr;
+    }
+    return PA_OK;
+}
+
 // Shared by pa_decode and pa_multi_query once the arguments are checked.
 pa_status run_attention(const AttnCall& a) {
     const int P = a.partition_tokens;
@@ -321,32 +356,8 @@ pa_status run_attention(const AttnCall& a) {
             p.tile_heads = group;
             p.tile_tokens = 128 / group;
             if (a.partition_default) {
-                // A chunk's query tiles already give many work items: split the
-                // context only as far as two items per SM need (each split costs
-                // partial states and a merge).  Never shorter than the default,
-                // so the workspace sized for it suffices.
-                int dev = 0, sms = 0;
-                if (cudaGetDevice(&dev) != cudaSuccess ||
-                    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-                    return PA_ERR_CUDA;
-                const long long step = a.block_size % 128 == 0 ? a.block_size
-                                       : 128 % a.block_size == 0 ? 128
-                                                                 : 128LL * a.block_size / gcd_int(128, a.block_size);
-                const long long max_ctx = static_cast<long long>(a.max_blocks_per_seq) * a.block_size;
-                const long long tiles = (a.num_query_tokens + p.tile_tokens - 1) / p.tile_tokens *
-                                        static_cast<long long>(a.num_kv_heads);
-                long long P2 = (max_ctx + step - 1) / step * step;
-                while (P2 > P && tiles * ((max_ctx + P2 - 1) / P2) < 2LL * sms)
-                    P2 = ((P2 / 2) + step - 1) / step * step;
-                if (P2 > P && P2 <= 0x7fffffffLL) {
-                    const int mp = max_parts_for(a.max_blocks_per_seq, a.block_size, static_cast<int>(P2));
-                    const WsLayout w2 = ws_layout(a.num_query_tokens, a.num_q_heads, a.head_dim, mp);
-                    p.partition_tokens = static_cast<int>(P2);
-                    p.max_parts = mp;
-                    p.ws_m = mp > 1 ? reinterpret_cast<float*>(wsb + w2.m_off) : nullptr;
-                    p.ws_l = mp > 1 ? reinterpret_cast<float*>(wsb + w2.l_off) : nullptr;
-                    p.ws_o = mp > 1 ? reinterpret_cast<float*>(wsb + w2.o_off) : nullptr;
-                }
+                const pa_status e = lengthen_partitions(a, p, wsb);
+                if (e != PA_OK) return e;
             }
             return a.dtype == PA_BF16 ? launch_prefill_tc_bf16(p, map_k, map_v, map_q, st)
                                       : launch_prefill_tc_f16(p, map_k, map_v, map_q, st);
@@ -359,9 +370,14 @@ pa_status run_attention(const AttnCall& a) {
             p.head_tiles = a.num_kv_heads;
             p.tile_heads = group;
             p.tile_tokens = tc_tokens;
-            if (a.query_start != nullptr)
+            if (a.query_start != nullptr) {
+                if (a.partition_default) {
+                    const pa_status e = lengthen_partitions(a, p, wsb);
+                    if (e != PA_OK) return e;
+                }
                 return a.dtype == PA_BF16 ? launch_multi_query_tc_bf16(p, map_k, map_v, st)
                                           : launch_multi_query_tc_f16(p, map_k, map_v, st);
+            }
             return a.dtype == PA_BF16 ? launch_decode_tc_bf16(p, map_k, map_v, st)
                                       : launch_decode_tc_f16(p, map_k, map_v, st);
         }
