@@ -13,22 +13,24 @@
 // padded to N = 16 (g <= 16; padding rows are zero).
 //
 // The paging is unchanged: the block table is walked block by block in
-// order, every 16-token block of a stage is fetched through its table entry
-// ("PagedAttention" (compassingai.com) §5, §8) by a 2-D TMA tensor copy of a
-// [16 rows x 64 columns] box with 128-byte swizzle (the K/V pools are viewed
-// as [NB*Hkv*B rows x d columns]); the swizzled tiles are the MMA operands as
-// they land.
+// order, every 16-token group of a stage is fetched through its table entry
+// ("PagedAttention" (compassingai.com) §5, §8) by one 4-D TMA tensor copy
+// with 128-byte swizzle (the K/V pools viewed as {64 columns, 8 rows, 2
+// halves, rows/8}: the box is two 8-row blocks of [half][row][64 columns],
+// 4 KB); the swizzled tiles are the MMA operands as they land.  E4M3 caches:
+// one [16 rows x 128 B] byte box per group, widened in shared memory.
 //
 // Warp roles (416 threads, persistent, one CTA per SM):
 //   warp 0   producer: item cursor over context_lens (as in the SIMT path),
 //            block-table slice, TMA loads into a 3-stage ring (64 KB/stage;
-//            one [16 x 64] box per lane), bulk copy of the item's query rows
+//            the K boxes of groups 0-3), bulk copy of the item's query rows
 //            into a staging slot
 //   warp 1   allocates tensor memory, issues the MMAs (one thread); S and
 //            O^T are double-buffered in tensor memory (64 columns)
-//   warps 10-12 issue the other three quarters of each stage's TMA boxes (V
-//            half 0, K half 1, V half 1) from the producer's plan: one warp's
-//            TMA issue rate would bound the stage rate
+//   warps 10-12 issue the other boxes of each stage from the producer's plan
+//            (V groups 0-3, K groups 4-7, V groups 4-7): one warp's TMA issue
+//            rate would bound the stage rate.  E4M3 (480 threads): warp 10
+//            issues the V boxes, warps 11-14 widen the codes
 //   warps 2-9 two "teams" of four warps, each owning half of the heads:
 //            thread = row (token for S, head dimension for O), reading the
 //            accumulator lanes of its warp's quadrant
@@ -87,8 +89,8 @@ struct TcTile {
     static constexpr int kNumBars = kConvVBar + kStages;
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;  // tmem base, abort, team and converter flags
     static constexpr int kSmemBytes = kMiscOff + 32 + 1024;       // + alignment slack
-    // producer, MMA, two teams of 4 warps, three copy warps: the 32 TMA boxes of a
-    // stage are issued by four warps (the producer and warps 10-12, 8 boxes each),
+    // producer, MMA, two teams of 4 warps, three copy warps: the 16 TMA boxes of a
+    // stage are issued by four warps (the producer and warps 10-12, 4 boxes each),
     // since one warp's TMA issue rate would bound the stage rate
     static constexpr int kThreads = 416;
     // E4M3 caches: the producer and warp 10 issue the stage's 16 boxes (warps 11
@@ -430,10 +432,11 @@ __device__ __forceinline__ void tc_produce(const DecodeParams& p, const CUtensor
 }
 
 // A copy warp: for each stage, in ring order, it waits for the plan the
-// producer leaves once the slot's K (or V) half is free, and issues that
-// tensor's boxes of one 64-column half (one per lane, lanes 0-7 = the stage's
-// eight 16-token groups); they complete on fullK / fullV, whose arrivals the
-// producer posts with the expected bytes.
+// producer leaves once the slot's K (or V) half is free, and issues the boxes
+// of the plan entries it owns (lane r: 16-token group r; 16-bit caches: warp
+// 10 V groups 0-3, 11 K groups 4-7, 12 V groups 4-7, each box both 64-column
+// halves; E4M3: warp 10 every V box); they complete on fullK / fullV, whose
+// arrivals the producer posts with the expected bytes.
 template <typename T, bool kFp8>
 __device__ __forceinline__ void tc_copy(const DecodeParams& p, const CUtensorMap* map,
                                         unsigned char* sm, uint32_t base, bool is_v, int half) {
