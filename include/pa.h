@@ -260,8 +260,12 @@ pa_status pa_multi_query(void* out, const void* q, int num_query_tokens,
  *     PA_DECODE_STATIC_SCRATCH_BYTES, it returns PA_ERR_WORKSPACE_TOO_SMALL
  *     and enqueues nothing; use pa_decode with your own workspace then.
  *   - Set-up: the first call on a device, with that device current, looks up
- *     the array's device address once; make that first call before capturing
- *     the stream into a graph.
+ *     the array's device address once (again after the device's context
+ *     changes, e.g. after cudaDeviceReset, since the array moves with the
+ *     reloaded module); make that first call before capturing the stream
+ *     into a graph.
+ *   - Checks: every host check of pa_decode runs before anything is
+ *     enqueued; a call that fails them leaves the array untouched.
  *   - Sharing: every call uses the same array and it keeps the last call's
  *     contents; each call clears the part that must start at zero (the work
  *     counters) on `stream` first.  Calls whose work overlaps on the GPU (other

@@ -425,13 +425,15 @@ pa_status check_attention(const void* out, const void* q, const void* k_cache, c
 }  // namespace
 }  // namespace pa
 
-extern "C" pa_status pa_decode(void* out, const void* q, const void* k_cache, const void* v_cache,
-                               const int32_t* block_tables, int max_blocks_per_seq,
-                               const int32_t* context_lens, int num_seqs, int num_q_heads,
-                               int num_kv_heads, int head_dim, int block_size, int num_blocks,
-                               float scale, int partition_tokens, pa_dtype dtype, void* workspace,
-                               size_t workspace_bytes, uint32_t* d_err, pa_stream_t stream) {
-    using namespace pa;
+namespace pa {
+
+// Every host check of pa_decode except the workspace's: PA_OK when a call
+// with these arguments (and a large enough workspace) would be enqueued.
+pa_status check_decode(const void* out, const void* q, const void* k_cache, const void* v_cache,
+                       const int32_t* block_tables, int max_blocks_per_seq,
+                       const int32_t* context_lens, int num_seqs, int num_q_heads,
+                       int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                       float scale, int partition_tokens, pa_dtype dtype) {
     const pa_status c = check_attention(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq,
                                         context_lens, num_seqs, num_q_heads, num_kv_heads,
                                         head_dim, block_size, num_blocks, scale, partition_tokens,
@@ -442,6 +444,25 @@ extern "C" pa_status pa_decode(void* out, const void* q, const void* k_cache, co
     if (P <= 0) return PA_ERR_INVALID_ARG;
     if (num_seqs == 0) return PA_OK;
     if (static_cast<long long>(num_seqs) * num_q_heads > 0x7fffffffLL) return PA_ERR_UNSUPPORTED;
+    return PA_OK;
+}
+
+}  // namespace pa
+
+extern "C" pa_status pa_decode(void* out, const void* q, const void* k_cache, const void* v_cache,
+                               const int32_t* block_tables, int max_blocks_per_seq,
+                               const int32_t* context_lens, int num_seqs, int num_q_heads,
+                               int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                               float scale, int partition_tokens, pa_dtype dtype, void* workspace,
+                               size_t workspace_bytes, uint32_t* d_err, pa_stream_t stream) {
+    using namespace pa;
+    const pa_status c = check_decode(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq,
+                                     context_lens, num_seqs, num_q_heads, num_kv_heads, head_dim,
+                                     block_size, num_blocks, scale, partition_tokens, dtype);
+    if (c != PA_OK) return c;
+    if (num_seqs == 0) return PA_OK;
+    const int P = pa_decode_partition_tokens(num_q_heads, num_kv_heads, head_dim,
+                                             max_blocks_per_seq, block_size, dtype, partition_tokens);
     const AttnCall a{out, q, nullptr, num_seqs, k_cache, v_cache, nullptr, nullptr, block_tables,
                      max_blocks_per_seq, context_lens, num_seqs, num_q_heads, num_kv_heads,
                      head_dim, block_size, num_blocks, scale, P, false, dtype, workspace,

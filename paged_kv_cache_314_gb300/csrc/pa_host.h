@@ -40,4 +40,11 @@ inline pa_status ensure_smem(Kernel kernel, int bytes, std::atomic<uint64_t>& do
     return PA_OK;
 }
 
+// Every host check pa_decode makes before it looks at the workspace (decode.cu).
+pa_status check_decode(const void* out, const void* q, const void* k_cache, const void* v_cache,
+                       const int32_t* block_tables, int max_blocks_per_seq,
+                       const int32_t* context_lens, int num_seqs, int num_q_heads,
+                       int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                       float scale, int partition_tokens, pa_dtype dtype);
+
 }  // namespace pa

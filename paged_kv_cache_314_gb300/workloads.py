@@ -491,7 +491,7 @@ def custom(name: str, ctx: Sequence[int], *, dtype: str, num_q_heads: int, num_k
            head_dim: int, block_size: int, seed: int, pool_factor: float = 1.25,
            max_blocks_per_seq: Optional[int] = None, partition_tokens: int = 0,
            scale: Optional[float] = None, poison: bool = True, min_pool: int = 0,
-           query_lens: Optional[Sequence[int]] = None) -> Workload:
+           query_lens: Optional[Sequence[int]] = None, layout: str = "paged") -> Workload:
     B = block_size
     mb = max_blocks_per_seq
     if mb is None:
@@ -499,7 +499,7 @@ def custom(name: str, ctx: Sequence[int], *, dtype: str, num_q_heads: int, num_k
     return _independent(name, ctx, dtype=dtype, Hq=num_q_heads, Hkv=num_kv_heads, d=head_dim, B=B,
                         pool_factor=pool_factor, MB=mb, seed=seed, scale=scale,
                         partition_tokens=partition_tokens, poison=poison, min_pool=min_pool,
-                        query_lens=query_lens)
+                        query_lens=query_lens, layout=layout)
 
 
 E4M3_NAN = 0x7F  # poison code of E4M3 pools

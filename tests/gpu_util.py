@@ -99,28 +99,75 @@ def oracle_decode_parallel(q, kc, vc, tables, ctx, *, scale, dtype, threads=None
     return out, e
 
 
-def oracle_multi_query_parallel(q, query_start, kc, vc, tables, ctx, *, scale, dtype,
-                                threads=None):
-    """The oracle's multi-query attention, sequences split over host threads."""
-    S = ctx.shape[0]
-    threads = max(1, min(S, threads or os.cpu_count() or 4))
-    bounds = np.linspace(0, S, threads + 1).astype(int)
+def oracle_decode_heads_parallel(q, kc, vc, tables, ctx, *, scale, dtype, threads=None):
+    """The oracle's decode of every (sequence, query head), spread over host
+    threads one (sequence, head) at a time: the work of a few very long
+    sequences still reaches every core."""
+    S, Hq, d = q.shape
+    units = [(s, h) for s in range(S) for h in range(Hq)]
+    threads = max(1, min(len(units), threads or os.cpu_count() or 4))
     out = np.zeros(q.shape, np.float64)
 
-    def run(i):
-        a, b = bounds[i], bounds[i + 1]
-        if a == b:
-            return 0
-        r0, r1 = int(query_start[a]), int(query_start[b])
-        o, e = oracle.multi_query(np.ascontiguousarray(q[r0:r1]),
-                                  np.ascontiguousarray(query_start[a:b + 1] - r0), kc, vc,
-                                  np.ascontiguousarray(tables[a:b]),
-                                  np.ascontiguousarray(ctx[a:b]), scale=scale, dtype=dtype)
-        out[r0:r1] = o
+    def run(u):
+        s, h = u
+        o, e = oracle.decode_head(q, kc, vc, tables, ctx, s, h, scale=scale, dtype=dtype)
+        out[s, h] = o
         return e
 
     with cf.ThreadPoolExecutor(threads) as ex:
-        errs = list(ex.map(run, range(threads)))
+        errs = list(ex.map(run, units))
+    e = 0
+    for x in errs:
+        e |= x
+    return out, e
+
+
+def _row_chunks(query_start, ctx, max_blocks_per_seq, block_size, rows_per_unit):
+    """Work units of the multi-query oracle: (sequence, first row, end row,
+    context of the unit).  Row i of a sequence with L queries and n tokens
+    attends to its first n - L + i + 1 tokens, so rows [a, b) of a valid
+    sequence are the same attention as a sequence of b - a queries over its
+    first n - L + b tokens; sequences the oracle must reject stay whole."""
+    units = []
+    for s in range(len(ctx)):
+        q0, q1, n = int(query_start[s]), int(query_start[s + 1]), int(ctx[s])
+        L = q1 - q0
+        valid = q0 >= 0 and 0 <= L <= n <= max_blocks_per_seq * block_size
+        if not valid or L <= rows_per_unit:
+            units.append((s, 0, L, n))
+            continue
+        for a in range(0, L, rows_per_unit):
+            b = min(L, a + rows_per_unit)
+            units.append((s, a, b, n - L + b))
+    return units
+
+
+def oracle_multi_query_parallel(q, query_start, kc, vc, tables, ctx, *, scale, dtype,
+                                threads=None, rows_per_unit=16):
+    """The oracle's multi-query attention, (sequence, run of query rows) units
+    spread over host threads."""
+    S = ctx.shape[0]
+    qs = np.asarray(query_start)
+    if S == 0 or np.any(np.diff(qs) < 0) or qs[0] < 0 or qs[-1] > q.shape[0]:
+        return oracle.multi_query(q, query_start, kc, vc, tables, ctx, scale=scale, dtype=dtype)
+    units = _row_chunks(qs, ctx, tables.shape[1], kc.shape[2], rows_per_unit)
+    threads = max(1, min(len(units), threads or os.cpu_count() or 4))
+    out = np.zeros(q.shape, np.float64)
+
+    def run(u):
+        s, a, b, n = u
+        if a == b:
+            return 0
+        r0 = int(qs[s]) + a
+        o, e = oracle.multi_query(np.ascontiguousarray(q[r0:r0 + b - a]),
+                                  np.array([0, b - a], np.int32), kc, vc,
+                                  np.ascontiguousarray(tables[s:s + 1]),
+                                  np.array([n], np.int32), scale=scale, dtype=dtype)
+        out[r0:r0 + b - a] = o
+        return e
+
+    with cf.ThreadPoolExecutor(threads) as ex:
+        errs = list(ex.map(run, units))
     e = 0
     for x in errs:
         e |= x

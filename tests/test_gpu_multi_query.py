@@ -63,31 +63,12 @@ def test_speculative_verification_full_size():
     print("spec_verify", stats)
 
 
-def test_chunked_prefill_full_size_sampled():
-    w = wl.chunked_prefill()
-    d = upload(w)
-    out = out_f64(gpu_step(w, d))
-    assert int(d["d_err"].item()) == 0 and np.isfinite(out).all()
-    kc = to_numpy(d["k_cache"], w.dtype)
-    vc = to_numpy(d["v_cache"], w.dtype)
-    # every query token's K/V landed in its slot
-    for t in range(w.num_tokens):
-        b, o = divmod(int(w.slot_mapping[t]), w.block_size)
-        assert same_bits(kc[b, :, o], w.k_new[t]) and same_bits(vc[b, :, o], w.v_new[t])
-    # sampled rows: first, last and random query tokens of every sequence, all heads;
-    # row i of a sequence is one query over the first n - L + i + 1 tokens
-    rng = np.random.default_rng(6)
-    qs = w.query_start
-    for s in range(w.num_seqs):
-        n, L = int(w.context_lens[s]), int(qs[s + 1] - qs[s])
-        for i in sorted({0, L - 1, int(rng.integers(L)), int(rng.integers(L))}):
-            r = int(qs[s]) + i
-            ref, err = oracle.multi_query(w.q[r:r + 1], np.array([0, 1], np.int32), kc, vc,
-                                          w.block_tables[s:s + 1],
-                                          np.array([n - L + i + 1], np.int32), scale=w.scale,
-                                          dtype=w.dtype)
-            assert err == 0
-            assert_close(out[r:r + 1], ref, w.dtype, f"chunked_prefill s={s} i={i}")
+def test_chunked_prefill_full_size():
+    """All 4096 query rows x 32 heads of the chunked-prefill batch (8 sequences
+    appending 512-token chunks) against the oracle, which runs 16-row units of
+    a sequence per host thread."""
+    stats, _, _ = _check(wl.chunked_prefill())
+    print("chunked_prefill", stats)
 
 
 def test_one_query_per_sequence_matches_decode_bitwise():

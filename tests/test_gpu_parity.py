@@ -2,9 +2,9 @@
 
 kv_write and copy_blocks must match bit for bit over the whole pool (untouched
 blocks and poison included); decode must be within the tolerances of
-tests/gpu_util.TOL.  Every named workload runs at full size; the long-context
-ones are checked on sampled (sequence, head) outputs, which the oracle
-computes one at a time.
+tests/gpu_util.TOL.  Every named workload runs at full size and every output
+is compared, the long-context ones too (the oracle then runs one (sequence,
+head) per host thread).
 """
 import math
 
@@ -17,7 +17,8 @@ import paged_kv_cache_314_gb300 as pa
 from paged_kv_cache_314_gb300 import _build
 from paged_kv_cache_314_gb300 import workloads as wl
 
-from gpu_util import (assert_close, gpu_step, oracle_step, out_f64, same_bits, to_numpy, upload)
+from gpu_util import (assert_close, gpu_step, oracle_decode_heads_parallel, oracle_step, out_f64,
+                      same_bits, to_numpy, upload)
 
 pytestmark = pytest.mark.gpu
 
@@ -149,7 +150,10 @@ def test_named_full_size(name):
 
 
 @pytest.mark.parametrize("name", ["long_b16", "long_b128"])
-def test_long_context_sampled(name):
+def test_long_context_full(name):
+    """Every (sequence, head) output of the long-context batch (8 sequences of
+    32k-131k tokens, 512-token partitions and their merge) against the oracle,
+    which runs one (sequence, head) per host thread."""
     w = wl.by_name(name)
     d = upload(w)
     out = out_f64(gpu_step(w, d))
@@ -161,14 +165,33 @@ def test_long_context_sampled(name):
         slot = int(w.slot_mapping[t])
         b, o = divmod(slot, w.block_size)
         assert same_bits(kc[b, :, o], w.k_new[t]) and same_bits(vc[b, :, o], w.v_new[t])
-    rng = np.random.default_rng(5)
-    picks = [(s, int(rng.integers(w.num_q_heads))) for s in range(w.num_seqs)]
-    picks += [(int(np.argmax(w.context_lens)), 0), (int(np.argmin(w.context_lens)), w.num_q_heads - 1)]
-    ref = np.stack([oracle.decode_head(w.q, kc, vc, w.block_tables, w.context_lens, s, h,
-                                       scale=w.scale, dtype=w.dtype)[0] for s, h in picks])
-    got = np.stack([out[s, h] for s, h in picks])
-    assert np.isfinite(out).all()
-    assert_close(got, ref, w.dtype, name)
+    ref, err = oracle_decode_heads_parallel(w.q, kc, vc, w.block_tables, w.context_lens,
+                                            scale=w.scale, dtype=w.dtype)
+    assert err == 0
+    stats = assert_close(out, ref, w.dtype, name)
+    print(name, stats)
+
+
+def test_contiguous_layout_full_size():
+    """The contiguous comparator: the 7B-shaped batch with each sequence's
+    blocks consecutive in the pool (the layout the paged kernel is compared
+    against), every output against the oracle."""
+    w = wl.llama7b(layout="contiguous")
+    assert w.meta["layout"] == "contiguous"
+    t = w.block_tables
+    for s in range(w.num_seqs):  # consecutive physical blocks
+        nb = -(-int(w.context_lens[s]) // w.block_size)
+        assert np.all(np.diff(t[s, :nb]) == 1)
+    stats, _, _ = _check_step(w)
+    print("llama7b contiguous", stats)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+def test_contiguous_layout_grouped_heads(dtype):
+    """Contiguous layout on the tensor-core path (8 query heads per kv head)."""
+    w = wl.custom("gqa_contig", [1, 16, 17, 300, 1024, 2049], dtype=dtype, num_q_heads=32,
+                  num_kv_heads=4, head_dim=128, block_size=16, seed=230, layout="contiguous")
+    _check_step(w)
 
 
 # ---------------------------------------------------------------------------

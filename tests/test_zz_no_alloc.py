@@ -6,8 +6,9 @@ serving loop where cudaMalloc could synchronise the device.  For them the
 library offers one decode entry point whose scratch is a static device array
 inside the library.  This test calls it through the C ABI, twice in a row on
 the same array, and checks each result against pa_decode with a workspace the
-caller allocated, within the decode tolerance of the other GPU tests.  It also
-checks that sizes beyond the array are rejected before anything is launched.
+caller allocated and against the fp64 oracle, within the decode tolerance of
+the other GPU tests.  It also checks that sizes beyond the array, and
+arguments pa_decode rejects, are rejected before anything is launched.
 
 The file is named so that pytest collects it last.
 """
@@ -21,7 +22,7 @@ import paged_kv_cache_314_gb300 as pa
 from paged_kv_cache_314_gb300 import _build
 from paged_kv_cache_314_gb300 import workloads as wl
 
-from gpu_util import assert_close, out_f64, upload
+from gpu_util import assert_close, oracle_step, out_f64, upload
 
 pytestmark = pytest.mark.gpu
 
@@ -69,12 +70,15 @@ def test_static_workspace_matches_pa_decode(lib, case):
     pa.decode(ref, d["q"], d["k_cache"], d["v_cache"], d["block_tables"], d["context_lens"],
               w.scale, partition_tokens=P)
     torch.cuda.synchronize()
+    _, _, oracle_out, oracle_err = oracle_step(w)
+    assert oracle_err == 0
     for _ in range(2):  # the second call reuses the array the first one left behind
         out = torch.full_like(d["q"], float("nan"))
         assert _static_decode(lib, out, d, w, P) == 0
         torch.cuda.synchronize()
         assert int(d["d_err"].item()) == 0
-        assert_close(out_f64(out), out_f64(ref), w.dtype, f"static {case}")
+        assert_close(out_f64(out), out_f64(ref), w.dtype, f"static {case} vs pa_decode")
+        assert_close(out_f64(out), oracle_out, w.dtype, f"static {case} vs oracle")
 
 
 def test_sizes_beyond_the_static_array_are_rejected(lib):
@@ -86,3 +90,16 @@ def test_sizes_beyond_the_static_array_are_rejected(lib):
                                         vp(256), 4096, 64, 8, 128, 16, 100000, ctypes.c_float(0.1),
                                         128, 2, None, None)
     assert st == 3  # PA_ERR_WORKSPACE_TOO_SMALL, nothing enqueued
+
+
+def test_arguments_pa_decode_rejects_are_rejected_first(lib):
+    """A non-finite scale and a row count beyond 32 bits fail the host checks
+    of pa_decode: the call returns that status and enqueues nothing."""
+    vp = ctypes.c_void_p
+    args = [vp(256), vp(256), vp(256), vp(256), vp(256), 64, vp(256)]
+    st = lib.pa_decode_static_workspace(*args, 4, 8, 8, 128, 16, 1000, ctypes.c_float(float("nan")),
+                                        0, 2, None, None)
+    assert st == 1  # PA_ERR_INVALID_ARG
+    st = lib.pa_decode_static_workspace(*args, 1 << 26, 64, 8, 128, 16, 1000, ctypes.c_float(0.1),
+                                        0, 2, None, None)
+    assert st == 2  # PA_ERR_UNSUPPORTED: num_seqs * num_q_heads does not fit in 32 bits
