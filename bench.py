@@ -3,28 +3,33 @@
 
 A step is one pass of the whole hot path over one batch: copy_blocks (when the
 workload has copy-on-write pairs), kv_write of the step's new tokens, and
-paged decode attention (partition kernel + split-K merge).  The default
-workload is the LLaMA-7B-shaped decode batch (64 sequences, 32 heads,
-head_dim 128, fp16 K/V, 16-token blocks, context lengths uniform in
-[128, 2048], physical blocks randomly permuted, pool 1.1x the blocks needed).
+paged decode attention (with its split-K merge).  The default workload is the
+LLaMA-7B-shaped decode batch (64 sequences, 32 heads, head_dim 128, fp16 K/V,
+16-token blocks, context lengths uniform in [128, 2048], physical blocks
+randomly permuted, pool 1.1x the blocks needed); the same run also measures
+the LLaMA-13B-shaped batch and the 7B-shaped batch in the contiguous layout
+(the comparison the pages make), reported under "also".
 
 value = K+V bytes decode must read per step / device time per step (GB/s),
 with every input resident in HBM before timing starts; the KV pool (>1 GB) is
 larger than L2 and L2 is also flushed (256 MB write) before every step,
-outside the timed events.  e2e = the same bytes over a step that also copies
-that step's inputs from pinned host memory and reads the output back.
+outside the timed events.  The headline steps carry no events between their
+kernels; a second timed pass of the same steps puts events around each call
+to time the components and the attention call (the roofline).  e2e = the
+same bytes over a step made through pa_step_host: the step's inputs packed
+in pinned host memory, one host-to-device copy, the kernels, and the output
+copied back to pinned host memory, every step.
 
---impl reference times the fp64 CPU oracle on the same workload (kv_write and
-decode of the whole batch per step, host threads), the baseline arm.
+--impl reference times the fp64 CPU oracle on the same workload (copy_blocks,
+kv_write and attention of a bounded sample of query rows per step, host
+threads), the baseline arm.
 """
 from __future__ import annotations
 
 import argparse
-import hashlib
 import json
 import math
 import os
-import re
 import subprocess
 import sys
 import time
@@ -38,6 +43,9 @@ if ROOT not in sys.path:
 METRIC = "paged decode attn KV-read GB/s (fraction of GB300 HBM peak); seq-heads/s"
 L2_FLUSH_BYTES = 256 << 20
 L2_BYTES = 129 << 20  # GB300 L2
+# GB300 HBM3e nominal bandwidth (8 TB/s class; the pages' target is stated
+# against "about 8 TB/s").  Reported beside the measured copy bandwidth.
+NOMINAL_HBM_GBS = 8000.0
 
 WORKLOAD_TEXT = {
     "llama7b": "LLaMA-7B-shaped single-layer decode: 64 seqs, 32 q/kv heads, head_dim 128, fp16 "
@@ -66,27 +74,42 @@ WORKLOAD_TEXT = {
                        "tokens; GQA 32 q / 8 kv heads, head_dim 128, bf16, block 16",
 }
 
+# Measured alongside the default (7B-shaped) workload, same method.
+ALSO = (("llama13b", "paged"), ("llama7b", "contiguous"))
+
 # fp32 FMA lanes per SM (sm_100 family): the SIMT path's arithmetic roofline is
 # SMs x 128 lanes x 2 flop x the maximum SM clock.
 FP32_LANES_PER_SM = 128
+TC_KERNELS = ("tc_grouped", "tc_grouped_fp8", "tc_128_rows")
+
+
+def _measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f)
+    except (OSError, ValueError):
+        return None
+
+
+def _hbm_peak():
+    d = _measured_peaks()
+    if d and "hbm_gbs" in d:
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
 
 
 def _tensor_peak():
     """Dense bf16 tensor peak: the measured burst figure (the attention call is
     timed on its own, well under a second)."""
-    try:
-        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
-            return float(json.load(f)["bf16_tflops"]), "measured"
-    except (OSError, ValueError, KeyError):
-        return 1900.0, "fallback"
+    d = _measured_peaks()
+    if d and "bf16_tflops" in d:
+        return float(d["bf16_tflops"]), "measured"
+    return 1900.0, "fallback"
 
 
 def _alu_peak_tflops(sm_count):
-    try:
-        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
-            mhz = float(json.load(f).get("sm_max_mhz", 2070.0))
-    except (OSError, ValueError):
-        mhz = 2070.0
+    d = _measured_peaks() or {}
+    mhz = float(d.get("sm_max_mhz", 2070.0))
     return sm_count * FP32_LANES_PER_SM * 2 * mhz * 1e6 / 1e12
 
 
@@ -147,37 +170,40 @@ def _dist_env():
     return ws, rank, local
 
 
-def _peaks():
-    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+def _host_cpus():
+    """Host core counts as the OS reports them three ways."""
+    out = {"os_cpu_count": os.cpu_count()}
+    try:
+        out["sched_getaffinity"] = len(os.sched_getaffinity(0))
+    except (AttributeError, OSError):
+        out["sched_getaffinity"] = None
+    try:
+        out["nproc"] = int(subprocess.run(["nproc"], capture_output=True, text=True,
+                                          timeout=10).stdout.strip())
+    except (OSError, ValueError, subprocess.SubprocessError):
+        out["nproc"] = None
+    return out
+
+
+def _ncu_record(config: str):
+    """The committed ncu summary of this workload's attention kernel
+    (profiles/decode_<config>_ncu.json, written by
+    paged_kv_cache_314_gb300.ncu_summary from ncu's CSV), if it was taken on
+    the current kernel sources; else None."""
+    from paged_kv_cache_314_gb300 import ncu_summary
+    path = os.path.join(ROOT, "profiles", f"decode_{config}_ncu.json")
     try:
         with open(path) as f:
-            d = json.load(f)
-        return float(d["hbm_gbs"]), "measured"
-    except Exception:
-        return 6800.0, "fallback"
-
-
-def _kernel_source_hash():
-    csrc = os.path.join(ROOT, "paged_kv_cache_314_gb300", "csrc")
-    h = hashlib.sha256()
-    for name in ("decode_kernels.cuh", "decode_tc.cuh", "prefill_tc.cuh", "tc_ptx.cuh", "pa_device.cuh"):
-        with open(os.path.join(csrc, name), "rb") as f:
-            h.update(f.read())
-    return h.hexdigest()[:16]
-
-
-def _ncu_traffic(config: str):
-    """DRAM bytes per decode launch from the committed ncu summary, if it was
-    taken on the current kernel sources (else None)."""
-    path = os.path.join(ROOT, "profiles", f"decode_{config}_ncu.md")
-    if not os.path.exists(path):
+            rec = json.load(f)
+    except (OSError, ValueError):
         return None
-    text = open(path).read()
-    m = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]+)", text)
-    t = re.search(r"traffic_bytes_per_launch:\s*([0-9]+)", text)
-    if not m or not t or m.group(1) != _kernel_source_hash():
+    try:
+        if rec.get("kernel_source_sha256_16") != ncu_summary.kernel_source_hash(
+                rec["kernel_sources"]):
+            return None
+    except (KeyError, OSError):
         return None
-    return int(t.group(1))
+    return rec
 
 
 class ClockSampler:
@@ -270,13 +296,13 @@ def _to_torch(a, dtype):
     return torch.from_numpy(np.ascontiguousarray(a))
 
 
-def _cpu_baseline(w, cpu_seconds=16.0, max_wall_s=20.0):
-    """The oracle, as it stands, on this workload's attention on all host cores:
-    query rows (all heads) in order, passes repeated until about cpu_seconds
-    of CPU work (threads x wall time) are done.  GB/s-equivalent: the step's
-    K/V bytes x (tokens attended by the rows done / by all rows) / time."""
+def _oracle_pass(w, threads, cpu_seconds, max_wall_s):
+    """The oracle on this workload's attention: query rows (all heads) in
+    order on ``threads`` host threads, passes repeated until about
+    cpu_seconds of CPU work (threads x wall time) are done.  GB/s-equivalent:
+    the step's K/V bytes x (tokens attended by the rows done / by all rows)
+    / time."""
     import concurrent.futures as cf
-    threads = os.cpu_count() or 1
     kc, vc = w.k_cache, w.v_cache
     rows = _rows(w)
     total = max(1, sum(n for _, _, n in rows))
@@ -294,18 +320,295 @@ def _cpu_baseline(w, cpu_seconds=16.0, max_wall_s=20.0):
             n_rows += len(batch)
     dt = time.perf_counter() - t0
     eq = kv_bytes * done / total
+    return eq / dt / 1e9, n_rows, eq, dt, len(rows)
+
+
+def _cpu_baseline(w, cpu_seconds=16.0, max_wall_s=20.0, single_seconds=4.0):
+    """The oracle, as it stands, on all host cores and on one."""
+    threads = os.cpu_count() or 1
+    v, n_rows, eq, dt, nrows = _oracle_pass(w, threads, cpu_seconds, max_wall_s)
+    v1, n1, eq1, dt1, _ = _oracle_pass(w, 1, single_seconds, single_seconds)
     unit = "sequences" if w.query_start is None else "query rows"
-    return {"value": eq / dt / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
-            "sample": f"attention of {n_rows} {unit} ({n_rows / len(rows):.3f} passes over the "
-                      f"step's {len(rows)}; {eq / 1e6:.0f} MB of the step's K/V bytes in "
+    return {"value": v, "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "sample": f"attention of {n_rows} {unit} ({n_rows / nrows:.3f} passes over the "
+                      f"step's {nrows}; {eq / 1e6:.0f} MB of the step's K/V bytes in "
                       f"proportion to the tokens attended), fp64 C oracle, one row per host "
-                      f"thread, {dt:.1f} s wall"}
+                      f"thread, {dt:.1f} s wall",
+            "single_thread": {"value": v1, "unit": "GB/s", "cores": 1,
+                              "sample": f"{n1} {unit}, {eq1 / 1e6:.0f} MB, {dt1:.1f} s wall"},
+            "host_cpus": _host_cpus()}
+
+
+def _plan(pa, w):
+    fp8 = w.kv_dtype == "e4m3"
+    return pa.attention_plan(w.num_seqs, w.num_q_heads, w.num_kv_heads, w.head_dim,
+                             w.max_blocks_per_seq, w.block_size, w.num_blocks, w.dtype,
+                             w.partition_tokens,
+                             num_query_tokens=w.num_query_tokens if w.query_start is not None
+                             else None, kv_dtype="e4m3" if fp8 else None)
+
+
+def _measure(args, name, layout, dev, dist, ws_world):
+    """Time one workload: headline steps, component pass and end-to-end steps.
+    Returns the figures of its JSON line."""
+    import torch
+    import paged_kv_cache_314_gb300 as pa
+    from paged_kv_cache_314_gb300 import workloads as wl
+
+    kw = {"partition_tokens": args.partition} if args.partition is not None else {}
+    if layout != "paged":
+        kw["layout"] = layout
+    w = wl.by_name(name, poison=False, **kw)
+    mq = w.query_start is not None
+    fp8 = w.kv_dtype == "e4m3"
+    plan = _plan(pa, w)
+    dt = w.dtype
+    pool = (lambda a: torch.from_numpy(a)) if fp8 else (lambda a: _to_torch(a, dt))
+    d = {k: v.to(dev) for k, v in {
+        "q": _to_torch(w.q, dt), "k_cache": pool(w.k_cache),
+        "v_cache": pool(w.v_cache), "k_new": _to_torch(w.k_new, dt),
+        "v_new": _to_torch(w.v_new, dt), "block_tables": torch.from_numpy(w.block_tables),
+        "context_lens": torch.from_numpy(w.context_lens),
+        "slot_mapping": torch.from_numpy(w.slot_mapping),
+        "block_mapping": torch.from_numpy(w.block_mapping.reshape(-1, 2)),
+        **({"query_start": torch.from_numpy(w.query_start)} if mq else {}),
+        **({"k_scale": torch.from_numpy(w.k_scale), "v_scale": torch.from_numpy(w.v_scale)}
+           if fp8 else {})}.items()}
+    out = torch.empty_like(d["q"])
+    if mq:
+        ws_bytes = pa.multi_query_workspace_size(w.num_query_tokens, w.num_q_heads,
+                                                 w.num_kv_heads, w.head_dim, w.max_blocks_per_seq,
+                                                 w.block_size, w.dtype, w.partition_tokens)
+    else:
+        ws_bytes = pa.decode_workspace_size(w.num_seqs, w.num_q_heads, w.num_kv_heads, w.head_dim,
+                                            w.max_blocks_per_seq, w.block_size,
+                                            "e4m3" if fp8 else w.dtype, w.partition_tokens)
+    workspace = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)
+    d_err = torch.zeros(1, dtype=torch.int32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(dd, ev=None):
+        """copy_blocks, kv_write, attention; ev: events recorded after each call."""
+        if w.num_pairs and fp8:
+            pa.copy_blocks_fp8(dd["k_cache"], dd["v_cache"], dd["k_scale"], dd["v_scale"],
+                               dd["block_mapping"], d_err=d_err)
+        elif w.num_pairs:
+            pa.copy_blocks(dd["k_cache"], dd["v_cache"], dd["block_mapping"], d_err=d_err)
+        if ev is not None:
+            ev[1].record(stream)
+        if w.num_tokens and fp8:
+            pa.kv_write_fp8(dd["k_new"], dd["v_new"], dd["k_cache"], dd["v_cache"],
+                            dd["k_scale"], dd["v_scale"], dd["slot_mapping"], d_err=d_err)
+        elif w.num_tokens:
+            pa.kv_write(dd["k_new"], dd["v_new"], dd["k_cache"], dd["v_cache"],
+                        dd["slot_mapping"], d_err=d_err)
+        if ev is not None:
+            ev[2].record(stream)
+        if fp8:
+            pa.decode_fp8(out, dd["q"], dd["k_cache"], dd["v_cache"], dd["k_scale"],
+                          dd["v_scale"], dd["block_tables"], dd["context_lens"], w.scale,
+                          partition_tokens=w.partition_tokens, workspace=workspace, d_err=d_err)
+        elif mq:
+            pa.multi_query(out, dd["q"], dd["query_start"], dd["k_cache"], dd["v_cache"],
+                           dd["block_tables"], dd["context_lens"], w.scale,
+                           partition_tokens=w.partition_tokens, workspace=workspace, d_err=d_err)
+        else:
+            pa.decode(out, dd["q"], dd["k_cache"], dd["v_cache"], dd["block_tables"],
+                      dd["context_lens"], w.scale, partition_tokens=w.partition_tokens,
+                      workspace=workspace, d_err=d_err)
+
+    def new_events(n):
+        return [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step(d)
+    torch.cuda.synchronize()
+    if int(d_err.item()) != 0:
+        raise RuntimeError(f"{name}: device error word {int(d_err.item())} during warm-up")
+
+    # ---- headline: K whole steps, no events between their kernels
+    ev = [new_events(2) for _ in range(args.steps)]
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(dev.index) as clk:
+        t_wall = time.perf_counter()
+        for i in range(args.steps):
+            flush.zero_()
+            ev[i][0].record(stream)
+            step(d)
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        t_wall = time.perf_counter() - t_wall
+    if dist is not None:
+        dist.barrier()
+    ms_per_step = float(np.mean([a.elapsed_time(b) for a, b in ev]))
+
+    # ---- components: the same steps with events around each call
+    evc = [new_events(4) for _ in range(args.steps)]
+    torch.cuda.synchronize()
+    for i in range(args.steps):
+        flush.zero_()
+        evc[i][0].record(stream)
+        step(d, evc[i])
+        evc[i][3].record(stream)
+    torch.cuda.synchronize()
+    copy_ms = float(np.mean([e[0].elapsed_time(e[1]) for e in evc]))
+    kvw_ms = float(np.mean([e[1].elapsed_time(e[2]) for e in evc]))
+    dec_ms = float(np.mean([e[2].elapsed_time(e[3]) for e in evc]))
+    ms_per_step, dec_ms = _max_over_ranks([ms_per_step, dec_ms], dist, dev)
+
+    # ---- end to end through pa_step_host: inputs packed in pinned host memory,
+    # one host-to-device copy, the kernels, the output back to pinned host memory
+    dims = pa.StepDims(w.num_seqs, w.num_query_tokens if mq else 0, w.num_tokens, w.num_pairs,
+                       w.num_q_heads, w.num_kv_heads, w.head_dim, w.block_size, w.num_blocks,
+                       w.max_blocks_per_seq, pa.DTYPE_CODE[d["q"].dtype])
+    total, offs = pa.step_layout(dims)
+    host_in = torch.zeros(total, dtype=torch.uint8, pin_memory=True)
+    for k in pa.STEP_INPUTS:
+        if k in d and d[k].numel() and not (k == "query_start" and not mq):
+            n = d[k].numel() * d[k].element_size()
+            host_in[offs[k]:offs[k] + n].copy_(d[k].reshape(-1).view(torch.uint8).cpu())
+    dev_stage = torch.empty(total, dtype=torch.uint8, device=dev)
+    host_out = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    h2d = total
+    d2h = host_out.numel() * host_out.element_size()
+    e2e_ms = []
+    for i in range(args.warmup + args.steps):
+        flush.zero_()
+        e0, e1 = new_events(2)
+        e0.record(stream)
+        pa.step_host(dims, host_in, dev_stage, host_out, out, d["k_cache"], d["v_cache"], w.scale,
+                     w.partition_tokens, workspace, d_err,
+                     k_scale=d.get("k_scale"), v_scale=d.get("v_scale"))
+        e1.record(stream)
+        torch.cuda.synchronize()
+        if i >= args.warmup:
+            e2e_ms.append(e0.elapsed_time(e1))
+    e2e_avg = _max_over_ranks([float(np.mean(e2e_ms))], dist, dev)[0]
+    if int(d_err.item()) != 0:
+        raise RuntimeError(f"{name}: device error word {int(d_err.item())} during timing")
+
+    # ---- roofline of the attention call
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    kv_bytes = w.kv_read_bytes()
+    unique_bytes = w.kv_unique_read_bytes() if w.num_pairs or "gqa" in w.name else kv_bytes
+    peak, peak_kind = _hbm_peak()
+    flops = 4 * w.head_dim * w.num_q_heads * sum(n for _, _, n in _rows(w))
+    tensor_peak, tensor_kind = _tensor_peak()
+    alu_peak = _alu_peak_tflops(sms)
+    tc_path = plan["kernel"] in TC_KERNELS
+    tensor_bound = tc_path and flops / (tensor_peak * 1e12) > unique_bytes / (peak * 1e9)
+    alu_bound = not tc_path and flops / (alu_peak * 1e12) > unique_bytes / (peak * 1e9)
+    ncu = _ncu_record(name + ("" if layout == "paged" else "_" + layout))
+    traffic = ncu.get("traffic_bytes_per_launch") if ncu else None
+    kernel = f"{'pa_multi_query' if mq else 'pa_decode_fp8' if fp8 else 'pa_decode'}: " \
+             f"{plan['kernel']} kernel, merge {plan['merge']}, {plan['launches']} launch(es)"
+    hbm_ach = unique_bytes / (dec_ms * 1e-3) / 1e9
+    common = {"kernel": kernel, "avg_launch_ms": round(dec_ms, 5), "traffic": traffic,
+              "l2_hit_rate_pct": round(ncu["l2_hit_rate_pct"], 2)
+              if ncu and ncu.get("l2_hit_rate_pct") is not None else None,
+              "traffic_source": "profiles/decode_*_ncu.json (ncu dram__bytes_read.sum + "
+                                "dram__bytes_write.sum per launch, same kernel sources)"
+              if ncu else "no capture on the current kernel sources"}
+    if tensor_bound or alu_bound:
+        pk = tensor_peak if tensor_bound else round(alu_peak, 1)
+        ach = flops / (dec_ms * 1e-3) / 1e12
+        roof = {"bound": "tensor" if tensor_bound else "alu", "achieved": round(ach, 3),
+                "peak": pk, "unit": "TFLOP/s", "frac": round(ach / pk, 4),
+                "peak_source": f"{tensor_kind} bf16_tflops (fp16 MMA runs at the bf16 rate)"
+                if tensor_bound else
+                f"derived: {sms} SMs x {FP32_LANES_PER_SM} fp32 FMA lanes x 2 flop x maximum "
+                "SM clock (MEASURED_PEAKS sm_max_mhz)",
+                "flops": "4 x head_dim per (query row, head, token attended)",
+                "algorithmic_flops_per_launch": int(flops),
+                "hbm_achieved_gbs": round(hbm_ach, 2), **common}
+    else:
+        roof = {"bound": "hbm", "achieved": round(hbm_ach, 2), "peak": peak, "unit": "GB/s",
+                "frac": round(hbm_ach / peak, 4), "peak_source": f"{peak_kind} hbm_gbs",
+                "frac_of_nominal": round(hbm_ach / NOMINAL_HBM_GBS, 4),
+                "nominal_peak_gbs": NOMINAL_HBM_GBS,
+                "bytes": "distinct K/V bytes read (shared prefix blocks once)"
+                         if unique_bytes != kv_bytes else "K/V bytes of the cached tokens",
+                "logical_achieved": round(kv_bytes / (dec_ms * 1e-3) / 1e9, 2),
+                "algorithmic_bytes_per_launch": unique_bytes,
+                "logical_bytes_per_launch": kv_bytes,
+                "attn_tflops": round(flops / (dec_ms * 1e-3) / 1e12, 3), **common}
+    value = _weak_value(ws_world, kv_bytes, ms_per_step)
+    launches = (1 if w.num_pairs else 0) + (1 if w.num_tokens else 0) + plan["launches"]
+    res = {
+        "w": w, "plan": plan, "value": value, "ms_per_step": ms_per_step, "dec_ms": dec_ms,
+        "kv_bytes": kv_bytes, "unique_bytes": unique_bytes, "roofline": roof,
+        "hbm_frac": value / ws_world / peak, "hbm_frac_of_nominal": value / ws_world / NOMINAL_HBM_GBS,
+        "seq_heads_per_s": ws_world * w.num_seqs * w.num_q_heads / (ms_per_step * 1e-3),
+        "e2e": {"value": round(_weak_value(ws_world, kv_bytes, e2e_avg), 2), "unit": "GB/s",
+                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+                "ms_per_step": round(e2e_avg, 5),
+                "path": "pa_step_host (C ABI): packed pinned host inputs, one H2D copy, the "
+                        "step's kernels, D2H of out"},
+        "components": {
+            "copy_blocks": {"ms": round(copy_ms, 5), "pairs": w.num_pairs,
+                            "gb_per_s": round(4 * w.num_pairs * w.num_kv_heads * w.block_size *
+                                              w.head_dim * w.kv_elem_bytes / max(copy_ms, 1e-9)
+                                              / 1e6, 2) if w.num_pairs else None,
+                            "bytes": "K and V blocks read + written"},
+            "kv_write": {"ms": round(kvw_ms, 5), "tokens": w.num_tokens,
+                         "gb_per_s": round(2 * w.num_tokens * w.num_kv_heads * w.head_dim *
+                                           (w.elem_bytes + w.kv_elem_bytes) / max(kvw_ms, 1e-9)
+                                           / 1e6, 2),
+                         "bytes": "K and V rows read + written"},
+            "attention": {"ms": round(dec_ms, 5)},
+            "timing": "a second timed pass of the same steps with events around each call "
+                      "(each pair of events adds ~2 us of its own)"},
+        "gpu_launches": launches * args.steps,
+        "clocks": clk.summary(),
+        "wall_s_timed_region": round(t_wall, 4),
+        "memory": {k: (round(v, 5) if isinstance(v, float) else v)
+                   for k, v in wl.memory_stats(w.block_tables, w.context_lens, w.block_size,
+                                               w.max_blocks_per_seq).items()},
+    }
+    del d, out, workspace, flush, dev_stage
+    torch.cuda.empty_cache()
+    return res
+
+
+def _config(w, res, args, ws, name):
+    mq = w.query_start is not None
+    return {"workload": WORKLOAD_TEXT.get(name, name), "name": name,
+            "num_seqs": w.num_seqs, "num_q_heads": w.num_q_heads,
+            "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim,
+            "block_size": w.block_size, "num_blocks": w.num_blocks,
+            "partition_tokens": res["plan"]["partition_tokens"],
+            "kv_read_bytes_per_step": res["kv_bytes"],
+            **({"query_tokens": w.num_query_tokens} if mq else {}),
+            "layout": w.meta.get("layout", "paged"),
+            "l2": ("KV pool larger than L2 and a 256 MB L2 flush before every step "
+                   "(outside the timed events)")
+                  if 2 * w.k_cache.nbytes > L2_BYTES else
+                  "a 256 MB L2 flush before every step (outside the timed events); the "
+                  "KV pool itself fits in L2",
+            "parallelism": f"weak: {ws} independent replicas of the batch, one per GPU"}
+
+
+def _sub_line(res, args, ws, name):
+    w = res["w"]
+    return {"value": round(res["value"], 2), "unit": "GB/s",
+            "ms_per_step": round(res["ms_per_step"], 5),
+            "hbm_frac": round(res["hbm_frac"], 4),
+            "hbm_frac_of_nominal": round(res["hbm_frac_of_nominal"], 4),
+            "seq_heads_per_s": round(res["seq_heads_per_s"], 1),
+            "dtype": "e4m3" if w.kv_dtype == "e4m3" else w.dtype,
+            "config": _config(w, res, args, ws, name), "roofline": res["roofline"],
+            "e2e": res["e2e"], "components": res["components"], "clocks": res["clocks"],
+            "memory": res["memory"]}
 
 
 def run_gpu(args):
     import torch
     import paged_kv_cache_314_gb300 as pa
-    from paged_kv_cache_314_gb300 import _build, workloads as wl
+    from paged_kv_cache_314_gb300 import _build
 
     ws, rank, local = _dist_env()
     torch.cuda.set_device(local)
@@ -320,282 +623,49 @@ def run_gpu(args):
         dist.barrier()
     pa.load()
 
-    kw = {"partition_tokens": args.partition} if args.partition is not None else {}
-    if args.layout != "paged":
-        kw["layout"] = args.layout
-    w = wl.by_name(args.config, poison=False, **kw)
-    mq = w.query_start is not None
-    fp8 = w.kv_dtype == "e4m3"
-    if fp8:
-        P = pa.decode_partition_tokens(w.num_q_heads, w.num_kv_heads, w.head_dim,
-                                       w.max_blocks_per_seq, w.block_size, "e4m3",
-                                       w.partition_tokens)
-    elif mq:
-        P = pa.multi_query_partition_tokens(w.num_query_tokens, w.num_q_heads, w.num_kv_heads,
-                                            w.head_dim, w.max_blocks_per_seq, w.block_size,
-                                            w.dtype, w.partition_tokens)
-    else:
-        P = pa.decode_partition_tokens(w.num_q_heads, w.num_kv_heads, w.head_dim,
-                                       w.max_blocks_per_seq, w.block_size, w.dtype,
-                                       w.partition_tokens)
-    dt = w.dtype
-    pool = (lambda a: torch.from_numpy(a)) if fp8 else (lambda a: _to_torch(a, dt))
-    d = {k: v.to(dev) for k, v in {
-        "q": _to_torch(w.q, dt), "k_cache": pool(w.k_cache),
-        "v_cache": pool(w.v_cache), "k_new": _to_torch(w.k_new, dt),
-        "v_new": _to_torch(w.v_new, dt), "block_tables": torch.from_numpy(w.block_tables),
-        "context_lens": torch.from_numpy(w.context_lens),
-        "slot_mapping": torch.from_numpy(w.slot_mapping),
-        "block_mapping": torch.from_numpy(w.block_mapping.reshape(-1, 2)),
-        **({"query_start": torch.from_numpy(w.query_start)} if mq else {}),
-        **({"k_scale": torch.from_numpy(w.k_scale), "v_scale": torch.from_numpy(w.v_scale)}
-           if fp8 else {})}.items()}
-    out = torch.empty_like(d["q"])
-    if fp8:
-        workspace = torch.zeros(pa.decode_workspace_size(
-            w.num_seqs, w.num_q_heads, w.num_kv_heads, w.head_dim, w.max_blocks_per_seq,
-            w.block_size, "e4m3", w.partition_tokens), dtype=torch.uint8, device=dev)
-    elif mq:
-        workspace = pa.multi_query_workspace(d["q"], d["k_cache"], d["block_tables"],
-                                             w.partition_tokens)
-    else:
-        workspace = pa.decode_workspace(d["q"], d["k_cache"], d["block_tables"],
-                                        w.partition_tokens)
-    d_err = torch.zeros(1, dtype=torch.int32, device=dev)
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
-    stream = torch.cuda.current_stream(dev)
-    max_parts = math.ceil(w.max_blocks_per_seq * w.block_size / P)
-    launches_per_step = (1 if w.num_pairs else 0) + (1 if w.num_tokens else 0) + 1 + (
-        1 if max_parts > 1 else 0)
-
-    def step(dd, ev_mid=None):
-        """copy_blocks, kv_write, decode; ev_mid: events after copy_blocks and after kv_write."""
-        if w.num_pairs and fp8:
-            pa.copy_blocks_fp8(dd["k_cache"], dd["v_cache"], dd["k_scale"], dd["v_scale"],
-                               dd["block_mapping"], d_err=d_err)
-        elif w.num_pairs:
-            pa.copy_blocks(dd["k_cache"], dd["v_cache"], dd["block_mapping"], d_err=d_err)
-        if ev_mid is not None:
-            ev_mid[0].record(stream)
-        if w.num_tokens and fp8:
-            pa.kv_write_fp8(dd["k_new"], dd["v_new"], dd["k_cache"], dd["v_cache"],
-                            dd["k_scale"], dd["v_scale"], dd["slot_mapping"], d_err=d_err)
-        elif w.num_tokens:
-            pa.kv_write(dd["k_new"], dd["v_new"], dd["k_cache"], dd["v_cache"],
-                        dd["slot_mapping"], d_err=d_err)
-        if ev_mid is not None:
-            ev_mid[1].record(stream)
-        if fp8:
-            pa.decode_fp8(out, dd["q"], dd["k_cache"], dd["v_cache"], dd["k_scale"],
-                          dd["v_scale"], dd["block_tables"], dd["context_lens"], w.scale,
-                          partition_tokens=w.partition_tokens, workspace=workspace, d_err=d_err)
-        elif mq:
-            pa.multi_query(out, dd["q"], dd["query_start"], dd["k_cache"], dd["v_cache"],
-                           dd["block_tables"], dd["context_lens"], w.scale,
-                           partition_tokens=w.partition_tokens, workspace=workspace, d_err=d_err)
-        else:
-            pa.decode(out, dd["q"], dd["k_cache"], dd["v_cache"], dd["block_tables"],
-                      dd["context_lens"], w.scale, partition_tokens=w.partition_tokens,
-                      workspace=workspace, d_err=d_err)
-
-    for _ in range(args.warmup):
-        flush.zero_()
-        step(d)
-    torch.cuda.synchronize()
-    if int(d_err.item()) != 0:
-        raise RuntimeError(f"device error word {int(d_err.item())} during warm-up")
-
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
-           torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(args.steps)]
-    if dist is not None:
-        dist.barrier()
-    torch.cuda.synchronize()
-    with ClockSampler(local) as clk:
-        t_wall = time.perf_counter()
-        for i in range(args.steps):
-            flush.zero_()
-            ev[i][0].record(stream)
-            step(d, (ev[i][1], ev[i][2]))
-            ev[i][3].record(stream)
-        torch.cuda.synchronize()
-        t_wall = time.perf_counter() - t_wall
-    step_ms = [a.elapsed_time(b) for a, _, _, b in ev]
-    dec_ms = [a.elapsed_time(b) for _, _, a, b in ev]
-    copy_ms = float(np.mean([a.elapsed_time(b) for a, b, _, _ in ev]))
-    kvw_ms = float(np.mean([a.elapsed_time(b) for _, a, b, _ in ev]))
-    ms_per_step = float(np.mean(step_ms))
-    dec_ms_avg = float(np.mean(dec_ms))
-    ms_per_step, dec_ms_avg = _max_over_ranks([ms_per_step, dec_ms_avg], dist, dev)
-
-    # end to end through the public API: the step's inputs from pinned host memory,
-    # the output back to pinned host memory, every step.  The inputs sit in one
-    # pinned staging buffer (each at a 256-byte offset), so a step's host-to-device
-    # transfer is one copy; the calls read views of its device image.
-    in_keys = ("q", "k_new", "v_new", "slot_mapping", "block_tables", "context_lens",
-               "block_mapping") + (("query_start",) if mq else ())
-    offs, total = {}, 0
-    for k in in_keys:
-        offs[k] = total
-        total += -(-d[k].numel() * d[k].element_size() // 256) * 256
-    host_stage = torch.empty(max(total, 256), dtype=torch.uint8, pin_memory=True)
-    dev_stage = torch.empty_like(host_stage, device=dev)
-    dstep = dict(d)
-    for k in in_keys:
-        n = d[k].numel() * d[k].element_size()
-        host_stage[offs[k]:offs[k] + n].copy_(d[k].reshape(-1).view(torch.uint8).cpu())
-        dstep[k] = dev_stage[offs[k]:offs[k] + n].view(d[k].dtype).view(d[k].shape)
-    host_out = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
-    h2d = sum(d[k].numel() * d[k].element_size() for k in in_keys)
-    d2h = host_out.numel() * host_out.element_size()
-    e2e_ms = []
-    for i in range(args.warmup + args.steps):
-        flush.zero_()
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        dev_stage.copy_(host_stage, non_blocking=True)
-        step(dstep)
-        host_out.copy_(out, non_blocking=True)
-        e1.record(stream)
-        torch.cuda.synchronize()
-        if i >= args.warmup:
-            e2e_ms.append(e0.elapsed_time(e1))
-    e2e_avg = _max_over_ranks([float(np.mean(e2e_ms))], dist, dev)[0]
-    torch.cuda.synchronize()
-    if int(d_err.item()) != 0:
-        raise RuntimeError(f"device error word {int(d_err.item())} during timing")
-
-    kv_bytes = w.kv_read_bytes()
-    unique_bytes = w.kv_unique_read_bytes() if w.num_pairs or "gqa" in w.name else kv_bytes
-    value = _weak_value(ws, kv_bytes, ms_per_step)
-    peak, peak_kind = _peaks()
-    achieved = kv_bytes / (dec_ms_avg * 1e-3) / 1e9
-    seq_heads = w.num_seqs * w.num_q_heads
-    # attention flops: 2 d (q.K) + 2 d (P.V) per (query row, head, token attended)
-    flops = 4 * w.head_dim * w.num_q_heads * sum(n for _, _, n in _rows(w))
-    sms = torch.cuda.get_device_properties(dev).multi_processor_count
-    alu_peak = _alu_peak_tflops(sms)
-    g = w.num_q_heads // w.num_kv_heads
-    # the library's 128-row multi-query kernel (16-bit K/V, d = 128, g a power of
-    # two <= 16, >= 64 query rows per sequence and kv head on average); with the
-    # default partition it splits a context only as far as two items per SM need
-    rows128 = (mq and not fp8 and w.dtype in ("f16", "bf16") and w.head_dim == 128 and
-               g <= 16 and (g & (g - 1)) == 0 and P % 128 == 0 and
-               -(-w.num_query_tokens // w.num_seqs) * g >= 64)
-    tc_tokens = 1  # query tokens per item of the 16-row tensor-core kernel
-    if mq:
-        avg = -(-w.num_query_tokens // w.num_seqs)
-        while tc_tokens * 2 * g <= 16 and tc_tokens < avg:
-            tc_tokens *= 2
-    tc_mq = (mq and not fp8 and w.dtype in ("f16", "bf16") and w.head_dim == 128 and g <= 16 and
-             P % 128 == 0 and tc_tokens * g >= 4)
-    P_eff = P
-    if (rows128 or tc_mq) and w.partition_tokens == 0:
-        B = w.block_size
-        step = B if B % 128 == 0 else (128 if 128 % B == 0 else 128 * B // math.gcd(128, B))
-        max_ctx = w.max_blocks_per_seq * B
-        tiles = -(-w.num_query_tokens // (128 // g if rows128 else tc_tokens)) * w.num_kv_heads
-        P2 = -(-max_ctx // step) * step
-        while P2 > P and tiles * -(-max_ctx // P2) < 2 * sms:
-            P2 = -(-(P2 // 2) // step) * step
-        P_eff = max(P, P2)
-    n_parts = -(-w.max_blocks_per_seq * w.block_size // P_eff)
-    kernel = ("pa_multi_query, 128-row tensor-core kernel" if rows128 else "pa_multi_query") if mq \
-        else "pa_decode"
-    kernel += " (partitions + split-K merge)" if n_parts > 1 else " (one partition per context)"
-    # The binding roofline: HBM for the K/V stream unless the arithmetic needs
-    # longer at its peak (many query rows per K/V byte): fp32 FMA on the SIMT
-    # path, bf16/fp16 tensor cores on the tensor-core path (the library's
-    # dispatch rule: 16-bit K/V, head_dim 128, partitions of 128k tokens, and
-    # at least 4 query rows per kv head in an item).
-    # (E4M3 caches: grouped-head decode, its codes widened to 16 bits in shared memory)
-    tc_path = (w.head_dim == 128 and g <= 16 and P % 128 == 0 and
-               ((fp8 and not mq and g >= 4) or
-                (not fp8 and w.dtype in ("f16", "bf16") and (tc_tokens * g >= 4 if mq else g >= 4))))
-    tensor_peak, tensor_kind = _tensor_peak()
-    tensor_bound = tc_path and flops / (tensor_peak * 1e12) > unique_bytes / (peak * 1e9)
-    alu_bound = not tc_path and flops / (alu_peak * 1e12) > unique_bytes / (peak * 1e9)
-    if tensor_bound:
-        ach = flops / (dec_ms_avg * 1e-3) / 1e12
-        roof = {"bound": "tensor", "kernel": kernel, "achieved": round(ach, 3),
-                "peak": tensor_peak, "unit": "TFLOP/s", "frac": round(ach / tensor_peak, 4),
-                "peak_source": f"{tensor_kind} bf16_tflops (fp16 MMA runs at the bf16 rate)",
-                "flops": "4 x head_dim per (query row, head, token attended)",
-                "traffic": _ncu_traffic(args.config), "algorithmic_flops_per_launch": int(flops),
-                "hbm_achieved_gbs": round(unique_bytes / (dec_ms_avg * 1e-3) / 1e9, 2),
-                "avg_launch_ms": round(dec_ms_avg, 5)}
-    elif alu_bound:
-        ach = flops / (dec_ms_avg * 1e-3) / 1e12
-        roof = {"bound": "alu", "kernel": kernel, "achieved": round(ach, 3),
-                "peak": round(alu_peak, 1), "unit": "TFLOP/s", "frac": round(ach / alu_peak, 4),
-                "peak_source": f"derived: {sms} SMs x {FP32_LANES_PER_SM} fp32 FMA lanes x 2 "
-                               "flop x maximum SM clock (MEASURED_PEAKS sm_max_mhz)",
-                "flops": "4 x head_dim per (query row, head, token attended)",
-                "traffic": _ncu_traffic(args.config), "algorithmic_flops_per_launch": int(flops),
-                "hbm_achieved_gbs": round(unique_bytes / (dec_ms_avg * 1e-3) / 1e9, 2),
-                "avg_launch_ms": round(dec_ms_avg, 5)}
-    else:
-        roof = {"bound": "hbm", "kernel": kernel,
-                "achieved": round(unique_bytes / (dec_ms_avg * 1e-3) / 1e9, 2), "peak": peak,
-                "unit": "GB/s",
-                "frac": round(unique_bytes / (dec_ms_avg * 1e-3) / 1e9 / peak, 4),
-                "peak_source": f"{peak_kind} hbm_gbs",
-                "bytes": "distinct K/V bytes read (shared prefix blocks once)"
-                         if unique_bytes != kv_bytes else "K/V bytes of the cached tokens",
-                "logical_achieved": round(achieved, 2),
-                "traffic": _ncu_traffic(args.config),
-                "algorithmic_bytes_per_launch": unique_bytes,
-                "logical_bytes_per_launch": kv_bytes,
-                "attn_tflops": round(flops / (dec_ms_avg * 1e-3) / 1e12, 3),
-                "avg_launch_ms": round(dec_ms_avg, 5)}
+    res = _measure(args, args.config, args.layout, dev, dist, ws)
+    also = {}
+    if args.config == "llama7b" and args.layout == "paged" and not args.no_also:
+        for name, layout in ALSO:
+            key = name if layout == "paged" else f"{name}_{layout}"
+            also[key] = _measure(args, name, layout, dev, dist, ws)
     if rank != 0:
         if dist is not None:
             dist.destroy_process_group()
         return
+    w = res["w"]
+    mq = w.query_start is not None
     line = {
-        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": ws,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
+        "metric": METRIC, "value": round(res["value"], 2), "unit": "GB/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(res["ms_per_step"], 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "e4m3" if fp8 else dt,
+        "dtype": "e4m3" if w.kv_dtype == "e4m3" else w.dtype,
         "data": "synthetic (seeded PCG64 N(0,1) K/V/q; block tables from a seeded random "
                 "permutation of the pool)",
-        "config": {"workload": WORKLOAD_TEXT.get(args.config, args.config), "name": args.config,
-                   "num_seqs": w.num_seqs, "num_q_heads": w.num_q_heads,
-                   "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim,
-                   "block_size": w.block_size, "num_blocks": w.num_blocks,
-                   "partition_tokens": P_eff, "kv_read_bytes_per_step": kv_bytes,
-                   **({"query_tokens": w.num_query_tokens} if mq else {}),
-                   "layout": w.meta.get("layout", "paged"),
-                   "l2": ("KV pool larger than L2 and a 256 MB L2 flush before every step "
-                          "(outside the timed events)")
-                         if 2 * w.k_cache.nbytes > L2_BYTES else
-                         "a 256 MB L2 flush before every step (outside the timed events); the "
-                         "KV pool itself fits in L2",
-                   "parallelism": f"weak: {ws} independent replicas of the batch, one per GPU"},
-        "seq_heads_per_s": round(ws * seq_heads / (ms_per_step * 1e-3), 1),
-        "hbm_frac": round(value / ws / peak, 4),
-        "roofline": roof,
-        **({"query_tokens_per_s": round(ws * w.num_query_tokens / (ms_per_step * 1e-3), 1)}
+        "config": _config(w, res, args, ws, args.config),
+        "seq_heads_per_s": round(res["seq_heads_per_s"], 1),
+        "hbm_frac": round(res["hbm_frac"], 4),
+        "hbm_frac_of_nominal": round(res["hbm_frac_of_nominal"], 4),
+        "roofline": res["roofline"],
+        **({"query_tokens_per_s": round(ws * w.num_query_tokens / (res["ms_per_step"] * 1e-3), 1)}
            if mq else {}),
-        "e2e": {"value": round(_weak_value(ws, kv_bytes, e2e_avg), 2), "unit": "GB/s",
-                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-                "ms_per_step": round(e2e_avg, 5)},
-        "components": {
-            "kv_write": {"ms": round(kvw_ms, 5), "tokens": w.num_tokens,
-                         "gb_per_s": round(4 * w.num_tokens * w.num_kv_heads * w.head_dim *
-                                           w.elem_bytes / max(kvw_ms, 1e-9) / 1e6, 2),
-                         "bytes": "K and V rows read + written"},
-            "copy_blocks": {"ms": round(copy_ms, 5), "pairs": w.num_pairs,
-                            "gb_per_s": round(4 * w.num_pairs * w.num_kv_heads * w.block_size *
-                                              w.head_dim * w.elem_bytes / max(copy_ms, 1e-9) / 1e6, 2)
-                            if w.num_pairs else None,
-                            "bytes": "K and V blocks read + written"},
-            "decode": {"ms": round(dec_ms_avg, 5)}},
-        "gpu_launches": launches_per_step * args.steps,
-        "clocks": clk.summary(),
-        "wall_s_timed_region": round(t_wall, 4),
+        "e2e": res["e2e"],
+        "components": res["components"],
+        "gpu_launches": res["gpu_launches"],
+        "clocks": res["clocks"],
+        "wall_s_timed_region": res["wall_s_timed_region"],
+        "memory": res["memory"],
     }
+    if also:
+        line["also"] = {k: _sub_line(r, args, ws, k) for k, r in also.items()}
+        if "llama7b_contiguous" in also:
+            c = also["llama7b_contiguous"]
+            line["also"]["paged_over_contiguous"] = {
+                "attention": round(c["dec_ms"] / res["dec_ms"], 4),
+                "step": round(c["ms_per_step"] / res["ms_per_step"], 4),
+                "what": "paged throughput as a fraction of the contiguous layout's (same "
+                        "kernel, identity-like block tables), attention call and whole step"}
+        line["gpu_launches_also"] = sum(r["gpu_launches"] for r in also.values())
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = _cpu_baseline(w)
     print(json.dumps(line), flush=True)
@@ -666,7 +736,8 @@ def run_reference(args):
                          "sample": f"per step: oracle copy_blocks + kv_write + attention of the "
                                    f"first {n} of {len(rows)} query rows ({sample_bytes / 1e6:.0f}"
                                    f" MB of the step's K/V bytes in proportion to the tokens "
-                                   f"attended), fp64 C oracle, {threads} host threads"},
+                                   f"attended), fp64 C oracle, {threads} host threads",
+                         "host_cpus": _host_cpus()},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -726,6 +797,8 @@ def main():
     ap.add_argument("--partition", type=int, default=None,
                     help="tokens per split-K partition (default: the workload's, else the library's)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-also", action="store_true",
+                    help="skip the 13B-shaped and contiguous-layout lines of the default run")
     ap.add_argument("--layout", choices=("paged", "contiguous"), default="paged",
                     help="contiguous: identity-like block tables (each sequence's blocks adjacent), "
                          "the contiguous-KV comparison")

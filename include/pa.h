@@ -178,13 +178,17 @@ size_t pa_decode_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads,
  * and P.V of a 128-token stage are dense tiles computed on the tensor cores
  * (tcgen05) from tiles fetched by TMA tensor copies.  Long sequences are split into
  * partitions of pa_decode_partition_tokens() tokens whose partial softmax
- * states are merged by a second kernel (log-sum-exp).
+ * states are merged (log-sum-exp) by a second kernel: one warp per
+ * (sequence, head) when a context has at most 32 partitions, else one CTA.
  * workspace: device memory of at least pa_decode_workspace_size() bytes,
  * 256-byte aligned and zero-filled once before its first use.  Its first 256
  * bytes are work counters that every call returns to zero (a call that
  * reported PA_DERR_TIMEOUT included), so a workspace can be reused for any
  * number of calls without clearing it again; calls that share one must not
  * overlap on the GPU.
+ * The SIMT kernel and the merge kernel are launched with programmatic stream
+ * serialisation: their CTAs may be set up while the previous kernel in the
+ * stream ends, and read nothing before that kernel has completed.
  * n == 0 gives a zero row.  Accumulation is fp32; out has dtype `dtype`.
  * Supported: head_dim 64 or 128; block_size a multiple of 16 up to 256;
  * num_q_heads a multiple of num_kv_heads.
@@ -340,6 +344,88 @@ pa_status pa_decode_fp8(void* out, const void* q, pa_dtype q_dtype, const void* 
                         int num_kv_heads, int head_dim, int block_size, int num_blocks,
                         float scale, int partition_tokens, void* workspace,
                         size_t workspace_bytes, uint32_t* d_err, pa_stream_t stream);
+
+/* pa_attention_plan -- which kernels a pa_decode, pa_decode_fp8 or
+ * pa_multi_query call with these sizes would enqueue, without enqueuing
+ * anything (no device memory is touched; the checks are the calls' own host
+ * checks).  multi_query = 0 plans pa_decode / pa_decode_fp8 (num_query_tokens
+ * is then num_seqs), 1 plans pa_multi_query with num_query_tokens rows in
+ * all.  kv_dtype PA_E4M3 plans pa_decode_fp8 with q and out of type q_dtype;
+ * otherwise q_dtype must equal kv_dtype.  On PA_OK *plan holds the kernel
+ * family, the partition length the call will use (the tensor-core
+ * multi-query kernels lengthen the default), the partitions of the longest
+ * allowed context, how the partitions are merged and the number of kernel
+ * launches. */
+#define PA_KERNEL_SIMT 1            /* persistent SIMT kernel, 16- or 32-bit K/V               */
+#define PA_KERNEL_SIMT_FP8 2        /* persistent SIMT kernel over E4M3 K/V                    */
+#define PA_KERNEL_TC_GROUPED 3      /* tcgen05 kernel, items of up to 16 query rows            */
+#define PA_KERNEL_TC_GROUPED_FP8 4  /* tcgen05 kernel over E4M3 K/V widened in shared memory   */
+#define PA_KERNEL_TC_128_ROWS 5     /* tcgen05 kernel, items of 128 query rows (chunked prefill) */
+#define PA_MERGE_NONE 0             /* one partition per context: no merge                      */
+#define PA_MERGE_KERNEL 1           /* a second kernel merges the partitions                    */
+typedef struct pa_attention_plan_t {
+    int kernel;            /* PA_KERNEL_* */
+    int partition_tokens;  /* tokens per split-K partition */
+    int max_parts;         /* partitions of a context of max_blocks_per_seq * block_size tokens */
+    int merge;             /* PA_MERGE_* */
+    int launches;          /* kernels the call enqueues */
+} pa_attention_plan_t;
+pa_status pa_attention_plan(int num_seqs, int num_query_tokens, int multi_query, int num_q_heads,
+                            int num_kv_heads, int head_dim, int max_blocks_per_seq, int block_size,
+                            int num_blocks, int partition_tokens, pa_dtype kv_dtype,
+                            pa_dtype q_dtype, pa_attention_plan_t* plan);
+
+/* ---- one step with host inputs and output --------------------------------
+ *
+ * pa_step_host runs a whole step -- copy-on-write copies (pa_copy_blocks),
+ * the new tokens' K/V write (pa_kv_write) and attention (pa_decode, or
+ * pa_multi_query when num_query_tokens > 0) -- on a device-resident cache,
+ * with the step's inputs taken from host memory and its output returned to
+ * host memory: the per-step data a serving loop produces on the host.  The
+ * caller packs the inputs into one host buffer at the offsets pa_step_layout
+ * gives (each 256-byte aligned), in this order:
+ *   0 q             [rows][num_q_heads][head_dim], dtype (rows = num_query_tokens,
+ *                   or num_seqs when num_query_tokens is 0)
+ *   1 k_new, 2 v_new [num_new_tokens][num_kv_heads][head_dim], dtype
+ *   3 slot_mapping  int64 [num_new_tokens]
+ *   4 block_tables  int32 [num_seqs][max_blocks_per_seq]
+ *   5 context_lens  int32 [num_seqs]
+ *   6 block_mapping int32 [num_pairs][2]
+ *   7 query_start   int32 [num_seqs + 1] (multi-query steps only)
+ * The call enqueues on `stream`: one host-to-device copy of the whole buffer
+ * into dev_stage (device memory of pa_step_layout() bytes, 256-byte
+ * aligned, owned by the caller), the kernels of the three operations reading
+ * their inputs there, and one device-to-host copy of out (dev_out, device
+ * memory [rows][num_q_heads][head_dim]) into host_out.  host_in and host_out
+ * should be pinned (cudaHostAlloc) for the copies to be asynchronous; the
+ * caller synchronises the stream before reading host_out or reusing host_in.
+ * E4M3 caches: pass k_scale / v_scale (device, [num_blocks][num_kv_heads]);
+ * the step then uses the *_fp8 calls (decode only, dtype F16 or BF16).
+ * Semantics, errors and the workspace: those of the calls it makes; every
+ * host check runs before anything is enqueued.
+ */
+#define PA_STEP_NUM_INPUTS 8
+typedef struct pa_step_dims {
+    int num_seqs;
+    int num_query_tokens;  /* 0: decode, one query per sequence */
+    int num_new_tokens;
+    int num_pairs;
+    int num_q_heads;
+    int num_kv_heads;
+    int head_dim;
+    int block_size;
+    int num_blocks;
+    int max_blocks_per_seq;
+    pa_dtype dtype;        /* of q, out and the new tokens (and the cache unless E4M3) */
+} pa_step_dims;
+/* Byte offsets of the eight inputs in the packed buffer; returns its size
+ * (0 for invalid dimensions). */
+size_t pa_step_layout(const pa_step_dims* dims, size_t offsets[PA_STEP_NUM_INPUTS]);
+pa_status pa_step_host(const pa_step_dims* dims, const void* host_in, void* dev_stage,
+                       void* host_out, void* dev_out, void* k_cache, void* v_cache,
+                       float* k_scale, float* v_scale, float scale, int partition_tokens,
+                       void* workspace, size_t workspace_bytes, uint32_t* d_err,
+                       pa_stream_t stream);
 
 /* pa_selftest_wait_timeout -- exercises the bounded waits the kernels use.
  * One warp waits on a barrier nothing ever arrives at; after the wait limit

@@ -32,7 +32,26 @@ EXPORTED = ("pa_abi_version", "pa_status_string", "pa_kv_write", "pa_copy_blocks
             "pa_decode", "pa_decode_static_workspace", "pa_multi_query_partition_tokens",
             "pa_multi_query_workspace_size", "pa_multi_query", "pa_kv_write_fp8",
             "pa_copy_blocks_fp8", "pa_swap_blocks_fp8", "pa_decode_fp8",
-            "pa_selftest_wait_timeout")
+            "pa_attention_plan", "pa_step_layout", "pa_step_host", "pa_selftest_wait_timeout")
+STEP_INPUTS = ("q", "k_new", "v_new", "slot_mapping", "block_tables", "context_lens",
+               "block_mapping", "query_start")
+KERNEL_NAMES = {1: "simt", 2: "simt_fp8", 3: "tc_grouped", 4: "tc_grouped_fp8", 5: "tc_128_rows"}
+MERGE_NAMES = {0: "none", 1: "kernel"}
+
+
+class StepDims(ctypes.Structure):
+    """pa_step_dims of include/pa.h."""
+    _fields_ = [("num_seqs", ctypes.c_int), ("num_query_tokens", ctypes.c_int),
+                ("num_new_tokens", ctypes.c_int), ("num_pairs", ctypes.c_int),
+                ("num_q_heads", ctypes.c_int), ("num_kv_heads", ctypes.c_int),
+                ("head_dim", ctypes.c_int), ("block_size", ctypes.c_int),
+                ("num_blocks", ctypes.c_int), ("max_blocks_per_seq", ctypes.c_int),
+                ("dtype", ctypes.c_int)]
+
+
+class _Plan(ctypes.Structure):
+    _fields_ = [("kernel", ctypes.c_int), ("partition_tokens", ctypes.c_int),
+                ("max_parts", ctypes.c_int), ("merge", ctypes.c_int), ("launches", ctypes.c_int)]
 PA_E4M3 = 3
 
 _lock = threading.Lock()
@@ -100,6 +119,14 @@ def load() -> ctypes.CDLL:
         lib.pa_decode_fp8.restype = i32
         lib.pa_decode_fp8.argtypes = [vp, vp, i32, vp, vp, vp, vp, vp, i32, vp, i32, i32, i32,
                                       i32, i32, i32, ctypes.c_float, i32, vp, u64, vp, vp]
+        lib.pa_step_layout.restype = u64
+        lib.pa_step_layout.argtypes = [ctypes.POINTER(StepDims), ctypes.POINTER(ctypes.c_size_t)]
+        lib.pa_step_host.restype = i32
+        lib.pa_step_host.argtypes = [ctypes.POINTER(StepDims), vp, vp, vp, vp, vp, vp, vp, vp,
+                                     ctypes.c_float, i32, vp, u64, vp, vp]
+        lib.pa_attention_plan.restype = i32
+        lib.pa_attention_plan.argtypes = [i32, i32, i32, i32, i32, i32, i32, i32, i32, i32, i32,
+                                          i32, ctypes.POINTER(_Plan)]
         _lib = lib
         return lib
 
@@ -424,3 +451,49 @@ def decode_fp8(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor, v_cach
                               _stream(stream, q.device))
     _check(st, "pa_decode_fp8")
     return out
+
+
+def attention_plan(num_seqs: int, num_q_heads: int, num_kv_heads: int, head_dim: int,
+                   max_blocks_per_seq: int, block_size: int, num_blocks: int, dtype,
+                   partition_tokens: int = 0, num_query_tokens: Optional[int] = None,
+                   kv_dtype=None) -> dict:
+    """What a pa_decode (num_query_tokens None), pa_decode_fp8 (kv_dtype
+    "e4m3") or pa_multi_query call with these sizes would launch: kernel
+    family, partition length, partitions of the longest context, merge kind
+    and number of kernel launches."""
+    q_code = _dtype_code(dtype)
+    kv_code = PA_E4M3 if kv_dtype == "e4m3" else q_code
+    plan = _Plan()
+    multi = num_query_tokens is not None
+    _check(load().pa_attention_plan(num_seqs, num_query_tokens if multi else num_seqs, int(multi),
+                                    num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq,
+                                    block_size, num_blocks, partition_tokens, kv_code, q_code,
+                                    ctypes.byref(plan)), "pa_attention_plan")
+    return {"kernel": KERNEL_NAMES.get(plan.kernel, plan.kernel),
+            "partition_tokens": plan.partition_tokens, "max_parts": plan.max_parts,
+            "merge": MERGE_NAMES.get(plan.merge, plan.merge), "launches": plan.launches}
+
+
+def step_layout(dims: StepDims):
+    """(total bytes, {input name: byte offset}) of pa_step_host's packed inputs."""
+    offs = (ctypes.c_size_t * len(STEP_INPUTS))()
+    total = int(load().pa_step_layout(ctypes.byref(dims), offs))
+    if total == 0:
+        raise PaError(1, "pa_step_layout")
+    return total, {k: int(o) for k, o in zip(STEP_INPUTS, offs)}
+
+
+def step_host(dims: StepDims, host_in: torch.Tensor, dev_stage: torch.Tensor,
+              host_out: torch.Tensor, dev_out: torch.Tensor, k_cache: torch.Tensor,
+              v_cache: torch.Tensor, scale: float, partition_tokens: int = 0,
+              workspace: Optional[torch.Tensor] = None, d_err: Optional[torch.Tensor] = None,
+              k_scale: Optional[torch.Tensor] = None, v_scale: Optional[torch.Tensor] = None,
+              stream=None) -> None:
+    """pa_step_host: one step with its inputs packed in (pinned) host memory
+    host_in and its output copied to host_out; asynchronous on the stream."""
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(load().pa_step_host(ctypes.byref(dims), _ptr(host_in), _ptr(dev_stage),
+                               _ptr(host_out), _ptr(dev_out), _ptr(k_cache), _ptr(v_cache),
+                               _ptr(k_scale), _ptr(v_scale), scale, partition_tokens,
+                               _ptr(workspace), ws_bytes, _ptr(d_err),
+                               _stream(stream, dev_out.device)), "pa_step_host")

@@ -207,6 +207,7 @@ struct AttnCall {
     size_t workspace_bytes;
     uint32_t* d_err;
     pa_stream_t stream;
+    pa_attention_plan_t* plan;  // non-null: only describe what would be launched
 };
 
 int gcd_int(int a, int b) {
@@ -252,21 +253,35 @@ pa_status lengthen_partitions(const AttnCall& a, DecodeParams& p, unsigned char*
         const WsLayout w2 = ws_layout(a.num_query_tokens, a.num_q_heads, a.head_dim, mp);
         p.partition_tokens = static_cast<int>(P2);
         p.max_parts = mp;
-        p.ws_m = mp > 1 ? reinterpret_cast<float*>(wsb + w2.m_off) : nullptr;
-        p.ws_l = mp > 1 ? reinterpret_cast<float*>(wsb + w2.l_off) : nullptr;
-        p.ws_o = mp > 1 ? reinterpret_cast<float*>(wsb + w2.o_off) : nullptr;
+        const bool split = mp > 1 && wsb != nullptr;
+        p.ws_m = split ? reinterpret_cast<float*>(wsb + w2.m_off) : nullptr;
+        p.ws_l = split ? reinterpret_cast<float*>(wsb + w2.l_off) : nullptr;
+        p.ws_o = split ? reinterpret_cast<float*>(wsb + w2.o_off) : nullptr;
     }
     return PA_OK;
 }
 
-// Shared by pa_decode and pa_multi_query once the arguments are checked.
+// What a call launches, for pa_attention_plan.
+pa_status describe(pa_attention_plan_t* plan, int kernel, const DecodeParams& p) {
+    plan->kernel = kernel;
+    plan->partition_tokens = p.partition_tokens;
+    plan->max_parts = p.max_parts;
+    plan->merge = p.max_parts <= 1 ? PA_MERGE_NONE : PA_MERGE_KERNEL;
+    plan->launches = plan->merge == PA_MERGE_KERNEL ? 2 : 1;
+    return PA_OK;
+}
+
+// Shared by pa_decode, pa_multi_query and pa_attention_plan once the
+// arguments are checked.
 pa_status run_attention(const AttnCall& a) {
     const int P = a.partition_tokens;
     const int max_parts = max_parts_for(a.max_blocks_per_seq, a.block_size, P);
     const WsLayout ws = ws_layout(a.num_query_tokens, a.num_q_heads, a.head_dim, max_parts);
-    if (a.workspace == nullptr) return PA_ERR_INVALID_ARG;
-    if (a.workspace_bytes < ws.bytes) return PA_ERR_WORKSPACE_TOO_SMALL;
-    if ((reinterpret_cast<uintptr_t>(a.workspace) & 255u) != 0) return PA_ERR_INVALID_ARG;
+    if (a.plan == nullptr) {
+        if (a.workspace == nullptr) return PA_ERR_INVALID_ARG;
+        if (a.workspace_bytes < ws.bytes) return PA_ERR_WORKSPACE_TOO_SMALL;
+        if ((reinterpret_cast<uintptr_t>(a.workspace) & 255u) != 0) return PA_ERR_INVALID_ARG;
+    }
     const int group = a.num_q_heads / a.num_kv_heads;
     // E4M3 caches widen 16 elements per lane: at most 4 rows per tile keep the
     // query slices and accumulators in registers.
@@ -287,11 +302,13 @@ pa_status run_attention(const AttnCall& a) {
     p.block_tables = a.block_tables;
     p.context_lens = a.context_lens;
     p.query_start = a.query_start;
-    unsigned char* wsb = static_cast<unsigned char*>(a.workspace);
+    unsigned char* wsb = a.plan != nullptr ? nullptr : static_cast<unsigned char*>(a.workspace);
+    const bool split = max_parts > 1 && wsb != nullptr;
     p.counters = reinterpret_cast<unsigned int*>(wsb);
-    p.ws_m = max_parts > 1 ? reinterpret_cast<float*>(wsb + ws.m_off) : nullptr;
-    p.ws_l = max_parts > 1 ? reinterpret_cast<float*>(wsb + ws.l_off) : nullptr;
-    p.ws_o = max_parts > 1 ? reinterpret_cast<float*>(wsb + ws.o_off) : nullptr;
+    p.ws_m = split ? reinterpret_cast<float*>(wsb + ws.m_off) : nullptr;
+    p.ws_l = split ? reinterpret_cast<float*>(wsb + ws.l_off) : nullptr;
+    p.ws_o = split ? reinterpret_cast<float*>(wsb + ws.o_off) : nullptr;
+    const bool plan = a.plan != nullptr;  // tensor maps are not encoded for a plan
     p.d_err = a.d_err;
     p.num_seqs = a.num_seqs;
     p.num_q_heads = a.num_q_heads;
@@ -317,16 +334,18 @@ pa_status run_attention(const AttnCall& a) {
         if (tc_shape(a.num_q_heads, a.num_kv_heads, a.head_dim, PA_E4M3) && P % 128 == 0 &&
             pool_rows < 0x7fffffffLL) {
             CUtensorMap map_k, map_v;
-            if (make_pool_map_fp8(&map_k, a.k_cache, pool_rows) &&
-                make_pool_map_fp8(&map_v, a.v_cache, pool_rows)) {
+            if (plan || (make_pool_map_fp8(&map_k, a.k_cache, pool_rows) &&
+                         make_pool_map_fp8(&map_v, a.v_cache, pool_rows))) {
                 p.head_tiles = a.num_kv_heads;
                 p.tile_heads = group;
                 p.tile_tokens = 1;
+                if (plan) return describe(a.plan, PA_KERNEL_TC_GROUPED_FP8, p);
                 return a.dtype == PA_BF16 ? launch_decode_tc_fp8_bf16(p, map_k, map_v, st)
                                           : launch_decode_tc_fp8_f16(p, map_k, map_v, st);
             }
         }
         const int gt = heads * tokens;
+        if (plan) return describe(a.plan, PA_KERNEL_SIMT_FP8, p);
         return a.dtype == PA_BF16 ? launch_decode_fp8_bf16(p, gt, st)
                                   : launch_decode_fp8_f16(p, gt, st);
     }
@@ -349,9 +368,10 @@ pa_status run_attention(const AttnCall& a) {
     if (tc_ok && a.query_start != nullptr && a.num_seqs > 0 && (group & (group - 1)) == 0) {
         const long long avg = (static_cast<long long>(a.num_query_tokens) + a.num_seqs - 1) / a.num_seqs;
         CUtensorMap map_k, map_v, map_q;
-        if (avg * group >= 64 && make_pool_map(&map_k, a.k_cache, pool_rows, a.dtype) &&
-            make_pool_map(&map_v, a.v_cache, pool_rows, a.dtype) &&
-            make_q_map(&map_q, a.q, a.num_query_tokens, a.num_q_heads, group, a.dtype)) {
+        if (avg * group >= 64 &&
+            (plan || (make_pool_map(&map_k, a.k_cache, pool_rows, a.dtype) &&
+                      make_pool_map(&map_v, a.v_cache, pool_rows, a.dtype) &&
+                      make_q_map(&map_q, a.q, a.num_query_tokens, a.num_q_heads, group, a.dtype)))) {
             p.head_tiles = a.num_kv_heads;
             p.tile_heads = group;
             p.tile_tokens = 128 / group;
@@ -359,14 +379,15 @@ pa_status run_attention(const AttnCall& a) {
                 const pa_status e = lengthen_partitions(a, p, wsb);
                 if (e != PA_OK) return e;
             }
+            if (plan) return describe(a.plan, PA_KERNEL_TC_128_ROWS, p);
             return a.dtype == PA_BF16 ? launch_prefill_tc_bf16(p, map_k, map_v, map_q, st)
                                       : launch_prefill_tc_f16(p, map_k, map_v, map_q, st);
         }
     }
     if (tc_ok && tc_rows) {
         CUtensorMap map_k, map_v;
-        if (make_pool_map(&map_k, a.k_cache, pool_rows, a.dtype) &&
-            make_pool_map(&map_v, a.v_cache, pool_rows, a.dtype)) {
+        if (plan || (make_pool_map(&map_k, a.k_cache, pool_rows, a.dtype) &&
+                     make_pool_map(&map_v, a.v_cache, pool_rows, a.dtype))) {
             p.head_tiles = a.num_kv_heads;
             p.tile_heads = group;
             p.tile_tokens = tc_tokens;
@@ -375,14 +396,17 @@ pa_status run_attention(const AttnCall& a) {
                     const pa_status e = lengthen_partitions(a, p, wsb);
                     if (e != PA_OK) return e;
                 }
+                if (plan) return describe(a.plan, PA_KERNEL_TC_GROUPED, p);
                 return a.dtype == PA_BF16 ? launch_multi_query_tc_bf16(p, map_k, map_v, st)
                                           : launch_multi_query_tc_f16(p, map_k, map_v, st);
             }
+            if (plan) return describe(a.plan, PA_KERNEL_TC_GROUPED, p);
             return a.dtype == PA_BF16 ? launch_decode_tc_bf16(p, map_k, map_v, st)
                                       : launch_decode_tc_f16(p, map_k, map_v, st);
         }
     }
     const int gt = heads * tokens;
+    if (plan) return describe(a.plan, PA_KERNEL_SIMT, p);
     if (a.query_start != nullptr) {
         switch (a.dtype) {
             case PA_F32: return launch_multi_query_f32(p, a.head_dim, gt, st);
@@ -551,5 +575,44 @@ extern "C" pa_status pa_multi_query(void* out, const void* q, int num_query_toke
                      max_blocks_per_seq, context_lens, num_seqs, num_q_heads, num_kv_heads,
                      head_dim, block_size, num_blocks, scale, P, partition_tokens == 0, dtype,
                      workspace, workspace_bytes, d_err, stream};
+    return run_attention(a);
+}
+
+extern "C" pa_status pa_attention_plan(int num_seqs, int num_query_tokens, int multi_query,
+                                       int num_q_heads, int num_kv_heads, int head_dim,
+                                       int max_blocks_per_seq, int block_size, int num_blocks,
+                                       int partition_tokens, pa_dtype kv_dtype, pa_dtype q_dtype,
+                                       pa_attention_plan_t* plan) {
+    using namespace pa;
+    if (plan == nullptr) return PA_ERR_INVALID_ARG;
+    const bool fp8 = kv_dtype == PA_E4M3;
+    if (fp8 ? (q_dtype != PA_F16 && q_dtype != PA_BF16) : q_dtype != kv_dtype)
+        return PA_ERR_INVALID_ARG;
+    if (fp8 && (head_dim != 128 || multi_query)) return PA_ERR_UNSUPPORTED;
+    if (!multi_query) num_query_tokens = num_seqs;
+    if (num_seqs <= 0 || num_query_tokens <= 0) return PA_ERR_INVALID_ARG;
+    // every host check of the calls, on stand-in (aligned, never read) pointers
+    const void* any = reinterpret_cast<const void*>(static_cast<uintptr_t>(256));
+    const pa_status c = check_attention(any, any, any, any, static_cast<const int32_t*>(any),
+                                        max_blocks_per_seq, static_cast<const int32_t*>(any),
+                                        num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                                        num_blocks, 1.0f, partition_tokens, q_dtype);
+    if (c != PA_OK) return c;
+    const int P = multi_query
+                      ? pa_multi_query_partition_tokens(num_query_tokens, num_q_heads, num_kv_heads,
+                                                        head_dim, max_blocks_per_seq, block_size,
+                                                        q_dtype, partition_tokens)
+                      : pa_decode_partition_tokens(num_q_heads, num_kv_heads, head_dim,
+                                                   max_blocks_per_seq, block_size, kv_dtype,
+                                                   partition_tokens);
+    if (P <= 0) return PA_ERR_INVALID_ARG;
+    if (static_cast<long long>(num_query_tokens) * num_q_heads > 0x7fffffffLL)
+        return PA_ERR_UNSUPPORTED;
+    const float* scales = fp8 ? static_cast<const float*>(any) : nullptr;
+    const AttnCall a{nullptr, nullptr, multi_query ? static_cast<const int32_t*>(any) : nullptr,
+                     num_query_tokens, nullptr, nullptr, scales, scales, nullptr,
+                     max_blocks_per_seq, nullptr, num_seqs, num_q_heads, num_kv_heads, head_dim,
+                     block_size, num_blocks, 1.0f, P, multi_query && partition_tokens == 0, q_dtype,
+                     nullptr, 0, nullptr, nullptr, plan};
     return run_attention(a);
 }

@@ -100,6 +100,19 @@ struct DecodeParams {
 
 __host__ __device__ constexpr int align16(int x) { return (x + 15) / 16 * 16; }
 
+// Sequences of at most this many partitions are merged by one warp per
+// (query row, head) (decode_merge_rows_kernel); longer ones by a CTA per row
+// (decode_reduce_kernel).
+constexpr int kRowMergeMaxParts = 32;
+
+// Waits until the grids this one depends on through programmatic stream
+// serialisation have completed and their writes are visible (returns at once
+// when there are none).  Not a spin loop: the hardware holds the threads
+// until the preceding kernel in the stream (which has no waits) ends.
+__device__ __forceinline__ void wait_prior_grids() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // Stage flags written by the producer next to each stage.
 constexpr uint32_t kStageFirst = 1u;  // first stage of its item for the consuming warp
 constexpr uint32_t kStageLast = 2u;   // last stage of its item for the consuming warp
@@ -153,6 +166,8 @@ struct DecodeTile {
     // (one row per tile with 8- or 16-bit elements: a 32 KB ring, so that five CTAs
     // -- twenty consumer warps -- share an SM, 160 KB of copies still in flight)
     static constexpr int kStages = (kElem <= 2 && GT == 1) ? 32768 / kStageBytes : 65536 / kStageBytes;
+    // CTAs per SM the register budget must allow: five with the 32 KB ring
+    static constexpr int kMinCtasPerSm = (kElem <= 2 && GT == 1) ? 5 : 1;
     static constexpr int kItems = GT >= 4 ? 2 : 3;    // item slots in flight
     static constexpr int kQBytes = GT * D * sizeof(T);  // query rows of one item
     static constexpr int kMergeFloats = kConsumerWarps * GT * (D + 2);  // per item slot
@@ -651,6 +666,65 @@ __device__ __forceinline__ void decode_produce(const DecodeParams& p, unsigned c
 }
 
 
+// Split-K merge of one (query row, head) by one warp: M = max_i m_i,
+// out = sum_i 2^(m_i-M) o_i / sum_i 2^(m_i-M) l_i over its nparts partial
+// states.  The states are read from L2 (the decode kernel just wrote them),
+// eight partitions at a time with every load of a chunk in flight together, and
+// merged online across chunks.  A lane owns D/32 output columns.
+template <typename T, int D>
+__device__ __forceinline__ void merge_row(const DecodeParams& p, size_t row, int nparts,
+                                          int lane) {
+    constexpr int kCols = D / 32;
+    constexpr int kChunk = 8;
+    static_assert(kCols == 2 || kCols == 4, "head_dim 64 or 128");
+    const size_t base = row * p.max_parts;
+    float M = -INFINITY, L = 0.f, O[kCols];
+#pragma unroll
+    for (int c = 0; c < kCols; ++c) O[c] = 0.f;
+#pragma unroll 1
+    for (int i0 = 0; i0 < nparts; i0 += kChunk) {
+        float mi[kChunk], li[kChunk], oi[kChunk][kCols];
+#pragma unroll
+        for (int k = 0; k < kChunk; ++k) {
+            const bool in = i0 + k < nparts;
+            const size_t r = base + (in ? i0 + k : i0);  // an address inside the row either way
+            mi[k] = in ? __ldcg(p.ws_m + r) : -INFINITY;
+            li[k] = in ? __ldcg(p.ws_l + r) : 0.f;
+            const float* po = p.ws_o + r * D + lane * kCols;
+            if constexpr (kCols == 4) {
+                const float4 v = __ldcg(reinterpret_cast<const float4*>(po));
+                oi[k][0] = v.x;
+                oi[k][1] = v.y;
+                oi[k][2] = v.z;
+                oi[k][3] = v.w;
+            } else {
+                const float2 v = __ldcg(reinterpret_cast<const float2*>(po));
+                oi[k][0] = v.x;
+                oi[k][1] = v.y;
+            }
+        }
+        float Mc = M;
+#pragma unroll
+        for (int k = 0; k < kChunk; ++k) Mc = fmaxf(Mc, mi[k]);
+        if (Mc == -INFINITY) continue;  // no token in any partition so far
+        const float a = fast_exp2(M - Mc);  // 0 while M was -inf
+        L *= a;
+#pragma unroll
+        for (int c = 0; c < kCols; ++c) O[c] *= a;
+#pragma unroll
+        for (int k = 0; k < kChunk; ++k) {
+            const float sc = fast_exp2(mi[k] - Mc);  // empty or absent partition: 2^-inf = 0
+            L = fmaf(sc, li[k], L);
+#pragma unroll
+            for (int c = 0; c < kCols; ++c) O[c] = fmaf(sc, oi[k][c], O[c]);
+        }
+        M = Mc;
+    }
+    T* out = static_cast<T*>(p.out) + row * D + lane * kCols;
+#pragma unroll
+    for (int c = 0; c < kCols; ++c) out[c] = Elem<T>::from_float(L > 0.f ? O[c] / L : 0.f);
+}
+
 template <typename T, int D, int GT, bool kMulti, typename TC>
 __device__ __forceinline__ void decode_consume(const DecodeParams& p, unsigned char* smem) {
     using C = DecodeTile<T, D, GT, TC>;
@@ -821,7 +895,8 @@ __device__ __forceinline__ void decode_consume(const DecodeParams& p, unsigned c
 }
 
 template <typename T, int D, int GT, bool kMulti, typename TC>
-__global__ void __launch_bounds__(DecodeTile<T, D, GT, TC>::kThreads)
+__global__ void __launch_bounds__(DecodeTile<T, D, GT, TC>::kThreads,
+                                  DecodeTile<T, D, GT, TC>::kMinCtasPerSm)
     decode_persistent_kernel(const DecodeParams p) {
     using C = DecodeTile<T, D, GT, TC>;
     extern __shared__ __align__(128) unsigned char smem[];
@@ -840,11 +915,17 @@ __global__ void __launch_bounds__(DecodeTile<T, D, GT, TC>::kThreads)
         fence_barrier_init();
     }
     __syncthreads();
+    // Everything above overlaps the end of the kernel before this one (the
+    // step's kv_write) when the launch allows it; the cache is read only after.
+    wait_prior_grids();
     if ((threadIdx.x >> 5) == C::kConsumerWarps)
         decode_produce<T, D, GT, kMulti, TC>(p, smem);
     else
         decode_consume<T, D, GT, kMulti, TC>(p, smem);
     __syncthreads();
+    // The merge kernel that follows may be set up now; it waits for this
+    // grid's completion before it reads the partial states.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if (threadIdx.x == 0) {
         // The last CTA out returns both counters to zero for the next call.
         __threadfence();
@@ -921,6 +1002,59 @@ __global__ void __launch_bounds__(128) decode_reduce_kernel(const DecodeParams p
     }
 }
 
+// Split-K merge as its own kernel, one warp per (query row, head), for
+// sequences of at most kRowMergeMaxParts partitions.
+template <typename T, int D>
+__global__ void __launch_bounds__(128) decode_merge_rows_kernel(const DecodeParams p) {
+    wait_prior_grids();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const long long sh = static_cast<long long>(blockIdx.x) * 4 + warp;  // row x query head
+    if (sh >= static_cast<long long>(p.num_query_tokens) * p.num_q_heads) return;
+    const int tok = static_cast<int>(sh / p.num_q_heads);
+    int s = tok;
+    if (p.query_start != nullptr) {  // the sequence whose queries hold row tok
+        int lo = 0, hi = p.num_seqs;  // first k in [lo, hi) with query_start[k + 1] > tok
+        while (lo < hi) {
+            const int mid = (lo + hi) >> 1;
+            if (p.query_start[mid + 1] > tok) hi = mid;
+            else lo = mid + 1;
+        }
+        if (lo >= p.num_seqs) return;
+        s = lo;
+    }
+    const SeqQueries sq = seq_queries(p, s);
+    const int max_ctx = p.max_blocks_per_seq * p.block_size;
+    if (!sq.rows_ok(p.num_query_tokens) || tok < sq.q0 || tok >= sq.q1 || !sq.ctx_ok(max_ctx))
+        return;
+    const int nparts = items_of(sq.ctx, max_ctx, p.partition_tokens);
+    if (nparts <= 1) return;
+    merge_row<T, D>(p, static_cast<size_t>(sh), nparts, lane);
+}
+
+// Launches the split-K merge kernel after a decode kernel (programmatic
+// stream serialisation: it waits for the decode kernel inside).
+template <typename T, int D>
+inline pa_status launch_merge(const DecodeParams& p, cudaStream_t stream) {
+    const long long rows = static_cast<long long>(p.num_query_tokens) * p.num_q_heads;
+    if (p.max_parts <= kRowMergeMaxParts) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(static_cast<unsigned>((rows + 3) / 4));
+        cfg.blockDim = dim3(128);
+        cfg.dynamicSmemBytes = 0;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if (cudaLaunchKernelEx(&cfg, decode_merge_rows_kernel<T, D>, p) != cudaSuccess)
+            return PA_ERR_CUDA;
+    } else {
+        decode_reduce_kernel<T, D><<<static_cast<unsigned>(rows), 128, 0, stream>>>(p);
+    }
+    return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
 template <typename T, int D, int GT, bool kMulti, typename TC = T>
 inline pa_status launch_decode_tile(const DecodeParams& p, cudaStream_t stream) {
     using C = DecodeTile<T, D, GT, TC>;
@@ -949,12 +1083,22 @@ inline pa_status launch_decode_tile(const DecodeParams& p, cudaStream_t stream) 
     if (work > 0x7fffffffLL) return PA_ERR_UNSUPPORTED;
     long long grid = static_cast<long long>(sms) * per_sm;
     if (grid > work) grid = work;
-    kernel<<<static_cast<unsigned>(grid), C::kThreads, C::kSmemBytes, stream>>>(p);
+    // Programmatic stream serialisation: the CTAs may start (barrier set-up)
+    // while the previous kernel in the stream finishes; they read nothing
+    // before wait_prior_grids().
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(C::kThreads);
+    cfg.dynamicSmemBytes = C::kSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, kernel, p) != cudaSuccess) return PA_ERR_CUDA;
     if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
-    if (p.max_parts > 1) {
-        decode_reduce_kernel<T, D><<<p.num_query_tokens * p.num_q_heads, 128, 0, stream>>>(p);
-        if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
-    }
+    if (p.max_parts > 1) return launch_merge<T, D>(p, stream);
     return PA_OK;
 }
 

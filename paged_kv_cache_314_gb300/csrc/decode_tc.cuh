@@ -1044,10 +1044,7 @@ inline pa_status launch_decode_tc_typed(const DecodeParams& p, const CUtensorMap
     kernel<<<static_cast<unsigned>(grid), kFp8 ? C::kThreadsFp8 : C::kThreads, C::kSmemBytes, stream>>>(
         p, mapK, mapV);
     if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
-    if (p.max_parts > 1) {
-        decode_reduce_kernel<T, C::D><<<p.num_query_tokens * p.num_q_heads, 128, 0, stream>>>(p);
-        if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
-    }
+    if (p.max_parts > 1) return launch_merge<T, C::D>(p, stream);
     return PA_OK;
 }
 

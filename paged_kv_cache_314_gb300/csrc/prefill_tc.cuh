@@ -799,10 +799,7 @@ inline pa_status launch_prefill_tc_typed(const DecodeParams& p, const CUtensorMa
     if (grid > work) grid = work;
     kernel<<<static_cast<unsigned>(grid), C::kThreads, C::kSmemBytes, stream>>>(p, mapK, mapV, mapQ);
     if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
-    if (p.max_parts > 1) {
-        decode_reduce_kernel<T, C::D><<<p.num_query_tokens * p.num_q_heads, 128, 0, stream>>>(p);
-        if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
-    }
+    if (p.max_parts > 1) return launch_merge<T, C::D>(p, stream);
     return PA_OK;
 }
 

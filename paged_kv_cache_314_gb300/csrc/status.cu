@@ -1,7 +1,7 @@
 // status.cu -- ABI version and status strings.
 #include "pa.h"
 
-extern "C" int pa_abi_version(void) { return 1; }
+extern "C" int pa_abi_version(void) { return 2; }
 
 extern "C" const char* pa_status_string(pa_status status) {
     switch (status) {

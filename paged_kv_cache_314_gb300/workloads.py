@@ -36,8 +36,10 @@ holding the bfloat16 bit pattern (round-to-nearest-even from float32).
 """
 from __future__ import annotations
 
+import concurrent.futures as cf
 import dataclasses
 import math
+import os
 from typing import Dict, List, Optional, Sequence, Tuple
 
 import numpy as np
@@ -185,6 +187,50 @@ class Workload:
         return rows * 2 * self.num_kv_heads * self.head_dim * self.kv_elem_bytes
 
 
+def memory_stats(block_tables: np.ndarray, context_lens: np.ndarray, block_size: int,
+                 max_blocks_per_seq: Optional[int] = None) -> Dict[str, float]:
+    """Cache-memory figures of one batch, from its block tables alone.
+
+    * emu_paged: tokens held / slots of the blocks the sequences' tables
+      cover (each sequence counted on its own): the effective memory
+      utilisation of the paged layout, measured.
+    * emu_paged_closed_form: 1 - (B/2) / mean context, the pages' estimate
+      (the last block of a sequence is half empty on average:
+      "PagedAttention" (compassingai.com) §7).
+    * emu_contiguous: tokens held / (sequences x max context), what a
+      contiguous allocator that reserves the maximum length per sequence uses
+      ("PagedAttention" (compassingai.com) §7).
+    * share_rate: fraction of block-table entries that point at a block some
+      other entry also points at (refcount above one); the block share rate of
+      kwkr.cn "vLLM PagedAttention 技术深度解析" §1.4.1.  Reading of the
+      pages: the rate is taken over the entries in use, i.e. the logical
+      blocks of all sequences.
+    * physical_blocks / logical_blocks: distinct blocks in use, and entries.
+    """
+    B = int(block_size)
+    ctx = np.clip(np.asarray(context_lens, dtype=np.int64), 0, None)
+    S = len(ctx)
+    MB = int(block_tables.shape[1] if max_blocks_per_seq is None else max_blocks_per_seq)
+    nblk = (ctx + B - 1) // B
+    entries = [int(block_tables[s, i]) for s in range(S) for i in range(int(nblk[s]))]
+    counts: Dict[int, int] = {}
+    for b in entries:
+        counts[b] = counts.get(b, 0) + 1
+    tokens = int(ctx.sum())
+    logical = len(entries)
+    shared_entries = sum(c for c in counts.values() if c > 1)
+    mean_ctx = tokens / S if S else 0.0
+    return {
+        "tokens": tokens,
+        "logical_blocks": logical,
+        "physical_blocks": len(counts),
+        "emu_paged": tokens / (logical * B) if logical else 1.0,
+        "emu_paged_closed_form": 1.0 - (B / 2.0) / mean_ctx if mean_ctx > 0 else 0.0,
+        "emu_contiguous": tokens / (S * MB * B) if S else 1.0,
+        "share_rate": shared_entries / logical if logical else 0.0,
+    }
+
+
 def _to_storage(x32: np.ndarray, dtype: str) -> np.ndarray:
     if dtype == "f32":
         return np.ascontiguousarray(x32, dtype=np.float32)
@@ -225,17 +271,32 @@ class _Plan:
     query_lens: Optional[np.ndarray] = None  # [S] queries per sequence; None: decode
 
 
-def _fill_pool(rng, NB, Hkv, B, d, dtype, data_slots, poison, chunk_blocks):
+def _fill_pool(seed_seq: np.random.SeedSequence, NB, Hkv, B, d, dtype, data_slots, poison,
+               chunk_blocks):
+    """A [NB][Hkv][B][d] pool: N(0,1) values in the slots that hold tokens,
+    poison (or zero) elsewhere.  Chunks of blocks are drawn from independent
+    child streams of ``seed_seq`` (one per chunk, so the values do not depend
+    on how the chunks are spread over host threads)."""
     pool = _poison_fill((NB, Hkv, B, d), dtype, poison)
-    for b0 in range(0, NB, chunk_blocks):
+    starts = list(range(0, NB, chunk_blocks))
+    kids = seed_seq.spawn(len(starts))
+
+    def fill(i):
+        b0 = starts[i]
         b1 = min(NB, b0 + chunk_blocks)
-        vals = _normals(rng, (b1 - b0, Hkv, B, d), dtype)
+        vals = _normals(np.random.default_rng(kids[i]), (b1 - b0, Hkv, B, d), dtype)
         m = data_slots[b0:b1]  # [nb][B]
         if m.all():
             pool[b0:b1] = vals
         else:
             mm = np.broadcast_to(m[:, None, :, None], vals.shape)
             np.copyto(pool[b0:b1], vals, where=mm)
+
+    if len(starts) == 1:
+        fill(0)
+    else:
+        with cf.ThreadPoolExecutor(min(len(starts), os.cpu_count() or 1)) as ex:
+            list(ex.map(fill, range(len(starts))))
     return pool
 
 
@@ -252,24 +313,25 @@ def build_workload(name: str, plan: _Plan, *, dtype: str, num_q_heads: int, num_
                    meta: Optional[dict] = None) -> Workload:
     if dtype not in DTYPES:
         raise ValueError(dtype)
-    rng = np.random.default_rng(seed)
+    # independent streams for the two pools, q and the new tokens' K and V
+    k_seq, v_seq, q_seq, kn_seq, vn_seq = np.random.SeedSequence(seed).spawn(5)
     S = plan.tables.shape[0]
     MB = plan.tables.shape[1]
     B, d, Hkv, Hq, NB = block_size, head_dim, num_kv_heads, num_q_heads, num_blocks
     row_elems = Hkv * B * d
-    chunk = max(1, (1 << 26) // row_elems)
-    k_cache = _fill_pool(rng, NB, Hkv, B, d, dtype, plan.data_slots, poison, chunk)
-    v_cache = _fill_pool(rng, NB, Hkv, B, d, dtype, plan.data_slots, poison, chunk)
+    chunk = max(1, (1 << 24) // row_elems)
+    k_cache = _fill_pool(k_seq, NB, Hkv, B, d, dtype, plan.data_slots, poison, chunk)
+    v_cache = _fill_pool(v_seq, NB, Hkv, B, d, dtype, plan.data_slots, poison, chunk)
     query_start = None
     if plan.query_lens is None:
-        q = _normals(rng, (S, Hq, d), dtype)
+        q = _normals(np.random.default_rng(q_seq), (S, Hq, d), dtype)
     else:
         query_start = np.zeros(S + 1, dtype=np.int32)
         query_start[1:] = np.cumsum(plan.query_lens)
-        q = _normals(rng, (int(query_start[-1]), Hq, d), dtype)
+        q = _normals(np.random.default_rng(q_seq), (int(query_start[-1]), Hq, d), dtype)
     T = len(plan.write_tokens)
-    k_new = _normals(rng, (T, Hkv, d), dtype)
-    v_new = _normals(rng, (T, Hkv, d), dtype)
+    k_new = _normals(np.random.default_rng(kn_seq), (T, Hkv, d), dtype)
+    v_new = _normals(np.random.default_rng(vn_seq), (T, Hkv, d), dtype)
     pairs = np.asarray(plan.pairs, dtype=np.int32).reshape(-1, 2)
     return Workload(
         name=name, dtype=dtype, num_seqs=S, num_q_heads=Hq, num_kv_heads=Hkv, head_dim=d,

@@ -75,11 +75,12 @@ def test_one_query_per_sequence_matches_decode_bitwise():
     w = wl.custom("mq_vs_decode", [1, 40, 333, 1000, 2048], dtype="f16", num_q_heads=8,
                   num_kv_heads=8, head_dim=128, block_size=16, seed=410)
     d = upload(w)
-    ref = gpu_step(w, d)
+    ref = gpu_step(w, d, partition_tokens=256)
     qs = torch.arange(w.num_seqs + 1, dtype=torch.int32, device="cuda")
     out = torch.empty_like(d["q"])
+    # the same partitions as the decode call (the two calls' defaults differ)
     pa.multi_query(out, d["q"], qs, d["k_cache"], d["v_cache"], d["block_tables"],
-                   d["context_lens"], w.scale, d_err=d["d_err"])
+                   d["context_lens"], w.scale, partition_tokens=256, d_err=d["d_err"])
     torch.cuda.synchronize()
     assert int(d["d_err"].item()) == 0
     assert torch.equal(out, ref)

@@ -22,6 +22,9 @@ from gpu_util import (assert_close, gpu_step, oracle_decode_heads_parallel, orac
 
 pytestmark = pytest.mark.gpu
 
+# Workspace bytes that every call returns to zero: the work counters.
+HEADER_BYTES = 256
+
 
 @pytest.fixture(scope="module", autouse=True)
 def _built():
@@ -132,7 +135,8 @@ def test_many_short_sequences_and_bad_lengths():
                   w.scale, partition_tokens=256, workspace=ws, d_err=d["d_err"])
         torch.cuda.synchronize()
         outs.append(out)
-        assert int(ws[:8].view(torch.int32).abs().sum().item()) == 0, "work counters not reset"
+        assert int(ws[:HEADER_BYTES].view(torch.int32).abs().sum().item()) == 0, \
+            "work counters not reset"
     assert int(d["d_err"].item()) == err
     assert torch.equal(outs[0], outs[1])
     assert_close(out_f64(outs[0]), ref, "bf16", "many")

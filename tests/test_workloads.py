@@ -156,3 +156,41 @@ def test_fp8_workload_codes_are_finite_where_data_lives():
             b = int(w.block_tables[s, t // B])
             assert np.all((w.k_cache[b, :, t % B] & 0x7F) != 0x7F)
             assert np.all((w.v_cache[b, :, t % B] & 0x7F) != 0x7F)
+
+
+def test_memory_stats_on_the_pages_examples():
+    """EMU and share rate on the worked examples: the 100-token request of
+    tests/golden/p3_block_table.json (7 blocks of 16: 100 of 112 slots used),
+    and the two requests of tests/golden/p2_sharing.json that share physical
+    blocks 1, 3, 4 and then diverge to 2 and 5 (6 of 8 table entries point at
+    a shared block)."""
+    g3 = json.load(open(os.path.join(GOLDEN, "p3_block_table.json")))
+    t = np.array([g3["block_table"]], np.int32)
+    st = wl.memory_stats(t, np.array([g3["num_tokens"]], np.int32), g3["block_size"])
+    assert st["logical_blocks"] == g3["num_logical_blocks"] == st["physical_blocks"]
+    assert st["emu_paged"] == 100 / 112
+    assert st["emu_paged_closed_form"] == 1 - 8 / 100
+    assert st["emu_contiguous"] == 100 / 112  # the table is exactly as long as needed
+    assert st["share_rate"] == 0.0
+    g2 = json.load(open(os.path.join(GOLDEN, "p2_sharing.json")))
+    B = g2["block_size"]
+    shared = g2["shared_requests"]["shared_physical"]
+    div = g2["shared_requests"]["diverged_physical"]
+    tables = np.array([shared + [div[0]], shared + [div[1]]], np.int32)
+    ctx = np.array([4 * B - 1, 3 * B + 2], np.int32)  # both reach into their fourth block
+    st = wl.memory_stats(tables, ctx, B, max_blocks_per_seq=6)
+    assert st["logical_blocks"] == 8 and st["physical_blocks"] == 5
+    assert st["share_rate"] == 6 / 8
+    assert st["emu_paged"] == (int(ctx.sum())) / (8 * B)
+    assert st["emu_contiguous"] == int(ctx.sum()) / (2 * 6 * B)
+
+
+def test_memory_stats_of_the_shared_prefix_workload():
+    w = wl.gqa_share(groups=2, samples=4, prefix_len=64, max_suffix=40, num_q_heads=8,
+                     num_kv_heads=2)
+    st = wl.memory_stats(w.block_tables, w.context_lens, w.block_size)
+    # 3 of the 4 prefix blocks stay shared by the 4 samples of a group; the
+    # fourth is copied on write by samples 1..3
+    shared = 2 * 4 * 3
+    assert st["share_rate"] == shared / st["logical_blocks"]
+    assert st["physical_blocks"] == st["logical_blocks"] - 2 * 3 * 3
