@@ -362,6 +362,13 @@ def _measure(args, name, layout, dev, dist, ws_world):
     mq = w.query_start is not None
     fp8 = w.kv_dtype == "e4m3"
     plan = _plan(pa, w)
+    # parallel sampling: the groups' shared prefix blocks are read once per group
+    G = int(w.meta.get("samples", 1))
+    shared = (not mq and not fp8 and not args.no_shared_prefix and G > 1 and
+              int(w.meta.get("shared_prefix_tokens", 0)) > 0)
+    if shared:
+        plan = dict(plan, kernel="tc_128_rows prefix pass + " + plan["kernel"] + " own pass",
+                    merge="kernel", launches=3)
     dt = w.dtype
     pool = (lambda a: torch.from_numpy(a)) if fp8 else (lambda a: _to_torch(a, dt))
     d = {k: v.to(dev) for k, v in {
@@ -373,9 +380,15 @@ def _measure(args, name, layout, dev, dist, ws_world):
         "block_mapping": torch.from_numpy(w.block_mapping.reshape(-1, 2)),
         **({"query_start": torch.from_numpy(w.query_start)} if mq else {}),
         **({"k_scale": torch.from_numpy(w.k_scale), "v_scale": torch.from_numpy(w.v_scale)}
-           if fp8 else {})}.items()}
+           if fp8 else {}),
+        **({"prefix_lens": torch.full((w.num_seqs // G,), int(w.meta["shared_prefix_tokens"]),
+                                      dtype=torch.int32)} if shared else {})}.items()}
     out = torch.empty_like(d["q"])
-    if mq:
+    if shared:
+        ws_bytes = pa.decode_shared_prefix_workspace_size(
+            w.num_seqs, w.num_q_heads, w.num_kv_heads, w.head_dim, w.max_blocks_per_seq,
+            w.block_size, w.dtype, w.partition_tokens, G)
+    elif mq:
         ws_bytes = pa.multi_query_workspace_size(w.num_query_tokens, w.num_q_heads,
                                                  w.num_kv_heads, w.head_dim, w.max_blocks_per_seq,
                                                  w.block_size, w.dtype, w.partition_tokens)
@@ -409,6 +422,11 @@ def _measure(args, name, layout, dev, dist, ws_world):
             pa.decode_fp8(out, dd["q"], dd["k_cache"], dd["v_cache"], dd["k_scale"],
                           dd["v_scale"], dd["block_tables"], dd["context_lens"], w.scale,
                           partition_tokens=w.partition_tokens, workspace=workspace, d_err=d_err)
+        elif shared:
+            pa.decode_shared_prefix(out, dd["q"], dd["k_cache"], dd["v_cache"],
+                                    dd["block_tables"], dd["context_lens"], w.scale, G,
+                                    dd["prefix_lens"], partition_tokens=w.partition_tokens,
+                                    workspace=workspace, d_err=d_err)
         elif mq:
             pa.multi_query(out, dd["q"], dd["query_start"], dd["k_cache"], dd["v_cache"],
                            dd["block_tables"], dd["context_lens"], w.scale,
@@ -464,7 +482,7 @@ def _measure(args, name, layout, dev, dist, ws_world):
     # one host-to-device copy, the kernels, the output back to pinned host memory
     dims = pa.StepDims(w.num_seqs, w.num_query_tokens if mq else 0, w.num_tokens, w.num_pairs,
                        w.num_q_heads, w.num_kv_heads, w.head_dim, w.block_size, w.num_blocks,
-                       w.max_blocks_per_seq, pa.DTYPE_CODE[d["q"].dtype])
+                       w.max_blocks_per_seq, pa.DTYPE_CODE[d["q"].dtype], G if shared else 0)
     total, offs = pa.step_layout(dims)
     host_in = torch.zeros(total, dtype=torch.uint8, pin_memory=True)
     for k in pa.STEP_INPUTS:
@@ -499,12 +517,12 @@ def _measure(args, name, layout, dev, dist, ws_world):
     flops = 4 * w.head_dim * w.num_q_heads * sum(n for _, _, n in _rows(w))
     tensor_peak, tensor_kind = _tensor_peak()
     alu_peak = _alu_peak_tflops(sms)
-    tc_path = plan["kernel"] in TC_KERNELS
+    tc_path = plan["kernel"] in TC_KERNELS or shared
     tensor_bound = tc_path and flops / (tensor_peak * 1e12) > unique_bytes / (peak * 1e9)
     alu_bound = not tc_path and flops / (alu_peak * 1e12) > unique_bytes / (peak * 1e9)
     ncu = _ncu_record(name + ("" if layout == "paged" else "_" + layout))
     traffic = ncu.get("traffic_bytes_per_launch") if ncu else None
-    kernel = f"{'pa_multi_query' if mq else 'pa_decode_fp8' if fp8 else 'pa_decode'}: " \
+    kernel = f"{'pa_multi_query' if mq else 'pa_decode_fp8' if fp8 else 'pa_decode_shared_prefix' if shared else 'pa_decode'}: " \
              f"{plan['kernel']} kernel, merge {plan['merge']}, {plan['launches']} launch(es)"
     hbm_ach = unique_bytes / (dec_ms * 1e-3) / 1e9
     common = {"kernel": kernel, "avg_launch_ms": round(dec_ms, 5), "traffic": traffic,
@@ -797,6 +815,9 @@ def main():
     ap.add_argument("--partition", type=int, default=None,
                     help="tokens per split-K partition (default: the workload's, else the library's)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-shared-prefix", action="store_true",
+                    help="decode shared-prefix workloads with pa_decode instead of "
+                         "pa_decode_shared_prefix")
     ap.add_argument("--no-also", action="store_true",
                     help="skip the 13B-shaped and contiguous-layout lines of the default run")
     ap.add_argument("--layout", choices=("paged", "contiguous"), default="paged",

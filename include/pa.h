@@ -249,6 +249,48 @@ pa_status pa_multi_query(void* out, const void* q, int num_query_tokens,
                          float scale, int partition_tokens, pa_dtype dtype, void* workspace,
                          size_t workspace_bytes, uint32_t* d_err, pa_stream_t stream);
 
+/* pa_decode_shared_prefix -- pa_decode for groups of sequences that share a
+ * prompt prefix (parallel sampling, beam candidates).
+ *
+ * Sequences come in groups of group_size consecutive sequences (num_seqs a
+ * multiple of group_size); the first prefix_lens[j] tokens of every sequence
+ * of group j are the same physical blocks -- the first prefix_lens[j] /
+ * block_size entries of their block tables are equal, blocks shared with a
+ * reference count ("PagedAttention" (compassingai.com) §6; wmrh.cn "paged
+ * attention", the shared-KV-block part: sequences that share a prompt share
+ * its blocks until they diverge).  The result is exactly pa_decode's
+ * definition; what changes is the reading: the prefix of each group is read
+ * once, for all its sequences and the query heads of a kv head together
+ * (rows: group_size x num_q_heads / num_kv_heads, on the 128-row tensor-core
+ * kernel, through the table of the group's first sequence), and each
+ * sequence reads only its own tokens after the prefix (the grouped
+ * tensor-core decode kernel); a merge kernel combines the two partial
+ * softmax states of every (sequence, head).
+ *   prefix_lens  device int32 [num_seqs / group_size].  A group whose prefix
+ *                is not a positive multiple of block_size, or is longer than
+ *                the context of one of its sequences (or a context is out of
+ *                range), is decoded without sharing -- the same result.  The
+ *                equality of the shared table entries is the caller's promise:
+ *                the prefix is read through the group's first table.
+ * The shared passes run for 16-bit K/V, head_dim 128, 4 to 16 query heads per
+ * kv head, group_size x (num_q_heads / num_kv_heads) <= 128 and a partition
+ * length that is a multiple of 128 tokens; other shapes (and group_size 1)
+ * run pa_decode itself.  Workspace: pa_decode_shared_prefix_workspace_size()
+ * bytes, with pa_decode's rules.  Kernels: 3 (prefix pass, own pass, merge).
+ */
+size_t pa_decode_shared_prefix_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads,
+                                              int head_dim, int max_blocks_per_seq,
+                                              int block_size, pa_dtype dtype,
+                                              int partition_tokens, int group_size);
+pa_status pa_decode_shared_prefix(void* out, const void* q, const void* k_cache,
+                                  const void* v_cache, const int32_t* block_tables,
+                                  int max_blocks_per_seq, const int32_t* context_lens,
+                                  int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                                  int block_size, int num_blocks, float scale, int group_size,
+                                  const int32_t* prefix_lens, int partition_tokens,
+                                  pa_dtype dtype, void* workspace, size_t workspace_bytes,
+                                  uint32_t* d_err, pa_stream_t stream);
+
 /* pa_decode_static_workspace -- pa_decode for callers that cannot allocate.
  *
  * The pages have no counterpart to this call: it exists for callers that must
@@ -392,6 +434,7 @@ pa_status pa_attention_plan(int num_seqs, int num_query_tokens, int multi_query,
  *   5 context_lens  int32 [num_seqs]
  *   6 block_mapping int32 [num_pairs][2]
  *   7 query_start   int32 [num_seqs + 1] (multi-query steps only)
+ *   8 prefix_lens   int32 [num_seqs / prefix_group] (shared-prefix decode only)
  * The call enqueues on `stream`: one host-to-device copy of the whole buffer
  * into dev_stage (device memory of pa_step_layout() bytes, 256-byte
  * aligned, owned by the caller), the kernels of the three operations reading
@@ -401,10 +444,12 @@ pa_status pa_attention_plan(int num_seqs, int num_query_tokens, int multi_query,
  * caller synchronises the stream before reading host_out or reusing host_in.
  * E4M3 caches: pass k_scale / v_scale (device, [num_blocks][num_kv_heads]);
  * the step then uses the *_fp8 calls (decode only, dtype F16 or BF16).
+ * prefix_group > 0 (decode over 16-bit caches): attention is
+ * pa_decode_shared_prefix with groups of prefix_group sequences.
  * Semantics, errors and the workspace: those of the calls it makes; every
  * host check runs before anything is enqueued.
  */
-#define PA_STEP_NUM_INPUTS 8
+#define PA_STEP_NUM_INPUTS 9
 typedef struct pa_step_dims {
     int num_seqs;
     int num_query_tokens;  /* 0: decode, one query per sequence */
@@ -417,6 +462,7 @@ typedef struct pa_step_dims {
     int num_blocks;
     int max_blocks_per_seq;
     pa_dtype dtype;        /* of q, out and the new tokens (and the cache unless E4M3) */
+    int prefix_group;      /* > 0: groups of this many sequences share prefixes */
 } pa_step_dims;
 /* Byte offsets of the eight inputs in the packed buffer; returns its size
  * (0 for invalid dimensions). */

@@ -32,9 +32,11 @@ EXPORTED = ("pa_abi_version", "pa_status_string", "pa_kv_write", "pa_copy_blocks
             "pa_decode", "pa_decode_static_workspace", "pa_multi_query_partition_tokens",
             "pa_multi_query_workspace_size", "pa_multi_query", "pa_kv_write_fp8",
             "pa_copy_blocks_fp8", "pa_swap_blocks_fp8", "pa_decode_fp8",
-            "pa_attention_plan", "pa_step_layout", "pa_step_host", "pa_selftest_wait_timeout")
+            "pa_attention_plan", "pa_step_layout", "pa_step_host",
+            "pa_decode_shared_prefix_workspace_size", "pa_decode_shared_prefix",
+            "pa_selftest_wait_timeout")
 STEP_INPUTS = ("q", "k_new", "v_new", "slot_mapping", "block_tables", "context_lens",
-               "block_mapping", "query_start")
+               "block_mapping", "query_start", "prefix_lens")
 KERNEL_NAMES = {1: "simt", 2: "simt_fp8", 3: "tc_grouped", 4: "tc_grouped_fp8", 5: "tc_128_rows"}
 MERGE_NAMES = {0: "none", 1: "kernel"}
 
@@ -46,7 +48,7 @@ class StepDims(ctypes.Structure):
                 ("num_q_heads", ctypes.c_int), ("num_kv_heads", ctypes.c_int),
                 ("head_dim", ctypes.c_int), ("block_size", ctypes.c_int),
                 ("num_blocks", ctypes.c_int), ("max_blocks_per_seq", ctypes.c_int),
-                ("dtype", ctypes.c_int)]
+                ("dtype", ctypes.c_int), ("prefix_group", ctypes.c_int)]
 
 
 class _Plan(ctypes.Structure):
@@ -124,6 +126,12 @@ def load() -> ctypes.CDLL:
         lib.pa_step_host.restype = i32
         lib.pa_step_host.argtypes = [ctypes.POINTER(StepDims), vp, vp, vp, vp, vp, vp, vp, vp,
                                      ctypes.c_float, i32, vp, u64, vp, vp]
+        lib.pa_decode_shared_prefix_workspace_size.restype = u64
+        lib.pa_decode_shared_prefix_workspace_size.argtypes = [i32] * 9
+        lib.pa_decode_shared_prefix.restype = i32
+        lib.pa_decode_shared_prefix.argtypes = [vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32,
+                                                i32, i32, ctypes.c_float, i32, vp, i32, i32, vp,
+                                                u64, vp, vp]
         lib.pa_attention_plan.restype = i32
         lib.pa_attention_plan.argtypes = [i32, i32, i32, i32, i32, i32, i32, i32, i32, i32, i32,
                                           i32, ctypes.POINTER(_Plan)]
@@ -306,6 +314,49 @@ def multi_query_partition_tokens(num_query_tokens: int, num_q_heads: int, num_kv
     return int(load().pa_multi_query_partition_tokens(num_query_tokens, num_q_heads, num_kv_heads,
                                                       head_dim, max_blocks_per_seq, block_size,
                                                       _dtype_code(dtype), partition_tokens))
+
+
+def decode_shared_prefix_workspace_size(num_seqs: int, num_q_heads: int, num_kv_heads: int,
+                                        head_dim: int, max_blocks_per_seq: int, block_size: int,
+                                        dtype, partition_tokens: int = 0,
+                                        group_size: int = 1) -> int:
+    return int(load().pa_decode_shared_prefix_workspace_size(
+        num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq, block_size,
+        _dtype_code(dtype), partition_tokens, group_size))
+
+
+def decode_shared_prefix(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor,
+                         v_cache: torch.Tensor, block_tables: torch.Tensor,
+                         context_lens: torch.Tensor, scale: float, group_size: int,
+                         prefix_lens: torch.Tensor, partition_tokens: int = 0,
+                         workspace: Optional[torch.Tensor] = None,
+                         d_err: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """pa_decode for groups of group_size consecutive sequences whose first
+    prefix_lens[group] tokens are the same physical blocks (read once per
+    group); the result is pa_decode's."""
+    for n, t in (("out", out), ("q", q), ("k_cache", k_cache), ("v_cache", v_cache),
+                 ("block_tables", block_tables), ("context_lens", context_lens),
+                 ("prefix_lens", prefix_lens)):
+        _cuda_contig(n, t)
+    if (block_tables.dtype != torch.int32 or context_lens.dtype != torch.int32 or
+            prefix_lens.dtype != torch.int32):
+        raise ValueError("block_tables, context_lens and prefix_lens must be int32")
+    S, Hq, d = q.shape
+    NB, Hkv, B, d2 = k_cache.shape
+    if d2 != d or out.shape != q.shape or out.dtype != q.dtype or k_cache.dtype != q.dtype:
+        raise ValueError("q, out, k_cache and v_cache must agree in head_dim and dtype")
+    MB = block_tables.shape[1]
+    if workspace is None:
+        workspace = torch.zeros(decode_shared_prefix_workspace_size(
+            S, Hq, Hkv, d, MB, B, q.dtype, partition_tokens, group_size),
+            dtype=torch.uint8, device=q.device)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    _check(load().pa_decode_shared_prefix(
+        _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), MB,
+        _ptr(context_lens), S, Hq, Hkv, d, B, NB, float(scale), int(group_size),
+        _ptr(prefix_lens), int(partition_tokens), DTYPE_CODE[q.dtype], _ptr(workspace),
+        ws_bytes, _ptr(d_err), _stream(stream, q.device)), "pa_decode_shared_prefix")
+    return out
 
 
 def multi_query_workspace_size(num_query_tokens: int, num_q_heads: int, num_kv_heads: int,

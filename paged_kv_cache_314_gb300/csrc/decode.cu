@@ -105,15 +105,17 @@ bool make_pool_map(CUtensorMap* map, const void* pool, long long rows, pa_dtype 
 // The query rows [tokens][Hq][128] of 16-bit elements as a 3-D tensor
 // {128 columns, Hq heads, tokens}: one [64 x g x 128/g] box with 128-byte
 // swizzle holds one 64-column half of the 128 rows (token-major, then head) of
-// a multi-query item of the 128-row kernel.
+// a multi-query item of the 128-row kernel (box_tokens: other than 128/g for
+// the shared-prefix pass, whose "tokens" are the decode sequences of a group).
 bool make_q_map(CUtensorMap* map, const void* q, int num_tokens, int num_q_heads, int group,
-                pa_dtype dtype) {
+                pa_dtype dtype, int box_tokens = 0) {
     PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
-    if (encode == nullptr || group <= 0 || 128 % group != 0) return false;
+    if (box_tokens == 0) box_tokens = group > 0 ? 128 / group : 0;
+    if (encode == nullptr || group <= 0 || box_tokens <= 0 || group * box_tokens > 128) return false;
     const cuuint64_t dims[3] = {128, static_cast<cuuint64_t>(num_q_heads),
                                 static_cast<cuuint64_t>(num_tokens)};
     const cuuint64_t strides[2] = {128 * 2, static_cast<cuuint64_t>(num_q_heads) * 128 * 2};
-    const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(group), static_cast<cuuint32_t>(128 / group)};
+    const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(group), static_cast<cuuint32_t>(box_tokens)};
     const cuuint32_t elem_strides[3] = {1, 1, 1};
     return encode(map, dtype == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
                   3, const_cast<void*>(q), dims, strides, box, elem_strides,
@@ -615,4 +617,166 @@ extern "C" pa_status pa_attention_plan(int num_seqs, int num_query_tokens, int m
                      block_size, num_blocks, 1.0f, P, multi_query && partition_tokens == 0, q_dtype,
                      nullptr, 0, nullptr, nullptr, plan};
     return run_attention(a);
+}
+
+// ---- shared-prefix decode -----------------------------------------------------
+
+namespace pa {
+namespace {
+
+// Partition length of the prefix pass: the sequences' own partition length,
+// halved (in multiples of 128 tokens) while the groups' kv heads would give
+// fewer than kPrefixItems work items for contexts of the longest allowed
+// length (a fixed function of the sizes, so the workspace size needs no
+// device query).
+constexpr long long kPrefixItems = 384;
+
+int prefix_partition(int num_groups, int num_kv_heads, long long max_ctx, int P) {
+    int Pp = P;
+    while (Pp > 128 && static_cast<long long>(num_groups) * num_kv_heads * ((max_ctx + Pp - 1) / Pp) <
+                           kPrefixItems)
+        Pp = std::max(128, (Pp / 2) / 128 * 128);
+    return Pp;
+}
+
+// The shapes the shared-prefix passes run on: 16-bit K/V, head_dim 128, 4-16
+// query heads per kv head (the grouped tensor-core decode kernel for each
+// sequence's own tokens), a group's rows (sequences x heads) within one
+// 128-row tile, partitions a multiple of 128 tokens.
+bool prefix_shape(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                  int num_blocks, pa_dtype dtype, int group_size, int P) {
+    if (group_size < 2 || num_seqs % group_size != 0) return false;
+    if (!tc_shape(num_q_heads, num_kv_heads, head_dim, dtype) || dtype == PA_E4M3) return false;
+    const int g = num_q_heads / num_kv_heads;
+    const long long pool_rows = static_cast<long long>(num_blocks) * num_kv_heads * block_size;
+    return group_size * g <= 128 && P % 128 == 0 && pool_rows < 0x7fffffffLL;
+}
+
+struct PrefixPlan {
+    int P, Pp, prefix_parts, max_parts;
+    WsLayout ws;
+};
+
+PrefixPlan prefix_plan(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                       int max_blocks_per_seq, int block_size, int group_size, int P) {
+    PrefixPlan r;
+    const long long max_ctx = static_cast<long long>(max_blocks_per_seq) * block_size;
+    r.P = P;
+    r.Pp = prefix_partition(num_seqs / group_size, num_kv_heads, max_ctx, P);
+    r.prefix_parts = static_cast<int>((max_ctx + r.Pp - 1) / r.Pp);
+    r.max_parts = r.prefix_parts + static_cast<int>((max_ctx + P - 1) / P);
+    r.ws = ws_layout(num_seqs, num_q_heads, head_dim, r.max_parts);
+    return r;
+}
+
+}  // namespace
+}  // namespace pa
+
+extern "C" size_t pa_decode_shared_prefix_workspace_size(int num_seqs, int num_q_heads,
+                                                         int num_kv_heads, int head_dim,
+                                                         int max_blocks_per_seq, int block_size,
+                                                         pa_dtype dtype, int partition_tokens,
+                                                         int group_size) {
+    using namespace pa;
+    const size_t plain = pa_decode_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim,
+                                                  max_blocks_per_seq, block_size, dtype,
+                                                  partition_tokens);
+    if (plain == 0) return 0;
+    const int P = pa_decode_partition_tokens(num_q_heads, num_kv_heads, head_dim,
+                                             max_blocks_per_seq, block_size, dtype, partition_tokens);
+    if (!prefix_shape(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, 1, dtype,
+                      group_size, P))
+        return plain;
+    const PrefixPlan pl = prefix_plan(num_seqs, num_q_heads, num_kv_heads, head_dim,
+                                      max_blocks_per_seq, block_size, group_size, P);
+    return std::max(plain, pl.ws.bytes);
+}
+
+extern "C" pa_status pa_decode_shared_prefix(
+    void* out, const void* q, const void* k_cache, const void* v_cache,
+    const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
+    int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int block_size, int num_blocks,
+    float scale, int group_size, const int32_t* prefix_lens, int partition_tokens, pa_dtype dtype,
+    void* workspace, size_t workspace_bytes, uint32_t* d_err, pa_stream_t stream) {
+    using namespace pa;
+    const pa_status c = check_decode(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq,
+                                     context_lens, num_seqs, num_q_heads, num_kv_heads, head_dim,
+                                     block_size, num_blocks, scale, partition_tokens, dtype);
+    if (c != PA_OK) return c;
+    if (group_size <= 0) return PA_ERR_INVALID_ARG;
+    if (num_seqs == 0) return PA_OK;
+    if (num_seqs % group_size != 0 || prefix_lens == nullptr) return PA_ERR_INVALID_ARG;
+    const int P = pa_decode_partition_tokens(num_q_heads, num_kv_heads, head_dim,
+                                             max_blocks_per_seq, block_size, dtype, partition_tokens);
+    if (!prefix_shape(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, dtype,
+                      group_size, P))  // no shared pass for this shape: plain decode
+        return pa_decode(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
+                         num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks,
+                         scale, partition_tokens, dtype, workspace, workspace_bytes, d_err, stream);
+    const PrefixPlan pl = prefix_plan(num_seqs, num_q_heads, num_kv_heads, head_dim,
+                                      max_blocks_per_seq, block_size, group_size, P);
+    if (workspace == nullptr) return PA_ERR_INVALID_ARG;
+    if (workspace_bytes < pl.ws.bytes) return PA_ERR_WORKSPACE_TOO_SMALL;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return PA_ERR_INVALID_ARG;
+    const int g = num_q_heads / num_kv_heads;
+    const long long pool_rows = static_cast<long long>(num_blocks) * num_kv_heads * block_size;
+    CUtensorMap map_k, map_v, map_q;
+    if (!make_pool_map(&map_k, k_cache, pool_rows, dtype) ||
+        !make_pool_map(&map_v, v_cache, pool_rows, dtype) ||
+        !make_q_map(&map_q, q, num_seqs, num_q_heads, g, dtype, group_size))
+        return PA_ERR_CUDA;
+
+    unsigned char* wsb = static_cast<unsigned char*>(workspace);
+    DecodeParams p;
+    p.out = out;
+    p.q = q;
+    p.k_cache = static_cast<const unsigned char*>(k_cache);
+    p.v_cache = static_cast<const unsigned char*>(v_cache);
+    p.k_scale = nullptr;
+    p.v_scale = nullptr;
+    p.block_tables = block_tables;
+    p.context_lens = context_lens;
+    p.query_start = nullptr;
+    p.counters = reinterpret_cast<unsigned int*>(wsb);
+    p.ws_m = reinterpret_cast<float*>(wsb + pl.ws.m_off);
+    p.ws_l = reinterpret_cast<float*>(wsb + pl.ws.l_off);
+    p.ws_o = reinterpret_cast<float*>(wsb + pl.ws.o_off);
+    p.d_err = d_err;
+    p.num_seqs = num_seqs;
+    p.num_q_heads = num_q_heads;
+    p.num_kv_heads = num_kv_heads;
+    p.num_query_tokens = num_seqs;
+    p.group = g;
+    p.head_tiles = num_kv_heads;
+    p.tile_heads = g;
+    p.tile_heads_log2 = log2_exact(g);
+    p.tile_tokens = 1;
+    p.max_blocks_per_seq = max_blocks_per_seq;
+    p.block_size = block_size;
+    p.num_blocks = num_blocks;
+    p.partition_tokens = P;
+    p.max_parts = pl.max_parts;
+    p.qk_scale_log2 = scale * 1.4426950408889634f;  // log2(e)
+    p.prefix_lens = prefix_lens;
+    p.prefix_group = group_size;
+    p.prefix_partition_tokens = pl.Pp;
+    p.prefix_parts = pl.prefix_parts;
+    p.skip_merge = 1;
+    const cudaStream_t st = as_cuda(stream);
+    // 1. each group's prefix, once, on the 128-row kernel (rows: the group's
+    //    sequences x the g heads of a kv head)
+    DecodeParams pp = p;
+    pp.partition_tokens = pl.Pp;
+    pp.tile_tokens = group_size;
+    pa_status r = dtype == PA_BF16 ? launch_prefill_tc_bf16(pp, map_k, map_v, map_q, st)
+                                   : launch_prefill_tc_f16(pp, map_k, map_v, map_q, st);
+    if (r != PA_OK) return r;
+    // 2. each sequence's own tokens on the grouped tensor-core decode kernel
+    r = dtype == PA_BF16 ? launch_decode_tc_bf16(p, map_k, map_v, st)
+                         : launch_decode_tc_f16(p, map_k, map_v, st);
+    if (r != PA_OK) return r;
+    // 3. both ranges of partial states merged per (sequence, head)
+    p.skip_merge = 0;
+    return dtype == PA_BF16 ? launch_merge<__nv_bfloat16, 128>(p, st)
+                            : launch_merge<__half, 128>(p, st);
 }

@@ -96,6 +96,18 @@ struct DecodeParams {
     int partition_tokens;
     int max_parts;
     float qk_scale_log2;  // scale * log2(e)
+    // Shared-prefix decode (pa_decode_shared_prefix): sequences come in groups
+    // of prefix_group consecutive sequences whose first prefix_lens[group]
+    // tokens are the same physical blocks.  The prefix pass (128-row kernel)
+    // reads them once per group and writes partial states 0 .. into the
+    // partition slots of every member's rows; each sequence's own pass starts
+    // at the prefix and writes partition slots prefix_parts ..; the merge
+    // kernel combines both ranges.  Null: plain decode.
+    const int32_t* prefix_lens = nullptr;  // [num_seqs / prefix_group]
+    int prefix_group = 0;
+    int prefix_partition_tokens = 0;  // partition length of the prefix pass
+    int prefix_parts = 0;             // partition slots reserved for the prefix pass
+    int skip_merge = 0;               // the launch leaves the merge to a later kernel
 };
 
 __host__ __device__ constexpr int align16(int x) { return (x + 15) / 16 * 16; }
@@ -227,6 +239,32 @@ struct ReduceScatter {
 __device__ __forceinline__ int items_of(int ctx, int max_ctx, int P) {
     if (ctx < 0 || ctx > max_ctx) return 1;  // one item writes the zero rows
     return ctx == 0 ? 1 : (ctx + P - 1) / P;
+}
+
+// Shared-prefix decode: the prefix length of group grp if it can be used --
+// positive, a multiple of the block size, and within the (in-range) context
+// of every member -- else 0, and the group is decoded without sharing (the
+// same result).  The prefix's blocks are read through the table of the
+// group's first sequence.
+__device__ __forceinline__ int group_prefix(const DecodeParams& p, int grp) {
+    const int pre = __ldg(p.prefix_lens + grp);
+    const int max_ctx = p.max_blocks_per_seq * p.block_size;
+    bool ok = pre > 0 && pre % p.block_size == 0;
+    // no early exit: the members' loads are issued together
+#pragma unroll 8
+    for (int j = 0; j < p.prefix_group; ++j) {
+        const int c = __ldg(p.context_lens + grp * p.prefix_group + j);
+        ok = ok && c >= pre && c <= max_ctx;
+    }
+    return ok ? pre : 0;
+}
+
+// Items of a sequence's own pass over tokens [start, ctx) (start = 0 outside
+// shared-prefix decode): at least one, which writes an empty state (or the
+// zero row of an out-of-range context).
+__device__ __forceinline__ int items_from(int ctx, int start, int max_ctx, int P) {
+    if (ctx < 0 || ctx > max_ctx) return 1;
+    return ctx <= start ? 1 : (ctx - start + P - 1) / P;
 }
 
 // A sequence's queries and how many work items it has.  One query per
@@ -687,7 +725,7 @@ __device__ __forceinline__ void merge_row(const DecodeParams& p, size_t row, int
 #pragma unroll
         for (int k = 0; k < kChunk; ++k) {
             const bool in = i0 + k < nparts;
-            const size_t r = base + (in ? i0 + k : i0);  // an address inside the row either way
+            const size_t r = base + (in ? i0 + k : i0);  // a slot inside the row either way
             mi[k] = in ? __ldcg(p.ws_m + r) : -INFINITY;
             li[k] = in ? __ldcg(p.ws_l + r) : 0.f;
             const float* po = p.ws_o + r * D + lane * kCols;
@@ -1002,6 +1040,86 @@ __global__ void __launch_bounds__(128) decode_reduce_kernel(const DecodeParams p
     }
 }
 
+// Shared-prefix decode: the merge of one (sequence, head) row with a single
+// round of loads -- the group's prefix length, its members' contexts and the
+// row's first four prefix and first four own partial states are all requested
+// before any of them is used (which of the eight states exist is known only
+// from the lengths); states past those four are merged after, one by one.
+template <typename T, int D>
+__device__ __forceinline__ void merge_prefix_row(const DecodeParams& p, int s, size_t row,
+                                                 int lane) {
+    constexpr int kCols = D / 32;
+    constexpr int kQ = 4;  // states of each range requested up front
+    const int G = p.prefix_group, grp = s / G;
+    const int max_ctx = p.max_blocks_per_seq * p.block_size;
+    const size_t base = row * p.max_parts;
+    const int pre_raw = __ldg(p.prefix_lens + grp);
+    const int c = __ldg(p.context_lens + grp * G + min(lane, G - 1));
+    float mi[2 * kQ], li[2 * kQ], oi[2 * kQ][kCols];
+#pragma unroll
+    for (int k = 0; k < 2 * kQ; ++k) {
+        // only slots that can hold a state for some context (the ranges' sizes)
+        const bool may = k < kQ ? k < p.prefix_parts : k - kQ < p.max_parts - p.prefix_parts;
+        const int slot = min(k < kQ ? k : p.prefix_parts + (k - kQ), p.max_parts - 1);
+        mi[k] = may ? __ldcg(p.ws_m + base + slot) : -INFINITY;
+        li[k] = may ? __ldcg(p.ws_l + base + slot) : 0.f;
+        const float* po = p.ws_o + (base + slot) * D + lane * kCols;
+        if constexpr (kCols == 4) {
+            const float4 v = may ? __ldcg(reinterpret_cast<const float4*>(po))
+                                 : make_float4(0.f, 0.f, 0.f, 0.f);
+            oi[k][0] = v.x;
+            oi[k][1] = v.y;
+            oi[k][2] = v.z;
+            oi[k][3] = v.w;
+        } else {
+            const float2 v = may ? __ldcg(reinterpret_cast<const float2*>(po)) : make_float2(0.f, 0.f);
+            oi[k][0] = v.x;
+            oi[k][1] = v.y;
+        }
+    }
+    // the group's prefix as group_prefix decides it, lane j holding member j's context
+    const bool ok = __all_sync(0xffffffffu, c >= pre_raw && c <= max_ctx);
+    const int pre = ok && pre_raw > 0 && pre_raw % p.block_size == 0 ? pre_raw : 0;
+    const int ctx = __shfl_sync(0xffffffffu, c, s - grp * G);
+    const int npre = (pre + p.prefix_partition_tokens - 1) / p.prefix_partition_tokens;
+    const int nown = items_from(ctx, pre, max_ctx, p.partition_tokens);
+    float M = -INFINITY;
+#pragma unroll
+    for (int k = 0; k < 2 * kQ; ++k) {
+        const bool in = k < kQ ? k < npre : k - kQ < nown;
+        if (!in) mi[k] = -INFINITY;
+        M = fmaxf(M, mi[k]);
+    }
+    for (int j = kQ; j < npre; ++j) M = fmaxf(M, __ldcg(p.ws_m + base + j));
+    for (int j = kQ; j < nown; ++j) M = fmaxf(M, __ldcg(p.ws_m + base + p.prefix_parts + j));
+    float L = 0.f, O[kCols];
+#pragma unroll
+    for (int cc = 0; cc < kCols; ++cc) O[cc] = 0.f;
+    if (M != -INFINITY) {
+#pragma unroll
+        for (int k = 0; k < 2 * kQ; ++k) {
+            const float sc = fast_exp2(mi[k] - M);  // absent or empty state: 2^-inf = 0
+            L = fmaf(sc, li[k], L);
+#pragma unroll
+            for (int cc = 0; cc < kCols; ++cc) O[cc] = fmaf(sc, oi[k][cc], O[cc]);
+        }
+        for (int r = 0; r < 2; ++r) {  // the rest of each range (long contexts)
+            const int n = r == 0 ? npre : nown, off = r == 0 ? 0 : p.prefix_parts;
+            for (int j = kQ; j < n; ++j) {
+                const size_t w = base + off + j;
+                const float sc = fast_exp2(__ldcg(p.ws_m + w) - M);
+                L = fmaf(sc, __ldcg(p.ws_l + w), L);
+#pragma unroll
+                for (int cc = 0; cc < kCols; ++cc)
+                    O[cc] = fmaf(sc, __ldcg(p.ws_o + w * D + lane * kCols + cc), O[cc]);
+            }
+        }
+    }
+    T* out = static_cast<T*>(p.out) + row * D + lane * kCols;
+#pragma unroll
+    for (int cc = 0; cc < kCols; ++cc) out[cc] = Elem<T>::from_float(L > 0.f ? O[cc] / L : 0.f);
+}
+
 // Split-K merge as its own kernel, one warp per (query row, head), for
 // sequences of at most kRowMergeMaxParts partitions.
 template <typename T, int D>
@@ -1011,6 +1129,13 @@ __global__ void __launch_bounds__(128) decode_merge_rows_kernel(const DecodePara
     const long long sh = static_cast<long long>(blockIdx.x) * 4 + warp;  // row x query head
     if (sh >= static_cast<long long>(p.num_query_tokens) * p.num_q_heads) return;
     const int tok = static_cast<int>(sh / p.num_q_heads);
+    if (p.prefix_lens != nullptr) {  // decode: row tok is sequence tok
+        if (tok >= p.num_seqs) return;
+        const int ctx = __ldg(p.context_lens + tok);
+        if (ctx < 0 || ctx > p.max_blocks_per_seq * p.block_size) return;  // zero row written
+        merge_prefix_row<T, D>(p, tok, static_cast<size_t>(sh), lane);
+        return;
+    }
     int s = tok;
     if (p.query_start != nullptr) {  // the sequence whose queries hold row tok
         int lo = 0, hi = p.num_seqs;  // first k in [lo, hi) with query_start[k + 1] > tok
@@ -1035,8 +1160,9 @@ __global__ void __launch_bounds__(128) decode_merge_rows_kernel(const DecodePara
 // stream serialisation: it waits for the decode kernel inside).
 template <typename T, int D>
 inline pa_status launch_merge(const DecodeParams& p, cudaStream_t stream) {
+    if (p.skip_merge) return PA_OK;
     const long long rows = static_cast<long long>(p.num_query_tokens) * p.num_q_heads;
-    if (p.max_parts <= kRowMergeMaxParts) {
+    if (p.max_parts <= kRowMergeMaxParts || p.prefix_lens != nullptr) {
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(static_cast<unsigned>((rows + 3) / 4));
         cfg.blockDim = dim3(128);

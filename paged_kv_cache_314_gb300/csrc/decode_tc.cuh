@@ -152,6 +152,8 @@ __device__ __forceinline__ void tc_produce(const DecodeParams& p, const CUtensor
     int s_cur = 0, base_items = 0, win0 = 0;
     SeqQueries sq_lane{0, 0, 0, kMulti};
     int items_lane = 0;
+    int start_lane = 0;  // shared-prefix decode: the first token of the sequence's own pass
+    const bool prefix = !kMulti && p.prefix_lens != nullptr;
     auto load_window = [&]() {
         const int sl = win0 + lane;
         if constexpr (kMulti) {
@@ -160,7 +162,8 @@ __device__ __forceinline__ void tc_produce(const DecodeParams& p, const CUtensor
             if (sl < S && !sq_lane.rows_ok(p.num_query_tokens)) report(p.d_err, PA_DERR_CTX_OOB);
         } else {
             sq_lane.ctx = sl < S ? __ldg(p.context_lens + sl) : 0;
-            items_lane = sl < S ? HT * items_of(sq_lane.ctx, max_ctx, P) : 0;
+            start_lane = (prefix && sl < S) ? group_prefix(p, sl / p.prefix_group) : 0;
+            items_lane = sl < S ? HT * items_from(sq_lane.ctx, start_lane, max_ctx, P) : 0;
         }
     };
     load_window();
@@ -216,7 +219,8 @@ __device__ __forceinline__ void tc_produce(const DecodeParams& p, const CUtensor
         const bool valid = sq.ctx_ok(max_ctx);
         const int tile_tokens = kMulti ? p.tile_tokens : 1;
         const int qlen = sq.q1 - sq.q0;
-        const int np = valid ? items_of(ctx, max_ctx, P) : 1;
+        const int start = prefix ? __shfl_sync(0xffffffffu, start_lane, s_cur - win0) : 0;
+        const int np = valid ? items_from(ctx, start, max_ctx, P) : 1;
         const int ntt = kMulti ? (qlen + tile_tokens - 1) / tile_tokens : 1;
         const int i_loc = item_id - base_items;
         if (kMulti && (i_loc < 0 || i_loc >= __shfl_sync(0xffffffffu, items_lane, s_cur - win0))) {
@@ -233,7 +237,7 @@ __device__ __forceinline__ void tc_produce(const DecodeParams& p, const CUtensor
         const int ntok = kMulti ? min(tile_tokens, qlen - i0) : 1;
         const int lim_first = ctx - qlen + i0 + 1;  // tokens the item's first query sees
         const int lim_last = lim_first + ntok - 1;
-        const int tok_begin = part * P;
+        const int tok_begin = start + part * P;
         const int tok_end = valid ? max(tok_begin, min(tok_begin + P, lim_last)) : tok_begin;
         const int nst = tok_end > tok_begin ? (tok_end - tok_begin + C::kStageTok - 1) / C::kStageTok : 1;
         if (!valid && lane == 0) report(p.d_err, PA_DERR_CTX_OOB);
@@ -248,8 +252,9 @@ __device__ __forceinline__ void tc_produce(const DecodeParams& p, const CUtensor
         if (lane == 0) {
             recs[qs].row0 = sq.q0 + i0;
             recs[qs].hq0 = hq0;
-            recs[qs].part = part;
-            recs[qs].nparts = valid ? np : 0;
+            // shared-prefix decode: always a partial state, in the slots after the prefix's
+            recs[qs].part = prefix ? p.prefix_parts + part : part;
+            recs[qs].nparts = valid ? (prefix ? p.prefix_parts + np : np) : 0;
             recs[qs].nrows = ntok * g;
             const uint32_t qf = qfull0 + 8 * qs;
             mbar_arrive_expect_tx(qf, row_bytes * ntok);

@@ -181,9 +181,16 @@ __device__ __forceinline__ void pf_produce(const DecodeParams& p, const CUtensor
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + C::kMiscOff + 4);
     int k_only = -1;  // a stage whose K copies were issued but not its V copies (abort)
 
-    const int S = p.num_seqs, P = p.partition_tokens, B = p.block_size, g = p.group;
-    const int Tq = p.tile_tokens;  // query tokens per item: 128 / g
+    // Shared-prefix decode (prefix pass): the "sequences" walked are the groups
+    // of prefix_group decode sequences; a group's rows are its sequences x the
+    // g heads of one kv head, its context is its shared prefix (no causal
+    // limit), and it is read through its first sequence's block table.
+    const bool prefix = p.prefix_lens != nullptr;
+    const int S = prefix ? p.num_seqs / p.prefix_group : p.num_seqs;
+    const int P = p.partition_tokens, B = p.block_size, g = p.group;
+    const int Tq = p.tile_tokens;  // query tokens per item: 128 / g (prefix pass: prefix_group)
     const int max_ctx = p.max_blocks_per_seq * B;
+    const uint32_t q_bytes = static_cast<uint32_t>(g * Tq) * 256u;  // both halves of the rows
 
     // Cursor over the sequence-major item numbering: lane l holds sequence
     // win0 + l and its number of items.
@@ -192,6 +199,12 @@ __device__ __forceinline__ void pf_produce(const DecodeParams& p, const CUtensor
     int items_lane = 0;
     auto load_window = [&]() {
         const int sl = win0 + lane;
+        if (prefix) {
+            const int pre = sl < S ? group_prefix(p, sl) : 0;
+            sq_lane = SeqQueries{pre, sl * p.prefix_group, sl * p.prefix_group + p.prefix_group, true};
+            items_lane = pre > 0 ? p.head_tiles * ((pre + P - 1) / P) : 0;
+            return;
+        }
         sq_lane = sl < S ? seq_queries(p, sl) : SeqQueries{0, 0, 0, true};
         items_lane = sl < S ? seq_items(sq_lane, p, max_ctx) : 0;
         if (sl < S && !sq_lane.rows_ok(p.num_query_tokens)) report(p.d_err, PA_DERR_CTX_OOB);
@@ -241,9 +254,9 @@ __device__ __forceinline__ void pf_produce(const DecodeParams& p, const CUtensor
         sq.q1 = __shfl_sync(0xffffffffu, sq_lane.q1, s_cur - win0);
         sq.multi = true;
         const int ctx = sq.ctx;
-        const bool valid = sq.ctx_ok(max_ctx);
+        const bool valid = prefix || sq.ctx_ok(max_ctx);
         const int qlen = sq.q1 - sq.q0;
-        const int np = valid ? items_of(ctx, max_ctx, P) : 1;
+        const int np = prefix ? (ctx + P - 1) / P : valid ? items_of(ctx, max_ctx, P) : 1;
         const int ntt = (qlen + Tq - 1) / Tq;
         const int i_loc = item_id - base_items;
         if (i_loc < 0 || i_loc >= __shfl_sync(0xffffffffu, items_lane, s_cur - win0)) {
@@ -258,8 +271,9 @@ __device__ __forceinline__ void pf_produce(const DecodeParams& p, const CUtensor
         const int hq0 = hk * g;
         const int i0 = it * Tq;
         const int ntok = min(Tq, qlen - i0);
-        const int lim_first = ctx - qlen + i0 + 1;  // tokens the item's first query sees
-        const int lim_last = lim_first + ntok - 1;
+        // tokens the item's first and last query see (prefix pass: all of them)
+        const int lim_first = prefix ? 0x40000000 : ctx - qlen + i0 + 1;
+        const int lim_last = prefix ? ctx : lim_first + ntok - 1;
         const int tok_begin = part * P;
         const int tok_end = valid ? max(tok_begin, min(tok_begin + P, lim_last)) : tok_begin;
         const int nst = tok_end > tok_begin ? (tok_end - tok_begin + C::kStageTok - 1) / C::kStageTok : 1;
@@ -275,14 +289,15 @@ __device__ __forceinline__ void pf_produce(const DecodeParams& p, const CUtensor
             // the item's query rows: [token][head][64 columns] boxes, one per half
             // (rows past the sequence's queries are loaded too, never stored)
             const uint32_t qf = bar(C::kQFull + qs);
-            mbar_arrive_expect_tx(qf, C::kOpBytes);
+            mbar_arrive_expect_tx(qf, q_bytes);
             for (int h = 0; h < 2; ++h)
                 pf::tma_load_3d(base + C::kQOff + qs * C::kOpBytes + h * C::kHalf, mapQ, 64 * h, hq0,
                                 sq.q0 + i0, qf);
         }
         q_issued = item_seq + 1;
 
-        const int32_t* trow = p.block_tables + static_cast<size_t>(s) * p.max_blocks_per_seq;
+        const int32_t* trow =
+            p.block_tables + static_cast<size_t>(prefix ? sq.q0 : s) * p.max_blocks_per_seq;
         const int blk_end = (tok_end + B - 1) / B;
         int win = tok_begin / B;
         int32_t entry = (win + lane < blk_end) ? __ldg(trow + win + lane) : -1;
@@ -339,7 +354,8 @@ __device__ __forceinline__ void pf_produce(const DecodeParams& p, const CUtensor
                 m.row0 = sq.q0 + i0;
                 m.hq0 = hq0;
                 m.part = part;
-                m.nparts = valid ? np : 0;
+                // prefix pass: always a partial state (the merge adds each sequence's own)
+                m.nparts = prefix ? p.prefix_parts + 1 : valid ? np : 0;
                 m.ntok = ntok;
                 // the meta is written before either arrival: the MMA warp reads it
                 // after fullK, the softmax warps after fullV
@@ -784,16 +800,21 @@ inline pa_status launch_prefill_tc_typed(const DecodeParams& p, const CUtensorMa
                                          cudaStream_t stream) {
     using C = PfTile<T>;
     static std::atomic<uint64_t> smem_configured{0};
-    if (p.group * p.tile_tokens != C::kRows) return PA_ERR_UNSUPPORTED;
+    if (p.prefix_lens != nullptr ? p.group * p.tile_tokens > C::kRows
+                                 : p.group * p.tile_tokens != C::kRows)
+        return PA_ERR_UNSUPPORTED;
     auto kernel = prefill_tc_kernel<T>;
     if (ensure_smem(kernel, C::kSmemBytes, smem_configured) != PA_OK) return PA_ERR_CUDA;
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
         return PA_ERR_CUDA;
-    // upper bound of the work items (query-token tiles: rows / tile_tokens + one ragged per sequence)
-    const long long tiles = p.num_query_tokens / p.tile_tokens + p.num_seqs;
-    const long long work = tiles * p.head_tiles * p.max_parts;
+    // upper bound of the work items (query-token tiles: rows / tile_tokens + one ragged per
+    // sequence; prefix pass: one tile per group, prefix_parts partitions)
+    const long long tiles = p.prefix_lens != nullptr ? p.num_seqs / p.prefix_group
+                                                     : p.num_query_tokens / p.tile_tokens + p.num_seqs;
+    const long long work =
+        tiles * p.head_tiles * (p.prefix_lens != nullptr ? p.prefix_parts : p.max_parts);
     if (work > 0x7fffffffLL) return PA_ERR_UNSUPPORTED;
     long long grid = sms;
     if (grid > work) grid = work;

@@ -3,10 +3,11 @@
 //
 // The step inputs a serving loop produces on the host each step (the queries,
 // the new tokens' K/V, their slots, the block tables, context lengths,
-// copy-on-write pairs and query offsets) are packed by the caller into one
-// host buffer laid out by pa_step_layout; the call copies it to a device
-// staging buffer in one transfer, runs copy_blocks, kv_write and attention on
-// the resident cache, and copies the output back, all on one stream.
+// copy-on-write pairs, query offsets and shared prefix lengths) are packed by
+// the caller into one host buffer laid out by pa_step_layout; the call copies
+// it to a device staging buffer in one transfer, runs copy_blocks, kv_write
+// and attention on the resident cache, and copies the output back, all on one
+// stream.
 #include <cuda_runtime.h>
 
 #include "pa.h"
@@ -22,7 +23,9 @@ bool dims_ok(const pa_step_dims* d) {
     return d != nullptr && d->num_seqs > 0 && d->num_query_tokens >= 0 && d->num_new_tokens >= 0 &&
            d->num_pairs >= 0 && d->num_q_heads > 0 && d->num_kv_heads > 0 && d->head_dim > 0 &&
            d->block_size > 0 && d->num_blocks > 0 && d->max_blocks_per_seq > 0 &&
-           (d->dtype == PA_F32 || d->dtype == PA_F16 || d->dtype == PA_BF16);
+           (d->dtype == PA_F32 || d->dtype == PA_F16 || d->dtype == PA_BF16) &&
+           d->prefix_group >= 0 &&
+           (d->prefix_group == 0 || (d->num_query_tokens == 0 && d->num_seqs % d->prefix_group == 0));
 }
 
 }  // namespace
@@ -41,6 +44,7 @@ extern "C" size_t pa_step_layout(const pa_step_dims* d, size_t offsets[PA_STEP_N
         static_cast<size_t>(d->num_seqs) * 4,                                      // context_lens
         static_cast<size_t>(d->num_pairs) * 8,                                     // block_mapping
         d->num_query_tokens > 0 ? static_cast<size_t>(d->num_seqs + 1) * 4 : 0,   // query_start
+        d->prefix_group > 0 ? static_cast<size_t>(d->num_seqs / d->prefix_group) * 4 : 0,  // prefix_lens
     };
     size_t off = 0;
     for (int i = 0; i < PA_STEP_NUM_INPUTS; ++i) {
@@ -63,7 +67,7 @@ extern "C" pa_status pa_step_host(const pa_step_dims* d, const void* host_in, vo
     if ((reinterpret_cast<uintptr_t>(dev_stage) & (kAlign - 1)) != 0) return PA_ERR_INVALID_ARG;
     const bool fp8 = k_scale != nullptr || v_scale != nullptr;
     if (fp8 && (k_scale == nullptr || v_scale == nullptr || d->num_query_tokens > 0 ||
-                d->dtype == PA_F32))
+                d->dtype == PA_F32 || d->prefix_group > 0))
         return PA_ERR_INVALID_ARG;
     const bool multi = d->num_query_tokens > 0;
     unsigned char* st = static_cast<unsigned char*>(dev_stage);
@@ -75,6 +79,8 @@ extern "C" pa_status pa_step_host(const pa_step_dims* d, const void* host_in, vo
     const int32_t* ctx = reinterpret_cast<const int32_t*>(st + off[5]);
     const int32_t* pairs = reinterpret_cast<const int32_t*>(st + off[6]);
     const int32_t* qstart = reinterpret_cast<const int32_t*>(st + off[7]);
+    const int32_t* prefix_lens = reinterpret_cast<const int32_t*>(st + off[8]);
+    const bool shared = d->prefix_group > 0;
     const int rows = multi ? d->num_query_tokens : d->num_seqs;
 
     // The host checks of every call of the step before anything is enqueued.
@@ -90,6 +96,10 @@ extern "C" pa_status pa_step_host(const pa_step_dims* d, const void* host_in, vo
         multi ? pa_multi_query_workspace_size(rows, d->num_q_heads, d->num_kv_heads, d->head_dim,
                                               d->max_blocks_per_seq, d->block_size, d->dtype,
                                               partition_tokens)
+        : shared ? pa_decode_shared_prefix_workspace_size(
+                       d->num_seqs, d->num_q_heads, d->num_kv_heads, d->head_dim,
+                       d->max_blocks_per_seq, d->block_size, d->dtype, partition_tokens,
+                       d->prefix_group)
               : pa_decode_workspace_size(d->num_seqs, d->num_q_heads, d->num_kv_heads, d->head_dim,
                                          d->max_blocks_per_seq, d->block_size,
                                          fp8 ? PA_E4M3 : d->dtype, partition_tokens);
@@ -123,6 +133,12 @@ extern "C" pa_status pa_step_host(const pa_step_dims* d, const void* host_in, vo
                            d->max_blocks_per_seq, ctx, d->num_seqs, d->num_q_heads,
                            d->num_kv_heads, d->head_dim, d->block_size, d->num_blocks, scale,
                            partition_tokens, d->dtype, workspace, workspace_bytes, d_err, stream);
+    else if (shared)
+        r = pa_decode_shared_prefix(dev_out, q, k_cache, v_cache, tables, d->max_blocks_per_seq,
+                                    ctx, d->num_seqs, d->num_q_heads, d->num_kv_heads,
+                                    d->head_dim, d->block_size, d->num_blocks, scale,
+                                    d->prefix_group, prefix_lens, partition_tokens, d->dtype,
+                                    workspace, workspace_bytes, d_err, stream);
     else if (fp8)
         r = pa_decode_fp8(dev_out, q, d->dtype, k_cache, v_cache, k_scale, v_scale, tables,
                           d->max_blocks_per_seq, ctx, d->num_seqs, d->num_q_heads,

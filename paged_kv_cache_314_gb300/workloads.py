@@ -488,10 +488,15 @@ def llama13b(seed: int = 316, poison: bool = True, num_seqs: int = 256, num_head
 
 def gqa_share(seed: int = 317, poison: bool = True, groups: int = 32, samples: int = 8,
               prefix_len: int = 1024, max_suffix: int = 256, num_q_heads: int = 64,
-              num_kv_heads: int = 8, partition_tokens: int = 0) -> Workload:
-    """Parallel sampling with a shared prefix, GQA 64 q heads / 8 kv heads, bf16, B=16."""
+              num_kv_heads: int = 8, partition_tokens: int = 0, block_size: int = 16,
+              dtype: str = "bf16") -> Workload:
+    """Parallel sampling with a shared prefix, GQA 64 q heads / 8 kv heads, bf16, B=16.
+
+    meta["shared_prefix_tokens"]: tokens at the start of every sample that
+    stay in blocks shared by the whole group after the step's copy-on-write
+    (the prefix blocks but the last, which samples 1.. copy)."""
     rng = np.random.default_rng(seed)
-    B = 16
+    B = block_size
     S = groups * samples
     suffix = rng.integers(0, max_suffix + 1, size=S)
     ctx = prefix_len + suffix + 1
@@ -501,11 +506,13 @@ def gqa_share(seed: int = 317, poison: bool = True, groups: int = 32, samples: i
     NB = pool_size(needed, 1.1)
     MB = (prefix_len + max_suffix + 1 + B - 1) // B
     plan = plan_shared_prefix(groups, samples, prefix_len, suffix, B, MB, NB, rng)
+    shared = (npre - 1) * B if samples > 1 else npre * B
     return build_workload("gqa_share" if prefix_len == 1024 else f"gqa_share_p{prefix_len}", plan,
-                          dtype="bf16", num_q_heads=num_q_heads, num_kv_heads=num_kv_heads,
+                          dtype=dtype, num_q_heads=num_q_heads, num_kv_heads=num_kv_heads,
                           head_dim=128, block_size=B, num_blocks=NB, scale=None,
                           partition_tokens=partition_tokens, seed=seed + 1_000_003, poison=poison,
-                          meta={"groups": groups, "samples": samples, "prefix_len": prefix_len})
+                          meta={"groups": groups, "samples": samples, "prefix_len": prefix_len,
+                                "shared_prefix_tokens": shared})
 
 
 def long_context(seed: int = 318, poison: bool = True, block_size: int = 16, num_seqs: int = 8,

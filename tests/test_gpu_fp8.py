@@ -217,3 +217,35 @@ def test_fp8_tensor_core_widening_covers_every_code(dtype):
             nz = ref != 0
             rel = np.abs(row[nz] - ref[nz]) / np.abs(ref[nz])
             assert rel.max() <= 2.0 ** -8, (s, h, float(rel.max()))
+
+
+def test_fp8_step_through_host_buffers():
+    """pa_step_host over an E4M3 cache (copy_blocks_fp8, kv_write_fp8,
+    decode_fp8 from one packed pinned host buffer): codes and scales
+    bit-exact, output within tolerance of the oracle."""
+    w = wl.to_fp8(wl.gqa_share(groups=2, samples=4, prefix_len=1016, max_suffix=40,
+                               num_q_heads=16, num_kv_heads=2), seed=12)
+    d = _upload(w)
+    dims = pa.StepDims(w.num_seqs, 0, w.num_tokens, w.num_pairs, w.num_q_heads, w.num_kv_heads,
+                       w.head_dim, w.block_size, w.num_blocks, w.max_blocks_per_seq,
+                       pa.DTYPE_CODE[d["q"].dtype])
+    total, offs = pa.step_layout(dims)
+    host_in = torch.zeros(total, dtype=torch.uint8).pin_memory()
+    for k in pa.STEP_INPUTS:
+        if k in d and d[k].numel():
+            n = d[k].numel() * d[k].element_size()
+            host_in[offs[k]:offs[k] + n].copy_(d[k].reshape(-1).view(torch.uint8).cpu())
+    stage = torch.empty(total, dtype=torch.uint8, device="cuda")
+    ws = torch.zeros(pa.decode_workspace_size(w.num_seqs, w.num_q_heads, w.num_kv_heads,
+                                              w.head_dim, w.max_blocks_per_seq, w.block_size,
+                                              "e4m3", 0), dtype=torch.uint8, device="cuda")
+    dev_out = torch.empty_like(d["q"])
+    host_out = torch.full(dev_out.shape, float("nan"), dtype=dev_out.dtype).pin_memory()
+    pa.step_host(dims, host_in, stage, host_out, dev_out, d["k_cache"], d["v_cache"], w.scale, 0,
+                 ws, d["d_err"], k_scale=d["k_scale"], v_scale=d["v_scale"])
+    torch.cuda.synchronize()
+    (kc, ks), (vc, vs), ref, err = oracle.step(w)
+    assert int(d["d_err"].item()) == err == 0
+    assert same_bits(d["k_cache"].cpu().numpy(), kc) and same_bits(d["v_cache"].cpu().numpy(), vc)
+    assert same_bits(d["k_scale"].cpu().numpy(), ks) and same_bits(d["v_scale"].cpu().numpy(), vs)
+    assert_close(out_f64(host_out), ref, w.dtype, "fp8 step_host")

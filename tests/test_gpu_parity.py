@@ -317,3 +317,65 @@ def test_bounded_wait_gives_up_and_reports():
     assert int(err.item()) == pa.DERR_TIMEOUT
     # the context is still usable afterwards
     _check_step(wl.tiny())
+
+
+# ---------------------------------------------------------------------------
+# a whole step through pa_step_host: packed host inputs, host output
+# ---------------------------------------------------------------------------
+
+def _host_step(w, d, partition_tokens=0):
+    """One pa_step_host call with the workload's step inputs packed in pinned
+    host memory; returns the host output."""
+    mq = w.query_start is not None
+    fp8 = w.kv_dtype == "e4m3"
+    dims = pa.StepDims(w.num_seqs, w.num_query_tokens if mq else 0, w.num_tokens, w.num_pairs,
+                       w.num_q_heads, w.num_kv_heads, w.head_dim, w.block_size, w.num_blocks,
+                       w.max_blocks_per_seq, pa.DTYPE_CODE[d["q"].dtype])
+    total, offs = pa.step_layout(dims)
+    host_in = torch.full((total,), 0xAB, dtype=torch.uint8).pin_memory()
+    for k in pa.STEP_INPUTS:
+        if k in d and d[k].numel():
+            n = d[k].numel() * d[k].element_size()
+            host_in[offs[k]:offs[k] + n].copy_(d[k].reshape(-1).view(torch.uint8).cpu())
+    stage = torch.empty(total, dtype=torch.uint8, device="cuda")
+    if mq:
+        ws = torch.zeros(pa.multi_query_workspace_size(w.num_query_tokens, w.num_q_heads,
+                                                       w.num_kv_heads, w.head_dim,
+                                                       w.max_blocks_per_seq, w.block_size,
+                                                       w.dtype, partition_tokens),
+                         dtype=torch.uint8, device="cuda")
+    else:
+        ws = torch.zeros(pa.decode_workspace_size(w.num_seqs, w.num_q_heads, w.num_kv_heads,
+                                                  w.head_dim, w.max_blocks_per_seq, w.block_size,
+                                                  "e4m3" if fp8 else w.dtype, partition_tokens),
+                         dtype=torch.uint8, device="cuda")
+    dev_out = torch.empty_like(d["q"])
+    host_out = torch.empty(dev_out.shape, dtype=dev_out.dtype).pin_memory()
+    host_out.fill_(float("nan"))
+    pa.step_host(dims, host_in, stage, host_out, dev_out, d["k_cache"], d["v_cache"], w.scale,
+                 partition_tokens, ws, d["d_err"], k_scale=d.get("k_scale"),
+                 v_scale=d.get("v_scale"))
+    torch.cuda.synchronize()
+    return host_out
+
+
+@pytest.mark.parametrize("kind", ["decode_cow", "multi_query", "mha_split"])
+def test_step_host_matches_oracle(kind):
+    """pa_step_host runs copy_blocks, kv_write and attention from one packed
+    host buffer: pools bit-exact and output within tolerance of the oracle."""
+    if kind == "decode_cow":
+        w = wl.gqa_share(groups=2, samples=4, prefix_len=1016, max_suffix=40, num_q_heads=16,
+                         num_kv_heads=2)
+    elif kind == "multi_query":
+        w = wl.custom("sh_mq", [40, 300, 129], dtype="bf16", num_q_heads=8, num_kv_heads=2,
+                      head_dim=128, block_size=16, seed=240, query_lens=[40, 9, 4])
+    else:
+        w = wl.custom("sh_mha", [1, 17, 600, 2100], dtype="f16", num_q_heads=4, num_kv_heads=4,
+                      head_dim=128, block_size=16, seed=241)
+    d = upload(w)
+    out = _host_step(w, d, partition_tokens=256 if kind == "mha_split" else 0)
+    kc, vc, ref, err = oracle_step(w)
+    assert int(d["d_err"].item()) == err == 0
+    assert same_bits(to_numpy(d["k_cache"], w.dtype), kc)
+    assert same_bits(to_numpy(d["v_cache"], w.dtype), vc)
+    assert_close(out_f64(out), ref, w.dtype, f"step_host {kind}")

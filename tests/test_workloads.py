@@ -194,3 +194,19 @@ def test_memory_stats_of_the_shared_prefix_workload():
     shared = 2 * 4 * 3
     assert st["share_rate"] == shared / st["logical_blocks"]
     assert st["physical_blocks"] == st["logical_blocks"] - 2 * 3 * 3
+
+
+@pytest.mark.parametrize("prefix_len,B", [(1024, 16), (1016, 16), (200, 32), (64, 16)])
+def test_shared_prefix_tokens_are_the_shared_table_entries(prefix_len, B):
+    """meta["shared_prefix_tokens"] names exactly the table entries every
+    sample of a group keeps in common after the copy-on-write."""
+    w = wl.gqa_share(groups=3, samples=4, prefix_len=prefix_len, max_suffix=40, num_q_heads=8,
+                     num_kv_heads=2, block_size=B)
+    shared = w.meta["shared_prefix_tokens"]
+    assert shared % B == 0 and shared <= prefix_len
+    nb = shared // B
+    for g in range(3):
+        rows = w.block_tables[4 * g:4 * g + 4]
+        assert (rows[:, :nb] == rows[0, :nb]).all()
+        assert len(set(rows[:, nb].tolist())) == 4  # the copied block: one per sample
+        assert (w.context_lens[4 * g:4 * g + 4] > shared).all()
