@@ -335,15 +335,17 @@ pa_status run_attention(const AttnCall& a) {
         // grouped heads: the tensor-core kernel, which widens the codes in shared memory
         if (tc_shape(a.num_q_heads, a.num_kv_heads, a.head_dim, PA_E4M3) && P % 128 == 0 &&
             pool_rows < 0x7fffffffLL) {
-            CUtensorMap map_k, map_v;
+            CUtensorMap map_k, map_v, map_q;
             if (plan || (make_pool_map_fp8(&map_k, a.k_cache, pool_rows) &&
-                         make_pool_map_fp8(&map_v, a.v_cache, pool_rows))) {
+                         make_pool_map_fp8(&map_v, a.v_cache, pool_rows) &&
+                         make_q_map(&map_q, a.q, a.num_query_tokens, a.num_q_heads, group, a.dtype,
+                                    1))) {
                 p.head_tiles = a.num_kv_heads;
                 p.tile_heads = group;
                 p.tile_tokens = 1;
                 if (plan) return describe(a.plan, PA_KERNEL_TC_GROUPED_FP8, p);
-                return a.dtype == PA_BF16 ? launch_decode_tc_fp8_bf16(p, map_k, map_v, st)
-                                          : launch_decode_tc_fp8_f16(p, map_k, map_v, st);
+                return a.dtype == PA_BF16 ? launch_decode_tc_fp8_bf16(p, map_k, map_v, map_q, st)
+                                          : launch_decode_tc_fp8_f16(p, map_k, map_v, map_q, st);
             }
         }
         const int gt = heads * tokens;
@@ -387,9 +389,11 @@ pa_status run_attention(const AttnCall& a) {
         }
     }
     if (tc_ok && tc_rows) {
-        CUtensorMap map_k, map_v;
+        CUtensorMap map_k, map_v, map_q;
         if (plan || (make_pool_map(&map_k, a.k_cache, pool_rows, a.dtype) &&
-                     make_pool_map(&map_v, a.v_cache, pool_rows, a.dtype))) {
+                     make_pool_map(&map_v, a.v_cache, pool_rows, a.dtype) &&
+                     make_q_map(&map_q, a.q, a.num_query_tokens, a.num_q_heads, group, a.dtype,
+                                tc_tokens))) {
             p.head_tiles = a.num_kv_heads;
             p.tile_heads = group;
             p.tile_tokens = tc_tokens;
@@ -399,12 +403,12 @@ pa_status run_attention(const AttnCall& a) {
                     if (e != PA_OK) return e;
                 }
                 if (plan) return describe(a.plan, PA_KERNEL_TC_GROUPED, p);
-                return a.dtype == PA_BF16 ? launch_multi_query_tc_bf16(p, map_k, map_v, st)
-                                          : launch_multi_query_tc_f16(p, map_k, map_v, st);
+                return a.dtype == PA_BF16 ? launch_multi_query_tc_bf16(p, map_k, map_v, map_q, st)
+                                          : launch_multi_query_tc_f16(p, map_k, map_v, map_q, st);
             }
             if (plan) return describe(a.plan, PA_KERNEL_TC_GROUPED, p);
-            return a.dtype == PA_BF16 ? launch_decode_tc_bf16(p, map_k, map_v, st)
-                                      : launch_decode_tc_f16(p, map_k, map_v, st);
+            return a.dtype == PA_BF16 ? launch_decode_tc_bf16(p, map_k, map_v, map_q, st)
+                                      : launch_decode_tc_f16(p, map_k, map_v, map_q, st);
         }
     }
     const int gt = heads * tokens;
@@ -720,10 +724,11 @@ extern "C" pa_status pa_decode_shared_prefix(
     if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return PA_ERR_INVALID_ARG;
     const int g = num_q_heads / num_kv_heads;
     const long long pool_rows = static_cast<long long>(num_blocks) * num_kv_heads * block_size;
-    CUtensorMap map_k, map_v, map_q;
+    CUtensorMap map_k, map_v, map_q, map_q1;
     if (!make_pool_map(&map_k, k_cache, pool_rows, dtype) ||
         !make_pool_map(&map_v, v_cache, pool_rows, dtype) ||
-        !make_q_map(&map_q, q, num_seqs, num_q_heads, g, dtype, group_size))
+        !make_q_map(&map_q, q, num_seqs, num_q_heads, g, dtype, group_size) ||
+        !make_q_map(&map_q1, q, num_seqs, num_q_heads, g, dtype, 1))
         return PA_ERR_CUDA;
 
     unsigned char* wsb = static_cast<unsigned char*>(workspace);
@@ -772,8 +777,8 @@ extern "C" pa_status pa_decode_shared_prefix(
                                    : launch_prefill_tc_f16(pp, map_k, map_v, map_q, st);
     if (r != PA_OK) return r;
     // 2. each sequence's own tokens on the grouped tensor-core decode kernel
-    r = dtype == PA_BF16 ? launch_decode_tc_bf16(p, map_k, map_v, st)
-                         : launch_decode_tc_f16(p, map_k, map_v, st);
+    r = dtype == PA_BF16 ? launch_decode_tc_bf16(p, map_k, map_v, map_q1, st)
+                         : launch_decode_tc_f16(p, map_k, map_v, map_q1, st);
     if (r != PA_OK) return r;
     // 3. both ranges of partial states merged per (sequence, head)
     p.skip_merge = 0;

@@ -12,11 +12,13 @@ pa_status launch_decode_fp8_bf16(const DecodeParams& p, int gt, cudaStream_t str
     return launch_decode_fp8_typed<__nv_bfloat16, false>(p, gt, stream);
 }
 pa_status launch_decode_tc_fp8_f16(const DecodeParams& p, const CUtensorMap& mapK,
-                                   const CUtensorMap& mapV, cudaStream_t stream) {
-    return launch_decode_tc_typed<__half, false, true>(p, mapK, mapV, stream);
+                                   const CUtensorMap& mapV, const CUtensorMap& mapQ,
+        cudaStream_t stream) {
+    return launch_decode_tc_typed<__half, false, true>(p, mapK, mapV, mapQ, stream);
 }
 pa_status launch_decode_tc_fp8_bf16(const DecodeParams& p, const CUtensorMap& mapK,
-                                    const CUtensorMap& mapV, cudaStream_t stream) {
-    return launch_decode_tc_typed<__nv_bfloat16, false, true>(p, mapK, mapV, stream);
+                                    const CUtensorMap& mapV, const CUtensorMap& mapQ,
+        cudaStream_t stream) {
+    return launch_decode_tc_typed<__nv_bfloat16, false, true>(p, mapK, mapV, mapQ, stream);
 }
 }  // namespace pa

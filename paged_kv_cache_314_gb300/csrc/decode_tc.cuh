@@ -23,8 +23,9 @@
 // Warp roles (416 threads, persistent, one CTA per SM):
 //   warp 0   producer: item cursor over context_lens (as in the SIMT path),
 //            block-table slice, TMA loads into a 3-stage ring (64 KB/stage;
-//            the K boxes of groups 0-3), bulk copy of the item's query rows
-//            into a staging slot
+//            the K boxes of groups 0-3), the item's query rows by a 3-D TMA
+//            copy straight into one of two swizzled Q operand slots (so MMA1 of
+//            the next item can start while the teams finish this one)
 //   warp 1   allocates tensor memory, issues the MMAs (one thread); S and
 //            O^T are double-buffered in tensor memory (64 columns)
 //   warps 10-12 issue the other boxes of each stage from the producer's plan
@@ -57,12 +58,12 @@ struct TcTile {
     static constexpr int kStageBytes = 2 * kTileBytes;            // 64 KB
     static constexpr int kStages = 3;
     static constexpr int kQSlots = 2;
-    static constexpr int kQBytes = kN * D * 2;                    // staged query rows (linear)
     static constexpr int kOpBytes = 2 * kN * 128;                 // Q or P operand, swizzled: 4 KB
     static constexpr int kRingOff = 0;
+    // the item's query rows, loaded by TMA straight into the swizzled K-major
+    // Q operand, one slot per item in flight
     static constexpr int kQsOff = kStages * kStageBytes;
-    static constexpr int kQopOff = kQsOff + kQSlots * kQBytes;
-    static constexpr int kPopOff = kQopOff + kOpBytes;
+    static constexpr int kPopOff = kQsOff + kQSlots * kOpBytes;
     static constexpr int kRedOff = kPopOff + 2 * kOpBytes;        // P double-buffered; [4][16] floats
     static constexpr int kRecOff = kRedOff + 4 * kN * 4;          // item records [kQSlots]
     static constexpr int kMetaOff = kRecOff + kQSlots * 32;       // stage meta [kStages]
@@ -74,11 +75,11 @@ struct TcTile {
     // E4M3 caches: the K and V scales of each stage's eight 16-token groups [kStages][16]
     static constexpr int kScaleOff = kPlanOff + kStages * kPlanInts * 4;
     static constexpr int kBarOff = kScaleOff + kStages * 16 * 4;
-    // fullK[S], emptyK[S], qfull[Q], qempty[Q], q_ready, s_full[2], p_full[2], o_full[2],
+    // fullK[S], emptyK[S], qfull[Q], qempty[Q], s_full[2], p_full[2], o_full[2],
     // drain, fullV[S], emptyV[S], vplan[S]: the K and V halves of a ring slot land and
     // are released separately (K after MMA1 of its stage, V after MMA2); a stage's V
     // copies are issued by their own warp from the plan the producer leaves
-    static constexpr int kFullVBar = 2 * kStages + 2 * kQSlots + 8;
+    static constexpr int kFullVBar = 2 * kStages + 2 * kQSlots + 7;
     static constexpr int kEmptyVBar = kFullVBar + kStages;
     static constexpr int kVPlanBar = kEmptyVBar + kStages;
     static constexpr int kKPlanBar = kVPlanBar + kStages;
@@ -125,8 +126,8 @@ struct TcItemRec {
 // tile (the teams widen it in place); the blocks' scales go beside the stage.
 template <typename T, bool kMulti, bool kFp8>
 __device__ __forceinline__ void tc_produce(const DecodeParams& p, const CUtensorMap* mapK,
-                                           const CUtensorMap* mapV, unsigned char* sm,
-                                           uint32_t base) {
+                                           const CUtensorMap* mapV, const CUtensorMap* mapQ,
+                                           unsigned char* sm, uint32_t base) {
     using C = TcTile<T>;
     const int lane = threadIdx.x & 31;
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::kBarOff);
@@ -145,7 +146,8 @@ __device__ __forceinline__ void tc_produce(const DecodeParams& p, const CUtensor
     const int S = p.num_seqs, HT = p.head_tiles, P = p.partition_tokens, B = p.block_size;
     const int g = p.group;
     const int max_ctx = p.max_blocks_per_seq * B;
-    const uint32_t row_bytes = static_cast<uint32_t>(g * C::D * 2);  // one token's g query rows
+    // the Q box: tile_tokens tokens x g heads x 64 columns, twice (one per half)
+    const uint32_t q_bytes = static_cast<uint32_t>((kMulti ? p.tile_tokens : 1) * g) * 256u;
 
     // Cursor over the sequence-major item numbering (as in the SIMT path):
     // lane l holds sequence win0 + l and its number of items.
@@ -256,13 +258,13 @@ __device__ __forceinline__ void tc_produce(const DecodeParams& p, const CUtensor
             recs[qs].part = prefix ? p.prefix_parts + part : part;
             recs[qs].nparts = valid ? (prefix ? p.prefix_parts + np : np) : 0;
             recs[qs].nrows = ntok * g;
+            // rows (token, head) of the swizzled operand, both 64-column halves; a
+            // ragged last tile loads rows past its queries too (never used)
             const uint32_t qf = qfull0 + 8 * qs;
-            mbar_arrive_expect_tx(qf, row_bytes * ntok);
-            for (int ti = 0; ti < ntok; ++ti)
-                bulk_g2s(base + C::kQsOff + qs * C::kQBytes + ti * row_bytes,
-                         static_cast<const T*>(p.q) +
-                             (static_cast<size_t>(sq.q0 + i0 + ti) * p.num_q_heads + hq0) * C::D,
-                         row_bytes, qf, policy);
+            mbar_arrive_expect_tx(qf, q_bytes);
+            for (int h = 0; h < 2; ++h)
+                tc::tma_load_3d(base + C::kQsOff + qs * C::kOpBytes + h * 2048, mapQ, 64 * h, hq0,
+                                sq.q0 + i0, qf, policy);
         }
         q_issued = item_seq + 1;
 
@@ -498,8 +500,7 @@ __device__ __forceinline__ uint2 widen_e4m3x4(uint32_t four_codes) {
 template <typename T>
 struct TcBars {
     using C = TcTile<T>;
-    static constexpr int kQReady = 2 * C::kStages + 2 * C::kQSlots;
-    static constexpr int kSFull = kQReady + 1;  // [2]
+    static constexpr int kSFull = 2 * C::kStages + 2 * C::kQSlots;  // [2]
     static constexpr int kPFull = kSFull + 2;   // [2]
     static constexpr int kOFull = kPFull + 2;   // [2]
     static constexpr int kDrain = kOFull + 2;
@@ -550,19 +551,19 @@ __device__ __forceinline__ void tc_mma(const DecodeParams& p, unsigned char* sm,
     const uint32_t emptyK0 = smem_addr(bars + C::kStages);
     const uint32_t emptyV0 = smem_addr(bars + C::kEmptyVBar);
     const uint32_t convV0 = smem_addr(bars + C::kConvVBar);  // E4M3: V widened
-    const uint32_t qready = smem_addr(bars + Bi::kQReady);
+    const uint32_t qfull0 = smem_addr(bars + 2 * C::kStages);
+    const uint32_t qempty0 = smem_addr(bars + 2 * C::kStages + C::kQSlots);
     const uint32_t sfull0 = smem_addr(bars + Bi::kSFull), pfull0 = smem_addr(bars + Bi::kPFull);
     const uint32_t ofull0 = smem_addr(bars + Bi::kOFull), drain = smem_addr(bars + Bi::kDrain);
     const TcStageMeta* meta = reinterpret_cast<const TcStageMeta*>(sm + C::kMetaOff);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + C::kMiscOff + 4);
-    const uint32_t qop = base + C::kQopOff, pop0 = base + C::kPopOff;
+    const uint32_t pop0 = base + C::kPopOff;
     auto stage_k = [&](int c) { return base + C::kRingOff + (c % C::kStages) * C::kStageBytes; };
     auto fail = [&]() {
         if (lane == 0) report(p.d_err, PA_DERR_TIMEOUT);
         *abort_flag = 1;
     };
 
-    int nitems = 0;
     // MMA1 of stage c (waiting for its data, and for its query rows at an item start).
     // Returns 0 = issued, 1 = end marker, -1 = gave up.
     auto issue_mma1 = [&](int c) -> int {
@@ -570,15 +571,18 @@ __device__ __forceinline__ void tc_mma(const DecodeParams& p, unsigned char* sm,
         if (!mbar_wait_warp(fullK0 + 8 * st, static_cast<uint32_t>(c / C::kStages) & 1)) return -1;
         const uint32_t flags = meta[st].flags;
         if (flags & kStageEnd) return 1;
-        if (flags & kStageFirst) {
-            if (!mbar_wait_warp(qready, static_cast<uint32_t>(nitems) & 1)) return -1;
-            ++nitems;
-        }
+        const int item_seq = static_cast<int>(meta[st].item_seq);
+        const int qs = item_seq % C::kQSlots;
+        if ((flags & kStageFirst) &&
+            !mbar_wait_warp(qfull0 + 8 * qs, static_cast<uint32_t>(item_seq / C::kQSlots) & 1))
+            return -1;
         tc::fence_after_sync();
         // the whole warp runs the issue code, one elected lane (lane 0) issues
-        tc_mma1<T, kFp8>(stage_k(c), qop, tmem + (c & 1) * C::kN);
+        tc_mma1<T, kFp8>(stage_k(c), base + C::kQsOff + qs * C::kOpBytes, tmem + (c & 1) * C::kN);
         tc::mma_commit_warp(sfull0 + 8 * (c & 1));
         tc::mma_commit_warp(emptyK0 + 8 * st);  // K_c is free once MMA1 completed
+        // the item's last MMA1 read its query rows: one of the slot's releases
+        if (flags & kStageLast) tc::mma_commit_warp(qempty0 + 8 * qs);
         __syncwarp();
         return 0;
     };
@@ -690,8 +694,9 @@ __device__ __forceinline__ float warp_reduce_scatter(const float (&v)[N], int la
 // (thread = token row of S), then the deferred O-accumulate of stage c-1 of
 // the same item (thread = head dimension of O^T); at an item's last stage its
 // own O-accumulate and the output rows of the team's heads.  Team 0 also
-// zeroes the V rows of invalid tokens.  Each team signals p_full, q_ready and
-// qempty once (those barriers count two arrivals).
+// zeroes the V rows of invalid tokens.  Each team signals p_full once (two
+// arrivals) and qempty once when it has the item record (with the item's last
+// MMA1, three arrivals).
 // E4M3 caches (kFp8): the tiles hold the codes widened exactly to T (by the
 // converter warps); the scales stay in fp32: the K scale of a token's block
 // multiplies its logits, the V scale its softmax weight before that is rounded
@@ -712,7 +717,6 @@ __device__ __forceinline__ void tc_team(const DecodeParams& p, unsigned char* sm
     const uint32_t fullV0 = smem_addr(bars + C::kFullVBar);  // V landed (and the stage's meta)
     const uint32_t qfull0 = smem_addr(bars + 2 * C::kStages);
     const uint32_t qempty0 = smem_addr(bars + 2 * C::kStages + C::kQSlots);
-    const uint32_t qready = smem_addr(bars + Bi::kQReady);
     const uint32_t sfull0 = smem_addr(bars + Bi::kSFull), pfull0 = smem_addr(bars + Bi::kPFull);
     const uint32_t ofull0 = smem_addr(bars + Bi::kOFull);
     const TcStageMeta* meta = reinterpret_cast<const TcStageMeta*>(sm + C::kMetaOff);
@@ -764,22 +768,8 @@ __device__ __forceinline__ void tc_team(const DecodeParams& p, unsigned char* sm
             if (!team.wait(qfull0 + 8 * qs, static_cast<uint32_t>(item_seq / C::kQSlots) & 1, p.d_err, abort_flag))
                 break;
             rec = recs[qs];  // the slot is reused once qempty is released below
-            // query rows of this team's heads -> the swizzled K-major Q operand
-            const unsigned char* src = sm + C::kQsOff + qs * C::kQBytes;
-            for (int idx = tid; idx < H * 16; idx += 128) {
-                const int h = h0 + (idx >> 4), ch = idx & 15;
-                if (h < rec.nrows) {
-                    const uint4 v = *reinterpret_cast<const uint4*>(src + (h * C::D + ch * 8) * 2);
-                    *reinterpret_cast<uint4*>(sm + C::kQopOff + (ch >> 3) * 2048 + (h >> 3) * 1024 +
-                                              (h & 7) * 128 + (((ch & 7) ^ (h & 7)) << 4)) = v;
-                }
-            }
-            tc::fence_async_smem();
-            team.sync();
-            if (tid == 0) {
-                mbar_arrive(qempty0 + 8 * qs);
-                mbar_arrive(qready);
-            }
+            team.sync();     // every thread of the team has its copy of the record
+            if (tid == 0) mbar_arrive(qempty0 + 8 * qs);
 #pragma unroll
             for (int h = 0; h < H; ++h) {
                 m[h] = -INFINITY;
@@ -959,7 +949,7 @@ __device__ __forceinline__ void tc_convert(const DecodeParams& p, unsigned char*
 template <typename T, int G, bool kMulti, bool kFp8>
 __global__ void __launch_bounds__(kFp8 ? TcTile<T>::kThreadsFp8 : TcTile<T>::kThreads, 1)
     decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap mapK,
-                     const __grid_constant__ CUtensorMap mapV) {
+                     const __grid_constant__ CUtensorMap mapV, const __grid_constant__ CUtensorMap mapQ) {
     using C = TcTile<T>;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
@@ -971,19 +961,21 @@ __global__ void __launch_bounds__(kFp8 ? TcTile<T>::kThreadsFp8 : TcTile<T>::kTh
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < C::kNumBars; ++i) {
-            // qempty, q_ready and p_full are signalled once by each of the two teams
-            const bool two = (i >= 2 * C::kStages + C::kQSlots && i <= TcBars<T>::kQReady) ||
-                             i == TcBars<T>::kPFull || i == TcBars<T>::kPFull + 1;
-            mbar_init(smem_addr(bars + i), two ? 2 : 1);
+            // p_full is signalled once by each of the two teams; qempty by both teams
+            // (their copies of the item record) and by the item's last MMA1
+            const bool qempty = i >= 2 * C::kStages + C::kQSlots && i < 2 * C::kStages + 2 * C::kQSlots;
+            const bool two = i == TcBars<T>::kPFull || i == TcBars<T>::kPFull + 1;
+            mbar_init(smem_addr(bars + i), qempty ? 3 : two ? 2 : 1);
         }
         *reinterpret_cast<volatile int*>(sm + C::kMiscOff + 4) = 0;
         fence_barrier_init();
         tc::prefetch_tensormap(&mapK);
         tc::prefetch_tensormap(&mapV);
+        tc::prefetch_tensormap(&mapQ);
     }
-    // zero the Q and both P operands once: padding rows (heads >= g) stay zero
-    for (int i = threadIdx.x; i < 3 * C::kOpBytes / 16; i += blockDim.x)
-        reinterpret_cast<uint4*>(sm + C::kQopOff)[i] = make_uint4(0, 0, 0, 0);
+    // zero the Q slots and both P operands once: padding rows (heads >= g) stay zero
+    for (int i = threadIdx.x; i < 4 * C::kOpBytes / 16; i += blockDim.x)
+        reinterpret_cast<uint4*>(sm + C::kQsOff)[i] = make_uint4(0, 0, 0, 0);
     tc::fence_async_smem();
     if (warp == 1) tc::tmem_alloc(smem_addr(tmem_slot), 64);  // S[2], O^T[2]: 16 columns each
     tc::fence_before_sync();
@@ -992,7 +984,7 @@ __global__ void __launch_bounds__(kFp8 ? TcTile<T>::kThreadsFp8 : TcTile<T>::kTh
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
 
     if (warp == 0)
-        tc_produce<T, kMulti, kFp8>(p, &mapK, &mapV, sm, base);
+        tc_produce<T, kMulti, kFp8>(p, &mapK, &mapV, &mapQ, sm, base);
     else if (warp == 1)
         tc_mma<T, kFp8>(p, sm, base, tmem);
     else if (warp < 10)
@@ -1024,7 +1016,8 @@ __global__ void __launch_bounds__(kFp8 ? TcTile<T>::kThreadsFp8 : TcTile<T>::kTh
 
 template <typename T, bool kMulti, bool kFp8 = false>
 inline pa_status launch_decode_tc_typed(const DecodeParams& p, const CUtensorMap& mapK,
-                                        const CUtensorMap& mapV, cudaStream_t stream) {
+                                        const CUtensorMap& mapV, const CUtensorMap& mapQ,
+                                        cudaStream_t stream) {
     using C = TcTile<T>;
     static std::atomic<uint64_t> smem_configured[3];
     const int rows = kMulti ? p.tile_tokens * p.group : p.group;
@@ -1047,24 +1040,24 @@ inline pa_status launch_decode_tc_typed(const DecodeParams& p, const CUtensorMap
     long long grid = sms;
     if (grid > work) grid = work;
     kernel<<<static_cast<unsigned>(grid), kFp8 ? C::kThreadsFp8 : C::kThreads, C::kSmemBytes, stream>>>(
-        p, mapK, mapV);
+        p, mapK, mapV, mapQ);
     if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
     if (p.max_parts > 1) return launch_merge<T, C::D>(p, stream);
     return PA_OK;
 }
 
 pa_status launch_decode_tc_f16(const DecodeParams& p, const CUtensorMap& mapK,
-                               const CUtensorMap& mapV, cudaStream_t stream);
+                               const CUtensorMap& mapV, const CUtensorMap& mapQ, cudaStream_t stream);
 pa_status launch_decode_tc_bf16(const DecodeParams& p, const CUtensorMap& mapK,
-                                const CUtensorMap& mapV, cudaStream_t stream);
+                                const CUtensorMap& mapV, const CUtensorMap& mapQ, cudaStream_t stream);
 pa_status launch_multi_query_tc_f16(const DecodeParams& p, const CUtensorMap& mapK,
-                                    const CUtensorMap& mapV, cudaStream_t stream);
+                                    const CUtensorMap& mapV, const CUtensorMap& mapQ, cudaStream_t stream);
 pa_status launch_multi_query_tc_bf16(const DecodeParams& p, const CUtensorMap& mapK,
-                                     const CUtensorMap& mapV, cudaStream_t stream);
+                                     const CUtensorMap& mapV, const CUtensorMap& mapQ, cudaStream_t stream);
 // E4M3 K/V, 16-bit queries (maps over the 8-bit pools: 128-byte rows, 16-row boxes)
 pa_status launch_decode_tc_fp8_f16(const DecodeParams& p, const CUtensorMap& mapK,
-                                   const CUtensorMap& mapV, cudaStream_t stream);
+                                   const CUtensorMap& mapV, const CUtensorMap& mapQ, cudaStream_t stream);
 pa_status launch_decode_tc_fp8_bf16(const DecodeParams& p, const CUtensorMap& mapK,
-                                    const CUtensorMap& mapV, cudaStream_t stream);
+                                    const CUtensorMap& mapV, const CUtensorMap& mapQ, cudaStream_t stream);
 
 }  // namespace pa

@@ -8,7 +8,8 @@ pa_status launch_multi_query_f16(const DecodeParams& p, int head_dim, int gt, cu
     return launch_decode_typed<__half, true>(p, head_dim, gt, stream);
 }
 pa_status launch_multi_query_tc_f16(const DecodeParams& p, const CUtensorMap& mapK,
-                                    const CUtensorMap& mapV, cudaStream_t stream) {
-    return launch_decode_tc_typed<__half, true>(p, mapK, mapV, stream);
+                                    const CUtensorMap& mapV, const CUtensorMap& mapQ,
+        cudaStream_t stream) {
+    return launch_decode_tc_typed<__half, true>(p, mapK, mapV, mapQ, stream);
 }
 }  // namespace pa
