@@ -521,7 +521,8 @@ def _measure(args, name, layout, dev, dist, ws_world):
     tensor_bound = tc_path and flops / (tensor_peak * 1e12) > unique_bytes / (peak * 1e9)
     alu_bound = not tc_path and flops / (alu_peak * 1e12) > unique_bytes / (peak * 1e9)
     ncu = _ncu_record(name + ("" if layout == "paged" else "_" + layout))
-    traffic = ncu.get("traffic_bytes_per_launch") if ncu else None
+    # DRAM bytes of one attention call (every kernel of it), from the capture
+    traffic = (ncu.get("call_traffic_bytes") or ncu.get("traffic_bytes_per_launch")) if ncu else None
     kernel = f"{'pa_multi_query' if mq else 'pa_decode_fp8' if fp8 else 'pa_decode_shared_prefix' if shared else 'pa_decode'}: " \
              f"{plan['kernel']} kernel, merge {plan['merge']}, {plan['launches']} launch(es)"
     hbm_ach = unique_bytes / (dec_ms * 1e-3) / 1e9
@@ -529,7 +530,8 @@ def _measure(args, name, layout, dev, dist, ws_world):
               "l2_hit_rate_pct": round(ncu["l2_hit_rate_pct"], 2)
               if ncu and ncu.get("l2_hit_rate_pct") is not None else None,
               "traffic_source": "profiles/decode_*_ncu.json (ncu dram__bytes_read.sum + "
-                                "dram__bytes_write.sum per launch, same kernel sources)"
+                                "dram__bytes_write.sum of the attention call's kernels, same "
+                                "kernel sources)"
               if ncu else "no capture on the current kernel sources"}
     if tensor_bound or alu_bound:
         pk = tensor_peak if tensor_bound else round(alu_peak, 1)
@@ -797,6 +799,46 @@ def run_swap(args):
         nbytes = 2 * n * d_k[0].numel() * d_k.element_size()
         res[name] = {"ms": round(ms, 4), "gb_per_s": round(nbytes / (ms * 1e-3) / 1e9, 2),
                      "bytes": nbytes}
+    # the copy engines for comparison: one cudaMemcpyAsync per block and tensor
+    # (the ids are scattered: no two consecutive pairs are adjacent on both
+    # sides), and one copy of the same bytes as a single contiguous range
+    src_l, dst_l = src.tolist(), list(range(n))
+    for name, a, b, ia, ib in (("swap_out_copy_engine_per_block", d_k, h_k, src_l, dst_l),
+                               ("swap_in_copy_engine_per_block", h_k, d_k, dst_l, src_l)):
+        bv = b.view(b.shape[0], -1)
+        av = a.view(a.shape[0], -1)
+        bv2 = (h_v if b is h_k else d_v).view(b.shape[0], -1)
+        av2 = (d_v if a is d_k else h_v).view(a.shape[0], -1)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        e0.record(stream)
+        for i, j in zip(ia, ib):
+            bv[j].copy_(av[i], non_blocking=True)
+            bv2[j].copy_(av2[i], non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        cpu_ms = (time.perf_counter() - t0) * 1e3
+        ms = e0.elapsed_time(e1)
+        nbytes = 2 * n * d_k[0].numel() * d_k.element_size()
+        res[name] = {"ms": round(ms, 4), "gb_per_s": round(nbytes / (ms * 1e-3) / 1e9, 2),
+                     "host_submit_ms": round(cpu_ms, 3), "copies": 2 * n}
+    flat_h = h_k.view(-1)
+    flat_d = d_k.view(-1)[:flat_h.numel()]
+    for name, a, b in (("out_contiguous_copy_engine", flat_d, flat_h),
+                       ("in_contiguous_copy_engine", flat_h, flat_d)):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        b.copy_(a, non_blocking=True)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(args.steps):
+            b.copy_(a, non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / args.steps
+        res[name] = {"ms": round(ms, 4),
+                     "gb_per_s": round(a.numel() * a.element_size() / (ms * 1e-3) / 1e9, 2),
+                     "what": "one cudaMemcpyAsync of one pool's swapped bytes, contiguous"}
     print(json.dumps({"metric": "pa_swap_blocks GB/s (K+V blocks, device <-> pinned host)",
                       "value": res["swap_out"]["gb_per_s"], "unit": "GB/s", "n_gpus": 1,
                       "steps": args.steps, "warmup": args.warmup, "higher_is_better": True,

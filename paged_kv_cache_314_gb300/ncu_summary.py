@@ -34,6 +34,8 @@ KERNEL_SOURCES = {
     "simt": ("decode_kernels.cuh", "pa_device.cuh"),
     "tc": ("decode_kernels.cuh", "decode_tc.cuh", "tc_ptx.cuh", "pa_device.cuh"),
     "tc128": ("decode_kernels.cuh", "prefill_tc.cuh", "tc_ptx.cuh", "pa_device.cuh"),
+    "shared_prefix": ("decode_kernels.cuh", "decode_tc.cuh", "prefill_tc.cuh", "tc_ptx.cuh",
+                      "pa_device.cuh"),
 }
 
 _SCALE = {
@@ -162,18 +164,34 @@ def summarise_kernel(text: str, kernel_regex: str, config: str, command: str,
     launches = parse_raw(text, kernel_regex)
     if not launches:
         raise SystemExit(f"no launch of {kernel_regex!r} in the listing")
-    traffic = [x["traffic_bytes"] for x in launches if x.get("traffic_bytes") is not None]
-    l2 = [x["l2_hit_rate_pct"] for x in launches if x.get("l2_hit_rate_pct") is not None]
+    first = _short(str(launches[0]["kernel"]))
+    per: Dict[str, List[Dict[str, object]]] = {}
+    for x in launches:
+        per.setdefault(_short(str(x["kernel"])), []).append(x)
+
+    def mean(xs, key):
+        v = [x[key] for x in xs if x.get(key) is not None]
+        return sum(v) / len(v) if v else None
+
+    kernels = {k: {"launches": len(v), "traffic_bytes": mean(v, "traffic_bytes"),
+                   "duration_s": mean(v, "duration_s"), "l2_hit_rate_pct": mean(v, "l2_hit_rate_pct"),
+                   "dram_throughput_pct": mean(v, "dram_throughput_pct")} for k, v in per.items()}
+    main = kernels[first]
+    call = [v["traffic_bytes"] for v in kernels.values()]
     return {
         "config": config,
         "kernel_regex": kernel_regex,
-        "kernel": _short(str(launches[0]["kernel"])),
+        "kernel": first,
         "command": command,
         "kernel_sources": list(KERNEL_SOURCES[family]),
         "kernel_source_sha256_16": kernel_source_hash(KERNEL_SOURCES[family]),
         "launches": launches,
-        "traffic_bytes_per_launch": int(sum(traffic) / len(traffic)) if traffic else None,
-        "l2_hit_rate_pct": sum(l2) / len(l2) if l2 else None,
+        "kernels": kernels,
+        # the first matching kernel (the attention call's main kernel)
+        "traffic_bytes_per_launch": int(main["traffic_bytes"]) if main["traffic_bytes"] else None,
+        "l2_hit_rate_pct": main["l2_hit_rate_pct"],
+        # every kernel of one attention call (the distinct kernels matched, one launch each)
+        "call_traffic_bytes": int(sum(call)) if call and all(c is not None for c in call) else None,
     }
 
 
