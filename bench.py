@@ -464,6 +464,30 @@ def _measure(args, name, layout, dev, dist, ws_world):
         dist.barrier()
     ms_per_step = float(np.mean([a.elapsed_time(b) for a, b in ev]))
 
+    # the same step captured once into a CUDA graph and replayed (the L2 flush
+    # stays outside the graph): what the launches cost between the kernels
+    graph_ms = None
+    if not args.no_graph:
+        g = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            step(d)  # first launches outside capture (lazy set-up)
+            with torch.cuda.graph(g, stream=side):
+                step(d)
+        stream.wait_stream(side)
+        torch.cuda.synchronize()
+        evg = [new_events(2) for _ in range(args.steps)]
+        for i in range(args.steps):
+            flush.zero_()
+            evg[i][0].record(stream)
+            g.replay()
+            evg[i][1].record(stream)
+        torch.cuda.synchronize()
+        graph_ms = float(np.mean([a.elapsed_time(b) for a, b in evg]))
+        graph_ms = _max_over_ranks([graph_ms], dist, dev)[0]
+        del g
+
     # ---- components: the same steps with events around each call
     evc = [new_events(4) for _ in range(args.steps)]
     torch.cuda.synchronize()
@@ -582,6 +606,10 @@ def _measure(args, name, layout, dev, dist, ws_world):
             "attention": {"ms": round(dec_ms, 5)},
             "timing": "a second timed pass of the same steps with events around each call "
                       "(each pair of events adds ~2 us of its own)"},
+        "graph": None if graph_ms is None else {
+            "ms_per_step": round(graph_ms, 5),
+            "value": round(_weak_value(ws_world, kv_bytes, graph_ms), 2),
+            "what": "the same step captured once in a CUDA graph and replayed"},
         "gpu_launches": launches * args.steps,
         "clocks": clk.summary(),
         "wall_s_timed_region": round(t_wall, 4),
@@ -672,6 +700,7 @@ def run_gpu(args):
         "e2e": res["e2e"],
         "components": res["components"],
         "gpu_launches": res["gpu_launches"],
+        "graph": res["graph"],
         "clocks": res["clocks"],
         "wall_s_timed_region": res["wall_s_timed_region"],
         "memory": res["memory"],
@@ -860,6 +889,8 @@ def main():
     ap.add_argument("--no-shared-prefix", action="store_true",
                     help="decode shared-prefix workloads with pa_decode instead of "
                          "pa_decode_shared_prefix")
+    ap.add_argument("--no-graph", action="store_true",
+                    help="skip the CUDA-graph replay of the step")
     ap.add_argument("--no-also", action="store_true",
                     help="skip the 13B-shaped and contiguous-layout lines of the default run")
     ap.add_argument("--layout", choices=("paged", "contiguous"), default="paged",

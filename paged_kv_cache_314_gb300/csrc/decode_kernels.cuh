@@ -704,28 +704,31 @@ __device__ __forceinline__ void decode_produce(const DecodeParams& p, unsigned c
 }
 
 
-// Split-K merge of one (query row, head) by one warp: M = max_i m_i,
-// out = sum_i 2^(m_i-M) o_i / sum_i 2^(m_i-M) l_i over its nparts partial
-// states.  The states are read from L2 (the decode kernel just wrote them),
-// eight partitions at a time with every load of a chunk in flight together, and
-// merged online across chunks.  A lane owns D/32 output columns.
-template <typename T, int D>
-__device__ __forceinline__ void merge_row(const DecodeParams& p, size_t row, int nparts,
-                                          int lane) {
+// Online merge, by one warp, of the partial states in slots first,
+// first + step, ... (below n) of one row: returns the running maximum M, the
+// sum L = sum_i 2^(m_i-M) l_i and this lane's D/32 columns of
+// O = sum_i 2^(m_i-M) o_i.  The states are read from L2 (the decode kernel
+// just wrote them), eight at a time with every load of a chunk in flight
+// together.
+template <int D>
+__device__ __forceinline__ void merge_online(const DecodeParams& p, size_t base, int first,
+                                             int step, int n, int lane, float& M, float& L,
+                                             float (&O)[D / 32]) {
     constexpr int kCols = D / 32;
     constexpr int kChunk = 8;
     static_assert(kCols == 2 || kCols == 4, "head_dim 64 or 128");
-    const size_t base = row * p.max_parts;
-    float M = -INFINITY, L = 0.f, O[kCols];
+    M = -INFINITY;
+    L = 0.f;
 #pragma unroll
     for (int c = 0; c < kCols; ++c) O[c] = 0.f;
 #pragma unroll 1
-    for (int i0 = 0; i0 < nparts; i0 += kChunk) {
+    for (int i0 = first; i0 < n; i0 += kChunk * step) {
         float mi[kChunk], li[kChunk], oi[kChunk][kCols];
 #pragma unroll
         for (int k = 0; k < kChunk; ++k) {
-            const bool in = i0 + k < nparts;
-            const size_t r = base + (in ? i0 + k : i0);  // a slot inside the row either way
+            const int i = i0 + k * step;
+            const bool in = i < n;
+            const size_t r = base + (in ? i : i0);  // a slot inside the row either way
             mi[k] = in ? __ldcg(p.ws_m + r) : -INFINITY;
             li[k] = in ? __ldcg(p.ws_l + r) : 0.f;
             const float* po = p.ws_o + r * D + lane * kCols;
@@ -758,6 +761,16 @@ __device__ __forceinline__ void merge_row(const DecodeParams& p, size_t row, int
         }
         M = Mc;
     }
+}
+
+// Split-K merge of one (query row, head) by one warp over its nparts partial
+// states; a lane writes D/32 output columns.
+template <typename T, int D>
+__device__ __forceinline__ void merge_row(const DecodeParams& p, size_t row, int nparts,
+                                          int lane) {
+    constexpr int kCols = D / 32;
+    float M, L, O[kCols];
+    merge_online<D>(p, row * p.max_parts, 0, 1, nparts, lane, M, L, O);
     T* out = static_cast<T*>(p.out) + row * D + lane * kCols;
 #pragma unroll
     for (int c = 0; c < kCols; ++c) out[c] = Elem<T>::from_float(L > 0.f ? O[c] / L : 0.f);
@@ -975,12 +988,15 @@ __global__ void __launch_bounds__(DecodeTile<T, D, GT, TC>::kThreads,
     }
 }
 
-// Merges the partitions of one (sequence, query head): M = max_i m_i,
-// out = sum_i 2^(m_i-M) o_i / sum_i 2^(m_i-M) l_i.  Four warps split the
-// partitions; each lane owns D/32 output columns.
+// Merges the partitions of one (sequence, query head) when a context has
+// more than kRowMergeMaxParts of them: M = max_i m_i, out = sum_i 2^(m_i-M)
+// o_i / sum_i 2^(m_i-M) l_i.  Eight warps take every eighth partition, each
+// merging its share online with eight partial states requested at once, and
+// combine their (M, L, O) through shared memory; a lane owns D/32 columns.
 template <typename T, int D>
-__global__ void __launch_bounds__(128) decode_reduce_kernel(const DecodeParams p) {
+__global__ void __launch_bounds__(256) decode_reduce_kernel(const DecodeParams p) {
     constexpr int kCols = D / 32;
+    constexpr int kWarps = 8;
     const int sh = blockIdx.x;  // q / out row x query head
     const int tok = sh / p.num_q_heads;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -1001,42 +1017,35 @@ __global__ void __launch_bounds__(128) decode_reduce_kernel(const DecodeParams p
         return;
     const int nparts = items_of(sq.ctx, max_ctx, p.partition_tokens);
     if (nparts <= 1) return;
-    const size_t row = static_cast<size_t>(sh) * p.max_parts;
+    const size_t base = static_cast<size_t>(sh) * p.max_parts;
 
-    __shared__ float red_m[4];
-    __shared__ float red_l[4];
-    __shared__ float red_o[4][D];
-    float M = -INFINITY;
-    for (int i = threadIdx.x; i < nparts; i += 128) M = fmaxf(M, p.ws_m[row + i]);
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-    if (lane == 0) red_m[warp] = M;
-    __syncthreads();
-    M = fmaxf(fmaxf(red_m[0], red_m[1]), fmaxf(red_m[2], red_m[3]));
-
-    float L = 0.f, O[kCols];
-#pragma unroll
-    for (int c = 0; c < kCols; ++c) O[c] = 0.f;
-    if (M != -INFINITY) {
-#pragma unroll 4
-        for (int i = warp; i < nparts; i += 4) {
-            const float mi = p.ws_m[row + i];
-            const float sc = fast_exp2(mi - M);  // empty partition: m = -inf -> 0
-            L = fmaf(sc, p.ws_l[row + i], L);
-            const float* po = p.ws_o + (row + i) * D + lane * kCols;
-#pragma unroll
-            for (int c = 0; c < kCols; ++c) O[c] = fmaf(sc, po[c], O[c]);
-        }
+    float M, L, O[kCols];
+    merge_online<D>(p, base, warp, kWarps, nparts, lane, M, L, O);
+    __shared__ float red_m[kWarps];
+    __shared__ float red_l[kWarps];
+    __shared__ float red_o[kWarps][D];
+    if (lane == 0) {
+        red_m[warp] = M;
+        red_l[warp] = L;
     }
-    if (lane == 0) red_l[warp] = L;
 #pragma unroll
     for (int c = 0; c < kCols; ++c) red_o[warp][lane * kCols + c] = O[c];
     __syncthreads();
-    const float Lt = red_l[0] + red_l[1] + red_l[2] + red_l[3];
+    float Mt = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) Mt = fmaxf(Mt, red_m[w]);
     T* out = static_cast<T*>(p.out) + static_cast<size_t>(sh) * D;
-    for (int dd = threadIdx.x; dd < D; dd += 128) {
-        const float Ot = red_o[0][dd] + red_o[1][dd] + red_o[2][dd] + red_o[3][dd];
-        out[dd] = Elem<T>::from_float(Lt > 0.f ? Ot / Lt : 0.f);
+    if (threadIdx.x < D) {
+        float Lt = 0.f, Ot = 0.f;
+        if (Mt != -INFINITY) {
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w) {
+                const float sc = fast_exp2(red_m[w] - Mt);  // a warp with no tokens: 0
+                Lt = fmaf(sc, red_l[w], Lt);
+                Ot = fmaf(sc, red_o[w][threadIdx.x], Ot);
+            }
+        }
+        out[threadIdx.x] = Elem<T>::from_float(Lt > 0.f ? Ot / Lt : 0.f);
     }
 }
 
@@ -1176,7 +1185,7 @@ inline pa_status launch_merge(const DecodeParams& p, cudaStream_t stream) {
         if (cudaLaunchKernelEx(&cfg, decode_merge_rows_kernel<T, D>, p) != cudaSuccess)
             return PA_ERR_CUDA;
     } else {
-        decode_reduce_kernel<T, D><<<static_cast<unsigned>(rows), 128, 0, stream>>>(p);
+        decode_reduce_kernel<T, D><<<static_cast<unsigned>(rows), 256, 0, stream>>>(p);
     }
     return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
