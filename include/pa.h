@@ -150,7 +150,11 @@ pa_status pa_copy_blocks_check(const int32_t* block_mapping, int num_pairs, uint
  * tensor cores; otherwise 256 when max_blocks_per_seq * block_size <= 2048
  * for 32- or 16-bit K/V (short contexts split into few partitions, so the
  * last items of the persistent grid are a large share of the run: shorter
- * items even it out), else 512.  Returns -1 for invalid sizes. */
+ * items even it out), else 512.  Returns -1 for invalid sizes.  (With
+ * partition_tokens = 0, a one-query decode on the SIMT kernel with at most 256
+ * sequences, contexts of at most 4096 tokens and at least 6144 (sequence,
+ * head tile) pairs uses no partitions at all: each pair is one work item over
+ * its whole context, items handed out longest first.) */
 int pa_decode_partition_tokens(int num_q_heads, int num_kv_heads, int head_dim,
                                int max_blocks_per_seq, int block_size, pa_dtype dtype,
                                int partition_tokens);

@@ -203,7 +203,7 @@ struct AttnCall {
     int num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks;
     float scale;
     int partition_tokens;  // resolved, > 0
-    bool partition_default;  // the caller passed 0: the library may lengthen it
+    bool partition_default;  // the caller passed 0: the library may choose other partitions
     pa_dtype dtype;
     void* workspace;
     size_t workspace_bytes;
@@ -271,6 +271,30 @@ pa_status describe(pa_attention_plan_t* plan, int kernel, const DecodeParams& p)
     plan->merge = p.max_parts <= 1 ? PA_MERGE_NONE : PA_MERGE_KERNEL;
     plan->launches = plan->merge == PA_MERGE_KERNEL ? 2 : 1;
     return PA_OK;
+}
+
+// Decode on the SIMT kernel with one query head per tile, the default
+// partitions, contexts of at most kLptMaxContext tokens, at most kLptMaxSeqs
+// sequences and at least
+// kLptMinItems (sequence, head tile) pairs -- about eight per CTA of the
+// persistent grid, so whole contexts are fine enough a grain: one work item
+// per pair over the whole context, handed out longest first, so the grid's
+// last items are its shortest and no partial states or merge kernel are
+// needed.  (With fewer pairs, 256- or 512-token partitions balance better:
+// the 7B-shaped batch, 2048 pairs, takes 0.236 ms whole and 0.219 ms split.)
+constexpr long long kLptMaxContext = 4096;
+constexpr long long kLptMinItems = 6144;
+
+void use_lpt(const AttnCall& a, DecodeParams& p) {
+    const long long max_ctx = static_cast<long long>(a.max_blocks_per_seq) * a.block_size;
+    if (a.query_start != nullptr || !a.partition_default || max_ctx > kLptMaxContext ||
+        a.num_seqs > kLptMaxSeqs || p.tile_heads != 1 ||
+        static_cast<long long>(a.num_seqs) * p.head_tiles < kLptMinItems)
+        return;
+    p.lpt = 1;
+    p.partition_tokens = static_cast<int>(max_ctx);
+    p.max_parts = 1;
+    p.ws_m = p.ws_l = p.ws_o = nullptr;
 }
 
 // Shared by pa_decode, pa_multi_query and pa_attention_plan once the
@@ -349,6 +373,7 @@ pa_status run_attention(const AttnCall& a) {
             }
         }
         const int gt = heads * tokens;
+        use_lpt(a, p);
         if (plan) return describe(a.plan, PA_KERNEL_SIMT_FP8, p);
         return a.dtype == PA_BF16 ? launch_decode_fp8_bf16(p, gt, st)
                                   : launch_decode_fp8_f16(p, gt, st);
@@ -412,6 +437,7 @@ pa_status run_attention(const AttnCall& a) {
         }
     }
     const int gt = heads * tokens;
+    use_lpt(a, p);
     if (plan) return describe(a.plan, PA_KERNEL_SIMT, p);
     if (a.query_start != nullptr) {
         switch (a.dtype) {
@@ -495,8 +521,8 @@ extern "C" pa_status pa_decode(void* out, const void* q, const void* k_cache, co
                                              max_blocks_per_seq, block_size, dtype, partition_tokens);
     const AttnCall a{out, q, nullptr, num_seqs, k_cache, v_cache, nullptr, nullptr, block_tables,
                      max_blocks_per_seq, context_lens, num_seqs, num_q_heads, num_kv_heads,
-                     head_dim, block_size, num_blocks, scale, P, false, dtype, workspace,
-                     workspace_bytes, d_err, stream};
+                     head_dim, block_size, num_blocks, scale, P, partition_tokens == 0, dtype,
+                     workspace, workspace_bytes, d_err, stream};
     return run_attention(a);
 }
 
@@ -524,8 +550,8 @@ extern "C" pa_status pa_decode_fp8(void* out, const void* q, pa_dtype q_dtype, c
     if (static_cast<long long>(num_seqs) * num_q_heads > 0x7fffffffLL) return PA_ERR_UNSUPPORTED;
     const AttnCall a{out, q, nullptr, num_seqs, k_cache, v_cache, k_scale, v_scale, block_tables,
                      max_blocks_per_seq, context_lens, num_seqs, num_q_heads, num_kv_heads,
-                     head_dim, block_size, num_blocks, scale, P, false, q_dtype, workspace,
-                     workspace_bytes, d_err, stream};
+                     head_dim, block_size, num_blocks, scale, P, partition_tokens == 0, q_dtype,
+                     workspace, workspace_bytes, d_err, stream};
     return run_attention(a);
 }
 
@@ -618,7 +644,7 @@ extern "C" pa_status pa_attention_plan(int num_seqs, int num_query_tokens, int m
     const AttnCall a{nullptr, nullptr, multi_query ? static_cast<const int32_t*>(any) : nullptr,
                      num_query_tokens, nullptr, nullptr, scales, scales, nullptr,
                      max_blocks_per_seq, nullptr, num_seqs, num_q_heads, num_kv_heads, head_dim,
-                     block_size, num_blocks, 1.0f, P, multi_query && partition_tokens == 0, q_dtype,
+                     block_size, num_blocks, 1.0f, P, partition_tokens == 0, q_dtype,
                      nullptr, 0, nullptr, nullptr, plan};
     return run_attention(a);
 }

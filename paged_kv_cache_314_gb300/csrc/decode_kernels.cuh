@@ -108,9 +108,20 @@ struct DecodeParams {
     int prefix_partition_tokens = 0;  // partition length of the prefix pass
     int prefix_parts = 0;             // partition slots reserved for the prefix pass
     int skip_merge = 0;               // the launch leaves the merge to a later kernel
+    // Decode with whole-context work items handed out longest first (one query
+    // per sequence and query head per tile, at most kLptMaxSeqs sequences):
+    // item r * head_tiles + h is head h of the r-th sequence in decreasing
+    // order of context length, by classes of kLptClass tokens; no partial
+    // states.
+    int lpt = 0;
 };
 
 __host__ __device__ constexpr int align16(int x) { return (x + 15) / 16 * 16; }
+
+// Longest-first whole-context decode (DecodeParams::lpt): sequences per call
+// (eight per lane of the producer warp), and the width of a length class.
+constexpr int kLptMaxSeqs = 256;
+constexpr int kLptClass = 256;
 
 // Sequences of at most this many partitions are merged by one warp per
 // (query row, head) (decode_merge_rows_kernel); longer ones by a CTA per row
@@ -178,8 +189,9 @@ struct DecodeTile {
     // (one row per tile with 8- or 16-bit elements: a 32 KB ring, so that five CTAs
     // -- twenty consumer warps -- share an SM, 160 KB of copies still in flight)
     static constexpr int kStages = (kElem <= 2 && GT == 1) ? 32768 / kStageBytes : 65536 / kStageBytes;
-    // CTAs per SM the register budget must allow: five with the 32 KB ring
-    static constexpr int kMinCtasPerSm = (kElem <= 2 && GT == 1) ? 5 : 1;
+    // CTAs per SM the register budget must allow: five with the 32 KB ring,
+    // three with the 64 KB ring (what shared memory allows, up to 4 rows)
+    static constexpr int kMinCtasPerSm = (kElem <= 2 && GT == 1) ? 5 : GT <= 4 ? 3 : 1;
     static constexpr int kItems = GT >= 4 ? 2 : 3;    // item slots in flight
     static constexpr int kQBytes = GT * D * sizeof(T);  // query rows of one item
     static constexpr int kMergeFloats = kConsumerWarps * GT * (D + 2);  // per item slot
@@ -411,7 +423,8 @@ __device__ __forceinline__ void decode_stage(const unsigned char* sK, const unsi
 
 // kMulti: several query tokens per sequence (query_start given); false
 // compiles the one-query-per-sequence decode without any of that logic.
-template <typename T, int D, int GT, bool kMulti, typename TC>
+// kLongestFirst: whole-context items handed out longest first (DecodeParams::lpt).
+template <typename T, int D, int GT, bool kMulti, typename TC, bool kLongestFirst>
 __device__ __forceinline__ void decode_produce(const DecodeParams& p, unsigned char* smem) {
     using C = DecodeTile<T, D, GT, TC>;
     constexpr int W = C::kConsumerWarps;
@@ -447,7 +460,38 @@ __device__ __forceinline__ void decode_produce(const DecodeParams& p, unsigned c
             items_lane = sl < S ? HT * items_of(sq_lane.ctx, max_ctx, P) : 0;
         }
     };
-    load_window();
+    if constexpr (!kLongestFirst) load_window();
+
+    // Longest-first order (p.lpt): lane l holds sequences l + 32 j, their
+    // context lengths and length classes (class 0: empty or out of range, no
+    // tokens to read; else ceil(ctx / kLptClass)); lane k < nclass counts the
+    // sequences of class nclass-1-k (longest first) and where they start.
+    int lpt_len[kLptMaxSeqs / 32], lpt_cls[kLptMaxSeqs / 32];
+    int lpt_start = 0, lpt_cnt = 0;
+    const int nclass = (max_ctx + kLptClass - 1) / kLptClass + 1;
+    if constexpr (kLongestFirst) {
+#pragma unroll
+        for (int j = 0; j < kLptMaxSeqs / 32; ++j) {
+            const int sj = lane + 32 * j;
+            const int cj = sj < S ? __ldg(p.context_lens + sj) : -1;
+            lpt_len[j] = cj;
+            lpt_cls[j] = sj >= S ? -1 : (cj <= 0 || cj > max_ctx) ? 0 : (cj + kLptClass - 1) / kLptClass;
+        }
+        for (int k = 0; k < nclass; ++k) {
+            int n = 0;
+#pragma unroll
+            for (int j = 0; j < kLptMaxSeqs / 32; ++j)
+                n += __popc(__ballot_sync(0xffffffffu, lpt_cls[j] == nclass - 1 - k));
+            if (lane == k) lpt_cnt = n;
+        }
+        int incl = lpt_cnt;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, incl, off);
+            if (lane >= off) incl += y;
+        }
+        lpt_start = incl - lpt_cnt;
+    }
     int c = 0;         // stages issued by this CTA
     int item_seq = 0;  // items taken by this CTA
     int q_issued = 0;  // items whose query rows were requested
@@ -460,6 +504,31 @@ __device__ __forceinline__ void decode_produce(const DecodeParams& p, unsigned c
     while (!aborted) {
         // ---- which sequence holds item_id?
         bool found = false;
+        int lpt_ctx = 0;
+        if constexpr (kLongestFirst) {
+            // item_id = r * HT + head tile; the r-th sequence longest first
+            const int r = item_id / HT;
+            if (r < S) {
+                const unsigned hitc = __ballot_sync(0xffffffffu, lane < nclass && r >= lpt_start &&
+                                                                     r < lpt_start + lpt_cnt);
+                const int k = __ffs(hitc) - 1;  // the class, as a lane
+                int kk = r - __shfl_sync(0xffffffffu, lpt_start, k);
+                const int cl = nclass - 1 - k;
+#pragma unroll
+                for (int j = 0; j < kLptMaxSeqs / 32; ++j) {
+                    const unsigned mk = __ballot_sync(0xffffffffu, lpt_cls[j] == cl);
+                    const int n = __popc(mk);
+                    if (!found && kk < n) {
+                        const int pos = __fns(mk, 0, kk + 1);  // the kk-th sequence of the class
+                        s_cur = pos + 32 * j;
+                        lpt_ctx = __shfl_sync(0xffffffffu, lpt_len[j], pos);
+                        base = r * HT;
+                        found = true;
+                    }
+                    kk -= n;
+                }
+            }
+        } else {
         while (s_cur < S) {
             if (s_cur - win0 >= 32) {
                 win0 = s_cur;
@@ -485,6 +554,7 @@ __device__ __forceinline__ void decode_produce(const DecodeParams& p, unsigned c
             base += total;
             s_cur = win0 + 32;
         }
+        }
         if (!found) break;
         // take the next item now; its number is needed only after this item is issued
         int next_id = 0;
@@ -492,7 +562,8 @@ __device__ __forceinline__ void decode_produce(const DecodeParams& p, unsigned c
 
         const int s = s_cur;
         SeqQueries sq;
-        sq.ctx = __shfl_sync(0xffffffffu, sq_lane.ctx, s_cur - win0);
+        if constexpr (kLongestFirst) sq.ctx = lpt_ctx;
+        else sq.ctx = __shfl_sync(0xffffffffu, sq_lane.ctx, s_cur - win0);
         sq.multi = kMulti;
         if constexpr (kMulti) {
             sq.q0 = __shfl_sync(0xffffffffu, sq_lane.q0, s_cur - win0);
@@ -945,7 +1016,7 @@ __device__ __forceinline__ void decode_consume(const DecodeParams& p, unsigned c
     }
 }
 
-template <typename T, int D, int GT, bool kMulti, typename TC>
+template <typename T, int D, int GT, bool kMulti, typename TC, bool kLongestFirst>
 __global__ void __launch_bounds__(DecodeTile<T, D, GT, TC>::kThreads,
                                   DecodeTile<T, D, GT, TC>::kMinCtasPerSm)
     decode_persistent_kernel(const DecodeParams p) {
@@ -970,7 +1041,7 @@ __global__ void __launch_bounds__(DecodeTile<T, D, GT, TC>::kThreads,
     // step's kv_write) when the launch allows it; the cache is read only after.
     wait_prior_grids();
     if ((threadIdx.x >> 5) == C::kConsumerWarps)
-        decode_produce<T, D, GT, kMulti, TC>(p, smem);
+        decode_produce<T, D, GT, kMulti, TC, kLongestFirst>(p, smem);
     else
         decode_consume<T, D, GT, kMulti, TC>(p, smem);
     __syncthreads();
@@ -1190,12 +1261,12 @@ inline pa_status launch_merge(const DecodeParams& p, cudaStream_t stream) {
     return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
-template <typename T, int D, int GT, bool kMulti, typename TC = T>
+template <typename T, int D, int GT, bool kMulti, typename TC = T, bool kLongestFirst = false>
 inline pa_status launch_decode_tile(const DecodeParams& p, cudaStream_t stream) {
     using C = DecodeTile<T, D, GT, TC>;
     static std::atomic<uint64_t> smem_configured{0};  // one per instantiation
     static std::atomic<int> ctas_per_sm{0};
-    auto kernel = decode_persistent_kernel<T, D, GT, kMulti, TC>;
+    auto kernel = decode_persistent_kernel<T, D, GT, kMulti, TC, kLongestFirst>;
     if (ensure_smem(kernel, C::kSmemBytes, smem_configured) != PA_OK) return PA_ERR_CUDA;
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
@@ -1240,7 +1311,10 @@ inline pa_status launch_decode_tile(const DecodeParams& p, cudaStream_t stream) 
 template <typename T, int D, bool kMulti>
 inline pa_status launch_decode_dim(const DecodeParams& p, int gt, cudaStream_t stream) {
     switch (gt) {
-        case 1: return launch_decode_tile<T, D, 1, kMulti>(p, stream);
+        case 1:
+            if constexpr (!kMulti)
+                if (p.lpt) return launch_decode_tile<T, D, 1, false, T, true>(p, stream);
+            return launch_decode_tile<T, D, 1, kMulti>(p, stream);
         case 2: return launch_decode_tile<T, D, 2, kMulti>(p, stream);
         case 4: return launch_decode_tile<T, D, 4, kMulti>(p, stream);
         case 8: return launch_decode_tile<T, D, 8, kMulti>(p, stream);
@@ -1262,7 +1336,10 @@ inline pa_status launch_decode_typed(const DecodeParams& p, int head_dim, int gt
 template <typename T, bool kMulti>
 inline pa_status launch_decode_fp8_typed(const DecodeParams& p, int gt, cudaStream_t stream) {
     switch (gt) {
-        case 1: return launch_decode_tile<T, 128, 1, kMulti, __nv_fp8_e4m3>(p, stream);
+        case 1:
+            if constexpr (!kMulti)
+                if (p.lpt) return launch_decode_tile<T, 128, 1, false, __nv_fp8_e4m3, true>(p, stream);
+            return launch_decode_tile<T, 128, 1, kMulti, __nv_fp8_e4m3>(p, stream);
         case 2: return launch_decode_tile<T, 128, 2, kMulti, __nv_fp8_e4m3>(p, stream);
         case 4: return launch_decode_tile<T, 128, 4, kMulti, __nv_fp8_e4m3>(p, stream);
     }

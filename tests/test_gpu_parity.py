@@ -142,6 +142,31 @@ def test_many_short_sequences_and_bad_lengths():
     assert_close(out_f64(outs[0]), ref, "bf16", "many")
 
 
+def test_longest_first_whole_context_items():
+    """Decode with the default partitions over at most 256 sequences, contexts
+    of at most 4096 tokens and >= 6144 (sequence, head) pairs runs one work
+    item per pair over its whole context, longest first (no merge): every
+    output against the oracle, with empty, out-of-range and maximal contexts
+    among them, and the same batch with explicit partitions agrees."""
+    rng = np.random.default_rng(250)
+    ctx = rng.integers(1, 700, size=256)
+    ctx[[0, 7, 100]] = [0, 4096, 1]
+    w = wl.custom("lpt", list(ctx), dtype="f16", num_q_heads=32, num_kv_heads=32, head_dim=64,
+                  block_size=16, seed=251, max_blocks_per_seq=256, pool_factor=1.1)
+    w.context_lens[5] = 4096 + 16   # out of range: zero row, flagged
+    w.context_lens[9] = -2
+    plan = pa.attention_plan(256, 32, 32, 64, 256, 16, w.num_blocks, "f16")
+    assert plan["max_parts"] == 1 and plan["merge"] == "none"
+    d = upload(w)
+    out = gpu_step(w, d, partition_tokens=0)
+    _, _, ref, err = oracle_step(w)
+    assert err == oracle.ERR_CTX_OOB and int(d["d_err"].item()) == err
+    assert_close(out_f64(out), ref, "f16", "longest first")
+    assert (out[5] == 0).all() and (out[9] == 0).all() and (out[0] == 0).all()
+    split = gpu_step(w, upload(w), partition_tokens=256)
+    assert_close(out_f64(split), ref, "f16", "longest first, split")
+
+
 # ---------------------------------------------------------------------------
 # named workloads at full size
 # ---------------------------------------------------------------------------
