@@ -113,24 +113,38 @@ def _alu_peak_tflops(sm_count):
     return sm_count * FP32_LANES_PER_SM * 2 * mhz * 1e6 / 1e12
 
 
-def _rows(w):
-    """(sequence, row, tokens attended) for every query row of the step."""
+def _rows(w, threads=1):
+    """Work units of the oracle over the step's query rows: (sequence, row,
+    tokens attended, query head or None for all heads).  A decode step with
+    fewer sequences than host threads is cut into (sequence, head) units so
+    that a few very long sequences still reach every core; the bytes a unit
+    stands for are the step's K/V bytes x its share of the tokens attended
+    (a head unit: 1 / num_q_heads of its sequence's)."""
     out = []
     if w.query_start is None:
+        per_head = w.kv_dtype != "e4m3" and w.num_seqs < threads
         for s in range(w.num_seqs):
-            out.append((s, s, max(0, int(w.context_lens[s]))))
+            n = max(0, int(w.context_lens[s]))
+            if per_head:
+                out.extend((s, s, n / w.num_q_heads, h) for h in range(w.num_q_heads))
+            else:
+                out.append((s, s, n, None))
     else:
         for s in range(w.num_seqs):
             q0, q1 = int(w.query_start[s]), int(w.query_start[s + 1])
             n = int(w.context_lens[s])
             for i in range(q1 - q0):
-                out.append((s, q0 + i, n - (q1 - q0) + i + 1))
+                out.append((s, q0 + i, n - (q1 - q0) + i + 1, None))
     return out
 
 
-def _oracle_row(w, kc, vc, s, r, n):
-    """The oracle on one query row (all heads) of the step."""
+def _oracle_row(w, kc, vc, s, r, n, h=None):
+    """The oracle on one work unit of the step: a query row (all heads), or
+    one head of a decode row."""
     import oracle
+    if h is not None:
+        return oracle.decode_head(w.q, kc, vc, w.block_tables, w.context_lens, s, h, scale=w.scale,
+                                  dtype=w.dtype)
     if w.kv_dtype == "e4m3":
         return oracle.decode_fp8(np.ascontiguousarray(w.q[r:r + 1]), kc, vc, w.k_scale, w.v_scale,
                                  np.ascontiguousarray(w.block_tables[s:s + 1]),
@@ -304,8 +318,8 @@ def _oracle_pass(w, threads, cpu_seconds, max_wall_s):
     / time."""
     import concurrent.futures as cf
     kc, vc = w.k_cache, w.v_cache
-    rows = _rows(w)
-    total = max(1, sum(n for _, _, n in rows))
+    rows = _rows(w, threads)
+    total = max(1, sum(r[2] for r in rows))
     kv_bytes = w.kv_read_bytes()
     done, n_rows, t0 = 0, 0, time.perf_counter()
     with cf.ThreadPoolExecutor(threads) as ex:
@@ -316,7 +330,7 @@ def _oracle_pass(w, threads, cpu_seconds, max_wall_s):
             first = n_rows % len(rows)
             batch = rows[first:first + threads]
             list(ex.map(lambda x: _oracle_row(w, kc, vc, *x), batch))
-            done += sum(n for _, _, n in batch)
+            done += sum(r[2] for r in batch)
             n_rows += len(batch)
     dt = time.perf_counter() - t0
     eq = kv_bytes * done / total
@@ -328,14 +342,17 @@ def _cpu_baseline(w, cpu_seconds=16.0, max_wall_s=20.0, single_seconds=4.0):
     threads = os.cpu_count() or 1
     v, n_rows, eq, dt, nrows = _oracle_pass(w, threads, cpu_seconds, max_wall_s)
     v1, n1, eq1, dt1, _ = _oracle_pass(w, 1, single_seconds, single_seconds)
-    unit = "sequences" if w.query_start is None else "query rows"
+
+    def unit(t):
+        return ("query rows" if w.query_start is not None else
+                "(sequence, head) pairs" if w.kv_dtype != "e4m3" and w.num_seqs < t else "sequences")
     return {"value": v, "unit": "GB/s", "cores": threads, "kind": "oracle",
-            "sample": f"attention of {n_rows} {unit} ({n_rows / nrows:.3f} passes over the "
-                      f"step's {nrows}; {eq / 1e6:.0f} MB of the step's K/V bytes in "
-                      f"proportion to the tokens attended), fp64 C oracle, one row per host "
+            "sample": f"attention of {n_rows} {unit(threads)} ({n_rows / nrows:.3f} passes over "
+                      f"the step's {nrows}; {eq / 1e6:.0f} MB of the step's K/V bytes in "
+                      f"proportion to the tokens attended), fp64 C oracle, one unit per host "
                       f"thread, {dt:.1f} s wall",
             "single_thread": {"value": v1, "unit": "GB/s", "cores": 1,
-                              "sample": f"{n1} {unit}, {eq1 / 1e6:.0f} MB, {dt1:.1f} s wall"},
+                              "sample": f"{n1} {unit(1)}, {eq1 / 1e6:.0f} MB, {dt1:.1f} s wall"},
             "host_cpus": _host_cpus()}
 
 
@@ -538,7 +555,7 @@ def _measure(args, name, layout, dev, dist, ws_world):
     kv_bytes = w.kv_read_bytes()
     unique_bytes = w.kv_unique_read_bytes() if w.num_pairs or "gqa" in w.name else kv_bytes
     peak, peak_kind = _hbm_peak()
-    flops = 4 * w.head_dim * w.num_q_heads * sum(n for _, _, n in _rows(w))
+    flops = 4 * w.head_dim * w.num_q_heads * sum(r[2] for r in _rows(w))
     tensor_peak, tensor_kind = _tensor_peak()
     alu_peak = _alu_peak_tflops(sms)
     tc_path = plan["kernel"] in TC_KERNELS or shared
@@ -738,10 +755,12 @@ def run_reference(args):
                                                    if args.partition is not None else {}))
     threads = os.cpu_count() or 1
     # each step: the oracle's copy_blocks and kv_write, then attention of a
-    # bounded sample of query rows (all heads; whole sequences for decode), in
-    # order, spread over host threads.  Bytes: the step's K/V bytes in
-    # proportion to the tokens the sampled rows attend to.
-    rows = _rows(w)
+    # bounded sample of the step's work units (query rows with all their heads;
+    # (sequence, head) pairs when a decode step has fewer sequences than host
+    # threads), in order, spread over host threads.  Bytes: the step's K/V
+    # bytes in proportion to the tokens the sampled units attend to.
+    rows = _rows(w, threads)
+    unit = "(sequence, head) pairs" if rows and rows[0][3] is not None else "query rows"
     total = max(1, sum(r[2] for r in rows))
     kv_bytes = w.kv_read_bytes()
     cum = np.cumsum([r[2] for r in rows]).astype(np.float64) * kv_bytes / total
@@ -783,7 +802,7 @@ def run_reference(args):
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads,
                          "kind": "oracle",
                          "sample": f"per step: oracle copy_blocks + kv_write + attention of the "
-                                   f"first {n} of {len(rows)} query rows ({sample_bytes / 1e6:.0f}"
+                                   f"first {n} of {len(rows)} {unit} ({sample_bytes / 1e6:.0f}"
                                    f" MB of the step's K/V bytes in proportion to the tokens "
                                    f"attended), fp64 C oracle, {threads} host threads",
                          "host_cpus": _host_cpus()},
