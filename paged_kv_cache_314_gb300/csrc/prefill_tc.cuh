@@ -12,8 +12,10 @@
 // its causal span of the table, one 128-token K/V stage at a time:
 //
 //   S = Q . K^T   (tcgen05.mma, M = 128 rows, N = 128 tokens, fp32 in TMEM)
-//   P = 2^(S * scale * log2 e - m)     two threads per row, from TMEM
-//   O += P . V    (M = 128 rows, N = 128 head dimensions, fp32 in TMEM)
+//   P = 2^(S * scale * log2 e - m)     two threads per row, from TMEM, rounded
+//                                      to the 16-bit type back into TMEM
+//   O += P . V    (M = 128 rows, N = 128 head dimensions, fp32 in TMEM; P is
+//                  the A operand read from TMEM)
 //
 // with a running row maximum m that is raised only when a stage's maximum
 // exceeds it by more than 2^8 (then O in TMEM and the row sum are rescaled;
@@ -22,8 +24,14 @@
 // Warps: 0 walks the work items and issues the Q and K copies, 1 issues the
 // MMAs (one elected lane) and owns TMEM, 2-9 are the softmax warps (two
 // threads per query row, one per 64-column half; warp w reads TMEM lanes
-// 32*(w%4)..), 10 issues the V copies from a per-stage plan.  Shared memory: a 2-stage K/V ring (the K and
-// V halves of a slot released separately), two Q slots, one P tile.
+// 32*(w%4)..), 10 issues the V copies from a per-stage plan once the V half
+// of the slot is free.  Shared memory: a 2-stage K/V ring (the K and V halves
+// of a slot released separately), two Q slots.  TMEM: two S buffers, O, two P
+// buffers (stage c in buffer c % 2), so the softmax of stage c waits for P.V
+// of stage c-2, not c-1, unless O must be rescaled.  The softmax warps
+// take each stage's record from its own barrier and wait for the stage's V
+// only when some of its rows must be zeroed, so a stage's softmax never
+// waits on its V copies; the MMA warp waits for them before P.V.
 #pragma once
 
 #include <stdint.h>
@@ -43,42 +51,49 @@ struct PfTile {
     static constexpr int kStages = 2;
     static constexpr int kTileBytes = kStageTok * D * 2;  // K or V of a stage: 32 KB
     static constexpr int kStageBytes = 2 * kTileBytes;
-    static constexpr int kOpBytes = kRows * D * 2;       // Q or P: [2 halves][128 rows][128 B]
+    static constexpr int kOpBytes = kRows * D * 2;       // Q: [2 halves][128 rows][128 B]
     static constexpr int kHalf = kOpBytes / 2;
     static constexpr int kRingOff = 0;
     static constexpr int kQOff = kStages * kStageBytes;  // Q slots [2]
-    static constexpr int kPOff = kQOff + 2 * kOpBytes;
-    // stage meta, 64 B each, in 4 slots (stage c in slot c % 4): stage c+2's is
-    // written as soon as its K copies are issued, while stage c's is still read
-    static constexpr int kMetaSlots = 4;
-    static constexpr int kMetaOff = kPOff + kOpBytes;
-    static constexpr int kPlanOff = kMetaOff + kMetaSlots * 64;  // V box rows of a stage [8] + stop word
+
+    // stage meta (64 B) and V plan, in 8 slots each (stage c in slot c % 8),
+    // written as soon as the stage's K copies are issued, while earlier
+    // stages' are still read
+    static constexpr int kMetaShift = 3;
+    static constexpr int kMetaSlots = 1 << kMetaShift;
+    static constexpr int kMetaOff = kQOff + 2 * kOpBytes;
+    static constexpr int kPlanOff = kMetaOff + kMetaSlots * 64;  // V box rows [8], stop word, bytes
     static constexpr int kPlanInts = 12;
     static constexpr int kPlanStop = 8;
-    static constexpr int kBarOff = kPlanOff + kStages * kPlanInts * 4;
-    // barriers (indices)
-    static constexpr int kFullK = 0, kEmptyK = 2, kFullV = 4, kEmptyV = 6, kVPlan = 8;
-    static constexpr int kQFull = 10, kQEmpty = 12, kSFull = 14, kSFree = 16;
-    static constexpr int kPFull = 18, kPFree = 19, kDrain = 20, kNumBars = 21;
+    static constexpr int kPlanBytes = 9;
+    static constexpr int kBarOff = kPlanOff + kMetaSlots * kPlanInts * 4;
+    // barriers (indices): per ring slot, S or P buffer [2], per meta slot [8]
+    static constexpr int kFullK = 0, kEmptyK = 2, kFullV = 4, kEmptyV = 6, kVPlan = 8, kMetaFull = 16;
+    static constexpr int kQFull = 24, kQEmpty = 26, kSFull = 28, kSFree = 30;
+    static constexpr int kPFull = 32, kPFree = 34, kDrain = 36, kNumBars = 37;
     static constexpr int kRedOff = kBarOff + kNumBars * 8;    // row maxima / sums of the halves [2][128]
     static constexpr int kMiscOff = kRedOff + 2 * 128 * 4;    // tmem base, abort, group flags [2]
     static constexpr int kSmemBytes = kMiscOff + 32 + 1024;  // + alignment slack
     static constexpr int kThreads = 352;
-    static constexpr uint32_t kTmemCols = 512;  // S [2] x 128, O 128
+    static constexpr uint32_t kTmemCols = 512;  // S [2] x 128, O 128, P [2] x 64 (16-bit pairs)
     static constexpr uint32_t kOCol = 256;
+    static constexpr uint32_t kPCol = 384;
     static constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
     static_assert(kBf16 || std::is_same<T, __half>::value, "16-bit operands only");
     static_assert(kSmemBytes <= 232448, "shared memory per CTA");
-    // S = Q.K^T: A = Q (K-major), B = K tile (K-major); O += P.V: A = P (K-major),
+    // S = Q.K^T: A = Q (K-major), B = K tile (K-major); O += P.V: A = P (TMEM, K-major),
     // B = V tile (N = head dimension contiguous: MN-major)
     static constexpr uint32_t kIdescS = tc::instr_desc_f16(kBf16, 128, 128, false, false);
     static constexpr uint32_t kIdescO = tc::instr_desc_f16(kBf16, 128, 128, false, true);
 };
 
-// Written by the producer before the stage's arrivals on fullK and fullV.
-// Slot c % 4 is rewritten for stage c+4, whose K copies wait for MMA1 of
-// stage c+2, which the MMA warp issues after MMA2 of stage c and only once
-// the softmax warps have read S of stage c (so both are done with the slot).
+// Written by the producer before the stage's arrivals on fullK and on its
+// meta barrier.  Slot c % 8 (meta and V plan) is rewritten for stage c+8,
+// whose K copies wait for MMA1 of stage c+6, which needs the softmax warps to
+// have read S of stage c+4, so to have finished stage c+3, whose P buffer was
+// free only once MMA2 of stage c+1 completed: by then the MMA warp has read
+// the meta of stage c (its MMA2 went first), the copy warp the plan (V of
+// stage c+1 had landed), the softmax warps the meta.
 struct PfStageMeta {
     uint32_t item_seq;
     int nvalid;       // tokens of the stage before the item's span end
@@ -179,7 +194,6 @@ __device__ __forceinline__ void pf_produce(const DecodeParams& p, const CUtensor
     int* plan = reinterpret_cast<int*>(sm + C::kPlanOff);
     PfStageMeta* meta = reinterpret_cast<PfStageMeta*>(sm + C::kMetaOff);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + C::kMiscOff + 4);
-    int k_only = -1;  // a stage whose K copies were issued but not its V copies (abort)
 
     // Shared-prefix decode (prefix pass): the "sequences" walked are the groups
     // of prefix_group decode sequences; a group's rows are its sequences x the
@@ -341,8 +355,12 @@ __device__ __forceinline__ void pf_produce(const DecodeParams& p, const CUtensor
             const uint32_t tile_bytes = static_cast<uint32_t>(__popc(groups)) * 4096u;
             const uint32_t stage_base = base + C::kRingOff + st * C::kStageBytes;
             if (mine) pf::tma_load_4d(stage_base + r * 4096, mapK, row >> 3, bar(C::kFullK + st));
+            const int ms = cc & (C::kMetaSlots - 1);
+            if (lane < 8) plan[ms * C::kPlanInts + lane] = mine ? row : -1;
             if (lane == 0) {
-                PfStageMeta& m = meta[cc & (C::kMetaSlots - 1)];
+                plan[ms * C::kPlanInts + C::kPlanStop] = 0;
+                plan[ms * C::kPlanInts + C::kPlanBytes] = static_cast<int>(tile_bytes);
+                PfStageMeta& m = meta[ms];
                 uint32_t flags = 0;
                 if (i == 0) flags |= kStageFirst;
                 if (i == nst - 1) flags |= kStageLast;
@@ -357,26 +375,15 @@ __device__ __forceinline__ void pf_produce(const DecodeParams& p, const CUtensor
                 // prefix pass: always a partial state (the merge adds each sequence's own)
                 m.nparts = prefix ? p.prefix_parts + 1 : valid ? np : 0;
                 m.ntok = ntok;
-                // the meta is written before either arrival: the MMA warp reads it
-                // after fullK, the softmax warps after fullV
-                mbar_arrive_expect_tx(bar(C::kFullK + st), tile_bytes);
             }
-            __syncwarp();
-            // the V half is free once MMA2 of the slot's previous stage completed
-            if (cc >= C::kStages && !mbar_wait_warp(bar(C::kEmptyV + st), reuse)) {
-                if (lane == 0) report(p.d_err, PA_DERR_TIMEOUT);
-                *abort_flag = 1;
-                aborted = true;
-                k_only = cc;
-                c = cc + 1;
-                break;
-            }
-            if (lane < 8) plan[st * C::kPlanInts + lane] = mine ? row : -1;
-            if (lane == 0) plan[st * C::kPlanInts + C::kPlanStop] = 0;
             __syncwarp();
             if (lane == 0) {
-                mbar_arrive_expect_tx(bar(C::kFullV + st), tile_bytes);
-                mbar_arrive(bar(C::kVPlan + st));
+                // the meta and the plan are written before these arrivals: the MMA
+                // warp reads the meta after fullK, the softmax warps after the
+                // slot's meta barrier, the copy warp the plan after vPlan
+                mbar_arrive_expect_tx(bar(C::kFullK + st), tile_bytes);
+                mbar_arrive(bar(C::kMetaFull + ms));
+                mbar_arrive(bar(C::kVPlan + ms));
             }
         }
         if (aborted) break;
@@ -386,34 +393,32 @@ __device__ __forceinline__ void pf_produce(const DecodeParams& p, const CUtensor
         if (*abort_flag) aborted = true;
     }
     if (!aborted) {  // one end marker: the other warps read stages in order
-        const int st = c & 1;
+        const int st = c & 1, ms = c & (C::kMetaSlots - 1);
         const uint32_t reuse = static_cast<uint32_t>((c >> 1) - 1) & 1;
-        if (c >= C::kStages && (!mbar_wait_warp(bar(C::kEmptyK + st), reuse) ||
-                                !mbar_wait_warp(bar(C::kEmptyV + st), reuse))) {
+        if (c >= C::kStages && !mbar_wait_warp(bar(C::kEmptyK + st), reuse)) {
             if (lane == 0) report(p.d_err, PA_DERR_TIMEOUT);
             *abort_flag = 1;
         } else {
             if (lane == 0) {
-                PfStageMeta& m = meta[c & (C::kMetaSlots - 1)];
+                PfStageMeta& m = meta[ms];
                 m.flags = kStageEnd;
                 m.nvalid = 0;
                 m.groups = 0;
-                plan[st * C::kPlanInts + C::kPlanStop] = 1;  // the copy warp leaves
+                plan[ms * C::kPlanInts + C::kPlanStop] = 1;  // the copy warp leaves
                 mbar_arrive(bar(C::kFullK + st));
-                mbar_arrive(bar(C::kFullV + st));
-                mbar_arrive(bar(C::kVPlan + st));
+                mbar_arrive(bar(C::kMetaFull + ms));
+                mbar_arrive(bar(C::kVPlan + ms));
             }
             ++c;
         }
     }
     if (lane == 0) {
         if (oob) report(p.d_err, PA_DERR_BLOCK_OOB);
-        // every copy issued here has landed before the CTA may exit
-        for (int cc = max(0, c - C::kStages); cc < c; ++cc) {
-            const uint32_t par = static_cast<uint32_t>(cc >> 1) & 1;
-            if (!mbar_wait(bar(C::kFullK + (cc & 1)), par)) report(p.d_err, PA_DERR_TIMEOUT);
-            if (cc != k_only && !mbar_wait(bar(C::kFullV + (cc & 1)), par)) report(p.d_err, PA_DERR_TIMEOUT);
-        }
+        // every K copy issued here has landed before the CTA may exit (the copy
+        // warp waits for its V copies)
+        for (int cc = max(0, c - C::kStages); cc < c; ++cc)
+            if (!mbar_wait(bar(C::kFullK + (cc & 1)), static_cast<uint32_t>(cc >> 1) & 1))
+                report(p.d_err, PA_DERR_TIMEOUT);
         for (int k = max(0, q_issued - 2); k < q_issued; ++k)
             if (!mbar_wait(bar(C::kQFull + (k & 1)), static_cast<uint32_t>(k >> 1) & 1))
                 report(p.d_err, PA_DERR_TIMEOUT);
@@ -422,34 +427,61 @@ __device__ __forceinline__ void pf_produce(const DecodeParams& p, const CUtensor
 }
 
 // ---- warp 10: the V boxes of each stage, from the producer's plan ------------
+// Stage c: its plan (slot c % 4), then the V half of ring slot c % 2 once MMA2
+// of stage c-2 completed, then the boxes.
 template <typename T>
 __device__ __forceinline__ void pf_copy_v(const DecodeParams& p, const CUtensorMap* mapV,
                                           unsigned char* sm, uint32_t base) {
     using C = PfTile<T>;
     const int lane = threadIdx.x & 31;
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::kBarOff);
+    auto bar = [&](int i) { return smem_addr(bars + i); };
     const int* plan = reinterpret_cast<const int*>(sm + C::kPlanOff);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + C::kMiscOff + 4);
-    for (int c = 0;; ++c) {
-        const int st = c & 1;
-        if (!mbar_wait_warp(smem_addr(bars + C::kVPlan + st), static_cast<uint32_t>(c >> 1) & 1)) {
+    int c = 0;  // stages whose V copies were issued
+    for (;; ++c) {
+        const int st = c & 1, ms = c & (C::kMetaSlots - 1);
+        if (!mbar_wait_warp(bar(C::kVPlan + ms), static_cast<uint32_t>(c >> C::kMetaShift) & 1)) {
             if (lane == 0) report(p.d_err, PA_DERR_TIMEOUT);
             *abort_flag = 1;
             break;
         }
-        if (plan[st * C::kPlanInts + C::kPlanStop] != 0) break;
-        const int row = lane < 8 ? plan[st * C::kPlanInts + lane] : -1;
+        const int* pl = plan + ms * C::kPlanInts;
+        const int stop = pl[C::kPlanStop];
+        const int row = lane < 8 ? pl[lane] : -1;
+        const uint32_t bytes = static_cast<uint32_t>(pl[C::kPlanBytes]);
+        __syncwarp();
+        if (stop != 0) break;
+        if (c >= C::kStages &&
+            !mbar_wait_warp(bar(C::kEmptyV + st), static_cast<uint32_t>((c >> 1) - 1) & 1)) {
+            if (lane == 0) report(p.d_err, PA_DERR_TIMEOUT);
+            *abort_flag = 1;
+            break;
+        }
+        if (lane == 0) mbar_arrive_expect_tx(bar(C::kFullV + st), bytes);
+        __syncwarp();
         if (row >= 0)
             pf::tma_load_4d(base + C::kRingOff + st * C::kStageBytes + C::kTileBytes + lane * 4096, mapV,
-                            row >> 3, smem_addr(bars + C::kFullV + st));
+                            row >> 3, bar(C::kFullV + st));
         __syncwarp();
     }
+    // every V copy issued here has landed before the CTA may exit
+    if (lane == 0)
+        for (int cc = max(0, c - C::kStages); cc < c; ++cc)
+            if (!mbar_wait(bar(C::kFullV + (cc & 1)), static_cast<uint32_t>(cc >> 1) & 1))
+                report(p.d_err, PA_DERR_TIMEOUT);
+    __syncwarp();
 }
 
 // ---- warp 1: MMA issue -------------------------------------------------------
-// Stage c: S[c%2] = Q.K_c^T (MMA1), then O (+)= P_c.V_c (MMA2) once the
-// softmax warps have written P_c.  MMA1 of the next stage goes first when its
-// K has landed and its S buffer is free.
+// Two cursors: MMA1 of stage c1 (S[c1%2] = Q.K^T) once K of c1 has landed and
+// the softmax warps have read S of stage c1-2; MMA2 of stage c2 (O (+)= P.V,
+// P from TMEM buffer c2%2) once P of c2 is published and V of c2 has landed.
+// MMA1 runs ahead of MMA2, so the tensor pipe computes the next stages' S
+// while the softmax warps work on this one.  Whatever is ready is issued at
+// once; with nothing ready the warp polls (non-blocking tests, short sleeps)
+// and gives up after the wait limit without progress.  Lane 0 tests the
+// barriers, reads the meta and issues (the elected lane of a full warp).
 template <typename T>
 __device__ __forceinline__ void pf_mma(const DecodeParams& p, unsigned char* sm, uint32_t base,
                                        uint32_t tmem) {
@@ -459,85 +491,90 @@ __device__ __forceinline__ void pf_mma(const DecodeParams& p, unsigned char* sm,
     auto bar = [&](int i) { return smem_addr(bars + i); };
     const PfStageMeta* meta = reinterpret_cast<const PfStageMeta*>(sm + C::kMetaOff);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + C::kMiscOff + 4);
-    auto fail = [&]() {
-        if (lane == 0) report(p.d_err, PA_DERR_TIMEOUT);
-        *abort_flag = 1;
-    };
     auto stage_k = [&](int c) { return base + C::kRingOff + (c & 1) * C::kStageBytes; };
 
-    // Returns 0 = issued, 1 = end marker, -1 = gave up.
-    auto issue_mma1 = [&](int c) -> int {
-        const int st = c & 1;
-        if (!mbar_wait_warp(bar(C::kFullK + st), static_cast<uint32_t>(c >> 1) & 1)) return -1;
-        const PfStageMeta& m = meta[c & (C::kMetaSlots - 1)];
-        const uint32_t flags = m.flags;
-        if (flags & kStageEnd) return 1;
-        const int item_seq = static_cast<int>(m.item_seq);
-        const int qs = item_seq & 1;
-        if ((flags & kStageFirst) &&
-            !mbar_wait_warp(bar(C::kQFull + qs), static_cast<uint32_t>(item_seq >> 1) & 1))
-            return -1;
-        if (c >= 2 && !mbar_wait_warp(bar(C::kSFree + st), static_cast<uint32_t>((c >> 1) - 1) & 1))
-            return -1;
-        tc::fence_after_sync();
-        const uint32_t q = base + C::kQOff + qs * C::kOpBytes, k = stage_k(c);
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {  // 16 head dimensions per step
-            const uint64_t a = tc::smem_desc_sw128(q + (j / 4) * C::kHalf + (j % 4) * 32, 16, 1024);
-            const uint64_t b = tc::smem_desc_sw128(k + (j / 4) * 1024 + (j % 4) * 32, 16, 2048);
-            tc::mma_f16_warp(tmem + st * 128, a, b, C::kIdescS, j > 0);
-        }
-        tc::mma_commit_warp(bar(C::kSFull + st));
-        tc::mma_commit_warp(bar(C::kEmptyK + st));              // K_c is free once MMA1 completed
-        if (flags & kStageLast) tc::mma_commit_warp(bar(C::kQEmpty + qs));  // so is the Q slot
-        __syncwarp();
-        return 0;
-    };
-
-    int r = issue_mma1(0);
-    if (r < 0) fail();
-    for (int c = 0; r == 0; ++c) {
-        bool next_done = false;
-        {
-            const int c1 = c + 1, st1 = c1 & 1;
-            int early = 0;
-            if (lane == 0 && mbar_try_wait(bar(C::kFullK + st1), static_cast<uint32_t>(c1 >> 1) & 1) &&
-                !(meta[c1 & (C::kMetaSlots - 1)].flags & kStageEnd) &&
-                (c1 < 2 || mbar_try_wait(bar(C::kSFree + st1), static_cast<uint32_t>((c1 >> 1) - 1) & 1))) {
-                const PfStageMeta& m1 = meta[c1 & (C::kMetaSlots - 1)];
-                early = !(m1.flags & kStageFirst) ||
-                        mbar_try_wait(bar(C::kQFull + (m1.item_seq & 1)), (m1.item_seq >> 1) & 1);
+    int c1 = 0, c2 = 0;
+    bool end1 = false;     // MMA1 reached the end marker (at stage c1)
+    uint32_t firsts = 0;   // bit c % 32: stage c starts its item (its MMA2 overwrites O), c2 <= c < c1
+    unsigned long long idle0 = 0;
+    while (!(end1 && c2 == c1)) {
+        bool did = false;
+        if (!end1) {
+            const int st = c1 & 1;
+            // 0: not ready, 1: issue, 2: end marker; then the stage's flags and item
+            int ok = 0, flags = 0, item_seq = 0;
+            if (lane == 0 && mbar_test_wait(bar(C::kFullK + st), static_cast<uint32_t>(c1 >> 1) & 1)) {
+                const PfStageMeta& m = meta[c1 & (C::kMetaSlots - 1)];
+                flags = static_cast<int>(m.flags);
+                item_seq = static_cast<int>(m.item_seq);
+                if (flags & kStageEnd)
+                    ok = 2;
+                else if ((c1 < 2 || mbar_test_wait(bar(C::kSFree + st), static_cast<uint32_t>((c1 >> 1) - 1) & 1)) &&
+                         (!(flags & kStageFirst) ||
+                          mbar_test_wait(bar(C::kQFull + (item_seq & 1)), static_cast<uint32_t>(item_seq >> 1) & 1)))
+                    ok = 1;
             }
-            if (__shfl_sync(0xffffffffu, early, 0)) {
-                r = issue_mma1(c1);
-                next_done = true;
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (ok == 2) {
+                end1 = true;
+                did = true;
+            } else if (ok == 1) {
+                flags = __shfl_sync(0xffffffffu, flags, 0);
+                item_seq = __shfl_sync(0xffffffffu, item_seq, 0);
+                const int qs = item_seq & 1;
+                tc::fence_after_sync();
+                const uint32_t q = base + C::kQOff + qs * C::kOpBytes, k = stage_k(c1);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {  // 16 head dimensions per step
+                    const uint64_t a = tc::smem_desc_sw128(q + (j / 4) * C::kHalf + (j % 4) * 32, 16, 1024);
+                    const uint64_t b = tc::smem_desc_sw128(k + (j / 4) * 1024 + (j % 4) * 32, 16, 2048);
+                    tc::mma_f16_warp(tmem + st * 128, a, b, C::kIdescS, j > 0);
+                }
+                tc::mma_commit_warp(bar(C::kSFull + st));
+                tc::mma_commit_warp(bar(C::kEmptyK + st));  // K of c1 is free once MMA1 completed
+                if (flags & kStageLast) tc::mma_commit_warp(bar(C::kQEmpty + qs));  // so is the Q slot
+                __syncwarp();
+                const uint32_t bit = 1u << (c1 & 31);
+                firsts = (flags & kStageFirst) ? (firsts | bit) : (firsts & ~bit);
+                ++c1;
+                did = true;
             }
         }
-        if (r < 0) {
-            fail();
-            break;
-        }
-        if (!mbar_wait_warp(bar(C::kPFull), static_cast<uint32_t>(c) & 1)) {
-            fail();
-            break;
-        }
-        tc::fence_after_sync();
-        const bool first = (meta[c & (C::kMetaSlots - 1)].flags & kStageFirst) != 0;
-        const uint32_t pop = base + C::kPOff, v = stage_k(c) + C::kTileBytes;
+        if (c2 < c1) {
+            int ok = 0;
+            if (lane == 0)
+                ok = mbar_test_wait(bar(C::kPFull + (c2 & 1)), static_cast<uint32_t>(c2 >> 1) & 1) &&
+                     mbar_test_wait(bar(C::kFullV + (c2 & 1)), static_cast<uint32_t>(c2 >> 1) & 1);
+            if (__shfl_sync(0xffffffffu, ok, 0)) {
+                tc::fence_after_sync();
+                const bool first = ((firsts >> (c2 & 31)) & 1u) != 0;
+                const uint32_t pt = tmem + C::kPCol + 64u * (c2 & 1), v = stage_k(c2) + C::kTileBytes;
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {  // 16 tokens per step
-            const uint64_t a = tc::smem_desc_sw128(pop + (j / 4) * C::kHalf + (j % 4) * 32, 16, 1024);
-            const uint64_t b = tc::smem_desc_sw128(v + j * 4096, 1024, 2048);
-            tc::mma_f16_warp(tmem + C::kOCol, a, b, C::kIdescO, (j > 0 || !first) ? 1u : 0u);
+                for (int j = 0; j < 8; ++j) {  // 16 tokens (8 TMEM columns of P) per step
+                    const uint64_t b = tc::smem_desc_sw128(v + j * 4096, 1024, 2048);
+                    tc::mma_f16_tmem_a_warp(tmem + C::kOCol, pt + 8u * j, b, C::kIdescO,
+                                            (j > 0 || !first) ? 1u : 0u);
+                }
+                tc::mma_commit_warp(bar(C::kPFree + (c2 & 1)));  // P buffer c2 % 2 may be rewritten, O done
+                tc::mma_commit_warp(bar(C::kEmptyV + (c2 & 1)));  // V of c2 is free
+                __syncwarp();
+                ++c2;
+                did = true;
+            }
         }
-        tc::mma_commit_warp(bar(C::kPFree));             // P may be rewritten, O is complete
-        tc::mma_commit_warp(bar(C::kEmptyV + (c & 1)));  // V_c is free
-        __syncwarp();
-        if (!next_done) r = issue_mma1(c + 1);
-        if (r < 0) {
-            fail();
+        if (did) {
+            idle0 = 0;
+            continue;
+        }
+        const unsigned long long now = global_timer_ns();
+        if (idle0 == 0) {
+            idle0 = now;
+        } else if (now - idle0 > kWaitLimitNs) {
+            if (lane == 0) report(p.d_err, PA_DERR_TIMEOUT);
+            *abort_flag = 1;
             break;
         }
+        __nanosleep(32);
     }
     __syncwarp();
     tc::mma_commit_warp(bar(C::kDrain));
@@ -553,6 +590,17 @@ struct PfGroup {
     int tid;
     int k = 0;
     __device__ __forceinline__ void sync() const { named_barrier(1, 256); }
+    // sync() that also tells whether the predicate holds for any thread of the group
+    __device__ __forceinline__ bool any(bool v) const {
+        uint32_t r;
+        asm volatile(
+            "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.or.pred q, 1, 256, p;\n\t"
+            "selp.u32 %0, 1, 0, q;\n\t}"
+            : "=r"(r)
+            : "r"(v ? 1u : 0u)
+            : "memory");
+        return r != 0;
+    }
     __device__ __forceinline__ bool wait(uint32_t bar, uint32_t parity, uint32_t* d_err,
                                          volatile int* abort_flag) {
         const int slot = k++ & 1;
@@ -575,8 +623,8 @@ struct PfGroup {
 // stage: its half of the row of S from TMEM, the causal and validity mask,
 // the row maximum (the two halves exchange theirs through shared memory), the
 // running maximum (raised only past +8 in the log2 domain, then its half of O
-// and the row sum rescaled), P (rounded to T) into its 64-token half of the
-// swizzled P tile; at an item's last stage its half of the row of O divided by
+// and the row sum rescaled), P (rounded to T) into the 32 TMEM columns of its
+// 64-token half of P buffer c % 2; at an item's last stage its half of the row of O divided by
 // the row sum (or the partition's partial state).  The thread also zeroes its
 // half of V row `row` when token `row` holds no data, so 0 x garbage never
 // reaches O.
@@ -603,7 +651,9 @@ __device__ __forceinline__ void pf_softmax(const DecodeParams& p, unsigned char*
     int row0 = 0, hq0 = 0, part = 0, nparts = 0, ntok = 0;  // the current item
     for (int c = 0;; ++c) {
         const int st = c & 1;
-        if (!grp.wait(bar(C::kFullV + st), static_cast<uint32_t>(c >> 1) & 1, p.d_err, abort_flag)) break;
+        if (!grp.wait(bar(C::kMetaFull + (c & (C::kMetaSlots - 1))), static_cast<uint32_t>(c >> C::kMetaShift) & 1,
+                      p.d_err, abort_flag))
+            break;
         const PfStageMeta& m = meta[c & (C::kMetaSlots - 1)];
         const uint32_t flags = m.flags;
         if (flags & kStageEnd) break;
@@ -619,11 +669,16 @@ __device__ __forceinline__ void pf_softmax(const DecodeParams& p, unsigned char*
             m_ref = -INFINITY;
             l = 0.f;
         }
-        if (!(row < nvalid && ((groups >> (row >> 4)) & 1u))) {  // token `row` holds no data
-            unsigned char* vrow = sm + C::kRingOff + st * C::kStageBytes + C::kTileBytes +
-                                  (row >> 3) * 2048 + half * 1024 + (row & 7) * 128;
+        if (!(groups == 0xffu && nvalid >= C::kStageTok)) {
+            // some token of the stage holds no data: once the stage's V has
+            // landed, zero its rows (before P is published)
+            if (!grp.wait(bar(C::kFullV + st), static_cast<uint32_t>(c >> 1) & 1, p.d_err, abort_flag)) break;
+            if (!(row < nvalid && ((groups >> (row >> 4)) & 1u))) {  // token `row` holds no data
+                unsigned char* vrow = sm + C::kRingOff + st * C::kStageBytes + C::kTileBytes +
+                                      (row >> 3) * 2048 + half * 1024 + (row & 7) * 128;
 #pragma unroll
-            for (int k = 0; k < 8; ++k) *reinterpret_cast<uint4*>(vrow + k * 16) = make_uint4(0, 0, 0, 0);
+                for (int k = 0; k < 8; ++k) *reinterpret_cast<uint4*>(vrow + k * 16) = make_uint4(0, 0, 0, 0);
+            }
         }
 
         // ---- this half of the S row
@@ -662,48 +717,52 @@ __device__ __forceinline__ void pf_softmax(const DecodeParams& p, unsigned char*
             l *= alpha;
         }
 
-        // ---- P may be rewritten once MMA2 of the previous stage completed
-        if (c > 0 && !grp.wait(bar(C::kPFree), static_cast<uint32_t>(c - 1) & 1, p.d_err, abort_flag))
+        // ---- P buffer c % 2 may be rewritten once MMA2 of stage c-2 completed
+        if (c >= 2 && !grp.wait(bar(C::kPFree + (c & 1)), static_cast<uint32_t>((c >> 1) - 1) & 1, p.d_err,
+                                abort_flag))
             break;
-        tc::fence_after_sync();
-        if (!(flags & kStageFirst) && __any_sync(0xffffffffu, resc)) {  // rescale this warp's O
-            float ov[32];
+        // O may be rescaled once MMA2 of stage c-1 completed
+        if (!(flags & kStageFirst) && grp.any(resc)) {
+            if (!grp.wait(bar(C::kPFree + ((c - 1) & 1)), static_cast<uint32_t>((c - 1) >> 1) & 1, p.d_err,
+                          abort_flag))
+                break;
+            tc::fence_after_sync();
+            if (__any_sync(0xffffffffu, resc)) {  // rescale this warp's O
+                float ov[32];
 #pragma unroll
-            for (int k = 0; k < 2; ++k) {
-                const uint32_t ta = tmem + C::kOCol + col0 + 32 * k + lane_off;
-                pf::tmem_ld32(ta, ov);
+                for (int k = 0; k < 2; ++k) {
+                    const uint32_t ta = tmem + C::kOCol + col0 + 32 * k + lane_off;
+                    pf::tmem_ld32(ta, ov);
 #pragma unroll
-                for (int i = 0; i < 32; ++i) ov[i] *= alpha;
-                pf::tmem_st32(ta, ov);
+                    for (int i = 0; i < 32; ++i) ov[i] *= alpha;
+                    pf::tmem_st32(ta, ov);
+                }
             }
-            pf::tmem_wait_st();
         }
-        unsigned char* prow = sm + C::kPOff + half * C::kHalf + (row >> 3) * 1024 + (row & 7) * 128;
+        tc::fence_after_sync();
         const bool any_valid = m_ref != -INFINITY;
         float l4[4] = {0.f, 0.f, 0.f, 0.f};
+        float pw[32];  // this half of the row of P, 16-bit pairs (lower token in the low half)
 #pragma unroll
-        for (int ch = 0; ch < 8; ++ch) {  // 8 tokens per 16-byte chunk
-            uint32_t w[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int j = 8 * ch + 2 * i;
-                const float p0 = any_valid ? fast_exp2(x[j] - m_ref) : 0.f;  // masked: 2^-inf = 0
-                const float p1 = any_valid ? fast_exp2(x[j + 1] - m_ref) : 0.f;
-                w[i] = pf::pack2<T>(p0, p1);
-                const T* hp = reinterpret_cast<const T*>(&w[i]);
-                l4[i] += Elem<T>::to_float(hp[0]) + Elem<T>::to_float(hp[1]);
-            }
-            *reinterpret_cast<uint4*>(prow + (((ch & 7) ^ (row & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+        for (int i = 0; i < 32; ++i) {
+            const float p0 = any_valid ? fast_exp2(x[2 * i] - m_ref) : 0.f;  // masked: 2^-inf = 0
+            const float p1 = any_valid ? fast_exp2(x[2 * i + 1] - m_ref) : 0.f;
+            const uint32_t w = pf::pack2<T>(p0, p1);
+            const T* hp = reinterpret_cast<const T*>(&w);
+            l4[i & 3] += Elem<T>::to_float(hp[0]) + Elem<T>::to_float(hp[1]);
+            pw[i] = __uint_as_float(w);
         }
+        pf::tmem_st32(tmem + C::kPCol + 64u * (c & 1) + 32u * half + lane_off, pw);
         l += (l4[0] + l4[1]) + (l4[2] + l4[3]);
-        tc::fence_async_smem();
+        pf::tmem_wait_st();
+        tc::fence_async_smem();  // zeroed V rows, for the tensor core
         tc::fence_before_sync();
         grp.sync();
-        if (tid == 0) mbar_arrive(bar(C::kPFull));
+        if (tid == 0) mbar_arrive(bar(C::kPFull + (c & 1)));
         if (!(flags & kStageLast)) continue;
 
         // ---- item end: this half of the row of O, once MMA2 of this stage completed
-        if (!grp.wait(bar(C::kPFree), static_cast<uint32_t>(c) & 1, p.d_err, abort_flag)) break;
+        if (!grp.wait(bar(C::kPFree + (c & 1)), static_cast<uint32_t>(c >> 1) & 1, p.d_err, abort_flag)) break;
         tc::fence_after_sync();
         float o[64];
         pf::tmem_ld32(tmem + C::kOCol + col0 + lane_off, o);

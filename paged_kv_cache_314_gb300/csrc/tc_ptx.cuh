@@ -107,6 +107,18 @@ __device__ __forceinline__ void mma_f16_warp(uint32_t d_tmem, uint64_t a_desc, u
         : "memory");
 }
 
+// D[tmem] (+)= A[tmem] * B[smem]: A read from tensor memory (the lanes are
+// its M rows, 16-bit K pairs packed per 32-bit column); one elected lane of a
+// converged warp issues.
+__device__ __forceinline__ void mma_f16_tmem_a_warp(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                                    uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p, e;\n\tsetp.ne.b32 p, %4, 0;\n\telect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 __device__ __forceinline__ void mma_commit_warp(uint32_t bar) {
     asm volatile(
         "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
