@@ -690,12 +690,15 @@ __device__ __forceinline__ void pf_softmax(const DecodeParams& p, unsigned char*
         tc::fence_before_sync();
         mbar_arrive(bar(C::kSFree + st));  // every thread of the group (count 256)
         float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-        if (groups == 0xffu && lim >= 128) {  // every token valid for every row: no mask
+        // every token valid for every row: no mask, and the maximum is taken
+        // on the raw logits (scaled afterwards, kq > 0); the exponent below
+        // applies the scale.  Otherwise x is scaled and masked here.
+        const bool unmasked = groups == 0xffu && lim >= 128 && kq > 0.f;
+        if (unmasked) {
 #pragma unroll
-            for (int j = 0; j < 64; ++j) {
-                x[j] *= kq;
-                mx4[j & 3] = fmaxf(mx4[j & 3], x[j]);
-            }
+            for (int j = 0; j < 64; ++j) mx4[j & 3] = fmaxf(mx4[j & 3], x[j]);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) mx4[i] *= kq;
         } else {
 #pragma unroll
             for (int j = 0; j < 64; ++j) {
@@ -740,17 +743,19 @@ __device__ __forceinline__ void pf_softmax(const DecodeParams& p, unsigned char*
             }
         }
         tc::fence_after_sync();
-        const bool any_valid = m_ref != -INFINITY;
-        float l4[4] = {0.f, 0.f, 0.f, 0.f};
+        // exponent x * ks - m in one packed multiply-add per pair; a row with
+        // no valid token so far (m = -inf) has every x = -inf: 2^-inf = 0
+        const float ks = unmasked ? kq : 1.f;
+        const float negm = m_ref != -INFINITY ? -m_ref : 0.f;
+        float l4[4] = {0.f, 0.f, 0.f, 0.f};  // the row sum, of the weights before rounding
         float pw[32];  // this half of the row of P, 16-bit pairs (lower token in the low half)
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
-            const float p0 = any_valid ? fast_exp2(x[2 * i] - m_ref) : 0.f;  // masked: 2^-inf = 0
-            const float p1 = any_valid ? fast_exp2(x[2 * i + 1] - m_ref) : 0.f;
-            const uint32_t w = pf::pack2<T>(p0, p1);
-            const T* hp = reinterpret_cast<const T*>(&w);
-            l4[i & 3] += Elem<T>::to_float(hp[0]) + Elem<T>::to_float(hp[1]);
-            pw[i] = __uint_as_float(w);
+            float e0 = negm, e1 = negm;
+            fma2(e0, e1, x[2 * i], x[2 * i + 1], ks, ks);
+            const float p0 = fast_exp2(e0), p1 = fast_exp2(e1);
+            fma2(l4[2 * (i & 1)], l4[2 * (i & 1) + 1], p0, p1, 1.f, 1.f);
+            pw[i] = __uint_as_float(pf::pack2<T>(p0, p1));
         }
         pf::tmem_st32(tmem + C::kPCol + 64u * (c & 1) + 32u * half + lane_off, pw);
         l += (l4[0] + l4[1]) + (l4[2] + l4[3]);
