@@ -167,6 +167,13 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float* v) {
         : "memory");
 }
 
+// max(a, b, c) in one instruction (three-input max.f32, sm_100 family).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // Two floats rounded to T, packed (lower address first).
@@ -603,9 +610,33 @@ struct PfGroup {
     }
     __device__ __forceinline__ bool wait(uint32_t bar, uint32_t parity, uint32_t* d_err,
                                          volatile int* abort_flag) {
+        bool unused;
+        return wait_any(bar, parity, false, &unused, d_err, abort_flag);
+    }
+    // wait() whose barrier also ORs `pred` over the group into *any.
+    __device__ __forceinline__ bool wait_any(uint32_t bar, uint32_t parity, bool pred, bool* any,
+                                             uint32_t* d_err, volatile int* abort_flag) {
         const int slot = k++ & 1;
         if (tid == 0) {
             const bool ok = mbar_wait(bar, parity);
+            if (!ok) {
+                report(d_err, PA_DERR_TIMEOUT);
+                *abort_flag = 1;
+            }
+            flags[slot] = ok ? 1 : 0;
+        }
+        *any = this->any(pred);
+        return flags[slot] != 0;
+    }
+    // wait() for a stage's meta barrier and then, unless the meta it guards
+    // is the end marker, for its S: one group barrier for both.
+    __device__ __forceinline__ bool wait_stage(uint32_t bar, uint32_t parity, const uint32_t* meta_flags,
+                                               uint32_t bar2, uint32_t parity2, uint32_t* d_err,
+                                               volatile int* abort_flag) {
+        const int slot = k++ & 1;
+        if (tid == 0) {
+            bool ok = mbar_wait(bar, parity);
+            if (ok && !(*meta_flags & kStageEnd)) ok = mbar_wait(bar2, parity2);
             if (!ok) {
                 report(d_err, PA_DERR_TIMEOUT);
                 *abort_flag = 1;
@@ -651,10 +682,11 @@ __device__ __forceinline__ void pf_softmax(const DecodeParams& p, unsigned char*
     int row0 = 0, hq0 = 0, part = 0, nparts = 0, ntok = 0;  // the current item
     for (int c = 0;; ++c) {
         const int st = c & 1;
-        if (!grp.wait(bar(C::kMetaFull + (c & (C::kMetaSlots - 1))), static_cast<uint32_t>(c >> C::kMetaShift) & 1,
-                      p.d_err, abort_flag))
-            break;
         const PfStageMeta& m = meta[c & (C::kMetaSlots - 1)];
+        if (!grp.wait_stage(bar(C::kMetaFull + (c & (C::kMetaSlots - 1))),
+                            static_cast<uint32_t>(c >> C::kMetaShift) & 1, &m.flags, bar(C::kSFull + st),
+                            static_cast<uint32_t>(c >> 1) & 1, p.d_err, abort_flag))
+            break;
         const uint32_t flags = m.flags;
         if (flags & kStageEnd) break;
         const int nvalid = m.nvalid;
@@ -681,8 +713,7 @@ __device__ __forceinline__ void pf_softmax(const DecodeParams& p, unsigned char*
             }
         }
 
-        // ---- this half of the S row
-        if (!grp.wait(bar(C::kSFull + st), static_cast<uint32_t>(c >> 1) & 1, p.d_err, abort_flag)) break;
+        // ---- this half of the S row (S landed: waited for with the meta)
         tc::fence_after_sync();
         float x[64];
         pf::tmem_ld32(tmem + st * 128 + col0 + lane_off, x);
@@ -696,7 +727,7 @@ __device__ __forceinline__ void pf_softmax(const DecodeParams& p, unsigned char*
         const bool unmasked = groups == 0xffu && lim >= 128 && kq > 0.f;
         if (unmasked) {
 #pragma unroll
-            for (int j = 0; j < 64; ++j) mx4[j & 3] = fmaxf(mx4[j & 3], x[j]);
+            for (int j = 0; j < 64; j += 2) mx4[(j >> 1) & 3] = pf::fmax3(mx4[(j >> 1) & 3], x[j], x[j + 1]);
 #pragma unroll
             for (int i = 0; i < 4; ++i) mx4[i] *= kq;
         } else {
@@ -720,12 +751,18 @@ __device__ __forceinline__ void pf_softmax(const DecodeParams& p, unsigned char*
             l *= alpha;
         }
 
-        // ---- P buffer c % 2 may be rewritten once MMA2 of stage c-2 completed
-        if (c >= 2 && !grp.wait(bar(C::kPFree + (c & 1)), static_cast<uint32_t>((c >> 1) - 1) & 1, p.d_err,
-                                abort_flag))
-            break;
+        // ---- P buffer c % 2 may be rewritten once MMA2 of stage c-2 completed;
+        // the same group barrier tells whether any row raised its maximum
+        bool any_resc = false;
+        if (c >= 2) {
+            if (!grp.wait_any(bar(C::kPFree + (c & 1)), static_cast<uint32_t>((c >> 1) - 1) & 1, resc, &any_resc,
+                              p.d_err, abort_flag))
+                break;
+        } else {
+            any_resc = grp.any(resc);
+        }
         // O may be rescaled once MMA2 of stage c-1 completed
-        if (!(flags & kStageFirst) && grp.any(resc)) {
+        if (!(flags & kStageFirst) && any_resc) {
             if (!grp.wait(bar(C::kPFree + ((c - 1) & 1)), static_cast<uint32_t>((c - 1) >> 1) & 1, p.d_err,
                           abort_flag))
                 break;
