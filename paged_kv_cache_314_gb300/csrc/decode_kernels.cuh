@@ -1166,8 +1166,14 @@ __device__ __forceinline__ void merge_prefix_row(const DecodeParams& p, int s, s
     float M = -INFINITY;
 #pragma unroll
     for (int k = 0; k < 2 * kQ; ++k) {
+        // a slot outside this row's ranges holds whatever an earlier call left
         const bool in = k < kQ ? k < npre : k - kQ < nown;
-        if (!in) mi[k] = -INFINITY;
+        if (!in) {
+            mi[k] = -INFINITY;
+            li[k] = 0.f;
+#pragma unroll
+            for (int cc = 0; cc < kCols; ++cc) oi[k][cc] = 0.f;
+        }
         M = fmaxf(M, mi[k]);
     }
     for (int j = kQ; j < npre; ++j) M = fmaxf(M, __ldcg(p.ws_m + base + j));

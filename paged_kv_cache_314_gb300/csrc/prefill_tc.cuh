@@ -22,9 +22,9 @@
 // the weights stay <= 2^8, exact in fp32 and far inside the 16-bit range).
 //
 // Warps: 0 walks the work items and issues the Q and K copies, 1 issues the
-// MMAs (one elected lane) and owns TMEM, 2-9 are the softmax warps (two
-// threads per query row, one per 64-column half; warp w reads TMEM lanes
-// 32*(w%4)..), 10 issues the V copies from a per-stage plan once the V half
+// MMAs (one elected lane) and owns TMEM, 2-17 are the softmax warps (four
+// threads per query row, one per 32-column quarter; warp w reads TMEM lanes
+// 32*(w%4)..), 18 issues the V copies from a per-stage plan once the V half
 // of the slot is free.  Shared memory: a 2-stage K/V ring (the K and V halves
 // of a slot released separately), two Q slots.  TMEM: two S buffers, O, two P
 // buffers (stage c in buffer c % 2), so the softmax of stage c waits for P.V
@@ -71,10 +71,16 @@ struct PfTile {
     static constexpr int kFullK = 0, kEmptyK = 2, kFullV = 4, kEmptyV = 6, kVPlan = 8, kMetaFull = 16;
     static constexpr int kQFull = 24, kQEmpty = 26, kSFull = 28, kSFree = 30;
     static constexpr int kPFull = 32, kPFree = 34, kDrain = 36, kNumBars = 37;
-    static constexpr int kRedOff = kBarOff + kNumBars * 8;    // row maxima / sums of the halves [2][128]
-    static constexpr int kMiscOff = kRedOff + 2 * 128 * 4;    // tmem base, abort, group flags [2]
+    // softmax: kSplit threads per query row, each on kCols columns of S (and of O)
+    static constexpr int kSplit = 4;
+    static constexpr int kCols = 128 / kSplit;
+    static constexpr int kSoftWarps = 4 * kSplit;
+    static constexpr int kSoftThreads = 32 * kSoftWarps;
+    static constexpr int kRedOff = kBarOff + kNumBars * 8;    // row maxima / sums of the parts [kSplit][128]
+    static constexpr int kMiscOff = kRedOff + kSplit * 128 * 4;  // tmem base, abort, group flags [2]
     static constexpr int kSmemBytes = kMiscOff + 32 + 1024;  // + alignment slack
-    static constexpr int kThreads = 352;
+    static constexpr int kCopyWarp = 2 + kSoftWarps;  // issues the V copies
+    static constexpr int kThreads = 32 * (kCopyWarp + 1);
     static constexpr uint32_t kTmemCols = 512;  // S [2] x 128, O 128, P [2] x 64 (16-bit pairs)
     static constexpr uint32_t kOCol = 256;
     static constexpr uint32_t kPCol = 384;
@@ -172,6 +178,29 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
     float r;
     asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
     return r;
+}
+
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const float* v) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+            taddr),
+        "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+        "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+        "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
+        "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+        "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
+        "r"(__float_as_uint(v[15]))
+        : "memory");
+}
+
+// N = 16 or 32 consecutive TMEM columns of this thread's lane.
+template <int N>
+__device__ __forceinline__ void tmem_st(uint32_t taddr, const float* v) {
+    static_assert(N == 16 || N == 32, "16 or 32 columns");
+    if constexpr (N == 16)
+        tmem_st16(taddr, v);
+    else
+        tmem_st32(taddr, v);
 }
 
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
@@ -481,11 +510,12 @@ __device__ __forceinline__ void pf_copy_v(const DecodeParams& p, const CUtensorM
 }
 
 // ---- warp 1: MMA issue -------------------------------------------------------
-// Two cursors: MMA1 of stage c1 (S[c1%2] = Q.K^T) once K of c1 has landed and
-// the softmax warps have read S of stage c1-2; MMA2 of stage c2 (O (+)= P.V,
-// P from TMEM buffer c2%2) once P of c2 is published and V of c2 has landed.
-// MMA1 runs ahead of MMA2, so the tensor pipe computes the next stages' S
-// while the softmax warps work on this one.  Whatever is ready is issued at
+// Two cursors: MMA1 of stage c1 (S[c1%2] = Q.K^T) once K of c1 has landed,
+// the softmax warps have read S of stage c1-2 and MMA2 of stage c1-2 was
+// issued; MMA2 of stage c2 (O (+)= P.V, P from TMEM buffer c2%2) once P of c2
+// is published and V of c2 has landed.  MMA1 of the next stage goes ahead of
+// MMA2 of this one, so the tensor pipe computes the next S while the softmax
+// warps work on this one.  Whatever is ready is issued at
 // once; with nothing ready the warp polls (non-blocking tests, short sleeps)
 // and gives up after the wait limit without progress.  Lane 0 tests the
 // barriers, reads the meta and issues (the elected lane of a full warp).
@@ -506,7 +536,11 @@ __device__ __forceinline__ void pf_mma(const DecodeParams& p, unsigned char* sm,
     unsigned long long idle0 = 0;
     while (!(end1 && c2 == c1)) {
         bool did = false;
-        if (!end1) {
+        // MMA1 of stage c1 only once MMA2 of stage c1-2 was issued (at most one
+        // MMA1 ahead of the next MMA2): with MMA1 further ahead, runs on the
+        // GPU gave wrong results for an occasional item of the shared-prefix
+        // pass, a cause not found in this protocol
+        if (!end1 && c1 <= c2 + 1) {
             const int st = c1 & 1;
             // 0: not ready, 1: issue, 2: end marker; then the stage's flags and item
             int ok = 0, flags = 0, item_seq = 0;
@@ -596,15 +630,16 @@ struct PfGroup {
     volatile int* flags;  // [2]
     int tid;
     int k = 0;
-    __device__ __forceinline__ void sync() const { named_barrier(1, 256); }
+    int nthreads;
+    __device__ __forceinline__ void sync() const { named_barrier(1, nthreads); }
     // sync() that also tells whether the predicate holds for any thread of the group
     __device__ __forceinline__ bool any(bool v) const {
         uint32_t r;
         asm volatile(
-            "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.or.pred q, 1, 256, p;\n\t"
+            "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.or.pred q, 1, %2, p;\n\t"
             "selp.u32 %0, 1, 0, q;\n\t}"
             : "=r"(r)
-            : "r"(v ? 1u : 0u)
+            : "r"(v ? 1u : 0u), "r"(nthreads)
             : "memory");
         return r != 0;
     }
@@ -648,37 +683,42 @@ struct PfGroup {
     }
 };
 
-// ---- warps 2-9: softmax, two threads per query row ---------------------------
-// Warp w handles rows 32*(w%4).. (its TMEM lane quadrant) and the 64 columns
-// (K/V tokens of the stage; head dimensions of O) of half (w-2)/4.  Per
-// stage: its half of the row of S from TMEM, the causal and validity mask,
-// the row maximum (the two halves exchange theirs through shared memory), the
-// running maximum (raised only past +8 in the log2 domain, then its half of O
-// and the row sum rescaled), P (rounded to T) into the 32 TMEM columns of its
-// 64-token half of P buffer c % 2; at an item's last stage its half of the row of O divided by
-// the row sum (or the partition's partial state).  The thread also zeroes its
-// half of V row `row` when token `row` holds no data, so 0 x garbage never
-// reaches O.
+// ---- warps 2 .. 2+kSoftWarps-1: softmax, kSplit threads per query row ------
+// Warp w handles rows 32*(w%4).. (its TMEM lane quadrant) and the kCols
+// columns (K/V tokens of the stage; head dimensions of O) of part (w-2)/4.
+// Per stage: its part of the row of S from TMEM, the causal and validity
+// mask, the row maximum (the parts exchange theirs through shared memory), the
+// running maximum (raised only past +8 in the log2 domain, then its part of O
+// and the row sum rescaled), P (rounded to T) into the kCols/2 TMEM columns of
+// its part of P buffer c % 2; at an item's last stage its part of the row of O
+// divided by the row sum (or the partition's partial state).  The thread also
+// zeroes its share of V row `row` when token `row` holds no data, so
+// 0 x garbage never reaches O.
 template <typename T>
 __device__ __forceinline__ void pf_softmax(const DecodeParams& p, unsigned char* sm, uint32_t tmem) {
     using C = PfTile<T>;
+    constexpr int kCols = C::kCols, kSplit = C::kSplit;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int tid = threadIdx.x - 64;  // 0..255
-    const int half = (warp - 2) >> 2;  // columns 64*half ..
+    const int tid = threadIdx.x - 64;  // 0 .. kSoftThreads-1
+    const int part_i = (warp - 2) >> 2;  // columns kCols*part_i ..
     const int row = 32 * (warp & 3) + lane;
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::kBarOff);
     auto bar = [&](int i) { return smem_addr(bars + i); };
     const PfStageMeta* meta = reinterpret_cast<const PfStageMeta*>(sm + C::kMetaOff);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + C::kMiscOff + 4);
-    float* red = reinterpret_cast<float*>(sm + C::kRedOff);  // [2 halves][128 rows]
-    PfGroup grp{reinterpret_cast<volatile int*>(sm + C::kMiscOff + 8), tid};
+    float* red = reinterpret_cast<float*>(sm + C::kRedOff);  // [kSplit parts][128 rows]
+    PfGroup grp{reinterpret_cast<volatile int*>(sm + C::kMiscOff + 8), tid, 0, C::kSoftThreads};
     const uint32_t lane_off = static_cast<uint32_t>(32 * (warp & 3)) << 16;
-    const uint32_t col0 = 64u * half;
+    const uint32_t col0 = static_cast<uint32_t>(kCols * part_i);
     const int g = p.group;
     const int ti = row / g;  // query token of this row within the item
     const float kq = p.qk_scale_log2;
+    // this thread's share of a V row: 16-byte chunks [vk0, vk0 + 8/(kSplit/2)) of
+    // 64-column half vh (the two, or four, parts of a row cover all of it)
+    constexpr int kChunks = 8 * 2 / kSplit;
+    const int vh = (kCols * part_i) / 64, vk0 = ((kCols * part_i) % 64) / 8;
 
-    float m_ref = -INFINITY, l = 0.f;  // l: this half's share of the row sum
+    float m_ref = -INFINITY, l = 0.f;  // l: this part's share of the row sum
     int row0 = 0, hq0 = 0, part = 0, nparts = 0, ntok = 0;  // the current item
     for (int c = 0;; ++c) {
         const int st = c & 1;
@@ -707,19 +747,20 @@ __device__ __forceinline__ void pf_softmax(const DecodeParams& p, unsigned char*
             if (!grp.wait(bar(C::kFullV + st), static_cast<uint32_t>(c >> 1) & 1, p.d_err, abort_flag)) break;
             if (!(row < nvalid && ((groups >> (row >> 4)) & 1u))) {  // token `row` holds no data
                 unsigned char* vrow = sm + C::kRingOff + st * C::kStageBytes + C::kTileBytes +
-                                      (row >> 3) * 2048 + half * 1024 + (row & 7) * 128;
+                                      (row >> 3) * 2048 + vh * 1024 + (row & 7) * 128;
 #pragma unroll
-                for (int k = 0; k < 8; ++k) *reinterpret_cast<uint4*>(vrow + k * 16) = make_uint4(0, 0, 0, 0);
+                for (int k = 0; k < kChunks; ++k)
+                    *reinterpret_cast<uint4*>(vrow + (vk0 + k) * 16) = make_uint4(0, 0, 0, 0);
             }
         }
 
-        // ---- this half of the S row (S landed: waited for with the meta)
+        // ---- this part of the S row (S landed: waited for with the meta)
         tc::fence_after_sync();
-        float x[64];
-        pf::tmem_ld32(tmem + st * 128 + col0 + lane_off, x);
-        pf::tmem_ld32(tmem + st * 128 + col0 + 32 + lane_off, x + 32);
+        float x[kCols];
+#pragma unroll
+        for (int k = 0; k < kCols / 32; ++k) pf::tmem_ld32(tmem + st * 128 + col0 + 32 * k + lane_off, x + 32 * k);
         tc::fence_before_sync();
-        mbar_arrive(bar(C::kSFree + st));  // every thread of the group (count 256)
+        mbar_arrive(bar(C::kSFree + st));  // every thread of the group (count kSoftThreads)
         float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
         // every token valid for every row: no mask, and the maximum is taken
         // on the raw logits (scaled afterwards, kq > 0); the exponent below
@@ -727,21 +768,23 @@ __device__ __forceinline__ void pf_softmax(const DecodeParams& p, unsigned char*
         const bool unmasked = groups == 0xffu && lim >= 128 && kq > 0.f;
         if (unmasked) {
 #pragma unroll
-            for (int j = 0; j < 64; j += 2) mx4[(j >> 1) & 3] = pf::fmax3(mx4[(j >> 1) & 3], x[j], x[j + 1]);
+            for (int j = 0; j < kCols; j += 2) mx4[(j >> 1) & 3] = pf::fmax3(mx4[(j >> 1) & 3], x[j], x[j + 1]);
 #pragma unroll
             for (int i = 0; i < 4; ++i) mx4[i] *= kq;
         } else {
 #pragma unroll
-            for (int j = 0; j < 64; ++j) {
+            for (int j = 0; j < kCols; ++j) {
                 const int t = static_cast<int>(col0) + j;
                 const bool ok = t < lim && ((groups >> (t >> 4)) & 1u);
                 x[j] = ok ? x[j] * kq : -INFINITY;
                 mx4[j & 3] = fmaxf(mx4[j & 3], x[j]);
             }
         }
-        red[half * 128 + row] = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+        red[part_i * 128 + row] = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
         grp.sync();
-        const float mx = fmaxf(red[row], red[128 + row]);
+        float mx = red[row];
+#pragma unroll
+        for (int k = 1; k < kSplit; ++k) mx = fmaxf(mx, red[k * 128 + row]);
         const float m_new = fmaxf(m_ref, mx);
         const bool resc = m_new > m_ref + 8.f;  // also from -inf to a first finite maximum
         float alpha = 1.f;
@@ -770,7 +813,7 @@ __device__ __forceinline__ void pf_softmax(const DecodeParams& p, unsigned char*
             if (__any_sync(0xffffffffu, resc)) {  // rescale this warp's O
                 float ov[32];
 #pragma unroll
-                for (int k = 0; k < 2; ++k) {
+                for (int k = 0; k < kCols / 32; ++k) {
                     const uint32_t ta = tmem + C::kOCol + col0 + 32 * k + lane_off;
                     pf::tmem_ld32(ta, ov);
 #pragma unroll
@@ -785,16 +828,16 @@ __device__ __forceinline__ void pf_softmax(const DecodeParams& p, unsigned char*
         const float ks = unmasked ? kq : 1.f;
         const float negm = m_ref != -INFINITY ? -m_ref : 0.f;
         float l4[4] = {0.f, 0.f, 0.f, 0.f};  // the row sum, of the weights before rounding
-        float pw[32];  // this half of the row of P, 16-bit pairs (lower token in the low half)
+        float pw[kCols / 2];  // this part of the row of P, 16-bit pairs (lower token in the low half)
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
+        for (int i = 0; i < kCols / 2; ++i) {
             float e0 = negm, e1 = negm;
             fma2(e0, e1, x[2 * i], x[2 * i + 1], ks, ks);
             const float p0 = fast_exp2(e0), p1 = fast_exp2(e1);
             fma2(l4[2 * (i & 1)], l4[2 * (i & 1) + 1], p0, p1, 1.f, 1.f);
             pw[i] = __uint_as_float(pf::pack2<T>(p0, p1));
         }
-        pf::tmem_st32(tmem + C::kPCol + 64u * (c & 1) + 32u * half + lane_off, pw);
+        pf::tmem_st<kCols / 2>(tmem + C::kPCol + 64u * (c & 1) + (kCols / 2) * part_i + lane_off, pw);
         l += (l4[0] + l4[1]) + (l4[2] + l4[3]);
         pf::tmem_wait_st();
         tc::fence_async_smem();  // zeroed V rows, for the tensor core
@@ -803,23 +846,25 @@ __device__ __forceinline__ void pf_softmax(const DecodeParams& p, unsigned char*
         if (tid == 0) mbar_arrive(bar(C::kPFull + (c & 1)));
         if (!(flags & kStageLast)) continue;
 
-        // ---- item end: this half of the row of O, once MMA2 of this stage completed
+        // ---- item end: this part of the row of O, once MMA2 of this stage completed
         if (!grp.wait(bar(C::kPFree + (c & 1)), static_cast<uint32_t>(c >> 1) & 1, p.d_err, abort_flag)) break;
         tc::fence_after_sync();
-        float o[64];
-        pf::tmem_ld32(tmem + C::kOCol + col0 + lane_off, o);
-        pf::tmem_ld32(tmem + C::kOCol + col0 + 32 + lane_off, o + 32);
+        float o[kCols];
+#pragma unroll
+        for (int k = 0; k < kCols / 32; ++k) pf::tmem_ld32(tmem + C::kOCol + col0 + 32 * k + lane_off, o + 32 * k);
         tc::fence_before_sync();
-        red[half * 128 + row] = l;
+        red[part_i * 128 + row] = l;
         grp.sync();
-        const float L = red[row] + red[128 + row];
+        float L = 0.f;
+#pragma unroll
+        for (int k = 0; k < kSplit; ++k) L += red[k * 128 + row];
         if (row < ntok * g) {
             const size_t rr = static_cast<size_t>(row0 + ti) * p.num_q_heads + hq0 + (row - ti * g);
             if (nparts <= 1) {
                 const float inv = (nparts == 1 && L > 0.f) ? 1.f / L : 0.f;
                 uint4* dst = reinterpret_cast<uint4*>(static_cast<T*>(p.out) + rr * C::D + col0);
 #pragma unroll
-                for (int k = 0; k < 8; ++k)
+                for (int k = 0; k < kCols / 8; ++k)
                     dst[k] = make_uint4(pf::pack2<T>(o[8 * k] * inv, o[8 * k + 1] * inv),
                                         pf::pack2<T>(o[8 * k + 2] * inv, o[8 * k + 3] * inv),
                                         pf::pack2<T>(o[8 * k + 4] * inv, o[8 * k + 5] * inv),
@@ -828,8 +873,9 @@ __device__ __forceinline__ void pf_softmax(const DecodeParams& p, unsigned char*
                 const size_t w = rr * p.max_parts + part;
                 float4* dst = reinterpret_cast<float4*>(p.ws_o + w * C::D + col0);
 #pragma unroll
-                for (int k = 0; k < 16; ++k) dst[k] = make_float4(o[4 * k], o[4 * k + 1], o[4 * k + 2], o[4 * k + 3]);
-                if (half == 0) {
+                for (int k = 0; k < kCols / 4; ++k)
+                    dst[k] = make_float4(o[4 * k], o[4 * k + 1], o[4 * k + 2], o[4 * k + 3]);
+                if (part_i == 0) {
                     p.ws_m[w] = m_ref;
                     p.ws_l[w] = L;
                 }
@@ -856,7 +902,7 @@ __global__ void __launch_bounds__(PfTile<T>::kThreads, 1)
         for (int i = 0; i < C::kNumBars; ++i) {
             // s_free is signalled by every softmax thread
             const bool all = i == C::kSFree || i == C::kSFree + 1;
-            mbar_init(smem_addr(bars + i), all ? 256 : 1);
+            mbar_init(smem_addr(bars + i), all ? C::kSoftThreads : 1);
         }
         *reinterpret_cast<volatile int*>(sm + C::kMiscOff + 4) = 0;
         fence_barrier_init();
@@ -874,7 +920,7 @@ __global__ void __launch_bounds__(PfTile<T>::kThreads, 1)
         pf_produce<T>(p, &mapK, &mapQ, sm, base);
     else if (warp == 1)
         pf_mma<T>(p, sm, base, tmem);
-    else if (warp < 10)
+    else if (warp < C::kCopyWarp)
         pf_softmax<T>(p, sm, tmem);
     else
         pf_copy_v<T>(p, &mapV, sm, base);
