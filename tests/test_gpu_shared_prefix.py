@@ -159,3 +159,36 @@ def test_step_through_host_buffers_with_shared_prefixes():
     assert same_bits(to_numpy(d["k_cache"], w.dtype), kc)
     assert same_bits(to_numpy(d["v_cache"], w.dtype), vc)
     assert_close(out_f64(host_out), ref, w.dtype, "shared-prefix step_host")
+
+
+def test_full_size_repeated_calls_and_stale_workspace():
+    """The 256-sequence shared-prefix workload called twelve times on the same
+    inputs, each time through a workspace whose partial-state area holds NaN
+    bytes from before: every call matches the oracle (a state slot the merge
+    reads must have been written by this call, one it does not need must not
+    leak into the result), and all calls agree bit for bit."""
+    w = wl.by_name("gqa_share")
+    G = w.meta["samples"]
+    d = upload(w)
+    pa.copy_blocks(d["k_cache"], d["v_cache"], d["block_mapping"], d_err=d["d_err"])
+    pa.kv_write(d["k_new"], d["v_new"], d["k_cache"], d["v_cache"], d["slot_mapping"],
+                d_err=d["d_err"])
+    pre = torch.full((w.num_seqs // G,), int(w.meta["shared_prefix_tokens"]), dtype=torch.int32,
+                     device="cuda")
+    ws = torch.zeros(pa.decode_shared_prefix_workspace_size(
+        w.num_seqs, w.num_q_heads, w.num_kv_heads, w.head_dim, w.max_blocks_per_seq,
+        w.block_size, w.dtype, 0, G), dtype=torch.uint8, device="cuda")
+    _, _, ref, err = oracle_step(w)
+    first = None
+    for _ in range(12):
+        ws[256:].fill_(0xFF)  # the 256-byte counter header stays zero
+        out = torch.full_like(d["q"], float("nan"))
+        pa.decode_shared_prefix(out, d["q"], d["k_cache"], d["v_cache"], d["block_tables"],
+                                d["context_lens"], w.scale, G, pre, workspace=ws, d_err=d["d_err"])
+        torch.cuda.synchronize()
+        assert int(d["d_err"].item()) == err == 0
+        assert_close(out_f64(out), ref, w.dtype, "repeated shared-prefix call")
+        if first is None:
+            first = out.clone()
+        else:
+            assert torch.equal(out, first)
