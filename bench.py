@@ -381,11 +381,11 @@ def _measure(args, name, layout, dev, dist, ws_world):
     plan = _plan(pa, w)
     # parallel sampling: the groups' shared prefix blocks are read once per group
     G = int(w.meta.get("samples", 1))
-    shared = (not mq and not fp8 and not args.no_shared_prefix and G > 1 and
+    shared = (not mq and not args.no_shared_prefix and G > 1 and
               int(w.meta.get("shared_prefix_tokens", 0)) > 0)
     if shared:
-        plan = dict(plan, kernel="tc_128_rows prefix pass + " + plan["kernel"] + " own pass",
-                    merge="kernel", launches=3)
+        plan = dict(plan, kernel=("prefix widening + " if fp8 else "") + "tc_128_rows prefix pass + " +
+                    plan["kernel"] + " own pass", merge="kernel", launches=4 if fp8 else 3)
     dt = w.dtype
     pool = (lambda a: torch.from_numpy(a)) if fp8 else (lambda a: _to_torch(a, dt))
     d = {k: v.to(dev) for k, v in {
@@ -402,7 +402,8 @@ def _measure(args, name, layout, dev, dist, ws_world):
                                       dtype=torch.int32)} if shared else {})}.items()}
     out = torch.empty_like(d["q"])
     if shared:
-        ws_bytes = pa.decode_shared_prefix_workspace_size(
+        ws_bytes = (pa.decode_shared_prefix_fp8_workspace_size if fp8 else
+                    pa.decode_shared_prefix_workspace_size)(
             w.num_seqs, w.num_q_heads, w.num_kv_heads, w.head_dim, w.max_blocks_per_seq,
             w.block_size, w.dtype, w.partition_tokens, G)
     elif mq:
@@ -435,7 +436,13 @@ def _measure(args, name, layout, dev, dist, ws_world):
                         dd["slot_mapping"], d_err=d_err)
         if ev is not None:
             ev[2].record(stream)
-        if fp8:
+        if fp8 and shared:
+            pa.decode_shared_prefix_fp8(out, dd["q"], dd["k_cache"], dd["v_cache"],
+                                        dd["k_scale"], dd["v_scale"], dd["block_tables"],
+                                        dd["context_lens"], w.scale, G, dd["prefix_lens"],
+                                        partition_tokens=w.partition_tokens, workspace=workspace,
+                                        d_err=d_err)
+        elif fp8:
             pa.decode_fp8(out, dd["q"], dd["k_cache"], dd["v_cache"], dd["k_scale"],
                           dd["v_scale"], dd["block_tables"], dd["context_lens"], w.scale,
                           partition_tokens=w.partition_tokens, workspace=workspace, d_err=d_err)
@@ -564,7 +571,9 @@ def _measure(args, name, layout, dev, dist, ws_world):
     ncu = _ncu_record(name + ("" if layout == "paged" else "_" + layout))
     # DRAM bytes of one attention call (every kernel of it), from the capture
     traffic = (ncu.get("call_traffic_bytes") or ncu.get("traffic_bytes_per_launch")) if ncu else None
-    kernel = f"{'pa_multi_query' if mq else 'pa_decode_fp8' if fp8 else 'pa_decode_shared_prefix' if shared else 'pa_decode'}: " \
+    call = ("pa_multi_query" if mq else "pa_decode_shared_prefix_fp8" if fp8 and shared else
+            "pa_decode_fp8" if fp8 else "pa_decode_shared_prefix" if shared else "pa_decode")
+    kernel = f"{call}: " \
              f"{plan['kernel']} kernel, merge {plan['merge']}, {plan['launches']} launch(es)"
     hbm_ach = unique_bytes / (dec_ms * 1e-3) / 1e9
     common = {"kernel": kernel, "avg_launch_ms": round(dec_ms, 5), "traffic": traffic,

@@ -391,6 +391,40 @@ pa_status pa_decode_fp8(void* out, const void* q, pa_dtype q_dtype, const void* 
                         float scale, int partition_tokens, void* workspace,
                         size_t workspace_bytes, uint32_t* d_err, pa_stream_t stream);
 
+/* pa_decode_shared_prefix_fp8 -- pa_decode_fp8 for groups of sequences that
+ * share prefix blocks ("PagedAttention" (compassingai.com) §6; the wmrh.cn
+ * tutorial's part on sharing KV blocks), as pa_decode_shared_prefix does for
+ * 16-bit caches: group_size, prefix_lens and the rule for a usable prefix are
+ * the same.  Each usable prefix is first widened once into the workspace, each
+ * element code x scale rounded once to q_dtype (so a prefix token's K and V
+ * carry one rounding to q's type that pa_decode_fp8 does not make); the 128-row
+ * tensor-core kernel then reads it once per group and kv head, the E4M3
+ * grouped kernel reads each sequence's own tokens, and the partial states are
+ * merged.  Shapes the shared pass does not cover (not 4-16 query heads per kv
+ * head, group_size * heads per kv head over 128, a group of one) run
+ * pa_decode_fp8 itself.  Workspace: pa_decode_shared_prefix_fp8_workspace_size()
+ * bytes (the partial states, two scratch pools of num_seqs / group_size x
+ * max_blocks_per_seq blocks in q_dtype and a [num_seqs][max_blocks_per_seq]
+ * int32 table), 256-byte aligned, its first 256 bytes zero before the first
+ * call and left zero.  Kernels: 4 (widen, prefix pass, own pass, merge).
+ */
+size_t pa_decode_shared_prefix_fp8_workspace_size(int num_seqs, int num_q_heads,
+                                                  int num_kv_heads, int head_dim,
+                                                  int max_blocks_per_seq, int block_size,
+                                                  pa_dtype q_dtype, int partition_tokens,
+                                                  int group_size);
+pa_status pa_decode_shared_prefix_fp8(void* out, const void* q, pa_dtype q_dtype,
+                                      const void* k_cache, const void* v_cache,
+                                      const float* k_scale, const float* v_scale,
+                                      const int32_t* block_tables, int max_blocks_per_seq,
+                                      const int32_t* context_lens, int num_seqs,
+                                      int num_q_heads, int num_kv_heads, int head_dim,
+                                      int block_size, int num_blocks, float scale,
+                                      int group_size, const int32_t* prefix_lens,
+                                      int partition_tokens, void* workspace,
+                                      size_t workspace_bytes, uint32_t* d_err,
+                                      pa_stream_t stream);
+
 /* pa_attention_plan -- which kernels a pa_decode, pa_decode_fp8 or
  * pa_multi_query call with these sizes would enqueue, without enqueuing
  * anything (no device memory is touched; the checks are the calls' own host
@@ -448,8 +482,9 @@ pa_status pa_attention_plan(int num_seqs, int num_query_tokens, int multi_query,
  * caller synchronises the stream before reading host_out or reusing host_in.
  * E4M3 caches: pass k_scale / v_scale (device, [num_blocks][num_kv_heads]);
  * the step then uses the *_fp8 calls (decode only, dtype F16 or BF16).
- * prefix_group > 0 (decode over 16-bit caches): attention is
- * pa_decode_shared_prefix with groups of prefix_group sequences.
+ * prefix_group > 0 (decode): attention is pa_decode_shared_prefix (16-bit
+ * caches) or pa_decode_shared_prefix_fp8 (E4M3 caches) with groups of
+ * prefix_group sequences.
  * Semantics, errors and the workspace: those of the calls it makes; every
  * host check runs before anything is enqueued.
  */

@@ -34,6 +34,7 @@ EXPORTED = ("pa_abi_version", "pa_status_string", "pa_kv_write", "pa_copy_blocks
             "pa_copy_blocks_fp8", "pa_swap_blocks_fp8", "pa_decode_fp8",
             "pa_attention_plan", "pa_step_layout", "pa_step_host",
             "pa_decode_shared_prefix_workspace_size", "pa_decode_shared_prefix",
+            "pa_decode_shared_prefix_fp8_workspace_size", "pa_decode_shared_prefix_fp8",
             "pa_selftest_wait_timeout")
 STEP_INPUTS = ("q", "k_new", "v_new", "slot_mapping", "block_tables", "context_lens",
                "block_mapping", "query_start", "prefix_lens")
@@ -132,6 +133,12 @@ def load() -> ctypes.CDLL:
         lib.pa_decode_shared_prefix.argtypes = [vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32,
                                                 i32, i32, ctypes.c_float, i32, vp, i32, i32, vp,
                                                 u64, vp, vp]
+        lib.pa_decode_shared_prefix_fp8_workspace_size.restype = u64
+        lib.pa_decode_shared_prefix_fp8_workspace_size.argtypes = [i32] * 9
+        lib.pa_decode_shared_prefix_fp8.restype = i32
+        lib.pa_decode_shared_prefix_fp8.argtypes = [vp, vp, i32, vp, vp, vp, vp, vp, i32, vp, i32,
+                                                    i32, i32, i32, i32, i32, ctypes.c_float, i32,
+                                                    vp, i32, vp, u64, vp, vp]
         lib.pa_attention_plan.restype = i32
         lib.pa_attention_plan.argtypes = [i32, i32, i32, i32, i32, i32, i32, i32, i32, i32, i32,
                                           i32, ctypes.POINTER(_Plan)]
@@ -501,6 +508,50 @@ def decode_fp8(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor, v_cach
                               int(partition_tokens), _ptr(workspace), ws_bytes, _ptr(d_err),
                               _stream(stream, q.device))
     _check(st, "pa_decode_fp8")
+    return out
+
+
+def decode_shared_prefix_fp8_workspace_size(num_seqs: int, num_q_heads: int, num_kv_heads: int,
+                                            head_dim: int, max_blocks_per_seq: int,
+                                            block_size: int, q_dtype, partition_tokens: int = 0,
+                                            group_size: int = 1) -> int:
+    return int(load().pa_decode_shared_prefix_fp8_workspace_size(
+        num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq, block_size,
+        _dtype_code(q_dtype), partition_tokens, group_size))
+
+
+def decode_shared_prefix_fp8(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor,
+                             v_cache: torch.Tensor, k_scale: torch.Tensor, v_scale: torch.Tensor,
+                             block_tables: torch.Tensor, context_lens: torch.Tensor, scale: float,
+                             group_size: int, prefix_lens: torch.Tensor, partition_tokens: int = 0,
+                             workspace: Optional[torch.Tensor] = None,
+                             d_err: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """pa_decode_fp8 for groups of group_size consecutive sequences whose first
+    prefix_lens[group] tokens are the same physical blocks (widened once to
+    q's type, then read once per group)."""
+    for n, t in (("out", out), ("q", q), ("k_cache", k_cache), ("v_cache", v_cache),
+                 ("k_scale", k_scale), ("v_scale", v_scale), ("block_tables", block_tables),
+                 ("context_lens", context_lens), ("prefix_lens", prefix_lens)):
+        _cuda_contig(n, t)
+    _fp8_pool("k_cache", k_cache)
+    _fp8_pool("v_cache", v_cache)
+    if prefix_lens.dtype != torch.int32:
+        raise ValueError("prefix_lens must be int32")
+    S, Hq, d = q.shape
+    NB, Hkv, B, d2 = k_cache.shape
+    if d2 != d or out.shape != q.shape or out.dtype != q.dtype:
+        raise ValueError("q, out and the cache must agree in head_dim; out has q's dtype")
+    MB = block_tables.shape[1]
+    if workspace is None:
+        workspace = torch.zeros(decode_shared_prefix_fp8_workspace_size(
+            S, Hq, Hkv, d, MB, B, q.dtype, partition_tokens, group_size),
+            dtype=torch.uint8, device=q.device)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    _check(load().pa_decode_shared_prefix_fp8(
+        _ptr(out), _ptr(q), DTYPE_CODE[q.dtype], _ptr(k_cache), _ptr(v_cache), _ptr(k_scale),
+        _ptr(v_scale), _ptr(block_tables), MB, _ptr(context_lens), S, Hq, Hkv, d, B, NB,
+        float(scale), int(group_size), _ptr(prefix_lens), int(partition_tokens), _ptr(workspace),
+        ws_bytes, _ptr(d_err), _stream(stream, q.device)), "pa_decode_shared_prefix_fp8")
     return out
 
 

@@ -811,3 +811,177 @@ extern "C" pa_status pa_decode_shared_prefix(
     return dtype == PA_BF16 ? launch_merge<__nv_bfloat16, 128>(p, st)
                             : launch_merge<__half, 128>(p, st);
 }
+
+namespace pa {
+pa_status launch_prefix_widen(const DecodeParams& p, pa_dtype q_dtype, void* k_out, void* v_out,
+                              int32_t* table_out, cudaStream_t stream);
+namespace {
+
+// Shared-prefix decode over E4M3 caches: the workspace holds the partial
+// states, then the groups' prefix blocks widened to q's type (K, then V:
+// groups x max_blocks_per_seq blocks each, laid out like the cache), then the
+// scratch block table [num_seqs][max_blocks_per_seq].
+struct PrefixFp8Layout {
+    PrefixPlan pl;
+    size_t k_off, v_off, table_off, bytes;
+};
+
+PrefixFp8Layout prefix_fp8_layout(int num_seqs, int num_q_heads, int num_kv_heads,
+                                  int max_blocks_per_seq, int block_size, int group_size, int P) {
+    PrefixFp8Layout r;
+    r.pl = prefix_plan(num_seqs, num_q_heads, num_kv_heads, 128, max_blocks_per_seq, block_size,
+                       group_size, P);
+    const size_t blocks = static_cast<size_t>(num_seqs / group_size) * max_blocks_per_seq;
+    const size_t pool = blocks * num_kv_heads * block_size * 128 * 2;
+    r.k_off = round_up(r.pl.ws.bytes, 256);
+    r.v_off = round_up(r.k_off + pool, 256);
+    r.table_off = round_up(r.v_off + pool, 256);
+    r.bytes = r.table_off + static_cast<size_t>(num_seqs) * max_blocks_per_seq * 4;
+    return r;
+}
+
+// The shared pass applies: grouped heads on the tensor cores (the E4M3 own
+// pass, the 16-bit prefix pass) and a scratch pool the TMA can address.
+bool prefix_fp8_shape(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                      int max_blocks_per_seq, int block_size, int num_blocks, pa_dtype q_dtype,
+                      int group_size, int P) {
+    if (!tc_shape(num_q_heads, num_kv_heads, head_dim, PA_E4M3)) return false;
+    if (group_size < 2 || num_seqs % group_size != 0) return false;
+    const long long scratch_rows = static_cast<long long>(num_seqs / group_size) * max_blocks_per_seq *
+                                   num_kv_heads * block_size;
+    return prefix_shape(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, q_dtype,
+                        group_size, P) &&
+           scratch_rows < 0x7fffffffLL;
+}
+
+}  // namespace
+}  // namespace pa
+
+extern "C" size_t pa_decode_shared_prefix_fp8_workspace_size(int num_seqs, int num_q_heads,
+                                                             int num_kv_heads, int head_dim,
+                                                             int max_blocks_per_seq, int block_size,
+                                                             pa_dtype q_dtype, int partition_tokens,
+                                                             int group_size) {
+    using namespace pa;
+    const size_t plain = pa_decode_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim,
+                                                  max_blocks_per_seq, block_size, PA_E4M3,
+                                                  partition_tokens);
+    if (plain == 0 || (q_dtype != PA_F16 && q_dtype != PA_BF16)) return 0;
+    const int P = pa_decode_partition_tokens(num_q_heads, num_kv_heads, head_dim,
+                                             max_blocks_per_seq, block_size, PA_E4M3, partition_tokens);
+    if (!prefix_fp8_shape(num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq,
+                          block_size, 1, q_dtype, group_size, P))
+        return plain;
+    const PrefixFp8Layout L = prefix_fp8_layout(num_seqs, num_q_heads, num_kv_heads,
+                                                max_blocks_per_seq, block_size, group_size, P);
+    return std::max(plain, L.bytes);
+}
+
+extern "C" pa_status pa_decode_shared_prefix_fp8(
+    void* out, const void* q, pa_dtype q_dtype, const void* k_cache, const void* v_cache,
+    const float* k_scale, const float* v_scale, const int32_t* block_tables, int max_blocks_per_seq,
+    const int32_t* context_lens, int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+    int block_size, int num_blocks, float scale, int group_size, const int32_t* prefix_lens,
+    int partition_tokens, void* workspace, size_t workspace_bytes, uint32_t* d_err,
+    pa_stream_t stream) {
+    using namespace pa;
+    if (q_dtype != PA_F16 && q_dtype != PA_BF16) return PA_ERR_UNSUPPORTED;
+    const pa_status c = check_attention(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq,
+                                        context_lens, num_seqs, num_q_heads, num_kv_heads,
+                                        head_dim, block_size, num_blocks, scale, partition_tokens,
+                                        q_dtype);
+    if (c != PA_OK) return c;
+    if (head_dim != 128) return PA_ERR_UNSUPPORTED;
+    if (group_size <= 0) return PA_ERR_INVALID_ARG;
+    if (num_seqs == 0) return PA_OK;
+    if (k_scale == nullptr || v_scale == nullptr) return PA_ERR_INVALID_ARG;
+    if (num_seqs % group_size != 0 || prefix_lens == nullptr) return PA_ERR_INVALID_ARG;
+    const int P = pa_decode_partition_tokens(num_q_heads, num_kv_heads, head_dim,
+                                             max_blocks_per_seq, block_size, PA_E4M3, partition_tokens);
+    if (P <= 0) return PA_ERR_INVALID_ARG;
+    if (!prefix_fp8_shape(num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq,
+                          block_size, num_blocks, q_dtype, group_size, P))  // plain E4M3 decode
+        return pa_decode_fp8(out, q, q_dtype, k_cache, v_cache, k_scale, v_scale, block_tables,
+                             max_blocks_per_seq, context_lens, num_seqs, num_q_heads, num_kv_heads,
+                             head_dim, block_size, num_blocks, scale, partition_tokens, workspace,
+                             workspace_bytes, d_err, stream);
+    const PrefixFp8Layout L = prefix_fp8_layout(num_seqs, num_q_heads, num_kv_heads,
+                                                max_blocks_per_seq, block_size, group_size, P);
+    if (workspace == nullptr) return PA_ERR_INVALID_ARG;
+    if (workspace_bytes < L.bytes) return PA_ERR_WORKSPACE_TOO_SMALL;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return PA_ERR_INVALID_ARG;
+    const int g = num_q_heads / num_kv_heads;
+    unsigned char* wsb = static_cast<unsigned char*>(workspace);
+    const int scratch_blocks = num_seqs / group_size * max_blocks_per_seq;
+    const long long pool_rows = static_cast<long long>(num_blocks) * num_kv_heads * block_size;
+    const long long scratch_rows = static_cast<long long>(scratch_blocks) * num_kv_heads * block_size;
+    CUtensorMap map_k8, map_v8, map_k16, map_v16, map_q, map_q1;
+    if (!make_pool_map_fp8(&map_k8, k_cache, pool_rows) || !make_pool_map_fp8(&map_v8, v_cache, pool_rows) ||
+        !make_pool_map(&map_k16, wsb + L.k_off, scratch_rows, q_dtype) ||
+        !make_pool_map(&map_v16, wsb + L.v_off, scratch_rows, q_dtype) ||
+        !make_q_map(&map_q, q, num_seqs, num_q_heads, g, q_dtype, group_size) ||
+        !make_q_map(&map_q1, q, num_seqs, num_q_heads, g, q_dtype, 1))
+        return PA_ERR_CUDA;
+
+    DecodeParams p;
+    p.out = out;
+    p.q = q;
+    p.k_cache = static_cast<const unsigned char*>(k_cache);
+    p.v_cache = static_cast<const unsigned char*>(v_cache);
+    p.k_scale = k_scale;
+    p.v_scale = v_scale;
+    p.block_tables = block_tables;
+    p.context_lens = context_lens;
+    p.query_start = nullptr;
+    p.counters = reinterpret_cast<unsigned int*>(wsb);
+    p.ws_m = reinterpret_cast<float*>(wsb + L.pl.ws.m_off);
+    p.ws_l = reinterpret_cast<float*>(wsb + L.pl.ws.l_off);
+    p.ws_o = reinterpret_cast<float*>(wsb + L.pl.ws.o_off);
+    p.d_err = d_err;
+    p.num_seqs = num_seqs;
+    p.num_q_heads = num_q_heads;
+    p.num_kv_heads = num_kv_heads;
+    p.num_query_tokens = num_seqs;
+    p.group = g;
+    p.head_tiles = num_kv_heads;
+    p.tile_heads = g;
+    p.tile_heads_log2 = log2_exact(g);
+    p.tile_tokens = 1;
+    p.max_blocks_per_seq = max_blocks_per_seq;
+    p.block_size = block_size;
+    p.num_blocks = num_blocks;
+    p.partition_tokens = P;
+    p.max_parts = L.pl.max_parts;
+    p.qk_scale_log2 = scale * 1.4426950408889634f;  // log2(e)
+    p.prefix_lens = prefix_lens;
+    p.prefix_group = group_size;
+    p.prefix_partition_tokens = L.pl.Pp;
+    p.prefix_parts = L.pl.prefix_parts;
+    p.skip_merge = 1;
+    const cudaStream_t st = as_cuda(stream);
+    int32_t* table = reinterpret_cast<int32_t*>(wsb + L.table_off);
+    // 1. each usable group prefix, widened once to q's type
+    pa_status r = launch_prefix_widen(p, q_dtype, wsb + L.k_off, wsb + L.v_off, table, st);
+    if (r != PA_OK) return r;
+    // 2. each group's prefix, once, on the 128-row kernel over the widened blocks
+    DecodeParams pp = p;
+    pp.k_cache = wsb + L.k_off;
+    pp.v_cache = wsb + L.v_off;
+    pp.k_scale = nullptr;
+    pp.v_scale = nullptr;
+    pp.block_tables = table;
+    pp.num_blocks = scratch_blocks;
+    pp.partition_tokens = L.pl.Pp;
+    pp.tile_tokens = group_size;
+    r = q_dtype == PA_BF16 ? launch_prefill_tc_bf16(pp, map_k16, map_v16, map_q, st)
+                           : launch_prefill_tc_f16(pp, map_k16, map_v16, map_q, st);
+    if (r != PA_OK) return r;
+    // 3. each sequence's own tokens on the E4M3 grouped tensor-core kernel
+    r = q_dtype == PA_BF16 ? launch_decode_tc_fp8_bf16(p, map_k8, map_v8, map_q1, st)
+                           : launch_decode_tc_fp8_f16(p, map_k8, map_v8, map_q1, st);
+    if (r != PA_OK) return r;
+    // 4. both ranges of partial states merged per (sequence, head)
+    p.skip_merge = 0;
+    return q_dtype == PA_BF16 ? launch_merge<__nv_bfloat16, 128>(p, st)
+                              : launch_merge<__half, 128>(p, st);
+}

@@ -67,7 +67,7 @@ extern "C" pa_status pa_step_host(const pa_step_dims* d, const void* host_in, vo
     if ((reinterpret_cast<uintptr_t>(dev_stage) & (kAlign - 1)) != 0) return PA_ERR_INVALID_ARG;
     const bool fp8 = k_scale != nullptr || v_scale != nullptr;
     if (fp8 && (k_scale == nullptr || v_scale == nullptr || d->num_query_tokens > 0 ||
-                d->dtype == PA_F32 || d->prefix_group > 0))
+                d->dtype == PA_F32))
         return PA_ERR_INVALID_ARG;
     const bool multi = d->num_query_tokens > 0;
     unsigned char* st = static_cast<unsigned char*>(dev_stage);
@@ -96,7 +96,8 @@ extern "C" pa_status pa_step_host(const pa_step_dims* d, const void* host_in, vo
         multi ? pa_multi_query_workspace_size(rows, d->num_q_heads, d->num_kv_heads, d->head_dim,
                                               d->max_blocks_per_seq, d->block_size, d->dtype,
                                               partition_tokens)
-        : shared ? pa_decode_shared_prefix_workspace_size(
+        : shared ? (fp8 ? pa_decode_shared_prefix_fp8_workspace_size
+                        : pa_decode_shared_prefix_workspace_size)(
                        d->num_seqs, d->num_q_heads, d->num_kv_heads, d->head_dim,
                        d->max_blocks_per_seq, d->block_size, d->dtype, partition_tokens,
                        d->prefix_group)
@@ -133,6 +134,13 @@ extern "C" pa_status pa_step_host(const pa_step_dims* d, const void* host_in, vo
                            d->max_blocks_per_seq, ctx, d->num_seqs, d->num_q_heads,
                            d->num_kv_heads, d->head_dim, d->block_size, d->num_blocks, scale,
                            partition_tokens, d->dtype, workspace, workspace_bytes, d_err, stream);
+    else if (shared && fp8)
+        r = pa_decode_shared_prefix_fp8(dev_out, q, d->dtype, k_cache, v_cache, k_scale, v_scale,
+                                        tables, d->max_blocks_per_seq, ctx, d->num_seqs,
+                                        d->num_q_heads, d->num_kv_heads, d->head_dim,
+                                        d->block_size, d->num_blocks, scale, d->prefix_group,
+                                        prefix_lens, partition_tokens, workspace, workspace_bytes,
+                                        d_err, stream);
     else if (shared)
         r = pa_decode_shared_prefix(dev_out, q, k_cache, v_cache, tables, d->max_blocks_per_seq,
                                     ctx, d->num_seqs, d->num_q_heads, d->num_kv_heads,

@@ -36,6 +36,8 @@ KERNEL_SOURCES = {
     "tc128": ("decode_kernels.cuh", "prefill_tc.cuh", "tc_ptx.cuh", "pa_device.cuh"),
     "shared_prefix": ("decode_kernels.cuh", "decode_tc.cuh", "prefill_tc.cuh", "tc_ptx.cuh",
                       "pa_device.cuh"),
+    "shared_prefix_fp8": ("decode_kernels.cuh", "decode_tc.cuh", "prefill_tc.cuh", "tc_ptx.cuh",
+                          "pa_device.cuh", "prefix_widen.cu"),
 }
 
 _SCALE = {

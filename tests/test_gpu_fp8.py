@@ -249,3 +249,86 @@ def test_fp8_step_through_host_buffers():
     assert same_bits(d["k_cache"].cpu().numpy(), kc) and same_bits(d["v_cache"].cpu().numpy(), vc)
     assert same_bits(d["k_scale"].cpu().numpy(), ks) and same_bits(d["v_scale"].cpu().numpy(), vs)
     assert_close(out_f64(host_out), ref, w.dtype, "fp8 step_host")
+
+
+# ---- shared-prefix decode over E4M3 caches -----------------------------------
+
+def _shared_step(w, d, group, prefix, partition_tokens=0, workspace=None):
+    """copy_blocks, kv_write, then pa_decode_shared_prefix_fp8."""
+    if w.num_pairs:
+        pa.copy_blocks_fp8(d["k_cache"], d["v_cache"], d["k_scale"], d["v_scale"],
+                           d["block_mapping"], d_err=d["d_err"])
+    pa.kv_write_fp8(d["k_new"], d["v_new"], d["k_cache"], d["v_cache"], d["k_scale"],
+                    d["v_scale"], d["slot_mapping"], d_err=d["d_err"])
+    out = torch.full_like(d["q"], float("nan"))
+    pl = torch.as_tensor(np.asarray(prefix, np.int32)).cuda()
+    pa.decode_shared_prefix_fp8(out, d["q"], d["k_cache"], d["v_cache"], d["k_scale"],
+                                d["v_scale"], d["block_tables"], d["context_lens"], w.scale, group,
+                                pl, partition_tokens=partition_tokens, workspace=workspace,
+                                d_err=d["d_err"])
+    torch.cuda.synchronize()
+    return out
+
+
+def _shared_check(w, group, prefix, partition_tokens=0):
+    """Against the oracle's E4M3 decode: the prefix tokens' K and V carry one
+    rounding to q's type (code x scale widened once), inside the 16-bit
+    tolerance."""
+    d = _upload(w)
+    out = _shared_step(w, d, group, prefix, partition_tokens)
+    (kc, ks), (vc, vs), ref, err = oracle.step(w)
+    assert int(d["d_err"].item()) == err == 0
+    assert same_bits(d["k_cache"].cpu().numpy(), kc) and same_bits(d["v_cache"].cpu().numpy(), vc)
+    return assert_close(out_f64(out), ref, w.dtype, w.name), out
+
+
+FP8_SHARED = [
+    # dtype, Hq, Hkv, B, groups, samples, prefix_len, max_suffix, partition
+    ("bf16", 32, 4, 16, 3, 4, 300, 200, 0),      # g = 8: 32 rows per group
+    ("f16", 16, 4, 16, 2, 8, 1016, 300, 0),     # g = 4, partial last prefix block
+    ("bf16", 64, 4, 32, 2, 8, 700, 64, 512),    # g = 16, 8 samples: 128 rows
+    ("f16", 64, 8, 16, 4, 2, 2500, 900, 0),      # long prefix: several prefix parts
+    ("bf16", 32, 4, 16, 2, 4, 3000, 2000, 0),    # contexts past 4096: own pass split
+]
+
+
+@pytest.mark.parametrize("case", range(len(FP8_SHARED)))
+def test_fp8_shared_prefix_parity(case):
+    dtype, Hq, Hkv, B, G, n, pre_len, suf, P = FP8_SHARED[case]
+    w = wl.to_fp8(wl.gqa_share(seed=600 + case, groups=G, samples=n, prefix_len=pre_len,
+                               max_suffix=suf, num_q_heads=Hq, num_kv_heads=Hkv, block_size=B,
+                               dtype=dtype), seed=610 + case)
+    shared = w.meta["shared_prefix_tokens"]
+    _shared_check(w, n, [shared] * G, P)
+    # per group: a shorter prefix, none, one that is not a multiple of the block size
+    _shared_check(w, n, ([max(0, shared - 3 * B), 0, shared - 5] + [shared] * G)[:G], P)
+
+
+def test_fp8_shared_prefix_full_size_repeated():
+    """The 256-sequence E4M3 shared-prefix workload: against the oracle, then
+    three more calls through a workspace holding NaN bytes from before, all
+    bit-identical to the first."""
+    w = wl.by_name("gqa_share_fp8")
+    G = w.meta["samples"]
+    pre = [w.meta["shared_prefix_tokens"]] * (w.num_seqs // G)
+    stats, first = _shared_check(w, G, pre)
+    print("gqa_share_fp8 shared prefix", stats)
+    ws = torch.zeros(pa.decode_shared_prefix_fp8_workspace_size(
+        w.num_seqs, w.num_q_heads, w.num_kv_heads, w.head_dim, w.max_blocks_per_seq,
+        w.block_size, w.dtype, 0, G), dtype=torch.uint8, device="cuda")
+    for _ in range(3):
+        ws[256:].fill_(0xFF)  # the 256-byte counter header stays zero
+        d = _upload(w)
+        out = _shared_step(w, d, G, pre, workspace=ws)
+        assert int(d["d_err"].item()) == 0
+        assert torch.equal(out, first)
+
+
+def test_fp8_shared_prefix_other_shapes_run_plain_decode():
+    """MHA and a group of one: the call is pa_decode_fp8."""
+    for w, G in ((wl.to_fp8(wl.gqa_share(seed=620, groups=2, samples=4, prefix_len=100,
+                                         max_suffix=30, num_q_heads=8, num_kv_heads=8), seed=621), 4),
+                 (wl.to_fp8(wl.gqa_share(seed=622, groups=2, samples=4, prefix_len=100,
+                                         max_suffix=30, num_q_heads=16, num_kv_heads=2), seed=623), 1)):
+        shared = w.meta["shared_prefix_tokens"]
+        _shared_check(w, G, [shared] * (w.num_seqs // G))
