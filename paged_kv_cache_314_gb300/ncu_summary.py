@@ -146,10 +146,12 @@ def parse_launch_list(text: str) -> Dict[str, Dict[str, float]]:
 
 
 def _short(name: str) -> str:
-    """Kernel name without return type, namespaces, template arguments and
-    parameters: ``void pa::decode_persistent_kernel<__half, 128>(...)`` ->
-    ``decode_persistent_kernel``."""
+    """Kernel name without return type, namespaces (anonymous ones too),
+    template arguments and parameters: ``void pa::decode_persistent_kernel<__half,
+    128>(...)`` -> ``decode_persistent_kernel``."""
     n = re.sub(r"^void\s+", "", name.strip())
+    for anon in ("(anonymous namespace)::", "<unnamed>::", "unnamed>::"):
+        n = n.replace(anon, "")
     depth, flat = 0, []
     for ch in n:
         if ch == "<":

@@ -71,3 +71,8 @@ def test_short_names():
                      "(pa::DecodeParams)") == "decode_persistent_kernel"
     assert ns._short("pa::<unnamed>::kv_write_kernel(pa::<unnamed>::KvWriteParams)") == \
         "kv_write_kernel"
+    assert ns._short("void pa::(anonymous namespace)::prefix_widen_kernel<__nv_bfloat16>"
+                     "(pa::DecodeParams, __nv_bfloat16 *, __nv_bfloat16 *, int *)") == \
+        "prefix_widen_kernel"
+    assert ns._short("void unnamed>::prefix_widen_kernel<__nv_bfloat16>(DecodeParams, T1 *, T1 *, "
+                     "int *)") == "prefix_widen_kernel"
