@@ -802,9 +802,13 @@ extern "C" pa_status pa_decode_shared_prefix(
     pa_status r = dtype == PA_BF16 ? launch_prefill_tc_bf16(pp, map_k, map_v, map_q, st)
                                    : launch_prefill_tc_f16(pp, map_k, map_v, map_q, st);
     if (r != PA_OK) return r;
-    // 2. each sequence's own tokens on the grouped tensor-core decode kernel
-    r = dtype == PA_BF16 ? launch_decode_tc_bf16(p, map_k, map_v, map_q1, st)
-                         : launch_decode_tc_f16(p, map_k, map_v, map_q1, st);
+    // 2. each sequence's own tokens on the grouped tensor-core decode kernel,
+    //    started on the SMs the prefix pass leaves (its own work counters)
+    DecodeParams po = p;
+    po.counters = p.counters + 4;
+    po.overlap_prior = 1;
+    r = dtype == PA_BF16 ? launch_decode_tc_bf16(po, map_k, map_v, map_q1, st)
+                         : launch_decode_tc_f16(po, map_k, map_v, map_q1, st);
     if (r != PA_OK) return r;
     // 3. both ranges of partial states merged per (sequence, head)
     p.skip_merge = 0;
@@ -976,9 +980,13 @@ extern "C" pa_status pa_decode_shared_prefix_fp8(
     r = q_dtype == PA_BF16 ? launch_prefill_tc_bf16(pp, map_k16, map_v16, map_q, st)
                            : launch_prefill_tc_f16(pp, map_k16, map_v16, map_q, st);
     if (r != PA_OK) return r;
-    // 3. each sequence's own tokens on the E4M3 grouped tensor-core kernel
-    r = q_dtype == PA_BF16 ? launch_decode_tc_fp8_bf16(p, map_k8, map_v8, map_q1, st)
-                           : launch_decode_tc_fp8_f16(p, map_k8, map_v8, map_q1, st);
+    // 3. each sequence's own tokens on the E4M3 grouped tensor-core kernel,
+    //    started on the SMs the prefix pass leaves (its own work counters)
+    DecodeParams po = p;
+    po.counters = p.counters + 4;
+    po.overlap_prior = 1;
+    r = q_dtype == PA_BF16 ? launch_decode_tc_fp8_bf16(po, map_k8, map_v8, map_q1, st)
+                           : launch_decode_tc_fp8_f16(po, map_k8, map_v8, map_q1, st);
     if (r != PA_OK) return r;
     // 4. both ranges of partial states merged per (sequence, head)
     p.skip_merge = 0;

@@ -114,6 +114,11 @@ struct DecodeParams {
     // order of context length, by classes of kLptClass tokens; no partial
     // states.
     int lpt = 0;
+    // Grouped tensor-core decode: launched with programmatic stream
+    // serialisation so that its CTAs start on SMs the previous kernel (which
+    // signals its dependents at its start) has left; it reads nothing that
+    // kernel writes, and waits for that kernel's completion at its own end.
+    int overlap_prior = 0;
 };
 
 __host__ __device__ constexpr int align16(int x) { return (x + 15) / 16 * 16; }

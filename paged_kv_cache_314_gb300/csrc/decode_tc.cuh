@@ -1004,6 +1004,10 @@ __global__ void __launch_bounds__(kFp8 ? TcTile<T>::kThreadsFp8 : TcTile<T>::kTh
         tc::fence_after_sync();
         tc::tmem_free(tmem, 64);
     }
+    // launched to overlap the previous kernel: this grid completes only after
+    // that one did, so a kernel waiting for this grid also waits for it
+    // (returns at once otherwise)
+    wait_prior_grids();
     if (threadIdx.x == 0) {
         __threadfence();
         const unsigned prev = atomicAdd(p.counters + 1, 1u);
@@ -1039,8 +1043,22 @@ inline pa_status launch_decode_tc_typed(const DecodeParams& p, const CUtensorMap
     if (work > 0x7fffffffLL) return PA_ERR_UNSUPPORTED;
     long long grid = sms;
     if (grid > work) grid = work;
-    kernel<<<static_cast<unsigned>(grid), kFp8 ? C::kThreadsFp8 : C::kThreads, C::kSmemBytes, stream>>>(
-        p, mapK, mapV, mapQ);
+    if (p.overlap_prior) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(static_cast<unsigned>(grid));
+        cfg.blockDim = dim3(kFp8 ? C::kThreadsFp8 : C::kThreads);
+        cfg.dynamicSmemBytes = C::kSmemBytes;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if (cudaLaunchKernelEx(&cfg, kernel, p, mapK, mapV, mapQ) != cudaSuccess) return PA_ERR_CUDA;
+    } else {
+        kernel<<<static_cast<unsigned>(grid), kFp8 ? C::kThreadsFp8 : C::kThreads, C::kSmemBytes, stream>>>(
+            p, mapK, mapV, mapQ);
+    }
     if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
     if (p.max_parts > 1) return launch_merge<T, C::D>(p, stream);
     return PA_OK;

@@ -915,6 +915,9 @@ __global__ void __launch_bounds__(PfTile<T>::kThreads, 1)
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
+    // a kernel launched after this one with programmatic stream serialisation
+    // (the shared-prefix own pass) may start on SMs this grid leaves
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     if (warp == 0)
         pf_produce<T>(p, &mapK, &mapQ, sm, base);
