@@ -842,8 +842,8 @@ __device__ __forceinline__ void pf_softmax(const DecodeParams& p, unsigned char*
         pf::tmem_wait_st();
         tc::fence_async_smem();  // zeroed V rows, for the tensor core
         tc::fence_before_sync();
-        grp.sync();
-        if (tid == 0) mbar_arrive(bar(C::kPFull + (c & 1)));
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(C::kPFull + (c & 1)));  // one of the kSoftWarps arrivals
         if (!(flags & kStageLast)) continue;
 
         // ---- item end: this part of the row of O, once MMA2 of this stage completed
@@ -900,9 +900,10 @@ __global__ void __launch_bounds__(PfTile<T>::kThreads, 1)
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < C::kNumBars; ++i) {
-            // s_free is signalled by every softmax thread
+            // s_free is signalled by every softmax thread, p_full by every softmax warp
             const bool all = i == C::kSFree || i == C::kSFree + 1;
-            mbar_init(smem_addr(bars + i), all ? C::kSoftThreads : 1);
+            const bool warps = i == C::kPFull || i == C::kPFull + 1;
+            mbar_init(smem_addr(bars + i), all ? C::kSoftThreads : warps ? C::kSoftWarps : 1);
         }
         *reinterpret_cast<volatile int*>(sm + C::kMiscOff + 4) = 0;
         fence_barrier_init();
