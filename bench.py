@@ -384,8 +384,14 @@ def _measure(args, name, layout, dev, dist, ws_world):
     shared = (not mq and not args.no_shared_prefix and G > 1 and
               int(w.meta.get("shared_prefix_tokens", 0)) > 0)
     if shared:
-        plan = dict(plan, kernel=("prefix widening + " if fp8 else "") + "tc_128_rows prefix pass + " +
-                    plan["kernel"] + " own pass", merge="kernel", launches=4 if fp8 else 3)
+        sp = pa.shared_prefix_plan(w.num_seqs, w.num_q_heads, w.num_kv_heads, w.head_dim,
+                                   w.max_blocks_per_seq, w.block_size, w.num_blocks, w.dtype, G,
+                                   w.partition_tokens, kv_dtype="e4m3" if fp8 else None)
+        label = ("tc_128_rows fused pass (each group's prefix, then its members' own tokens)"
+                 if sp["merge"] == "none" else
+                 ("prefix widening + " if fp8 else "") + "tc_128_rows prefix pass + " +
+                 plan["kernel"] + " own pass")
+        plan = dict(plan, kernel=label, merge=sp["merge"], launches=sp["launches"])
     dt = w.dtype
     pool = (lambda a: torch.from_numpy(a)) if fp8 else (lambda a: _to_torch(a, dt))
     d = {k: v.to(dev) for k, v in {

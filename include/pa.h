@@ -280,7 +280,13 @@ pa_status pa_multi_query(void* out, const void* q, int num_query_tokens,
  * kv head, group_size x (num_q_heads / num_kv_heads) <= 128 and a partition
  * length that is a multiple of 128 tokens; other shapes (and group_size 1)
  * run pa_decode itself.  Workspace: pa_decode_shared_prefix_workspace_size()
- * bytes, with pa_decode's rules.  Kernels: 3 (prefix pass, own pass, merge).
+ * bytes, with pa_decode's rules.  Kernels: 3 (prefix pass, own pass, merge),
+ * or 1 (fused) when the groups x kv heads are at least the device's SM count,
+ * group_size <= 32 and max_blocks_per_seq x block_size <= 4096: then one pass
+ * of the 128-row kernel takes, per (group, kv head), the prefix and then the
+ * members' own tokens (each member's 16-token groups seen by its rows alone)
+ * and writes the final rows; no partial states, no merge.
+ * pa_shared_prefix_plan() tells which.
  */
 size_t pa_decode_shared_prefix_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads,
                                               int head_dim, int max_blocks_per_seq,
@@ -454,6 +460,23 @@ pa_status pa_attention_plan(int num_seqs, int num_query_tokens, int multi_query,
                             int num_kv_heads, int head_dim, int max_blocks_per_seq, int block_size,
                             int num_blocks, int partition_tokens, pa_dtype kv_dtype,
                             pa_dtype q_dtype, pa_attention_plan_t* plan);
+
+/* pa_shared_prefix_plan -- what a pa_decode_shared_prefix (kv_dtype ==
+ * q_dtype) or pa_decode_shared_prefix_fp8 (kv_dtype PA_E4M3) call with these
+ * sizes would enqueue, on the current device, without enqueuing anything.
+ * Shapes without a shared pass: pa_attention_plan's plan of the plain decode.
+ * Otherwise kernel PA_KERNEL_TC_128_ROWS (the first pass that reads the
+ * cache) and either the fused pass (merge PA_MERGE_NONE, max_parts 1,
+ * partition_tokens the longest allowed context, launches 1) or the separate
+ * passes (PA_MERGE_KERNEL, partition_tokens of the own pass, max_parts of
+ * both passes, launches 3; E4M3: 4; also what a call without a usable device
+ * is planned as).  PA_ERR_INVALID_ARG: plan null,
+ * group_size <= 0, num_seqs <= 0 or not a multiple of group_size; otherwise
+ * the checks of pa_attention_plan. */
+pa_status pa_shared_prefix_plan(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                                int max_blocks_per_seq, int block_size, int num_blocks,
+                                int partition_tokens, pa_dtype kv_dtype, pa_dtype q_dtype,
+                                int group_size, pa_attention_plan_t* plan);
 
 /* ---- one step with host inputs and output --------------------------------
  *

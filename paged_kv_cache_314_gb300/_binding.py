@@ -32,7 +32,7 @@ EXPORTED = ("pa_abi_version", "pa_status_string", "pa_kv_write", "pa_copy_blocks
             "pa_decode", "pa_decode_static_workspace", "pa_multi_query_partition_tokens",
             "pa_multi_query_workspace_size", "pa_multi_query", "pa_kv_write_fp8",
             "pa_copy_blocks_fp8", "pa_swap_blocks_fp8", "pa_decode_fp8",
-            "pa_attention_plan", "pa_step_layout", "pa_step_host",
+            "pa_attention_plan", "pa_shared_prefix_plan", "pa_step_layout", "pa_step_host",
             "pa_decode_shared_prefix_workspace_size", "pa_decode_shared_prefix",
             "pa_decode_shared_prefix_fp8_workspace_size", "pa_decode_shared_prefix_fp8",
             "pa_selftest_wait_timeout")
@@ -142,6 +142,8 @@ def load() -> ctypes.CDLL:
         lib.pa_attention_plan.restype = i32
         lib.pa_attention_plan.argtypes = [i32, i32, i32, i32, i32, i32, i32, i32, i32, i32, i32,
                                           i32, ctypes.POINTER(_Plan)]
+        lib.pa_shared_prefix_plan.restype = i32
+        lib.pa_shared_prefix_plan.argtypes = [i32] * 11 + [ctypes.POINTER(_Plan)]
         _lib = lib
         return lib
 
@@ -571,6 +573,25 @@ def attention_plan(num_seqs: int, num_q_heads: int, num_kv_heads: int, head_dim:
                                     num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq,
                                     block_size, num_blocks, partition_tokens, kv_code, q_code,
                                     ctypes.byref(plan)), "pa_attention_plan")
+    return {"kernel": KERNEL_NAMES.get(plan.kernel, plan.kernel),
+            "partition_tokens": plan.partition_tokens, "max_parts": plan.max_parts,
+            "merge": MERGE_NAMES.get(plan.merge, plan.merge), "launches": plan.launches}
+
+
+def shared_prefix_plan(num_seqs: int, num_q_heads: int, num_kv_heads: int, head_dim: int,
+                       max_blocks_per_seq: int, block_size: int, num_blocks: int, dtype,
+                       group_size: int, partition_tokens: int = 0, kv_dtype=None) -> dict:
+    """What a decode_shared_prefix (kv_dtype None) or decode_shared_prefix_fp8
+    (kv_dtype "e4m3", q and out of type dtype) call with these sizes would
+    launch on the current device: the fused pass ("merge" "none", 1 launch),
+    the separate passes (prefix, own, merge) or the plain decode's plan."""
+    q_code = _dtype_code(dtype)
+    kv_code = PA_E4M3 if kv_dtype == "e4m3" else q_code
+    plan = _Plan()
+    _check(load().pa_shared_prefix_plan(num_seqs, num_q_heads, num_kv_heads, head_dim,
+                                        max_blocks_per_seq, block_size, num_blocks,
+                                        partition_tokens, kv_code, q_code, group_size,
+                                        ctypes.byref(plan)), "pa_shared_prefix_plan")
     return {"kernel": KERNEL_NAMES.get(plan.kernel, plan.kernel),
             "partition_tokens": plan.partition_tokens, "max_parts": plan.max_parts,
             "merge": MERGE_NAMES.get(plan.merge, plan.merge), "launches": plan.launches}

@@ -687,6 +687,21 @@ struct PrefixPlan {
     WsLayout ws;
 };
 
+// One fused pass (an item per group and kv head: the prefix, then every
+// member's own tokens) rather than prefix pass + own pass + merge, when the
+// items fill every SM at least once and no member can hold more than
+// kFusedMaxCtx tokens (an item's work grows with its members' contexts).
+constexpr long long kFusedMaxCtx = 4096;
+
+bool prefix_fused_ok(int num_groups, int num_kv_heads, long long max_ctx, int group_size) {
+    if (group_size > 32 || max_ctx > kFusedMaxCtx) return false;
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return false;
+    return static_cast<long long>(num_groups) * num_kv_heads >= sms;
+}
+
 PrefixPlan prefix_plan(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
                        int max_blocks_per_seq, int block_size, int group_size, int P) {
     PrefixPlan r;
@@ -794,6 +809,15 @@ extern "C" pa_status pa_decode_shared_prefix(
     p.prefix_parts = pl.prefix_parts;
     p.skip_merge = 1;
     const cudaStream_t st = as_cuda(stream);
+    if (prefix_fused_ok(num_seqs / group_size, num_kv_heads,
+                        static_cast<long long>(max_blocks_per_seq) * block_size, group_size)) {
+        // one pass: per (group, kv head) the prefix, then the members' own tokens
+        DecodeParams pf = p;
+        pf.tile_tokens = group_size;
+        pf.prefix_fused = 1;
+        return dtype == PA_BF16 ? launch_prefill_tc_bf16(pf, map_k, map_v, map_q, st)
+                                : launch_prefill_tc_f16(pf, map_k, map_v, map_q, st);
+    }
     // 1. each group's prefix, once, on the 128-row kernel (rows: the group's
     //    sequences x the g heads of a kv head)
     DecodeParams pp = p;
@@ -992,4 +1016,44 @@ extern "C" pa_status pa_decode_shared_prefix_fp8(
     p.skip_merge = 0;
     return q_dtype == PA_BF16 ? launch_merge<__nv_bfloat16, 128>(p, st)
                               : launch_merge<__half, 128>(p, st);
+}
+
+extern "C" pa_status pa_shared_prefix_plan(int num_seqs, int num_q_heads, int num_kv_heads,
+                                          int head_dim, int max_blocks_per_seq, int block_size,
+                                          int num_blocks, int partition_tokens, pa_dtype kv_dtype,
+                                          pa_dtype q_dtype, int group_size,
+                                          pa_attention_plan_t* plan) {
+    using namespace pa;
+    if (plan == nullptr || group_size <= 0 || num_seqs <= 0 || num_seqs % group_size != 0)
+        return PA_ERR_INVALID_ARG;
+    // the plain decode's plan (and every host check of the call)
+    const pa_status r = pa_attention_plan(num_seqs, num_seqs, 0, num_q_heads, num_kv_heads, head_dim,
+                                          max_blocks_per_seq, block_size, num_blocks,
+                                          partition_tokens, kv_dtype, q_dtype, plan);
+    if (r != PA_OK) return r;
+    const bool fp8 = kv_dtype == PA_E4M3;
+    const int P = pa_decode_partition_tokens(num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq,
+                                             block_size, kv_dtype, partition_tokens);
+    const bool shared = fp8 ? prefix_fp8_shape(num_seqs, num_q_heads, num_kv_heads, head_dim,
+                                               max_blocks_per_seq, block_size, num_blocks, q_dtype,
+                                               group_size, P)
+                            : prefix_shape(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                                           num_blocks, kv_dtype, group_size, P);
+    if (!shared) return PA_OK;  // the call is the plain decode
+    const long long max_ctx = static_cast<long long>(max_blocks_per_seq) * block_size;
+    plan->kernel = PA_KERNEL_TC_128_ROWS;  // the first kernel reading the cache
+    if (!fp8 && prefix_fused_ok(num_seqs / group_size, num_kv_heads, max_ctx, group_size)) {
+        plan->partition_tokens = static_cast<int>(max_ctx);
+        plan->max_parts = 1;
+        plan->merge = PA_MERGE_NONE;
+        plan->launches = 1;
+        return PA_OK;
+    }
+    const PrefixPlan pl = prefix_plan(num_seqs, num_q_heads, num_kv_heads, head_dim,
+                                      max_blocks_per_seq, block_size, group_size, P);
+    plan->partition_tokens = P;
+    plan->max_parts = pl.max_parts;
+    plan->merge = PA_MERGE_KERNEL;
+    plan->launches = fp8 ? 4 : 3;
+    return PA_OK;
 }

@@ -107,6 +107,10 @@ struct DecodeParams {
     int prefix_group = 0;
     int prefix_partition_tokens = 0;  // partition length of the prefix pass
     int prefix_parts = 0;             // partition slots reserved for the prefix pass
+    // Fused shared-prefix decode (128-row kernel alone): an item per (group, kv
+    // head) reads the prefix once, then every member's own tokens (each member's
+    // rows alone see its own), and writes the final rows.  prefix_group <= 32.
+    int prefix_fused = 0;
     int skip_merge = 0;               // the launch leaves the merge to a later kernel
     // Decode with whole-context work items handed out longest first (one query
     // per sequence and query head per tile, at most kLptMaxSeqs sequences):

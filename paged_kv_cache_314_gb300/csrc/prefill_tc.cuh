@@ -104,16 +104,23 @@ struct PfStageMeta {
     uint32_t item_seq;
     int nvalid;       // tokens of the stage before the item's span end
     uint32_t groups;  // bit r: 16-token group r was loaded (its block id passed the check)
-    uint32_t flags;   // kStageFirst / kStageLast / kStageEnd
+    uint32_t flags;   // kStageFirst / kStageLast / kStageEnd / kStageOwn
     int lim_rel;      // tokens of this stage the item's first query token sees
     int row0;         // the item: q / out row of its first query token
     int hq0;          // first query head (the g heads of one kv head)
     int part;         // partition index
     int nparts;       // 0: context length out of range (zero rows)
     int ntok;         // query tokens
-    int pad[6];
+    // kStageOwn (fused shared-prefix decode): byte r of gcnt = tokens of group r
+    // (a leading run of 0..16), byte r of gown = the query token (member) whose
+    // rows alone see them; nvalid and lim_rel are not used
+    uint32_t gcnt[2];
+    uint32_t gown[2];
+    int pad[2];
 };
 static_assert(sizeof(PfStageMeta) == 64, "stage meta slot");
+// a stage of members' own tokens, packed 16-token groups at a time
+constexpr uint32_t kStageOwn = 8u;
 
 namespace pf {
 
@@ -220,7 +227,7 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
 }  // namespace pf
 
 // ---- warp 0: work items, Q and K copies, stage meta, V plan ------------------
-template <typename T>
+template <typename T, bool kFused>
 __device__ __forceinline__ void pf_produce(const DecodeParams& p, const CUtensorMap* mapK,
                                            const CUtensorMap* mapQ, unsigned char* sm, uint32_t base) {
     using C = PfTile<T>;
@@ -236,6 +243,10 @@ __device__ __forceinline__ void pf_produce(const DecodeParams& p, const CUtensor
     // g heads of one kv head, its context is its shared prefix (no causal
     // limit), and it is read through its first sequence's block table.
     const bool prefix = p.prefix_lens != nullptr;
+    // Fused shared-prefix decode: an item (group, kv head) reads the prefix,
+    // then every member's own tokens, and writes final rows (no partial
+    // states, no merge).
+    constexpr bool fused = kFused;  // (launched only with prefix_lens set)
     const int S = prefix ? p.num_seqs / p.prefix_group : p.num_seqs;
     const int P = p.partition_tokens, B = p.block_size, g = p.group;
     const int Tq = p.tile_tokens;  // query tokens per item: 128 / g (prefix pass: prefix_group)
@@ -252,7 +263,7 @@ __device__ __forceinline__ void pf_produce(const DecodeParams& p, const CUtensor
         if (prefix) {
             const int pre = sl < S ? group_prefix(p, sl) : 0;
             sq_lane = SeqQueries{pre, sl * p.prefix_group, sl * p.prefix_group + p.prefix_group, true};
-            items_lane = pre > 0 ? p.head_tiles * ((pre + P - 1) / P) : 0;
+            items_lane = sl >= S ? 0 : fused ? p.head_tiles : pre > 0 ? p.head_tiles * ((pre + P - 1) / P) : 0;
             return;
         }
         sq_lane = sl < S ? seq_queries(p, sl) : SeqQueries{0, 0, 0, true};
@@ -267,6 +278,8 @@ __device__ __forceinline__ void pf_produce(const DecodeParams& p, const CUtensor
     item_id = __shfl_sync(0xffffffffu, item_id, 0);
 
     while (!aborted) {
+        int s, i_loc, next_id = 0;
+        SeqQueries sq;
         bool found = false;
         while (s_cur < S) {
             if (s_cur - win0 >= 32) {
@@ -294,26 +307,24 @@ __device__ __forceinline__ void pf_produce(const DecodeParams& p, const CUtensor
             s_cur = win0 + 32;
         }
         if (!found) break;
-        int next_id = 0;
         if (lane == 0) next_id = static_cast<int>(atomicAdd(p.counters, 1u));
 
-        const int s = s_cur;
-        SeqQueries sq;
+        s = s_cur;
         sq.ctx = __shfl_sync(0xffffffffu, sq_lane.ctx, s_cur - win0);
         sq.q0 = __shfl_sync(0xffffffffu, sq_lane.q0, s_cur - win0);
         sq.q1 = __shfl_sync(0xffffffffu, sq_lane.q1, s_cur - win0);
         sq.multi = true;
-        const int ctx = sq.ctx;
-        const bool valid = prefix || sq.ctx_ok(max_ctx);
-        const int qlen = sq.q1 - sq.q0;
-        const int np = prefix ? (ctx + P - 1) / P : valid ? items_of(ctx, max_ctx, P) : 1;
-        const int ntt = (qlen + Tq - 1) / Tq;
-        const int i_loc = item_id - base_items;
+        i_loc = item_id - base_items;
         if (i_loc < 0 || i_loc >= __shfl_sync(0xffffffffu, items_lane, s_cur - win0)) {
             // only reachable when query_start is not ascending (item counts can overflow)
             if (lane == 0) report(p.d_err, PA_DERR_CTX_OOB);
             break;
         }
+        const int ctx = sq.ctx;
+        const bool valid = prefix || sq.ctx_ok(max_ctx);
+        const int qlen = sq.q1 - sq.q0;
+        const int np = fused ? 1 : prefix ? (ctx + P - 1) / P : valid ? items_of(ctx, max_ctx, P) : 1;
+        const int ntt = (qlen + Tq - 1) / Tq;
         const int tile = i_loc / np;  // (kv head, query-token tile)
         const int part = i_loc - tile * np;
         const int hk = tile / ntt;
@@ -325,8 +336,8 @@ __device__ __forceinline__ void pf_produce(const DecodeParams& p, const CUtensor
         const int lim_first = prefix ? 0x40000000 : ctx - qlen + i0 + 1;
         const int lim_last = prefix ? ctx : lim_first + ntok - 1;
         const int tok_begin = part * P;
-        const int tok_end = valid ? max(tok_begin, min(tok_begin + P, lim_last)) : tok_begin;
-        const int nst = tok_end > tok_begin ? (tok_end - tok_begin + C::kStageTok - 1) / C::kStageTok : 1;
+        const int tok_end = fused ? ctx : valid ? max(tok_begin, min(tok_begin + P, lim_last)) : tok_begin;
+        int nst = tok_end > tok_begin ? (tok_end - tok_begin + C::kStageTok - 1) / C::kStageTok : 1;
         if (!valid && lane == 0) report(p.d_err, PA_DERR_CTX_OOB);
 
         const int qs = item_seq & 1;
@@ -349,34 +360,70 @@ __device__ __forceinline__ void pf_produce(const DecodeParams& p, const CUtensor
         const int32_t* trow =
             p.block_tables + static_cast<size_t>(prefix ? sq.q0 : s) * p.max_blocks_per_seq;
         const int blk_end = (tok_end + B - 1) / B;
-        int win = tok_begin / B;
-        int32_t entry = (win + lane < blk_end) ? __ldg(trow + win + lane) : -1;
 
-        for (int i = 0; i < nst; ++i) {
-            const int cc = c + i;
-            const int st = cc & 1;
-            const uint32_t reuse = static_cast<uint32_t>((cc >> 1) - 1) & 1;
-            if (cc >= C::kStages && !mbar_wait_warp(bar(C::kEmptyK + st), reuse)) {
-                if (lane == 0) report(p.d_err, PA_DERR_TIMEOUT);
-                *abort_flag = 1;
-                aborted = true;
-                c = cc;
-                break;
+        // Fused: after the prefix's stages, the members' own tokens [ctx, ctx_j)
+        // as one run of 16-token groups (member j's padded to whole groups, in
+        // member order), 8 groups a stage, each read through its member's table
+        // row.  Lane j < qlen: member j's context, first group and groups.
+        int ctx_lane = ctx, g0_lane = 0, k_lane = 0, n_own = 0;
+        if (fused) {
+            const int cj = lane < qlen ? __ldg(p.context_lens + sq.q0 + lane) : ctx;
+            const bool ok = cj >= ctx && cj <= max_ctx;
+            if (!__all_sync(0xffffffffu, ok) && lane == 0) report(p.d_err, PA_DERR_CTX_OOB);
+            ctx_lane = ok ? cj : ctx;  // out of range: no own tokens (a zero row)
+            k_lane = (ctx_lane - ctx + 15) >> 4;
+            int incl = k_lane;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, incl, off);
+                if (lane >= off) incl += y;
             }
-            const int t0 = tok_begin + i * C::kStageTok;
-            const int t1 = min(t0 + C::kStageTok, tok_end);
-            if (t1 > t0 && (t1 - 1) / B - win >= 32) {  // window must hold the stage's blocks
-                win = t0 / B;
-                entry = (win + lane < blk_end) ? __ldg(trow + win + lane) : -1;
-            }
-            // lane r < 8: the stage's 16-token group r
+            g0_lane = incl - k_lane;
+            const int groups_own = __shfl_sync(0xffffffffu, incl, 31);
+            n_own = (groups_own + 7) >> 3;
+            nst = (ctx + C::kStageTok - 1) / C::kStageTok;
+            if (nst + n_own == 0) nst = 1;  // an empty item: one empty stage
+        }
+        const int nst_all = nst + n_own;
+
+        // A walk over the item's stages: the table window (lane l: entry win + l)
+        // and the window of 32 own groups [wv, wv + 32) (lane l: group wv + l's
+        // cache row, -1 for none or out of range, its tokens and member).
+        struct Walk {
+            int win;
+            int32_t entry;
+            int wv, own_row, own_cnt, own_mem;
+            bool own_bad;
+        };
+        auto walk_start = [&](Walk& w) {
+            w.win = tok_begin / B;
+            w.entry = (w.win + lane < blk_end) ? __ldg(trow + w.win + lane) : -1;
+            w.wv = -64;
+            w.own_row = -1;
+            w.own_cnt = 0;
+            w.own_mem = 0;
+            w.own_bad = false;
+        };
+        // Stage i's 16-token groups (lane r < 8: group r): its cache row, whether
+        // it holds data (mine) or its block id is out of range (bad), and for
+        // an own stage its tokens and member.  Stages are visited in order.
+        auto locate = [&](Walk& w, int i, int& row, bool& mine, bool& bad, int& gcnt, int& gmem) {
             const int r = lane & 7;
-            const int t = t0 + 16 * r;
-            int row = 0;
-            bool mine = false, bad = false;
-            {
-                const int lb = t < t1 ? t / B : win;
-                const int pb = __shfl_sync(0xffffffffu, entry, lb - win);
+            row = 0;
+            gcnt = 0;
+            gmem = 0;
+            mine = false;
+            bad = false;
+            if (!kFused || i < nst) {
+                const int t0 = tok_begin + i * C::kStageTok;
+                const int t1 = min(t0 + C::kStageTok, tok_end);
+                if (t1 > t0 && (t1 - 1) / B - w.win >= 32) {  // window must hold the stage's blocks
+                    w.win = t0 / B;
+                    w.entry = (w.win + lane < blk_end) ? __ldg(trow + w.win + lane) : -1;
+                }
+                const int t = t0 + 16 * r;
+                const int lb = t < t1 ? t / B : w.win;
+                const int pb = __shfl_sync(0xffffffffu, w.entry, lb - w.win);
                 if (lane < 8 && t < t1) {
                     if (static_cast<unsigned>(pb) < static_cast<unsigned>(p.num_blocks)) {
                         row = (pb * p.num_kv_heads + hk) * B + (t - lb * B);
@@ -385,9 +432,79 @@ __device__ __forceinline__ void pf_produce(const DecodeParams& p, const CUtensor
                         bad = true;
                     }
                 }
+                return;
             }
+            const int v0 = 8 * (i - nst);  // the stage's first own group
+            if (v0 + 8 > w.wv + 32) {
+                w.wv = v0;
+                const int v = w.wv + lane;
+                int j = 0;  // the member of group v: members whose groups end at or before v
+                for (int m = 0; m < qlen; ++m) j += __shfl_sync(0xffffffffu, g0_lane + k_lane, m) <= v;
+                const int jj = min(j, 31);
+                const int gj = __shfl_sync(0xffffffffu, g0_lane, jj);
+                const int cj = __shfl_sync(0xffffffffu, ctx_lane, jj);
+                w.own_row = -1;
+                w.own_cnt = 0;
+                w.own_mem = jj;
+                w.own_bad = false;
+                if (j < qlen) {
+                    const int tk = ctx + 16 * (v - gj);  // a multiple of 16 (ctx: of the block size)
+                    const int lb = tk / B;
+                    const int pb =
+                        __ldg(p.block_tables + static_cast<size_t>(sq.q0 + j) * p.max_blocks_per_seq + lb);
+                    w.own_cnt = min(16, cj - tk);
+                    if (static_cast<unsigned>(pb) < static_cast<unsigned>(p.num_blocks))
+                        w.own_row = (pb * p.num_kv_heads + hk) * B + (tk - lb * B);
+                    else
+                        w.own_bad = true;
+                }
+            }
+            const int src = v0 + r - w.wv;
+            const int orow = __shfl_sync(0xffffffffu, w.own_row, src);
+            const int ocnt = __shfl_sync(0xffffffffu, w.own_cnt, src);
+            const int omem = __shfl_sync(0xffffffffu, w.own_mem, src);
+            const bool obad = __shfl_sync(0xffffffffu, w.own_bad, src);
+            if (lane < 8) {
+                mine = orow >= 0;
+                bad = obad;
+                row = mine ? orow : 0;
+                gcnt = mine ? ocnt : 0;
+                gmem = omem;
+            }
+        };
+        Walk wl;  // the loads' walk
+        walk_start(wl);
+
+        for (int i = 0; i < nst_all; ++i) {
+            const int cc = c + i;
+            const int st = cc & 1;
+            const uint32_t reuse = static_cast<uint32_t>((cc >> 1) - 1) & 1;
+            // the stage's rows first (table reads included), then the wait for its K slot
+            const bool own = kFused && i >= nst;
+            const int t0 = tok_begin + i * C::kStageTok;
+            const int t1 = own ? t0 : min(t0 + C::kStageTok, tok_end);
+            const int r = lane & 7;
+            int row, gcnt, gmem;
+            bool mine, bad;
+            locate(wl, i, row, mine, bad, gcnt, gmem);
             const uint32_t groups = __ballot_sync(0xffffffffu, mine) & 0xffu;
+            // bytes r of the own stage's counts and members
+            uint32_t gc[2] = {0u, 0u}, gm[2] = {0u, 0u};
+            if (own) {
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    gc[q >> 2] |= static_cast<uint32_t>(__shfl_sync(0xffffffffu, gcnt, q)) << (8 * (q & 3));
+                    gm[q >> 2] |= static_cast<uint32_t>(__shfl_sync(0xffffffffu, gmem, q)) << (8 * (q & 3));
+                }
+            }
             if (__any_sync(0xffffffffu, bad)) oob = true;
+            if (cc >= C::kStages && !mbar_wait_warp(bar(C::kEmptyK + st), reuse)) {
+                if (lane == 0) report(p.d_err, PA_DERR_TIMEOUT);
+                *abort_flag = 1;
+                aborted = true;
+                c = cc;
+                break;
+            }
             const uint32_t tile_bytes = static_cast<uint32_t>(__popc(groups)) * 4096u;
             const uint32_t stage_base = base + C::kRingOff + st * C::kStageBytes;
             if (mine) pf::tma_load_4d(stage_base + r * 4096, mapK, row >> 3, bar(C::kFullK + st));
@@ -399,7 +516,8 @@ __device__ __forceinline__ void pf_produce(const DecodeParams& p, const CUtensor
                 PfStageMeta& m = meta[ms];
                 uint32_t flags = 0;
                 if (i == 0) flags |= kStageFirst;
-                if (i == nst - 1) flags |= kStageLast;
+                if (i == nst_all - 1) flags |= kStageLast;
+                if (own) flags |= kStageOwn;
                 m.item_seq = static_cast<uint32_t>(item_seq);
                 m.nvalid = max(0, t1 - t0);
                 m.groups = groups;
@@ -408,9 +526,14 @@ __device__ __forceinline__ void pf_produce(const DecodeParams& p, const CUtensor
                 m.row0 = sq.q0 + i0;
                 m.hq0 = hq0;
                 m.part = part;
-                // prefix pass: always a partial state (the merge adds each sequence's own)
-                m.nparts = prefix ? p.prefix_parts + 1 : valid ? np : 0;
+                // prefix pass: a partial state (the merge adds each sequence's own),
+                // fused: final rows
+                m.nparts = fused ? 1 : prefix ? p.prefix_parts + 1 : valid ? np : 0;
                 m.ntok = ntok;
+                m.gcnt[0] = gc[0];
+                m.gcnt[1] = gc[1];
+                m.gown[0] = gm[0];
+                m.gown[1] = gm[1];
             }
             __syncwarp();
             if (lane == 0) {
@@ -423,7 +546,7 @@ __device__ __forceinline__ void pf_produce(const DecodeParams& p, const CUtensor
             }
         }
         if (aborted) break;
-        c += nst;
+        c += nst_all;
         ++item_seq;
         item_id = __shfl_sync(0xffffffffu, next_id, 0);
         if (*abort_flag) aborted = true;
@@ -694,10 +817,11 @@ struct PfGroup {
 // divided by the row sum (or the partition's partial state).  The thread also
 // zeroes its share of V row `row` when token `row` holds no data, so
 // 0 x garbage never reaches O.
-template <typename T>
+template <typename T, bool kFused>
 __device__ __forceinline__ void pf_softmax(const DecodeParams& p, unsigned char* sm, uint32_t tmem) {
     using C = PfTile<T>;
     constexpr int kCols = C::kCols, kSplit = C::kSplit;
+    static_assert(kCols == 32, "a thread's columns are two 16-token groups");
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int tid = threadIdx.x - 64;  // 0 .. kSoftThreads-1
     const int part_i = (warp - 2) >> 2;  // columns kCols*part_i ..
@@ -731,7 +855,8 @@ __device__ __forceinline__ void pf_softmax(const DecodeParams& p, unsigned char*
         if (flags & kStageEnd) break;
         const int nvalid = m.nvalid;
         const uint32_t groups = m.groups;
-        const int lim = min(nvalid, m.lim_rel + ti);  // tokens of this stage the row sees
+        const bool own = kFused && (flags & kStageOwn);
+        const uint32_t gc0 = m.gcnt[0], gc1 = m.gcnt[1];
         if (flags & kStageFirst) {
             row0 = m.row0;
             hq0 = m.hq0;
@@ -741,11 +866,24 @@ __device__ __forceinline__ void pf_softmax(const DecodeParams& p, unsigned char*
             m_ref = -INFINITY;
             l = 0.f;
         }
-        if (!(groups == 0xffu && nvalid >= C::kStageTok)) {
+        // whether every token of the stage holds data, and if not, whether
+        // token `row` does not (its V row is zeroed below)
+        const bool full = groups == 0xffu && (own ? (gc0 & gc1) == 0x10101010u : nvalid >= C::kStageTok);
+        bool zero_row = false;
+        if (!full) {
+            const int rg = row >> 4;
+            zero_row = !(((groups >> rg) & 1u) &&
+                         (own ? (row & 15) < static_cast<int>(((rg < 4 ? gc0 : gc1) >> (8 * (rg & 3))) & 0xffu)
+                              : row < nvalid));
+        }
+
+        if (!kFused && !full) {
             // some token of the stage holds no data: once the stage's V has
-            // landed, zero its rows (before P is published)
+            // landed, zero its rows (before P is published; the fused pass,
+            // whose stages of members' tokens are often partial, does it late
+            // in the stage, when the V copy has had more time to land)
             if (!grp.wait(bar(C::kFullV + st), static_cast<uint32_t>(c >> 1) & 1, p.d_err, abort_flag)) break;
-            if (!(row < nvalid && ((groups >> (row >> 4)) & 1u))) {  // token `row` holds no data
+            if (zero_row) {  // token `row` holds no data
                 unsigned char* vrow = sm + C::kRingOff + st * C::kStageBytes + C::kTileBytes +
                                       (row >> 3) * 2048 + vh * 1024 + (row & 7) * 128;
 #pragma unroll
@@ -762,10 +900,24 @@ __device__ __forceinline__ void pf_softmax(const DecodeParams& p, unsigned char*
         tc::fence_before_sync();
         mbar_arrive(bar(C::kSFree + st));  // every thread of the group (count kSoftThreads)
         float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-        // every token valid for every row: no mask, and the maximum is taken
-        // on the raw logits (scaled afterwards, kq > 0); the exponent below
-        // applies the scale.  Otherwise x is scaled and masked here.
-        const bool unmasked = groups == 0xffu && lim >= 128 && kq > 0.f;
+        // tokens of this thread's two 16-token groups (2 part_i, 2 part_i + 1)
+        // that the row sees: a leading run of each
+        int na, nb;
+        if (own) {  // the group's tokens if the row's query token is the group's member
+            const uint32_t cw = part_i < 2 ? gc0 : gc1;
+            const uint32_t ow = part_i < 2 ? m.gown[0] : m.gown[1];
+            const int sh = 16 * (part_i & 1);
+            na = static_cast<int>((ow >> sh) & 0xffu) == ti ? static_cast<int>((cw >> sh) & 0xffu) : 0;
+            nb = static_cast<int>((ow >> (sh + 8)) & 0xffu) == ti ? static_cast<int>((cw >> (sh + 8)) & 0xffu) : 0;
+        } else {  // tokens before the row's limit, of loaded groups
+            const int lim = min(nvalid, m.lim_rel + ti);
+            na = ((groups >> (2 * part_i)) & 1u) ? max(0, min(16, lim - kCols * part_i)) : 0;
+            nb = ((groups >> (2 * part_i + 1)) & 1u) ? max(0, min(16, lim - kCols * part_i - 16)) : 0;
+        }
+        // every token valid: no mask, and the maximum is taken on the raw
+        // logits (scaled afterwards, kq > 0); the exponent below applies the
+        // scale.  Otherwise x is scaled and masked here.
+        const bool unmasked = __all_sync(0xffffffffu, na == 16 && nb == 16) && kq > 0.f;
         if (unmasked) {
 #pragma unroll
             for (int j = 0; j < kCols; j += 2) mx4[(j >> 1) & 3] = pf::fmax3(mx4[(j >> 1) & 3], x[j], x[j + 1]);
@@ -774,8 +926,7 @@ __device__ __forceinline__ void pf_softmax(const DecodeParams& p, unsigned char*
         } else {
 #pragma unroll
             for (int j = 0; j < kCols; ++j) {
-                const int t = static_cast<int>(col0) + j;
-                const bool ok = t < lim && ((groups >> (t >> 4)) & 1u);
+                const bool ok = j < 16 ? j < na : j - 16 < nb;
                 x[j] = ok ? x[j] * kq : -INFINITY;
                 mx4[j & 3] = fmaxf(mx4[j & 3], x[j]);
             }
@@ -839,6 +990,19 @@ __device__ __forceinline__ void pf_softmax(const DecodeParams& p, unsigned char*
         }
         pf::tmem_st<kCols / 2>(tmem + C::kPCol + 64u * (c & 1) + (kCols / 2) * part_i + lane_off, pw);
         l += (l4[0] + l4[1]) + (l4[2] + l4[3]);
+        if (kFused && !full) {
+            // some token of the stage holds no data: once the stage's V has
+            // landed, zero its rows (before P is published; late in the
+            // stage, so the V copy has had time to land)
+            if (!grp.wait(bar(C::kFullV + st), static_cast<uint32_t>(c >> 1) & 1, p.d_err, abort_flag)) break;
+            if (zero_row) {  // token `row` holds no data
+                unsigned char* vrow = sm + C::kRingOff + st * C::kStageBytes + C::kTileBytes +
+                                      (row >> 3) * 2048 + vh * 1024 + (row & 7) * 128;
+#pragma unroll
+                for (int k = 0; k < kChunks; ++k)
+                    *reinterpret_cast<uint4*>(vrow + (vk0 + k) * 16) = make_uint4(0, 0, 0, 0);
+            }
+        }
         pf::tmem_wait_st();
         tc::fence_async_smem();  // zeroed V rows, for the tensor core
         tc::fence_before_sync();
@@ -885,7 +1049,7 @@ __device__ __forceinline__ void pf_softmax(const DecodeParams& p, unsigned char*
     tc::fence_before_sync();
 }
 
-template <typename T>
+template <typename T, bool kFused>
 __global__ void __launch_bounds__(PfTile<T>::kThreads, 1)
     prefill_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap mapK,
                       const __grid_constant__ CUtensorMap mapV, const __grid_constant__ CUtensorMap mapQ) {
@@ -921,11 +1085,11 @@ __global__ void __launch_bounds__(PfTile<T>::kThreads, 1)
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     if (warp == 0)
-        pf_produce<T>(p, &mapK, &mapQ, sm, base);
+        pf_produce<T, kFused>(p, &mapK, &mapQ, sm, base);
     else if (warp == 1)
         pf_mma<T>(p, sm, base, tmem);
     else if (warp < C::kCopyWarp)
-        pf_softmax<T>(p, sm, tmem);
+        pf_softmax<T, kFused>(p, sm, tmem);
     else
         pf_copy_v<T>(p, &mapV, sm, base);
 
@@ -950,12 +1114,16 @@ inline pa_status launch_prefill_tc_typed(const DecodeParams& p, const CUtensorMa
                                          const CUtensorMap& mapV, const CUtensorMap& mapQ,
                                          cudaStream_t stream) {
     using C = PfTile<T>;
-    static std::atomic<uint64_t> smem_configured{0};
+    static std::atomic<uint64_t> smem_configured[2] = {{0}, {0}};  // per kernel: plain, fused
     if (p.prefix_lens != nullptr ? p.group * p.tile_tokens > C::kRows
                                  : p.group * p.tile_tokens != C::kRows)
         return PA_ERR_UNSUPPORTED;
-    auto kernel = prefill_tc_kernel<T>;
-    if (ensure_smem(kernel, C::kSmemBytes, smem_configured) != PA_OK) return PA_ERR_CUDA;
+    // fused: a group's members are the lanes of the producer warp
+    if (p.prefix_fused != 0 && (p.prefix_lens == nullptr || p.prefix_group > 32 || p.block_size % 16 != 0))
+        return PA_ERR_UNSUPPORTED;
+    auto kernel = p.prefix_fused != 0 ? prefill_tc_kernel<T, true> : prefill_tc_kernel<T, false>;
+    if (ensure_smem(kernel, C::kSmemBytes, smem_configured[p.prefix_fused != 0 ? 1 : 0]) != PA_OK)
+        return PA_ERR_CUDA;
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
@@ -965,7 +1133,7 @@ inline pa_status launch_prefill_tc_typed(const DecodeParams& p, const CUtensorMa
     const long long tiles = p.prefix_lens != nullptr ? p.num_seqs / p.prefix_group
                                                      : p.num_query_tokens / p.tile_tokens + p.num_seqs;
     const long long work =
-        tiles * p.head_tiles * (p.prefix_lens != nullptr ? p.prefix_parts : p.max_parts);
+        tiles * p.head_tiles * (p.prefix_fused != 0 ? 1 : p.prefix_lens != nullptr ? p.prefix_parts : p.max_parts);
     if (work > 0x7fffffffLL) return PA_ERR_UNSUPPORTED;
     long long grid = sms;
     if (grid > work) grid = work;

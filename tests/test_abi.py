@@ -5,6 +5,7 @@ import os
 import re
 
 import pytest
+import torch
 
 import paged_kv_cache_314_gb300 as pa
 from paged_kv_cache_314_gb300 import _build
@@ -97,6 +98,28 @@ def test_attention_plan_names_the_kernels(lib):
         pa.attention_plan(4, 3, 2, 64, 4, 16, 64, "f32")  # q heads not a multiple of kv heads
     with pytest.raises(pa.PaError):
         pa.attention_plan(4, 4, 4, 64, 4, 16, 64, "f32", partition_tokens=24)
+
+
+def test_shared_prefix_plan_without_a_device(lib):
+    """pa_shared_prefix_plan: shapes without a shared pass get the plain
+    decode's plan; shared shapes the separate passes (prefix, own, merge; E4M3
+    adds the widening) when no device can be asked for its SM count; invalid
+    groupings are refused."""
+    if torch.cuda.is_available():
+        pytest.skip("the fused pass depends on the device: covered by the GPU tests")
+    p = pa.shared_prefix_plan(256, 64, 8, 128, 81, 16, 6000, "bf16", 8)
+    assert (p["kernel"], p["merge"], p["launches"]) == ("tc_128_rows", "kernel", 3)
+    p = pa.shared_prefix_plan(256, 64, 8, 128, 81, 16, 6000, "bf16", 8, kv_dtype="e4m3")
+    assert (p["kernel"], p["merge"], p["launches"]) == ("tc_128_rows", "kernel", 4)
+    # MHA: no grouped heads, the plain decode
+    assert pa.shared_prefix_plan(64, 32, 32, 128, 128, 16, 5682, "f16", 8) == \
+        pa.attention_plan(64, 32, 32, 128, 128, 16, 5682, "f16")
+    # a group of one: the plain decode
+    assert pa.shared_prefix_plan(256, 64, 8, 128, 81, 16, 6000, "bf16", 1) == \
+        pa.attention_plan(256, 64, 8, 128, 81, 16, 6000, "bf16")
+    for bad_group in (0, 3):
+        with pytest.raises(pa.PaError):
+            pa.shared_prefix_plan(256, 64, 8, 128, 81, 16, 6000, "bf16", bad_group)
 
 
 def test_step_layout_and_host_checks(lib):

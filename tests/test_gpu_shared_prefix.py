@@ -192,3 +192,81 @@ def test_full_size_repeated_calls_and_stale_workspace():
             first = out.clone()
         else:
             assert torch.equal(out, first)
+
+
+# ---- the fused pass: one 128-row kernel pass per (group, kv head) reads the
+# prefix and then every member's own tokens (groups x kv heads >= the SM count,
+# contexts of at most 4096 tokens, at most 32 members)
+
+def _fused_groups(num_kv_heads, want=1):
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    return max(want, -(-sms // num_kv_heads))
+
+
+def _assert_fused(w, group):
+    plan = pa.shared_prefix_plan(w.num_seqs, w.num_q_heads, w.num_kv_heads, w.head_dim,
+                                 w.max_blocks_per_seq, w.block_size, w.num_blocks, w.dtype, group)
+    assert (plan["kernel"], plan["merge"], plan["launches"]) == ("tc_128_rows", "none", 1), plan
+
+
+FUSED_CASES = [
+    # dtype, Hq, Hkv, B, samples, prefix_len, max_suffix, groups (None: just enough)
+    ("bf16", 64, 8, 16, 8, 1024, 256, None),   # the named shape, fewer groups
+    ("f16", 32, 8, 16, 8, 300, 100, None),     # g = 4: 32 rows per group
+    ("bf16", 128, 8, 32, 8, 700, 64, None),    # g = 16: 128 rows, 32-token blocks
+    ("bf16", 64, 8, 128, 4, 1000, 300, None),  # 128-token blocks
+    ("f16", 64, 8, 16, 2, 2000, 900, None),    # 2 samples, contexts up to 2901 tokens
+    ("bf16", 16, 4, 16, 32, 200, 40, None),    # 32 members x 4 heads: one member per producer lane
+    ("bf16", 64, 8, 16, 2, 300, 300, 90),      # more groups than the static split takes
+]
+
+
+@pytest.mark.parametrize("case", range(len(FUSED_CASES)))
+def test_fused_pass(case):
+    """Every output of the fused pass against the oracle's plain decode, with
+    groups whose prefix is unusable (zero, not a block multiple, negative:
+    every token is then a member's own) and one shorter than the blocks
+    allow among the shared ones.  Up to 64 groups the items' stages are split
+    evenly over the CTAs (items cut in pieces, merged in the kernel); with
+    more, items are handed out whole."""
+    dtype, Hq, Hkv, B, n, pre_len, suf, groups = FUSED_CASES[case]
+    G = _fused_groups(Hkv, groups or 1)
+    w = wl.gqa_share(seed=600 + case, groups=G, samples=n, prefix_len=pre_len, max_suffix=suf,
+                     num_q_heads=Hq, num_kv_heads=Hkv, block_size=B, dtype=dtype)
+    _assert_fused(w, n)
+    shared = w.meta["shared_prefix_tokens"]
+    pre = [shared] * G
+    pre[1], pre[2], pre[3], pre[4] = 0, shared - 5, -B, max(0, shared - 3 * B)
+    stats, _ = _check(w, n, pre)
+    print("fused", FUSED_CASES[case], stats)
+
+
+def test_fused_pass_edge_cases():
+    """Fused pass: a member with no own tokens (context = prefix), one with a
+    single whole 16-token group, a group whose members hold only the prefix,
+    a member past the table (zero row, flagged: its group is decoded without
+    sharing), an empty member and a group of empty members (zero rows), a
+    member's own block id past the pool (its tokens skipped, flagged)."""
+    G = _fused_groups(8, 20)
+    w = wl.gqa_share(seed=640, groups=G, samples=8, prefix_len=512, max_suffix=200,
+                     num_q_heads=64, num_kv_heads=8)
+    shared = w.meta["shared_prefix_tokens"]
+    max_ctx = w.max_blocks_per_seq * w.block_size
+    ctx = w.context_lens
+    ctx[0], ctx[1] = shared, shared + 16
+    ctx[8 * 3:8 * 4] = shared
+    ctx[8 * 1 + 3] = max_ctx + 16
+    ctx[8 * 4 + 2] = 0
+    ctx[8 * 6:8 * 7] = 0
+    s_bad = next(s for s in range(16, 24) if ctx[s] >= shared + 40)  # group 2
+    w.block_tables[s_bad, shared // 16 + 1] = w.num_blocks + 7
+    pre = [shared] * G
+    pre[6] = 0
+    _assert_fused(w, 8)
+    out, d = _step(w, 8, pre)
+    _, _, ref, err = oracle_step(w)
+    assert err == oracle.ERR_CTX_OOB | oracle.ERR_BLOCK_OOB
+    assert int(d["d_err"].item()) == err
+    assert_close(out_f64(out), ref, w.dtype, "fused pass, edge cases")
+    for s in [8 + 3, 8 * 4 + 2] + list(range(8 * 6, 8 * 7)):
+        assert (out[s] == 0).all()
