@@ -1080,8 +1080,12 @@ __global__ void __launch_bounds__(PfTile<T>::kThreads, 1)
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
-    // a kernel launched after this one with programmatic stream serialisation
-    // (the shared-prefix own pass) may start on SMs this grid leaves
+    // Launched with programmatic stream serialisation: the set-up above may
+    // overlap the end of the previous kernel in the stream (the step's
+    // kv_write); nothing in global memory is read before it has completed.
+    wait_prior_grids();
+    // then a kernel launched after this one the same way (the shared-prefix
+    // own pass) may start on SMs this grid leaves
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     if (warp == 0)
@@ -1137,7 +1141,17 @@ inline pa_status launch_prefill_tc_typed(const DecodeParams& p, const CUtensorMa
     if (work > 0x7fffffffLL) return PA_ERR_UNSUPPORTED;
     long long grid = sms;
     if (grid > work) grid = work;
-    kernel<<<static_cast<unsigned>(grid), C::kThreads, C::kSmemBytes, stream>>>(p, mapK, mapV, mapQ);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(C::kThreads);
+    cfg.dynamicSmemBytes = C::kSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, kernel, p, mapK, mapV, mapQ) != cudaSuccess) return PA_ERR_CUDA;
     if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
     if (p.max_parts > 1) return launch_merge<T, C::D>(p, stream);
     return PA_OK;
