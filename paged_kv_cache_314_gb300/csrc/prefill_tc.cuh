@@ -78,7 +78,10 @@ struct PfTile {
     static constexpr int kSoftThreads = 32 * kSoftWarps;
     static constexpr int kRedOff = kBarOff + kNumBars * 8;    // row maxima / sums of the parts [kSplit][128]
     static constexpr int kMiscOff = kRedOff + kSplit * 128 * 4;  // tmem base, abort, group flags [2]
-    static constexpr int kSmemBytes = kMiscOff + 32 + 1024;  // + alignment slack
+    // two-stream tiles: the lower rows' O, half of it at a time [64 rows][2 parts][32], then m, L [64][2]
+    static constexpr int kXchOff = (kMiscOff + 32 + 15) / 16 * 16;
+    static constexpr int kXchBytes = 64 * 2 * 32 * 4 + 64 * 2 * 4;
+    static constexpr int kSmemBytes = kXchOff + kXchBytes + 1024;  // + alignment slack
     static constexpr int kCopyWarp = 2 + kSoftWarps;  // issues the V copies
     static constexpr int kThreads = 32 * (kCopyWarp + 1);
     static constexpr uint32_t kTmemCols = 512;  // S [2] x 128, O 128, P [2] x 64 (16-bit pairs)
@@ -180,6 +183,30 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float* v) {
         : "memory");
 }
 
+// 16 consecutive TMEM columns of this thread's lane (load and wait in one statement).
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, "
+        "[%16];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr)
+        : "memory");
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const float* v) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr),
+                 "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+                 "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+                 "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7]))
+                 : "memory");
+}
+
 // max(a, b, c) in one instruction (three-input max.f32, sm_100 family).
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
     float r;
@@ -200,11 +227,13 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const float* v) {
         : "memory");
 }
 
-// N = 16 or 32 consecutive TMEM columns of this thread's lane.
+// N = 8, 16 or 32 consecutive TMEM columns of this thread's lane.
 template <int N>
 __device__ __forceinline__ void tmem_st(uint32_t taddr, const float* v) {
-    static_assert(N == 16 || N == 32, "16 or 32 columns");
-    if constexpr (N == 16)
+    static_assert(N == 8 || N == 16 || N == 32, "8, 16 or 32 columns");
+    if constexpr (N == 8)
+        tmem_st8(taddr, v);
+    else if constexpr (N == 16)
         tmem_st16(taddr, v);
     else
         tmem_st32(taddr, v);
@@ -227,7 +256,7 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
 }  // namespace pf
 
 // ---- warp 0: work items, Q and K copies, stage meta, V plan ------------------
-template <typename T, bool kFused>
+template <typename T, bool kFused, bool kDual>
 __device__ __forceinline__ void pf_produce(const DecodeParams& p, const CUtensorMap* mapK,
                                            const CUtensorMap* mapQ, unsigned char* sm, uint32_t base) {
     using C = PfTile<T>;
@@ -251,7 +280,8 @@ __device__ __forceinline__ void pf_produce(const DecodeParams& p, const CUtensor
     const int P = p.partition_tokens, B = p.block_size, g = p.group;
     const int Tq = p.tile_tokens;  // query tokens per item: 128 / g (prefix pass: prefix_group)
     const int max_ctx = p.max_blocks_per_seq * B;
-    const uint32_t q_bytes = static_cast<uint32_t>(g * Tq) * 256u;  // both halves of the rows
+    // both halves of the rows (two-stream: twice, the second copy from row 64)
+    const uint32_t q_bytes = static_cast<uint32_t>(g * Tq) * 256u * (kDual ? 2u : 1u);
 
     // Cursor over the sequence-major item numbering: lane l holds sequence
     // win0 + l and its number of items.
@@ -351,9 +381,13 @@ __device__ __forceinline__ void pf_produce(const DecodeParams& p, const CUtensor
             // (rows past the sequence's queries are loaded too, never stored)
             const uint32_t qf = bar(C::kQFull + qs);
             mbar_arrive_expect_tx(qf, q_bytes);
-            for (int h = 0; h < 2; ++h)
+            for (int h = 0; h < 2; ++h) {
                 pf::tma_load_3d(base + C::kQOff + qs * C::kOpBytes + h * C::kHalf, mapQ, 64 * h, hq0,
                                 sq.q0 + i0, qf);
+                if (kDual)
+                    pf::tma_load_3d(base + C::kQOff + qs * C::kOpBytes + h * C::kHalf + 64 * 128, mapQ, 64 * h,
+                                    hq0, sq.q0 + i0, qf);
+            }
         }
         q_issued = item_seq + 1;
 
@@ -817,15 +851,22 @@ struct PfGroup {
 // divided by the row sum (or the partition's partial state).  The thread also
 // zeroes its share of V row `row` when token `row` holds no data, so
 // 0 x garbage never reaches O.
-template <typename T, bool kFused>
+template <typename T, bool kFused, bool kDual>
 __device__ __forceinline__ void pf_softmax(const DecodeParams& p, unsigned char* sm, uint32_t tmem) {
     using C = PfTile<T>;
-    constexpr int kCols = C::kCols, kSplit = C::kSplit;
-    static_assert(kCols == 32, "a thread's columns are two 16-token groups");
+    constexpr int kCols = C::kCols, kSplit = C::kSplit;  // O (head) columns of a thread
+    static_assert(kCols == 32, "a thread's S columns are two 16-token groups");
+    // S columns of a thread: the two-stream tile's rows 0-63 and 64-127 are the
+    // same query rows, the lower ones reading tokens 0-63 of each stage, the
+    // upper ones tokens 64-127 (one 16-token group per thread); their two
+    // states are merged at the item end
+    constexpr int kSC = kDual ? 16 : 32;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int tid = threadIdx.x - 64;  // 0 .. kSoftThreads-1
     const int part_i = (warp - 2) >> 2;  // columns kCols*part_i ..
     const int row = 32 * (warp & 3) + lane;
+    const int half = kDual ? row >> 6 : 0;     // two-stream: the stage's token half this row reads
+    const int qrow = kDual ? row & 63 : row;   // the item row (query token x head)
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::kBarOff);
     auto bar = [&](int i) { return smem_addr(bars + i); };
     const PfStageMeta* meta = reinterpret_cast<const PfStageMeta*>(sm + C::kMetaOff);
@@ -833,14 +874,25 @@ __device__ __forceinline__ void pf_softmax(const DecodeParams& p, unsigned char*
     float* red = reinterpret_cast<float*>(sm + C::kRedOff);  // [kSplit parts][128 rows]
     PfGroup grp{reinterpret_cast<volatile int*>(sm + C::kMiscOff + 8), tid, 0, C::kSoftThreads};
     const uint32_t lane_off = static_cast<uint32_t>(32 * (warp & 3)) << 16;
-    const uint32_t col0 = static_cast<uint32_t>(kCols * part_i);
+    const uint32_t col0 = static_cast<uint32_t>(kCols * part_i);  // of O
+    const uint32_t scol0 = kDual ? static_cast<uint32_t>(64 * half + 16 * part_i) : col0;  // of S
     const int g = p.group;
-    const int ti = row / g;  // query token of this row within the item
+    const int ti = qrow / g;  // query token of this row within the item
     const float kq = p.qk_scale_log2;
     // this thread's share of a V row: 16-byte chunks [vk0, vk0 + 8/(kSplit/2)) of
     // 64-column half vh (the two, or four, parts of a row cover all of it)
     constexpr int kChunks = 8 * 2 / kSplit;
     const int vh = (kCols * part_i) / 64, vk0 = ((kCols * part_i) % 64) / 8;
+
+    if constexpr (kDual) {
+        // the P columns of the other half's tokens stay zero in both buffers
+        // (each stage writes only its own half's): 8 of the row's 32 per part
+        const float z[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        const uint32_t lane_off0 = static_cast<uint32_t>(32 * (warp & 3)) << 16;
+        for (int b = 0; b < 2; ++b)
+            pf::tmem_st<8>(tmem + C::kPCol + 64u * b + 32u * (1 - half) + 8u * part_i + lane_off0, z);
+        pf::tmem_wait_st();
+    }
 
     float m_ref = -INFINITY, l = 0.f;  // l: this part's share of the row sum
     int row0 = 0, hq0 = 0, part = 0, nparts = 0, ntok = 0;  // the current item
@@ -894,16 +946,29 @@ __device__ __forceinline__ void pf_softmax(const DecodeParams& p, unsigned char*
 
         // ---- this part of the S row (S landed: waited for with the meta)
         tc::fence_after_sync();
-        float x[kCols];
-#pragma unroll
-        for (int k = 0; k < kCols / 32; ++k) pf::tmem_ld32(tmem + st * 128 + col0 + 32 * k + lane_off, x + 32 * k);
+        float x[kSC];
+        if constexpr (kDual)
+            pf::tmem_ld16(tmem + st * 128 + scol0 + lane_off, x);
+        else
+            pf::tmem_ld32(tmem + st * 128 + scol0 + lane_off, x);
         tc::fence_before_sync();
         mbar_arrive(bar(C::kSFree + st));  // every thread of the group (count kSoftThreads)
         float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
         // tokens of this thread's two 16-token groups (2 part_i, 2 part_i + 1)
         // that the row sees: a leading run of each
         int na, nb;
-        if (own) {  // the group's tokens if the row's query token is the group's member
+        if constexpr (kDual) {  // one group: 4 half + part_i
+            const int gi = 4 * half + part_i;
+            nb = 16;
+            if (own) {
+                const uint32_t cw = gi < 4 ? gc0 : gc1, ow = gi < 4 ? m.gown[0] : m.gown[1];
+                const int sh = 8 * (gi & 3);
+                na = static_cast<int>((ow >> sh) & 0xffu) == ti ? static_cast<int>((cw >> sh) & 0xffu) : 0;
+            } else {
+                const int lim = min(nvalid, m.lim_rel + ti);
+                na = ((groups >> gi) & 1u) ? max(0, min(16, lim - 16 * gi)) : 0;
+            }
+        } else if (own) {  // the group's tokens if the row's query token is the group's member
             const uint32_t cw = part_i < 2 ? gc0 : gc1;
             const uint32_t ow = part_i < 2 ? m.gown[0] : m.gown[1];
             const int sh = 16 * (part_i & 1);
@@ -920,12 +985,12 @@ __device__ __forceinline__ void pf_softmax(const DecodeParams& p, unsigned char*
         const bool unmasked = __all_sync(0xffffffffu, na == 16 && nb == 16) && kq > 0.f;
         if (unmasked) {
 #pragma unroll
-            for (int j = 0; j < kCols; j += 2) mx4[(j >> 1) & 3] = pf::fmax3(mx4[(j >> 1) & 3], x[j], x[j + 1]);
+            for (int j = 0; j < kSC; j += 2) mx4[(j >> 1) & 3] = pf::fmax3(mx4[(j >> 1) & 3], x[j], x[j + 1]);
 #pragma unroll
             for (int i = 0; i < 4; ++i) mx4[i] *= kq;
         } else {
 #pragma unroll
-            for (int j = 0; j < kCols; ++j) {
+            for (int j = 0; j < kSC; ++j) {
                 const bool ok = j < 16 ? j < na : j - 16 < nb;
                 x[j] = ok ? x[j] * kq : -INFINITY;
                 mx4[j & 3] = fmaxf(mx4[j & 3], x[j]);
@@ -979,16 +1044,16 @@ __device__ __forceinline__ void pf_softmax(const DecodeParams& p, unsigned char*
         const float ks = unmasked ? kq : 1.f;
         const float negm = m_ref != -INFINITY ? -m_ref : 0.f;
         float l4[4] = {0.f, 0.f, 0.f, 0.f};  // the row sum, of the weights before rounding
-        float pw[kCols / 2];  // this part of the row of P, 16-bit pairs (lower token in the low half)
+        float pw[kSC / 2];  // this part of the row of P, 16-bit pairs (lower token in the low half)
 #pragma unroll
-        for (int i = 0; i < kCols / 2; ++i) {
+        for (int i = 0; i < kSC / 2; ++i) {
             float e0 = negm, e1 = negm;
             fma2(e0, e1, x[2 * i], x[2 * i + 1], ks, ks);
             const float p0 = fast_exp2(e0), p1 = fast_exp2(e1);
             fma2(l4[2 * (i & 1)], l4[2 * (i & 1) + 1], p0, p1, 1.f, 1.f);
             pw[i] = __uint_as_float(pf::pack2<T>(p0, p1));
         }
-        pf::tmem_st<kCols / 2>(tmem + C::kPCol + 64u * (c & 1) + (kCols / 2) * part_i + lane_off, pw);
+        pf::tmem_st<kSC / 2>(tmem + C::kPCol + 64u * (c & 1) + scol0 / 2 + lane_off, pw);
         l += (l4[0] + l4[1]) + (l4[2] + l4[3]);
         if (kFused && !full) {
             // some token of the stage holds no data: once the stage's V has
@@ -1022,8 +1087,42 @@ __device__ __forceinline__ void pf_softmax(const DecodeParams& p, unsigned char*
         float L = 0.f;
 #pragma unroll
         for (int k = 0; k < kSplit; ++k) L += red[k * 128 + row];
-        if (row < ntok * g) {
-            const size_t rr = static_cast<size_t>(row0 + ti) * p.num_q_heads + hq0 + (row - ti * g);
+        if constexpr (kDual) {
+            // the upper rows' states (tokens 64-127 of each stage) into the
+            // lower rows' (tokens 0-63): O half a row at a time through shared memory
+            float* xo = reinterpret_cast<float*>(sm + C::kXchOff);  // [64 rows][2 parts][32]
+            float* xml = xo + 64 * 2 * 32;                           // [64 rows]: m, L
+            if (half == 1 && part_i == 0) {
+                xml[2 * qrow] = m_ref;
+                xml[2 * qrow + 1] = L;
+            }
+            for (int rd = 0; rd < 2; ++rd) {
+                float4* x4 = reinterpret_cast<float4*>(xo + (qrow * 2 + (part_i & 1)) * 32);
+                if (half == 1 && (part_i >> 1) == rd)
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) x4[k] = make_float4(o[4 * k], o[4 * k + 1], o[4 * k + 2], o[4 * k + 3]);
+                grp.sync();
+                if (half == 0 && (part_i >> 1) == rd) {
+                    const float mb = xml[2 * qrow], lb = xml[2 * qrow + 1];
+                    const float M = fmaxf(m_ref, mb);
+                    // a state without any token (reference -inf) weighs 0
+                    const float wa = m_ref == -INFINITY ? 0.f : fast_exp2(m_ref - M);
+                    const float wb = mb == -INFINITY ? 0.f : fast_exp2(mb - M);
+                    L = wa * L + wb * lb;
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) {
+                        const float4 v = x4[k];
+                        o[4 * k] = wa * o[4 * k] + wb * v.x;
+                        o[4 * k + 1] = wa * o[4 * k + 1] + wb * v.y;
+                        o[4 * k + 2] = wa * o[4 * k + 2] + wb * v.z;
+                        o[4 * k + 3] = wa * o[4 * k + 3] + wb * v.w;
+                    }
+                }
+                grp.sync();
+            }
+        }
+        if (half == 0 && qrow < ntok * g) {
+            const size_t rr = static_cast<size_t>(row0 + ti) * p.num_q_heads + hq0 + (qrow - ti * g);
             if (nparts <= 1) {
                 const float inv = (nparts == 1 && L > 0.f) ? 1.f / L : 0.f;
                 uint4* dst = reinterpret_cast<uint4*>(static_cast<T*>(p.out) + rr * C::D + col0);
@@ -1049,7 +1148,7 @@ __device__ __forceinline__ void pf_softmax(const DecodeParams& p, unsigned char*
     tc::fence_before_sync();
 }
 
-template <typename T, bool kFused>
+template <typename T, bool kFused, bool kDual>
 __global__ void __launch_bounds__(PfTile<T>::kThreads, 1)
     prefill_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap mapK,
                       const __grid_constant__ CUtensorMap mapV, const __grid_constant__ CUtensorMap mapQ) {
@@ -1089,11 +1188,11 @@ __global__ void __launch_bounds__(PfTile<T>::kThreads, 1)
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     if (warp == 0)
-        pf_produce<T, kFused>(p, &mapK, &mapQ, sm, base);
+        pf_produce<T, kFused, kDual>(p, &mapK, &mapQ, sm, base);
     else if (warp == 1)
         pf_mma<T>(p, sm, base, tmem);
     else if (warp < C::kCopyWarp)
-        pf_softmax<T, kFused>(p, sm, tmem);
+        pf_softmax<T, kFused, kDual>(p, sm, tmem);
     else
         pf_copy_v<T>(p, &mapV, sm, base);
 
@@ -1118,16 +1217,19 @@ inline pa_status launch_prefill_tc_typed(const DecodeParams& p, const CUtensorMa
                                          const CUtensorMap& mapV, const CUtensorMap& mapQ,
                                          cudaStream_t stream) {
     using C = PfTile<T>;
-    static std::atomic<uint64_t> smem_configured[2] = {{0}, {0}};  // per kernel: plain, fused
+    static std::atomic<uint64_t> smem_configured[3] = {{0}, {0}, {0}};  // per kernel: plain, fused, two-stream
     if (p.prefix_lens != nullptr ? p.group * p.tile_tokens > C::kRows
                                  : p.group * p.tile_tokens != C::kRows)
         return PA_ERR_UNSUPPORTED;
     // fused: a group's members are the lanes of the producer warp
     if (p.prefix_fused != 0 && (p.prefix_lens == nullptr || p.prefix_group > 32 || p.block_size % 16 != 0))
         return PA_ERR_UNSUPPORTED;
-    auto kernel = p.prefix_fused != 0 ? prefill_tc_kernel<T, true> : prefill_tc_kernel<T, false>;
-    if (ensure_smem(kernel, C::kSmemBytes, smem_configured[p.prefix_fused != 0 ? 1 : 0]) != PA_OK)
-        return PA_ERR_CUDA;
+    // fused with at most 64 rows per item (group x heads): the two-stream tile
+    const int mode = p.prefix_fused == 0 ? 0 : p.group * p.tile_tokens <= 64 ? 2 : 1;
+    auto kernel = mode == 0   ? prefill_tc_kernel<T, false, false>
+                  : mode == 1 ? prefill_tc_kernel<T, true, false>
+                              : prefill_tc_kernel<T, true, true>;
+    if (ensure_smem(kernel, C::kSmemBytes, smem_configured[mode]) != PA_OK) return PA_ERR_CUDA;
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
