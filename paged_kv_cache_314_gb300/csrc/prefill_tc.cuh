@@ -255,6 +255,21 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
 
 }  // namespace pf
 
+// Fused shared-prefix pass: the stages of an item of group grp (the same for
+// each kv head) -- its usable prefix (returned in pre) in 128-token stages,
+// then its members' own tokens in 16-token groups (a member's run padded to
+// whole groups; a member whose context is out of range has none), 8 groups a
+// stage, at least one stage -- the count the producer's walk below makes.
+__device__ __forceinline__ int fused_group_stages(const DecodeParams& p, int grp, int max_ctx, int& pre) {
+    pre = group_prefix(p, grp);
+    int own = 0;
+    for (int j = 0; j < p.prefix_group; ++j) {
+        const int c = __ldg(p.context_lens + grp * p.prefix_group + j);
+        if (c >= pre && c <= max_ctx) own += (c - pre + 15) >> 4;
+    }
+    return max(1, (pre + 127) / 128 + (own + 7) / 8);
+}
+
 // ---- warp 0: work items, Q and K copies, stage meta, V plan ------------------
 template <typename T, bool kFused, bool kDual>
 __device__ __forceinline__ void pf_produce(const DecodeParams& p, const CUtensorMap* mapK,
@@ -300,7 +315,25 @@ __device__ __forceinline__ void pf_produce(const DecodeParams& p, const CUtensor
         items_lane = sl < S ? seq_items(sq_lane, p, max_ctx) : 0;
         if (sl < S && !sq_lane.rows_ok(p.num_query_tokens)) report(p.d_err, PA_DERR_CTX_OOB);
     };
-    load_window();
+    // Fused, at most 64 groups: items handed out longest first.  Lane l holds
+    // the rank of groups l and l + 32 by stages per item (more first, then the
+    // lower group) and their usable prefixes; item i is kv head i % kv heads
+    // of the group ranked i / kv heads.
+    const bool lpt = kFused && S <= 64;
+    int rank_lo = 64, rank_hi = 64, pre_lo = 0, pre_hi = 0;
+    if (lpt) {
+        const int n_lo = lane < S ? fused_group_stages(p, lane, max_ctx, pre_lo) : -1;
+        const int n_hi = lane + 32 < S ? fused_group_stages(p, lane + 32, max_ctx, pre_hi) : -1;
+        rank_lo = 0;
+        rank_hi = 0;
+        for (int j = 0; j < 32; ++j) {
+            const int a = __shfl_sync(0xffffffffu, n_lo, j), b = __shfl_sync(0xffffffffu, n_hi, j);
+            rank_lo += (a > n_lo || (a == n_lo && j < lane)) + (b > n_lo);
+            rank_hi += (a >= n_hi) + (b > n_hi || (b == n_hi && j < lane));
+        }
+    } else {
+        load_window();
+    }
     int c = 0, item_seq = 0, q_issued = 0;
     bool aborted = false, oob = false;
     int item_id = 0;
@@ -310,6 +343,19 @@ __device__ __forceinline__ void pf_produce(const DecodeParams& p, const CUtensor
     while (!aborted) {
         int s, i_loc, next_id = 0;
         SeqQueries sq;
+        if (lpt) {
+            const int H = p.head_tiles;
+            if (item_id >= S * H) break;
+            const int R = item_id / H;
+            const unsigned blo = __ballot_sync(0xffffffffu, rank_lo == R);
+            const unsigned bhi = __ballot_sync(0xffffffffu, rank_hi == R);
+            const int L = __ffs(blo != 0 ? blo : bhi) - 1;
+            s = blo != 0 ? L : L + 32;
+            const int pre = __shfl_sync(0xffffffffu, blo != 0 ? pre_lo : pre_hi, L);
+            sq = SeqQueries{pre, s * p.prefix_group, s * p.prefix_group + p.prefix_group, true};
+            i_loc = item_id - R * H;
+            if (lane == 0) next_id = static_cast<int>(atomicAdd(p.counters, 1u));
+        } else {
         bool found = false;
         while (s_cur < S) {
             if (s_cur - win0 >= 32) {
@@ -349,6 +395,7 @@ __device__ __forceinline__ void pf_produce(const DecodeParams& p, const CUtensor
             // only reachable when query_start is not ascending (item counts can overflow)
             if (lane == 0) report(p.d_err, PA_DERR_CTX_OOB);
             break;
+        }
         }
         const int ctx = sq.ctx;
         const bool valid = prefix || sq.ctx_ok(max_ctx);
