@@ -1043,29 +1043,36 @@ __device__ __forceinline__ void pf_softmax(const DecodeParams& p, unsigned char*
                 mx4[j & 3] = fmaxf(mx4[j & 3], x[j]);
             }
         }
-        red[part_i * 128 + row] = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
-        grp.sync();
-        float mx = red[row];
-#pragma unroll
-        for (int k = 1; k < kSplit; ++k) mx = fmaxf(mx, red[k * 128 + row]);
-        const float m_new = fmaxf(m_ref, mx);
-        const bool resc = m_new > m_ref + 8.f;  // also from -inf to a first finite maximum
-        float alpha = 1.f;
-        if (resc) {
-            alpha = fast_exp2(m_ref - m_new);  // 0 from -inf
-            m_ref = m_new;
-            l *= alpha;
-        }
-
-        // ---- P buffer c % 2 may be rewritten once MMA2 of stage c-2 completed;
-        // the same group barrier tells whether any row raised its maximum
+        // The row's reference m_ref is raised only when some part of the row
+        // exceeds it by more than 8 (log2 units; also from -inf to a first
+        // finite maximum): one group vote, carried by the wait for the P buffer
+        // (free once MMA2 of stage c-2 completed), and the parts' maxima are
+        // exchanged only when some row needs it.
+        const float mxl = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+        const bool need = mxl > m_ref + 8.f;
         bool any_resc = false;
         if (c >= 2) {
-            if (!grp.wait_any(bar(C::kPFree + (c & 1)), static_cast<uint32_t>((c >> 1) - 1) & 1, resc, &any_resc,
+            if (!grp.wait_any(bar(C::kPFree + (c & 1)), static_cast<uint32_t>((c >> 1) - 1) & 1, need, &any_resc,
                               p.d_err, abort_flag))
                 break;
         } else {
-            any_resc = grp.any(resc);
+            any_resc = grp.any(need);
+        }
+        bool resc = false;
+        float alpha = 1.f;
+        if (any_resc) {
+            red[part_i * 128 + row] = mxl;
+            grp.sync();
+            float mx = red[row];
+#pragma unroll
+            for (int k = 1; k < kSplit; ++k) mx = fmaxf(mx, red[k * 128 + row]);
+            const float m_new = fmaxf(m_ref, mx);
+            resc = m_new > m_ref + 8.f;
+            if (resc) {
+                alpha = fast_exp2(m_ref - m_new);  // 0 from -inf
+                m_ref = m_new;
+                l *= alpha;
+            }
         }
         // O may be rescaled once MMA2 of stage c-1 completed
         if (!(flags & kStageFirst) && any_resc) {
