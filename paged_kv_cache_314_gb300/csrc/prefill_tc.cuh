@@ -1045,19 +1045,15 @@ __device__ __forceinline__ void pf_softmax(const DecodeParams& p, unsigned char*
         }
         // The row's reference m_ref is raised only when some part of the row
         // exceeds it by more than 8 (log2 units; also from -inf to a first
-        // finite maximum): one group vote, carried by the wait for the P buffer
-        // (free once MMA2 of stage c-2 completed), and the parts' maxima are
-        // exchanged only when some row needs it.
+        // finite maximum): one group vote, and the parts' maxima are exchanged
+        // only when some row needs it.  P buffer c % 2 needs no wait: S of
+        // stage c was committed after MMA2 of stage c-2 was issued (the MMA
+        // warp never runs MMA1 more than one stage ahead of MMA2, and commits
+        // from the same thread), so its completion, waited for above, covers
+        // that MMA2's.
         const float mxl = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
         const bool need = mxl > m_ref + 8.f;
-        bool any_resc = false;
-        if (c >= 2) {
-            if (!grp.wait_any(bar(C::kPFree + (c & 1)), static_cast<uint32_t>((c >> 1) - 1) & 1, need, &any_resc,
-                              p.d_err, abort_flag))
-                break;
-        } else {
-            any_resc = grp.any(need);
-        }
+        const bool any_resc = grp.any(need);
         bool resc = false;
         float alpha = 1.f;
         if (any_resc) {
