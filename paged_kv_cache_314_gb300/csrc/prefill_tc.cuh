@@ -999,7 +999,8 @@ __device__ __forceinline__ void pf_softmax(const DecodeParams& p, unsigned char*
         else
             pf::tmem_ld32(tmem + st * 128 + scol0 + lane_off, x);
         tc::fence_before_sync();
-        mbar_arrive(bar(C::kSFree + st));  // every thread of the group (count kSoftThreads)
+        __syncwarp();  // the warp's loads (collective, waited for) are done
+        if (lane == 0) mbar_arrive(bar(C::kSFree + st));  // one of the kSoftWarps arrivals
         float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
         // tokens of this thread's two 16-token groups (2 part_i, 2 part_i + 1)
         // that the row sees: a leading run of each
@@ -1213,10 +1214,9 @@ __global__ void __launch_bounds__(PfTile<T>::kThreads, 1)
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < C::kNumBars; ++i) {
-            // s_free is signalled by every softmax thread, p_full by every softmax warp
-            const bool all = i == C::kSFree || i == C::kSFree + 1;
-            const bool warps = i == C::kPFull || i == C::kPFull + 1;
-            mbar_init(smem_addr(bars + i), all ? C::kSoftThreads : warps ? C::kSoftWarps : 1);
+            // s_free and p_full are signalled by every softmax warp
+            const bool warps = i == C::kSFree || i == C::kSFree + 1 || i == C::kPFull || i == C::kPFull + 1;
+            mbar_init(smem_addr(bars + i), warps ? C::kSoftWarps : 1);
         }
         *reinterpret_cast<volatile int*>(sm + C::kMiscOff + 4) = 0;
         fence_barrier_init();
