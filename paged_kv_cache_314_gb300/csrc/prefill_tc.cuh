@@ -827,13 +827,11 @@ __device__ __forceinline__ void pf_mma(const DecodeParams& p, unsigned char* sm,
     __syncwarp();
 }
 
-// The softmax warps agree on every wait: thread 0 waits (bounded), the
-// outcome goes through one of two alternating shared flags and the group's
-// named barrier, so no thread can stay behind at a later barrier.
+// The softmax warps agree on every wait: thread 0 waits (bounded) and the
+// outcome is the OR the group's named barrier reduces, so no thread can stay
+// behind at a later barrier.
 struct PfGroup {
-    volatile int* flags;  // [2]
     int tid;
-    int k = 0;
     int nthreads;
     __device__ __forceinline__ void sync() const { named_barrier(1, nthreads); }
     // sync() that also tells whether the predicate holds for any thread of the group
@@ -847,43 +845,34 @@ struct PfGroup {
             : "memory");
         return r != 0;
     }
+    // Thread 0 waits (bounded); the group barrier's OR carries whether it gave up.
     __device__ __forceinline__ bool wait(uint32_t bar, uint32_t parity, uint32_t* d_err,
                                          volatile int* abort_flag) {
-        bool unused;
-        return wait_any(bar, parity, false, &unused, d_err, abort_flag);
-    }
-    // wait() whose barrier also ORs `pred` over the group into *any.
-    __device__ __forceinline__ bool wait_any(uint32_t bar, uint32_t parity, bool pred, bool* any,
-                                             uint32_t* d_err, volatile int* abort_flag) {
-        const int slot = k++ & 1;
+        bool ok = true;
         if (tid == 0) {
-            const bool ok = mbar_wait(bar, parity);
+            ok = mbar_wait(bar, parity);
             if (!ok) {
                 report(d_err, PA_DERR_TIMEOUT);
                 *abort_flag = 1;
             }
-            flags[slot] = ok ? 1 : 0;
         }
-        *any = this->any(pred);
-        return flags[slot] != 0;
+        return !any(!ok);
     }
     // wait() for a stage's meta barrier and then, unless the meta it guards
     // is the end marker, for its S: one group barrier for both.
     __device__ __forceinline__ bool wait_stage(uint32_t bar, uint32_t parity, const uint32_t* meta_flags,
                                                uint32_t bar2, uint32_t parity2, uint32_t* d_err,
                                                volatile int* abort_flag) {
-        const int slot = k++ & 1;
+        bool ok = true;
         if (tid == 0) {
-            bool ok = mbar_wait(bar, parity);
+            ok = mbar_wait(bar, parity);
             if (ok && !(*meta_flags & kStageEnd)) ok = mbar_wait(bar2, parity2);
             if (!ok) {
                 report(d_err, PA_DERR_TIMEOUT);
                 *abort_flag = 1;
             }
-            flags[slot] = ok ? 1 : 0;
         }
-        sync();
-        return flags[slot] != 0;
+        return !any(!ok);
     }
 };
 
@@ -919,7 +908,7 @@ __device__ __forceinline__ void pf_softmax(const DecodeParams& p, unsigned char*
     const PfStageMeta* meta = reinterpret_cast<const PfStageMeta*>(sm + C::kMetaOff);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + C::kMiscOff + 4);
     float* red = reinterpret_cast<float*>(sm + C::kRedOff);  // [kSplit parts][128 rows]
-    PfGroup grp{reinterpret_cast<volatile int*>(sm + C::kMiscOff + 8), tid, 0, C::kSoftThreads};
+    PfGroup grp{tid, C::kSoftThreads};
     const uint32_t lane_off = static_cast<uint32_t>(32 * (warp & 3)) << 16;
     const uint32_t col0 = static_cast<uint32_t>(kCols * part_i);  // of O
     const uint32_t scol0 = kDual ? static_cast<uint32_t>(64 * half + 16 * part_i) : col0;  // of S
