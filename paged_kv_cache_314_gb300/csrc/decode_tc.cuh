@@ -637,24 +637,30 @@ __device__ __forceinline__ void tc_mma(const DecodeParams& p, unsigned char* sm,
 // the outcome goes through one of two alternating shared flags and the team's
 // named barrier, so no team thread can stay behind at a later barrier.
 struct TeamSync {
-    volatile int* flags;  // [2]
+    volatile int* flags;  // (unused: the outcome rides on the barrier)
     int tid;
     int barrier_id;
     int k = 0;
     __device__ __forceinline__ void sync() const { named_barrier(barrier_id, 128); }
+    // Thread 0 waits (bounded); the team's barrier ORs whether it gave up.
     __device__ __forceinline__ bool wait(uint32_t bar, uint32_t parity, uint32_t* d_err,
                                          volatile int* abort_flag) {
-        const int slot = k++ & 1;
+        bool ok = true;
         if (tid == 0) {
-            const bool ok = mbar_wait(bar, parity);
+            ok = mbar_wait(bar, parity);
             if (!ok) {
                 report(d_err, PA_DERR_TIMEOUT);
                 *abort_flag = 1;
             }
-            flags[slot] = ok ? 1 : 0;
         }
-        sync();
-        return flags[slot] != 0;
+        uint32_t r;
+        asm volatile(
+            "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.or.pred q, %2, 128, p;\n\t"
+            "selp.u32 %0, 1, 0, q;\n\t}"
+            : "=r"(r)
+            : "r"(ok ? 0u : 1u), "r"(barrier_id)
+            : "memory");
+        return r == 0;
     }
 };
 
