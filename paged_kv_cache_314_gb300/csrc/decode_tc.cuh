@@ -88,7 +88,7 @@ struct TcTile {
     static constexpr int kConvBar = kKPlanBar + kStages;
     static constexpr int kConvVBar = kConvBar + kStages;
     static constexpr int kNumBars = kConvVBar + kStages;
-    static constexpr int kMiscOff = kBarOff + kNumBars * 8;  // tmem base, abort, team and converter flags
+    static constexpr int kMiscOff = kBarOff + kNumBars * 8;  // tmem base, abort
     static constexpr int kSmemBytes = kMiscOff + 32 + 1024;       // + alignment slack
     // producer, MMA, two teams of 4 warps, three copy warps: the 16 TMA boxes of a
     // stage are issued by four warps (the producer and warps 10-12, 4 boxes each),
@@ -633,14 +633,12 @@ __device__ __forceinline__ void tc_mma(const DecodeParams& p, unsigned char* sm,
     __syncwarp();
 }
 
-// The four warps of a team agree on every wait: thread 0 waits (bounded),
-// the outcome goes through one of two alternating shared flags and the team's
-// named barrier, so no team thread can stay behind at a later barrier.
+// The four warps of a team agree on every wait: thread 0 waits (bounded) and
+// the outcome is the OR the team's named barrier reduces, so no team thread
+// can stay behind at a later barrier.
 struct TeamSync {
-    volatile int* flags;  // (unused: the outcome rides on the barrier)
     int tid;
     int barrier_id;
-    int k = 0;
     __device__ __forceinline__ void sync() const { named_barrier(barrier_id, 128); }
     // Thread 0 waits (bounded); the team's barrier ORs whether it gave up.
     __device__ __forceinline__ bool wait(uint32_t bar, uint32_t parity, uint32_t* d_err,
@@ -729,8 +727,7 @@ __device__ __forceinline__ void tc_team(const DecodeParams& p, unsigned char* sm
     const TcItemRec* recs = reinterpret_cast<const TcItemRec*>(sm + C::kRecOff);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + C::kMiscOff + 4);
     float* red = reinterpret_cast<float*>(sm + C::kRedOff);  // [4][16]: [quadrant][head]
-    TeamSync team{reinterpret_cast<volatile int*>(sm + C::kMiscOff + 8 + 8 * team_id), tid,
-                  1 + team_id};
+    TeamSync team{tid, 1 + team_id};
     const uint32_t lane_off = static_cast<uint32_t>(32 * quad) << 16;
     const int g = p.group;
 
@@ -903,7 +900,7 @@ __device__ __forceinline__ void tc_convert(const DecodeParams& p, unsigned char*
     const uint32_t conv0 = smem_addr(bars + C::kConvBar), convV0 = smem_addr(bars + C::kConvVBar);
     const TcStageMeta* meta = reinterpret_cast<const TcStageMeta*>(sm + C::kMetaOff);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + C::kMiscOff + 4);
-    TeamSync grp{reinterpret_cast<volatile int*>(sm + C::kMiscOff + 24), row, 3};
+    TeamSync grp{row, 3};
 
     auto widen = [&](int sl, int which) {  // which: 0 = K, 1 = V
         const int nv = meta[sl].nvalid;

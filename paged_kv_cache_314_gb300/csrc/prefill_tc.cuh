@@ -77,7 +77,7 @@ struct PfTile {
     static constexpr int kSoftWarps = 4 * kSplit;
     static constexpr int kSoftThreads = 32 * kSoftWarps;
     static constexpr int kRedOff = kBarOff + kNumBars * 8;    // row maxima / sums of the parts [kSplit][128]
-    static constexpr int kMiscOff = kRedOff + kSplit * 128 * 4;  // tmem base, abort, group flags [2]
+    static constexpr int kMiscOff = kRedOff + kSplit * 128 * 4;  // tmem base, abort
     // two-stream tiles: the lower rows' O, half of it at a time [64 rows][2 parts][32], then m, L [64][2]
     static constexpr int kXchOff = (kMiscOff + 32 + 15) / 16 * 16;
     static constexpr int kXchBytes = 64 * 2 * 32 * 4 + 64 * 2 * 4;
