@@ -12,7 +12,7 @@
 // its causal span of the table, one 128-token K/V stage at a time:
 //
 //   S = Q . K^T   (tcgen05.mma, M = 128 rows, N = 128 tokens, fp32 in TMEM)
-//   P = 2^(S * scale * log2 e - m)     two threads per row, from TMEM, rounded
+//   P = 2^(S * scale * log2 e - m)     four threads per row, from TMEM, rounded
 //                                      to the 16-bit type back into TMEM
 //   O += P . V    (M = 128 rows, N = 128 head dimensions, fp32 in TMEM; P is
 //                  the A operand read from TMEM)
@@ -21,17 +21,27 @@
 // exceeds it by more than 2^8 (then O in TMEM and the row sum are rescaled;
 // the weights stay <= 2^8, exact in fp32 and far inside the 16-bit range).
 //
+// The same kernel serves shared-prefix decode ("PagedAttention"
+// (compassingai.com) §6: blocks shared by the sequences of a group): in prefix
+// mode an item is a group's sequences x the heads of a kv head against the
+// group's shared prefix (partial states merged with each sequence's own pass);
+// in the fused forms an item also walks every member's own tokens, packed
+// 16-token groups at a time with each group's member in the stage record, and
+// writes the final rows.  Items of at most 64 rows run two-stream: the rows
+// are loaded twice and the upper copy reads the other half of every stage.
+//
 // Warps: 0 walks the work items and issues the Q and K copies, 1 issues the
 // MMAs (one elected lane) and owns TMEM, 2-17 are the softmax warps (four
 // threads per query row, one per 32-column quarter; warp w reads TMEM lanes
 // 32*(w%4)..), 18 issues the V copies from a per-stage plan once the V half
 // of the slot is free.  Shared memory: a 2-stage K/V ring (the K and V halves
 // of a slot released separately), two Q slots.  TMEM: two S buffers, O, two P
-// buffers (stage c in buffer c % 2), so the softmax of stage c waits for P.V
-// of stage c-2, not c-1, unless O must be rescaled.  The softmax warps
-// take each stage's record from its own barrier and wait for the stage's V
-// only when some of its rows must be zeroed, so a stage's softmax never
-// waits on its V copies; the MMA warp waits for them before P.V.
+// buffers (stage c in buffer c % 2): S of stage c is committed after P.V of
+// stage c-2 was issued, so P buffer c % 2 is free once S is there, and the
+// softmax of stage c waits for P.V of stage c-1 only when O must be rescaled.
+// The softmax warps take each stage's record from its own barrier and wait for
+// the stage's V only when some of its rows must be zeroed; the MMA warp waits
+// for it before P.V.
 #pragma once
 
 #include <stdint.h>
@@ -880,11 +890,12 @@ struct PfGroup {
 // Warp w handles rows 32*(w%4).. (its TMEM lane quadrant) and the kCols
 // columns (K/V tokens of the stage; head dimensions of O) of part (w-2)/4.
 // Per stage: its part of the row of S from TMEM, the causal and validity
-// mask, the row maximum (the parts exchange theirs through shared memory), the
-// running maximum (raised only past +8 in the log2 domain, then its part of O
-// and the row sum rescaled), P (rounded to T) into the kCols/2 TMEM columns of
-// its part of P buffer c % 2; at an item's last stage its part of the row of O
-// divided by the row sum (or the partition's partial state).  The thread also
+// mask, its part's maximum and one group vote on whether any row must raise
+// its running maximum (past +8 in the log2 domain; then the parts exchange
+// their maxima through shared memory and O and the row sum are rescaled), P
+// (rounded to T) into its TMEM columns of P buffer c % 2; at an item's last
+// stage its part of the row of O divided by the row sum (or the partition's
+// partial state).  The thread also
 // zeroes its share of V row `row` when token `row` holds no data, so
 // 0 x garbage never reaches O.
 template <typename T, bool kFused, bool kDual>
