@@ -401,18 +401,24 @@ pa_status pa_decode_fp8(void* out, const void* q, pa_dtype q_dtype, const void* 
  * share prefix blocks ("PagedAttention" (compassingai.com) §6; the wmrh.cn
  * tutorial's part on sharing KV blocks), as pa_decode_shared_prefix does for
  * 16-bit caches: group_size, prefix_lens and the rule for a usable prefix are
- * the same.  Each usable prefix is first widened once into the workspace, each
- * element code x scale rounded once to q_dtype (so a prefix token's K and V
- * carry one rounding to q's type that pa_decode_fp8 does not make); the 128-row
- * tensor-core kernel then reads it once per group and kv head, the E4M3
- * grouped kernel reads each sequence's own tokens, and the partial states are
- * merged.  Shapes the shared pass does not cover (not 4-16 query heads per kv
- * head, group_size * heads per kv head over 128, a group of one) run
- * pa_decode_fp8 itself.  Workspace: pa_decode_shared_prefix_fp8_workspace_size()
- * bytes (the partial states, two scratch pools of num_seqs / group_size x
- * max_blocks_per_seq blocks in q_dtype and a [num_seqs][max_blocks_per_seq]
- * int32 table), 256-byte aligned, its first 256 bytes zero before the first
- * call and left zero.  Kernels: 4 (widen, prefix pass, own pass, merge).
+ * the same.  When the groups x kv heads are at least the device's SM count,
+ * group_size <= 32 and max_blocks_per_seq x block_size <= 4096, one pass of
+ * the 128-row tensor-core kernel takes, per (group, kv head), the prefix and
+ * then the members' own tokens, widening each stage's codes in shared memory
+ * (every element code x scale rounded once to q_dtype, a rounding that
+ * pa_decode_fp8 does not make), and writes the final rows: 1 kernel.
+ * Otherwise each usable prefix is first widened once into the workspace (the
+ * same rounding), the 128-row kernel reads it once per group and kv head, the
+ * E4M3 grouped kernel reads each sequence's own tokens (fp32 scales, no
+ * rounding), and the partial states are merged: 4 kernels.
+ * pa_shared_prefix_plan() tells which.  Shapes the shared pass does not cover
+ * (not 4-16 query heads per kv head, group_size * heads per kv head over 128,
+ * a group of one) run pa_decode_fp8 itself.  Workspace:
+ * pa_decode_shared_prefix_fp8_workspace_size() bytes (the partial states, two
+ * scratch pools of num_seqs / group_size x max_blocks_per_seq blocks in
+ * q_dtype and a [num_seqs][max_blocks_per_seq] int32 table; the fused pass
+ * uses only the first 256 bytes), 256-byte aligned, its first 256 bytes zero
+ * before the first call and left zero.
  */
 size_t pa_decode_shared_prefix_fp8_workspace_size(int num_seqs, int num_q_heads,
                                                   int num_kv_heads, int head_dim,

@@ -987,6 +987,16 @@ extern "C" pa_status pa_decode_shared_prefix_fp8(
     p.prefix_parts = L.pl.prefix_parts;
     p.skip_merge = 1;
     const cudaStream_t st = as_cuda(stream);
+    if (prefix_fused_ok(num_seqs / group_size, num_kv_heads,
+                        static_cast<long long>(max_blocks_per_seq) * block_size, group_size)) {
+        // one pass over the E4M3 cache: per (group, kv head) the prefix, then the
+        // members' own tokens, each stage's codes widened in shared memory
+        DecodeParams pf = p;
+        pf.tile_tokens = group_size;
+        pf.prefix_fused = 1;
+        return q_dtype == PA_BF16 ? launch_prefill_tc_fp8_bf16(pf, map_k8, map_v8, map_q, st)
+                                  : launch_prefill_tc_fp8_f16(pf, map_k8, map_v8, map_q, st);
+    }
     int32_t* table = reinterpret_cast<int32_t*>(wsb + L.table_off);
     // 1. each usable group prefix, widened once to q's type
     pa_status r = launch_prefix_widen(p, q_dtype, wsb + L.k_off, wsb + L.v_off, table, st);
@@ -1042,7 +1052,7 @@ extern "C" pa_status pa_shared_prefix_plan(int num_seqs, int num_q_heads, int nu
     if (!shared) return PA_OK;  // the call is the plain decode
     const long long max_ctx = static_cast<long long>(max_blocks_per_seq) * block_size;
     plan->kernel = PA_KERNEL_TC_128_ROWS;  // the first kernel reading the cache
-    if (!fp8 && prefix_fused_ok(num_seqs / group_size, num_kv_heads, max_ctx, group_size)) {
+    if (prefix_fused_ok(num_seqs / group_size, num_kv_heads, max_ctx, group_size)) {
         plan->partition_tokens = static_cast<int>(max_ctx);
         plan->max_parts = 1;
         plan->merge = PA_MERGE_NONE;

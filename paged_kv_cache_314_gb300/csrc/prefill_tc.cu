@@ -5,10 +5,10 @@
 namespace pa {
 pa_status launch_prefill_tc_f16(const DecodeParams& p, const CUtensorMap& mapK, const CUtensorMap& mapV,
                                 const CUtensorMap& mapQ, cudaStream_t stream) {
-    return launch_prefill_tc_typed<__half>(p, mapK, mapV, mapQ, stream);
+    return launch_prefill_tc_typed<__half, false>(p, mapK, mapV, mapQ, stream);
 }
 pa_status launch_prefill_tc_bf16(const DecodeParams& p, const CUtensorMap& mapK, const CUtensorMap& mapV,
                                  const CUtensorMap& mapQ, cudaStream_t stream) {
-    return launch_prefill_tc_typed<__nv_bfloat16>(p, mapK, mapV, mapQ, stream);
+    return launch_prefill_tc_typed<__nv_bfloat16, false>(p, mapK, mapV, mapQ, stream);
 }
 }  // namespace pa

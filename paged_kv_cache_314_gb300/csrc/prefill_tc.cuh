@@ -77,10 +77,11 @@ struct PfTile {
     static constexpr int kPlanStop = 8;
     static constexpr int kPlanBytes = 9;
     static constexpr int kBarOff = kPlanOff + kMetaSlots * kPlanInts * 4;
-    // barriers (indices): per ring slot, S or P buffer [2], per meta slot [8]
+    // barriers (indices): per ring slot, S or P buffer [2], per meta slot [8];
+    // E4M3 caches: a slot's K widened in place (convK, two warps)
     static constexpr int kFullK = 0, kEmptyK = 2, kFullV = 4, kEmptyV = 6, kVPlan = 8, kMetaFull = 16;
     static constexpr int kQFull = 24, kQEmpty = 26, kSFull = 28, kSFree = 30;
-    static constexpr int kPFull = 32, kPFree = 34, kDrain = 36, kNumBars = 37;
+    static constexpr int kPFull = 32, kPFree = 34, kDrain = 36, kConvK = 37, kNumBars = 39;
     // softmax: kSplit threads per query row, each on kCols columns of S (and of O)
     static constexpr int kSplit = 4;
     static constexpr int kCols = 128 / kSplit;
@@ -94,6 +95,12 @@ struct PfTile {
     static constexpr int kSmemBytes = kXchOff + kXchBytes + 1024;  // + alignment slack
     static constexpr int kCopyWarp = 2 + kSoftWarps;  // issues the V copies
     static constexpr int kThreads = 32 * (kCopyWarp + 1);
+    // E4M3 caches (the fused pass): warp kCopyWarp + 1 and the copy warp widen K
+    // (rows 0-63 and 64-127), the softmax warps V
+    static constexpr int kThreadsFp8 = 32 * (kCopyWarp + 2);
+    // tile layouts: 16-bit [16 blocks of 8 rows][2 halves of 64 columns][8 rows][128 B];
+    // E4M3 (widened in place) [2 halves][128 rows][128 B]
+    static constexpr int kHalfFp8 = kTileBytes / 2;
     static constexpr uint32_t kTmemCols = 512;  // S [2] x 128, O 128, P [2] x 64 (16-bit pairs)
     static constexpr uint32_t kOCol = 256;
     static constexpr uint32_t kPCol = 384;
@@ -143,6 +150,15 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst_smem, const CUtensorMap
         "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
         " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst_smem),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
+        : "memory");
+}
+
+// [16 rows x 128 B] of E4M3 codes (a 16-token group) from row c1 of the byte map.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst_smem, const CUtensorMap* map, int c1, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst_smem),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(c1), "r"(bar)
         : "memory");
 }
 
@@ -263,6 +279,17 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
     }
 }
 
+// Two E4M3 codes (the lower address in the low half-word) times sc, each
+// rounded once to T, packed: the code pair exact in binary16 (the hardware
+// conversion), then the product in fp32.
+template <typename T>
+__device__ __forceinline__ uint32_t widen_pair(uint32_t two_codes, float sc) {
+    const __half2_raw hr =
+        __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two_codes & 0xffffu), __NV_E4M3);
+    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&hr));
+    return pack2<T>(f.x * sc, f.y * sc);
+}
+
 }  // namespace pf
 
 // Fused shared-prefix pass: the stages of an item of group grp (the same for
@@ -281,7 +308,9 @@ __device__ __forceinline__ int fused_group_stages(const DecodeParams& p, int grp
 }
 
 // ---- warp 0: work items, Q and K copies, stage meta, V plan ------------------
-template <typename T, bool kFused, bool kDual>
+// kFp8: each 16-token group's K codes land row-major in the upper half of the
+// stage's K tile (one [16 x 128 B] box), for the K converter warp.
+template <typename T, bool kFused, bool kDual, bool kFp8>
 __device__ __forceinline__ void pf_produce(const DecodeParams& p, const CUtensorMap* mapK,
                                            const CUtensorMap* mapQ, unsigned char* sm, uint32_t base) {
     using C = PfTile<T>;
@@ -596,9 +625,14 @@ __device__ __forceinline__ void pf_produce(const DecodeParams& p, const CUtensor
                 c = cc;
                 break;
             }
-            const uint32_t tile_bytes = static_cast<uint32_t>(__popc(groups)) * 4096u;
+            const uint32_t tile_bytes = static_cast<uint32_t>(__popc(groups)) * (kFp8 ? 2048u : 4096u);
             const uint32_t stage_base = base + C::kRingOff + st * C::kStageBytes;
-            if (mine) pf::tma_load_4d(stage_base + r * 4096, mapK, row >> 3, bar(C::kFullK + st));
+            if (mine) {
+                if constexpr (kFp8)
+                    pf::tma_load_2d(stage_base + C::kHalfFp8 + r * 2048, mapK, row, bar(C::kFullK + st));
+                else
+                    pf::tma_load_4d(stage_base + r * 4096, mapK, row >> 3, bar(C::kFullK + st));
+            }
             const int ms = cc & (C::kMetaSlots - 1);
             if (lane < 8) plan[ms * C::kPlanInts + lane] = mine ? row : -1;
             if (lane == 0) {
@@ -676,8 +710,103 @@ __device__ __forceinline__ void pf_produce(const DecodeParams& p, const CUtensor
     }
 }
 
-// ---- warp 10: the V boxes of each stage, from the producer's plan ------------
-// Stage c: its plan (slot c % 4), then the V half of ring slot c % 2 once MMA2
+// ---- E4M3 caches: a stage's K codes widened in place ------------------------
+// A 16-token group's codes land row-major ([16 rows][128 B]) in the upper half
+// of the stage's tile; token row t becomes code x scale of its (block, kv
+// head), rounded once to T, in the layout [2 halves of 64 columns][128
+// rows][128 B] with the 128-byte swizzle: its first half at t * 128, its
+// second half in the 128 bytes its codes occupied, so a lane that widens whole
+// rows overwrites only codes it has read.  K rows of groups that were not
+// loaded are left alone (the softmax masks them).  The stage's loaded groups
+// and lane r < 8's scale of group r:
+struct PfWiden {
+    uint32_t groups;
+    float sc_lane;
+};
+
+__device__ __forceinline__ PfWiden pf_widen_record(const PfStageMeta& m, const int* pl, const float* scales,
+                                                   int block_size, int lane) {
+    PfWiden w;
+    w.groups = m.groups;
+    const int grow = lane < 8 ? pl[lane] : -1;  // group `lane`'s cache row, -1: not loaded
+    w.sc_lane = grow >= 0 ? __ldg(scales + grow / block_size) : 0.f;
+    return w;
+}
+
+// Rows lane + 32 k, k0 <= k < k0 + 2, of the K tile at `tile`.
+template <typename T>
+__device__ __forceinline__ void pf_widen_k(unsigned char* tile, const PfWiden& w, int k0, int lane) {
+    using C = PfTile<T>;
+#pragma unroll 1
+    for (int k = k0; k < k0 + 2; ++k) {
+        const int t = lane + 32 * k;  // token row
+        const float sc = __shfl_sync(0xffffffffu, w.sc_lane, t >> 4);
+        if (((w.groups >> (t >> 4)) & 1u) == 0) continue;
+        const uint4* src = reinterpret_cast<const uint4*>(tile + C::kHalfFp8 + t * 128);
+        // every 16-byte piece of the row is read before any is written; lane t
+        // starts at piece t % 8, so the 8 rows of a wavefront touch 8 distinct
+        // bank groups (on the writes too, through the swizzle)
+        uint4 codes[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) codes[i] = src[(i + t) & 7];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {  // piece pc: codes of columns 16 pc .. 16 pc + 15
+            const int pc = (i + t) & 7;
+            const uint4 u = codes[i];
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {  // 16-byte chunk 2 pc + h of the widened row
+                const int ch = 2 * pc + h;
+                const uint32_t a = h ? u.z : u.x, b = h ? u.w : u.y;
+                const uint4 v = make_uint4(pf::widen_pair<T>(a, sc), pf::widen_pair<T>(a >> 16, sc),
+                                           pf::widen_pair<T>(b, sc), pf::widen_pair<T>(b >> 16, sc));
+                *reinterpret_cast<uint4*>(tile + (ch >> 3) * C::kHalfFp8 + t * 128 + (((ch & 7) ^ (t & 7)) << 4)) =
+                    v;
+            }
+        }
+    }
+    tc::fence_async_smem();  // the widened tile is read by the MMAs
+    __syncwarp();
+}
+
+// ---- warp 19, E4M3 caches: rows 0-63 of each stage's K, in stage order -------
+// Stage c: its plan (posted with the copies) and the groups' scales, then its
+// codes; the end marker is passed on to the MMA warp (so does the copy warp,
+// which widens rows 64-127).
+template <typename T>
+__device__ __forceinline__ void pf_convert_k(const DecodeParams& p, unsigned char* sm) {
+    using C = PfTile<T>;
+    const int lane = threadIdx.x & 31;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::kBarOff);
+    auto bar = [&](int i) { return smem_addr(bars + i); };
+    const int* plan = reinterpret_cast<const int*>(sm + C::kPlanOff);
+    const PfStageMeta* meta = reinterpret_cast<const PfStageMeta*>(sm + C::kMetaOff);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + C::kMiscOff + 4);
+    for (int c = 0;; ++c) {
+        const int st = c & 1, ms = c & (C::kMetaSlots - 1);
+        if (!mbar_wait_warp(bar(C::kVPlan + ms), static_cast<uint32_t>(c >> C::kMetaShift) & 1)) {
+            if (lane == 0) report(p.d_err, PA_DERR_TIMEOUT);
+            *abort_flag = 1;
+            break;
+        }
+        const int* pl = plan + ms * C::kPlanInts;
+        if (pl[C::kPlanStop] != 0) {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(C::kConvK + st));
+            break;
+        }
+        const PfWiden w = pf_widen_record(meta[ms], pl, p.k_scale, p.block_size, lane);
+        if (!mbar_wait_warp(bar(C::kFullK + st), static_cast<uint32_t>(c >> 1) & 1)) {
+            if (lane == 0) report(p.d_err, PA_DERR_TIMEOUT);
+            *abort_flag = 1;
+            break;
+        }
+        pf_widen_k<T>(sm + C::kRingOff + st * C::kStageBytes, w, 0, lane);
+        if (lane == 0) mbar_arrive(bar(C::kConvK + st));
+    }
+}
+
+// ---- warp 18: the V boxes of each stage, from the producer's plan ------------
+// Stage c: its plan (slot c % 8), then the V half of ring slot c % 2 once MMA2
 // of stage c-2 completed, then the boxes.
 template <typename T>
 __device__ __forceinline__ void pf_copy_v(const DecodeParams& p, const CUtensorMap* mapV,
@@ -723,6 +852,97 @@ __device__ __forceinline__ void pf_copy_v(const DecodeParams& p, const CUtensorM
     __syncwarp();
 }
 
+// ---- warp 18, E4M3 caches: the V code boxes, and rows 64-127 of K ----------
+// Stage c: its plan; then, whichever is ready first, the V code boxes of stage
+// c (once MMA2 of stage c-2 completed) and the widening of rows 64-127 of its
+// K (once they landed), polling both without blocking.
+template <typename T>
+__device__ __forceinline__ void pf_copy_v_fp8(const DecodeParams& p, const CUtensorMap* mapV,
+                                              unsigned char* sm, uint32_t base) {
+    using C = PfTile<T>;
+    const int lane = threadIdx.x & 31;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::kBarOff);
+    auto bar = [&](int i) { return smem_addr(bars + i); };
+    const int* plan = reinterpret_cast<const int*>(sm + C::kPlanOff);
+    const PfStageMeta* meta = reinterpret_cast<const PfStageMeta*>(sm + C::kMetaOff);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + C::kMiscOff + 4);
+    bool failed = false;
+    int c = 0;  // stages whose V copies were issued
+    for (;; ++c) {
+        const int st = c & 1, ms = c & (C::kMetaSlots - 1);
+        if (!mbar_wait_warp(bar(C::kVPlan + ms), static_cast<uint32_t>(c >> C::kMetaShift) & 1)) {
+            failed = true;
+            break;
+        }
+        const int* pl = plan + ms * C::kPlanInts;
+        const int stop = pl[C::kPlanStop];
+        const int row = lane < 8 ? pl[lane] : -1;
+        const uint32_t bytes = static_cast<uint32_t>(pl[C::kPlanBytes]);
+        __syncwarp();
+        if (stop != 0) {  // the end marker, passed on to the MMA warp
+            if (lane == 0) mbar_arrive(bar(C::kConvK + st));
+            break;
+        }
+        const PfWiden w = pf_widen_record(meta[ms], pl, p.k_scale, p.block_size, lane);
+        bool need_issue = true, need_widen = true;
+        unsigned long long idle0 = 0;
+        while (need_issue || need_widen) {
+            bool did = false;
+            // every lane tests (and so acquires) the barriers it proceeds on
+            if (need_issue) {
+                const bool ok = c < C::kStages ||
+                                mbar_test_wait(bar(C::kEmptyV + st), static_cast<uint32_t>((c >> 1) - 1) & 1);
+                if (__all_sync(0xffffffffu, ok)) {
+                    if (lane == 0) mbar_arrive_expect_tx(bar(C::kFullV + st), bytes);
+                    __syncwarp();
+                    if (row >= 0)  // codes row-major into the tile's upper half
+                        pf::tma_load_2d(base + C::kRingOff + st * C::kStageBytes + C::kTileBytes + C::kHalfFp8 +
+                                            lane * 2048,
+                                        mapV, row, bar(C::kFullV + st));
+                    __syncwarp();
+                    need_issue = false;
+                    did = true;
+                }
+            }
+            if (need_widen) {
+                const bool ok = mbar_test_wait(bar(C::kFullK + st), static_cast<uint32_t>(c >> 1) & 1);
+                if (__all_sync(0xffffffffu, ok)) {
+                    pf_widen_k<T>(sm + C::kRingOff + st * C::kStageBytes, w, 2, lane);
+                    if (lane == 0) mbar_arrive(bar(C::kConvK + st));
+                    need_widen = false;
+                    did = true;
+                }
+            }
+            if (did) {
+                idle0 = 0;
+                continue;
+            }
+            const unsigned long long now = global_timer_ns();
+            if (idle0 == 0) {
+                idle0 = now;
+            } else if (now - idle0 > kWaitLimitNs) {
+                failed = true;
+                break;
+            }
+            __nanosleep(32);
+        }
+        if (failed) {
+            if (!need_issue) ++c;  // the copies of stage c are in flight
+            break;
+        }
+    }
+    if (failed) {
+        if (lane == 0) report(p.d_err, PA_DERR_TIMEOUT);
+        *abort_flag = 1;
+    }
+    // every V copy issued here has landed before the CTA may exit
+    if (lane == 0)
+        for (int cc = max(0, c - C::kStages); cc < c; ++cc)
+            if (!mbar_wait(bar(C::kFullV + (cc & 1)), static_cast<uint32_t>(cc >> 1) & 1))
+                report(p.d_err, PA_DERR_TIMEOUT);
+    __syncwarp();
+}
+
 // ---- warp 1: MMA issue -------------------------------------------------------
 // Two cursors: MMA1 of stage c1 (S[c1%2] = Q.K^T) once K of c1 has landed,
 // the softmax warps have read S of stage c1-2 and MMA2 of stage c1-2 was
@@ -733,7 +953,10 @@ __device__ __forceinline__ void pf_copy_v(const DecodeParams& p, const CUtensorM
 // once; with nothing ready the warp polls (non-blocking tests, short sleeps)
 // and gives up after the wait limit without progress.  Lane 0 tests the
 // barriers, reads the meta and issues (the elected lane of a full warp).
-template <typename T>
+// kFp8: K is ready once widened (convK, whose converters pass the end marker
+// on), V once P of its stage is published (the softmax warps widen it), and
+// the tiles have the E4M3 layout.
+template <typename T, bool kFp8>
 __device__ __forceinline__ void pf_mma(const DecodeParams& p, unsigned char* sm, uint32_t base,
                                        uint32_t tmem) {
     using C = PfTile<T>;
@@ -743,6 +966,10 @@ __device__ __forceinline__ void pf_mma(const DecodeParams& p, unsigned char* sm,
     const PfStageMeta* meta = reinterpret_cast<const PfStageMeta*>(sm + C::kMetaOff);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + C::kMiscOff + 4);
     auto stage_k = [&](int c) { return base + C::kRingOff + (c & 1) * C::kStageBytes; };
+    // operand layouts: one 64-column half of consecutive 8-row blocks lies
+    // kGroupStep apart, the other half kHalfStep after it
+    constexpr uint32_t kHalfStep = kFp8 ? C::kHalfFp8 : 1024, kGroupStep = kFp8 ? 1024 : 2048;
+    constexpr int kReadyK = kFp8 ? C::kConvK : C::kFullK;
 
     int c1 = 0, c2 = 0;
     bool end1 = false;     // MMA1 reached the end marker (at stage c1)
@@ -758,7 +985,7 @@ __device__ __forceinline__ void pf_mma(const DecodeParams& p, unsigned char* sm,
             const int st = c1 & 1;
             // 0: not ready, 1: issue, 2: end marker; then the stage's flags and item
             int ok = 0, flags = 0, item_seq = 0;
-            if (lane == 0 && mbar_test_wait(bar(C::kFullK + st), static_cast<uint32_t>(c1 >> 1) & 1)) {
+            if (lane == 0 && mbar_test_wait(bar(kReadyK + st), static_cast<uint32_t>(c1 >> 1) & 1)) {
                 const PfStageMeta& m = meta[c1 & (C::kMetaSlots - 1)];
                 flags = static_cast<int>(m.flags);
                 item_seq = static_cast<int>(m.item_seq);
@@ -782,7 +1009,7 @@ __device__ __forceinline__ void pf_mma(const DecodeParams& p, unsigned char* sm,
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {  // 16 head dimensions per step
                     const uint64_t a = tc::smem_desc_sw128(q + (j / 4) * C::kHalf + (j % 4) * 32, 16, 1024);
-                    const uint64_t b = tc::smem_desc_sw128(k + (j / 4) * 1024 + (j % 4) * 32, 16, 2048);
+                    const uint64_t b = tc::smem_desc_sw128(k + (j / 4) * kHalfStep + (j % 4) * 32, 16, kGroupStep);
                     tc::mma_f16_warp(tmem + st * 128, a, b, C::kIdescS, j > 0);
                 }
                 tc::mma_commit_warp(bar(C::kSFull + st));
@@ -806,7 +1033,7 @@ __device__ __forceinline__ void pf_mma(const DecodeParams& p, unsigned char* sm,
                 const uint32_t pt = tmem + C::kPCol + 64u * (c2 & 1), v = stage_k(c2) + C::kTileBytes;
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {  // 16 tokens (8 TMEM columns of P) per step
-                    const uint64_t b = tc::smem_desc_sw128(v + j * 4096, 1024, 2048);
+                    const uint64_t b = tc::smem_desc_sw128(v + j * 2 * kGroupStep, kHalfStep, kGroupStep);
                     tc::mma_f16_tmem_a_warp(tmem + C::kOCol, pt + 8u * j, b, C::kIdescO,
                                             (j > 0 || !first) ? 1u : 0u);
                 }
@@ -897,8 +1124,8 @@ struct PfGroup {
 // stage its part of the row of O divided by the row sum (or the partition's
 // partial state).  The thread also
 // zeroes its share of V row `row` when token `row` holds no data, so
-// 0 x garbage never reaches O.
-template <typename T, bool kFused, bool kDual>
+// 0 x garbage never reaches O (kFp8: the V converter writes those rows as zeros).
+template <typename T, bool kFused, bool kDual, bool kFp8>
 __device__ __forceinline__ void pf_softmax(const DecodeParams& p, unsigned char* sm, uint32_t tmem) {
     using C = PfTile<T>;
     constexpr int kCols = C::kCols, kSplit = C::kSplit;  // O (head) columns of a thread
@@ -919,6 +1146,7 @@ __device__ __forceinline__ void pf_softmax(const DecodeParams& p, unsigned char*
     const PfStageMeta* meta = reinterpret_cast<const PfStageMeta*>(sm + C::kMetaOff);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + C::kMiscOff + 4);
     float* red = reinterpret_cast<float*>(sm + C::kRedOff);  // [kSplit parts][128 rows]
+    const int* plan = reinterpret_cast<const int*>(sm + C::kPlanOff);
     PfGroup grp{tid, C::kSoftThreads};
     const uint32_t lane_off = static_cast<uint32_t>(32 * (warp & 3)) << 16;
     const uint32_t col0 = static_cast<uint32_t>(kCols * part_i);  // of O
@@ -956,6 +1184,12 @@ __device__ __forceinline__ void pf_softmax(const DecodeParams& p, unsigned char*
         const uint32_t groups = m.groups;
         const bool own = kFused && (flags & kStageOwn);
         const uint32_t gc0 = m.gcnt[0], gc1 = m.gcnt[1];
+        // E4M3: the V scale of token `row`'s group, loaded while S is read
+        float vsc = 0.f;
+        if constexpr (kFp8) {
+            const int prow = plan[(c & (C::kMetaSlots - 1)) * C::kPlanInts + (row >> 4)];
+            if (prow >= 0) vsc = __ldg(p.v_scale + prow / p.block_size);
+        }
         if (flags & kStageFirst) {
             row0 = m.row0;
             hq0 = m.hq0;
@@ -1106,7 +1340,39 @@ __device__ __forceinline__ void pf_softmax(const DecodeParams& p, unsigned char*
         }
         pf::tmem_st<kSC / 2>(tmem + C::kPCol + 64u * (c & 1) + scol0 / 2 + lane_off, pw);
         l += (l4[0] + l4[1]) + (l4[2] + l4[3]);
-        if (kFused && !full) {
+        if constexpr (kFp8) {
+            // E4M3: the stage's V, widened in place once it landed (before P is
+            // published).  Thread (row, part_i) widens token row `row`'s
+            // pieces (2 part_i + row) % 8 and (2 part_i + 1 + row) % 8 (16 codes
+            // each; rows of consecutive threads start on distinct bank groups):
+            // code x scale rounded once to T, or zeros when the token holds no
+            // data.  All four parts read their codes before any writes, since
+            // the row's second 64 columns land where its codes were.
+            if (!grp.wait(bar(C::kFullV + st), static_cast<uint32_t>(c >> 1) & 1, p.d_err, abort_flag)) break;
+            unsigned char* vt = sm + C::kRingOff + st * C::kStageBytes + C::kTileBytes;
+            uint4 cd[2];
+#pragma unroll
+            for (int k = 0; k < 2; ++k)
+                cd[k] = zero_row ? make_uint4(0, 0, 0, 0)
+                                 : *reinterpret_cast<const uint4*>(vt + C::kHalfFp8 + row * 128 +
+                                                                   ((2 * part_i + k + row) & 7) * 16);
+            grp.sync();
+            const float sc = zero_row ? 0.f : vsc;
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+                const int pc = (2 * part_i + k + row) & 7;
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int ch = 2 * pc + h;
+                    const uint32_t a = h ? cd[k].z : cd[k].x, b = h ? cd[k].w : cd[k].y;
+                    *reinterpret_cast<uint4*>(vt + (ch >> 3) * C::kHalfFp8 + row * 128 +
+                                              (((ch & 7) ^ (row & 7)) << 4)) =
+                        make_uint4(pf::widen_pair<T>(a, sc), pf::widen_pair<T>(a >> 16, sc),
+                                   pf::widen_pair<T>(b, sc), pf::widen_pair<T>(b >> 16, sc));
+                }
+            }
+        }
+        if (kFused && !kFp8 && !full) {
             // some token of the stage holds no data: once the stage's V has
             // landed, zero its rows (before P is published; late in the
             // stage, so the V copy has had time to land)
@@ -1199,8 +1465,8 @@ __device__ __forceinline__ void pf_softmax(const DecodeParams& p, unsigned char*
     tc::fence_before_sync();
 }
 
-template <typename T, bool kFused, bool kDual>
-__global__ void __launch_bounds__(PfTile<T>::kThreads, 1)
+template <typename T, bool kFused, bool kDual, bool kFp8>
+__global__ void __launch_bounds__(kFp8 ? PfTile<T>::kThreadsFp8 : PfTile<T>::kThreads, 1)
     prefill_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap mapK,
                       const __grid_constant__ CUtensorMap mapV, const __grid_constant__ CUtensorMap mapQ) {
     using C = PfTile<T>;
@@ -1216,7 +1482,8 @@ __global__ void __launch_bounds__(PfTile<T>::kThreads, 1)
         for (int i = 0; i < C::kNumBars; ++i) {
             // s_free and p_full are signalled by every softmax warp
             const bool warps = i == C::kSFree || i == C::kSFree + 1 || i == C::kPFull || i == C::kPFull + 1;
-            mbar_init(smem_addr(bars + i), warps ? C::kSoftWarps : 1);
+            const bool conv = i == C::kConvK || i == C::kConvK + 1;  // the two K converter warps
+            mbar_init(smem_addr(bars + i), warps ? C::kSoftWarps : conv ? 2 : 1);
         }
         *reinterpret_cast<volatile int*>(sm + C::kMiscOff + 4) = 0;
         fence_barrier_init();
@@ -1238,13 +1505,19 @@ __global__ void __launch_bounds__(PfTile<T>::kThreads, 1)
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     if (warp == 0)
-        pf_produce<T, kFused, kDual>(p, &mapK, &mapQ, sm, base);
+        pf_produce<T, kFused, kDual, kFp8>(p, &mapK, &mapQ, sm, base);
     else if (warp == 1)
-        pf_mma<T>(p, sm, base, tmem);
+        pf_mma<T, kFp8>(p, sm, base, tmem);
     else if (warp < C::kCopyWarp)
-        pf_softmax<T, kFused, kDual>(p, sm, tmem);
-    else
-        pf_copy_v<T>(p, &mapV, sm, base);
+        pf_softmax<T, kFused, kDual, kFp8>(p, sm, tmem);
+    else if (warp == C::kCopyWarp) {
+        if constexpr (kFp8)
+            pf_copy_v_fp8<T>(p, &mapV, sm, base);
+        else
+            pf_copy_v<T>(p, &mapV, sm, base);
+    } else if constexpr (kFp8) {
+        pf_convert_k<T>(p, sm);
+    }
 
     tc::fence_before_sync();
     __syncthreads();
@@ -1262,7 +1535,9 @@ __global__ void __launch_bounds__(PfTile<T>::kThreads, 1)
     }
 }
 
-template <typename T>
+// kFp8: E4M3 caches (mapK / mapV: the byte maps of [16 rows x 128 B] boxes,
+// k_scale / v_scale set), the fused shared-prefix pass only.
+template <typename T, bool kFp8>
 inline pa_status launch_prefill_tc_typed(const DecodeParams& p, const CUtensorMap& mapK,
                                          const CUtensorMap& mapV, const CUtensorMap& mapQ,
                                          cudaStream_t stream) {
@@ -1274,11 +1549,17 @@ inline pa_status launch_prefill_tc_typed(const DecodeParams& p, const CUtensorMa
     // fused: a group's members are the lanes of the producer warp
     if (p.prefix_fused != 0 && (p.prefix_lens == nullptr || p.prefix_group > 32 || p.block_size % 16 != 0))
         return PA_ERR_UNSUPPORTED;
+    if (kFp8 && (p.prefix_fused == 0 || p.k_scale == nullptr || p.v_scale == nullptr)) return PA_ERR_UNSUPPORTED;
     // fused with at most 64 rows per item (group x heads): the two-stream tile
     const int mode = p.prefix_fused == 0 ? 0 : p.group * p.tile_tokens <= 64 ? 2 : 1;
-    auto kernel = mode == 0   ? prefill_tc_kernel<T, false, false>
-                  : mode == 1 ? prefill_tc_kernel<T, true, false>
-                              : prefill_tc_kernel<T, true, true>;
+    using Kernel = void (*)(const DecodeParams, const CUtensorMap, const CUtensorMap, const CUtensorMap);
+    Kernel kernel;
+    if constexpr (kFp8)
+        kernel = mode == 1 ? prefill_tc_kernel<T, true, false, true> : prefill_tc_kernel<T, true, true, true>;
+    else
+        kernel = mode == 0   ? prefill_tc_kernel<T, false, false, false>
+                 : mode == 1 ? prefill_tc_kernel<T, true, false, false>
+                             : prefill_tc_kernel<T, true, true, false>;
     if (ensure_smem(kernel, C::kSmemBytes, smem_configured[mode]) != PA_OK) return PA_ERR_CUDA;
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
@@ -1295,7 +1576,7 @@ inline pa_status launch_prefill_tc_typed(const DecodeParams& p, const CUtensorMa
     if (grid > work) grid = work;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid));
-    cfg.blockDim = dim3(C::kThreads);
+    cfg.blockDim = dim3(kFp8 ? C::kThreadsFp8 : C::kThreads);
     cfg.dynamicSmemBytes = C::kSmemBytes;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
@@ -1313,5 +1594,9 @@ pa_status launch_prefill_tc_f16(const DecodeParams& p, const CUtensorMap& mapK, 
                                 const CUtensorMap& mapQ, cudaStream_t stream);
 pa_status launch_prefill_tc_bf16(const DecodeParams& p, const CUtensorMap& mapK, const CUtensorMap& mapV,
                                  const CUtensorMap& mapQ, cudaStream_t stream);
+pa_status launch_prefill_tc_fp8_f16(const DecodeParams& p, const CUtensorMap& mapK, const CUtensorMap& mapV,
+                                    const CUtensorMap& mapQ, cudaStream_t stream);
+pa_status launch_prefill_tc_fp8_bf16(const DecodeParams& p, const CUtensorMap& mapK, const CUtensorMap& mapV,
+                                     const CUtensorMap& mapQ, cudaStream_t stream);
 
 }  // namespace pa

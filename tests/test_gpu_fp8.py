@@ -332,3 +332,81 @@ def test_fp8_shared_prefix_other_shapes_run_plain_decode():
                                          max_suffix=30, num_q_heads=16, num_kv_heads=2), seed=623), 1)):
         shared = w.meta["shared_prefix_tokens"]
         _shared_check(w, G, [shared] * (w.num_seqs // G))
+
+
+# ---- the fused pass over E4M3 caches: one 128-row kernel pass per (group, kv
+# head) widens each stage's codes in shared memory and reads the prefix, then
+# every member's own tokens (groups x kv heads >= the SM count)
+
+def _fused_groups(num_kv_heads, want=1):
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    return max(want, -(-sms // num_kv_heads))
+
+
+def _assert_fused(w, group):
+    plan = pa.shared_prefix_plan(w.num_seqs, w.num_q_heads, w.num_kv_heads, w.head_dim,
+                                 w.max_blocks_per_seq, w.block_size, w.num_blocks, w.dtype, group,
+                                 kv_dtype="e4m3")
+    assert (plan["kernel"], plan["merge"], plan["launches"]) == ("tc_128_rows", "none", 1), plan
+
+
+FP8_FUSED = [
+    # dtype, Hq, Hkv, B, samples, prefix_len, max_suffix, groups (None: just enough)
+    ("bf16", 64, 8, 16, 8, 1024, 256, None),   # the named shape, fewer groups: two-stream tiles
+    ("f16", 32, 8, 16, 8, 300, 100, None),     # g = 4: 32 rows per group
+    ("bf16", 128, 8, 32, 8, 700, 64, None),    # g = 16: 128 rows, 32-token blocks
+    ("f16", 64, 8, 128, 4, 1000, 300, None),   # 128-token blocks
+    ("bf16", 64, 8, 16, 2, 300, 300, 90),      # more groups than the longest-first order takes
+]
+
+
+@pytest.mark.parametrize("case", range(len(FP8_FUSED)))
+def test_fp8_fused_pass(case):
+    """Every output of the E4M3 fused pass against the oracle's E4M3 decode
+    (every token's K and V carry one rounding of code x scale to q's type,
+    inside the 16-bit tolerance), with groups whose prefix is unusable (zero,
+    not a block multiple, negative) and one shorter than the blocks allow."""
+    dtype, Hq, Hkv, B, n, pre_len, suf, groups = FP8_FUSED[case]
+    G = _fused_groups(Hkv, groups or 1)
+    w = wl.to_fp8(wl.gqa_share(seed=660 + case, groups=G, samples=n, prefix_len=pre_len,
+                               max_suffix=suf, num_q_heads=Hq, num_kv_heads=Hkv, block_size=B,
+                               dtype=dtype), seed=670 + case)
+    _assert_fused(w, n)
+    shared = w.meta["shared_prefix_tokens"]
+    pre = [shared] * G
+    pre[1], pre[2], pre[3], pre[4] = 0, shared - 5, -B, max(0, shared - 3 * B)
+    stats, _ = _shared_check(w, n, pre)
+    print("fp8 fused", FP8_FUSED[case], stats)
+
+
+def test_fp8_fused_pass_edge_cases():
+    """E4M3 fused pass: a member with no own tokens, one with a single whole
+    16-token group, a group whose members hold only the prefix, a member past
+    the table (zero row, flagged), an empty member and a group of empty
+    members (zero rows), a member's own block id past the pool (its tokens
+    skipped, flagged); NaN codes in every slot past a context."""
+    G = _fused_groups(8, 20)
+    w = wl.gqa_share(seed=680, groups=G, samples=8, prefix_len=512, max_suffix=200,
+                     num_q_heads=64, num_kv_heads=8)
+    shared = w.meta["shared_prefix_tokens"]
+    max_ctx = w.max_blocks_per_seq * w.block_size
+    ctx = w.context_lens
+    ctx[0], ctx[1] = shared, shared + 16
+    ctx[8 * 3:8 * 4] = shared
+    ctx[8 * 1 + 3] = max_ctx + 16
+    ctx[8 * 4 + 2] = 0
+    ctx[8 * 6:8 * 7] = 0
+    s_bad = next(s for s in range(16, 24) if ctx[s] >= shared + 40)  # group 2
+    w.block_tables[s_bad, shared // 16 + 1] = w.num_blocks + 7
+    w = wl.to_fp8(w, seed=681)
+    pre = [shared] * G
+    pre[6] = 0
+    _assert_fused(w, 8)
+    d = _upload(w)
+    out = _shared_step(w, d, 8, pre)
+    (kc, _), (vc, _), ref, err = oracle.step(w)
+    assert err == oracle.ERR_CTX_OOB | oracle.ERR_BLOCK_OOB
+    assert int(d["d_err"].item()) == err
+    assert_close(out_f64(out), ref, w.dtype, "fp8 fused pass, edge cases")
+    for s in [8 + 3, 8 * 4 + 2] + list(range(8 * 6, 8 * 7)):
+        assert (out[s] == 0).all()

@@ -226,9 +226,8 @@ def test_fused_pass(case):
     """Every output of the fused pass against the oracle's plain decode, with
     groups whose prefix is unusable (zero, not a block multiple, negative:
     every token is then a member's own) and one shorter than the blocks
-    allow among the shared ones.  Up to 64 groups the items' stages are split
-    evenly over the CTAs (items cut in pieces, merged in the kernel); with
-    more, items are handed out whole."""
+    allow among the shared ones.  Up to 64 groups the items are handed out
+    longest first; with more, in group order."""
     dtype, Hq, Hkv, B, n, pre_len, suf, groups = FUSED_CASES[case]
     G = _fused_groups(Hkv, groups or 1)
     w = wl.gqa_share(seed=600 + case, groups=G, samples=n, prefix_len=pre_len, max_suffix=suf,
