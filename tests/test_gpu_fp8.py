@@ -410,3 +410,63 @@ def test_fp8_fused_pass_edge_cases():
     assert_close(out_f64(out), ref, w.dtype, "fp8 fused pass, edge cases")
     for s in [8 + 3, 8 * 4 + 2] + list(range(8 * 6, 8 * 7)):
         assert (out[s] == 0).all()
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+def test_fp8_fused_pass_widening_covers_every_code(dtype):
+    """Fused E4M3 pass, closed form: every K code is zero (all logits 0, equal
+    weights) and every valid token's V row of kv head h holds the same 128
+    codes, half of the finite E4M3 codes each (NaN codes 0x7f / 0xff replaced
+    by their neighbours), so each output row is exactly that V row, code
+    value x 1/8 (exact in q's type).  Groups with a shared one-block prefix
+    (read in prefix stages) alternate with groups whose prefix is unusable
+    (the same tokens read as the members' own); the second member of each
+    group also owns one token of a private block whose other slots hold NaN
+    codes.  A wrong bit placement, a lost sign, flushed subnormal codes or a
+    NaN slot leaking into the widened V shows up."""
+    tdt = {"f16": torch.float16, "bf16": torch.bfloat16}[dtype]
+    Hkv, g, B, D, n = 8, 4, 16, 128, 2
+    G = _fused_groups(Hkv, 2)
+    S, Hq = G * n, Hkv * g
+    NB = 2 * G + 3
+    codes = np.arange(256, dtype=np.uint8)
+    codes[0x7F], codes[0xFF] = 0x7E, 0xFE
+    rows = np.stack([codes[128 * (h % 2):128 * (h % 2) + 128] for h in range(Hkv)])  # [Hkv][128]
+    kc = np.zeros((NB, Hkv, B, D), np.uint8)
+    vc = np.full((NB, Hkv, B, D), 0x7F, np.uint8)  # NaN codes everywhere not valid
+    tables = np.full((S, 2), NB + 5, np.int32)     # entries past the context: never read
+    ctx = np.zeros(S, np.int32)
+    for grp in range(G):
+        shared, own = 2 * grp, 2 * grp + 1
+        vc[shared] = rows[:, None, :]              # all 16 tokens of the shared block
+        vc[own, :, 0] = rows                       # one valid token in the private block
+        for j in range(n):
+            s = grp * n + j
+            tables[s, 0] = shared
+            ctx[s] = B
+            if j == 1:
+                tables[s, 1] = own
+                ctx[s] = B + 1
+    prefix = np.array([B if grp % 2 == 0 else 0 for grp in range(G)], np.int32)
+    scales = np.full((NB, Hkv), 0.125, np.float32)
+    plan = pa.shared_prefix_plan(S, Hq, Hkv, D, 2, B, NB, dtype, n, kv_dtype="e4m3")
+    assert (plan["kernel"], plan["merge"], plan["launches"]) == ("tc_128_rows", "none", 1), plan
+    q = torch.randn((S, Hq, D), generator=torch.Generator().manual_seed(690)).to(tdt).cuda()
+    dev = {k: torch.from_numpy(v).cuda() for k, v in
+           dict(kc=kc, vc=vc, s=scales, t=tables, c=ctx, pre=prefix).items()}
+    out = torch.full_like(q, float("nan"))
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    pa.decode_shared_prefix_fp8(out, q, dev["kc"], dev["vc"], dev["s"], dev["s"], dev["t"],
+                                dev["c"], 0.088, n, dev["pre"], d_err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    want = oracle.e4m3_to_f64(rows) * 0.125  # [Hkv][128]
+    got = out.double().cpu().numpy()
+    for s in range(S):
+        for h in range(Hq):
+            ref, row = want[h // g], got[s, h]
+            assert ((row == 0) == (ref == 0)).all(), (s, h)
+            nz = ref != 0
+            assert (np.signbit(row[nz]) == np.signbit(ref[nz])).all(), (s, h)
+            rel = np.abs(row[nz] - ref[nz]) / np.abs(ref[nz])
+            assert rel.max() <= 2.0 ** -8, (s, h, float(rel.max()))
